@@ -1,0 +1,319 @@
+/*
+ * oracle.c -- plain, slow, single-threaded CPU reference for the fused Q4_K
+ * SwiGLU feed-forward block.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, loads or
+ * calls this file; only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark do.  It shares no code, header, table or constant with the CUDA
+ * library.
+ *
+ * What it computes (sources):
+ *   - The block:  y = W_down . (silu(W_gate . x) (*) (W_up . x)), hidden width H
+ *     projected up twice to the intermediate width I, combined by SwiGLU and
+ *     projected back down.  "Fused SwiGLU MLP: ZINC RDNA4 Down-Projection
+ *     Bandwidth", section "The MLP is two trips up to a wider width".
+ *   - Weights in Q4_K super-blocks ("Fused SwiGLU MLP...", FAQ "Why is fusing
+ *     the SwiGLU intermediate harder..."; "VGPR pressure caps the fused RDNA4
+ *     prefill GEMM at nine waves", section "What the fused GEMM actually spends
+ *     registers on").  The pages name the format but do not lay out its bytes;
+ *     the reading used here is the GGUF Q4_K arrangement:
+ *       bytes 0..1   d     (IEEE binary16, little endian)
+ *       bytes 2..3   dmin  (IEEE binary16)
+ *       bytes 4..15  scales[12]: eight 6-bit (sc, m) pairs, one per sub-block
+ *                    of 32 weights
+ *       bytes 16..143 qs[128]: 4-bit quants; byte qs[32g+l] holds weight 64g+l
+ *                    in its low nibble and weight 64g+32+l in its high nibble
+ *       w = d*sc*q - dmin*m
+ *   - Mixture of experts: y_t = sum_j w_{t,j} FFN_{e_{t,j}}(x_t), expert ids and
+ *     weights given per token ("Four bottlenecks, one CUDA backend...",
+ *     section "Bottleneck 2 -- MoE decode was paying for its routing twice").
+ *
+ * Precision: Q4_K dequantisation is done in fp32 exactly as the format states
+ * (both products are exact in fp32, so only the final subtraction rounds); the
+ * matrix products, silu and the down projection are evaluated in fp64.  The
+ * quantiser decides integer codes, so it works in fp32 step by step (see
+ * oracle_q4k_quantize_row).
+ *
+ * Compile with -O2 -ffp-contract=off (no fast-math).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define QK 256        /* weights per super-block            */
+#define QK_BYTES 144  /* bytes per super-block              */
+
+/* ---- scalar formats ---------------------------------------------------- */
+
+/* IEEE binary16 -> float, written out from the format's definition:
+ * sign, 5-bit biased exponent (bias 15), 10-bit fraction. */
+float oracle_f16_to_f32(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 31;
+    int f = h & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);               /* subnormal: f * 2^-14 / 1024 */
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp(1024.0 + f, e - 25);           /* (1 + f/1024) * 2^(e-15) */
+    return (float)(sign ? -v : v);
+}
+
+/* float -> IEEE binary16, round to nearest even (the C compiler's _Float16
+ * conversion is correctly rounded). */
+uint16_t oracle_f32_to_f16(float x)
+{
+    _Float16 v = (_Float16)x;
+    uint16_t h;
+    memcpy(&h, &v, 2);
+    return h;
+}
+
+/* bfloat16 bits -> float: the upper half of an IEEE binary32. */
+float oracle_bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* ---- Q4_K block ------------------------------------------------------------ */
+
+/* 6-bit scale and min of sub-block j (0..7) from the 12 packed bytes.
+ * Sub-blocks 0..3 keep their 6 bits in the low bits of scales[j] (scale) and
+ * scales[j+4] (min).  Sub-blocks 4..7 keep their low 4 bits in the nibbles of
+ * scales[j+4] (scale: low nibble, min: high nibble) and their top 2 bits in
+ * the two spare top bits of scales[j-4] (scale) and scales[j] (min). */
+void oracle_q4k_scale_min(const uint8_t *scales, int j, int *sc, int *m)
+{
+    if (j < 4) {
+        *sc = scales[j] & 63;
+        *m = scales[j + 4] & 63;
+    } else {
+        *sc = (scales[j + 4] & 15) | ((scales[j - 4] >> 6) << 4);
+        *m = (scales[j + 4] >> 4) | ((scales[j] >> 6) << 4);
+    }
+}
+
+/* 4-bit code of weight k (0..255) of a block. */
+static int q4k_code(const uint8_t *qs, int k)
+{
+    int g = k / 64, r = k % 64;
+    uint8_t byte = qs[32 * g + (r % 32)];
+    return r < 32 ? (byte & 15) : (byte >> 4);
+}
+
+/* Dequantise one row of ceil(cols/256) consecutive blocks into cols floats.
+ * Weights at positions >= cols in the last block are not written. */
+void oracle_q4k_dequant_row(const uint8_t *row, int64_t cols, float *out)
+{
+    int64_t nb = (cols + QK - 1) / QK;
+    for (int64_t b = 0; b < nb; ++b) {
+        const uint8_t *blk = row + b * QK_BYTES;
+        float d = oracle_f16_to_f32((uint16_t)(blk[0] | (blk[1] << 8)));
+        float dmin = oracle_f16_to_f32((uint16_t)(blk[2] | (blk[3] << 8)));
+        const uint8_t *scales = blk + 4;
+        const uint8_t *qs = blk + 16;
+        for (int k = 0; k < QK; ++k) {
+            int64_t col = b * QK + k;
+            if (col >= cols)
+                break;
+            int sc, m;
+            oracle_q4k_scale_min(scales, k / 32, &sc, &m);
+            float ds = d * (float)sc;      /* exact: 11 x 6 significant bits */
+            float dm = dmin * (float)m;    /* exact                          */
+            float wq = ds * (float)q4k_code(qs, k); /* exact: 17 x 4 bits    */
+            out[col] = wq - dm;            /* the only rounding              */
+        }
+    }
+}
+
+void oracle_q4k_dequant(const uint8_t *blocks, float *out, int64_t rows, int64_t cols)
+{
+    int64_t rb = ((cols + QK - 1) / QK) * QK_BYTES;
+    for (int64_t r = 0; r < rows; ++r)
+        oracle_q4k_dequant_row(blocks + r * rb, cols, out + r * cols);
+}
+
+/* ---- min/max quantiser ------------------------------------------------------
+ * The pages do not give a quantiser; this library's reading of a "min/max"
+ * Q4_K quantiser, every step in fp32 round-to-nearest (no fused operations,
+ * IEEE division), rint = round half to even:
+ *   per sub-block j of 32 weights:  lo = min(0, min w), hi = max w,
+ *                                   scale_j = (hi - lo) / 15, min_j = -lo
+ *   per block:   d = f16(max_j scale_j / 63), dmin = f16(max_j min_j / 63)
+ *                sc_j = clamp(rint(scale_j / d), 0, 63)   (0 when d == 0)
+ *                m_j  = clamp(rint(min_j / dmin), 0, 63)  (0 when dmin == 0)
+ *   per weight:  q = clamp(rint((w + dmin*m_j) / (d*sc_j)), 0, 15)
+ *                                                       (0 when d*sc_j == 0)
+ * Positions >= cols in the last block are quantised as zeros. */
+static int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
+
+static void q4k_pack_scales(uint8_t *scales, const int *sc, const int *m)
+{
+    memset(scales, 0, 12);
+    for (int j = 0; j < 4; ++j) {
+        scales[j] = (uint8_t)(sc[j] & 63);
+        scales[j + 4] = (uint8_t)(m[j] & 63);
+    }
+    for (int j = 4; j < 8; ++j) {
+        scales[j + 4] = (uint8_t)((sc[j] & 15) | ((m[j] & 15) << 4));
+        scales[j - 4] |= (uint8_t)((sc[j] >> 4) << 6);
+        scales[j] |= (uint8_t)((m[j] >> 4) << 6);
+    }
+}
+
+void oracle_q4k_quantize_row(const float *w, int64_t cols, uint8_t *row)
+{
+    int64_t nb = (cols + QK - 1) / QK;
+    for (int64_t b = 0; b < nb; ++b) {
+        float x[QK];
+        for (int k = 0; k < QK; ++k) {
+            int64_t col = b * QK + k;
+            x[k] = col < cols ? w[col] : 0.0f;
+        }
+        float scale[8], mn[8];
+        float max_scale = 0.0f, max_min = 0.0f;
+        for (int j = 0; j < 8; ++j) {
+            float lo = 0.0f, hi = x[32 * j];
+            for (int l = 0; l < 32; ++l) {
+                float v = x[32 * j + l];
+                if (v < lo) lo = v;
+                if (v > hi) hi = v;
+            }
+            float diff = hi - lo;
+            scale[j] = diff / 15.0f;
+            mn[j] = -lo;
+            if (scale[j] > max_scale) max_scale = scale[j];
+            if (mn[j] > max_min) max_min = mn[j];
+        }
+        float dq = max_scale / 63.0f;
+        float dmq = max_min / 63.0f;
+        uint16_t d16 = oracle_f32_to_f16(dq);
+        uint16_t dm16 = oracle_f32_to_f16(dmq);
+        float d = oracle_f16_to_f32(d16);
+        float dmin = oracle_f16_to_f32(dm16);
+        int sc[8], m[8];
+        for (int j = 0; j < 8; ++j) {
+            float rs = d > 0.0f ? scale[j] / d : 0.0f;
+            float rm = dmin > 0.0f ? mn[j] / dmin : 0.0f;
+            sc[j] = clampi((int)rintf(rs), 0, 63);
+            m[j] = clampi((int)rintf(rm), 0, 63);
+        }
+        uint8_t *blk = row + b * QK_BYTES;
+        blk[0] = (uint8_t)(d16 & 255);
+        blk[1] = (uint8_t)(d16 >> 8);
+        blk[2] = (uint8_t)(dm16 & 255);
+        blk[3] = (uint8_t)(dm16 >> 8);
+        q4k_pack_scales(blk + 4, sc, m);
+        uint8_t *qs = blk + 16;
+        memset(qs, 0, 128);
+        for (int k = 0; k < QK; ++k) {
+            int j = k / 32;
+            float ds = d * (float)sc[j];
+            float dm = dmin * (float)m[j];
+            int q = 0;
+            if (ds > 0.0f) {
+                float t = x[k] + dm;
+                float r = t / ds;
+                q = clampi((int)rintf(r), 0, 15);
+            }
+            int g = k / 64, r = k % 64;
+            if (r < 32)
+                qs[32 * g + r] |= (uint8_t)q;
+            else
+                qs[32 * g + (r - 32)] |= (uint8_t)(q << 4);
+        }
+    }
+}
+
+void oracle_q4k_quantize(const float *w, uint8_t *blocks, int64_t rows, int64_t cols)
+{
+    int64_t rb = ((cols + QK - 1) / QK) * QK_BYTES;
+    for (int64_t r = 0; r < rows; ++r)
+        oracle_q4k_quantize_row(w + r * cols, cols, blocks + r * rb);
+}
+
+/* ---- the feed-forward block ------------------------------------------------ */
+
+double oracle_silu(double g) { return g / (1.0 + exp(-g)); }
+
+/* y[T x H] (fp64) = W_down . (silu(W_gate . x) * (W_up . x)) for each token row
+ * of x[T x H] (bf16 bits, row-major).
+ *   Wg, Wu: I rows of H/256 blocks;  Wd: H rows of ceil(I/256) blocks.
+ * Each weight row is dequantised once (fp32), the sums run in fp64 in
+ * ascending index order. */
+void oracle_swiglu_ffn(const uint16_t *x, const uint8_t *Wg, const uint8_t *Wu,
+                       const uint8_t *Wd, int64_t T, int64_t H, int64_t I, double *y)
+{
+    int64_t rb_in = ((H + QK - 1) / QK) * QK_BYTES;
+    int64_t rb_dn = ((I + QK - 1) / QK) * QK_BYTES;
+    double *xf = (double *)malloc(sizeof(double) * (size_t)(T * H));
+    double *h = (double *)malloc(sizeof(double) * (size_t)(T * I));
+    float *wg = (float *)malloc(sizeof(float) * (size_t)H);
+    float *wu = (float *)malloc(sizeof(float) * (size_t)H);
+    float *wd = (float *)malloc(sizeof(float) * (size_t)I);
+    for (int64_t i = 0; i < T * H; ++i)
+        xf[i] = (double)oracle_bf16_to_f32(x[i]);
+    /* g = Wg x, u = Wu x, h = silu(g) * u */
+    for (int64_t i = 0; i < I; ++i) {
+        oracle_q4k_dequant_row(Wg + i * rb_in, H, wg);
+        oracle_q4k_dequant_row(Wu + i * rb_in, H, wu);
+        for (int64_t t = 0; t < T; ++t) {
+            const double *xt = xf + t * H;
+            double g = 0.0, u = 0.0;
+            for (int64_t k = 0; k < H; ++k) {
+                g += (double)wg[k] * xt[k];
+                u += (double)wu[k] * xt[k];
+            }
+            h[t * I + i] = oracle_silu(g) * u;
+        }
+    }
+    /* y = Wd h */
+    for (int64_t n = 0; n < H; ++n) {
+        oracle_q4k_dequant_row(Wd + n * rb_dn, I, wd);
+        for (int64_t t = 0; t < T; ++t) {
+            const double *ht = h + t * I;
+            double acc = 0.0;
+            for (int64_t i = 0; i < I; ++i)
+                acc += (double)wd[i] * ht[i];
+            y[t * H + n] = acc;
+        }
+    }
+    free(xf); free(h); free(wg); free(wu); free(wd);
+}
+
+/* Mixture of experts: y_t = sum_{j < top_k} w[t][j] * FFN_{ids[t][j]}(x_t).
+ * Experts are stacked: expert e's W_gate starts at Wg + e * I * rowbytes(H),
+ * likewise W_up; its W_down at Wd + e * H * rowbytes(I).  An id outside
+ * [0, E) contributes nothing. */
+void oracle_moe_swiglu_ffn(const uint16_t *x, const int32_t *ids, const float *wts,
+                           const uint8_t *Wg, const uint8_t *Wu, const uint8_t *Wd,
+                           int64_t T, int64_t H, int64_t I, int64_t E, int64_t top_k,
+                           double *y)
+{
+    int64_t rb_in = ((H + QK - 1) / QK) * QK_BYTES;
+    int64_t rb_dn = ((I + QK - 1) / QK) * QK_BYTES;
+    double *yt = (double *)malloc(sizeof(double) * (size_t)H);
+    for (int64_t t = 0; t < T; ++t) {
+        double *out = y + t * H;
+        for (int64_t n = 0; n < H; ++n)
+            out[n] = 0.0;
+        for (int64_t j = 0; j < top_k; ++j) {
+            int64_t e = ids[t * top_k + j];
+            if (e < 0 || e >= E)
+                continue;
+            oracle_swiglu_ffn(x + t * H, Wg + e * I * rb_in, Wu + e * I * rb_in,
+                              Wd + e * H * rb_dn, 1, H, I, yt);
+            double w = (double)wts[t * top_k + j];
+            for (int64_t n = 0; n < H; ++n)
+                out[n] += w * yt[n];
+        }
+    }
+    free(yt);
+}

@@ -1,0 +1,160 @@
+"""ctypes front end of the CPU oracle (oracle.c).
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this module; the product library
+never does.  It compiles ``oracle.c`` with gcc on first use (or when
+``build()`` is called) into ``oracle/_build/liboracle.so``.
+
+Arrays are numpy: bf16 activations travel as ``uint16`` bit patterns, Q4_K
+weights as ``uint8`` byte arrays of shape ``[rows, ceil(cols/256) * 144]``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+QK = 256
+QK_BYTES = 144
+
+
+def row_bytes(cols: int) -> int:
+    return ((cols + QK - 1) // QK) * QK_BYTES
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c (plain C, -O2, no fast-math, no FMA contraction)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        subprocess.check_call([
+            "gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+            "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I64 = ctypes.c_int64
+            lib.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
+            lib.oracle_f16_to_f32.restype = ctypes.c_float
+            lib.oracle_f32_to_f16.argtypes = [ctypes.c_float]
+            lib.oracle_f32_to_f16.restype = ctypes.c_uint16
+            lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_to_f32.restype = ctypes.c_float
+            lib.oracle_silu.argtypes = [ctypes.c_double]
+            lib.oracle_silu.restype = ctypes.c_double
+            lib.oracle_q4k_scale_min.argtypes = [P, ctypes.c_int, P, P]
+            lib.oracle_q4k_dequant.argtypes = [P, P, I64, I64]
+            lib.oracle_q4k_quantize.argtypes = [P, P, I64, I64]
+            lib.oracle_swiglu_ffn.argtypes = [P, P, P, P, I64, I64, I64, P]
+            lib.oracle_moe_swiglu_ffn.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, I64, P]
+            for f in ("oracle_q4k_dequant", "oracle_q4k_quantize",
+                      "oracle_swiglu_ffn", "oracle_moe_swiglu_ffn",
+                      "oracle_q4k_scale_min"):
+                getattr(lib, f).restype = None
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+# ---- scalar helpers ------------------------------------------------------
+
+def f16_to_f32(bits: int) -> float:
+    return float(_load().oracle_f16_to_f32(int(bits)))
+
+
+def f32_to_f16(x: float) -> int:
+    return int(_load().oracle_f32_to_f16(float(x)))
+
+
+def bf16_to_f32(bits: int) -> float:
+    return float(_load().oracle_bf16_to_f32(int(bits)))
+
+
+def silu(g: float) -> float:
+    return float(_load().oracle_silu(float(g)))
+
+
+def scale_min(scales12: bytes, j: int):
+    buf = np.frombuffer(bytes(scales12), dtype=np.uint8).copy()
+    sc = ctypes.c_int()
+    m = ctypes.c_int()
+    _load().oracle_q4k_scale_min(_ptr(buf), int(j), ctypes.byref(sc), ctypes.byref(m))
+    return sc.value, m.value
+
+
+# ---- Q4_K ----------------------------------------------------------------
+
+def q4k_dequant(blocks: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    """Dequantise ``rows`` rows of Q4_K blocks to an fp32 [rows, cols] array."""
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+    assert blocks.size >= rows * row_bytes(cols)
+    out = np.empty((rows, cols), dtype=np.float32)
+    _load().oracle_q4k_dequant(_ptr(blocks), _ptr(out), rows, cols)
+    return out
+
+
+def q4k_quantize(w: np.ndarray) -> np.ndarray:
+    """Quantise an fp32 [rows, cols] matrix to Q4_K rows (min/max quantiser)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    rows, cols = w.shape
+    out = np.zeros((rows, row_bytes(cols)), dtype=np.uint8)
+    _load().oracle_q4k_quantize(_ptr(w), _ptr(out), rows, cols)
+    return out
+
+
+# ---- feed-forward ----------------------------------------------------------
+
+def swiglu_ffn(x_bf16: np.ndarray, Wg: np.ndarray, Wu: np.ndarray, Wd: np.ndarray,
+               T: int, H: int, I: int) -> np.ndarray:
+    """y[T, H] in float64 for bf16 bits x[T, H] and Q4_K weights."""
+    x_bf16 = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    Wg = np.ascontiguousarray(Wg, dtype=np.uint8)
+    Wu = np.ascontiguousarray(Wu, dtype=np.uint8)
+    Wd = np.ascontiguousarray(Wd, dtype=np.uint8)
+    assert x_bf16.size == T * H
+    assert Wg.size == I * row_bytes(H) and Wu.size == I * row_bytes(H)
+    assert Wd.size == H * row_bytes(I)
+    y = np.empty((T, H), dtype=np.float64)
+    _load().oracle_swiglu_ffn(_ptr(x_bf16), _ptr(Wg), _ptr(Wu), _ptr(Wd), T, H, I, _ptr(y))
+    return y
+
+
+def moe_swiglu_ffn(x_bf16: np.ndarray, ids: np.ndarray, wts: np.ndarray,
+                   Wg: np.ndarray, Wu: np.ndarray, Wd: np.ndarray,
+                   T: int, H: int, I: int, E: int, top_k: int) -> np.ndarray:
+    """y[T, H] float64 for the routed experts; weights stacked [E, rows, bytes]."""
+    x_bf16 = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    wts = np.ascontiguousarray(wts, dtype=np.float32)
+    Wg = np.ascontiguousarray(Wg, dtype=np.uint8)
+    Wu = np.ascontiguousarray(Wu, dtype=np.uint8)
+    Wd = np.ascontiguousarray(Wd, dtype=np.uint8)
+    assert ids.size == T * top_k and wts.size == T * top_k
+    assert Wg.size == E * I * row_bytes(H) and Wd.size == E * H * row_bytes(I)
+    y = np.empty((T, H), dtype=np.float64)
+    _load().oracle_moe_swiglu_ffn(_ptr(x_bf16), _ptr(ids), _ptr(wts), _ptr(Wg), _ptr(Wu),
+                                  _ptr(Wd), T, H, I, E, top_k, _ptr(y))
+    return y
