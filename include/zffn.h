@@ -1,0 +1,159 @@
+/*
+ * zffn.h -- C ABI of the fused Q4_K SwiGLU feed-forward library (GB300, sm_103a).
+ *
+ * The block computed is
+ *     y = W_down . ( silu(W_gate . x)  (*)  (W_up . x) ),   silu(g) = g / (1 + e^-g)
+ * with the hidden state of width H projected up twice to the intermediate
+ * width I and back down ("Fused SwiGLU MLP: ZINC RDNA4 Down-Projection
+ * Bandwidth", section "The MLP is two trips up to a wider width").  Weights
+ * stay in Q4_K super-blocks and are unpacked on chip on their way into the
+ * multiply (same page, FAQ "Why is fusing the SwiGLU intermediate harder than
+ * fusing the weight dequant?"); the SwiGLU intermediate is produced and
+ * consumed on chip and never written to device memory (same page, section
+ * "Why this fusion is harder than the last one").
+ *
+ * Q4_K layout used throughout (144 bytes per 256 weights, little endian):
+ *   bytes 0..1 d (binary16), 2..3 dmin (binary16), 4..15 twelve bytes holding
+ *   eight 6-bit (scale, min) pairs, 16..143 the 4-bit codes; code byte 32g+l
+ *   holds weight 64g+l (low nibble) and weight 64g+32+l (high nibble);
+ *   w = d*scale*q - dmin*min.
+ * A matrix of R rows and C columns is R consecutive rows of ceil(C/256)
+ * consecutive blocks (zffn_q4k_row_bytes(C) bytes per row).  Weights past
+ * column C in a row's last block are ignored.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named x, y, W*, blocks, out, expert_* are DEVICE pointers owned
+ *     by the caller; the library never frees or retains them.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     call is asynchronous and stream-ordered; none synchronises the host
+ *     except zffn_get_device_error, and none reads device data on the host.
+ *   - Argument checks run on the host before anything is launched; a failed
+ *     check returns ZFFN_ERR_INVALID_ARG (or ZFFN_ERR_UNSUPPORTED) and launches
+ *     nothing.  A failed launch returns ZFFN_ERR_CUDA.
+ *   - Every device-side wait is bounded.  A wait that runs out records
+ *     ZFFN_ERR_TIMEOUT in the device error word (read with
+ *     zffn_get_device_error) and the kernel returns; it never traps or hangs.
+ *   - The current CUDA device at the time of the call is the device used.
+ */
+#ifndef ZFFN_H
+#define ZFFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ZFFN_OK = 0,
+    ZFFN_ERR_INVALID_ARG = 1,  /* a host-side argument check failed; nothing launched */
+    ZFFN_ERR_UNSUPPORTED = 2,  /* valid call, shape/device this build does not handle */
+    ZFFN_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed                 */
+    ZFFN_ERR_TIMEOUT = 4,      /* a bounded device-side wait ran out                   */
+    ZFFN_ERR_NO_WORKSPACE = 5  /* library workspace could not be allocated             */
+} zffn_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *zffn_status_string(zffn_status s);
+
+/* Bytes of one Q4_K row of `cols` weights: ceil(cols/256) * 144.  0 if cols <= 0. */
+size_t zffn_q4k_row_bytes(int64_t cols);
+
+/* Unpack Q4_K to fp32.
+ *   blocks: rows * zffn_q4k_row_bytes(cols) bytes (any alignment).
+ *   out:    fp32 [rows][cols] row-major.
+ * Each output is the correctly rounded fp32 value of d*scale*q - dmin*min (the
+ * two products are exact in fp32), so the result is bit-exact.
+ * Errors: INVALID_ARG if a pointer is NULL or rows/cols <= 0. */
+zffn_status zffn_q4k_dequant(const void *blocks, float *out, int64_t rows, int64_t cols,
+                             void *stream);
+
+/* Quantise fp32 weights to Q4_K with the min/max quantiser (the pages name no
+ * quantiser; the source workloads quantise fp32 weights "min/max"):
+ *   per 32-weight sub-block: lo = min(0, min w), hi = max w,
+ *                            scale = (hi-lo)/15, min = -lo;
+ *   per block: d = fp16(max scale / 63), dmin = fp16(max min / 63),
+ *              sc = clamp(rint(scale/d), 0, 63), m = clamp(rint(min/dmin), 0, 63);
+ *   per weight: q = clamp(rint((w + dmin*m) / (d*sc)), 0, 15);
+ * every step in IEEE fp32 round-to-nearest-even (0 where a divisor is 0).
+ * Columns past `cols` in a row's last block are quantised as zeros.
+ *   w:      fp32 [rows][cols] row-major.
+ *   blocks: output, rows * zffn_q4k_row_bytes(cols) bytes.
+ * Errors: INVALID_ARG if a pointer is NULL or rows/cols <= 0. */
+zffn_status zffn_q4k_quantize(const float *w, void *blocks, int64_t rows, int64_t cols,
+                              void *stream);
+
+/* Dense SwiGLU block over T tokens.
+ *   x:  bf16 [T][H] row-major, 16-byte aligned.
+ *   Wg, Wu: Q4_K, I rows of H/256 blocks (W_gate, W_up: [I x H]), 16-byte aligned.
+ *   Wd: Q4_K, H rows of ceil(I/256) blocks (W_down: [H x I]), 16-byte aligned.
+ *   y:  fp32 [T][H] row-major, overwritten, 16-byte aligned.
+ * Requirements: T >= 1, H % 256 == 0, I % 64 == 0, 256 <= H <= 16384,
+ * 64 <= I <= 65536.  T <= 1 runs the memory-bound single-token kernel; larger T
+ * run the tensor-core prefill kernel (the switch-over can be changed with
+ * zffn_set_option).  Accumulation is fp32; operands of the tensor-core path are
+ * rounded to bf16 (x is bf16 already; unpacked weights and the SwiGLU
+ * intermediate are rounded to bf16 on chip).
+ * Uses library workspace (see zffn_reserve) on the single-token path.
+ * Errors: INVALID_ARG (NULL, misaligned, bad sizes), CUDA, NO_WORKSPACE. */
+zffn_status zffn_swiglu_q4k(const void *x, const void *Wg, const void *Wu, const void *Wd,
+                            float *y, int T, int H, int I, void *stream);
+
+/* Mixture-of-experts SwiGLU block:
+ *     y[t] = sum_{j < top_k} expert_weights[t][j] * FFN_{expert_ids[t][j]}(x[t])
+ * ("Four bottlenecks, one CUDA backend...", section "Bottleneck 2 -- MoE decode
+ * was paying for its routing twice": the chosen expert ids are read from a
+ * device buffer by the kernels; nothing is read back to the host).
+ *   x:  bf16 [T][H].
+ *   expert_ids: int32 [T][top_k] (device).  An id outside [0, E) contributes 0.
+ *   expert_weights: fp32 [T][top_k] (device).
+ *   Wg, Wu: E stacked experts, each I rows of H/256 blocks.
+ *   Wd: E stacked experts, each H rows of ceil(I/256) blocks.
+ *   y:  fp32 [T][H], overwritten.
+ * Requirements as zffn_swiglu_q4k, plus 1 <= E <= 4096, 1 <= top_k <= 64.
+ * Uses library workspace (see zffn_reserve).
+ * Errors: INVALID_ARG, CUDA, NO_WORKSPACE. */
+zffn_status zffn_moe_swiglu_q4k(const void *x, const int32_t *expert_ids,
+                                const float *expert_weights, const void *Wg, const void *Wu,
+                                const void *Wd, float *y, int T, int H, int I, int E,
+                                int top_k, void *stream);
+
+/* Allocate (or grow) the current device's workspace for calls up to the given
+ * sizes, so that later calls allocate nothing (call it before capturing calls
+ * into a CUDA graph).  Calls that share a device share its workspace: issue
+ * them on one stream, or order them, since concurrent calls race on it.
+ * Errors: INVALID_ARG (a size < 1), NO_WORKSPACE. */
+zffn_status zffn_reserve(int T_max, int H_max, int I_max, int E_max, int top_k_max);
+
+/* Release every workspace the library holds (all devices).  Not stream-ordered:
+ * the caller makes sure no call is still running. */
+void zffn_release(void);
+
+/* Description of the last CUDA failure seen by a call on this host thread
+ * (static string, never NULL; "no error" if none). */
+const char *zffn_last_error(void);
+
+/* Synchronise `stream`, then return and clear the current device's error word:
+ * ZFFN_OK, or ZFFN_ERR_TIMEOUT if a bounded device wait ran out since the last
+ * read.  ZFFN_ERR_CUDA if the synchronisation itself failed. */
+zffn_status zffn_get_device_error(void *stream);
+
+/* Tunables (process-wide).  ZFFN_OPT_MATVEC_MAX_T: largest token count T, dense
+ * or routed, sent to the memory-bound single-token kernel (default 1; 0 sends
+ * every call to the tensor-core kernel).  Returns the previous value, or -1
+ * for an unknown key. */
+enum { ZFFN_OPT_MATVEC_MAX_T = 1 };
+int zffn_set_option(int key, int value);
+
+/* Self-test of the bounded-wait machinery: launches one block that waits on an
+ * mbarrier nothing will ever complete, with a budget of `budget_cycles` SM
+ * clocks; the wait gives up, records ZFFN_ERR_TIMEOUT in the device error word
+ * and the kernel returns normally.  Errors: INVALID_ARG (budget < 1), CUDA. */
+zffn_status zffn_selftest_wait_timeout(int64_t budget_cycles, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZFFN_H */

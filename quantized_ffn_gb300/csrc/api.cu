@@ -1,0 +1,357 @@
+// api.cu -- the C ABI: host-side argument checks, per-device state (error
+// word, workspace), and the choice between the single-token kernel and the
+// tensor-core kernel.  Every step of the computation runs in this library's
+// kernels; there is no host fallback.
+#include <mutex>
+
+#include "zffn_internal.cuh"
+
+namespace zffn {
+
+static __device__ int g_device_error;   // one per device that loads the library
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct Workspace {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+    unsigned *barrier = nullptr;   // first 256 bytes: grid-barrier words (zeroed)
+};
+
+std::mutex g_mu;
+DeviceInfo g_info[kMaxDevices];
+Workspace g_ws[kMaxDevices];
+int g_matvec_max_t = 1;
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+// Sub-buffers carved out of one device allocation.
+struct Layout {
+    size_t barrier, h, counts, offsets, cursors, tiles, n_tiles, row_token, row_weight, x_perm,
+        total;
+    int max_tiles;
+};
+
+Layout layout_for(int T, int H, int I, int E, int k) {
+    Layout L;
+    size_t o = 0;
+    const int64_t P = (int64_t)T * k;
+    L.max_tiles = (int)((P + 127) / 128 + (E < P ? E : P));
+    L.barrier = o; o = align_up(o + 2 * sizeof(unsigned));
+    L.h = o; o = align_up(o + (size_t)P * I * sizeof(float));
+    L.counts = o; o = align_up(o + (size_t)E * sizeof(int));
+    L.offsets = o; o = align_up(o + (size_t)(E + 1) * sizeof(int));
+    L.cursors = o; o = align_up(o + (size_t)E * sizeof(int));
+    L.tiles = o; o = align_up(o + (size_t)L.max_tiles * sizeof(int4));
+    L.n_tiles = o; o = align_up(o + sizeof(int));
+    L.row_token = o; o = align_up(o + (size_t)P * sizeof(int));
+    L.row_weight = o; o = align_up(o + (size_t)P * sizeof(float));
+    L.x_perm = o; o = align_up(o + (size_t)P * H * 2);
+    L.total = o;
+    return L;
+}
+
+int current_device() {
+    int d = -1;
+    if (cudaGetDevice(&d) != cudaSuccess) return -1;
+    return d;
+}
+
+// Make sure the current device's workspace holds at least `bytes`.
+zffn_status ensure_workspace(size_t bytes, Workspace **out) {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return ZFFN_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    Workspace &w = g_ws[dev];
+    if (w.bytes < bytes) {
+        if (w.ptr) {
+            // the old buffer may still be in use by queued work on the device
+            if (cudaDeviceSynchronize() != cudaSuccess) return ZFFN_ERR_CUDA;
+            cudaFree(w.ptr);
+            w = Workspace{};
+        }
+        void *p = nullptr;
+        if (cudaMalloc(&p, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return ZFFN_ERR_NO_WORKSPACE;
+        }
+        if (cudaMemset(p, 0, kAlign) != cudaSuccess) {
+            cudaFree(p);
+            return ZFFN_ERR_CUDA;
+        }
+        w.ptr = p;
+        w.bytes = bytes;
+        w.barrier = static_cast<unsigned *>(p);
+    }
+    *out = &w;
+    return ZFFN_OK;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+zffn_status check_shape(int T, int H, int I) {
+    if (T < 1 || H < 256 || H > 16384 || H % 256 != 0 || I < 64 || I > 65536 || I % 64 != 0)
+        return ZFFN_ERR_INVALID_ARG;
+    return ZFFN_OK;
+}
+
+thread_local const char *t_last_error = "no error";
+
+zffn_status to_status(cudaError_t e) {
+    if (e == cudaSuccess) return ZFFN_OK;
+    t_last_error = cudaGetErrorString(e);
+    cudaGetLastError();
+    return ZFFN_ERR_CUDA;
+}
+
+}  // namespace
+
+const DeviceInfo &device_info() {
+    const int dev = current_device();
+    static DeviceInfo none;
+    if (dev < 0 || dev >= kMaxDevices) return none;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo &di = g_info[dev];
+    if (di.device != dev) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return none;
+        di.num_sms = prop.multiProcessorCount;
+        di.max_smem_optin = (int)prop.sharedMemPerBlockOptin;
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess) return none;
+        di.err_word = static_cast<int *>(addr);
+        di.device = dev;
+    }
+    return di;
+}
+
+}  // namespace zffn
+
+using namespace zffn;
+
+extern "C" {
+
+const char *zffn_status_string(zffn_status s) {
+    switch (s) {
+        case ZFFN_OK: return "ZFFN_OK";
+        case ZFFN_ERR_INVALID_ARG: return "ZFFN_ERR_INVALID_ARG";
+        case ZFFN_ERR_UNSUPPORTED: return "ZFFN_ERR_UNSUPPORTED";
+        case ZFFN_ERR_CUDA: return "ZFFN_ERR_CUDA";
+        case ZFFN_ERR_TIMEOUT: return "ZFFN_ERR_TIMEOUT";
+        case ZFFN_ERR_NO_WORKSPACE: return "ZFFN_ERR_NO_WORKSPACE";
+    }
+    return "ZFFN_UNKNOWN_STATUS";
+}
+
+size_t zffn_q4k_row_bytes(int64_t cols) {
+    return cols <= 0 ? 0 : (size_t)q4k_row_bytes(cols);
+}
+
+zffn_status zffn_q4k_dequant(const void *blocks, float *out, int64_t rows, int64_t cols,
+                             void *stream) {
+    if (!blocks || !out || rows <= 0 || cols <= 0) return ZFFN_ERR_INVALID_ARG;
+    if (device_info().device < 0) return ZFFN_ERR_CUDA;
+    return to_status(launch_q4k_dequant(blocks, out, rows, cols, (cudaStream_t)stream));
+}
+
+zffn_status zffn_q4k_quantize(const float *w, void *blocks, int64_t rows, int64_t cols,
+                              void *stream) {
+    if (!w || !blocks || rows <= 0 || cols <= 0) return ZFFN_ERR_INVALID_ARG;
+    if (device_info().device < 0) return ZFFN_ERR_CUDA;
+    return to_status(launch_q4k_quantize(w, blocks, rows, cols, (cudaStream_t)stream));
+}
+
+zffn_status zffn_swiglu_q4k(const void *x, const void *Wg, const void *Wu, const void *Wd,
+                            float *y, int T, int H, int I, void *stream) {
+    if (!x || !Wg || !Wu || !Wd || !y) return ZFFN_ERR_INVALID_ARG;
+    if (check_shape(T, H, I) != ZFFN_OK) return ZFFN_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd) || !aligned16(y))
+        return ZFFN_ERR_INVALID_ARG;
+    const DeviceInfo &di = device_info();
+    if (di.device < 0) return ZFFN_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    int mv_max;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        mv_max = g_matvec_max_t;
+    }
+    if (T <= mv_max && matvec_smem_bytes(T, H, I, 1) <= (size_t)di.max_smem_optin) {
+        const Layout L = layout_for(T, H, I, 1, 1);
+        Workspace *w = nullptr;
+        zffn_status st = ensure_workspace(L.total, &w);
+        if (st != ZFFN_OK) return st;
+        uint8_t *base = static_cast<uint8_t *>(w->ptr);
+        MatvecArgs a{};
+        a.x = static_cast<const __nv_bfloat16 *>(x);
+        a.Wg = static_cast<const uint8_t *>(Wg);
+        a.Wu = static_cast<const uint8_t *>(Wu);
+        a.Wd = static_cast<const uint8_t *>(Wd);
+        a.ids = nullptr;
+        a.wts = nullptr;
+        a.y = y;
+        a.h = reinterpret_cast<float *>(base + L.h);
+        a.barrier = reinterpret_cast<unsigned *>(base + L.barrier);
+        a.err = di.err_word;
+        a.T = T; a.H = H; a.I = I; a.E = 1; a.k = 1;
+        return to_status(launch_ffn_matvec(a, s));
+    }
+    cudaError_t e = launch_zero_f32(y, (int64_t)T * H, s);
+    if (e != cudaSuccess) return to_status(e);
+    TcArgs a{};
+    a.x = x;
+    a.x_rows = T;
+    a.Wg = static_cast<const uint8_t *>(Wg);
+    a.Wu = static_cast<const uint8_t *>(Wu);
+    a.Wd = static_cast<const uint8_t *>(Wd);
+    a.y = y;
+    a.tiles = nullptr;
+    a.n_tiles_dev = nullptr;
+    a.row_token = nullptr;
+    a.row_weight = nullptr;
+    a.n_tiles_host = (T + 127) / 128;
+    a.err = di.err_word;
+    a.T = T; a.H = H; a.I = I;
+    return to_status(launch_ffn_tc(a, s));
+}
+
+zffn_status zffn_moe_swiglu_q4k(const void *x, const int32_t *expert_ids,
+                                const float *expert_weights, const void *Wg, const void *Wu,
+                                const void *Wd, float *y, int T, int H, int I, int E, int top_k,
+                                void *stream) {
+    if (!x || !expert_ids || !expert_weights || !Wg || !Wu || !Wd || !y)
+        return ZFFN_ERR_INVALID_ARG;
+    if (check_shape(T, H, I) != ZFFN_OK) return ZFFN_ERR_INVALID_ARG;
+    if (E < 1 || E > 4096 || top_k < 1 || top_k > 64) return ZFFN_ERR_INVALID_ARG;
+    if ((int64_t)T * top_k > (1 << 24)) return ZFFN_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd) || !aligned16(y) ||
+        (reinterpret_cast<uintptr_t>(expert_ids) & 3) ||
+        (reinterpret_cast<uintptr_t>(expert_weights) & 3))
+        return ZFFN_ERR_INVALID_ARG;
+    const DeviceInfo &di = device_info();
+    if (di.device < 0) return ZFFN_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    int mv_max;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        mv_max = g_matvec_max_t;
+    }
+    const Layout L = layout_for(T, H, I, E, top_k);
+    Workspace *w = nullptr;
+    zffn_status st = ensure_workspace(L.total, &w);
+    if (st != ZFFN_OK) return st;
+    uint8_t *base = static_cast<uint8_t *>(w->ptr);
+    if (T <= mv_max && matvec_smem_bytes(T, H, I, top_k) <= (size_t)di.max_smem_optin) {
+        MatvecArgs a{};
+        a.x = static_cast<const __nv_bfloat16 *>(x);
+        a.Wg = static_cast<const uint8_t *>(Wg);
+        a.Wu = static_cast<const uint8_t *>(Wu);
+        a.Wd = static_cast<const uint8_t *>(Wd);
+        a.ids = expert_ids;
+        a.wts = expert_weights;
+        a.y = y;
+        a.h = reinterpret_cast<float *>(base + L.h);
+        a.barrier = reinterpret_cast<unsigned *>(base + L.barrier);
+        a.err = di.err_word;
+        a.T = T; a.H = H; a.I = I; a.E = E; a.k = top_k;
+        return to_status(launch_ffn_matvec(a, s));
+    }
+    RouteArgs r{};
+    r.ids = expert_ids;
+    r.wts = expert_weights;
+    r.x = static_cast<const __nv_bfloat16 *>(x);
+    r.T = T; r.H = H; r.E = E; r.k = top_k;
+    r.counts = reinterpret_cast<int *>(base + L.counts);
+    r.offsets = reinterpret_cast<int *>(base + L.offsets);
+    r.cursors = reinterpret_cast<int *>(base + L.cursors);
+    r.tiles = reinterpret_cast<int4 *>(base + L.tiles);
+    r.n_tiles = reinterpret_cast<int *>(base + L.n_tiles);
+    r.row_token = reinterpret_cast<int *>(base + L.row_token);
+    r.row_weight = reinterpret_cast<float *>(base + L.row_weight);
+    r.x_perm = reinterpret_cast<__nv_bfloat16 *>(base + L.x_perm);
+    r.max_tiles = L.max_tiles;
+    cudaError_t e = launch_moe_route(r, s);
+    if (e != cudaSuccess) return to_status(e);
+    e = launch_zero_f32(y, (int64_t)T * H, s);
+    if (e != cudaSuccess) return to_status(e);
+    TcArgs a{};
+    a.x = r.x_perm;
+    a.x_rows = (int64_t)T * top_k;
+    a.Wg = static_cast<const uint8_t *>(Wg);
+    a.Wu = static_cast<const uint8_t *>(Wu);
+    a.Wd = static_cast<const uint8_t *>(Wd);
+    a.y = y;
+    a.tiles = r.tiles;
+    a.n_tiles_dev = r.n_tiles;
+    a.row_token = r.row_token;
+    a.row_weight = r.row_weight;
+    a.n_tiles_host = L.max_tiles;
+    a.err = di.err_word;
+    a.T = T; a.H = H; a.I = I;
+    return to_status(launch_ffn_tc(a, s));
+}
+
+zffn_status zffn_reserve(int T_max, int H_max, int I_max, int E_max, int top_k_max) {
+    if (T_max < 1 || H_max < 1 || I_max < 1 || E_max < 1 || top_k_max < 1)
+        return ZFFN_ERR_INVALID_ARG;
+    if (device_info().device < 0) return ZFFN_ERR_CUDA;
+    const Layout L = layout_for(T_max, H_max, I_max, E_max, top_k_max);
+    Workspace *w = nullptr;
+    return ensure_workspace(L.total, &w);
+}
+
+void zffn_release(void) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    int prev = -1;
+    cudaGetDevice(&prev);
+    for (int d = 0; d < kMaxDevices; ++d) {
+        if (g_ws[d].ptr) {
+            cudaSetDevice(d);
+            cudaFree(g_ws[d].ptr);
+            g_ws[d] = Workspace{};
+        }
+    }
+    if (prev >= 0) cudaSetDevice(prev);
+}
+
+zffn_status zffn_get_device_error(void *stream) {
+    const DeviceInfo &di = device_info();
+    if (di.device < 0) return ZFFN_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    int v = 0;
+    if (cudaMemcpyAsync(&v, di.err_word, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return to_status(cudaErrorUnknown);
+    if (cudaMemsetAsync(di.err_word, 0, sizeof(int), s) != cudaSuccess) return ZFFN_ERR_CUDA;
+    if (v != 0) {
+        // a timed-out grid barrier may have left its counter mid-way: reset it
+        std::lock_guard<std::mutex> lk(g_mu);
+        Workspace &w = g_ws[di.device];
+        if (w.barrier && cudaMemsetAsync(w.barrier, 0, 2 * sizeof(unsigned), s) != cudaSuccess)
+            return ZFFN_ERR_CUDA;
+    }
+    if (cudaStreamSynchronize(s) != cudaSuccess) return to_status(cudaErrorUnknown);
+    return v == 0 ? ZFFN_OK : (zffn_status)v;
+}
+
+const char *zffn_last_error(void) { return t_last_error; }
+
+int zffn_set_option(int key, int value) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (key == ZFFN_OPT_MATVEC_MAX_T) {
+        const int old = g_matvec_max_t;
+        g_matvec_max_t = value < 0 ? 0 : value;
+        return old;
+    }
+    return -1;
+}
+
+zffn_status zffn_selftest_wait_timeout(int64_t budget_cycles, void *stream) {
+    if (budget_cycles < 1) return ZFFN_ERR_INVALID_ARG;
+    const DeviceInfo &di = device_info();
+    if (di.device < 0) return ZFFN_ERR_CUDA;
+    return to_status(launch_wait_timeout_selftest(budget_cycles, di.err_word, (cudaStream_t)stream));
+}
+
+}  // extern "C"

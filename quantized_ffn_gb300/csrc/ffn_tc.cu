@@ -1,0 +1,551 @@
+// ffn_tc.cu -- the fused prefill kernel on the 5th-generation tensor cores.
+//
+// What it computes, per (token tile, intermediate chunk) work unit:
+//   for each 128-row slice s of the chunk:
+//       [G | U] = X_tile . [W_gate rows ; W_up rows]^T        (tcgen05, TMEM)
+//       h[:, s] = bf16( silu(G) * U )                           (epilogue -> SMEM)
+//   for each 256-column slice n of the output:
+//       Y = h . W_down[n rows, chunk cols]^T                   (tcgen05, TMEM)
+//       y[token, n cols] += Y                                   (fp32 reductions in L2)
+// This is the producer/consumer interleave along the intermediate dimension
+// ("Fused SwiGLU MLP: ZINC RDNA4 Down-Projection Bandwidth", section "Why
+// this fusion is harder than the last one"): a block of the intermediate is
+// computed, staged on chip, and contracted by the down projection before the
+// next block; only x and y touch device memory.  Q4_K weights are unpacked
+// on chip on their way into the multiply (same page, FAQ "Why is fusing the
+// SwiGLU intermediate harder..."): dedicated warps read the packed blocks and
+// write bf16 operand tiles straight into shared memory; no unpacked copy of a
+// weight ever exists in device memory.  The scale/min pair of a sub-block is
+// decoded once per row and step, not per weight ("VGPR pressure caps the
+// fused RDNA4 prefill GEMM at nine waves", section "The recoverable registers
+// versus the stubborn ones"); accumulators live in tensor memory, not in
+// registers, which removes the register-pressure problem at its root.
+//
+// Block roles (10 warps):
+//   warp 0      TMA producer: x tiles [128 x 64] bf16, 128-byte swizzle
+//   warp 1      TMEM allocator and single-thread MMA issuer
+//   warps 2-5   weight producers: Q4_K -> bf16 tiles [256 x 64], same swizzle
+//   warps 6-9   epilogue: TMEM -> registers; SwiGLU -> h in SMEM, or the
+//               down-projection tile -> y
+// Two TMEM accumulator slots of 256 columns each alternate between jobs, so
+// the epilogue of one job overlaps the MMAs of the next.
+#include <cudaTypedefs.h>
+
+#include "zffn_internal.cuh"
+
+namespace zffn {
+namespace tc {
+
+constexpr int BM = 128;                  // token rows per tile (UMMA M)
+constexpr int BK = 64;                   // K per pipeline step (128 bytes of bf16)
+constexpr int GU_ROWS = 128;             // intermediate rows per gate/up job
+constexpr int NJ = 256;                  // UMMA N of every job
+constexpr int IC = 256;                  // intermediate columns per work unit
+constexpr int NA = 3;                    // x stages
+constexpr int NB = 3;                    // weight stages
+constexpr int A_BYTES = BM * BK * 2;     // 16 KB
+constexpr int B_BYTES = NJ * BK * 2;     // 32 KB
+constexpr int HT_BYTES = BM * BK * 2;    // one 64-column slice of h: 16 KB
+constexpr int N_HT = IC / BK;            // 4
+constexpr int OFF_H = 0;
+constexpr int OFF_A = OFF_H + N_HT * HT_BYTES;
+constexpr int OFF_B = OFF_A + NA * A_BYTES;
+constexpr int OFF_BAR = OFF_B + NB * B_BYTES;
+constexpr int N_BARS = 2 * NA + 2 * NB + 4 + 3;
+constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + alignment slack
+static_assert(SMEM_BYTES <= 232448, "shared memory budget of one block");
+constexpr int THREADS = 320;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t IDESC = idesc_bf16_f32(BM, NJ);
+
+struct Params {
+    const uint8_t *Wg, *Wu, *Wd;
+    float *y;
+    const int4 *tiles;
+    const int *n_tiles_dev;
+    const int *row_token;
+    const float *row_weight;
+    int *err;
+    int n_tiles_host;
+    int T, H, I;
+};
+
+struct Tile {
+    int row_start, row_count, expert;
+};
+
+__device__ __forceinline__ Tile get_tile(const Params &p, int t) {
+    Tile r;
+    if (p.tiles) {
+        const int4 v = p.tiles[t];
+        r.row_start = v.x;
+        r.row_count = v.y;
+        r.expert = v.z;
+    } else {
+        r.row_start = t * BM;
+        r.row_count = min(BM, p.T - t * BM);
+        r.expert = 0;
+    }
+    return r;
+}
+
+// Byte offset of 16-byte chunk c of row r in a [rows x 64] bf16 tile laid out
+// K-major with the 128-byte swizzle (groups of 8 rows, 1024 bytes apart).
+__device__ __forceinline__ uint32_t sw128_row(int r) {
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
+}
+
+// Raw bytes of one weight row for one K step: block header + 32 code bytes.
+struct RawRow {
+    uint4 hd, q0, q1;
+};
+
+__device__ __forceinline__ void load_raw(RawRow &r, const uint8_t *blk, int g) {
+    r.hd = __ldg(reinterpret_cast<const uint4 *>(blk));
+    r.q0 = __ldg(reinterpret_cast<const uint4 *>(blk + 16 + 32 * g));
+    r.q1 = __ldg(reinterpret_cast<const uint4 *>(blk + 32 + 32 * g));
+}
+
+// Unpack 64 weights (K step g of a block) into one swizzled bf16 row.
+// A code q is turned into the float 1 + q/128 (low nibbles, placed at bits
+// 16..19) or 1 + q/2048 (high nibbles, bits 12..15) by OR-ing it into the
+// bits of 1.0f; then d*sc*q - dmin*m = (S*d*sc)*f - (S*d*sc + dmin*m) with
+// S = 128 or 2048, one fused multiply-add per weight.  The constant is
+// rounded once, an error below 2^-13 of one quantisation step, far under the
+// bf16 rounding of the result.
+__device__ __forceinline__ void unpack_row_to_smem(const RawRow &r, int g, uint32_t row_addr,
+                                                   int row) {
+    const float d = half_bits_to_float(r.hd.x), dmin = half_bits_to_float(r.hd.x >> 16);
+    int sc0, m0, sc1, m1;
+    q4k_scale_min(r.hd.y, r.hd.z, r.hd.w, 2 * g, sc0, m0);
+    q4k_scale_min(r.hd.y, r.hd.z, r.hd.w, 2 * g + 1, sc1, m1);
+    const float a0 = 128.0f * (d * (float)sc0);
+    const float c0 = -(a0 + dmin * (float)m0);
+    const float a1 = 2048.0f * (d * (float)sc1);
+    const float c1 = -(a1 + dmin * (float)m1);
+    const uint32_t w[8] = {r.q0.x, r.q0.y, r.q0.z, r.q0.w, r.q1.x, r.q1.y, r.q1.z, r.q1.w};
+    constexpr uint32_t ONE = 0x3F800000u, MLO = 0x000F0000u, MHI = 0x0000F000u;
+    uint32_t lo[16], hi[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t x = w[i], xl8 = x << 8, xr8 = x >> 8, xl16 = x << 16, xr16 = x >> 16;
+        // low nibbles of bytes 0..3 -> weights 4i..4i+3 of the step's first 32
+        const float l0 = fmaf(a0, __uint_as_float((xl16 & MLO) | ONE), c0);
+        const float l1 = fmaf(a0, __uint_as_float((xl8 & MLO) | ONE), c0);
+        const float l2 = fmaf(a0, __uint_as_float((x & MLO) | ONE), c0);
+        const float l3 = fmaf(a0, __uint_as_float((xr8 & MLO) | ONE), c0);
+        // high nibbles -> weights 32+4i..32+4i+3
+        const float h0 = fmaf(a1, __uint_as_float((xl8 & MHI) | ONE), c1);
+        const float h1 = fmaf(a1, __uint_as_float((x & MHI) | ONE), c1);
+        const float h2 = fmaf(a1, __uint_as_float((xr8 & MHI) | ONE), c1);
+        const float h3 = fmaf(a1, __uint_as_float((xr16 & MHI) | ONE), c1);
+        lo[2 * i] = pack_bf16x2(l0, l1);
+        lo[2 * i + 1] = pack_bf16x2(l2, l3);
+        hi[2 * i] = pack_bf16x2(h0, h1);
+        hi[2 * i + 1] = pack_bf16x2(h2, h3);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        st_shared_v4(row_addr + (((uint32_t)(c ^ (row & 7))) << 4), lo[4 * c], lo[4 * c + 1],
+                     lo[4 * c + 2], lo[4 * c + 3]);
+        st_shared_v4(row_addr + (((uint32_t)((c + 4) ^ (row & 7))) << 4), hi[4 * c],
+                     hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+    }
+}
+
+__device__ __forceinline__ void zero_row_smem(uint32_t row_addr) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) st_shared_v4(row_addr + (c << 4), 0u, 0u, 0u, 0u);
+}
+
+// Work-unit geometry shared by every role.
+struct Unit {
+    Tile tile;
+    int i0;       // first intermediate column of the chunk
+    int ic;       // columns in this chunk (multiple of 64)
+    int n_gu;     // gate/up jobs
+    int ks_gu;    // K steps per gate/up job
+    int ks_y;     // K steps per down job
+    int n_y;      // down jobs
+};
+
+__device__ __forceinline__ Unit make_unit(const Params &p, int u, int n_tiles) {
+    Unit un;
+    const int chunk = u / n_tiles;
+    un.tile = get_tile(p, u % n_tiles);
+    un.i0 = chunk * IC;
+    un.ic = min(IC, p.I - un.i0);
+    un.n_gu = (un.ic + GU_ROWS - 1) / GU_ROWS;
+    un.ks_gu = p.H / BK;
+    un.ks_y = un.ic / BK;
+    un.n_y = p.H / NJ;
+    return un;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    ffn_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the swizzled tiles
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
+    uint64_t *a_full = bars, *a_empty = bars + NA;
+    uint64_t *b_full = bars + 2 * NA, *b_empty = bars + 2 * NA + NB;
+    uint64_t *t_full = bars + 2 * NA + 2 * NB, *t_empty = t_full + 2;
+    uint64_t *h_full = t_empty + 2, *h_empty = h_full + 1, *drain = h_full + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + N_BARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t s_h = smem_u32(smem + OFF_H);
+    const uint32_t s_a = smem_u32(smem + OFF_A);
+    const uint32_t s_b = smem_u32(smem + OFF_B);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NA; ++i) {
+            mbar_init(&a_full[i], 1);
+            mbar_init(&a_empty[i], 1);
+        }
+        for (int i = 0; i < NB; ++i) {
+            mbar_init(&b_full[i], 128);
+            mbar_init(&b_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&t_full[i], 1);
+            mbar_init(&t_empty[i], 128);
+        }
+        mbar_init(h_full, 128);
+        mbar_init(h_empty, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        prefetch_tensormap(&tmap_x);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int n_tiles = p.n_tiles_dev ? min(*p.n_tiles_dev, p.n_tiles_host) : p.n_tiles_host;
+    const int n_chunks = (p.I + IC - 1) / IC;
+    const int n_units = n_tiles * n_chunks;
+    const int64_t rbH = (int64_t)(p.H / kQK) * kBlockBytes;
+    const int64_t rbI = q4k_row_bytes(p.I);
+
+    if (warp == 0) {
+        // ---------------- TMA producer: x tiles ----------------
+        if (lane == 0) {
+            uint32_t ai = 0, aph = 0;
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                const Unit un = make_unit(p, u, n_tiles);
+                for (int s = 0; s < un.n_gu && ok; ++s) {
+                    for (int ks = 0; ks < un.ks_gu; ++ks) {
+                        if (!mbar_wait(&a_empty[ai], aph ^ 1, abort_flag, p.err)) { ok = false; break; }
+                        mbar_arrive_expect_tx(&a_full[ai], A_BYTES);
+                        tma_load_2d(smem + OFF_A + ai * A_BYTES, &tmap_x, &a_full[ai], ks * BK,
+                                    un.tile.row_start);
+                        ++issued;
+                        if (++ai == NA) { ai = 0; aph ^= 1; }
+                    }
+                }
+            }
+            // Before the block may exit, every load issued here must have
+            // landed: wait (bounded) for the full barrier of the last NA
+            // stages issued (a phase that completed long ago passes at once).
+            for (uint32_t i = 0; i < NA && i < issued; ++i) {
+                if (ai == 0) { ai = NA; aph ^= 1; }
+                --ai;
+                mbar_wait(&a_full[ai], aph, nullptr, p.err, kWaitBudgetCycles / 8);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            uint32_t ai = 0, aph = 0, bi = 0, bph = 0, jc = 0, uc = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
+                const Unit un = make_unit(p, u, n_tiles);
+                for (int s = 0; s < un.n_gu && ok; ++s, ++jc) {
+                    const uint32_t slot = jc & 1, tph = (jc >> 1) & 1;
+                    if (!mbar_wait(&t_empty[slot], tph ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + slot * NJ;
+                    for (int ks = 0; ks < un.ks_gu; ++ks) {
+                        if (!mbar_wait(&a_full[ai], aph, abort_flag, p.err) ||
+                            !mbar_wait(&b_full[bi], bph, abort_flag, p.err)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint64_t da = smem_desc_k_sw128(s_a + ai * A_BYTES);
+                        const uint64_t db = smem_desc_k_sw128(s_b + bi * B_BYTES);
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            tc_mma_bf16(d_tmem, da + 2 * kk, db + 2 * kk, IDESC, (ks | kk) != 0);
+                        tc_commit(&a_empty[ai]);
+                        tc_commit(&b_empty[bi]);
+                        if (++ai == NA) { ai = 0; aph ^= 1; }
+                        if (++bi == NB) { bi = 0; bph ^= 1; }
+                    }
+                    if (ok) tc_commit(&t_full[slot]);
+                }
+                if (!ok) break;
+                // the down projection reads h: wait until the epilogue wrote all of it
+                if (!mbar_wait(h_full, uc & 1, abort_flag, p.err)) break;
+                tc_fence_after();
+                for (int n = 0; n < un.n_y && ok; ++n, ++jc) {
+                    const uint32_t slot = jc & 1, tph = (jc >> 1) & 1;
+                    if (!mbar_wait(&t_empty[slot], tph ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + slot * NJ;
+                    for (int ks = 0; ks < un.ks_y; ++ks) {
+                        if (!mbar_wait(&b_full[bi], bph, abort_flag, p.err)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint64_t da = smem_desc_k_sw128(s_h + ks * HT_BYTES);
+                        const uint64_t db = smem_desc_k_sw128(s_b + bi * B_BYTES);
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            tc_mma_bf16(d_tmem, da + 2 * kk, db + 2 * kk, IDESC, (ks | kk) != 0);
+                        tc_commit(&b_empty[bi]);
+                        if (++bi == NB) { bi = 0; bph ^= 1; }
+                    }
+                    if (ok) tc_commit(&t_full[slot]);
+                }
+                if (ok) tc_commit(h_empty);   // h may be overwritten once these MMAs finish
+            }
+            // every MMA issued here completes before TMEM is released
+            tc_commit(drain);
+            mbar_wait(drain, 0, nullptr, p.err, kWaitBudgetCycles / 8);
+        }
+    } else if (warp < 6) {
+        // ---------------- weight producers (128 threads) ----------------
+        const int tid = threadIdx.x - 64;           // 0..127: rows tid and tid + 128
+        uint32_t bi = 0, bph = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            const Unit un = make_unit(p, u, n_tiles);
+            const int e = un.tile.expert;
+            const int steps = un.n_gu * un.ks_gu + un.n_y * un.ks_y;
+            // source of row rr (0..255) at step st of this unit; nullptr = zero row
+            auto src = [&](int st, int rr, int &g) -> const uint8_t * {
+                if (st < un.n_gu * un.ks_gu) {
+                    const int s = st / un.ks_gu, ks = st % un.ks_gu;
+                    const int i = un.i0 + s * GU_ROWS + (rr & 127);
+                    g = ks & 3;
+                    if (i >= p.I) return nullptr;
+                    const uint8_t *w = rr < 128 ? p.Wg : p.Wu;
+                    return w + ((int64_t)e * p.I + i) * rbH + (int64_t)(ks >> 2) * kBlockBytes;
+                }
+                const int st2 = st - un.n_gu * un.ks_gu;
+                const int n = st2 / un.ks_y, ks = st2 % un.ks_y;
+                const int col = un.i0 + ks * BK;
+                g = (col & 255) >> 6;
+                return p.Wd + ((int64_t)e * p.H + n * NJ + rr) * rbI + (int64_t)(col >> 8) * kBlockBytes;
+            };
+            // L2 prefetch of this unit's weight rows for this thread
+            {
+                for (int s = 0; s < un.n_gu; ++s) {
+                    const int ii = un.i0 + s * GU_ROWS + tid;
+                    if (ii < p.I) {
+                        prefetch_l2_bulk(p.Wg + ((int64_t)e * p.I + ii) * rbH, (uint32_t)rbH);
+                        prefetch_l2_bulk(p.Wu + ((int64_t)e * p.I + ii) * rbH, (uint32_t)rbH);
+                    }
+                }
+                const int b0 = un.i0 >> 8, b1 = (un.i0 + un.ic + 255) >> 8;
+                const uint32_t bytes = (uint32_t)((b1 - b0) * kBlockBytes);
+                for (int n = 0; n < un.n_y; ++n)
+                    for (int h2 = 0; h2 < 2; ++h2)
+                        prefetch_l2_bulk(p.Wd + ((int64_t)e * p.H + n * NJ + tid + 128 * h2) * rbI +
+                                             (int64_t)b0 * kBlockBytes,
+                                         bytes);
+            }
+            RawRow cur0, cur1;
+            const uint8_t *p0, *p1;
+            int g0 = 0, g1 = 0;
+            p0 = src(0, tid, g0);
+            p1 = src(0, tid + 128, g1);
+            if (p0) load_raw(cur0, p0, g0);
+            if (p1) load_raw(cur1, p1, g1);
+            for (int st = 0; st < steps; ++st) {
+                // issue the next step's loads before waiting for a free stage
+                RawRow nx0, nx1;
+                const uint8_t *q0 = nullptr, *q1 = nullptr;
+                int ng0 = 0, ng1 = 0;
+                if (st + 1 < steps) {
+                    q0 = src(st + 1, tid, ng0);
+                    q1 = src(st + 1, tid + 128, ng1);
+                    if (q0) load_raw(nx0, q0, ng0);
+                    if (q1) load_raw(nx1, q1, ng1);
+                }
+                if (!mbar_wait(&b_empty[bi], bph ^ 1, abort_flag, p.err)) { ok = false; break; }
+                const uint32_t base = s_b + bi * B_BYTES;
+                const uint32_t r0 = base + sw128_row(tid);
+                const uint32_t r1 = base + sw128_row(tid + 128);
+                if (p0) unpack_row_to_smem(cur0, g0, r0, tid); else zero_row_smem(r0);
+                if (p1) unpack_row_to_smem(cur1, g1, r1, tid + 128); else zero_row_smem(r1);
+                fence_proxy_async_smem();
+                mbar_arrive(&b_full[bi]);
+                if (++bi == NB) { bi = 0; bph ^= 1; }
+                cur0 = nx0; cur1 = nx1; p0 = q0; p1 = q1; g0 = ng0; g1 = ng1;
+            }
+        }
+    } else {
+        // ---------------- epilogue (128 threads) ----------------
+        const int q = warp & 3;                      // TMEM lane quadrant of this warp
+        const int row = q * 32 + lane;               // token row within the tile
+        const uint32_t lane_bits = (uint32_t)(q * 32) << 16;
+        uint32_t jc = 0, uc = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
+            const Unit un = make_unit(p, u, n_tiles);
+            for (int s = 0; s < un.n_gu && ok; ++s, ++jc) {
+                const uint32_t slot = jc & 1, tph = (jc >> 1) & 1;
+                if (!mbar_wait(&t_full[slot], tph, abort_flag, p.err)) { ok = false; break; }
+                tc_fence_after();
+                if (s == 0 && !mbar_wait(h_empty, (uc & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
+                const uint32_t t_addr = tmem_base + lane_bits + slot * NJ;
+#pragma unroll 1
+                for (int c = 0; c < GU_ROWS; c += 32) {
+                    uint32_t gr[32], ur[32];
+                    tmem_ld_32x32b_x32(t_addr + c, gr);
+                    tmem_ld_32x32b_x32(t_addr + GU_ROWS + c, ur);
+                    tmem_ld_wait(gr);
+                    tmem_ld_wait(ur);
+                    uint32_t hw[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float g0 = __uint_as_float(gr[2 * j]), g1 = __uint_as_float(gr[2 * j + 1]);
+                        const float u0 = __uint_as_float(ur[2 * j]), u1 = __uint_as_float(ur[2 * j + 1]);
+                        const float h0 = __fdividef(g0 * u0, 1.0f + __expf(-g0));
+                        const float h1 = __fdividef(g1 * u1, 1.0f + __expf(-g1));
+                        hw[j] = pack_bf16x2(h0, h1);
+                    }
+                    const int col = s * GU_ROWS + c;               // h column of hw[0]
+                    const uint32_t tile_base = s_h + (col >> 6) * HT_BYTES + sw128_row(row);
+                    const int cb = (col & 63) >> 3;                // first 16-byte chunk
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        st_shared_v4(tile_base + ((uint32_t)((cb + j) ^ (row & 7)) << 4), hw[4 * j],
+                                     hw[4 * j + 1], hw[4 * j + 2], hw[4 * j + 3]);
+                }
+                tc_fence_before();
+                mbar_arrive(&t_empty[slot]);
+            }
+            if (!ok) break;
+            fence_proxy_async_smem();
+            mbar_arrive(h_full);
+            // this row's destination
+            const bool valid = row < un.tile.row_count;
+            int token = 0;
+            float wgt = 1.0f;
+            if (valid) {
+                const int xr = un.tile.row_start + row;
+                token = p.row_token ? p.row_token[xr] : xr;
+                wgt = p.row_weight ? p.row_weight[xr] : 1.0f;
+            }
+            float *yrow = p.y + (int64_t)token * p.H;
+            for (int n = 0; n < un.n_y && ok; ++n, ++jc) {
+                const uint32_t slot = jc & 1, tph = (jc >> 1) & 1;
+                if (!mbar_wait(&t_full[slot], tph, abort_flag, p.err)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t t_addr = tmem_base + lane_bits + slot * NJ;
+#pragma unroll 1
+                for (int c = 0; c < NJ; c += 32) {
+                    uint32_t yr[32];
+                    tmem_ld_32x32b_x32(t_addr + c, yr);
+                    tmem_ld_wait(yr);
+                    if (valid) {
+                        float *dst = yrow + n * NJ + c;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float v0 = __uint_as_float(yr[4 * j]) * wgt;
+                            const float v1 = __uint_as_float(yr[4 * j + 1]) * wgt;
+                            const float v2 = __uint_as_float(yr[4 * j + 2]) * wgt;
+                            const float v3 = __uint_as_float(yr[4 * j + 3]) * wgt;
+                            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4 * j),
+                                         "f"(v0), "f"(v1), "f"(v2), "f"(v3)
+                                         : "memory");
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&t_empty[slot]);
+            }
+        }
+    }
+
+    // Every role is done: all MMAs were consumed by the epilogue (or the
+    // launch is aborting, in which case let in-flight MMAs finish first).
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace tc
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+cudaError_t launch_ffn_tc(const TcArgs &a, cudaStream_t s) {
+    const DeviceInfo &di = device_info();
+    auto encode = get_encode_fn();
+    if (!encode) return cudaErrorNotSupported;
+    CUtensorMap tmap;
+    const cuuint64_t dims[2] = {(cuuint64_t)a.H, (cuuint64_t)a.x_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.H * 2};
+    const cuuint32_t box[2] = {tc::BK, tc::BM};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.x), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    static int attr_set_device = -1;
+    if (attr_set_device != di.device) {
+        cudaError_t e = cudaFuncSetAttribute(tc::ffn_tc_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             tc::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set_device = di.device;
+    }
+    tc::Params p;
+    p.Wg = a.Wg;
+    p.Wu = a.Wu;
+    p.Wd = a.Wd;
+    p.y = a.y;
+    p.tiles = a.tiles;
+    p.n_tiles_dev = a.n_tiles_dev;
+    p.row_token = a.row_token;
+    p.row_weight = a.row_weight;
+    p.err = a.err;
+    p.n_tiles_host = a.n_tiles_host;
+    p.T = a.T;
+    p.H = a.H;
+    p.I = a.I;
+    const int n_chunks = (a.I + tc::IC - 1) / tc::IC;
+    const int64_t units = (int64_t)a.n_tiles_host * n_chunks;
+    int grid = di.num_sms;
+    if (units < grid) grid = (int)units;
+    if (grid < 1) return cudaSuccess;
+    tc::ffn_tc_kernel<<<grid, tc::THREADS, tc::SMEM_BYTES, s>>>(tmap, p);
+    return cudaGetLastError();
+}
+
+}  // namespace zffn

@@ -1,0 +1,147 @@
+// moe_route.cu -- device-side preparation of a routed (mixture-of-experts)
+// call: the chosen expert ids are read from the caller's device buffer and
+// turned into per-expert row lists without any host readback ("Four
+// bottlenecks, one CUDA backend...", section "Bottleneck 2 -- MoE decode was
+// paying for its routing twice": the kernels index the right expert weights
+// themselves).
+//
+//   route kernel (one block): count pairs per expert, exclusive scan into
+//     row offsets, cut every expert's rows into tiles of at most 128 rows
+//     (the tensor-core kernel's M), record for each gathered row its token and
+//     routing weight.  Pairs with an id outside [0, E) are dropped.
+//   gather kernel: copy the x row of every gathered row into a contiguous
+//     buffer so that the tensor-core kernel can load expert tiles with TMA.
+#include "zffn_internal.cuh"
+
+namespace zffn {
+
+constexpr int kRouteThreads = 1024;
+constexpr int kTileRows = 128;
+
+// Exclusive scan of v[0..n) in shared memory by one block; returns the total.
+__device__ int block_exclusive_scan(int *v, int n, int *scratch) {
+    const int per = (n + blockDim.x - 1) / blockDim.x;
+    const int lo = threadIdx.x * per, hi = min(n, lo + per);
+    int sum = 0;
+    for (int i = lo; i < hi; ++i) sum += v[i];
+    scratch[threadIdx.x] = sum;
+    __syncthreads();
+    // Hillis-Steele over the per-thread sums
+    for (int o = 1; o < (int)blockDim.x; o <<= 1) {
+        const int add = threadIdx.x >= (unsigned)o ? scratch[threadIdx.x - o] : 0;
+        __syncthreads();
+        scratch[threadIdx.x] += add;
+        __syncthreads();
+    }
+    int run = scratch[threadIdx.x] - sum;   // exclusive prefix of this thread's range
+    for (int i = lo; i < hi; ++i) {
+        const int c = v[i];
+        v[i] = run;
+        run += c;
+    }
+    __syncthreads();
+    const int total = scratch[blockDim.x - 1];
+    __syncthreads();
+    return total;
+}
+
+__global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
+    extern __shared__ int sm[];
+    int *cnt = sm;                       // [E]
+    int *off = sm + a.E;                 // [E]
+    int *tix = sm + 2 * a.E;             // [E]
+    int *scratch = sm + 3 * a.E;         // [blockDim]
+    const int P = a.T * a.k;
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < P; i += blockDim.x) {
+        const int e = a.ids[i];
+        if (e >= 0 && e < a.E) atomicAdd(&cnt[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+        off[e] = cnt[e];
+        tix[e] = (cnt[e] + kTileRows - 1) / kTileRows;
+        a.counts[e] = cnt[e];
+    }
+    __syncthreads();
+    const int n_rows = block_exclusive_scan(off, a.E, scratch);
+    const int n_tiles = block_exclusive_scan(tix, a.E, scratch);
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+        a.offsets[e] = off[e];
+        const int nt = (cnt[e] + kTileRows - 1) / kTileRows;
+        for (int t = 0; t < nt; ++t) {
+            const int ti = tix[e] + t;
+            if (ti < a.max_tiles)
+                a.tiles[ti] = make_int4(off[e] + t * kTileRows, min(kTileRows, cnt[e] - t * kTileRows), e, 0);
+        }
+        cnt[e] = off[e];                 // becomes the fill cursor
+    }
+    if (threadIdx.x == 0) {
+        a.offsets[a.E] = n_rows;
+        *a.n_tiles = min(n_tiles, a.max_tiles);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < P; i += blockDim.x) {
+        const int e = a.ids[i];
+        if (e >= 0 && e < a.E) {
+            const int pos = atomicAdd(&cnt[e], 1);
+            a.row_token[pos] = i / a.k;
+            a.row_weight[pos] = a.wts[i];
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) moe_gather_kernel(const __nv_bfloat16 *__restrict__ x,
+                                                         const int *__restrict__ offsets, int E,
+                                                         const int *__restrict__ row_token,
+                                                         __nv_bfloat16 *__restrict__ x_perm,
+                                                         int rows_cap, int H) {
+    const int n_rows = min(offsets[E], rows_cap);
+    const int vec = H / 8;   // 16-byte vectors per row
+    for (int r = blockIdx.x; r < n_rows; r += gridDim.x) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)row_token[r] * H);
+        uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (int64_t)r * H);
+        for (int v = threadIdx.x; v < vec; v += blockDim.x) dst[v] = src[v];
+    }
+}
+
+cudaError_t launch_moe_route(const RouteArgs &a, cudaStream_t s) {
+    const size_t smem = (size_t)(3 * a.E + kRouteThreads) * sizeof(int);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(moe_route_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    moe_route_kernel<<<1, kRouteThreads, smem, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int P = a.T * a.k;
+    int grid = P < device_info().num_sms * 8 ? P : device_info().num_sms * 8;
+    if (grid < 1) grid = 1;
+    moe_gather_kernel<<<grid, 256, 0, s>>>(a.x, a.offsets, a.E, a.row_token, a.x_perm, P, a.H);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Bounded-wait self test: one block waits on an mbarrier whose expected
+// arrival never comes; the wait gives up after the budget and records
+// ZFFN_ERR_TIMEOUT, and the kernel returns normally.
+// ---------------------------------------------------------------------------
+__global__ void wait_timeout_selftest_kernel(long long budget, int *err) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 2);          // two arrivals expected ...
+        fence_mbarrier_init();
+        mbar_arrive(&bar);           // ... and only one ever happens
+        mbar_wait(&bar, 0, nullptr, err, budget);
+    }
+    __syncthreads();
+}
+
+cudaError_t launch_wait_timeout_selftest(int64_t budget_cycles, int *err, cudaStream_t s) {
+    wait_timeout_selftest_kernel<<<1, 32, 0, s>>>((long long)budget_cycles, err);
+    return cudaGetLastError();
+}
+
+}  // namespace zffn

@@ -1,0 +1,308 @@
+// zffn_internal.cuh -- shared pieces of the CUDA library: Q4_K unpacking on the
+// device, PTX wrappers for mbarrier / TMA / tcgen05, bounded waits, launch
+// declarations.  Library-internal; the public interface is include/zffn.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zffn.h"
+
+namespace zffn {
+
+// ---------------------------------------------------------------------------
+// Q4_K on the device.  144 bytes per 256 weights: fp16 d, fp16 dmin, 12 bytes
+// of 6-bit (scale, min) pairs, 128 bytes of 4-bit codes (byte 32g+l holds
+// weight 64g+l in its low nibble and 64g+32+l in its high nibble).
+// ---------------------------------------------------------------------------
+constexpr int kQK = 256;
+constexpr int kBlockBytes = 144;
+
+__host__ __device__ inline int64_t q4k_row_bytes(int64_t cols) {
+    return ((cols + kQK - 1) / kQK) * kBlockBytes;
+}
+
+// Scales as three little-endian words: s0 = bytes 0..3, s1 = 4..7, s2 = 8..11.
+// Sub-block j < 4: scale = low 6 bits of byte j, min = low 6 bits of byte j+4.
+// Sub-block j >= 4: low 4 bits in the nibbles of byte j+4, top 2 bits in the
+// spare top bits of byte j-4 (scale) and byte j (min).
+__device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t s2, int j,
+                                              int &sc, int &m) {
+    if (j < 4) {
+        sc = (s0 >> (8 * j)) & 63;
+        m = (s1 >> (8 * j)) & 63;
+    } else {
+        const int jj = j - 4;
+        sc = ((s2 >> (8 * jj)) & 15) | (((s0 >> (8 * jj + 6)) & 3) << 4);
+        m = ((s2 >> (8 * jj + 4)) & 15) | (((s1 >> (8 * jj + 6)) & 3) << 4);
+    }
+}
+
+__device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
+    return __half2float(__ushort_as_half((unsigned short)(bits16 & 0xFFFFu)));
+}
+
+// ---------------------------------------------------------------------------
+// Device error word and bounded waits.
+// ---------------------------------------------------------------------------
+// Budget of a bounded wait in SM clock cycles (about two seconds at boost
+// clock): far above any legitimate wait inside one launch.
+constexpr long long kWaitBudgetCycles = 4000000000LL;
+
+__device__ __forceinline__ void record_error(int *err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers (sm_100 family).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbarrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete.  Gives up after
+// `budget` SM cycles (or as soon as another role raised *abort), records
+// ZFFN_ERR_TIMEOUT, raises *abort and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                          int *err, long long budget = kWaitBudgetCycles) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if ((abort && *abort) || clock64() - t0 > budget) {
+            record_error(err, ZFFN_ERR_TIMEOUT);
+            if (abort) *abort = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 2-D TMA tile load global -> shared, completion counted on `bar` (bytes).
+__device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, uint64_t *bar,
+                                            int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2_bulk(const void *gptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gptr), "r"(bytes) : "memory");
+}
+
+// ---- tcgen05 ---------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 op this thread issued so far completes.
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns; thread i of the warp gets lane
+// (base + i), registers = columns.  The registers are undefined until
+// tmem_ld_wait(r) returns.
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+// Wait for every tcgen05.ld of this thread; the registers of `r` are passed
+// through the wait so that no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128 bytes
+// (64 bf16), groups of 8 rows 1024 bytes apart; the tile starts 1024-aligned.
+__device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+    d |= (uint64_t)1 << 16;                    // leading byte offset (unused here)
+    d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset: 8-row groups
+    d |= (uint64_t)1 << 46;                    // descriptor version (sm_100 family)
+    d |= (uint64_t)2 << 61;                    // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: kind::f16, A = B = bf16, D = fp32, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4)                          // D format f32
+           | (1u << 7)                        // A format bf16
+           | (1u << 10)                       // B format bf16
+           | ((uint32_t)(N >> 3) << 17)       // N / 8
+           | ((uint32_t)(M >> 4) << 24);      // M / 16
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_global_nc_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// Host-side launchers (defined in the kernel translation units).
+// ---------------------------------------------------------------------------
+struct DeviceInfo {
+    int device = -1;
+    int num_sms = 0;
+    int max_smem_optin = 0;
+    int *err_word = nullptr;   // device error word of this device
+};
+const DeviceInfo &device_info();   // current device (cached per device)
+
+cudaError_t launch_q4k_dequant(const void *blocks, float *out, int64_t rows, int64_t cols,
+                               cudaStream_t s);
+cudaError_t launch_q4k_quantize(const float *w, void *blocks, int64_t rows, int64_t cols,
+                                cudaStream_t s);
+cudaError_t launch_zero_f32(float *p, int64_t n, cudaStream_t s);
+
+// Single-token / few-pair matvec path (phase 1: gate/up + SwiGLU into an
+// on-device strip; grid barrier; phase 2: down projection).
+struct MatvecArgs {
+    const __nv_bfloat16 *x;      // [T][H]
+    const uint8_t *Wg, *Wu, *Wd; // expert-stacked
+    const int32_t *ids;          // [T][k] or nullptr (dense: expert 0, weight 1)
+    const float *wts;            // [T][k] or nullptr
+    float *y;                    // [T][H]
+    float *h;                    // workspace [T*k][I]
+    unsigned int *barrier;       // workspace, two words, zero-initialised once
+    int *err;
+    int T, H, I, E, k;
+};
+size_t matvec_smem_bytes(int T, int H, int I, int k);
+cudaError_t launch_ffn_matvec(const MatvecArgs &a, cudaStream_t s);
+
+// Tensor-core fused prefill path.
+struct TcArgs {
+    const void *x;               // bf16 rows (dense x or the gathered MoE rows)
+    int64_t x_rows;              // rows of x visible to the tensor map
+    const uint8_t *Wg, *Wu, *Wd;
+    float *y;                    // [T][H], zero-filled before the launch
+    // Dense: tiles == nullptr, tokens taken as x rows.  MoE: tile table and
+    // per-row (token, weight) maps produced on the device by the router pass.
+    const int4 *tiles;           // {row_start, row_count, expert, 0}
+    const int *n_tiles_dev;      // device count of tiles
+    const int *row_token;        // x row -> token
+    const float *row_weight;     // x row -> routing weight
+    int n_tiles_host;            // dense: exact count; MoE: upper bound
+    int *err;
+    int T, H, I;
+};
+cudaError_t launch_ffn_tc(const TcArgs &a, cudaStream_t s);
+
+// MoE routing on the device: bucket (token, slot) pairs by expert, build the
+// tile table and the row maps, gather x rows per expert.
+struct RouteArgs {
+    const int32_t *ids;
+    const float *wts;
+    const __nv_bfloat16 *x;
+    int T, H, E, k;
+    int *counts;        // [E]
+    int *offsets;       // [E + 1]
+    int *cursors;       // [E]
+    int4 *tiles;        // [max_tiles]
+    int *n_tiles;       // [1]
+    int *row_token;     // [T*k]
+    float *row_weight;  // [T*k]
+    __nv_bfloat16 *x_perm;  // [T*k][H]
+    int max_tiles;
+};
+cudaError_t launch_moe_route(const RouteArgs &a, cudaStream_t s);
+
+cudaError_t launch_wait_timeout_selftest(int64_t budget_cycles, int *err, cudaStream_t s);
+
+}  // namespace zffn

@@ -1,0 +1,165 @@
+"""Python binding of libzffn (include/zffn.h): argument marshalling only.
+
+Every function takes CUDA tensors, checks dtype/shape/contiguity, and passes
+raw device pointers and the current (or given) CUDA stream to the C ABI.  All
+computation happens in the library's kernels; if the library is not built,
+importing the functions raises -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libzffn.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_NO_WORKSPACE = range(6)
+OPT_MATVEC_MAX_T = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class ZffnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        detail = ""
+        if status == ERR_CUDA:
+            detail = " (" + load().zffn_last_error().decode() + ")"
+        super().__init__(f"{what}: {status_string(status)}{detail}")
+
+
+def load() -> ctypes.CDLL:
+    """Load libzffn.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with quantized_ffn_gb300.build.build()")
+            lib = ctypes.CDLL(LIB_PATH)
+            P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+            sigs = {
+                "zffn_status_string": ([I32], ctypes.c_char_p),
+                "zffn_last_error": ([], ctypes.c_char_p),
+                "zffn_q4k_row_bytes": ([I64], ctypes.c_size_t),
+                "zffn_q4k_dequant": ([P, P, I64, I64, P], I32),
+                "zffn_q4k_quantize": ([P, P, I64, I64, P], I32),
+                "zffn_swiglu_q4k": ([P, P, P, P, P, I32, I32, I32, P], I32),
+                "zffn_moe_swiglu_q4k": ([P, P, P, P, P, P, P, I32, I32, I32, I32, I32, P], I32),
+                "zffn_reserve": ([I32, I32, I32, I32, I32], I32),
+                "zffn_release": ([], None),
+                "zffn_get_device_error": ([P], I32),
+                "zffn_set_option": ([I32, I32], I32),
+                "zffn_selftest_wait_timeout": ([I64, P], I32),
+            }
+            for name, (args, res) in sigs.items():
+                f = getattr(lib, name)
+                f.argtypes = args
+                f.restype = res
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().zffn_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise ZffnError(status, what)
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _cuda(t: torch.Tensor, name: str, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def q4k_row_bytes(cols: int) -> int:
+    return int(load().zffn_q4k_row_bytes(int(cols)))
+
+
+def q4k_dequant(blocks: torch.Tensor, rows: int, cols: int, out: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+    if out is None:
+        out = torch.empty((rows, cols), dtype=torch.float32, device=blocks.device)
+    if blocks.numel() < rows * q4k_row_bytes(cols):
+        raise ValueError("blocks too small")
+    _check(load().zffn_q4k_dequant(_cuda(blocks, "blocks", torch.uint8),
+                                   _cuda(out, "out", torch.float32), rows, cols, _stream(stream)),
+           "zffn_q4k_dequant")
+    return out
+
+
+def q4k_quantize(w: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    rows, cols = w.shape
+    if out is None:
+        out = torch.empty((rows, q4k_row_bytes(cols)), dtype=torch.uint8, device=w.device)
+    _check(load().zffn_q4k_quantize(_cuda(w, "w", torch.float32), _cuda(out, "out", torch.uint8),
+                                    rows, cols, _stream(stream)), "zffn_q4k_quantize")
+    return out
+
+
+def swiglu_q4k(x: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor, Wd: torch.Tensor, I: int,
+               y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """y[T, H] fp32 = W_down (silu(W_gate x) * (W_up x)) with Q4_K weights."""
+    T, H = x.shape
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    _check(load().zffn_swiglu_q4k(_cuda(x, "x", torch.bfloat16), _cuda(Wg, "Wg", torch.uint8),
+                                  _cuda(Wu, "Wu", torch.uint8), _cuda(Wd, "Wd", torch.uint8),
+                                  _cuda(y, "y", torch.float32), T, H, I, _stream(stream)),
+           "zffn_swiglu_q4k")
+    return y
+
+
+def moe_swiglu_q4k(x: torch.Tensor, expert_ids: torch.Tensor, expert_weights: torch.Tensor,
+                   Wg: torch.Tensor, Wu: torch.Tensor, Wd: torch.Tensor, I: int, E: int,
+                   y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Routed experts: y[t] = sum_j w[t, j] FFN_{ids[t, j]}(x[t])."""
+    T, H = x.shape
+    top_k = expert_ids.shape[1]
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    _check(load().zffn_moe_swiglu_q4k(
+        _cuda(x, "x", torch.bfloat16), _cuda(expert_ids, "expert_ids", torch.int32),
+        _cuda(expert_weights, "expert_weights", torch.float32), _cuda(Wg, "Wg", torch.uint8),
+        _cuda(Wu, "Wu", torch.uint8), _cuda(Wd, "Wd", torch.uint8),
+        _cuda(y, "y", torch.float32), T, H, I, E, top_k, _stream(stream)), "zffn_moe_swiglu_q4k")
+    return y
+
+
+def reserve(T_max: int, H_max: int, I_max: int, E_max: int = 1, top_k_max: int = 1):
+    _check(load().zffn_reserve(T_max, H_max, I_max, E_max, top_k_max), "zffn_reserve")
+
+
+def release():
+    load().zffn_release()
+
+
+def get_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error word."""
+    return int(load().zffn_get_device_error(_stream(stream)))
+
+
+def set_option(key: int, value: int) -> int:
+    return int(load().zffn_set_option(key, value))
+
+
+def selftest_wait_timeout(budget_cycles: int, stream=None):
+    _check(load().zffn_selftest_wait_timeout(int(budget_cycles), _stream(stream)),
+           "zffn_selftest_wait_timeout")

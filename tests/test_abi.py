@@ -1,0 +1,95 @@
+"""The C ABI on the host (no GPU): the library loads, exports every function
+declared in include/zffn.h, and rejects invalid arguments before touching the
+device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from quantized_ffn_gb300 import build as zbuild
+from quantized_ffn_gb300 import zffn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    zbuild.build()
+    return zffn.load()
+
+
+def declared_functions():
+    names = []
+    with open(os.path.join(ROOT, "include", "zffn.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    for m in re.finditer(r"\b(zffn_\w+)\s*\(", text):
+        names.append(m.group(1))
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("zffn_q4k_dequant", "zffn_swiglu_q4k", "zffn_moe_swiglu_q4k"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["ZFFN_OK", "ZFFN_ERR_INVALID_ARG", "ZFFN_ERR_UNSUPPORTED",
+                                 "ZFFN_ERR_CUDA", "ZFFN_ERR_TIMEOUT", "ZFFN_ERR_NO_WORKSPACE"]):
+        assert zffn.status_string(code) == name
+
+
+def test_row_bytes(lib):
+    assert zffn.q4k_row_bytes(256) == 144
+    assert zffn.q4k_row_bytes(4096) == 16 * 144
+    assert zffn.q4k_row_bytes(11008) == 43 * 144
+    assert zffn.q4k_row_bytes(704) == 3 * 144
+    assert zffn.q4k_row_bytes(0) == 0
+
+
+FAKE = ctypes.c_void_p(0x10000)   # never dereferenced: the checks reject first
+
+
+@pytest.mark.parametrize("T,H,I", [(0, 256, 256), (4, 200, 256), (4, 256, 100), (4, 256, 0),
+                                   (4, 32768, 256), (-1, 256, 256)])
+def test_swiglu_rejects_bad_shapes(lib, T, H, I):
+    st = lib.zffn_swiglu_q4k(FAKE, FAKE, FAKE, FAKE, FAKE, T, H, I, None)
+    assert st == zffn.ERR_INVALID_ARG
+
+
+def test_swiglu_rejects_null_and_misaligned(lib):
+    assert lib.zffn_swiglu_q4k(None, FAKE, FAKE, FAKE, FAKE, 4, 256, 256, None) == zffn.ERR_INVALID_ARG
+    assert lib.zffn_swiglu_q4k(FAKE, FAKE, FAKE, None, FAKE, 4, 256, 256, None) == zffn.ERR_INVALID_ARG
+    odd = ctypes.c_void_p(0x10008)
+    assert lib.zffn_swiglu_q4k(odd, FAKE, FAKE, FAKE, FAKE, 4, 256, 256, None) == zffn.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("E,k", [(0, 1), (5000, 1), (8, 0), (8, 65)])
+def test_moe_rejects_bad_routing_sizes(lib, E, k):
+    st = lib.zffn_moe_swiglu_q4k(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 256, E, k, None)
+    assert st == zffn.ERR_INVALID_ARG
+
+
+def test_dequant_quantize_reject_bad_args(lib):
+    assert lib.zffn_q4k_dequant(None, FAKE, 1, 256, None) == zffn.ERR_INVALID_ARG
+    assert lib.zffn_q4k_dequant(FAKE, FAKE, 0, 256, None) == zffn.ERR_INVALID_ARG
+    assert lib.zffn_q4k_quantize(FAKE, None, 1, 256, None) == zffn.ERR_INVALID_ARG
+    assert lib.zffn_q4k_quantize(FAKE, FAKE, 1, -5, None) == zffn.ERR_INVALID_ARG
+
+
+def test_reserve_and_selftest_reject_bad_args(lib):
+    assert lib.zffn_reserve(0, 1, 1, 1, 1) == zffn.ERR_INVALID_ARG
+    assert lib.zffn_selftest_wait_timeout(0, None) == zffn.ERR_INVALID_ARG
+
+
+def test_options(lib):
+    old = zffn.set_option(zffn.OPT_MATVEC_MAX_T, 4)
+    assert zffn.set_option(zffn.OPT_MATVEC_MAX_T, old) == 4
+    assert zffn.set_option(999, 1) == -1

@@ -1,0 +1,103 @@
+"""Routed (mixture-of-experts) SwiGLU block on the GPU against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as orc
+from quantized_ffn_gb300 import synth, zffn
+from tests.gpu_util import assert_close, dev, moe_layer, x_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def experts(seed, E, H, I, dscale=1e-2):
+    rng = np.random.default_rng(seed)
+    Wg = np.stack([synth.random_q4k_blocks(rng, I, H, dscale) for _ in range(E)])
+    Wu = np.stack([synth.random_q4k_blocks(rng, I, H, dscale) for _ in range(E)])
+    Wd = np.stack([synth.random_q4k_blocks(rng, H, I, dscale) for _ in range(E)])
+    return Wg, Wu, Wd
+
+
+def routing(seed, T, E, k):
+    rng = np.random.default_rng(seed)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    return synth.route_top_k(logits, k)
+
+
+def run(x, ids, w, Wg, Wu, Wd, I, E, matvec_max_t=None):
+    old = None
+    if matvec_max_t is not None:
+        old = zffn.set_option(zffn.OPT_MATVEC_MAX_T, matvec_max_t)
+    try:
+        y = zffn.moe_swiglu_q4k(x_dev(x), dev(ids), dev(w), dev(Wg), dev(Wu), dev(Wd), I, E)
+        assert zffn.get_device_error() == zffn.OK
+    finally:
+        if old is not None:
+            zffn.set_option(zffn.OPT_MATVEC_MAX_T, old)
+    return y
+
+
+@pytest.mark.parametrize("T,E,H,I,k", [(40, 8, 512, 384, 2), (300, 16, 256, 704, 4),
+                                       (5, 32, 1024, 256, 8), (1, 8, 512, 384, 2)])
+def test_small_moe_tensor_core_path(T, E, H, I, k):
+    Wg, Wu, Wd = experts(T + E, E, H, I)
+    ids, w = routing(T * E, T, E, k)
+    x = synth.f32_to_bf16_bits(np.random.default_rng(9).standard_normal((T, H)).astype(np.float32))
+    y = run(x, ids, w, Wg, Wu, Wd, I, E, matvec_max_t=0)
+    ref = orc.moe_swiglu_ffn(x, ids, w, Wg, Wu, Wd, T, H, I, E, k)
+    assert_close(y, ref, f"moe tc T={T} E={E}")
+
+
+@pytest.mark.parametrize("E,H,I,k", [(8, 512, 384, 2), (16, 256, 704, 8)])
+def test_small_moe_single_token_path(E, H, I, k):
+    Wg, Wu, Wd = experts(E + 1, E, H, I)
+    ids, w = routing(E + 2, 1, E, k)
+    x = synth.f32_to_bf16_bits(np.random.default_rng(3).standard_normal((1, H)).astype(np.float32))
+    y = run(x, ids, w, Wg, Wu, Wd, I, E, matvec_max_t=1)
+    ref = orc.moe_swiglu_ffn(x, ids, w, Wg, Wu, Wd, 1, H, I, E, k)
+    assert_close(y, ref, "moe matvec")
+
+
+@pytest.mark.parametrize("path", [0, 1])
+def test_invalid_ids_contribute_nothing(path):
+    T = 1 if path else 20
+    E, H, I, k = 6, 256, 256, 3
+    Wg, Wu, Wd = experts(11, E, H, I)
+    ids, w = routing(12, T, E, k)
+    ids[0, 1] = -3
+    ids[-1, 2] = E + 5
+    x = synth.f32_to_bf16_bits(np.random.default_rng(4).standard_normal((T, H)).astype(np.float32))
+    y = run(x, ids, w, Wg, Wu, Wd, I, E, matvec_max_t=path)
+    ref = orc.moe_swiglu_ffn(x, ids, w, Wg, Wu, Wd, T, H, I, E, k)
+    assert_close(y, ref, "invalid ids")
+
+
+def test_single_expert_routing_equals_dense_call():
+    T, E, H, I = 70, 4, 512, 384
+    Wg, Wu, Wd = experts(21, E, H, I)
+    ids = np.full((T, 1), 2, dtype=np.int32)
+    w = np.ones((T, 1), dtype=np.float32)
+    x = synth.f32_to_bf16_bits(np.random.default_rng(5).standard_normal((T, H)).astype(np.float32))
+    y = run(x, ids, w, Wg, Wu, Wd, I, E, matvec_max_t=0)
+    y_dense = zffn.swiglu_q4k(x_dev(x), dev(Wg[2]), dev(Wu[2]), dev(Wd[2]), I)
+    torch.cuda.synchronize()
+    ref = orc.swiglu_ffn(x, Wg[2], Wu[2], Wd[2], T, H, I)
+    assert_close(y, ref, "moe k=1")
+    assert_close(y_dense, ref, "dense")
+
+
+def test_full_moe_config_single_token():
+    m = moe_layer(1)
+    y = run(m["x"], m["ids"], m["w"], m["Wg"], m["Wu"], m["Wd"], m["I"], m["E"])
+    ref = orc.moe_swiglu_ffn(m["x"], m["ids"], m["w"], m["Wg"], m["Wu"], m["Wd"], 1, m["H"],
+                             m["I"], m["E"], m["k"])
+    assert_close(y, ref, "moe T=1")
+
+
+def test_full_moe_config_256_tokens_sampled_rows():
+    m = moe_layer(256)
+    y = run(m["x"], m["ids"], m["w"], m["Wg"], m["Wu"], m["Wd"], m["I"], m["E"])
+    rows = [0, 1, 17, 100, 128, 200, 255]
+    ref = orc.moe_swiglu_ffn(m["x"][rows].copy(), m["ids"][rows].copy(), m["w"][rows].copy(),
+                             m["Wg"], m["Wu"], m["Wd"], len(rows), m["H"], m["I"], m["E"], m["k"])
+    assert_close(y[rows], ref, "moe T=256 sampled")
