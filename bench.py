@@ -1,0 +1,521 @@
+#!/usr/bin/env python
+"""Throughput of the fused Q4_K SwiGLU feed-forward block on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Default workload: one 4096 -> 11008 -> 4096 Q4_K SwiGLU layer at T=2048 tokens
+(bf16 activations with 1% outlier rows x20, weights N(0, 0.02) quantised with
+the min/max quantiser; seed 2).  A step is one call of the block over the
+whole batch, inputs resident in HBM, L2 flushed (512 MB write) between steps
+outside the timed events.  Under torchrun each rank runs its own replica of
+the workload on its own GPU (no collective on the data path: tokens are
+independent), so the scaling is weak and `value` is the tokens of all ranks
+divided by the slowest rank's time.
+
+The JSON line carries: the device-timed throughput (`value`, tok/s) and
+TFLOP/s, the end-to-end throughput through the public API with host buffers
+(`e2e`), the roofline of the dominant kernel (the fused tensor-core kernel,
+timed alone through the residual entry point), the CPU oracle timed on this
+host's cores on a bounded sample (`cpu_baseline`), SM clocks sampled during
+the timed region, and the number of this library's kernels launched.
+
+--impl reference times the CPU oracle itself (the only reference this
+build has: the source pages publish no code) on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused Q4_K SwiGLU-MLP tok/s & TFLOP/s at T=2048; % of BF16 TC / HBM roof"
+L2_FLUSH_BYTES = 512 << 20
+
+WORKLOADS = {
+    # name: (kind, T, H, I, seed, outlier_frac, E, top_k)
+    "prefill_T2048": ("dense", 2048, 4096, 11008, 2, 0.01, 1, 1),
+    "prefill_T256": ("dense", 256, 4096, 11008, 1, 0.0, 1, 1),
+    "decode_T1": ("dense", 1, 4096, 11008, 3, 0.0, 1, 1),
+    "moe_T256": ("moe", 256, 2048, 768, 4, 0.0, 128, 8),
+    "moe_T1": ("moe", 1, 2048, 768, 4, 0.0, 128, 8),
+}
+DESCR = {
+    "prefill_T2048": "Q4_K SwiGLU layer H=4096 I=11008, T=2048 prefill, 1% outlier rows x20 (seed 2)",
+    "prefill_T256": "Q4_K SwiGLU layer H=4096 I=11008, T=256 prefill (seed 1)",
+    "decode_T1": "Q4_K SwiGLU layer H=4096 I=11008, T=1 decode, one token per step (seed 3)",
+    "moe_T256": "Q4_K MoE layer E=128 H=2048 I=768 top-8, T=256 (seed 4)",
+    "moe_T1": "Q4_K MoE layer E=128 H=2048 I=768 top-8, T=1 (seed 4)",
+}
+
+
+def row_bytes(cols):
+    return ((cols + 255) // 256) * 144
+
+
+def algorithmic(kind, T, H, I, E, k):
+    """FLOP and HBM bytes the method must move once (Q4_K weights read once at
+    4.5 bits/weight, x read once in bf16, y written once in fp32)."""
+    if kind == "dense":
+        flop = 6.0 * T * H * I
+        wbytes = 2 * I * row_bytes(H) + H * row_bytes(I)
+    else:
+        flop = 6.0 * T * k * H * I
+        per_expert = 2 * I * row_bytes(H) + H * row_bytes(I)
+        touched = E if T * k >= E else min(E, T * k)
+        wbytes = touched * per_expert
+    return flop, wbytes + T * H * 2 + T * H * 4
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_ffn_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"ncu_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples every 100 ms while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        except Exception:
+            pass
+        finally:
+            if self.path and os.path.exists(self.path):
+                os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]
+                          and "Not" not in r[5 + i]})
+        loaded = [s for s in sm if s >= 0.5 * max(sm)] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# ---------------------------------------------------------------------------
+# inputs
+# ---------------------------------------------------------------------------
+
+def make_host_inputs(name):
+    from quantized_ffn_gb300 import synth
+    kind, T, H, I, seed, outl, E, k = WORKLOADS[name]
+    if kind == "dense":
+        if name == "decode_T1":
+            d = synth.decode(n_tokens=1000, seed=seed, H=H, I=I)
+        else:
+            d = synth.prefill(T, seed, H, I, outl)
+        return d
+    return synth.MoE(T, seed=seed, E=E, H=H, I=I, top_k=k)
+
+
+def quantize_on_gpu(w_f32, torch, zffn):
+    t = torch.from_numpy(w_f32).cuda()
+    q = zffn.q4k_quantize(t)
+    del t
+    return q
+
+
+# ---------------------------------------------------------------------------
+# GPU leg
+# ---------------------------------------------------------------------------
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from quantized_ffn_gb300 import build as zbuild
+    zbuild.build()
+    from quantized_ffn_gb300 import zffn
+
+    name = args.workload
+    kind, T, H, I, seed, outl, E, k = WORKLOADS[name]
+    flop, abytes = algorithmic(kind, T, H, I, E, k)
+    peaks = load_peaks()
+
+    host = make_host_inputs(name)
+    dev = torch.device("cuda", local)
+    if kind == "dense":
+        W = [quantize_on_gpu(host[n], torch, zffn) for n in ("Wg_f32", "Wu_f32", "Wd_f32")]
+        x_all = torch.from_numpy(host["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+        ids = wts = None
+    else:
+        Wg = torch.empty((E, I, row_bytes(H)), dtype=torch.uint8, device=dev)
+        Wu = torch.empty_like(Wg)
+        Wd = torch.empty((E, H, row_bytes(I)), dtype=torch.uint8, device=dev)
+        for e in range(E):
+            g, u, d = host.expert_f32(e)
+            Wg[e] = quantize_on_gpu(g, torch, zffn)
+            Wu[e] = quantize_on_gpu(u, torch, zffn)
+            Wd[e] = quantize_on_gpu(d, torch, zffn)
+        W = [Wg, Wu, Wd]
+        x_all = torch.from_numpy(host.x.view(np.int16)).to(dev).view(torch.bfloat16)
+        ids = torch.from_numpy(host.ids).to(dev)
+        wts = torch.from_numpy(host.weights).to(dev)
+    torch.cuda.synchronize()
+    # Decode reads 76 MB per token, less than the L2: rotate over copies of the
+    # weights at different addresses so that every step streams from HBM.
+    wbytes = sum(w.numel() for w in W)
+    n_sets = 1
+    if name == "decode_T1" or name == "moe_T1":
+        n_sets = max(1, math.ceil(3 * 129e6 / wbytes))
+    sets = [W] + [[w.clone() for w in W] for _ in range(n_sets - 1)]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    y = torch.empty((T, H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    zffn.reserve(max(T, 1), H, I, E, k)
+
+    def x_for(step):
+        if name == "decode_T1":
+            r = step % x_all.shape[0]
+            return x_all[r:r + 1]
+        return x_all
+
+    def call(step, residual=False, out=None, xin=None):
+        Wg_, Wu_, Wd_ = sets[step % n_sets]
+        xx = x_for(step) if xin is None else xin
+        if kind == "dense":
+            zffn.swiglu_q4k(xx, Wg_, Wu_, Wd_, I, y=y if out is None else out, residual=residual)
+        else:
+            zffn.moe_swiglu_q4k(xx, ids, wts, Wg_, Wu_, Wd_, I, E, y=y if out is None else out,
+                                residual=residual)
+
+    launches_per_call = 2 if T > 1 else 1          # zero fill + fused kernel, or one
+    if kind == "moe" and T > 1:
+        launches_per_call = 4                      # route, gather, zero fill, fused kernel
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for s in range(args.warmup):
+        flush.zero_()
+        call(s)
+    torch.cuda.synchronize()
+    assert zffn.get_device_error() == zffn.OK
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for s in range(args.steps):
+            flush.zero_()
+            starts[s].record(stream)
+            call(s)
+            ends[s].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+        barrier()
+        # the dominant kernel alone: the residual entry skips the zero fill
+        kst = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ken = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for s in range(args.steps):
+            flush.zero_()
+            kst[s].record(stream)
+            call(s, residual=True)
+            ken[s].record(stream)
+        torch.cuda.synchronize()
+    clocks = clk.summary()
+    assert zffn.get_device_error() == zffn.OK
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    kern_ms = [a.elapsed_time(b) for a, b in zip(kst, ken)]
+    ms = statistics.mean(step_ms)
+    kms = statistics.mean(kern_ms)
+
+    # end to end through the public API with pinned host buffers
+    x_host = torch.empty(x_for(0).shape, dtype=torch.bfloat16, pin_memory=True)
+    x_host.copy_(x_for(0))
+    y_host = torch.empty((x_host.shape[0], H), dtype=torch.float32, pin_memory=True)
+    x_dev = torch.empty_like(x_for(0))
+    y_e2e = torch.empty((x_host.shape[0], H), dtype=torch.float32, device=dev)
+    est = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    een = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    for s in range(args.steps):
+        flush.zero_()
+        est[s].record(stream)
+        x_dev.copy_(x_host, non_blocking=True)
+        call(s, out=y_e2e, xin=x_dev)
+        y_host.copy_(y_e2e, non_blocking=True)
+        een[s].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(est, een))
+
+    if world > 1:
+        t = torch.tensor([ms, kms, e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, kms, e2e_ms = (float(v) for v in t.tolist())
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    tok = T * world
+    value = tok / (ms * 1e-3)
+    tflops = flop / (ms * 1e-3) / 1e12
+    # prefill is a dense contraction; decode and the routed layer stream weights
+    bound = "tensor" if name.startswith("prefill") else "hbm"
+    if bound == "tensor":
+        achieved = flop / (kms * 1e-3) / 1e12
+        peak, unit = peaks["bf16"], "TFLOP/s"
+    else:
+        achieved = abytes / (kms * 1e-3) / 1e9
+        peak, unit = peaks["hbm"], "GB/s"
+    traffic = profiled_traffic(name)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(name, host, seconds=args.cpu_seconds)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tok/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": DESCR[name],
+            "name": name, "T": T, "H": H, "I": I,
+            **({"E": E, "top_k": k} if kind == "moe" else {}),
+            "parallelism": "replicas" if world > 1 else "single-gpu",
+            "l2": "flushed between steps (512 MB write outside the timed events)"
+                  + (f"; weights rotated over {n_sets} copies" if n_sets > 1 else ""),
+        },
+        "tflops": round(tflops, 2),
+        "roofline": {
+            "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "kernel": "ffn_tc_kernel" if bound == "tensor" else
+                      ("ffn_matvec_kernel" if T == 1 else "ffn_tc_kernel"),
+            "kernel_ms": round(kms, 4),
+            "peak_source": f"{peaks['source']} (burst)",
+            "algorithmic": {"flop": flop, "hbm_bytes": abytes},
+        },
+        "e2e": {"value": round(T * world / (e2e_ms * 1e-3), 1), "unit": "tok/s",
+                "h2d_bytes_per_step": int(x_host.numel() * 2),
+                "d2h_bytes_per_step": int(y_host.numel() * 4)},
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "gpu_launches": launches_per_call * args.steps,
+        "wall_s_timed_loop": round(wall, 4),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+
+def oracle_layer(name, host):
+    from oracle import oracle as orc
+    kind = WORKLOADS[name][0]
+    if kind == "dense":
+        return dict(Wg=orc.q4k_quantize(host["Wg_f32"]), Wu=orc.q4k_quantize(host["Wu_f32"]),
+                    Wd=orc.q4k_quantize(host["Wd_f32"]))
+    E = host.E
+    Wg = np.empty((E, host.I, row_bytes(host.H)), np.uint8)
+    Wu = np.empty_like(Wg)
+    Wd = np.empty((E, host.H, row_bytes(host.I)), np.uint8)
+    for e in range(E):
+        g, u, d = host.expert_f32(e)
+        Wg[e], Wu[e], Wd[e] = orc.q4k_quantize(g), orc.q4k_quantize(u), orc.q4k_quantize(d)
+    return dict(Wg=Wg, Wu=Wu, Wd=Wd)
+
+
+def oracle_tokens(name, host, layer, rows):
+    from oracle import oracle as orc
+    kind, T, H, I, seed, outl, E, k = WORKLOADS[name]
+    if kind == "dense":
+        x = host["x"][rows].copy()
+        return orc.swiglu_ffn(x, layer["Wg"], layer["Wu"], layer["Wd"], len(rows), H, I)
+    return orc.moe_swiglu_ffn(host.x[rows].copy(), host.ids[rows].copy(),
+                              host.weights[rows].copy(), layer["Wg"], layer["Wu"], layer["Wd"],
+                              len(rows), H, I, E, k)
+
+
+def cpu_baseline(name, host, seconds=10.0):
+    """The oracle as it stands, single-threaded, on a bounded sample of tokens."""
+    layer = oracle_layer(name, host)
+    T = WORKLOADS[name][1]
+    n_rows = host["x"].shape[0] if isinstance(host, dict) else host.x.shape[0]
+    done, t0, r = 0, time.perf_counter(), 0
+    per_call = 4 if T > 1 else 1
+    while time.perf_counter() - t0 < seconds:
+        rows = [(r + i) % n_rows for i in range(per_call)]
+        oracle_tokens(name, host, layer, rows)
+        done += per_call
+        r += per_call
+    dt = time.perf_counter() - t0
+    return {"value": round(done / dt, 3), "unit": "tok/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} tokens of the workload in calls of {per_call} "
+                      f"(full weights; oracle dequantises every weight row once per call)"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    name = args.workload
+    kind, T, H, I, seed, outl, E, k = WORKLOADS[name]
+    host = make_host_inputs(name)
+    layer = oracle_layer(name, host)
+    n_rows = host["x"].shape[0] if isinstance(host, dict) else host.x.shape[0]
+    per_step = 2 if T > 1 else 1
+    for s in range(args.warmup):
+        oracle_tokens(name, host, layer, [(s * per_step + i) % n_rows for i in range(per_step)])
+    times = []
+    for s in range(args.steps):
+        rows = [((s + args.warmup) * per_step + i) % n_rows for i in range(per_step)]
+        t0 = time.perf_counter()
+        oracle_tokens(name, host, layer, rows)
+        times.append(time.perf_counter() - t0)
+    mean = statistics.mean(times)
+    value = per_step / mean
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "tok/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(mean * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": DESCR[name], "name": name, "T": T, "H": H, "I": I},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tok/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} token(s) of the workload per step"},
+        "e2e": {"value": round(value, 3), "unit": "tok/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="prefill_T2048", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

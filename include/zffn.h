@@ -100,6 +100,13 @@ zffn_status zffn_q4k_quantize(const float *w, void *blocks, int64_t rows, int64_
 zffn_status zffn_swiglu_q4k(const void *x, const void *Wg, const void *Wu, const void *Wd,
                             float *y, int T, int H, int I, void *stream);
 
+/* As zffn_swiglu_q4k, but adds the block's output to y instead of overwriting
+ * it: y += W_down . (silu(W_gate . x) (*) (W_up . x)) -- the residual
+ * connection around the block.  y must hold valid fp32 values on entry. */
+zffn_status zffn_swiglu_q4k_residual(const void *x, const void *Wg, const void *Wu,
+                                     const void *Wd, float *y, int T, int H, int I,
+                                     void *stream);
+
 /* Mixture-of-experts SwiGLU block:
  *     y[t] = sum_{j < top_k} expert_weights[t][j] * FFN_{expert_ids[t][j]}(x[t])
  * ("Four bottlenecks, one CUDA backend...", section "Bottleneck 2 -- MoE decode
@@ -118,6 +125,12 @@ zffn_status zffn_moe_swiglu_q4k(const void *x, const int32_t *expert_ids,
                                 const float *expert_weights, const void *Wg, const void *Wu,
                                 const void *Wd, float *y, int T, int H, int I, int E,
                                 int top_k, void *stream);
+
+/* As zffn_moe_swiglu_q4k, but y += the routed block's output. */
+zffn_status zffn_moe_swiglu_q4k_residual(const void *x, const int32_t *expert_ids,
+                                         const float *expert_weights, const void *Wg,
+                                         const void *Wu, const void *Wd, float *y, int T, int H,
+                                         int I, int E, int top_k, void *stream);
 
 /* Allocate (or grow) the current device's workspace for calls up to the given
  * sizes, so that later calls allocate nothing (call it before capturing calls

@@ -164,8 +164,12 @@ zffn_status zffn_q4k_quantize(const float *w, void *blocks, int64_t rows, int64_
     return to_status(launch_q4k_quantize(w, blocks, rows, cols, (cudaStream_t)stream));
 }
 
-zffn_status zffn_swiglu_q4k(const void *x, const void *Wg, const void *Wu, const void *Wd,
-                            float *y, int T, int H, int I, void *stream) {
+}  // extern "C"
+
+namespace {
+
+zffn_status swiglu_dense(const void *x, const void *Wg, const void *Wu, const void *Wd, float *y,
+                         int T, int H, int I, void *stream, bool accumulate) {
     if (!x || !Wg || !Wu || !Wd || !y) return ZFFN_ERR_INVALID_ARG;
     if (check_shape(T, H, I) != ZFFN_OK) return ZFFN_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd) || !aligned16(y))
@@ -196,10 +200,13 @@ zffn_status zffn_swiglu_q4k(const void *x, const void *Wg, const void *Wu, const
         a.barrier = reinterpret_cast<unsigned *>(base + L.barrier);
         a.err = di.err_word;
         a.T = T; a.H = H; a.I = I; a.E = 1; a.k = 1;
+        a.accumulate = accumulate;
         return to_status(launch_ffn_matvec(a, s));
     }
-    cudaError_t e = launch_zero_f32(y, (int64_t)T * H, s);
-    if (e != cudaSuccess) return to_status(e);
+    if (!accumulate) {
+        cudaError_t e = launch_zero_f32(y, (int64_t)T * H, s);
+        if (e != cudaSuccess) return to_status(e);
+    }
     TcArgs a{};
     a.x = x;
     a.x_rows = T;
@@ -217,10 +224,9 @@ zffn_status zffn_swiglu_q4k(const void *x, const void *Wg, const void *Wu, const
     return to_status(launch_ffn_tc(a, s));
 }
 
-zffn_status zffn_moe_swiglu_q4k(const void *x, const int32_t *expert_ids,
-                                const float *expert_weights, const void *Wg, const void *Wu,
-                                const void *Wd, float *y, int T, int H, int I, int E, int top_k,
-                                void *stream) {
+zffn_status swiglu_moe(const void *x, const int32_t *expert_ids, const float *expert_weights,
+                       const void *Wg, const void *Wu, const void *Wd, float *y, int T, int H,
+                       int I, int E, int top_k, void *stream, bool accumulate) {
     if (!x || !expert_ids || !expert_weights || !Wg || !Wu || !Wd || !y)
         return ZFFN_ERR_INVALID_ARG;
     if (check_shape(T, H, I) != ZFFN_OK) return ZFFN_ERR_INVALID_ARG;
@@ -256,6 +262,7 @@ zffn_status zffn_moe_swiglu_q4k(const void *x, const int32_t *expert_ids,
         a.barrier = reinterpret_cast<unsigned *>(base + L.barrier);
         a.err = di.err_word;
         a.T = T; a.H = H; a.I = I; a.E = E; a.k = top_k;
+        a.accumulate = accumulate;
         return to_status(launch_ffn_matvec(a, s));
     }
     RouteArgs r{};
@@ -274,8 +281,10 @@ zffn_status zffn_moe_swiglu_q4k(const void *x, const int32_t *expert_ids,
     r.max_tiles = L.max_tiles;
     cudaError_t e = launch_moe_route(r, s);
     if (e != cudaSuccess) return to_status(e);
-    e = launch_zero_f32(y, (int64_t)T * H, s);
-    if (e != cudaSuccess) return to_status(e);
+    if (!accumulate) {
+        e = launch_zero_f32(y, (int64_t)T * H, s);
+        if (e != cudaSuccess) return to_status(e);
+    }
     TcArgs a{};
     a.x = r.x_perm;
     a.x_rows = (int64_t)T * top_k;
@@ -291,6 +300,37 @@ zffn_status zffn_moe_swiglu_q4k(const void *x, const int32_t *expert_ids,
     a.err = di.err_word;
     a.T = T; a.H = H; a.I = I;
     return to_status(launch_ffn_tc(a, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+zffn_status zffn_swiglu_q4k(const void *x, const void *Wg, const void *Wu, const void *Wd,
+                            float *y, int T, int H, int I, void *stream) {
+    return swiglu_dense(x, Wg, Wu, Wd, y, T, H, I, stream, false);
+}
+
+zffn_status zffn_swiglu_q4k_residual(const void *x, const void *Wg, const void *Wu,
+                                     const void *Wd, float *y, int T, int H, int I,
+                                     void *stream) {
+    return swiglu_dense(x, Wg, Wu, Wd, y, T, H, I, stream, true);
+}
+
+zffn_status zffn_moe_swiglu_q4k(const void *x, const int32_t *expert_ids,
+                                const float *expert_weights, const void *Wg, const void *Wu,
+                                const void *Wd, float *y, int T, int H, int I, int E, int top_k,
+                                void *stream) {
+    return swiglu_moe(x, expert_ids, expert_weights, Wg, Wu, Wd, y, T, H, I, E, top_k, stream,
+                      false);
+}
+
+zffn_status zffn_moe_swiglu_q4k_residual(const void *x, const int32_t *expert_ids,
+                                         const float *expert_weights, const void *Wg,
+                                         const void *Wu, const void *Wd, float *y, int T, int H,
+                                         int I, int E, int top_k, void *stream) {
+    return swiglu_moe(x, expert_ids, expert_weights, Wg, Wu, Wd, y, T, H, I, E, top_k, stream,
+                      true);
 }
 
 zffn_status zffn_reserve(int T_max, int H_max, int I_max, int E_max, int top_k_max) {

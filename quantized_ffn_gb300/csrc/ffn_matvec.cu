@@ -243,7 +243,10 @@ __global__ void __launch_bounds__(kMvThreads, 1) ffn_matvec_kernel(MatvecArgs a)
             }
         }
         acc = warp_sum(acc);
-        if (lane == 0) a.y[(int64_t)t * H + n] = acc;
+        if (lane == 0) {
+            float *dst = a.y + (int64_t)t * H + n;
+            *dst = a.accumulate ? *dst + acc : acc;
+        }
     }
 }
 

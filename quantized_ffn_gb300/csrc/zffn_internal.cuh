@@ -262,6 +262,7 @@ struct MatvecArgs {
     unsigned int *barrier;       // workspace, two words, zero-initialised once
     int *err;
     int T, H, I, E, k;
+    bool accumulate;             // y += result instead of y = result
 };
 size_t matvec_smem_bytes(int T, int H, int I, int k);
 cudaError_t launch_ffn_matvec(const MatvecArgs &a, cudaStream_t s);

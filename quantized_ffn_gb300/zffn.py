@@ -51,6 +51,9 @@ def load() -> ctypes.CDLL:
                 "zffn_q4k_quantize": ([P, P, I64, I64, P], I32),
                 "zffn_swiglu_q4k": ([P, P, P, P, P, I32, I32, I32, P], I32),
                 "zffn_moe_swiglu_q4k": ([P, P, P, P, P, P, P, I32, I32, I32, I32, I32, P], I32),
+                "zffn_swiglu_q4k_residual": ([P, P, P, P, P, I32, I32, I32, P], I32),
+                "zffn_moe_swiglu_q4k_residual": ([P, P, P, P, P, P, P, I32, I32, I32, I32, I32, P],
+                                                 I32),
                 "zffn_reserve": ([I32, I32, I32, I32, I32], I32),
                 "zffn_release": ([], None),
                 "zffn_get_device_error": ([P], I32),
@@ -115,27 +118,35 @@ def q4k_quantize(w: torch.Tensor, out: Optional[torch.Tensor] = None, stream=Non
 
 
 def swiglu_q4k(x: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor, Wd: torch.Tensor, I: int,
-               y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """y[T, H] fp32 = W_down (silu(W_gate x) * (W_up x)) with Q4_K weights."""
+               y: Optional[torch.Tensor] = None, stream=None, residual: bool = False
+               ) -> torch.Tensor:
+    """y[T, H] fp32 = W_down (silu(W_gate x) * (W_up x)) with Q4_K weights
+    (residual=True: y += that, y must be given)."""
     T, H = x.shape
     if y is None:
+        if residual:
+            raise ValueError("residual=True needs y")
         y = torch.empty((T, H), dtype=torch.float32, device=x.device)
-    _check(load().zffn_swiglu_q4k(_cuda(x, "x", torch.bfloat16), _cuda(Wg, "Wg", torch.uint8),
-                                  _cuda(Wu, "Wu", torch.uint8), _cuda(Wd, "Wd", torch.uint8),
-                                  _cuda(y, "y", torch.float32), T, H, I, _stream(stream)),
-           "zffn_swiglu_q4k")
+    fn = load().zffn_swiglu_q4k_residual if residual else load().zffn_swiglu_q4k
+    _check(fn(_cuda(x, "x", torch.bfloat16), _cuda(Wg, "Wg", torch.uint8),
+              _cuda(Wu, "Wu", torch.uint8), _cuda(Wd, "Wd", torch.uint8),
+              _cuda(y, "y", torch.float32), T, H, I, _stream(stream)), "zffn_swiglu_q4k")
     return y
 
 
 def moe_swiglu_q4k(x: torch.Tensor, expert_ids: torch.Tensor, expert_weights: torch.Tensor,
                    Wg: torch.Tensor, Wu: torch.Tensor, Wd: torch.Tensor, I: int, E: int,
-                   y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Routed experts: y[t] = sum_j w[t, j] FFN_{ids[t, j]}(x[t])."""
+                   y: Optional[torch.Tensor] = None, stream=None, residual: bool = False
+                   ) -> torch.Tensor:
+    """Routed experts: y[t] = sum_j w[t, j] FFN_{ids[t, j]}(x[t]) (residual: y += ...)."""
     T, H = x.shape
     top_k = expert_ids.shape[1]
     if y is None:
+        if residual:
+            raise ValueError("residual=True needs y")
         y = torch.empty((T, H), dtype=torch.float32, device=x.device)
-    _check(load().zffn_moe_swiglu_q4k(
+    fn = load().zffn_moe_swiglu_q4k_residual if residual else load().zffn_moe_swiglu_q4k
+    _check(fn(
         _cuda(x, "x", torch.bfloat16), _cuda(expert_ids, "expert_ids", torch.int32),
         _cuda(expert_weights, "expert_weights", torch.float32), _cuda(Wg, "Wg", torch.uint8),
         _cuda(Wu, "Wu", torch.uint8), _cuda(Wd, "Wd", torch.uint8),
