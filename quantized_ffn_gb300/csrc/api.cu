@@ -109,6 +109,8 @@ zffn_status to_status(cudaError_t e) {
 
 }  // namespace
 
+void set_last_error(const char *what) { t_last_error = what; }
+
 const DeviceInfo &device_info() {
     const int dev = current_device();
     static DeviceInfo none;

@@ -243,6 +243,7 @@ struct DeviceInfo {
     int *err_word = nullptr;   // device error word of this device
 };
 const DeviceInfo &device_info();   // current device (cached per device)
+void set_last_error(const char *what);   // text returned by zffn_last_error()
 
 cudaError_t launch_q4k_dequant(const void *blocks, float *out, int64_t rows, int64_t cols,
                                cudaStream_t s);
