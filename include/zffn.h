@@ -90,7 +90,7 @@ zffn_status zffn_q4k_quantize(const float *w, void *blocks, int64_t rows, int64_
  *   Wd: Q4_K, H rows of ceil(I/256) blocks (W_down: [H x I]), 16-byte aligned.
  *   y:  fp32 [T][H] row-major, overwritten, 16-byte aligned.
  * Requirements: T >= 1, H % 256 == 0, I % 64 == 0, 256 <= H <= 16384,
- * 64 <= I <= 65536.  T <= 1 runs the memory-bound single-token kernel; larger T
+ * 64 <= I <= 65536.  T = 1 runs the memory-bound single-token kernel; larger T
  * run the tensor-core prefill kernel (the switch-over can be changed with
  * zffn_set_option).  Accumulation is fp32; operands of the tensor-core path are
  * rounded to bf16 (x is bf16 already; unpacked weights and the SwiGLU
@@ -139,7 +139,7 @@ zffn_status zffn_moe_swiglu_q4k_residual(const void *x, const int32_t *expert_id
  * loop that forbids allocation after start-up.  It computes the same block as
  * zffn_swiglu_q4k with T = 1 (same kernel), but its scratch (the intermediate
  * strip and the grid-barrier words) lives in one fixed array compiled into the
- * library: about 64 KB that every GPU loading the library keeps until exit.
+ * library: 66 KB that every GPU loading the library keeps until exit.
  *   x: bf16 [H]; Wg, Wu, Wd and y as for zffn_swiglu_q4k with T = 1.
  * Limits: I <= 16384 (the array's size); larger I returns ZFFN_ERR_INVALID_ARG
  * and zffn_last_error() says why.  The first call on a device looks up the
@@ -171,10 +171,10 @@ const char *zffn_last_error(void);
  * read.  ZFFN_ERR_CUDA if the synchronisation itself failed. */
 zffn_status zffn_get_device_error(void *stream);
 
-/* Tunables (process-wide).  ZFFN_OPT_MATVEC_MAX_T: largest token count T, dense
- * or routed, sent to the memory-bound single-token kernel (default 1; 0 sends
- * every call to the tensor-core kernel).  Returns the previous value, or -1
- * for an unknown key. */
+/* Tunables (process-wide).  ZFFN_OPT_MATVEC_MAX_T: 1 (default) sends single-token
+ * calls (T = 1, dense or routed) to the memory-bound single-token kernel; 0
+ * sends every call to the tensor-core kernel (any value > 1 acts as 1).
+ * Returns the previous value, or -1 for an unknown key. */
 enum { ZFFN_OPT_MATVEC_MAX_T = 1 };
 int zffn_set_option(int key, int value);
 

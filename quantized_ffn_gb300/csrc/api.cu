@@ -40,7 +40,7 @@ Layout layout_for(int T, int H, int I, int E, int k) {
     size_t o = 0;
     const int64_t P = (int64_t)T * k;
     L.max_tiles = (int)((P + 127) / 128 + (E < P ? E : P));
-    L.barrier = o; o = align_up(o + 2 * sizeof(unsigned));
+    L.barrier = o; o = align_up(o + kGridBarrierWords * sizeof(unsigned));
     L.h = o; o = align_up(o + (size_t)P * I * sizeof(float));
     L.counts = o; o = align_up(o + (size_t)E * sizeof(int));
     L.offsets = o; o = align_up(o + (size_t)(E + 1) * sizeof(int));
@@ -78,7 +78,7 @@ zffn_status ensure_workspace(size_t bytes, Workspace **out) {
             cudaGetLastError();
             return ZFFN_ERR_NO_WORKSPACE;
         }
-        if (cudaMemset(p, 0, kAlign) != cudaSuccess) {
+        if (cudaMemset(p, 0, align_up(kGridBarrierWords * sizeof(unsigned))) != cudaSuccess) {
             cudaFree(p);
             return ZFFN_ERR_CUDA;
         }
@@ -184,7 +184,7 @@ zffn_status swiglu_dense(const void *x, const void *Wg, const void *Wu, const vo
         std::lock_guard<std::mutex> lk(g_mu);
         mv_max = g_matvec_max_t;
     }
-    if (T <= mv_max && matvec_smem_bytes(T, H, I, 1) <= (size_t)di.max_smem_optin) {
+    if (T == 1 && mv_max >= 1 && matvec_smem_bytes(T, H, I, 1) <= (size_t)di.max_smem_optin) {
         const Layout L = layout_for(T, H, I, 1, 1);
         Workspace *w = nullptr;
         zffn_status st = ensure_workspace(L.total, &w);
@@ -251,7 +251,7 @@ zffn_status swiglu_moe(const void *x, const int32_t *expert_ids, const float *ex
     zffn_status st = ensure_workspace(L.total, &w);
     if (st != ZFFN_OK) return st;
     uint8_t *base = static_cast<uint8_t *>(w->ptr);
-    if (T <= mv_max && matvec_smem_bytes(T, H, I, top_k) <= (size_t)di.max_smem_optin) {
+    if (T == 1 && mv_max >= 1 && matvec_smem_bytes(T, H, I, top_k) <= (size_t)di.max_smem_optin) {
         MatvecArgs a{};
         a.x = static_cast<const __nv_bfloat16 *>(x);
         a.Wg = static_cast<const uint8_t *>(Wg);
@@ -370,7 +370,7 @@ zffn_status zffn_get_device_error(void *stream) {
         // a timed-out grid barrier may have left its counter mid-way: reset it
         std::lock_guard<std::mutex> lk(g_mu);
         Workspace &w = g_ws[di.device];
-        if (w.barrier && cudaMemsetAsync(w.barrier, 0, 2 * sizeof(unsigned), s) != cudaSuccess)
+        if (w.barrier && cudaMemsetAsync(w.barrier, 0, kGridBarrierWords * sizeof(unsigned), s) != cudaSuccess)
             return ZFFN_ERR_CUDA;
     }
     if (cudaStreamSynchronize(s) != cudaSuccess) return to_status(cudaErrorUnknown);

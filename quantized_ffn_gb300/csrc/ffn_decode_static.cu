@@ -10,7 +10,7 @@
 // with its scratch in a fixed array compiled into the library instead.
 //
 // The array is a file-scope __device__ object: every GPU that loads the
-// library holds it (about 64 KB) until the process exits.  Host code cannot
+// library holds it (66 KB) until the process exits.  Host code cannot
 // use the array's name as a device address, so the first call on each device
 // looks the address up with cudaGetSymbolAddress (with that device current)
 // and caches it; that first call should therefore be made before any stream
@@ -24,7 +24,7 @@
 namespace zffn {
 
 constexpr int kStaticMaxI = 16384;                 // largest intermediate width
-constexpr int kStaticBarrierWords = 64;            // 256 bytes, first two used
+constexpr int kStaticBarrierWords = kGridBarrierWords;   // 2 KB of grid-barrier words
 constexpr size_t kStaticScratchFloats = kStaticMaxI + kStaticBarrierWords;
 
 static __device__ __align__(256) float g_static_scratch[kStaticScratchFloats];
@@ -88,7 +88,7 @@ zffn_status zffn_swiglu_q4k_token_static(const void *x, const void *Wg, const vo
     cudaStream_t s = (cudaStream_t)stream;
     // barrier words first (256-byte aligned), then the intermediate strip
     unsigned *barrier = reinterpret_cast<unsigned *>(scratch);
-    cudaError_t e = cudaMemsetAsync(barrier, 0, 2 * sizeof(unsigned), s);
+    cudaError_t e = cudaMemsetAsync(barrier, 0, kGridBarrierWords * sizeof(unsigned), s);
     if (e == cudaSuccess) {
         MatvecArgs a{};
         a.x = static_cast<const __nv_bfloat16 *>(x);

@@ -1,94 +1,128 @@
-// ffn_matvec.cu -- the memory-bound path for a single token (dense decode) and
-// for a handful of (token, expert) pairs (MoE decode).
+// ffn_matvec.cu -- the memory-bound path for one token: dense decode and the
+// routed (mixture-of-experts) decode over the token's top_k experts.
 //
-// One persistent launch (cooperative, one 512-thread block per SM) in two
-// phases separated by a bounded grid barrier:
-//   phase 1: for every pair p and intermediate row i, stream the W_gate and
-//            W_up rows once, dot them with x (same input, one pass: "fuse the
-//            same-input Q4_K matvec pairs", "Four bottlenecks, one CUDA
-//            backend...", Bottleneck 3) and store h[p][i] = silu(g) * u
-//            (fp32, a few tens of KB that stay in L2 and are consumed at once:
-//            for one token the intermediate is small, "Fused SwiGLU MLP...",
-//            FAQ "Does this affect decode?");
-//   phase 2: stream the W_down rows: y[t][n] = sum_p w_p * Wd_{e_p}[n] . h[p].
-// While phase 1 runs, every warp asks the L2 to prefetch the W_down rows it
-// will read in phase 2, so the barrier and phase 2 overlap HBM traffic.
-// Expert ids are read on the device ("Bottleneck 2"), never on the host.
+// One persistent launch (cooperative, one block per SM) in two phases
+// separated by a bounded grid barrier:
+//   phase 1: for every (expert slot p, intermediate row i) owned by this block,
+//            dot the W_gate and W_up rows with x (same input, one pass over x:
+//            "fuse the same-input Q4_K matvec pairs", "Four bottlenecks, one
+//            CUDA backend...", Bottleneck 3) and store h[p][i] = silu(g) * u in
+//            fp32.  For one token the intermediate is a few tens of KB that
+//            are consumed at once ("Fused SwiGLU MLP...", FAQ "Does this
+//            affect decode?").
+//   phase 2: y[n] = sum_p w_p * Wd_{e_p}[n] . h[p] for the output rows of
+//            this block.  Expert ids are read on the device ("Bottleneck 2").
 //
-// Lane layout for one 256-weight block: 8 lanes per block, 4 blocks per warp
-// step.  Lane (b, s) owns code bytes 32g+16h .. +15 (g = s/2, h = s%2):
-// weights 64g+16h+v (low nibbles, sub-block 2g) and 64g+32+16h+v (high
-// nibbles, sub-block 2g+1), v = 0..15.  The dot product of a sub-block is
-// d*sc*sum(q*x) - dmin*m*sum(x).  Vectors live in shared memory padded by 4
-// floats every 64, which makes the lanes' 16-byte reads bank-conflict free.
+// Data movement: one producer warp streams the packed weight rows of the
+// block's whole stage sequence (phase 1, then phase 2) into a 3-deep ring of
+// shared-memory stages with bulk asynchronous copies; it does not wait for
+// the grid barrier, so the first W_down stages are already in flight while
+// the block waits there.  Eight consumer warps unpack from shared memory.
+//
+// Arithmetic: the vector (x, later h) is stored in shared memory as int16 per
+// 128-element half-block with one fp32 scale each (relative rounding error
+// 2^-16 of the half-block's largest magnitude), plus the fp32 sum of every
+// 32-element sub-block.  A sub-block's dot product is
+//     d*sc * scale * sum(q * v_int) - dmin*m * sum(v)
+// where sum(q * v_int) is exact in int32: the 4-bit codes are masked into
+// int8 lanes (one LOP3 per four codes) and multiplied with int16 pairs by
+// dp2a.  Each lane owns one half-block (128 weights) of one row.
 #include "zffn_internal.cuh"
 
 namespace zffn {
 
-constexpr int kMvThreads = 512;
-constexpr int kMvWarps = kMvThreads / 32;
+constexpr int kMvConsumerWarps = 12;
+constexpr int kMvConsumers = kMvConsumerWarps * 32;
+constexpr int kMvThreads = kMvConsumers + 32;          // + producer warp
+constexpr int kMvStages = 3;
+constexpr int kMvStageBytes = 55296;                   // 54 KB, multiple of 16
+constexpr int kMvMaxRows = 64;                          // rows per stage cap
+constexpr int kHalfBytes = 272;                         // 128 int16 + 16 pad
 
-__host__ __device__ inline int padded_len(int n) { return n + (n / 64) * 4; }
-__device__ __forceinline__ int pad_index(int k) { return k + (k >> 6) * 4; }
-
-// Partial dot product of one lane's 32 weights of a block with a padded vector.
-struct BlockPart {
-    float ds0, dm0, ds1, dm1;
+struct MvGeom {
+    int P;            // expert slots of the token (dense: 1)
+    int nbH, nbI;     // blocks per W_gate/W_up row, per W_down row
+    int64_t rbH, rbI; // bytes per row
+    int R1, R2;       // rows per stage in phase 1 (row pairs) and phase 2
+    int nhalf1, nhalf2;   // vector half-blocks in phase 1 and phase 2
 };
 
-__device__ __forceinline__ BlockPart decode_head(uint4 hd, int g) {
-    BlockPart r;
-    const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
-    int sc, m;
-    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g, sc, m);
-    r.ds0 = d * (float)sc;
-    r.dm0 = dmin * (float)m;
-    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g + 1, sc, m);
-    r.ds1 = d * (float)sc;
-    r.dm1 = dmin * (float)m;
+// Half-block slots reserved per row: the real count 2*nb rounded up to a
+// power of two (<= 32) or to a multiple of 32, so that rows never straddle
+// a 32-lane chunk unevenly.
+__host__ __device__ inline int slots_per_row(int nb) {
+    const int lr = 2 * nb;
+    if (lr > 32) return (lr + 31) & ~31;
+    int lp = 1;
+    while (lp < lr) lp <<= 1;
+    return lp;
+}
+
+// Rows per stage: as many as fit (at most kMvMaxRows), trimmed so that the
+// stage's 32-lane chunks split evenly over the consumer warps when that
+// costs at most a quarter of the rows.
+__host__ __device__ inline int rows_per_stage(int64_t bytes_per_row, int nmat, int nb) {
+    int r = (int)(kMvStageBytes / bytes_per_row);
+    if (r > kMvMaxRows) r = kMvMaxRows;
+    const int lp = slots_per_row(nb);
+    for (int t = r; t >= 1 && 4 * t >= 3 * r; --t) {
+        const int chunks = (nmat * t * lp + 31) / 32;
+        if (chunks % kMvConsumerWarps == 0) return t;
+    }
     return r;
 }
 
-// sums of q*x over the low and high nibbles of 16 code bytes
-__device__ __forceinline__ void qx_sums(uint4 qs, const float *xlo, const float *xhi, float &slo,
-                                        float &shi) {
-    const uint32_t w[4] = {qs.x, qs.y, qs.z, qs.w};
-    float a = 0.f, b = 0.f;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const float4 l4 = *reinterpret_cast<const float4 *>(xlo + 4 * u);
-        const float4 h4 = *reinterpret_cast<const float4 *>(xhi + 4 * u);
-        const uint32_t ww = w[u];
-        a = fmaf((float)(ww & 15), l4.x, a);
-        a = fmaf((float)((ww >> 8) & 15), l4.y, a);
-        a = fmaf((float)((ww >> 16) & 15), l4.z, a);
-        a = fmaf((float)((ww >> 24) & 15), l4.w, a);
-        b = fmaf((float)((ww >> 4) & 15), h4.x, b);
-        b = fmaf((float)((ww >> 12) & 15), h4.y, b);
-        b = fmaf((float)((ww >> 20) & 15), h4.z, b);
-        b = fmaf((float)((ww >> 28) & 15), h4.w, b);
-    }
-    slo = a;
-    shi = b;
+__host__ __device__ inline MvGeom mv_geom(int H, int I, int k) {
+    MvGeom g;
+    g.P = k;
+    g.nbH = H / kQK;
+    g.nbI = (I + kQK - 1) / kQK;
+    g.rbH = (int64_t)g.nbH * kBlockBytes;
+    g.rbI = (int64_t)g.nbI * kBlockBytes;
+    g.R1 = rows_per_stage(2 * g.rbH, 2, g.nbH);
+    g.R2 = rows_per_stage(g.rbI, 1, g.nbI);
+    g.nhalf1 = 2 * g.nbH;
+    g.nhalf2 = g.P * 2 * g.nbI;
+    return g;
 }
 
-__device__ __forceinline__ void x_sums(const float *xlo, const float *xhi, float &slo, float &shi) {
-    float a = 0.f, b = 0.f;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const float4 l4 = *reinterpret_cast<const float4 *>(xlo + 4 * u);
-        const float4 h4 = *reinterpret_cast<const float4 *>(xhi + 4 * u);
-        a += (l4.x + l4.y) + (l4.z + l4.w);
-        b += (h4.x + h4.y) + (h4.z + h4.w);
-    }
-    slo = a;
-    shi = b;
+struct MvSmem {
+    size_t ring, vec, vscale, vsum, acc, yacc, bars, total;
+};
+
+__host__ __device__ inline MvSmem mv_smem_layout(const MvGeom &g) {
+    MvSmem L;
+    size_t o = 0;
+    const int nh = g.nhalf1 > g.nhalf2 ? g.nhalf1 : g.nhalf2;
+    L.ring = o; o += (size_t)kMvStages * kMvStageBytes;
+    L.vec = o; o += (size_t)nh * kHalfBytes;
+    L.vscale = o; o += (size_t)nh * 4;
+    L.vsum = o; o += (size_t)nh * 4 * 4;
+    L.acc = o; o += 2 * kMvMaxRows * 4;
+    L.yacc = o; o += kMvMaxRows * 4;
+    o = (o + 15) & ~(size_t)15;
+    L.bars = o; o += 2 * kMvStages * 8;
+    L.total = o;
+    return L;
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
+size_t matvec_smem_bytes(int T, int H, int I, int k) {
+    (void)T;
+    const MvGeom g = mv_geom(H, I, k);
+    if (g.R1 < 1 || g.R2 < 1) return (size_t)1 << 30;   // a row does not fit a stage
+    return mv_smem_layout(g).total;
+}
+
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kMvConsumers) : "memory");
 }
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
@@ -97,169 +131,391 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
     return v;
 }
 
-// Bounded grid barrier over all blocks of this launch (co-resident by the
-// cooperative launch).  bar[0] counts arrivals, bar[1] is the generation.
-__device__ void grid_barrier(unsigned *bar, int *err) {
-    __syncthreads();
+// Bounded grid barrier among the consumer threads of all blocks (co-resident
+// by the cooperative launch), without a chain of dependent atomics: bar[0] is
+// the launch epoch E (read at kernel start), bar[1 + b] is block b's flag.  A
+// block arriving stores E + 1 into its own flag, then waits until every flag
+// holds E + 1; block 0 then advances the epoch for the next launch (which
+// cannot start before this one ends).
+__device__ void grid_barrier(unsigned *bar, unsigned epoch, int *err) {
+    consumers_sync();
+    const unsigned target = epoch + 1;
     if (threadIdx.x == 0) {
-        const unsigned gen = ld_acquire_u32(bar + 1);
         __threadfence();
-        const unsigned arrived = atomicAdd(bar, 1u);
-        if (arrived == gridDim.x - 1) {
-            atomicExch(bar, 0u);
-            __threadfence();
-            atomicAdd(bar + 1, 1u);
-        } else {
-            const long long t0 = clock64();
-            while (ld_acquire_u32(bar + 1) == gen) {
-                if (clock64() - t0 > kWaitBudgetCycles) {
-                    record_error(err, ZFFN_ERR_TIMEOUT);
-                    break;
-                }
-                __nanosleep(32);
+        asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(bar + 1 + blockIdx.x), "r"(target)
+                     : "memory");
+    }
+    for (int b = threadIdx.x; b < (int)gridDim.x; b += kMvConsumers) {
+        const long long t0 = clock64();
+        while (ld_acquire_u32(bar + 1 + b) != target) {
+            if (clock64() - t0 > kWaitBudgetCycles) {
+                record_error(err, ZFFN_ERR_TIMEOUT);
+                break;
             }
         }
-        __threadfence();
     }
-    __syncthreads();
+    __threadfence();
+    consumers_sync();
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(bar), "r"(target) : "memory");
+}
+
+// Quantise one 128-element half-block of a vector (one warp, 4 values per
+// lane): int16 values, the half-block scale and the four sub-block sums.
+__device__ __forceinline__ void quantize_half(const float4 v4, int lane, uint8_t *vec_hb,
+                                              float *scale, float *sums) {
+    const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+    float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float inv = m > 0.0f ? 32766.0f / m : 0.0f;
+    int q[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) q[j] = __float2int_rn(v[j] * inv);
+    const uint32_t w0 = (uint32_t)(q[0] & 0xFFFF) | ((uint32_t)q[1] << 16);
+    const uint32_t w1 = (uint32_t)(q[2] & 0xFFFF) | ((uint32_t)q[3] << 16);
+    *reinterpret_cast<uint2 *>(vec_hb + 8 * lane) = make_uint2(w0, w1);
+    float s = (v[0] + v[1]) + (v[2] + v[3]);
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if ((lane & 7) == 0) sums[lane >> 3] = s;
+    if (lane == 0) *scale = m > 0.0f ? m / 32766.0f : 0.0f;
+}
+
+// Scale and min of sub-block 4*hh + jj without a branch on hh (lanes of one
+// warp own both halves; a branch would run both sides).
+__device__ __forceinline__ void scale_min_half(const uint4 &hd, int hh, int jj, int &sc, int &m) {
+    const uint32_t A = hh ? hd.w : hd.y;          // scale source: byte 8+jj or byte jj
+    const uint32_t B = hh ? hd.w : hd.z;          // min source:   byte 8+jj or byte 4+jj
+    const int sa = 8 * jj, sb = 8 * jj + 4 * hh;
+    const uint32_t low = hh ? 15u : 63u, top = hh ? 3u : 0u;
+    sc = (int)(((A >> sa) & low) | (((hd.y >> (sa + 6)) & top) << 4));
+    m = (int)(((B >> sb) & low) | (((hd.z >> (sa + 6)) & top) << 4));
+}
+
+// Dot product of one half-block of packed weights (header at blk, codes of
+// half hh) with a quantised vector half-block held in registers (xv: 128
+// int16), its scale and its four sub-block sums.
+__device__ __forceinline__ float half_block_dot(const uint8_t *blk, int hh, const uint4 (&xv)[16],
+                                                float vscale, const float (&vsum)[4]) {
+    const uint4 hd = *reinterpret_cast<const uint4 *>(blk);
+    const uint4 *qs = reinterpret_cast<const uint4 *>(blk + 16 + 64 * hh);
+    int acc_a[4] = {0, 0, 0, 0}, acc_b[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {            // the two 64-weight groups of the half
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {        // 16 code bytes: weights 16c.. (low) and 32+16c.. (high)
+            const uint4 qv = qs[2 * g + c];
+            const uint4 xlo0 = xv[8 * g + 2 * c], xlo1 = xv[8 * g + 2 * c + 1];
+            const uint4 xhi0 = xv[8 * g + 4 + 2 * c], xhi1 = xv[8 * g + 4 + 2 * c + 1];
+            const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+            const uint32_t lo[8] = {xlo0.x, xlo0.y, xlo0.z, xlo0.w, xlo1.x, xlo1.y, xlo1.z, xlo1.w};
+            const uint32_t hi[8] = {xhi0.x, xhi0.y, xhi0.z, xhi0.w, xhi1.x, xhi1.y, xhi1.z, xhi1.w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const int ql = (int)(qw[w] & 0x0F0F0F0Fu);
+                const int qh = (int)((qw[w] >> 4) & 0x0F0F0F0Fu);
+                acc_a[2 * g] = __dp2a_lo((int)lo[2 * w], ql, acc_a[2 * g]);
+                acc_b[2 * g] = __dp2a_hi((int)lo[2 * w + 1], ql, acc_b[2 * g]);
+                acc_a[2 * g + 1] = __dp2a_lo((int)hi[2 * w], qh, acc_a[2 * g + 1]);
+                acc_b[2 * g + 1] = __dp2a_hi((int)hi[2 * w + 1], qh, acc_b[2 * g + 1]);
+            }
+        }
+    }
+    const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
+    const float dv = d * vscale;
+    float r = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        int sc, m;
+        scale_min_half(hd, hh, j, sc, m);
+        r = fmaf(dv * (float)sc, (float)(acc_a[j] + acc_b[j]), r);
+        r = fmaf(-(dmin * (float)m), vsum[j], r);
+    }
+    return r;
+}
+
+__device__ __forceinline__ void load_half(const uint8_t *vec, const float *vscale,
+                                          const float *vsum, int hb, uint4 (&xv)[16], float &sc,
+                                          float (&sm)[4]) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(vec + (size_t)hb * kHalfBytes);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) xv[i] = src[i];
+    sc = vscale[hb];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) sm[j] = vsum[4 * hb + j];
+}
+
+// A lane keeps one vector half-block in registers when it always owns the
+// same slot of a row: rows of at most 32 slots (slot = lane mod slots), or
+// rows of several 32-slot chunks when the consumer warps split evenly into
+// one class per chunk position.
+__device__ __forceinline__ bool slot_resident(int Lp) {
+    return Lp <= 32 || kMvConsumerWarps % (Lp >> 5) == 0;
+}
+__device__ __forceinline__ int lane_slot(int Lp, int warp, int lane) {
+    return Lp <= 32 ? (lane & (Lp - 1)) : (warp % (Lp >> 5)) * 32 + lane;
 }
 
 __global__ void __launch_bounds__(kMvThreads, 1) ffn_matvec_kernel(MatvecArgs a) {
-    extern __shared__ __align__(16) float smem[];
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int gwarp = blockIdx.x * kMvWarps + warp;
-    const int nwarps = gridDim.x * kMvWarps;
-    const int H = a.H, I = a.I, k = a.k;
-    const int P = a.T * k;                      // (token, slot) pairs
-    const int nbH = H / kQK;
-    const int nbI = (I + kQK - 1) / kQK;
-    const int64_t rbH = (int64_t)nbH * kBlockBytes;
-    const int64_t rbI = (int64_t)nbI * kBlockBytes;
-    const int Hp = padded_len(H), Ip = padded_len(nbI * kQK);
-    const int sub = lane & 7, g = sub >> 1, hh = sub & 1, bl = lane >> 3;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const MvGeom G = mv_geom(a.H, a.I, a.k);
+    const MvSmem L = mv_smem_layout(G);
+    uint8_t *ring = smem + L.ring;
+    uint8_t *vec = smem + L.vec;
+    float *vscale = reinterpret_cast<float *>(smem + L.vscale);
+    float *vsum = reinterpret_cast<float *>(smem + L.vsum);
+    float *acc = reinterpret_cast<float *>(smem + L.acc);      // [2][kMvMaxRows]
+    float *yacc = reinterpret_cast<float *>(smem + L.yacc);    // [kMvMaxRows]
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *empty = full + kMvStages;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = a.H, I = a.I, P = G.P;
     const bool moe = a.ids != nullptr;
-
     auto expert_of = [&](int p) -> int { return moe ? a.ids[p] : 0; };
+    auto valid = [&](int e) -> bool { return e >= 0 && e < a.E; };
 
-    // ---- L2 prefetch of this warp's phase-2 W_down rows --------------------
-    if (lane == 0) {
-        for (int task = gwarp; task < a.T * H; task += nwarps) {
-            const int t = task / H, n = task % H;
-            for (int j = 0; j < k; ++j) {
-                const int e = expert_of(t * k + j);
-                if (e < 0 || e >= a.E) continue;
-                prefetch_l2_bulk(a.Wd + ((int64_t)e * H + n) * rbI, (uint32_t)rbI);
-            }
+    const int64_t rows1 = (int64_t)P * I;
+    const int r0 = (int)(rows1 * blockIdx.x / gridDim.x), r1 = (int)(rows1 * (blockIdx.x + 1) / gridDim.x);
+    const int n0 = (int)((int64_t)H * blockIdx.x / gridDim.x), n1 = (int)((int64_t)H * (blockIdx.x + 1) / gridDim.x);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kMvStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
         }
-    }
-
-    // ---- phase 1: h[p][i] = silu(Wg_e[i] . x_t) * (Wu_e[i] . x_t) ------------
-    for (int idx = threadIdx.x; idx < a.T * Hp; idx += blockDim.x) {
-        const int t = idx / Hp, kp = idx % Hp;
-        // inverse of pad_index: position kp belongs to 68-float groups
-        const int grp = kp / 68, off = kp % 68;
-        float v = 0.f;
-        if (off < 64) v = __bfloat162float(a.x[(int64_t)t * H + grp * 64 + off]);
-        smem[idx] = v;
+        fence_mbarrier_init();
     }
     __syncthreads();
 
-    for (int task = gwarp; task < P * I; task += nwarps) {
-        const int p = task / I, i = task % I;
-        const int e = expert_of(p);
-        const int t = p / k;
-        float gacc = 0.f, uacc = 0.f;
-        if (e >= 0 && e < a.E) {
-            const uint8_t *rg = a.Wg + ((int64_t)e * I + i) * rbH;
-            const uint8_t *ru = a.Wu + ((int64_t)e * I + i) * rbH;
-            const float *xs = smem + t * Hp;
-#pragma unroll 4
-            for (int b0 = 0; b0 < nbH; b0 += 4) {
-                const int b = b0 + bl;
-                if (b < nbH) {
-                    const int64_t off = (int64_t)b * kBlockBytes;
-                    const uint4 hg = __ldg(reinterpret_cast<const uint4 *>(rg + off));
-                    const uint4 qg = __ldg(reinterpret_cast<const uint4 *>(rg + off + 16 + 32 * g + 16 * hh));
-                    const uint4 hu = __ldg(reinterpret_cast<const uint4 *>(ru + off));
-                    const uint4 qu = __ldg(reinterpret_cast<const uint4 *>(ru + off + 16 + 32 * g + 16 * hh));
-                    const float *xlo = xs + pad_index(b * kQK + 64 * g + 16 * hh);
-                    const float *xhi = xlo + 32;
-                    float sxl, sxh;
-                    x_sums(xlo, xhi, sxl, sxh);
-                    float ql, qh;
-                    const BlockPart pg = decode_head(hg, g);
-                    qx_sums(qg, xlo, xhi, ql, qh);
-                    gacc += pg.ds0 * ql - pg.dm0 * sxl + pg.ds1 * qh - pg.dm1 * sxh;
-                    const BlockPart pu = decode_head(hu, g);
-                    qx_sums(qu, xlo, xhi, ql, qh);
-                    uacc += pu.ds0 * ql - pu.dm0 * sxl + pu.ds1 * qh - pu.dm1 * sxh;
-                }
-            }
-        }
-        gacc = warp_sum(gacc);
-        uacc = warp_sum(uacc);
+    if (warp == kMvConsumerWarps) {
+        // ------------------------- producer -------------------------------
         if (lane == 0) {
-            const float s = gacc / (1.0f + expf(-gacc));
-            a.h[(int64_t)p * I + i] = s * uacc;
-        }
-    }
-
-    grid_barrier(a.barrier, a.err);
-
-    // ---- phase 2: y[t][n] = sum_j w_{t,j} * Wd_{e_{t,j}}[n] . h[t*k+j] ---------
-    for (int idx = threadIdx.x; idx < P * Ip; idx += blockDim.x) {
-        const int p = idx / Ip, kp = idx % Ip;
-        const int grp = kp / 68, off = kp % 68;
-        const int col = grp * 64 + off;
-        float v = 0.f;
-        if (off < 64 && col < I) v = __ldcg(a.h + (int64_t)p * I + col);
-        smem[idx] = v;
-    }
-    __syncthreads();
-
-    const int items = k * nbI;   // (slot, block) pairs per output row
-    for (int task = gwarp; task < a.T * H; task += nwarps) {
-        const int t = task / H, n = task % H;
-        float acc = 0.f;
-        for (int it0 = 0; it0 < items; it0 += 4) {
-            const int it = it0 + bl;
-            if (it < items) {
-                const int j = it / nbI, b = it % nbI;
-                const int p = t * k + j;
+            uint32_t slot = 0, ph = 0;
+            bool ok = true;
+            auto next = [&]() { if (++slot == kMvStages) { slot = 0; ph ^= 1; } };
+            // phase 1 stages: chunks of up to R1 rows within one slot p
+            for (int r = r0; r < r1 && ok;) {
+                const int p = r / I, i = r % I;
+                const int cnt = min(min(G.R1, r1 - r), I - i);
                 const int e = expert_of(p);
-                if (e >= 0 && e < a.E) {
-                    const float wgt = moe ? a.wts[p] : 1.0f;
-                    const uint8_t *rd = a.Wd + ((int64_t)e * H + n) * rbI + (int64_t)b * kBlockBytes;
-                    const uint4 hd = __ldg(reinterpret_cast<const uint4 *>(rd));
-                    const uint4 qd = __ldg(reinterpret_cast<const uint4 *>(rd + 16 + 32 * g + 16 * hh));
-                    const float *hs = smem + p * Ip + pad_index(b * kQK + 64 * g + 16 * hh);
-                    float sxl, sxh, ql, qh;
-                    x_sums(hs, hs + 32, sxl, sxh);
-                    qx_sums(qd, hs, hs + 32, ql, qh);
-                    const BlockPart pd = decode_head(hd, g);
-                    acc += wgt * (pd.ds0 * ql - pd.dm0 * sxl + pd.ds1 * qh - pd.dm1 * sxh);
+                if (valid(e)) {
+                    if (!mbar_wait(&empty[slot], ph ^ 1, nullptr, a.err)) { ok = false; break; }
+                    const uint32_t bytes = (uint32_t)(cnt * G.rbH);
+                    mbar_arrive_expect_tx(&full[slot], 2 * bytes);
+                    uint8_t *dst = ring + slot * kMvStageBytes;
+                    bulk_g2s(dst, a.Wg + ((int64_t)e * I + i) * G.rbH, bytes, &full[slot]);
+                    bulk_g2s(dst + bytes, a.Wu + ((int64_t)e * I + i) * G.rbH, bytes, &full[slot]);
+                    next();
                 }
+                r += cnt;
+            }
+            // phase 2 stages: for each chunk of up to R2 output rows, one stage per valid slot
+            for (int n = n0; n < n1 && ok;) {
+                const int cnt = min(G.R2, n1 - n);
+                for (int p = 0; p < P && ok; ++p) {
+                    const int e = expert_of(p);
+                    if (!valid(e)) continue;
+                    if (!mbar_wait(&empty[slot], ph ^ 1, nullptr, a.err)) { ok = false; break; }
+                    const uint32_t bytes = (uint32_t)(cnt * G.rbI);
+                    mbar_arrive_expect_tx(&full[slot], bytes);
+                    bulk_g2s(ring + slot * kMvStageBytes, a.Wd + ((int64_t)e * H + n) * G.rbI, bytes,
+                             &full[slot]);
+                    next();
+                }
+                n += cnt;
+            }
+            // every copy issued here lands before the block exits
+            for (int s = 0; s < kMvStages; ++s) {
+                mbar_wait(&empty[slot], ph ^ 1, nullptr, a.err, kWaitBudgetCycles / 8);
+                next();
             }
         }
-        acc = warp_sum(acc);
-        if (lane == 0) {
-            float *dst = a.y + (int64_t)t * H + n;
-            *dst = a.accumulate ? *dst + acc : acc;
-        }
+        return;
     }
-}
 
-size_t matvec_smem_bytes(int T, int H, int I, int k) {
-    const int nbI = (I + kQK - 1) / kQK;
-    const size_t p1 = (size_t)T * padded_len(H);
-    const size_t p2 = (size_t)T * k * padded_len(nbI * kQK);
-    return 4 * (p1 > p2 ? p1 : p2);
+    // ----------------------------- consumers ---------------------------------
+    const int tid = threadIdx.x;
+    const unsigned epoch = ld_acquire_u32(a.barrier);
+    uint32_t slot = 0, ph = 0;
+    auto next = [&]() { if (++slot == kMvStages) { slot = 0; ph ^= 1; } };
+    bool ok = true;
+
+    // Quantise nhalf vector half-blocks; load4(hb) returns this lane's four
+    // values of half-block hb.  A warp issues the loads of up to 8 of its
+    // half-blocks before using any, so the vector arrives in one round trip.
+    auto quantize_vector = [&](int nhalf, auto load4) {
+        for (int b0 = warp; b0 < nhalf; b0 += 8 * kMvConsumerWarps) {
+            float4 v[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int hb = b0 + t * kMvConsumerWarps;
+                v[t] = load4(hb < nhalf ? hb : b0);   // always a valid half-block: no branch
+            }
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int hb = b0 + t * kMvConsumerWarps;
+                if (hb < nhalf)
+                    quantize_half(v[t], lane, vec + (size_t)hb * kHalfBytes, vscale + hb, vsum + 4 * hb);
+            }
+        }
+    };
+
+    // Process one stage: nmat matrices of nrows rows with nb blocks each; each
+    // row's dot product with the vector half-blocks starting at vec_base
+    // lands in acc[mat][row].  Rows hold slots_per_row(nb) slots (half-blocks,
+    // the real ones first).  With a resident vector the lane's half-block is
+    // already in xr.
+    uint4 xr[16];
+    float xs = 0.0f, xsum[4] = {0.f, 0.f, 0.f, 0.f};
+    auto run_stage = [&](int nmat, int nrows, int nb, int64_t rb, int vec_base) {
+        const int Lr = 2 * nb;
+        const int Lp = slots_per_row(nb);
+        const int nrg = nmat * nrows;
+        const uint8_t *base = ring + slot * kMvStageBytes;
+        auto write = [&](int rowg, float v, bool add) {
+            const int mat = rowg >= nrows;
+            float *dst = &acc[mat * kMvMaxRows + rowg - mat * nrows];
+            if (add) atomicAdd(dst, v); else *dst = v;
+        };
+        if (Lp <= 32) {
+            int lg = 0;
+            while ((1 << lg) < Lp) ++lg;
+            const int rpc = 32 >> lg;                     // rows per chunk
+            const int chunks = (nrg + rpc - 1) / rpc;
+            const int q = lane & (Lp - 1);
+            for (int c = warp; c < chunks; c += kMvConsumerWarps) {
+                const int rowg = c * rpc + (lane >> lg);
+                float part = 0.0f;
+                if (rowg < nrg && q < Lr)
+                    part = half_block_dot(base + (int64_t)rowg * rb + (q >> 1) * kBlockBytes, q & 1,
+                                          xr, xs, xsum);
+                for (int o = Lp >> 1; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                if (rowg < nrg && q == 0) write(rowg, part, false);
+            }
+        } else if (slot_resident(Lp)) {
+            const int cpr = Lp >> 5;
+            const int q = lane_slot(Lp, warp, lane);
+            for (int rowg = warp / cpr; rowg < nrg; rowg += kMvConsumerWarps / cpr) {
+                float part = 0.0f;
+                if (q < Lr)
+                    part = half_block_dot(base + (int64_t)rowg * rb + (q >> 1) * kBlockBytes, q & 1,
+                                          xr, xs, xsum);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                if (lane == 0) write(rowg, part, true);
+            }
+        } else {
+            const int cpr = Lp >> 5;
+            for (int c = warp; c < nrg * cpr; c += kMvConsumerWarps) {
+                const int rowg = c / cpr;
+                const int q = (c - rowg * cpr) * 32 + lane;
+                float part = 0.0f;
+                if (q < Lr) {
+                    uint4 xv[16];
+                    float sc, sm[4];
+                    load_half(vec, vscale, vsum, vec_base + q, xv, sc, sm);
+                    part = half_block_dot(base + (int64_t)rowg * rb + (q >> 1) * kBlockBytes, q & 1,
+                                          xv, sc, sm);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                if (lane == 0) write(rowg, part, true);
+            }
+        }
+    };
+    // load this lane's resident half-block of the vector starting at vec_base
+    auto load_resident = [&](int nb, int vec_base) {
+        const int Lp = slots_per_row(nb);
+        if (!slot_resident(Lp)) return;
+        const int q = lane_slot(Lp, warp, lane);
+        if (q < 2 * nb) load_half(vec, vscale, vsum, vec_base + q, xr, xs, xsum);
+    };
+
+    for (int i = tid; i < 3 * kMvMaxRows; i += kMvConsumers) acc[i] = 0.0f;   // acc and yacc
+
+    // ---- phase 1 ----------------------------------------------------------
+    quantize_vector(G.nhalf1, [&](int hb) -> float4 {
+        const uint2 raw = *reinterpret_cast<const uint2 *>(a.x + hb * 128 + 4 * lane);
+        return make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                           __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
+    });
+    consumers_sync();
+    load_resident(G.nbH, 0);
+    for (int r = r0; r < r1 && ok;) {
+        const int p = r / I, i = r % I;
+        const int cnt = min(min(G.R1, r1 - r), I - i);
+        const int e = expert_of(p);
+        if (!valid(e)) {
+            for (int t = tid; t < cnt; t += kMvConsumers) a.h[(int64_t)p * I + i + t] = 0.0f;
+            r += cnt;
+            continue;
+        }
+        if (!mbar_wait(&full[slot], ph, nullptr, a.err)) { ok = false; break; }
+        run_stage(2, cnt, G.nbH, G.rbH, 0);
+        consumers_sync();
+        if (tid == 0) mbar_arrive(&empty[slot]);
+        next();
+        if (tid < cnt) {
+            const float g = acc[tid], u = acc[kMvMaxRows + tid];
+            a.h[(int64_t)p * I + i + tid] = g / (1.0f + expf(-g)) * u;
+            acc[tid] = 0.0f;
+            acc[kMvMaxRows + tid] = 0.0f;
+        }
+        consumers_sync();
+        r += cnt;
+    }
+
+    grid_barrier(a.barrier, epoch, a.err);
+
+    // ---- phase 2 ----------------------------------------------------------
+    quantize_vector(G.nhalf2, [&](int hb) -> float4 {
+        const int p = hb / (2 * G.nbI), hl = hb - p * (2 * G.nbI);
+        const int col = hl * 128 + 4 * lane;
+        // load from a valid address whatever the column, then zero past I
+        const int colc = col < I ? col : 0;
+        float4 v = __ldcg(reinterpret_cast<const float4 *>(a.h + (int64_t)p * I + colc));
+        if (col >= I) v = make_float4(0.f, 0.f, 0.f, 0.f);
+        return v;
+    });
+    consumers_sync();
+    int loaded_p = -1;
+    for (int n = n0; n < n1 && ok;) {
+        const int cnt = min(G.R2, n1 - n);
+        for (int p = 0; p < P && ok; ++p) {
+            const int e = expert_of(p);
+            if (!valid(e)) continue;
+            if (p != loaded_p) {
+                load_resident(G.nbI, p * 2 * G.nbI);
+                loaded_p = p;
+            }
+            if (!mbar_wait(&full[slot], ph, nullptr, a.err)) { ok = false; break; }
+            run_stage(1, cnt, G.nbI, G.rbI, p * 2 * G.nbI);
+            consumers_sync();
+            if (tid == 0) mbar_arrive(&empty[slot]);
+            next();
+            if (tid < cnt) {
+                const float w = moe ? a.wts[p] : 1.0f;
+                yacc[tid] += w * acc[tid];
+                acc[tid] = 0.0f;
+            }
+            consumers_sync();
+        }
+        if (tid < cnt) {
+            float *dst = a.y + n + tid;
+            *dst = a.accumulate ? *dst + yacc[tid] : yacc[tid];
+            yacc[tid] = 0.0f;
+        }
+        consumers_sync();
+        n += cnt;
+    }
 }
 
 cudaError_t launch_ffn_matvec(const MatvecArgs &a, cudaStream_t s) {
     const DeviceInfo &di = device_info();
-    const size_t smem = matvec_smem_bytes(a.T, a.H, a.I, a.k);
+    if (a.T != 1) return cudaErrorInvalidValue;
+    const size_t smem = matvec_smem_bytes(1, a.H, a.I, a.k);
     cudaError_t e = cudaFuncSetAttribute(ffn_matvec_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -267,7 +523,8 @@ cudaError_t launch_ffn_matvec(const MatvecArgs &a, cudaStream_t s) {
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ffn_matvec_kernel, kMvThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    const int grid = di.num_sms;   // one block per SM: co-resident by construction
+    int grid = di.num_sms;   // one block per SM: co-resident by construction
+    if (grid > kGridBarrierWords - 1) grid = kGridBarrierWords - 1;
     MatvecArgs args = a;
     void *params[] = {&args};
     return cudaLaunchCooperativeKernel((const void *)ffn_matvec_kernel, dim3(grid),
