@@ -222,7 +222,7 @@ zffn_status swiglu_dense(const void *x, const void *Wg, const void *Wu, const vo
     a.row_weight = nullptr;
     a.n_tiles_host = (T + 127) / 128;
     a.err = di.err_word;
-    a.T = T; a.H = H; a.I = I;
+    a.T = T; a.H = H; a.I = I; a.E = 1;
     return to_status(launch_ffn_tc(a, s));
 }
 
@@ -300,7 +300,7 @@ zffn_status swiglu_moe(const void *x, const int32_t *expert_ids, const float *ex
     a.row_weight = r.row_weight;
     a.n_tiles_host = L.max_tiles;
     a.err = di.err_word;
-    a.T = T; a.H = H; a.I = I;
+    a.T = T; a.H = H; a.I = I; a.E = E;
     return to_status(launch_ffn_tc(a, s));
 }
 

@@ -39,24 +39,46 @@ namespace tc {
 constexpr int BM = 128;                  // token rows per tile (UMMA M)
 constexpr int BK = 64;                   // K per pipeline step (128 bytes of bf16)
 constexpr int GU_ROWS = 128;             // intermediate rows per gate/up job
-constexpr int NJ = 256;                  // UMMA N of every job
+constexpr int NJ = 256;                  // UMMA N of every job (= weight rows per step)
 constexpr int IC = 256;                  // intermediate columns per work unit
-constexpr int NA = 3;                    // x stages
-constexpr int NB = 3;                    // weight stages
+constexpr int NA = 2;                    // x stages (TMA)
+constexpr int NB = 2;                    // unpacked-weight stages (bf16, UMMA B operand)
+constexpr int NR = 4;                    // packed-weight stages (TMA)
 constexpr int A_BYTES = BM * BK * 2;     // 16 KB
 constexpr int B_BYTES = NJ * BK * 2;     // 32 KB
+constexpr int R_HDR = NJ * 16;           // block headers of the step's 256 rows: 4 KB
+constexpr int R_QS = NJ * 32;            // the step's 32 code bytes of each row: 8 KB
+constexpr int R_BYTES = R_HDR + R_QS;    // 12 KB
 constexpr int HT_BYTES = BM * BK * 2;    // one 64-column slice of h: 16 KB
 constexpr int N_HT = IC / BK;            // 4
 constexpr int OFF_H = 0;
 constexpr int OFF_A = OFF_H + N_HT * HT_BYTES;
 constexpr int OFF_B = OFF_A + NA * A_BYTES;
-constexpr int OFF_BAR = OFF_B + NB * B_BYTES;
-constexpr int N_BARS = 2 * NA + 2 * NB + 4 + 3;
+constexpr int OFF_R = OFF_B + NB * B_BYTES;
+// y staging for the TMA reductions: per epilogue warp two buffers of
+// [32 rows x 16 fp32] with the 64-byte swizzle (chunk j of row r at j ^ (r/2 % 4)).
+constexpr int Y_COLS = 16;
+constexpr int Y_BUF = 32 * Y_COLS * 4;   // 2 KB
+constexpr int OFF_Y = OFF_R + NR * R_BYTES;
+constexpr int OFF_BAR = OFF_Y + 4 * 2 * Y_BUF;
+constexpr int N_BARS = 2 * NA + 2 * NB + 2 * NR + 4 + 3;
 constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget of one block");
-constexpr int THREADS = 320;
+constexpr int UNPACK_WARPS = 8;          // one weight row per thread
+constexpr int THREADS = (2 + UNPACK_WARPS + 4) * 32;
+constexpr int EPI_WARP0 = 2 + UNPACK_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, NJ);
+
+// Tensor maps: x tiles, and the packed weights viewed as byte matrices
+// [rows][row bytes] with two box shapes each: the 16-byte block headers and
+// the 32 code bytes of one 64-wide K step.
+struct Maps {
+    CUtensorMap x;
+    CUtensorMap y;                          // fp32 [T][H], boxes of [32 rows x 16 cols]
+    CUtensorMap g_hdr, g_qs, u_hdr, u_qs;   // boxes of 128 rows
+    CUtensorMap d_hdr, d_qs;                // boxes of 256 rows
+};
 
 struct Params {
     const uint8_t *Wg, *Wu, *Wd;
@@ -89,22 +111,17 @@ __device__ __forceinline__ Tile get_tile(const Params &p, int t) {
     return r;
 }
 
-// Byte offset of 16-byte chunk c of row r in a [rows x 64] bf16 tile laid out
-// K-major with the 128-byte swizzle (groups of 8 rows, 1024 bytes apart).
+// Byte offset of row r in a [rows x 64] bf16 tile laid out K-major with the
+// 128-byte swizzle (groups of 8 rows, 1024 bytes apart); 16-byte chunk c of
+// the row sits at chunk position c ^ (r % 8).
 __device__ __forceinline__ uint32_t sw128_row(int r) {
     return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
 }
 
-// Raw bytes of one weight row for one K step: block header + 32 code bytes.
+// Packed bytes of one weight row for one K step: block header + 32 code bytes.
 struct RawRow {
     uint4 hd, q0, q1;
 };
-
-__device__ __forceinline__ void load_raw(RawRow &r, const uint8_t *blk, int g) {
-    r.hd = __ldg(reinterpret_cast<const uint4 *>(blk));
-    r.q0 = __ldg(reinterpret_cast<const uint4 *>(blk + 16 + 32 * g));
-    r.q1 = __ldg(reinterpret_cast<const uint4 *>(blk + 32 + 32 * g));
-}
 
 // Unpack 64 weights (K step g of a block) into one swizzled bf16 row.
 // A code q is turned into the float 1 + q/128 (low nibbles, placed at bits
@@ -153,9 +170,18 @@ __device__ __forceinline__ void unpack_row_to_smem(const RawRow &r, int g, uint3
     }
 }
 
-__device__ __forceinline__ void zero_row_smem(uint32_t row_addr) {
+__device__ __forceinline__ void zero_row_smem(uint32_t row_addr, int row) {
 #pragma unroll
-    for (int c = 0; c < 8; ++c) st_shared_v4(row_addr + (c << 4), 0u, 0u, 0u, 0u);
+    for (int c = 0; c < 8; ++c) st_shared_v4(row_addr + (((uint32_t)(c ^ (row & 7))) << 4), 0u, 0u, 0u, 0u);
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
 }
 
 // Work-unit geometry shared by every role.
@@ -182,16 +208,48 @@ __device__ __forceinline__ Unit make_unit(const Params &p, int u, int n_tiles) {
     return un;
 }
 
+// Where step st of a unit reads its packed weights: the block column, the
+// 64-wide group inside the block, and the first row of each tensor map.
+struct StepSrc {
+    bool gu;        // gate/up step (x tile too) or down step
+    int ks;         // K step inside the job
+    int s;          // gate/up job or down job index
+    int xcol;       // byte column of the block header
+    int g;          // 64-wide group inside the block (code bytes 32g..32g+31)
+};
+
+__device__ __forceinline__ StepSrc step_src(const Unit &un, int st) {
+    StepSrc r;
+    const int ngu = un.n_gu * un.ks_gu;
+    if (st < ngu) {
+        r.gu = true;
+        r.s = st / un.ks_gu;
+        r.ks = st - r.s * un.ks_gu;
+        r.xcol = (r.ks >> 2) * kBlockBytes;
+        r.g = r.ks & 3;
+    } else {
+        r.gu = false;
+        const int st2 = st - ngu;
+        r.s = st2 / un.ks_y;
+        r.ks = st2 - r.s * un.ks_y;
+        const int col = un.i0 + r.ks * BK;
+        r.xcol = (col >> 8) * kBlockBytes;
+        r.g = (col & 255) >> 6;
+    }
+    return r;
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
-    ffn_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const Params p) {
+    ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled tiles
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
     uint64_t *a_full = bars, *a_empty = bars + NA;
-    uint64_t *b_full = bars + 2 * NA, *b_empty = bars + 2 * NA + NB;
-    uint64_t *t_full = bars + 2 * NA + 2 * NB, *t_empty = t_full + 2;
+    uint64_t *b_full = bars + 2 * NA, *b_empty = b_full + NB;
+    uint64_t *r_full = b_empty + NB, *r_empty = r_full + NR;
+    uint64_t *t_full = r_empty + NR, *t_empty = t_full + 2;
     uint64_t *h_full = t_empty + 2, *h_empty = h_full + 1, *drain = h_full + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + N_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -200,6 +258,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t s_h = smem_u32(smem + OFF_H);
     const uint32_t s_a = smem_u32(smem + OFF_A);
     const uint32_t s_b = smem_u32(smem + OFF_B);
+    const uint32_t s_r = smem_u32(smem + OFF_R);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NA; ++i) {
@@ -207,8 +266,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&a_empty[i], 1);
         }
         for (int i = 0; i < NB; ++i) {
-            mbar_init(&b_full[i], 128);
+            mbar_init(&b_full[i], UNPACK_WARPS);
             mbar_init(&b_empty[i], 1);
+        }
+        for (int i = 0; i < NR; ++i) {
+            mbar_init(&r_full[i], 1);
+            mbar_init(&r_empty[i], UNPACK_WARPS);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&t_full[i], 1);
@@ -219,7 +282,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
-        prefetch_tensormap(&tmap_x);
+        prefetch_tensormap(&maps.x);
+        prefetch_tensormap(&maps.y);
+        prefetch_tensormap(&maps.g_hdr);
+        prefetch_tensormap(&maps.g_qs);
+        prefetch_tensormap(&maps.u_hdr);
+        prefetch_tensormap(&maps.u_qs);
+        prefetch_tensormap(&maps.d_hdr);
+        prefetch_tensormap(&maps.d_qs);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, TMEM_COLS);
@@ -237,31 +307,56 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int64_t rbI = q4k_row_bytes(p.I);
 
     if (warp == 0) {
-        // ---------------- TMA producer: x tiles ----------------
+        // ------------- TMA producer: x tiles and packed weights -------------
         if (lane == 0) {
-            uint32_t ai = 0, aph = 0;
-            uint32_t issued = 0;
+            uint32_t ai = 0, aph = 0, ri = 0, rph = 0;
+            uint32_t a_issued = 0, r_issued = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
                 const Unit un = make_unit(p, u, n_tiles);
-                for (int s = 0; s < un.n_gu && ok; ++s) {
-                    for (int ks = 0; ks < un.ks_gu; ++ks) {
+                const int e = un.tile.expert;
+                const int steps = un.n_gu * un.ks_gu + un.n_y * un.ks_y;
+                for (int st = 0; st < steps; ++st) {
+                    const StepSrc src = step_src(un, st);
+                    if (src.gu) {
                         if (!mbar_wait(&a_empty[ai], aph ^ 1, abort_flag, p.err)) { ok = false; break; }
                         mbar_arrive_expect_tx(&a_full[ai], A_BYTES);
-                        tma_load_2d(smem + OFF_A + ai * A_BYTES, &tmap_x, &a_full[ai], ks * BK,
+                        tma_load_2d(smem + OFF_A + ai * A_BYTES, &maps.x, &a_full[ai], src.ks * BK,
                                     un.tile.row_start);
-                        ++issued;
+                        ++a_issued;
                         if (++ai == NA) { ai = 0; aph ^= 1; }
                     }
+                    if (!mbar_wait(&r_empty[ri], rph ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&r_full[ri], R_BYTES);
+                    uint8_t *rs = smem + OFF_R + ri * R_BYTES;
+                    const int qcol = src.xcol + 16 + 32 * src.g;
+                    if (src.gu) {
+                        const int row = e * p.I + un.i0 + src.s * GU_ROWS;
+                        tma_load_2d(rs, &maps.g_hdr, &r_full[ri], src.xcol, row);
+                        tma_load_2d(rs + 128 * 16, &maps.u_hdr, &r_full[ri], src.xcol, row);
+                        tma_load_2d(rs + R_HDR, &maps.g_qs, &r_full[ri], qcol, row);
+                        tma_load_2d(rs + R_HDR + 128 * 32, &maps.u_qs, &r_full[ri], qcol, row);
+                    } else {
+                        const int row = e * p.H + src.s * NJ;
+                        tma_load_2d(rs, &maps.d_hdr, &r_full[ri], src.xcol, row);
+                        tma_load_2d(rs + R_HDR, &maps.d_qs, &r_full[ri], qcol, row);
+                    }
+                    ++r_issued;
+                    if (++ri == NR) { ri = 0; rph ^= 1; }
                 }
             }
             // Before the block may exit, every load issued here must have
-            // landed: wait (bounded) for the full barrier of the last NA
-            // stages issued (a phase that completed long ago passes at once).
-            for (uint32_t i = 0; i < NA && i < issued; ++i) {
+            // landed: wait (bounded) for the full barrier of the last stages
+            // issued (a phase that completed long ago passes at once).
+            for (uint32_t i = 0; i < NA && i < a_issued; ++i) {
                 if (ai == 0) { ai = NA; aph ^= 1; }
                 --ai;
                 mbar_wait(&a_full[ai], aph, nullptr, p.err, kWaitBudgetCycles / 8);
+            }
+            for (uint32_t i = 0; i < NR && i < r_issued; ++i) {
+                if (ri == 0) { ri = NR; rph ^= 1; }
+                --ri;
+                mbar_wait(&r_full[ri], rph, nullptr, p.err, kWaitBudgetCycles / 8);
             }
         }
     } else if (warp == 1) {
@@ -320,76 +415,58 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_commit(drain);
             mbar_wait(drain, 0, nullptr, p.err, kWaitBudgetCycles / 8);
         }
-    } else if (warp < 6) {
-        // ---------------- weight producers (128 threads) ----------------
-        const int tid = threadIdx.x - 64;           // 0..127: rows tid and tid + 128
-        uint32_t bi = 0, bph = 0;
+    } else if (warp < EPI_WARP0) {
+        // ------------- weight unpackers (256 threads, one row each) -------------
+        const int row = threadIdx.x - 64;             // 0..255
+        uint32_t bi = 0, bph = 0, ri = 0, rph = 0;
         bool ok = true;
+        // a quarter-warp's 16-byte reads of the 32-byte code rows are bank
+        // conflict free when rows 4..7 of each group of 8 read their halves
+        // in the other order
+        const int qfirst = (row >> 2) & 1;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
             const Unit un = make_unit(p, u, n_tiles);
             const int e = un.tile.expert;
-            const int steps = un.n_gu * un.ks_gu + un.n_y * un.ks_y;
-            // source of row rr (0..255) at step st of this unit; nullptr = zero row
-            auto src = [&](int st, int rr, int &g) -> const uint8_t * {
-                if (st < un.n_gu * un.ks_gu) {
-                    const int s = st / un.ks_gu, ks = st % un.ks_gu;
-                    const int i = un.i0 + s * GU_ROWS + (rr & 127);
-                    g = ks & 3;
-                    if (i >= p.I) return nullptr;
-                    const uint8_t *w = rr < 128 ? p.Wg : p.Wu;
-                    return w + ((int64_t)e * p.I + i) * rbH + (int64_t)(ks >> 2) * kBlockBytes;
+            // L2 prefetch of this unit's weight rows (one row pair / 16 down rows per thread)
+            for (int s = 0; s < un.n_gu; ++s) {
+                const int ii = un.i0 + s * GU_ROWS + (row & 127);
+                if (ii < p.I) {
+                    const uint8_t *w = row < 128 ? p.Wg : p.Wu;
+                    prefetch_l2_bulk(w + ((int64_t)e * p.I + ii) * rbH, (uint32_t)rbH);
                 }
-                const int st2 = st - un.n_gu * un.ks_gu;
-                const int n = st2 / un.ks_y, ks = st2 % un.ks_y;
-                const int col = un.i0 + ks * BK;
-                g = (col & 255) >> 6;
-                return p.Wd + ((int64_t)e * p.H + n * NJ + rr) * rbI + (int64_t)(col >> 8) * kBlockBytes;
-            };
-            // L2 prefetch of this unit's weight rows for this thread
+            }
             {
-                for (int s = 0; s < un.n_gu; ++s) {
-                    const int ii = un.i0 + s * GU_ROWS + tid;
-                    if (ii < p.I) {
-                        prefetch_l2_bulk(p.Wg + ((int64_t)e * p.I + ii) * rbH, (uint32_t)rbH);
-                        prefetch_l2_bulk(p.Wu + ((int64_t)e * p.I + ii) * rbH, (uint32_t)rbH);
-                    }
-                }
                 const int b0 = un.i0 >> 8, b1 = (un.i0 + un.ic + 255) >> 8;
                 const uint32_t bytes = (uint32_t)((b1 - b0) * kBlockBytes);
-                for (int n = 0; n < un.n_y; ++n)
-                    for (int h2 = 0; h2 < 2; ++h2)
-                        prefetch_l2_bulk(p.Wd + ((int64_t)e * p.H + n * NJ + tid + 128 * h2) * rbI +
-                                             (int64_t)b0 * kBlockBytes,
-                                         bytes);
+                for (int n = row; n < p.H; n += 256)
+                    prefetch_l2_bulk(p.Wd + ((int64_t)e * p.H + n) * rbI + (int64_t)b0 * kBlockBytes,
+                                     bytes);
             }
-            RawRow cur0, cur1;
-            const uint8_t *p0, *p1;
-            int g0 = 0, g1 = 0;
-            p0 = src(0, tid, g0);
-            p1 = src(0, tid + 128, g1);
-            if (p0) load_raw(cur0, p0, g0);
-            if (p1) load_raw(cur1, p1, g1);
+            const int steps = un.n_gu * un.ks_gu + un.n_y * un.ks_y;
             for (int st = 0; st < steps; ++st) {
-                // issue the next step's loads before waiting for a free stage
-                RawRow nx0, nx1;
-                const uint8_t *q0 = nullptr, *q1 = nullptr;
-                int ng0 = 0, ng1 = 0;
-                if (st + 1 < steps) {
-                    q0 = src(st + 1, tid, ng0);
-                    q1 = src(st + 1, tid + 128, ng1);
-                    if (q0) load_raw(nx0, q0, ng0);
-                    if (q1) load_raw(nx1, q1, ng1);
+                const StepSrc src = step_src(un, st);
+                const bool zero = src.gu && (un.i0 + src.s * GU_ROWS + (row & 127) >= p.I);
+                if (!mbar_wait(&r_full[ri], rph, abort_flag, p.err)) { ok = false; break; }
+                RawRow raw;
+                if (!zero) {
+                    const uint32_t rs = s_r + ri * R_BYTES;
+                    raw.hd = ld_shared_v4(rs + row * 16);
+                    const uint32_t qa = rs + R_HDR + row * 32;
+                    const uint4 first = ld_shared_v4(qa + 16 * qfirst);
+                    const uint4 second = ld_shared_v4(qa + 16 * (qfirst ^ 1));
+                    raw.q0 = qfirst ? second : first;
+                    raw.q1 = qfirst ? first : second;
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&r_empty[ri]);
+                if (++ri == NR) { ri = 0; rph ^= 1; }
                 if (!mbar_wait(&b_empty[bi], bph ^ 1, abort_flag, p.err)) { ok = false; break; }
-                const uint32_t base = s_b + bi * B_BYTES;
-                const uint32_t r0 = base + sw128_row(tid);
-                const uint32_t r1 = base + sw128_row(tid + 128);
-                if (p0) unpack_row_to_smem(cur0, g0, r0, tid); else zero_row_smem(r0);
-                if (p1) unpack_row_to_smem(cur1, g1, r1, tid + 128); else zero_row_smem(r1);
+                const uint32_t rb = s_b + bi * B_BYTES + sw128_row(row);
+                if (zero) zero_row_smem(rb, row); else unpack_row_to_smem(raw, src.g, rb, row);
                 fence_proxy_async_smem();
-                mbar_arrive(&b_full[bi]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&b_full[bi]);
                 if (++bi == NB) { bi = 0; bph ^= 1; }
-                cur0 = nx0; cur1 = nx1; p0 = q0; p1 = q1; g0 = ng0; g1 = ng1;
             }
         }
     } else {
@@ -397,6 +474,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int q = warp & 3;                      // TMEM lane quadrant of this warp
         const int row = q * 32 + lane;               // token row within the tile
         const uint32_t lane_bits = (uint32_t)(q * 32) << 16;
+        const uint32_t s_y = smem_u32(smem + OFF_Y), s_base = smem_u32(smem);
+        uint32_t y_use = 0;
         uint32_t jc = 0, uc = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
@@ -447,11 +526,50 @@ __global__ void __launch_bounds__(THREADS, 1)
                 wgt = p.row_weight ? p.row_weight[xr] : 1.0f;
             }
             float *yrow = p.y + (int64_t)token * p.H;
+            // dense tiles: y slices go through swizzled shared memory and one TMA
+            // reduction per warp and slice; routed tiles scatter rows, so each
+            // thread adds its own row with vector reductions
+            const bool tma_y = p.tiles == nullptr;
+            const int warp_row0 = un.tile.row_start + q * 32;
+            const bool warp_live = warp_row0 < p.T;
             for (int n = 0; n < un.n_y && ok; ++n, ++jc) {
                 const uint32_t slot = jc & 1, tph = (jc >> 1) & 1;
                 if (!mbar_wait(&t_full[slot], tph, abort_flag, p.err)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t t_addr = tmem_base + lane_bits + slot * NJ;
+                if (tma_y) {
+#pragma unroll 1
+                    for (int c = 0; c < NJ; c += 32) {
+                        uint32_t yr[32];
+                        tmem_ld_32x32b_x32(t_addr + c, yr);
+                        tmem_ld_wait(yr);
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            // buffer use: y_use alternates between the warp's two buffers
+                            if (lane == 0) bulk_wait_group_read<1>();
+                            __syncwarp();
+                            const uint32_t buf = s_y + (uint32_t)((q * 2 + (y_use & 1)) * Y_BUF);
+                            const uint32_t rowa = buf + lane * 64;
+                            const int sw = (lane >> 1) & 3;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                st_shared_v4(rowa + (((uint32_t)(j ^ sw)) << 4), yr[16 * half + 4 * j],
+                                             yr[16 * half + 4 * j + 1], yr[16 * half + 4 * j + 2],
+                                             yr[16 * half + 4 * j + 3]);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0 && warp_live) {
+                                tma_reduce_add_2d(&maps.y, smem + (buf - s_base), n * NJ + c + 16 * half,
+                                                  warp_row0);
+                                bulk_commit_group();
+                            }
+                            ++y_use;
+                        }
+                    }
+                    tc_fence_before();
+                    mbar_arrive(&t_empty[slot]);
+                    continue;
+                }
 #pragma unroll 1
                 for (int c = 0; c < NJ; c += 32) {
                     uint32_t yr[32];
@@ -475,10 +593,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mbar_arrive(&t_empty[slot]);
             }
         }
+        // the reductions must have finished reading shared memory (and be
+        // complete) before the block exits
+        if (lane == 0) bulk_wait_group_all();
+        __syncwarp();
     }
 
     // Every role is done: all MMAs were consumed by the epilogue (or the
-    // launch is aborting, in which case let in-flight MMAs finish first).
+    // launch is aborting, in which case the issuer waited for its MMAs).
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -503,20 +625,54 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     return fn;
 }
 
+static bool encode_bytes_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *m,
+                             const void *base, int64_t row_bytes, int64_t rows, int box_bytes,
+                             int box_rows) {
+    const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 cudaError_t launch_ffn_tc(const TcArgs &a, cudaStream_t s) {
     const DeviceInfo &di = device_info();
     auto encode = get_encode_fn();
     if (!encode) return cudaErrorNotSupported;
-    CUtensorMap tmap;
-    const cuuint64_t dims[2] = {(cuuint64_t)a.H, (cuuint64_t)a.x_rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)a.H * 2};
-    const cuuint32_t box[2] = {tc::BK, tc::BM};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.x), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    tc::Maps maps;
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)a.H, (cuuint64_t)a.x_rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)a.H * 2};
+        const cuuint32_t box[2] = {tc::BK, tc::BM};
+        const cuuint32_t estr[2] = {1, 1};
+        CUresult r = encode(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.x),
+                            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)a.H, (cuuint64_t)a.T};
+        const cuuint64_t strides[1] = {(cuuint64_t)a.H * 4};
+        const cuuint32_t box[2] = {tc::Y_COLS, 32};
+        const cuuint32_t estr[2] = {1, 1};
+        CUresult r = encode(&maps.y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.y, dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    const int64_t rbH = q4k_row_bytes(a.H), rbI = q4k_row_bytes(a.I);
+    const int64_t gu_rows = (int64_t)a.E * a.I, d_rows = (int64_t)a.E * a.H;
+    if (!encode_bytes_map(encode, &maps.g_hdr, a.Wg, rbH, gu_rows, 16, tc::GU_ROWS) ||
+        !encode_bytes_map(encode, &maps.g_qs, a.Wg, rbH, gu_rows, 32, tc::GU_ROWS) ||
+        !encode_bytes_map(encode, &maps.u_hdr, a.Wu, rbH, gu_rows, 16, tc::GU_ROWS) ||
+        !encode_bytes_map(encode, &maps.u_qs, a.Wu, rbH, gu_rows, 32, tc::GU_ROWS) ||
+        !encode_bytes_map(encode, &maps.d_hdr, a.Wd, rbI, d_rows, 16, tc::NJ) ||
+        !encode_bytes_map(encode, &maps.d_qs, a.Wd, rbI, d_rows, 32, tc::NJ))
+        return cudaErrorInvalidValue;
     static int attr_set_device = -1;
     if (attr_set_device != di.device) {
         cudaError_t e = cudaFuncSetAttribute(tc::ffn_tc_kernel,
@@ -544,7 +700,7 @@ cudaError_t launch_ffn_tc(const TcArgs &a, cudaStream_t s) {
     int grid = di.num_sms;
     if (units < grid) grid = (int)units;
     if (grid < 1) return cudaSuccess;
-    tc::ffn_tc_kernel<<<grid, tc::THREADS, tc::SMEM_BYTES, s>>>(tmap, p);
+    tc::ffn_tc_kernel<<<grid, tc::THREADS, tc::SMEM_BYTES, s>>>(maps, p);
     return cudaGetLastError();
 }
 

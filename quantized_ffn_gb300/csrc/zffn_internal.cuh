@@ -124,6 +124,29 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
+// 2-D TMA tile reduction shared -> global: global += tile (fp32 add), tracked
+// by the issuing thread's bulk-async group.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *map, const void *smem_src,
+                                                  int c0, int c1) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group"
+        " [%0, {%2, %3}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(smem_src)), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until all of this thread's bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_group_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -289,6 +312,7 @@ struct TcArgs {
     int n_tiles_host;            // dense: exact count; MoE: upper bound
     int *err;
     int T, H, I;
+    int E;                       // experts stacked in Wg/Wu/Wd (dense: 1)
 };
 cudaError_t launch_ffn_tc(const TcArgs &a, cudaStream_t s);
 
