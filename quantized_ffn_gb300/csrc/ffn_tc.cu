@@ -36,48 +36,59 @@
 namespace zffn {
 namespace tc {
 
-constexpr int BM = 128;                  // token rows per tile (UMMA M)
+constexpr int BM = 128;                  // token rows per CTA per tile (UMMA M per CTA)
 constexpr int BK = 64;                   // K per pipeline step (128 bytes of bf16)
 constexpr int GU_ROWS = 128;             // intermediate rows per gate/up job
-constexpr int NJ = 256;                  // UMMA N of every job (= weight rows per step)
+constexpr int NJ = 256;                  // UMMA N of every job
 constexpr int IC = 256;                  // intermediate columns per work unit
-constexpr int NA = 2;                    // x stages (TMA)
-constexpr int NB = 2;                    // unpacked-weight stages (bf16, UMMA B operand)
-constexpr int NR = 4;                    // packed-weight stages (TMA)
-constexpr int A_BYTES = BM * BK * 2;     // 16 KB
-constexpr int B_BYTES = NJ * BK * 2;     // 32 KB
-constexpr int R_HDR = NJ * 16;           // block headers of the step's 256 rows: 4 KB
-constexpr int R_QS = NJ * 32;            // the step's 32 code bytes of each row: 8 KB
-constexpr int R_BYTES = R_HDR + R_QS;    // 12 KB
+constexpr int A_BYTES = BM * BK * 2;     // 16 KB x tile per CTA
 constexpr int HT_BYTES = BM * BK * 2;    // one 64-column slice of h: 16 KB
 constexpr int N_HT = IC / BK;            // 4
-constexpr int OFF_H = 0;
-constexpr int OFF_A = OFF_H + N_HT * HT_BYTES;
-constexpr int OFF_B = OFF_A + NA * A_BYTES;
-constexpr int OFF_R = OFF_B + NB * B_BYTES;
+constexpr int UNPACK_WARPS = 8;
+constexpr int THREADS = (2 + UNPACK_WARPS + 4) * 32;
+constexpr int EPI_WARP0 = 2 + UNPACK_WARPS;
+constexpr uint32_t TMEM_COLS = 512;
 // y staging for the TMA reductions: per epilogue warp two buffers of
 // [32 rows x 16 fp32] with the 64-byte swizzle (chunk j of row r at j ^ (r/2 % 4)).
 constexpr int Y_COLS = 16;
 constexpr int Y_BUF = 32 * Y_COLS * 4;   // 2 KB
-constexpr int OFF_Y = OFF_R + NR * R_BYTES;
-constexpr int OFF_BAR = OFF_Y + 4 * 2 * Y_BUF;
-constexpr int N_BARS = 2 * NA + 2 * NB + 2 * NR + 4 + 3;
-constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + alignment slack
-static_assert(SMEM_BYTES <= 232448, "shared memory budget of one block");
-constexpr int UNPACK_WARPS = 8;          // one weight row per thread
-constexpr int THREADS = (2 + UNPACK_WARPS + 4) * 32;
-constexpr int EPI_WARP0 = 2 + UNPACK_WARPS;
-constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, NJ);
 
-// Tensor maps: x tiles, and the packed weights viewed as byte matrices
-// [rows][row bytes] with two box shapes each: the 16-byte block headers and
-// the 32 code bytes of one 64-wide K step.
+// Geometry of one kernel variant.  PAIR: a cluster of two CTAs shares each
+// 256-token tile; one UMMA of M = 256 covers both CTAs' rows, and the N = 256
+// weight rows of every step are split between the CTAs (each unpacks 128).
+template <bool PAIR>
+struct Cfg {
+    static constexpr int ROWS_B = PAIR ? 128 : 256;      // weight rows unpacked per CTA per step
+    static constexpr int TPR = 256 / ROWS_B;              // unpack threads per weight row
+    static constexpr int TILE = PAIR ? 256 : 128;         // tokens per work-unit tile
+    static constexpr int NA = PAIR ? 3 : 2;               // x stages
+    static constexpr int NB = PAIR ? 3 : 2;               // unpacked-weight stages
+    static constexpr int NR = PAIR ? 6 : 4;               // packed-weight stages
+    static constexpr int B_BYTES = ROWS_B * BK * 2;
+    static constexpr int R_HDR = ROWS_B * 16;
+    static constexpr int R_BYTES = ROWS_B * 48;
+    static constexpr int OFF_H = 0;
+    static constexpr int OFF_A = OFF_H + N_HT * HT_BYTES;
+    static constexpr int OFF_B = OFF_A + NA * A_BYTES;
+    static constexpr int OFF_R = OFF_B + NB * B_BYTES;
+    static constexpr int OFF_Y = ((OFF_R + NR * R_BYTES) + 1023) & ~1023;
+    static constexpr int OFF_BAR = OFF_Y + 4 * 2 * Y_BUF;
+    static constexpr int N_BARS = 2 * NA + 2 * NB + 2 * NR + 4 + 3;
+    static constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + alignment slack
+    static constexpr int EPI_ARRIVALS = PAIR ? 8 : 4;     // epilogue warps arriving per job
+    static constexpr int B_ARRIVALS = PAIR ? 2 * UNPACK_WARPS : UNPACK_WARPS;
+    static constexpr uint32_t IDESC = idesc_bf16_f32(PAIR ? 256 : 128, NJ);
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget of one block");
+};
+
+// Tensor maps: x tiles, y tiles, and the packed weights viewed as byte
+// matrices [rows][row bytes] with two box shapes each: the 16-byte block
+// headers and the 32 code bytes of one 64-wide K step.
 struct Maps {
     CUtensorMap x;
     CUtensorMap y;                          // fp32 [T][H], boxes of [32 rows x 16 cols]
     CUtensorMap g_hdr, g_qs, u_hdr, u_qs;   // boxes of 128 rows
-    CUtensorMap d_hdr, d_qs;                // boxes of 256 rows
+    CUtensorMap d_hdr, d_qs;                // boxes of ROWS_B rows
 };
 
 struct Params {
@@ -96,21 +107,6 @@ struct Tile {
     int row_start, row_count, expert;
 };
 
-__device__ __forceinline__ Tile get_tile(const Params &p, int t) {
-    Tile r;
-    if (p.tiles) {
-        const int4 v = p.tiles[t];
-        r.row_start = v.x;
-        r.row_count = v.y;
-        r.expert = v.z;
-    } else {
-        r.row_start = t * BM;
-        r.row_count = min(BM, p.T - t * BM);
-        r.expert = 0;
-    }
-    return r;
-}
-
 // Byte offset of row r in a [rows x 64] bf16 tile laid out K-major with the
 // 128-byte swizzle (groups of 8 rows, 1024 bytes apart); 16-byte chunk c of
 // the row sits at chunk position c ^ (r % 8).
@@ -118,40 +114,35 @@ __device__ __forceinline__ uint32_t sw128_row(int r) {
     return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
 }
 
-// Packed bytes of one weight row for one K step: block header + 32 code bytes.
-struct RawRow {
-    uint4 hd, q0, q1;
-};
-
-// Unpack 64 weights (K step g of a block) into one swizzled bf16 row.
-// A code q is turned into the float 1 + q/128 (low nibbles, placed at bits
-// 16..19) or 1 + q/2048 (high nibbles, bits 12..15) by OR-ing it into the
-// bits of 1.0f; then d*sc*q - dmin*m = (S*d*sc)*f - (S*d*sc + dmin*m) with
-// S = 128 or 2048, one fused multiply-add per weight.  The constant is
-// rounded once, an error below 2^-13 of one quantisation step, far under the
-// bf16 rounding of the result.
-__device__ __forceinline__ void unpack_row_to_smem(const RawRow &r, int g, uint32_t row_addr,
-                                                   int row) {
-    const float d = half_bits_to_float(r.hd.x), dmin = half_bits_to_float(r.hd.x >> 16);
+// Unpack 8 code words (4 bytes each, words wbeg..wbeg+nw-1 of the step's 32
+// code bytes) of one weight row into its swizzled bf16 row.  Word i holds
+// code bytes 4i..4i+3: low nibbles are weights 4i..4i+3 of the step, high
+// nibbles weights 32+4i..32+4i+3.  A code q becomes the float 1 + q/128
+// (low nibbles, at bits 16..19) or 1 + q/2048 (high nibbles, bits 12..15) by
+// OR-ing it into the bits of 1.0f; then d*sc*q - dmin*m = (S*d*sc)*f -
+// (S*d*sc + dmin*m) with S = 128 or 2048, one fused multiply-add per weight.
+// The constant is rounded once, an error below 2^-13 of one quantisation
+// step, far under the bf16 rounding of the result.
+template <int NW>
+__device__ __forceinline__ void unpack_words_to_smem(uint4 hd, const uint32_t (&w)[NW], int wbeg,
+                                                     int g, uint32_t row_addr, int row) {
+    const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
     int sc0, m0, sc1, m1;
-    q4k_scale_min(r.hd.y, r.hd.z, r.hd.w, 2 * g, sc0, m0);
-    q4k_scale_min(r.hd.y, r.hd.z, r.hd.w, 2 * g + 1, sc1, m1);
+    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g, sc0, m0);
+    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g + 1, sc1, m1);
     const float a0 = 128.0f * (d * (float)sc0);
     const float c0 = -(a0 + dmin * (float)m0);
     const float a1 = 2048.0f * (d * (float)sc1);
     const float c1 = -(a1 + dmin * (float)m1);
-    const uint32_t w[8] = {r.q0.x, r.q0.y, r.q0.z, r.q0.w, r.q1.x, r.q1.y, r.q1.z, r.q1.w};
     constexpr uint32_t ONE = 0x3F800000u, MLO = 0x000F0000u, MHI = 0x0000F000u;
-    uint32_t lo[16], hi[16];
+    uint32_t lo[2 * NW], hi[2 * NW];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < NW; ++i) {
         const uint32_t x = w[i], xl8 = x << 8, xr8 = x >> 8, xl16 = x << 16, xr16 = x >> 16;
-        // low nibbles of bytes 0..3 -> weights 4i..4i+3 of the step's first 32
         const float l0 = fmaf(a0, __uint_as_float((xl16 & MLO) | ONE), c0);
         const float l1 = fmaf(a0, __uint_as_float((xl8 & MLO) | ONE), c0);
         const float l2 = fmaf(a0, __uint_as_float((x & MLO) | ONE), c0);
         const float l3 = fmaf(a0, __uint_as_float((xr8 & MLO) | ONE), c0);
-        // high nibbles -> weights 32+4i..32+4i+3
         const float h0 = fmaf(a1, __uint_as_float((xl8 & MHI) | ONE), c1);
         const float h1 = fmaf(a1, __uint_as_float((x & MHI) | ONE), c1);
         const float h2 = fmaf(a1, __uint_as_float((xr8 & MHI) | ONE), c1);
@@ -161,18 +152,15 @@ __device__ __forceinline__ void unpack_row_to_smem(const RawRow &r, int g, uint3
         hi[2 * i] = pack_bf16x2(h0, h1);
         hi[2 * i + 1] = pack_bf16x2(h2, h3);
     }
+    // 16-byte chunk c holds weights 8c..8c+7; words wbeg.. cover chunks wbeg/2 ..
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        st_shared_v4(row_addr + (((uint32_t)(c ^ (row & 7))) << 4), lo[4 * c], lo[4 * c + 1],
-                     lo[4 * c + 2], lo[4 * c + 3]);
-        st_shared_v4(row_addr + (((uint32_t)((c + 4) ^ (row & 7))) << 4), hi[4 * c],
-                     hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+    for (int cc = 0; cc < NW / 2; ++cc) {
+        const int c = wbeg / 2 + cc;
+        st_shared_v4(row_addr + (((uint32_t)(c ^ (row & 7))) << 4), lo[4 * cc], lo[4 * cc + 1],
+                     lo[4 * cc + 2], lo[4 * cc + 3]);
+        st_shared_v4(row_addr + (((uint32_t)((c + 4) ^ (row & 7))) << 4), hi[4 * cc],
+                     hi[4 * cc + 1], hi[4 * cc + 2], hi[4 * cc + 3]);
     }
-}
-
-__device__ __forceinline__ void zero_row_smem(uint32_t row_addr, int row) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) st_shared_v4(row_addr + (((uint32_t)(c ^ (row & 7))) << 4), 0u, 0u, 0u, 0u);
 }
 
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
@@ -186,7 +174,7 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
 
 // Work-unit geometry shared by every role.
 struct Unit {
-    Tile tile;
+    Tile tile;    // the CTA's own token rows
     int i0;       // first intermediate column of the chunk
     int ic;       // columns in this chunk (multiple of 64)
     int n_gu;     // gate/up jobs
@@ -195,10 +183,21 @@ struct Unit {
     int n_y;      // down jobs
 };
 
-__device__ __forceinline__ Unit make_unit(const Params &p, int u, int n_tiles) {
+template <bool PAIR>
+__device__ __forceinline__ Unit make_unit(const Params &p, int u, int n_tiles, uint32_t rank) {
     Unit un;
     const int chunk = u / n_tiles;
-    un.tile = get_tile(p, u % n_tiles);
+    const int t = u % n_tiles;
+    if (p.tiles) {
+        const int4 v = p.tiles[t];
+        un.tile.row_start = v.x;
+        un.tile.row_count = v.y;
+        un.tile.expert = v.z;
+    } else {
+        un.tile.row_start = t * Cfg<PAIR>::TILE + (int)rank * BM;
+        un.tile.row_count = min(BM, p.T - un.tile.row_start);
+        un.tile.expert = 0;
+    }
     un.i0 = chunk * IC;
     un.ic = min(IC, p.I - un.i0);
     un.n_gu = (un.ic + GU_ROWS - 1) / GU_ROWS;
@@ -208,8 +207,7 @@ __device__ __forceinline__ Unit make_unit(const Params &p, int u, int n_tiles) {
     return un;
 }
 
-// Where step st of a unit reads its packed weights: the block column, the
-// 64-wide group inside the block, and the first row of each tensor map.
+// Where step st of a unit reads its packed weights.
 struct StepSrc {
     bool gu;        // gate/up step (x tile too) or down step
     int ks;         // K step inside the job
@@ -239,45 +237,55 @@ __device__ __forceinline__ StepSrc step_src(const Unit &un, int st) {
     return r;
 }
 
+template <bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     ffn_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
+    using C = Cfg<PAIR>;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled tiles
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
-    uint64_t *a_full = bars, *a_empty = bars + NA;
-    uint64_t *b_full = bars + 2 * NA, *b_empty = b_full + NB;
-    uint64_t *r_full = b_empty + NB, *r_empty = r_full + NR;
-    uint64_t *t_full = r_empty + NR, *t_empty = t_full + 2;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *a_full = bars, *a_empty = bars + C::NA;
+    uint64_t *b_full = bars + 2 * C::NA, *b_empty = b_full + C::NB;
+    uint64_t *r_full = b_empty + C::NB, *r_empty = r_full + C::NR;
+    uint64_t *t_full = r_empty + C::NR, *t_empty = t_full + 2;
     uint64_t *h_full = t_empty + 2, *h_empty = h_full + 1, *drain = h_full + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + N_BARS);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::N_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t s_h = smem_u32(smem + OFF_H);
-    const uint32_t s_a = smem_u32(smem + OFF_A);
-    const uint32_t s_b = smem_u32(smem + OFF_B);
-    const uint32_t s_r = smem_u32(smem + OFF_R);
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0;
+    const bool leader = rank == 0;
+    const uint32_t s_h = smem_u32(smem + C::OFF_H);
+    const uint32_t s_a = smem_u32(smem + C::OFF_A);
+    const uint32_t s_b = smem_u32(smem + C::OFF_B);
+    const uint32_t s_r = smem_u32(smem + C::OFF_R);
+    // Arrive on a barrier that the MMA issuer waits on: the local one, or the
+    // pair leader's copy at the same offset.
+    auto arrive_leader = [&](uint64_t *bar) {
+        if (PAIR) mbar_arrive_cluster(mapa_shared(smem_u32(bar), 0));
+        else mbar_arrive(bar);
+    };
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NA; ++i) {
+        for (int i = 0; i < C::NA; ++i) {
             mbar_init(&a_full[i], 1);
             mbar_init(&a_empty[i], 1);
         }
-        for (int i = 0; i < NB; ++i) {
-            mbar_init(&b_full[i], UNPACK_WARPS);
+        for (int i = 0; i < C::NB; ++i) {
+            mbar_init(&b_full[i], C::B_ARRIVALS);
             mbar_init(&b_empty[i], 1);
         }
-        for (int i = 0; i < NR; ++i) {
+        for (int i = 0; i < C::NR; ++i) {
             mbar_init(&r_full[i], 1);
             mbar_init(&r_empty[i], UNPACK_WARPS);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&t_full[i], 1);
-            mbar_init(&t_empty[i], 128);
+            mbar_init(&t_empty[i], C::EPI_ARRIVALS);
         }
-        mbar_init(h_full, 128);
+        mbar_init(h_full, C::EPI_ARRIVALS);
         mbar_init(h_empty, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -292,17 +300,25 @@ __global__ void __launch_bounds__(THREADS, 1)
         prefetch_tensormap(&maps.d_qs);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(tmem_slot, TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync_all();      // both CTAs' barriers exist before any remote arrive
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     const int n_tiles = p.n_tiles_dev ? min(*p.n_tiles_dev, p.n_tiles_host) : p.n_tiles_host;
     const int n_chunks = (p.I + IC - 1) / IC;
     const int n_units = n_tiles * n_chunks;
+    const int group = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int n_groups = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
     const int64_t rbH = (int64_t)(p.H / kQK) * kBlockBytes;
     const int64_t rbI = q4k_row_bytes(p.I);
 
@@ -312,60 +328,86 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t ai = 0, aph = 0, ri = 0, rph = 0;
             uint32_t a_issued = 0, r_issued = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const Unit un = make_unit(p, u, n_tiles);
+            for (int u = group; u < n_units && ok; u += n_groups) {
+                const Unit un = make_unit<PAIR>(p, u, n_tiles, rank);
                 const int e = un.tile.expert;
                 const int steps = un.n_gu * un.ks_gu + un.n_y * un.ks_y;
                 for (int st = 0; st < steps; ++st) {
                     const StepSrc src = step_src(un, st);
                     if (src.gu) {
                         if (!mbar_wait(&a_empty[ai], aph ^ 1, abort_flag, p.err)) { ok = false; break; }
-                        mbar_arrive_expect_tx(&a_full[ai], A_BYTES);
-                        tma_load_2d(smem + OFF_A + ai * A_BYTES, &maps.x, &a_full[ai], src.ks * BK,
-                                    un.tile.row_start);
+                        void *dst = smem + C::OFF_A + ai * A_BYTES;
+                        if (PAIR) {
+                            // both CTAs' tiles complete on the leader's barrier
+                            if (leader) mbar_arrive_expect_tx(&a_full[ai], 2 * A_BYTES);
+                            tma_load_2d_pair(dst, &maps.x, mapa_shared(smem_u32(&a_full[ai]), 0),
+                                             src.ks * BK, un.tile.row_start);
+                        } else {
+                            mbar_arrive_expect_tx(&a_full[ai], A_BYTES);
+                            tma_load_2d(dst, &maps.x, &a_full[ai], src.ks * BK, un.tile.row_start);
+                        }
                         ++a_issued;
-                        if (++ai == NA) { ai = 0; aph ^= 1; }
+                        if (++ai == C::NA) { ai = 0; aph ^= 1; }
                     }
                     if (!mbar_wait(&r_empty[ri], rph ^ 1, abort_flag, p.err)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&r_full[ri], R_BYTES);
-                    uint8_t *rs = smem + OFF_R + ri * R_BYTES;
+                    mbar_arrive_expect_tx(&r_full[ri], C::R_BYTES);
+                    uint8_t *rs = smem + C::OFF_R + ri * C::R_BYTES;
                     const int qcol = src.xcol + 16 + 32 * src.g;
                     if (src.gu) {
                         const int row = e * p.I + un.i0 + src.s * GU_ROWS;
-                        tma_load_2d(rs, &maps.g_hdr, &r_full[ri], src.xcol, row);
-                        tma_load_2d(rs + 128 * 16, &maps.u_hdr, &r_full[ri], src.xcol, row);
-                        tma_load_2d(rs + R_HDR, &maps.g_qs, &r_full[ri], qcol, row);
-                        tma_load_2d(rs + R_HDR + 128 * 32, &maps.u_qs, &r_full[ri], qcol, row);
+                        if (PAIR) {
+                            // the leader unpacks the gate rows, its peer the up rows
+                            const CUtensorMap *mh = leader ? &maps.g_hdr : &maps.u_hdr;
+                            const CUtensorMap *mq = leader ? &maps.g_qs : &maps.u_qs;
+                            tma_load_2d(rs, mh, &r_full[ri], src.xcol, row);
+                            tma_load_2d(rs + C::R_HDR, mq, &r_full[ri], qcol, row);
+                        } else {
+                            tma_load_2d(rs, &maps.g_hdr, &r_full[ri], src.xcol, row);
+                            tma_load_2d(rs + 128 * 16, &maps.u_hdr, &r_full[ri], src.xcol, row);
+                            tma_load_2d(rs + C::R_HDR, &maps.g_qs, &r_full[ri], qcol, row);
+                            tma_load_2d(rs + C::R_HDR + 128 * 32, &maps.u_qs, &r_full[ri], qcol, row);
+                        }
                     } else {
-                        const int row = e * p.H + src.s * NJ;
+                        const int row = e * p.H + src.s * NJ + (int)rank * C::ROWS_B;
                         tma_load_2d(rs, &maps.d_hdr, &r_full[ri], src.xcol, row);
-                        tma_load_2d(rs + R_HDR, &maps.d_qs, &r_full[ri], qcol, row);
+                        tma_load_2d(rs + C::R_HDR, &maps.d_qs, &r_full[ri], qcol, row);
                     }
                     ++r_issued;
-                    if (++ri == NR) { ri = 0; rph ^= 1; }
+                    if (++ri == C::NR) { ri = 0; rph ^= 1; }
                 }
             }
             // Before the block may exit, every load issued here must have
-            // landed: wait (bounded) for the full barrier of the last stages
-            // issued (a phase that completed long ago passes at once).
-            for (uint32_t i = 0; i < NA && i < a_issued; ++i) {
-                if (ai == 0) { ai = NA; aph ^= 1; }
-                --ai;
-                mbar_wait(&a_full[ai], aph, nullptr, p.err, kWaitBudgetCycles / 8);
+            // landed: wait (bounded) for the full barriers of the last stages
+            // issued (a phase that completed long ago passes at once).  In a
+            // pair the x tiles complete on the leader's barriers, which the
+            // leader's issuer has waited for before its final MMAs.
+            if (!PAIR || leader) {
+                for (uint32_t i = 0; i < (uint32_t)C::NA && i < a_issued; ++i) {
+                    if (ai == 0) { ai = C::NA; aph ^= 1; }
+                    --ai;
+                    mbar_wait(&a_full[ai], aph, nullptr, p.err, kWaitBudgetCycles / 8);
+                }
             }
-            for (uint32_t i = 0; i < NR && i < r_issued; ++i) {
-                if (ri == 0) { ri = NR; rph ^= 1; }
+            for (uint32_t i = 0; i < (uint32_t)C::NR && i < r_issued; ++i) {
+                if (ri == 0) { ri = C::NR; rph ^= 1; }
                 --ri;
                 mbar_wait(&r_full[ri], rph, nullptr, p.err, kWaitBudgetCycles / 8);
             }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
+        // ---------------- MMA issuer (the pair's leader only) ----------------
+        if (lane == 0 && leader) {
             uint32_t ai = 0, aph = 0, bi = 0, bph = 0, jc = 0, uc = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
-                const Unit un = make_unit(p, u, n_tiles);
+            auto mma = [&](uint32_t d, uint64_t da, uint64_t db, uint32_t acc) {
+                if (PAIR) tc_mma_bf16_pair(d, da, db, C::IDESC, acc);
+                else tc_mma_bf16(d, da, db, C::IDESC, acc);
+            };
+            auto commit = [&](uint64_t *bar) {
+                if (PAIR) tc_commit_pair(bar); else tc_commit(bar);
+            };
+            for (int u = group; u < n_units && ok; u += n_groups, ++uc) {
+                const Unit un = make_unit<PAIR>(p, u, n_tiles, rank);
                 for (int s = 0; s < un.n_gu && ok; ++s, ++jc) {
                     const uint32_t slot = jc & 1, tph = (jc >> 1) & 1;
                     if (!mbar_wait(&t_empty[slot], tph ^ 1, abort_flag, p.err)) { ok = false; break; }
@@ -376,19 +418,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                             !mbar_wait(&b_full[bi], bph, abort_flag, p.err)) { ok = false; break; }
                         tc_fence_after();
                         const uint64_t da = smem_desc_k_sw128(s_a + ai * A_BYTES);
-                        const uint64_t db = smem_desc_k_sw128(s_b + bi * B_BYTES);
+                        const uint64_t db = smem_desc_k_sw128(s_b + bi * C::B_BYTES);
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk)
-                            tc_mma_bf16(d_tmem, da + 2 * kk, db + 2 * kk, IDESC, (ks | kk) != 0);
-                        tc_commit(&a_empty[ai]);
-                        tc_commit(&b_empty[bi]);
-                        if (++ai == NA) { ai = 0; aph ^= 1; }
-                        if (++bi == NB) { bi = 0; bph ^= 1; }
+                            mma(d_tmem, da + 2 * kk, db + 2 * kk, (ks | kk) != 0);
+                        commit(&a_empty[ai]);
+                        commit(&b_empty[bi]);
+                        if (++ai == C::NA) { ai = 0; aph ^= 1; }
+                        if (++bi == C::NB) { bi = 0; bph ^= 1; }
                     }
-                    if (ok) tc_commit(&t_full[slot]);
+                    if (ok) commit(&t_full[slot]);
                 }
                 if (!ok) break;
-                // the down projection reads h: wait until the epilogue wrote all of it
+                // the down projection reads h: wait until the epilogues wrote all of it
                 if (!mbar_wait(h_full, uc & 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 for (int n = 0; n < un.n_y && ok; ++n, ++jc) {
@@ -400,86 +442,100 @@ __global__ void __launch_bounds__(THREADS, 1)
                         if (!mbar_wait(&b_full[bi], bph, abort_flag, p.err)) { ok = false; break; }
                         tc_fence_after();
                         const uint64_t da = smem_desc_k_sw128(s_h + ks * HT_BYTES);
-                        const uint64_t db = smem_desc_k_sw128(s_b + bi * B_BYTES);
+                        const uint64_t db = smem_desc_k_sw128(s_b + bi * C::B_BYTES);
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk)
-                            tc_mma_bf16(d_tmem, da + 2 * kk, db + 2 * kk, IDESC, (ks | kk) != 0);
-                        tc_commit(&b_empty[bi]);
-                        if (++bi == NB) { bi = 0; bph ^= 1; }
+                            mma(d_tmem, da + 2 * kk, db + 2 * kk, (ks | kk) != 0);
+                        commit(&b_empty[bi]);
+                        if (++bi == C::NB) { bi = 0; bph ^= 1; }
                     }
-                    if (ok) tc_commit(&t_full[slot]);
+                    if (ok) commit(&t_full[slot]);
                 }
-                if (ok) tc_commit(h_empty);   // h may be overwritten once these MMAs finish
+                if (ok) commit(h_empty);   // h may be overwritten once these MMAs finish
             }
             // every MMA issued here completes before TMEM is released
-            tc_commit(drain);
+            if (PAIR) tc_commit_pair(drain); else tc_commit(drain);
             mbar_wait(drain, 0, nullptr, p.err, kWaitBudgetCycles / 8);
         }
     } else if (warp < EPI_WARP0) {
-        // ------------- weight unpackers (256 threads, one row each) -------------
-        const int row = threadIdx.x - 64;             // 0..255
+        // ------------- weight unpackers (8 warps) -------------
+        const int ut = threadIdx.x - 64;               // 0..255
+        const int row = ut / C::TPR;                    // weight row of this thread
+        const int part = ut % C::TPR;                   // which code words (pairs: half)
         uint32_t bi = 0, bph = 0, ri = 0, rph = 0;
         bool ok = true;
-        // a quarter-warp's 16-byte reads of the 32-byte code rows are bank
-        // conflict free when rows 4..7 of each group of 8 read their halves
-        // in the other order
+        // bank-conflict-free order of the 16-byte reads of the 32-byte code rows
         const int qfirst = (row >> 2) & 1;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-            const Unit un = make_unit(p, u, n_tiles);
+        for (int u = group; u < n_units && ok; u += n_groups) {
+            const Unit un = make_unit<PAIR>(p, u, n_tiles, rank);
             const int e = un.tile.expert;
-            // L2 prefetch of this unit's weight rows (one row pair / 16 down rows per thread)
-            for (int s = 0; s < un.n_gu; ++s) {
-                const int ii = un.i0 + s * GU_ROWS + (row & 127);
-                if (ii < p.I) {
-                    const uint8_t *w = row < 128 ? p.Wg : p.Wu;
-                    prefetch_l2_bulk(w + ((int64_t)e * p.I + ii) * rbH, (uint32_t)rbH);
+            // L2 prefetch of this unit's packed weight rows
+            if (part == 0) {
+                for (int s = 0; s < un.n_gu; ++s) {
+                    const int ii = un.i0 + s * GU_ROWS + (row & 127);
+                    if (ii < p.I) {
+                        const bool gate = PAIR ? leader : row < 128;
+                        const uint8_t *w = gate ? p.Wg : p.Wu;
+                        prefetch_l2_bulk(w + ((int64_t)e * p.I + ii) * rbH, (uint32_t)rbH);
+                    }
                 }
-            }
-            {
                 const int b0 = un.i0 >> 8, b1 = (un.i0 + un.ic + 255) >> 8;
                 const uint32_t bytes = (uint32_t)((b1 - b0) * kBlockBytes);
-                for (int n = row; n < p.H; n += 256)
-                    prefetch_l2_bulk(p.Wd + ((int64_t)e * p.H + n) * rbI + (int64_t)b0 * kBlockBytes,
-                                     bytes);
+                for (int n = row + (int)rank * C::ROWS_B; n < p.H; n += NJ)
+                    for (int nn = n; nn < n + (PAIR ? 1 : 1); ++nn)
+                        prefetch_l2_bulk(p.Wd + ((int64_t)e * p.H + nn) * rbI +
+                                             (int64_t)b0 * kBlockBytes,
+                                         bytes);
             }
             const int steps = un.n_gu * un.ks_gu + un.n_y * un.ks_y;
             for (int st = 0; st < steps; ++st) {
                 const StepSrc src = step_src(un, st);
-                const bool zero = src.gu && (un.i0 + src.s * GU_ROWS + (row & 127) >= p.I);
+                const int grow = PAIR ? row : (row & 127);          // gate/up row within the job
+                const bool zero = src.gu && (un.i0 + src.s * GU_ROWS + grow >= p.I);
                 if (!mbar_wait(&r_full[ri], rph, abort_flag, p.err)) { ok = false; break; }
-                RawRow raw;
+                uint4 hd = make_uint4(0, 0, 0, 0), q0 = hd, q1 = hd;
                 if (!zero) {
-                    const uint32_t rs = s_r + ri * R_BYTES;
-                    raw.hd = ld_shared_v4(rs + row * 16);
-                    const uint32_t qa = rs + R_HDR + row * 32;
-                    const uint4 first = ld_shared_v4(qa + 16 * qfirst);
-                    const uint4 second = ld_shared_v4(qa + 16 * (qfirst ^ 1));
-                    raw.q0 = qfirst ? second : first;
-                    raw.q1 = qfirst ? first : second;
+                    const uint32_t rs = s_r + ri * C::R_BYTES;
+                    hd = ld_shared_v4(rs + row * 16);
+                    const uint32_t qa = rs + C::R_HDR + row * 32;
+                    if (C::TPR == 1) {
+                        const uint4 first = ld_shared_v4(qa + 16 * qfirst);
+                        const uint4 second = ld_shared_v4(qa + 16 * (qfirst ^ 1));
+                        q0 = qfirst ? second : first;
+                        q1 = qfirst ? first : second;
+                    } else {
+                        q0 = ld_shared_v4(qa + 16 * part);
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&r_empty[ri]);
-                if (++ri == NR) { ri = 0; rph ^= 1; }
+                if (++ri == C::NR) { ri = 0; rph ^= 1; }
                 if (!mbar_wait(&b_empty[bi], bph ^ 1, abort_flag, p.err)) { ok = false; break; }
-                const uint32_t rb = s_b + bi * B_BYTES + sw128_row(row);
-                if (zero) zero_row_smem(rb, row); else unpack_row_to_smem(raw, src.g, rb, row);
+                const uint32_t rb = s_b + bi * C::B_BYTES + sw128_row(row);
+                if (C::TPR == 1) {
+                    const uint32_t w8[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                    unpack_words_to_smem<8>(hd, w8, 0, src.g, rb, row);
+                } else {
+                    const uint32_t w4[4] = {q0.x, q0.y, q0.z, q0.w};
+                    unpack_words_to_smem<4>(hd, w4, 4 * part, src.g, rb, row);
+                }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&b_full[bi]);
-                if (++bi == NB) { bi = 0; bph ^= 1; }
+                if (lane == 0) arrive_leader(&b_full[bi]);
+                if (++bi == C::NB) { bi = 0; bph ^= 1; }
             }
         }
     } else {
-        // ---------------- epilogue (128 threads) ----------------
+        // ---------------- epilogue (4 warps) ----------------
         const int q = warp & 3;                      // TMEM lane quadrant of this warp
-        const int row = q * 32 + lane;               // token row within the tile
+        const int row = q * 32 + lane;               // token row within the CTA's tile
         const uint32_t lane_bits = (uint32_t)(q * 32) << 16;
-        const uint32_t s_y = smem_u32(smem + OFF_Y), s_base = smem_u32(smem);
+        const uint32_t s_y = smem_u32(smem + C::OFF_Y), s_base = smem_u32(smem);
         uint32_t y_use = 0;
         uint32_t jc = 0, uc = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
-            const Unit un = make_unit(p, u, n_tiles);
+        for (int u = group; u < n_units && ok; u += n_groups, ++uc) {
+            const Unit un = make_unit<PAIR>(p, u, n_tiles, rank);
             for (int s = 0; s < un.n_gu && ok; ++s, ++jc) {
                 const uint32_t slot = jc & 1, tph = (jc >> 1) & 1;
                 if (!mbar_wait(&t_full[slot], tph, abort_flag, p.err)) { ok = false; break; }
@@ -511,11 +567,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                                      hw[4 * j + 1], hw[4 * j + 2], hw[4 * j + 3]);
                 }
                 tc_fence_before();
-                mbar_arrive(&t_empty[slot]);
+                __syncwarp();
+                if (lane == 0) arrive_leader(&t_empty[slot]);
             }
             if (!ok) break;
             fence_proxy_async_smem();
-            mbar_arrive(h_full);
+            __syncwarp();
+            if (lane == 0) arrive_leader(h_full);
             // this row's destination
             const bool valid = row < un.tile.row_count;
             int token = 0;
@@ -537,15 +595,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!mbar_wait(&t_full[slot], tph, abort_flag, p.err)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t t_addr = tmem_base + lane_bits + slot * NJ;
-                if (tma_y) {
 #pragma unroll 1
-                    for (int c = 0; c < NJ; c += 32) {
-                        uint32_t yr[32];
-                        tmem_ld_32x32b_x32(t_addr + c, yr);
-                        tmem_ld_wait(yr);
+                for (int c = 0; c < NJ; c += 32) {
+                    uint32_t yr[32];
+                    tmem_ld_32x32b_x32(t_addr + c, yr);
+                    tmem_ld_wait(yr);
+                    if (tma_y) {
 #pragma unroll
                         for (int half = 0; half < 2; ++half) {
-                            // buffer use: y_use alternates between the warp's two buffers
                             if (lane == 0) bulk_wait_group_read<1>();
                             __syncwarp();
                             const uint32_t buf = s_y + (uint32_t)((q * 2 + (y_use & 1)) * Y_BUF);
@@ -565,17 +622,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             }
                             ++y_use;
                         }
-                    }
-                    tc_fence_before();
-                    mbar_arrive(&t_empty[slot]);
-                    continue;
-                }
-#pragma unroll 1
-                for (int c = 0; c < NJ; c += 32) {
-                    uint32_t yr[32];
-                    tmem_ld_32x32b_x32(t_addr + c, yr);
-                    tmem_ld_wait(yr);
-                    if (valid) {
+                    } else if (valid) {
                         float *dst = yrow + n * NJ + c;
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
@@ -590,23 +637,27 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(&t_empty[slot]);
+                __syncwarp();
+                if (lane == 0) arrive_leader(&t_empty[slot]);
             }
         }
-        // the reductions must have finished reading shared memory (and be
-        // complete) before the block exits
+        // the reductions must have finished before the block exits
         if (lane == 0) bulk_wait_group_all();
         __syncwarp();
     }
 
-    // Every role is done: all MMAs were consumed by the epilogue (or the
-    // launch is aborting, in which case the issuer waited for its MMAs).
+    // Every role is done: all MMAs were consumed by the epilogues (or the
+    // launch is aborting, in which case the issuer waited for its MMAs).  In a
+    // pair, neither CTA leaves while the leader's MMAs may still read the
+    // peer's shared memory or the peer may still arrive on the leader's barriers.
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync_all();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if (PAIR) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
@@ -642,6 +693,9 @@ cudaError_t launch_ffn_tc(const TcArgs &a, cudaStream_t s) {
     const DeviceInfo &di = device_info();
     auto encode = get_encode_fn();
     if (!encode) return cudaErrorNotSupported;
+    // Dense prefill with at least one full pair tile runs on CTA pairs.
+    const bool pair = a.tiles == nullptr && a.T >= 256 && di.num_sms >= 2;
+    const int rows_b = pair ? tc::Cfg<true>::ROWS_B : tc::Cfg<false>::ROWS_B;
     tc::Maps maps;
     {
         const cuuint64_t dims[2] = {(cuuint64_t)a.H, (cuuint64_t)a.x_rows};
@@ -670,16 +724,16 @@ cudaError_t launch_ffn_tc(const TcArgs &a, cudaStream_t s) {
         !encode_bytes_map(encode, &maps.g_qs, a.Wg, rbH, gu_rows, 32, tc::GU_ROWS) ||
         !encode_bytes_map(encode, &maps.u_hdr, a.Wu, rbH, gu_rows, 16, tc::GU_ROWS) ||
         !encode_bytes_map(encode, &maps.u_qs, a.Wu, rbH, gu_rows, 32, tc::GU_ROWS) ||
-        !encode_bytes_map(encode, &maps.d_hdr, a.Wd, rbI, d_rows, 16, tc::NJ) ||
-        !encode_bytes_map(encode, &maps.d_qs, a.Wd, rbI, d_rows, 32, tc::NJ))
+        !encode_bytes_map(encode, &maps.d_hdr, a.Wd, rbI, d_rows, 16, rows_b) ||
+        !encode_bytes_map(encode, &maps.d_qs, a.Wd, rbI, d_rows, 32, rows_b))
         return cudaErrorInvalidValue;
-    static int attr_set_device = -1;
-    if (attr_set_device != di.device) {
-        cudaError_t e = cudaFuncSetAttribute(tc::ffn_tc_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             tc::SMEM_BYTES);
+    static int attr_set_device[2] = {-1, -1};
+    const void *fn = pair ? (const void *)tc::ffn_tc_kernel<true> : (const void *)tc::ffn_tc_kernel<false>;
+    const int smem = pair ? tc::Cfg<true>::SMEM_BYTES : tc::Cfg<false>::SMEM_BYTES;
+    if (attr_set_device[pair] != di.device) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        attr_set_device = di.device;
+        attr_set_device[pair] = di.device;
     }
     tc::Params p;
     p.Wg = a.Wg;
@@ -691,16 +745,35 @@ cudaError_t launch_ffn_tc(const TcArgs &a, cudaStream_t s) {
     p.row_token = a.row_token;
     p.row_weight = a.row_weight;
     p.err = a.err;
-    p.n_tiles_host = a.n_tiles_host;
     p.T = a.T;
     p.H = a.H;
     p.I = a.I;
     const int n_chunks = (a.I + tc::IC - 1) / tc::IC;
+    if (pair) {
+        p.n_tiles_host = (a.T + 255) / 256;
+        const int64_t units = (int64_t)p.n_tiles_host * n_chunks;
+        int64_t pairs = di.num_sms / 2;
+        if (units < pairs) pairs = units;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(2 * pairs));
+        cfg.blockDim = dim3(tc::THREADS);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, tc::ffn_tc_kernel<true>, maps, p);
+    }
+    p.n_tiles_host = a.n_tiles_host;
     const int64_t units = (int64_t)a.n_tiles_host * n_chunks;
     int grid = di.num_sms;
     if (units < grid) grid = (int)units;
     if (grid < 1) return cudaSuccess;
-    tc::ffn_tc_kernel<<<grid, tc::THREADS, tc::SMEM_BYTES, s>>>(maps, p);
+    tc::ffn_tc_kernel<false><<<grid, tc::THREADS, smem, s>>>(maps, p);
     return cudaGetLastError();
 }
 
