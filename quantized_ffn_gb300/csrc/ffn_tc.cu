@@ -40,18 +40,15 @@ constexpr int BM = 128;                  // token rows per CTA per tile (UMMA M 
 constexpr int BK = 64;                   // K per pipeline step (128 bytes of bf16)
 constexpr int GU_ROWS = 128;             // intermediate rows per gate/up job
 constexpr int NJ = 256;                  // UMMA N of every job
-constexpr int IC = 256;                  // intermediate columns per work unit
 constexpr int A_BYTES = BM * BK * 2;     // 16 KB x tile per CTA
 constexpr int HT_BYTES = BM * BK * 2;    // one 64-column slice of h: 16 KB
-constexpr int N_HT = IC / BK;            // 4
 constexpr int UNPACK_WARPS = 8;
 constexpr int THREADS = (2 + UNPACK_WARPS + 4) * 32;
 constexpr int EPI_WARP0 = 2 + UNPACK_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
 // y staging for the TMA reductions: per epilogue warp two buffers of
-// [32 rows x 16 fp32] with the 64-byte swizzle (chunk j of row r at j ^ (r/2 % 4)).
-constexpr int Y_COLS = 16;
-constexpr int Y_BUF = 32 * Y_COLS * 4;   // 2 KB
+// [32 rows x Y_COLS fp32]; 32 columns use the 128-byte swizzle (chunk j of
+// row r at j ^ (r % 8)), 16 columns the 64-byte swizzle (j ^ (r/2 % 4)).
 
 // Geometry of one kernel variant.  PAIR: a cluster of two CTAs shares each
 // 256-token tile; one UMMA of M = 256 covers both CTAs' rows, and the N = 256
@@ -61,9 +58,13 @@ struct Cfg {
     static constexpr int ROWS_B = PAIR ? 128 : 256;      // weight rows unpacked per CTA per step
     static constexpr int TPR = 256 / ROWS_B;              // unpack threads per weight row
     static constexpr int TILE = PAIR ? 256 : 128;         // tokens per work-unit tile
+    static constexpr int IC = 256;                        // intermediate columns per work unit
+    static constexpr int N_HT = IC / BK;                  // 64-column slices of h
     static constexpr int NA = PAIR ? 3 : 2;               // x stages
     static constexpr int NB = PAIR ? 3 : 2;               // unpacked-weight stages
-    static constexpr int NR = PAIR ? 6 : 4;               // packed-weight stages
+    static constexpr int NR = PAIR ? 5 : 3;               // packed-weight stages
+    static constexpr int Y_COLS = PAIR ? 32 : 16;
+    static constexpr int Y_BUF = 32 * Y_COLS * 4;
     static constexpr int B_BYTES = ROWS_B * BK * 2;
     static constexpr int R_HDR = ROWS_B * 16;
     static constexpr int R_BYTES = ROWS_B * 48;
@@ -86,7 +87,7 @@ struct Cfg {
 // headers and the 32 code bytes of one 64-wide K step.
 struct Maps {
     CUtensorMap x;
-    CUtensorMap y;                          // fp32 [T][H], boxes of [32 rows x 16 cols]
+    CUtensorMap y;                          // fp32 [T][H], boxes of [32 rows x 32 cols]
     CUtensorMap g_hdr, g_qs, u_hdr, u_qs;   // boxes of 128 rows
     CUtensorMap d_hdr, d_qs;                // boxes of ROWS_B rows
 };
@@ -198,8 +199,8 @@ __device__ __forceinline__ Unit make_unit(const Params &p, int u, int n_tiles, u
         un.tile.row_count = min(BM, p.T - un.tile.row_start);
         un.tile.expert = 0;
     }
-    un.i0 = chunk * IC;
-    un.ic = min(IC, p.I - un.i0);
+    un.i0 = chunk * Cfg<PAIR>::IC;
+    un.ic = min(Cfg<PAIR>::IC, p.I - un.i0);
     un.n_gu = (un.ic + GU_ROWS - 1) / GU_ROWS;
     un.ks_gu = p.H / BK;
     un.ks_y = un.ic / BK;
@@ -207,35 +208,34 @@ __device__ __forceinline__ Unit make_unit(const Params &p, int u, int n_tiles, u
     return un;
 }
 
-// Where step st of a unit reads its packed weights.
+// Walks the K steps of a unit in order (gate/up jobs, then down jobs) and
+// says where each step reads its packed weights.
 struct StepSrc {
     bool gu;        // gate/up step (x tile too) or down step
     int ks;         // K step inside the job
     int s;          // gate/up job or down job index
     int xcol;       // byte column of the block header
     int g;          // 64-wide group inside the block (code bytes 32g..32g+31)
-};
-
-__device__ __forceinline__ StepSrc step_src(const Unit &un, int st) {
-    StepSrc r;
-    const int ngu = un.n_gu * un.ks_gu;
-    if (st < ngu) {
-        r.gu = true;
-        r.s = st / un.ks_gu;
-        r.ks = st - r.s * un.ks_gu;
-        r.xcol = (r.ks >> 2) * kBlockBytes;
-        r.g = r.ks & 3;
-    } else {
-        r.gu = false;
-        const int st2 = st - ngu;
-        r.s = st2 / un.ks_y;
-        r.ks = st2 - r.s * un.ks_y;
-        const int col = un.i0 + r.ks * BK;
-        r.xcol = (col >> 8) * kBlockBytes;
-        r.g = (col & 255) >> 6;
+    __device__ __forceinline__ void start() { gu = true; ks = 0; s = 0; }
+    __device__ __forceinline__ void locate(const Unit &un) {
+        if (gu) {
+            xcol = (ks >> 2) * kBlockBytes;
+            g = ks & 3;
+        } else {
+            const int col = un.i0 + ks * BK;
+            xcol = (col >> 8) * kBlockBytes;
+            g = (col & 255) >> 6;
+        }
     }
-    return r;
-}
+    __device__ __forceinline__ void advance(const Unit &un) {
+        if (gu) {
+            if (++ks == un.ks_gu) { ks = 0; if (++s == un.n_gu) { s = 0; gu = false; } }
+        } else if (++ks == un.ks_y) {
+            ks = 0;
+            ++s;
+        }
+    }
+};
 
 template <bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     const int n_tiles = p.n_tiles_dev ? min(*p.n_tiles_dev, p.n_tiles_host) : p.n_tiles_host;
-    const int n_chunks = (p.I + IC - 1) / IC;
+    const int n_chunks = (p.I + C::IC - 1) / C::IC;
     const int n_units = n_tiles * n_chunks;
     const int group = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
     const int n_groups = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
@@ -332,8 +332,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const Unit un = make_unit<PAIR>(p, u, n_tiles, rank);
                 const int e = un.tile.expert;
                 const int steps = un.n_gu * un.ks_gu + un.n_y * un.ks_y;
-                for (int st = 0; st < steps; ++st) {
-                    const StepSrc src = step_src(un, st);
+                StepSrc src;
+                src.start();
+                for (int st = 0; st < steps; ++st, src.advance(un)) {
+                    src.locate(un);
                     if (src.gu) {
                         if (!mbar_wait(&a_empty[ai], aph ^ 1, abort_flag, p.err)) { ok = false; break; }
                         void *dst = smem + C::OFF_A + ai * A_BYTES;
@@ -469,27 +471,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int u = group; u < n_units && ok; u += n_groups) {
             const Unit un = make_unit<PAIR>(p, u, n_tiles, rank);
             const int e = un.tile.expert;
-            // L2 prefetch of this unit's packed weight rows
-            if (part == 0) {
-                for (int s = 0; s < un.n_gu; ++s) {
-                    const int ii = un.i0 + s * GU_ROWS + (row & 127);
-                    if (ii < p.I) {
-                        const bool gate = PAIR ? leader : row < 128;
-                        const uint8_t *w = gate ? p.Wg : p.Wu;
-                        prefetch_l2_bulk(w + ((int64_t)e * p.I + ii) * rbH, (uint32_t)rbH);
-                    }
-                }
-                const int b0 = un.i0 >> 8, b1 = (un.i0 + un.ic + 255) >> 8;
-                const uint32_t bytes = (uint32_t)((b1 - b0) * kBlockBytes);
-                for (int n = row + (int)rank * C::ROWS_B; n < p.H; n += NJ)
-                    for (int nn = n; nn < n + (PAIR ? 1 : 1); ++nn)
-                        prefetch_l2_bulk(p.Wd + ((int64_t)e * p.H + nn) * rbI +
-                                             (int64_t)b0 * kBlockBytes,
-                                         bytes);
-            }
             const int steps = un.n_gu * un.ks_gu + un.n_y * un.ks_y;
-            for (int st = 0; st < steps; ++st) {
-                const StepSrc src = step_src(un, st);
+            StepSrc src;
+            src.start();
+            for (int st = 0; st < steps; ++st, src.advance(un)) {
+                src.locate(un);
                 const int grow = PAIR ? row : (row & 127);          // gate/up row within the job
                 const bool zero = src.gu && (un.i0 + src.s * GU_ROWS + grow >= p.I);
                 if (!mbar_wait(&r_full[ri], rph, abort_flag, p.err)) { ok = false; break; }
@@ -602,22 +588,23 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tmem_ld_wait(yr);
                     if (tma_y) {
 #pragma unroll
-                        for (int half = 0; half < 2; ++half) {
+                        for (int part = 0; part < 32 / C::Y_COLS; ++part) {
                             if (lane == 0) bulk_wait_group_read<1>();
                             __syncwarp();
-                            const uint32_t buf = s_y + (uint32_t)((q * 2 + (y_use & 1)) * Y_BUF);
-                            const uint32_t rowa = buf + lane * 64;
-                            const int sw = (lane >> 1) & 3;
+                            const uint32_t buf = s_y + (uint32_t)((q * 2 + (y_use & 1)) * C::Y_BUF);
+                            const uint32_t rowa = buf + lane * (C::Y_COLS * 4);
+                            constexpr int CH = C::Y_COLS / 4;            // 16-byte chunks per row
+                            const int sw = C::Y_COLS == 32 ? (lane & 7) : ((lane >> 1) & 3);
 #pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                st_shared_v4(rowa + (((uint32_t)(j ^ sw)) << 4), yr[16 * half + 4 * j],
-                                             yr[16 * half + 4 * j + 1], yr[16 * half + 4 * j + 2],
-                                             yr[16 * half + 4 * j + 3]);
+                            for (int j = 0; j < CH; ++j)
+                                st_shared_v4(rowa + (((uint32_t)(j ^ sw)) << 4),
+                                             yr[C::Y_COLS * part + 4 * j], yr[C::Y_COLS * part + 4 * j + 1],
+                                             yr[C::Y_COLS * part + 4 * j + 2], yr[C::Y_COLS * part + 4 * j + 3]);
                             fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0 && warp_live) {
-                                tma_reduce_add_2d(&maps.y, smem + (buf - s_base), n * NJ + c + 16 * half,
-                                                  warp_row0);
+                                tma_reduce_add_2d(&maps.y, smem + (buf - s_base),
+                                                  n * NJ + c + C::Y_COLS * part, warp_row0);
                                 bulk_commit_group();
                             }
                             ++y_use;
@@ -711,10 +698,12 @@ cudaError_t launch_ffn_tc(const TcArgs &a, cudaStream_t s) {
     {
         const cuuint64_t dims[2] = {(cuuint64_t)a.H, (cuuint64_t)a.T};
         const cuuint64_t strides[1] = {(cuuint64_t)a.H * 4};
-        const cuuint32_t box[2] = {tc::Y_COLS, 32};
+        const int ycols = pair ? tc::Cfg<true>::Y_COLS : tc::Cfg<false>::Y_COLS;
+        const cuuint32_t box[2] = {(cuuint32_t)ycols, 32};
         const cuuint32_t estr[2] = {1, 1};
         CUresult r = encode(&maps.y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.y, dims, strides, box,
-                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            ycols == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
@@ -748,7 +737,8 @@ cudaError_t launch_ffn_tc(const TcArgs &a, cudaStream_t s) {
     p.T = a.T;
     p.H = a.H;
     p.I = a.I;
-    const int n_chunks = (a.I + tc::IC - 1) / tc::IC;
+    const int n_chunks = (a.I + (pair ? tc::Cfg<true>::IC : tc::Cfg<false>::IC) - 1) /
+                         (pair ? tc::Cfg<true>::IC : tc::Cfg<false>::IC);
     if (pair) {
         p.n_tiles_host = (a.T + 255) / 256;
         const int64_t units = (int64_t)p.n_tiles_host * n_chunks;
