@@ -21,12 +21,19 @@
 // versus the stubborn ones"); accumulators live in tensor memory, not in
 // registers, which removes the register-pressure problem at its root.
 //
-// Block roles (10 warps):
-//   warp 0      TMA producer: x tiles [128 x 64] bf16, 128-byte swizzle
+// Block roles (20 warps; warp w runs on sub-partition w % 4):
 //   warp 1      TMEM allocator and single-thread MMA issuer
-//   warps 2-5   weight producers: Q4_K -> bf16 tiles [256 x 64], same swizzle
-//   warps 6-9   epilogue: TMEM -> registers; SwiGLU -> h in SMEM, or the
-//               down-projection tile -> y
+//   warp 5      TMA producer: packed Q4_K weight slices (block headers and
+//               the code bytes of one 64-wide K step) into a ring
+//   warp 9      TMA producer: x tiles [128 x 64] bf16, 128-byte swizzle
+//   warps 0, 13, 2, 3  epilogue for TMEM lane quadrants 0-3: TMEM ->
+//               registers; SwiGLU -> h in SMEM, or the down-projection
+//               tile -> y
+//   warps 4, 6-8, 10-12, 14-16, 18, 19  weight unpackers: packed slices ->
+//               bf16 tiles [rows x 64], 128-byte swizzle
+//   warp 17     idle
+// The two producers are separate threads so that the weight ring can run as
+// far ahead as its depth allows, independently of the x ring.
 // Two TMEM accumulator slots of 256 columns each alternate between jobs, so
 // the epilogue of one job overlaps the MMAs of the next.
 #include <cudaTypedefs.h>
@@ -42,9 +49,29 @@ constexpr int GU_ROWS = 128;             // intermediate rows per gate/up job
 constexpr int NJ = 256;                  // UMMA N of every job
 constexpr int A_BYTES = BM * BK * 2;     // 16 KB x tile per CTA
 constexpr int HT_BYTES = BM * BK * 2;    // one 64-column slice of h: 16 KB
-constexpr int UNPACK_WARPS = 8;
-constexpr int THREADS = (2 + UNPACK_WARPS + 4) * 32;
-constexpr int EPI_WARP0 = 2 + UNPACK_WARPS;
+// Warp roles.  Warp w is scheduled by sub-partition w % 4.  The MMA issuer
+// (warp 1) shares its sub-partition only with the two TMA producers and one
+// epilogue warp: an arithmetic-heavy warp beside it delays its tcgen05
+// issue and leaves the tensor cores idle (measured: one such warp costs
+// about a fifth of the MMA rate).  The epilogue needs one warp per
+// sub-partition, because a warp reads only the TMEM lane quadrant w % 4.
+constexpr int NUM_WARPS = 20;
+constexpr int THREADS = NUM_WARPS * 32;
+constexpr int UNPACK_GROUP_WARPS = 4;    // 128 weight rows, one thread per row
+constexpr int UNPACK_GROUPS = 3;         // groups take 128-row tasks in turn
+enum Role { ROLE_EPI, ROLE_MMA, ROLE_WPROD, ROLE_XPROD, ROLE_UNPACK, ROLE_IDLE };
+__device__ __forceinline__ int warp_role(int w) {
+    if (w == 1) return ROLE_MMA;
+    if (w == 5) return ROLE_WPROD;
+    if (w == 9) return ROLE_XPROD;
+    if (w == 0 || w == 2 || w == 3 || w == 13) return ROLE_EPI;
+    if ((w & 3) == 1) return ROLE_IDLE;
+    return ROLE_UNPACK;
+}
+// 0..11 over the unpack warps 4, 6, 7, 8, 10, 11, 12, 14, 15, 16, 18, 19
+__device__ __forceinline__ int unpack_index(int w) {
+    return ((w >> 2) - 1) * 3 + ((w & 3) == 0 ? 0 : (w & 3) - 1);
+}
 constexpr uint32_t TMEM_COLS = 512;
 // y staging for the TMA reductions: per epilogue warp two buffers of
 // [32 rows x Y_COLS fp32]; 32 columns use the 128-byte swizzle (chunk j of
@@ -56,7 +83,7 @@ constexpr uint32_t TMEM_COLS = 512;
 template <bool PAIR>
 struct Cfg {
     static constexpr int ROWS_B = PAIR ? 128 : 256;      // weight rows unpacked per CTA per step
-    static constexpr int TPR = 256 / ROWS_B;              // unpack threads per weight row
+    static constexpr int TASKS = ROWS_B / 128;            // 128-row unpack tasks per step
     static constexpr int TILE = PAIR ? 256 : 128;         // tokens per work-unit tile
     static constexpr int IC = 256;                        // intermediate columns per work unit
     static constexpr int N_HT = IC / BK;                  // 64-column slices of h
@@ -77,7 +104,7 @@ struct Cfg {
     static constexpr int N_BARS = 2 * NA + 2 * NB + 2 * NR + 4 + 3;
     static constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + alignment slack
     static constexpr int EPI_ARRIVALS = PAIR ? 8 : 4;     // epilogue warps arriving per job
-    static constexpr int B_ARRIVALS = PAIR ? 2 * UNPACK_WARPS : UNPACK_WARPS;
+    static constexpr int B_ARRIVALS = (PAIR ? 2 : 1) * TASKS * UNPACK_GROUP_WARPS;
     static constexpr uint32_t IDESC = idesc_bf16_f32(PAIR ? 256 : 128, NJ);
     static_assert(SMEM_BYTES <= 232448, "shared memory budget of one block");
 };
@@ -115,18 +142,17 @@ __device__ __forceinline__ uint32_t sw128_row(int r) {
     return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
 }
 
-// Unpack 8 code words (4 bytes each, words wbeg..wbeg+nw-1 of the step's 32
-// code bytes) of one weight row into its swizzled bf16 row.  Word i holds
-// code bytes 4i..4i+3: low nibbles are weights 4i..4i+3 of the step, high
-// nibbles weights 32+4i..32+4i+3.  A code q becomes the float 1 + q/128
-// (low nibbles, at bits 16..19) or 1 + q/2048 (high nibbles, bits 12..15) by
-// OR-ing it into the bits of 1.0f; then d*sc*q - dmin*m = (S*d*sc)*f -
-// (S*d*sc + dmin*m) with S = 128 or 2048, one fused multiply-add per weight.
-// The constant is rounded once, an error below 2^-13 of one quantisation
-// step, far under the bf16 rounding of the result.
-template <int NW>
-__device__ __forceinline__ void unpack_words_to_smem(uint4 hd, const uint32_t (&w)[NW], int wbeg,
-                                                     int g, uint32_t row_addr, int row) {
+// Unpack the 8 code words (32 bytes) of one weight row and K step into its
+// swizzled bf16 row.  Word i holds code bytes 4i..4i+3: low nibbles are
+// weights 4i..4i+3 of the step, high nibbles weights 32+4i..32+4i+3.  A code
+// q becomes the float 1 + q/128 (low nibbles, at bits 16..19) or 1 + q/2048
+// (high nibbles, bits 12..15) by OR-ing it into the bits of 1.0f; then
+// d*sc*q - dmin*m = (S*d*sc)*f - (S*d*sc + dmin*m) with S = 128 or 2048, one
+// fused multiply-add per weight.  The constant is rounded once, an error
+// below 2^-13 of one quantisation step, far under the bf16 rounding of the
+// result.
+__device__ __forceinline__ void unpack_row_to_smem(uint4 hd, const uint32_t (&w)[8], int g,
+                                                   uint32_t row_addr, int row) {
     const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
     int sc0, m0, sc1, m1;
     q4k_scale_min(hd.y, hd.z, hd.w, 2 * g, sc0, m0);
@@ -136,9 +162,9 @@ __device__ __forceinline__ void unpack_words_to_smem(uint4 hd, const uint32_t (&
     const float a1 = 2048.0f * (d * (float)sc1);
     const float c1 = -(a1 + dmin * (float)m1);
     constexpr uint32_t ONE = 0x3F800000u, MLO = 0x000F0000u, MHI = 0x0000F000u;
-    uint32_t lo[2 * NW], hi[2 * NW];
+    uint32_t lo[16], hi[16];
 #pragma unroll
-    for (int i = 0; i < NW; ++i) {
+    for (int i = 0; i < 8; ++i) {
         const uint32_t x = w[i], xl8 = x << 8, xr8 = x >> 8, xl16 = x << 16, xr16 = x >> 16;
         const float l0 = fmaf(a0, __uint_as_float((xl16 & MLO) | ONE), c0);
         const float l1 = fmaf(a0, __uint_as_float((xl8 & MLO) | ONE), c0);
@@ -153,14 +179,13 @@ __device__ __forceinline__ void unpack_words_to_smem(uint4 hd, const uint32_t (&
         hi[2 * i] = pack_bf16x2(h0, h1);
         hi[2 * i + 1] = pack_bf16x2(h2, h3);
     }
-    // 16-byte chunk c holds weights 8c..8c+7; words wbeg.. cover chunks wbeg/2 ..
+    // 16-byte chunk c holds weights 8c..8c+7 (chunks 0-3 low nibbles, 4-7 high)
 #pragma unroll
-    for (int cc = 0; cc < NW / 2; ++cc) {
-        const int c = wbeg / 2 + cc;
-        st_shared_v4(row_addr + (((uint32_t)(c ^ (row & 7))) << 4), lo[4 * cc], lo[4 * cc + 1],
-                     lo[4 * cc + 2], lo[4 * cc + 3]);
-        st_shared_v4(row_addr + (((uint32_t)((c + 4) ^ (row & 7))) << 4), hi[4 * cc],
-                     hi[4 * cc + 1], hi[4 * cc + 2], hi[4 * cc + 3]);
+    for (int c = 0; c < 4; ++c) {
+        st_shared_v4(row_addr + (((uint32_t)(c ^ (row & 7))) << 4), lo[4 * c], lo[4 * c + 1],
+                     lo[4 * c + 2], lo[4 * c + 3]);
+        st_shared_v4(row_addr + (((uint32_t)((c + 4) ^ (row & 7))) << 4), hi[4 * c],
+                     hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
     }
 }
 
@@ -255,6 +280,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int role = warp_role(warp);
     const uint32_t rank = PAIR ? cluster_ctarank() : 0;
     const bool leader = rank == 0;
     const uint32_t s_h = smem_u32(smem + C::OFF_H);
@@ -279,7 +305,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int i = 0; i < C::NR; ++i) {
             mbar_init(&r_full[i], 1);
-            mbar_init(&r_empty[i], UNPACK_WARPS);
+            mbar_init(&r_empty[i], C::TASKS * UNPACK_GROUP_WARPS);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&t_full[i], 1);
@@ -299,7 +325,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         prefetch_tensormap(&maps.d_hdr);
         prefetch_tensormap(&maps.d_qs);
     }
-    if (warp == 1) {
+    if (role == ROLE_MMA) {
         if (PAIR) {
             tmem_alloc_pair(tmem_slot, TMEM_COLS);
             tmem_relinquish_pair();
@@ -322,11 +348,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int64_t rbH = (int64_t)(p.H / kQK) * kBlockBytes;
     const int64_t rbI = q4k_row_bytes(p.I);
 
-    if (warp == 0) {
-        // ------------- TMA producer: x tiles and packed weights -------------
+    if (role == ROLE_WPROD) {
+        // ------------- TMA producer: packed weights -------------
         if (lane == 0) {
-            uint32_t ai = 0, aph = 0, ri = 0, rph = 0;
-            uint32_t a_issued = 0, r_issued = 0;
+            uint32_t ri = 0, rph = 0, r_issued = 0;
             bool ok = true;
             for (int u = group; u < n_units && ok; u += n_groups) {
                 const Unit un = make_unit<PAIR>(p, u, n_tiles, rank);
@@ -336,21 +361,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                 src.start();
                 for (int st = 0; st < steps; ++st, src.advance(un)) {
                     src.locate(un);
-                    if (src.gu) {
-                        if (!mbar_wait(&a_empty[ai], aph ^ 1, abort_flag, p.err)) { ok = false; break; }
-                        void *dst = smem + C::OFF_A + ai * A_BYTES;
-                        if (PAIR) {
-                            // both CTAs' tiles complete on the leader's barrier
-                            if (leader) mbar_arrive_expect_tx(&a_full[ai], 2 * A_BYTES);
-                            tma_load_2d_pair(dst, &maps.x, mapa_shared(smem_u32(&a_full[ai]), 0),
-                                             src.ks * BK, un.tile.row_start);
-                        } else {
-                            mbar_arrive_expect_tx(&a_full[ai], A_BYTES);
-                            tma_load_2d(dst, &maps.x, &a_full[ai], src.ks * BK, un.tile.row_start);
-                        }
-                        ++a_issued;
-                        if (++ai == C::NA) { ai = 0; aph ^= 1; }
-                    }
                     if (!mbar_wait(&r_empty[ri], rph ^ 1, abort_flag, p.err)) { ok = false; break; }
                     mbar_arrive_expect_tx(&r_full[ri], C::R_BYTES);
                     uint8_t *rs = smem + C::OFF_R + ri * C::R_BYTES;
@@ -380,8 +390,39 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             // Before the block may exit, every load issued here must have
             // landed: wait (bounded) for the full barriers of the last stages
-            // issued (a phase that completed long ago passes at once).  In a
-            // pair the x tiles complete on the leader's barriers, which the
+            // issued (a phase that completed long ago passes at once).
+            for (uint32_t i = 0; i < (uint32_t)C::NR && i < r_issued; ++i) {
+                if (ri == 0) { ri = C::NR; rph ^= 1; }
+                --ri;
+                mbar_wait(&r_full[ri], rph, nullptr, p.err, kWaitBudgetCycles / 8);
+            }
+        }
+    } else if (role == ROLE_XPROD) {
+        // ------------- TMA producer: x tiles of the gate/up steps -------------
+        if (lane == 0) {
+            uint32_t ai = 0, aph = 0, a_issued = 0;
+            bool ok = true;
+            for (int u = group; u < n_units && ok; u += n_groups) {
+                const Unit un = make_unit<PAIR>(p, u, n_tiles, rank);
+                for (int s = 0; s < un.n_gu && ok; ++s) {
+                    for (int ks = 0; ks < un.ks_gu; ++ks) {
+                        if (!mbar_wait(&a_empty[ai], aph ^ 1, abort_flag, p.err)) { ok = false; break; }
+                        void *dst = smem + C::OFF_A + ai * A_BYTES;
+                        if (PAIR) {
+                            // both CTAs' tiles complete on the leader's barrier
+                            if (leader) mbar_arrive_expect_tx(&a_full[ai], 2 * A_BYTES);
+                            tma_load_2d_pair(dst, &maps.x, mapa_shared(smem_u32(&a_full[ai]), 0),
+                                             ks * BK, un.tile.row_start);
+                        } else {
+                            mbar_arrive_expect_tx(&a_full[ai], A_BYTES);
+                            tma_load_2d(dst, &maps.x, &a_full[ai], ks * BK, un.tile.row_start);
+                        }
+                        ++a_issued;
+                        if (++ai == C::NA) { ai = 0; aph ^= 1; }
+                    }
+                }
+            }
+            // In a pair the x tiles complete on the leader's barriers, which the
             // leader's issuer has waited for before its final MMAs.
             if (!PAIR || leader) {
                 for (uint32_t i = 0; i < (uint32_t)C::NA && i < a_issued; ++i) {
@@ -390,13 +431,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     mbar_wait(&a_full[ai], aph, nullptr, p.err, kWaitBudgetCycles / 8);
                 }
             }
-            for (uint32_t i = 0; i < (uint32_t)C::NR && i < r_issued; ++i) {
-                if (ri == 0) { ri = C::NR; rph ^= 1; }
-                --ri;
-                mbar_wait(&r_full[ri], rph, nullptr, p.err, kWaitBudgetCycles / 8);
-            }
         }
-    } else if (warp == 1) {
+    } else if (role == ROLE_MMA) {
         // ---------------- MMA issuer (the pair's leader only) ----------------
         if (lane == 0 && leader) {
             uint32_t ai = 0, aph = 0, bi = 0, bph = 0, jc = 0, uc = 0;
@@ -459,59 +495,57 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (PAIR) tc_commit_pair(drain); else tc_commit(drain);
             mbar_wait(drain, 0, nullptr, p.err, kWaitBudgetCycles / 8);
         }
-    } else if (warp < EPI_WARP0) {
-        // ------------- weight unpackers (8 warps) -------------
-        const int ut = threadIdx.x - 64;               // 0..255
-        const int row = ut / C::TPR;                    // weight row of this thread
-        const int part = ut % C::TPR;                   // which code words (pairs: half)
-        uint32_t bi = 0, bph = 0, ri = 0, rph = 0;
+    } else if (role == ROLE_UNPACK) {
+        // ------------- weight unpackers (three groups of 4 warps) -------------
+        // A step's weight rows are split into 128-row tasks (one per step on
+        // CTA pairs, two on single CTAs); the groups take the tasks in turn,
+        // counted over every unit of this block, one thread per row.
+        const int uw = unpack_index(warp);
+        const uint32_t grp = (uint32_t)(uw / UNPACK_GROUP_WARPS);
+        const int trow = (uw % UNPACK_GROUP_WARPS) * 32 + lane;   // row within the task
+        uint32_t bi = 0, bph = 0, ri = 0, rph = 0, gt = 0;
         bool ok = true;
         // bank-conflict-free order of the 16-byte reads of the 32-byte code rows
-        const int qfirst = (row >> 2) & 1;
+        const int qfirst = (trow >> 2) & 1;
         for (int u = group; u < n_units && ok; u += n_groups) {
             const Unit un = make_unit<PAIR>(p, u, n_tiles, rank);
-            const int e = un.tile.expert;
             const int steps = un.n_gu * un.ks_gu + un.n_y * un.ks_y;
             StepSrc src;
             src.start();
-            for (int st = 0; st < steps; ++st, src.advance(un)) {
-                src.locate(un);
-                const int grow = PAIR ? row : (row & 127);          // gate/up row within the job
-                const bool zero = src.gu && (un.i0 + src.s * GU_ROWS + grow >= p.I);
-                if (!mbar_wait(&r_full[ri], rph, abort_flag, p.err)) { ok = false; break; }
-                uint4 hd = make_uint4(0, 0, 0, 0), q0 = hd, q1 = hd;
-                if (!zero) {
-                    const uint32_t rs = s_r + ri * C::R_BYTES;
-                    hd = ld_shared_v4(rs + row * 16);
-                    const uint32_t qa = rs + C::R_HDR + row * 32;
-                    if (C::TPR == 1) {
+            for (int st = 0; st < steps && ok; ++st, src.advance(un)) {
+#pragma unroll
+                for (int task = 0; task < C::TASKS; ++task, ++gt) {
+                    if (gt % UNPACK_GROUPS != grp) continue;
+                    const int row = task * 128 + trow;              // weight row of this thread
+                    src.locate(un);
+                    const int grow = PAIR ? row : (row & 127);      // gate/up row within the job
+                    const bool zero = src.gu && (un.i0 + src.s * GU_ROWS + grow >= p.I);
+                    if (!mbar_wait(&r_full[ri], rph, abort_flag, p.err)) { ok = false; break; }
+                    uint4 hd = make_uint4(0, 0, 0, 0), q0 = hd, q1 = hd;
+                    if (!zero) {
+                        const uint32_t rs = s_r + ri * C::R_BYTES;
+                        hd = ld_shared_v4(rs + row * 16);
+                        const uint32_t qa = rs + C::R_HDR + row * 32;
                         const uint4 first = ld_shared_v4(qa + 16 * qfirst);
                         const uint4 second = ld_shared_v4(qa + 16 * (qfirst ^ 1));
                         q0 = qfirst ? second : first;
                         q1 = qfirst ? first : second;
-                    } else {
-                        q0 = ld_shared_v4(qa + 16 * part);
                     }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&r_empty[ri]);
-                if (++ri == C::NR) { ri = 0; rph ^= 1; }
-                if (!mbar_wait(&b_empty[bi], bph ^ 1, abort_flag, p.err)) { ok = false; break; }
-                const uint32_t rb = s_b + bi * C::B_BYTES + sw128_row(row);
-                if (C::TPR == 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&r_empty[ri]);
+                    if (!mbar_wait(&b_empty[bi], bph ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    const uint32_t rb = s_b + bi * C::B_BYTES + sw128_row(row);
                     const uint32_t w8[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                    unpack_words_to_smem<8>(hd, w8, 0, src.g, rb, row);
-                } else {
-                    const uint32_t w4[4] = {q0.x, q0.y, q0.z, q0.w};
-                    unpack_words_to_smem<4>(hd, w4, 4 * part, src.g, rb, row);
+                    unpack_row_to_smem(hd, w8, src.g, rb, row);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) arrive_leader(&b_full[bi]);
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) arrive_leader(&b_full[bi]);
+                if (++ri == C::NR) { ri = 0; rph ^= 1; }
                 if (++bi == C::NB) { bi = 0; bph ^= 1; }
             }
         }
-    } else {
+    } else if (role == ROLE_EPI) {
         // ---------------- epilogue (4 warps) ----------------
         const int q = warp & 3;                      // TMEM lane quadrant of this warp
         const int row = q * 32 + lane;               // token row within the CTA's tile
@@ -529,15 +563,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (s == 0 && !mbar_wait(h_empty, (uc & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
                 const uint32_t t_addr = tmem_base + lane_bits + slot * NJ;
 #pragma unroll 1
-                for (int c = 0; c < GU_ROWS; c += 32) {
-                    uint32_t gr[32], ur[32];
-                    tmem_ld_32x32b_x32(t_addr + c, gr);
-                    tmem_ld_32x32b_x32(t_addr + GU_ROWS + c, ur);
+                for (int c = 0; c < GU_ROWS; c += 16) {
+                    uint32_t gr[16], ur[16];
+                    tmem_ld_32x32b_x16(t_addr + c, gr);
+                    tmem_ld_32x32b_x16(t_addr + GU_ROWS + c, ur);
                     tmem_ld_wait(gr);
                     tmem_ld_wait(ur);
-                    uint32_t hw[16];
+                    uint32_t hw[8];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
+                    for (int j = 0; j < 8; ++j) {
                         const float g0 = __uint_as_float(gr[2 * j]), g1 = __uint_as_float(gr[2 * j + 1]);
                         const float u0 = __uint_as_float(ur[2 * j]), u1 = __uint_as_float(ur[2 * j + 1]);
                         const float h0 = __fdividef(g0 * u0, 1.0f + __expf(-g0));
@@ -548,7 +582,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t tile_base = s_h + (col >> 6) * HT_BYTES + sw128_row(row);
                     const int cb = (col & 63) >> 3;                // first 16-byte chunk
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
+                    for (int j = 0; j < 2; ++j)
                         st_shared_v4(tile_base + ((uint32_t)((cb + j) ^ (row & 7)) << 4), hw[4 * j],
                                      hw[4 * j + 1], hw[4 * j + 2], hw[4 * j + 3]);
                 }
@@ -640,7 +674,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_before();
     __syncthreads();
     if (PAIR) cluster_sync_all();
-    if (warp == 1) {
+    if (role == ROLE_MMA) {
         __syncwarp();
         tc_fence_after();
         if (PAIR) tmem_dealloc_pair(tmem_base, TMEM_COLS);
