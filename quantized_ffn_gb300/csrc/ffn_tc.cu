@@ -3,8 +3,8 @@
 // What it computes, per (token tile, intermediate chunk) work unit:
 //   for each 128-row slice s of the chunk:
 //       [G | U] = X_tile . [W_gate rows ; W_up rows]^T        (tcgen05, TMEM)
-//       h[:, s] = bf16( silu(G) * U )                           (epilogue -> SMEM)
-//   for each 256-column slice n of the output:
+//       h[:, s] = bf16( silu(G) * U )                           (epilogue)
+//   for each 128-column slice n of the output:
 //       Y = h . W_down[n rows, chunk cols]^T                   (tcgen05, TMEM)
 //       y[token, n cols] += Y                                   (fp32 reductions in L2)
 // This is the producer/consumer interleave along the intermediate dimension
@@ -21,21 +21,28 @@
 // versus the stubborn ones"); accumulators live in tensor memory, not in
 // registers, which removes the register-pressure problem at its root.
 //
-// Block roles (20 warps; warp w runs on sub-partition w % 4):
-//   warp 1      TMEM allocator and single-thread MMA issuer
-//   warp 5      TMA producer: packed Q4_K weight slices (block headers and
-//               the code bytes of one 64-wide K step) into a ring
-//   warp 9      TMA producer: x tiles [128 x 64] bf16, 128-byte swizzle
-//   warps 0, 13, 2, 3  epilogue for TMEM lane quadrants 0-3: TMEM ->
-//               registers; SwiGLU -> h in SMEM, or the down-projection
-//               tile -> y
-//   warps 4, 6-8, 10-12, 14-16, 18, 19  weight unpackers: packed slices ->
-//               bf16 tiles [rows x 64], 128-byte swizzle
-//   warp 17     idle
-// The two producers are separate threads so that the weight ring can run as
-// far ahead as its depth allows, independently of the x ring.
-// Two TMEM accumulator slots of 256 columns each alternate between jobs, so
-// the epilogue of one job overlaps the MMAs of the next.
+// Schedule.  The y reductions of a unit (4 MB for 256 tokens) leave the SM
+// through a port of about 32 bytes per cycle, so a unit's down projection
+// cannot keep pace with its own MMAs.  The MMA program therefore interleaves
+// the down-projection jobs of unit i with the gate/up steps of unit i+1:
+//   G(0) | Y(0,0) G(1)... Y(0,1) G(1)... ... Y(0,31) G(1)... | Y(1,0) G(2)... |
+// (each Y job is followed by an equal share of the next unit's gate/up
+// steps), so the y traffic is spread over the whole run.  TMEM holds one
+// gate/up accumulator (256 columns), one down-projection accumulator (128
+// columns) and a stash of the next unit's h (128 columns of bf16 pairs),
+// copied into shared memory once the current unit's down projection has
+// consumed the previous h.
+//
+// Block roles (24 warps; warp w runs on sub-partition w % 4):
+//   warps 0-3   epilogue for TMEM lane quadrants 0-3: SwiGLU -> h stash,
+//               h stash -> shared memory, down-projection tile -> y
+//   warp 4      TMEM allocator and MMA issuer (one elected lane issues)
+//   warp 5      TMA producer: packed Q4_K weight slices into a ring
+//   warp 6      TMA producer: x tiles [128 x 64] bf16, 128-byte swizzle
+//   warps 8-19  weight unpackers: packed slices -> bf16 tiles, 128-byte
+//               swizzle
+//   warps 7, 20-23  idle
+// Every role walks the same step program (Prog below) in the same order.
 #include <cudaTypedefs.h>
 
 #include "zffn_internal.cuh"
@@ -44,46 +51,62 @@ namespace zffn {
 namespace tc {
 
 constexpr int BM = 128;                  // token rows per CTA per tile (UMMA M per CTA)
-constexpr int BK = 64;                   // K per pipeline step (128 bytes of bf16)
+constexpr int BK = 64;                   // K per gate/up step (128 bytes of bf16)
+constexpr int YK = 128;                  // K per down-projection step
 constexpr int GU_ROWS = 128;             // intermediate rows per gate/up job
-constexpr int NJ = 256;                  // UMMA N of every job
+constexpr int NJ_GU = 256;               // UMMA N of a gate/up job (128 gate + 128 up rows)
+constexpr int NJ_Y = 128;                // UMMA N of a down-projection job (output columns)
 constexpr int A_BYTES = BM * BK * 2;     // 16 KB x tile per CTA
 constexpr int HT_BYTES = BM * BK * 2;    // one 64-column slice of h: 16 KB
-// Warp roles.  Warp w is scheduled by sub-partition w % 4.  The MMA issuer
-// (warp 1) shares its sub-partition only with the two TMA producers and one
-// epilogue warp: an arithmetic-heavy warp beside it delays its tcgen05
-// issue and leaves the tensor cores idle (measured: one such warp costs
-// about a fifth of the MMA rate).  The epilogue needs one warp per
-// sub-partition, because a warp reads only the TMEM lane quadrant w % 4.
-constexpr int NUM_WARPS = 20;
+constexpr uint32_t COL_GU = 0, COL_Y = 256, COL_STASH = 384;   // TMEM columns
+// Warp roles.  Warp w is scheduled by sub-partition w % 4.  The epilogue
+// needs one warp per sub-partition, because a warp reads only the TMEM lane
+// quadrant w % 4: warps 0-3.  The unpackers (warps 8-19, three groups of one
+// warp per sub-partition) spread the arithmetic evenly over the four
+// sub-partitions.  The MMA issuer walks its program as a whole warp with
+// warp-uniform control flow and descriptors, so its tcgen05.mma issue stays
+// short even next to arithmetic-heavy warps.
+//
+// Groups and B stages: group k takes the tasks with index k modulo
+// UNPACK_GROUPS, and the waits on a stage's "empty" barrier test a phase
+// parity only.  A group's wait for phase n of a stage is unambiguous only if
+// phase n-1 has completed, which its own previous wait guarantees exactly
+// when UNPACK_GROUPS <= the stages a CTA pair cycles through (NB); on a
+// single CTA two tasks share a step, so each group keeps to one stage.
+constexpr int NUM_WARPS = 24;
 constexpr int THREADS = NUM_WARPS * 32;
-constexpr int UNPACK_GROUP_WARPS = 4;    // 128 weight rows, one thread per row
-constexpr int UNPACK_GROUPS = 3;         // groups take 128-row tasks in turn
+constexpr int UNPACK_GROUP_WARPS = 4;    // one 128-thread task
+constexpr int UNPACK_GROUPS = 3;         // groups take tasks in turn
 enum Role { ROLE_EPI, ROLE_MMA, ROLE_WPROD, ROLE_XPROD, ROLE_UNPACK, ROLE_IDLE };
 __device__ __forceinline__ int warp_role(int w) {
-    if (w == 1) return ROLE_MMA;
+    if (w < 4) return ROLE_EPI;
+    if (w == 4) return ROLE_MMA;
     if (w == 5) return ROLE_WPROD;
-    if (w == 9) return ROLE_XPROD;
-    if (w == 0 || w == 2 || w == 3 || w == 13) return ROLE_EPI;
-    if ((w & 3) == 1) return ROLE_IDLE;
-    return ROLE_UNPACK;
+    if (w == 6) return ROLE_XPROD;
+    if (w >= 8 && w < 8 + UNPACK_GROUPS * UNPACK_GROUP_WARPS) return ROLE_UNPACK;
+    return ROLE_IDLE;
 }
-// 0..11 over the unpack warps 4, 6, 7, 8, 10, 11, 12, 14, 15, 16, 18, 19
-__device__ __forceinline__ int unpack_index(int w) {
-    return ((w >> 2) - 1) * 3 + ((w & 3) == 0 ? 0 : (w & 3) - 1);
-}
+// 0..11 over the unpack warps 8..19
+__device__ __forceinline__ int unpack_index(int w) { return w - 8; }
 constexpr uint32_t TMEM_COLS = 512;
 // y staging for the TMA reductions: per epilogue warp two buffers of
 // [32 rows x Y_COLS fp32]; 32 columns use the 128-byte swizzle (chunk j of
 // row r at j ^ (r % 8)), 16 columns the 64-byte swizzle (j ^ (r/2 % 4)).
 
 // Geometry of one kernel variant.  PAIR: a cluster of two CTAs shares each
-// 256-token tile; one UMMA of M = 256 covers both CTAs' rows, and the N = 256
-// weight rows of every step are split between the CTAs (each unpacks 128).
+// 256-token tile; one UMMA of M = 256 covers both CTAs' rows, and the weight
+// rows of every step are split between the CTAs.
+//   gate/up step: ROWS_B weight rows x 64 K per CTA (pair: the leader the
+//                 gate rows, its peer the up rows)
+//   down step:    ROWS_Y W_down rows x 128 K per CTA, stored as two
+//                 64-column halves
+// Both kinds fill one B stage and take TASKS 128-thread unpack tasks, one
+// 64-weight slice per thread.
 template <bool PAIR>
 struct Cfg {
-    static constexpr int ROWS_B = PAIR ? 128 : 256;      // weight rows unpacked per CTA per step
-    static constexpr int TASKS = ROWS_B / 128;            // 128-row unpack tasks per step
+    static constexpr int ROWS_B = PAIR ? 128 : 256;
+    static constexpr int ROWS_Y = ROWS_B / 2;
+    static constexpr int TASKS = ROWS_B / 128;
     static constexpr int TILE = PAIR ? 256 : 128;         // tokens per work-unit tile
     static constexpr int IC = 256;                        // intermediate columns per work unit
     static constexpr int N_HT = IC / BK;                  // 64-column slices of h
@@ -92,31 +115,39 @@ struct Cfg {
     static constexpr int NR = PAIR ? 5 : 3;               // packed-weight stages
     static constexpr int Y_COLS = PAIR ? 32 : 16;
     static constexpr int Y_BUF = 32 * Y_COLS * 4;
-    static constexpr int B_BYTES = ROWS_B * BK * 2;
-    static constexpr int R_HDR = ROWS_B * 16;
-    static constexpr int R_BYTES = ROWS_B * 48;
+    static constexpr int B_BYTES = ROWS_B * BK * 2;       // = 2 * ROWS_Y * 128
+    static constexpr int R_HDR_GU = ROWS_B * 16;          // gate/up: headers, then 32 code bytes a row
+    static constexpr int R_HDR_Y = ROWS_Y * 16;           // down: headers, then 64 code bytes a row
+    static constexpr int R_BYTES_GU = ROWS_B * 48;
+    static constexpr int R_BYTES_Y = ROWS_Y * 80;
+    static constexpr int R_BYTES = R_BYTES_GU;            // stage size (the larger)
     static constexpr int OFF_H = 0;
     static constexpr int OFF_A = OFF_H + N_HT * HT_BYTES;
     static constexpr int OFF_B = OFF_A + NA * A_BYTES;
     static constexpr int OFF_R = OFF_B + NB * B_BYTES;
     static constexpr int OFF_Y = ((OFF_R + NR * R_BYTES) + 1023) & ~1023;
     static constexpr int OFF_BAR = OFF_Y + 4 * 2 * Y_BUF;
-    static constexpr int N_BARS = 2 * NA + 2 * NB + 2 * NR + 4 + 3;
+    static constexpr int N_BARS = 2 * NA + 2 * NB + 2 * NR + 7;
     static constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + alignment slack
     static constexpr int EPI_ARRIVALS = PAIR ? 8 : 4;     // epilogue warps arriving per job
     static constexpr int B_ARRIVALS = (PAIR ? 2 : 1) * TASKS * UNPACK_GROUP_WARPS;
-    static constexpr uint32_t IDESC = idesc_bf16_f32(PAIR ? 256 : 128, NJ);
+    static constexpr uint32_t IDESC_GU = idesc_bf16_f32(PAIR ? 256 : 128, NJ_GU);
+    static constexpr uint32_t IDESC_Y = idesc_bf16_f32(PAIR ? 256 : 128, NJ_Y);
+    static_assert(R_BYTES_Y <= R_BYTES, "down-step slice fits a weight stage");
+    static_assert(!PAIR || UNPACK_GROUPS <= NB, "parity waits on B stages stay unambiguous");
+    static_assert(PAIR || UNPACK_GROUPS <= 2 * NB, "parity waits on B stages stay unambiguous");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget of one block");
 };
 
 // Tensor maps: x tiles, y tiles, and the packed weights viewed as byte
 // matrices [rows][row bytes] with two box shapes each: the 16-byte block
-// headers and the 32 code bytes of one 64-wide K step.
+// headers and the code bytes of one step (32 for a gate/up step of 64
+// weights, 64 for a down step of 128).
 struct Maps {
     CUtensorMap x;
-    CUtensorMap y;                          // fp32 [T][H], boxes of [32 rows x 32 cols]
+    CUtensorMap y;                          // fp32 [T][H], boxes of [32 rows x Y_COLS]
     CUtensorMap g_hdr, g_qs, u_hdr, u_qs;   // boxes of 128 rows
-    CUtensorMap d_hdr, d_qs;                // boxes of ROWS_B rows
+    CUtensorMap d_hdr, d_qs;                // boxes of ROWS_Y rows
 };
 
 struct Params {
@@ -203,10 +234,6 @@ struct Unit {
     Tile tile;    // the CTA's own token rows
     int i0;       // first intermediate column of the chunk
     int ic;       // columns in this chunk (multiple of 64)
-    int n_gu;     // gate/up jobs
-    int ks_gu;    // K steps per gate/up job
-    int ks_y;     // K steps per down job
-    int n_y;      // down jobs
 };
 
 template <bool PAIR>
@@ -226,38 +253,52 @@ __device__ __forceinline__ Unit make_unit(const Params &p, int u, int n_tiles, u
     }
     un.i0 = chunk * Cfg<PAIR>::IC;
     un.ic = min(Cfg<PAIR>::IC, p.I - un.i0);
-    un.n_gu = (un.ic + GU_ROWS - 1) / GU_ROWS;
-    un.ks_gu = p.H / BK;
-    un.ks_y = un.ic / BK;
-    un.n_y = p.H / NJ;
     return un;
 }
 
-// Walks the K steps of a unit in order (gate/up jobs, then down jobs) and
-// says where each step reads its packed weights.
-struct StepSrc {
-    bool gu;        // gate/up step (x tile too) or down step
-    int ks;         // K step inside the job
-    int s;          // gate/up job or down job index
-    int xcol;       // byte column of the block header
-    int g;          // 64-wide group inside the block (code bytes 32g..32g+31)
-    __device__ __forceinline__ void start() { gu = true; ks = 0; s = 0; }
-    __device__ __forceinline__ void locate(const Unit &un) {
-        if (gu) {
-            xcol = (ks >> 2) * kBlockBytes;
-            g = ks & 3;
-        } else {
-            const int col = un.i0 + ks * BK;
-            xcol = (col >> 8) * kBlockBytes;
-            g = (col & 255) >> 6;
-        }
+// The step program of one block, walked in the same order by every role.
+// Units k = 0..m-1 of the block (global unit group + k * n_groups).  First
+// the gate/up steps of unit 0 (two jobs of ksg steps); then, for each unit
+// k, its NY down jobs (YS steps each), each followed by the next GU_PER_Y
+// gate/up steps of unit k+1.  With a 256-wide chunk a unit has 2 * H/64
+// gate/up steps and H/128 down jobs, so GU_PER_Y = 4 spreads the next unit's
+// gate/up steps exactly over the current unit's down jobs.  The walk is
+// incremental (no divisions): the MMA issuer's scalar work per step sits on
+// the critical path of the tensor pipe.
+constexpr int GU_PER_Y = 4;
+struct Prog {
+    int m, NY, YS, ksg;
+    int blk;        // -1: leading gate/up steps of unit 0; k >= 0: down jobs of unit k
+    int n, ys;      // down job and step within it
+    int s, ks;      // gate/up job and step (of the unit whose gate/up steps run)
+    int gb;         // gate/up steps left in the current share
+    bool gu, done;
+    __device__ __forceinline__ void start(int m_, int ksg_, int NY_, int YS_) {
+        m = m_; ksg = ksg_; NY = NY_; YS = YS_;
+        blk = -1; n = 0; ys = 0; s = 0; ks = 0; gb = 2 * ksg; gu = true; done = m <= 0;
     }
-    __device__ __forceinline__ void advance(const Unit &un) {
+    // index (0..m-1) of the unit the current step belongs to
+    __device__ __forceinline__ int unit() const { return gu ? blk + 1 : blk; }
+    __device__ __forceinline__ bool gu_last() const { return ks == ksg - 1; }
+    __device__ __forceinline__ void next_job() {
+        gu = false;
+        ys = 0;
+        if (++n < NY) return;
+        n = 0;
+        s = 0;
+        ks = 0;
+        if (++blk >= m) done = true;
+    }
+    __device__ __forceinline__ void next() {
         if (gu) {
-            if (++ks == un.ks_gu) { ks = 0; if (++s == un.n_gu) { s = 0; gu = false; } }
-        } else if (++ks == un.ks_y) {
-            ks = 0;
-            ++s;
+            if (++ks == ksg) { ks = 0; ++s; }
+            if (--gb > 0) return;
+            if (blk < 0) { blk = 0; n = 0; ys = 0; s = 0; ks = 0; gu = false; return; }
+            next_job();
+        } else {
+            if (++ys < YS) return;
+            if (blk + 1 < m) { gu = true; gb = GU_PER_Y; return; }
+            next_job();
         }
     }
 };
@@ -274,8 +315,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t *a_full = bars, *a_empty = bars + C::NA;
     uint64_t *b_full = bars + 2 * C::NA, *b_empty = b_full + C::NB;
     uint64_t *r_full = b_empty + C::NB, *r_empty = r_full + C::NR;
-    uint64_t *t_full = r_empty + C::NR, *t_empty = t_full + 2;
-    uint64_t *h_full = t_empty + 2, *h_empty = h_full + 1, *drain = h_full + 2;
+    uint64_t *g_full = r_empty + C::NR, *g_empty = g_full + 1;
+    uint64_t *y_full = g_full + 2, *y_empty = g_full + 3;
+    uint64_t *h_full = g_full + 4, *h_empty = g_full + 5, *drain = g_full + 6;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::N_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -307,10 +349,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&r_full[i], 1);
             mbar_init(&r_empty[i], C::TASKS * UNPACK_GROUP_WARPS);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&t_full[i], 1);
-            mbar_init(&t_empty[i], C::EPI_ARRIVALS);
-        }
+        mbar_init(g_full, 1);
+        mbar_init(g_empty, C::EPI_ARRIVALS);
+        mbar_init(y_full, 1);
+        mbar_init(y_empty, C::EPI_ARRIVALS);
         mbar_init(h_full, C::EPI_ARRIVALS);
         mbar_init(h_empty, 1);
         mbar_init(drain, 1);
@@ -345,48 +387,56 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int n_units = n_tiles * n_chunks;
     const int group = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
     const int n_groups = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-    const int64_t rbH = (int64_t)(p.H / kQK) * kBlockBytes;
-    const int64_t rbI = q4k_row_bytes(p.I);
+    const int m_units = group < n_units ? (n_units - group + n_groups - 1) / n_groups : 0;
+    // Gate/up steps of a unit, steps of a K = 128 down job, down jobs.  The
+    // chunk width is IC for every unit (I is a multiple of 256).
+    const int ks_gu = p.H / BK;
+    const int YS = C::IC / YK;
+    const int NY = p.H / NJ_Y;
+    auto unit_of = [&](int k) { return make_unit<PAIR>(p, group + k * n_groups, n_tiles, rank); };
 
     if (role == ROLE_WPROD) {
         // ------------- TMA producer: packed weights -------------
         if (lane == 0) {
             uint32_t ri = 0, rph = 0, r_issued = 0;
-            bool ok = true;
-            for (int u = group; u < n_units && ok; u += n_groups) {
-                const Unit un = make_unit<PAIR>(p, u, n_tiles, rank);
+            Prog pg;
+            pg.start(m_units, ks_gu, NY, YS);
+            int cur = -1;
+            Unit un{};
+            for (; !pg.done; pg.next()) {
+                if (pg.unit() != cur) { cur = pg.unit(); un = unit_of(cur); }
                 const int e = un.tile.expert;
-                const int steps = un.n_gu * un.ks_gu + un.n_y * un.ks_y;
-                StepSrc src;
-                src.start();
-                for (int st = 0; st < steps; ++st, src.advance(un)) {
-                    src.locate(un);
-                    if (!mbar_wait(&r_empty[ri], rph ^ 1, abort_flag, p.err)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&r_full[ri], C::R_BYTES);
-                    uint8_t *rs = smem + C::OFF_R + ri * C::R_BYTES;
-                    const int qcol = src.xcol + 16 + 32 * src.g;
-                    if (src.gu) {
-                        const int row = e * p.I + un.i0 + src.s * GU_ROWS;
-                        if (PAIR) {
-                            // the leader unpacks the gate rows, its peer the up rows
-                            const CUtensorMap *mh = leader ? &maps.g_hdr : &maps.u_hdr;
-                            const CUtensorMap *mq = leader ? &maps.g_qs : &maps.u_qs;
-                            tma_load_2d(rs, mh, &r_full[ri], src.xcol, row);
-                            tma_load_2d(rs + C::R_HDR, mq, &r_full[ri], qcol, row);
-                        } else {
-                            tma_load_2d(rs, &maps.g_hdr, &r_full[ri], src.xcol, row);
-                            tma_load_2d(rs + 128 * 16, &maps.u_hdr, &r_full[ri], src.xcol, row);
-                            tma_load_2d(rs + C::R_HDR, &maps.g_qs, &r_full[ri], qcol, row);
-                            tma_load_2d(rs + C::R_HDR + 128 * 32, &maps.u_qs, &r_full[ri], qcol, row);
-                        }
+                if (!mbar_wait(&r_empty[ri], rph ^ 1, abort_flag, p.err)) break;
+                uint8_t *rs = smem + C::OFF_R + ri * C::R_BYTES;
+                if (pg.gu) {
+                    const int s = pg.s, ks = pg.ks;
+                    const int xcol = (ks >> 2) * kBlockBytes;
+                    const int qcol = xcol + 16 + 32 * (ks & 3);
+                    const int row = e * p.I + un.i0 + s * GU_ROWS;
+                    mbar_arrive_expect_tx(&r_full[ri], C::R_BYTES_GU);
+                    if (PAIR) {
+                        // the leader unpacks the gate rows, its peer the up rows
+                        const CUtensorMap *mh = leader ? &maps.g_hdr : &maps.u_hdr;
+                        const CUtensorMap *mq = leader ? &maps.g_qs : &maps.u_qs;
+                        tma_load_2d(rs, mh, &r_full[ri], xcol, row);
+                        tma_load_2d(rs + C::R_HDR_GU, mq, &r_full[ri], qcol, row);
                     } else {
-                        const int row = e * p.H + src.s * NJ + (int)rank * C::ROWS_B;
-                        tma_load_2d(rs, &maps.d_hdr, &r_full[ri], src.xcol, row);
-                        tma_load_2d(rs + C::R_HDR, &maps.d_qs, &r_full[ri], qcol, row);
+                        tma_load_2d(rs, &maps.g_hdr, &r_full[ri], xcol, row);
+                        tma_load_2d(rs + 128 * 16, &maps.u_hdr, &r_full[ri], xcol, row);
+                        tma_load_2d(rs + C::R_HDR_GU, &maps.g_qs, &r_full[ri], qcol, row);
+                        tma_load_2d(rs + C::R_HDR_GU + 128 * 32, &maps.u_qs, &r_full[ri], qcol, row);
                     }
-                    ++r_issued;
-                    if (++ri == C::NR) { ri = 0; rph ^= 1; }
+                } else {
+                    // W_down rows n*128 + rank*ROWS_Y .. +ROWS_Y, chunk columns
+                    // [i0 + 128*ys, +128): one Q4_K block per row, code bytes 64*ys..
+                    const int xcol = (un.i0 >> 8) * kBlockBytes;
+                    const int row = e * p.H + pg.n * NJ_Y + (int)rank * C::ROWS_Y;
+                    mbar_arrive_expect_tx(&r_full[ri], C::R_BYTES_Y);
+                    tma_load_2d(rs, &maps.d_hdr, &r_full[ri], xcol, row);
+                    tma_load_2d(rs + C::R_HDR_Y, &maps.d_qs, &r_full[ri], xcol + 16 + 64 * pg.ys, row);
                 }
+                ++r_issued;
+                if (++ri == C::NR) { ri = 0; rph ^= 1; }
             }
             // Before the block may exit, every load issued here must have
             // landed: wait (bounded) for the full barriers of the last stages
@@ -401,26 +451,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------- TMA producer: x tiles of the gate/up steps -------------
         if (lane == 0) {
             uint32_t ai = 0, aph = 0, a_issued = 0;
-            bool ok = true;
-            for (int u = group; u < n_units && ok; u += n_groups) {
-                const Unit un = make_unit<PAIR>(p, u, n_tiles, rank);
-                for (int s = 0; s < un.n_gu && ok; ++s) {
-                    for (int ks = 0; ks < un.ks_gu; ++ks) {
-                        if (!mbar_wait(&a_empty[ai], aph ^ 1, abort_flag, p.err)) { ok = false; break; }
-                        void *dst = smem + C::OFF_A + ai * A_BYTES;
-                        if (PAIR) {
-                            // both CTAs' tiles complete on the leader's barrier
-                            if (leader) mbar_arrive_expect_tx(&a_full[ai], 2 * A_BYTES);
-                            tma_load_2d_pair(dst, &maps.x, mapa_shared(smem_u32(&a_full[ai]), 0),
-                                             ks * BK, un.tile.row_start);
-                        } else {
-                            mbar_arrive_expect_tx(&a_full[ai], A_BYTES);
-                            tma_load_2d(dst, &maps.x, &a_full[ai], ks * BK, un.tile.row_start);
-                        }
-                        ++a_issued;
-                        if (++ai == C::NA) { ai = 0; aph ^= 1; }
-                    }
+            Prog pg;
+            pg.start(m_units, ks_gu, NY, YS);
+            int cur = -1;
+            Unit un{};
+            for (; !pg.done; pg.next()) {
+                if (!pg.gu) continue;
+                if (pg.unit() != cur) { cur = pg.unit(); un = unit_of(cur); }
+                const int ks = pg.ks;
+                if (!mbar_wait(&a_empty[ai], aph ^ 1, abort_flag, p.err)) break;
+                void *dst = smem + C::OFF_A + ai * A_BYTES;
+                if (PAIR) {
+                    // both CTAs' tiles complete on the leader's barrier
+                    if (leader) mbar_arrive_expect_tx(&a_full[ai], 2 * A_BYTES);
+                    tma_load_2d_pair(dst, &maps.x, mapa_shared(smem_u32(&a_full[ai]), 0), ks * BK,
+                                     un.tile.row_start);
+                } else {
+                    mbar_arrive_expect_tx(&a_full[ai], A_BYTES);
+                    tma_load_2d(dst, &maps.x, &a_full[ai], ks * BK, un.tile.row_start);
                 }
+                ++a_issued;
+                if (++ai == C::NA) { ai = 0; aph ^= 1; }
             }
             // In a pair the x tiles complete on the leader's barriers, which the
             // leader's issuer has waited for before its final MMAs.
@@ -434,142 +485,178 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (role == ROLE_MMA) {
         // ---------------- MMA issuer (the pair's leader only) ----------------
-        if (lane == 0 && leader) {
-            uint32_t ai = 0, aph = 0, bi = 0, bph = 0, jc = 0, uc = 0;
+        // The whole warp walks the program (its control flow and descriptors
+        // stay warp-uniform, which keeps the issue of each tcgen05.mma short);
+        // one elected lane issues the MMAs and commits.
+        if (leader) {
+            const bool issuer = elect_one();
+            uint32_t ai = 0, aph = 0, bi = 0, bph = 0, jg = 0, jy = 0;
             bool ok = true;
-            auto mma = [&](uint32_t d, uint64_t da, uint64_t db, uint32_t acc) {
-                if (PAIR) tc_mma_bf16_pair(d, da, db, C::IDESC, acc);
-                else tc_mma_bf16(d, da, db, C::IDESC, acc);
-            };
             auto commit = [&](uint64_t *bar) {
-                if (PAIR) tc_commit_pair(bar); else tc_commit(bar);
+                if (issuer) {
+                    if (PAIR) tc_commit_pair(bar); else tc_commit(bar);
+                }
             };
-            for (int u = group; u < n_units && ok; u += n_groups, ++uc) {
-                const Unit un = make_unit<PAIR>(p, u, n_tiles, rank);
-                for (int s = 0; s < un.n_gu && ok; ++s, ++jc) {
-                    const uint32_t slot = jc & 1, tph = (jc >> 1) & 1;
-                    if (!mbar_wait(&t_empty[slot], tph ^ 1, abort_flag, p.err)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + slot * NJ;
-                    for (int ks = 0; ks < un.ks_gu; ++ks) {
-                        if (!mbar_wait(&a_full[ai], aph, abort_flag, p.err) ||
-                            !mbar_wait(&b_full[bi], bph, abort_flag, p.err)) { ok = false; break; }
-                        tc_fence_after();
-                        const uint64_t da = smem_desc_k_sw128(s_a + ai * A_BYTES);
-                        const uint64_t db = smem_desc_k_sw128(s_b + bi * C::B_BYTES);
-#pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk)
-                            mma(d_tmem, da + 2 * kk, db + 2 * kk, (ks | kk) != 0);
-                        commit(&a_empty[ai]);
-                        commit(&b_empty[bi]);
-                        if (++ai == C::NA) { ai = 0; aph ^= 1; }
-                        if (++bi == C::NB) { bi = 0; bph ^= 1; }
-                    }
-                    if (ok) commit(&t_full[slot]);
+            auto mma = [&](uint32_t d, uint64_t da, uint64_t db, uint32_t idesc, bool acc) {
+                if (issuer) {
+                    if (PAIR) tc_mma_bf16_pair(d, da, db, idesc, acc);
+                    else tc_mma_bf16(d, da, db, idesc, acc);
                 }
-                if (!ok) break;
-                // the down projection reads h: wait until the epilogues wrote all of it
-                if (!mbar_wait(h_full, uc & 1, abort_flag, p.err)) break;
-                tc_fence_after();
-                for (int n = 0; n < un.n_y && ok; ++n, ++jc) {
-                    const uint32_t slot = jc & 1, tph = (jc >> 1) & 1;
-                    if (!mbar_wait(&t_empty[slot], tph ^ 1, abort_flag, p.err)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + slot * NJ;
-                    for (int ks = 0; ks < un.ks_y; ++ks) {
-                        if (!mbar_wait(&b_full[bi], bph, abort_flag, p.err)) { ok = false; break; }
+            };
+            // Descriptors advance by the stage strides (start address field in
+            // 16-byte units); every operand lies below 256 KB.
+            const uint64_t da0 = smem_desc_k_sw128(s_a), db0 = smem_desc_k_sw128(s_b);
+            const uint64_t dh0 = smem_desc_k_sw128(s_h);
+            constexpr uint64_t A_STEP = A_BYTES >> 4, B_STEP = C::B_BYTES >> 4;
+            constexpr uint64_t HT_STEP = HT_BYTES >> 4, YH_STEP = (C::ROWS_Y * 128) >> 4;
+            uint64_t da = da0, db = db0;
+            const uint32_t d_gu = tmem_base + COL_GU, d_y = tmem_base + COL_Y;
+            Prog pg;
+            pg.start(m_units, ks_gu, NY, YS);
+            for (; !pg.done && ok; pg.next()) {
+                if (pg.gu) {
+                    if (pg.ks == 0) {
+                        if (!mbar_wait(g_empty, (jg & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
                         tc_fence_after();
-                        const uint64_t da = smem_desc_k_sw128(s_h + ks * HT_BYTES);
-                        const uint64_t db = smem_desc_k_sw128(s_b + bi * C::B_BYTES);
-#pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk)
-                            mma(d_tmem, da + 2 * kk, db + 2 * kk, (ks | kk) != 0);
-                        commit(&b_empty[bi]);
-                        if (++bi == C::NB) { bi = 0; bph ^= 1; }
                     }
-                    if (ok) commit(&t_full[slot]);
+                    if (!mbar_wait(&a_full[ai], aph, abort_flag, p.err) ||
+                        !mbar_wait(&b_full[bi], bph, abort_flag, p.err)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma(d_gu, da + 2 * kk, db + 2 * kk, C::IDESC_GU, (pg.ks | kk) != 0);
+                    commit(&a_empty[ai]);
+                    commit(&b_empty[bi]);
+                    if (++ai == C::NA) { ai = 0; aph ^= 1; da = da0; } else { da += A_STEP; }
+                    if (++bi == C::NB) { bi = 0; bph ^= 1; db = db0; } else { db += B_STEP; }
+                    if (pg.gu_last()) { commit(g_full); ++jg; }
+                } else {
+                    if (pg.ys == 0) {
+                        // the first down job of a unit reads its h: wait until
+                        // the epilogues placed all of it in shared memory
+                        if (pg.n == 0 && !mbar_wait(h_full, (uint32_t)pg.blk & 1, abort_flag, p.err)) { ok = false; break; }
+                        if (!mbar_wait(y_empty, (jy & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
+                        tc_fence_after();
+                    }
+                    if (!mbar_wait(&b_full[bi], bph, abort_flag, p.err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t dh = dh0 + (uint64_t)(2 * pg.ys) * HT_STEP;
+#pragma unroll
+                    for (int kk = 0; kk < YK / 16; ++kk)
+                        mma(d_y, dh + (kk / 4) * HT_STEP + 2 * (kk & 3), db + (kk / 4) * YH_STEP + 2 * (kk & 3),
+                            C::IDESC_Y, (pg.ys | kk) != 0);
+                    commit(&b_empty[bi]);
+                    if (++bi == C::NB) { bi = 0; bph ^= 1; db = db0; } else { db += B_STEP; }
+                    if (pg.ys == YS - 1) {
+                        commit(y_full);
+                        ++jy;
+                        // h may be overwritten once the unit's last down MMAs finish
+                        if (pg.n == NY - 1) commit(h_empty);
+                    }
                 }
-                if (ok) commit(h_empty);   // h may be overwritten once these MMAs finish
             }
             // every MMA issued here completes before TMEM is released
-            if (PAIR) tc_commit_pair(drain); else tc_commit(drain);
+            commit(drain);
+            __syncwarp();
             mbar_wait(drain, 0, nullptr, p.err, kWaitBudgetCycles / 8);
         }
     } else if (role == ROLE_UNPACK) {
         // ------------- weight unpackers (three groups of 4 warps) -------------
-        // A step's weight rows are split into 128-row tasks (one per step on
-        // CTA pairs, two on single CTAs); the groups take the tasks in turn,
-        // counted over every unit of this block, one thread per row.
+        // A step's weights are split into 128-thread tasks of one 64-weight
+        // slice per thread; the groups take the tasks in turn, counted over
+        // the whole program of this block.
         const int uw = unpack_index(warp);
         const uint32_t grp = (uint32_t)(uw / UNPACK_GROUP_WARPS);
-        const int trow = (uw % UNPACK_GROUP_WARPS) * 32 + lane;   // row within the task
+        const int tt = (uw % UNPACK_GROUP_WARPS) * 32 + lane;    // thread within the task
         uint32_t bi = 0, bph = 0, ri = 0, rph = 0, gt = 0;
         bool ok = true;
-        // bank-conflict-free order of the 16-byte reads of the 32-byte code rows
-        const int qfirst = (trow >> 2) & 1;
-        for (int u = group; u < n_units && ok; u += n_groups) {
-            const Unit un = make_unit<PAIR>(p, u, n_tiles, rank);
-            const int steps = un.n_gu * un.ks_gu + un.n_y * un.ks_y;
-            StepSrc src;
-            src.start();
-            for (int st = 0; st < steps && ok; ++st, src.advance(un)) {
+        Prog pg;
+        pg.start(m_units, ks_gu, NY, YS);
+        int cur = -1;
+        Unit un{};
+        for (; !pg.done && ok; pg.next()) {
 #pragma unroll
-                for (int task = 0; task < C::TASKS; ++task, ++gt) {
-                    if (gt % UNPACK_GROUPS != grp) continue;
-                    const int row = task * 128 + trow;              // weight row of this thread
-                    src.locate(un);
+            for (int task = 0; task < C::TASKS; ++task, ++gt) {
+                if (gt % UNPACK_GROUPS != grp) continue;
+                if (pg.unit() != cur) { cur = pg.unit(); un = unit_of(cur); }
+                const int f = task * 128 + tt;
+                int row, half, g;
+                uint32_t qoff, hdr_base;
+                bool zero = false;
+                if (pg.gu) {
+                    const int s = pg.s, ks = pg.ks;
+                    row = f;
+                    half = 0;
+                    g = ks & 3;
+                    qoff = C::R_HDR_GU + row * 32;
                     const int grow = PAIR ? row : (row & 127);      // gate/up row within the job
-                    const bool zero = src.gu && (un.i0 + src.s * GU_ROWS + grow >= p.I);
-                    if (!mbar_wait(&r_full[ri], rph, abort_flag, p.err)) { ok = false; break; }
-                    uint4 hd = make_uint4(0, 0, 0, 0), q0 = hd, q1 = hd;
-                    if (!zero) {
-                        const uint32_t rs = s_r + ri * C::R_BYTES;
-                        hd = ld_shared_v4(rs + row * 16);
-                        const uint32_t qa = rs + C::R_HDR + row * 32;
-                        const uint4 first = ld_shared_v4(qa + 16 * qfirst);
-                        const uint4 second = ld_shared_v4(qa + 16 * (qfirst ^ 1));
-                        q0 = qfirst ? second : first;
-                        q1 = qfirst ? first : second;
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&r_empty[ri]);
-                    if (!mbar_wait(&b_empty[bi], bph ^ 1, abort_flag, p.err)) { ok = false; break; }
-                    const uint32_t rb = s_b + bi * C::B_BYTES + sw128_row(row);
-                    const uint32_t w8[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                    unpack_row_to_smem(hd, w8, src.g, rb, row);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) arrive_leader(&b_full[bi]);
+                    zero = un.i0 + s * GU_ROWS + grow >= p.I;
+                } else {
+                    row = f % C::ROWS_Y;
+                    half = f / C::ROWS_Y;
+                    g = 2 * pg.ys + half;
+                    qoff = C::R_HDR_Y + row * 64 + 32 * half;
                 }
-                if (++ri == C::NR) { ri = 0; rph ^= 1; }
-                if (++bi == C::NB) { bi = 0; bph ^= 1; }
+                hdr_base = row * 16;
+                if (!mbar_wait(&r_full[ri], rph, abort_flag, p.err)) { ok = false; break; }
+                uint4 hd = make_uint4(0, 0, 0, 0), q0 = hd, q1 = hd;
+                if (!zero) {
+                    const uint32_t rs = s_r + ri * C::R_BYTES;
+                    hd = ld_shared_v4(rs + hdr_base);
+                    // bank-conflict-free order of the two 16-byte reads
+                    const int qfirst = (row >> 2) & 1;
+                    const uint4 first = ld_shared_v4(rs + qoff + 16 * qfirst);
+                    const uint4 second = ld_shared_v4(rs + qoff + 16 * (qfirst ^ 1));
+                    q0 = qfirst ? second : first;
+                    q1 = qfirst ? first : second;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&r_empty[ri]);
+                if (!mbar_wait(&b_empty[bi], bph ^ 1, abort_flag, p.err)) { ok = false; break; }
+                const uint32_t rb = s_b + bi * C::B_BYTES + half * (C::ROWS_Y * 128) + sw128_row(row);
+                const uint32_t w8[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                unpack_row_to_smem(hd, w8, g, rb, row);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) arrive_leader(&b_full[bi]);
             }
+            if (++ri == C::NR) { ri = 0; rph ^= 1; }
+            if (++bi == C::NB) { bi = 0; bph ^= 1; }
         }
     } else if (role == ROLE_EPI) {
         // ---------------- epilogue (4 warps) ----------------
         const int q = warp & 3;                      // TMEM lane quadrant of this warp
         const int row = q * 32 + lane;               // token row within the CTA's tile
         const uint32_t lane_bits = (uint32_t)(q * 32) << 16;
+        const uint32_t t_lane = tmem_base + lane_bits;
         const uint32_t s_y = smem_u32(smem + C::OFF_Y), s_base = smem_u32(smem);
-        uint32_t y_use = 0;
-        uint32_t jc = 0, uc = 0;
+        // dense tiles: y slices go through swizzled shared memory and one TMA
+        // reduction per warp and slice; routed tiles scatter rows, so each
+        // thread adds its own row with vector reductions
+        const bool tma_y = p.tiles == nullptr;
+        uint32_t jg = 0, jy = 0;
         bool ok = true;
-        for (int u = group; u < n_units && ok; u += n_groups, ++uc) {
-            const Unit un = make_unit<PAIR>(p, u, n_tiles, rank);
-            for (int s = 0; s < un.n_gu && ok; ++s, ++jc) {
-                const uint32_t slot = jc & 1, tph = (jc >> 1) & 1;
-                if (!mbar_wait(&t_full[slot], tph, abort_flag, p.err)) { ok = false; break; }
+        Prog pg;
+        pg.start(m_units, ks_gu, NY, YS);
+        int cur = -1;
+        Unit un{};
+        bool valid = false, warp_live = false;
+        int token = 0, warp_row0 = 0;
+        float wgt = 1.0f;
+        for (; !pg.done && ok; pg.next()) {
+            if (pg.gu) {
+                if (!pg.gu_last()) continue;
+                // ---- gate/up job complete: h = silu(G) * U -> the TMEM stash
+                const int s = pg.s;
+                if (!mbar_wait(g_full, jg & 1, abort_flag, p.err)) { ok = false; break; }
                 tc_fence_after();
-                if (s == 0 && !mbar_wait(h_empty, (uc & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
-                const uint32_t t_addr = tmem_base + lane_bits + slot * NJ;
 #pragma unroll 1
                 for (int c = 0; c < GU_ROWS; c += 16) {
-                    uint32_t gr[16], ur[16];
-                    tmem_ld_32x32b_x16(t_addr + c, gr);
-                    tmem_ld_32x32b_x16(t_addr + GU_ROWS + c, ur);
+                    uint32_t gr[16], ur[16], hw[8];
+                    tmem_ld_32x32b_x16(t_lane + COL_GU + c, gr);
+                    tmem_ld_32x32b_x16(t_lane + COL_GU + GU_ROWS + c, ur);
                     tmem_ld_wait(gr);
                     tmem_ld_wait(ur);
-                    uint32_t hw[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const float g0 = __uint_as_float(gr[2 * j]), g1 = __uint_as_float(gr[2 * j + 1]);
@@ -578,89 +665,117 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const float h1 = __fdividef(g1 * u1, 1.0f + __expf(-g1));
                         hw[j] = pack_bf16x2(h0, h1);
                     }
-                    const int col = s * GU_ROWS + c;               // h column of hw[0]
-                    const uint32_t tile_base = s_h + (col >> 6) * HT_BYTES + sw128_row(row);
-                    const int cb = (col & 63) >> 3;                // first 16-byte chunk
-#pragma unroll
-                    for (int j = 0; j < 2; ++j)
-                        st_shared_v4(tile_base + ((uint32_t)((cb + j) ^ (row & 7)) << 4), hw[4 * j],
-                                     hw[4 * j + 1], hw[4 * j + 2], hw[4 * j + 3]);
+                    // stash column s*64 + c/2 holds h columns s*128 + c, +1
+                    tmem_st_32x32b_x8(t_lane + COL_STASH + s * 64 + c / 2, hw);
                 }
+                tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) arrive_leader(&t_empty[slot]);
+                if (lane == 0) arrive_leader(g_empty);
+                ++jg;
+                continue;
             }
-            if (!ok) break;
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) arrive_leader(h_full);
-            // this row's destination
-            const bool valid = row < un.tile.row_count;
-            int token = 0;
-            float wgt = 1.0f;
-            if (valid) {
-                const int xr = un.tile.row_start + row;
-                token = p.row_token ? p.row_token[xr] : xr;
-                wgt = p.row_weight ? p.row_weight[xr] : 1.0f;
-            }
-            float *yrow = p.y + (int64_t)token * p.H;
-            // dense tiles: y slices go through swizzled shared memory and one TMA
-            // reduction per warp and slice; routed tiles scatter rows, so each
-            // thread adds its own row with vector reductions
-            const bool tma_y = p.tiles == nullptr;
-            const int warp_row0 = un.tile.row_start + q * 32;
-            const bool warp_live = warp_row0 < p.T;
-            for (int n = 0; n < un.n_y && ok; ++n, ++jc) {
-                const uint32_t slot = jc & 1, tph = (jc >> 1) & 1;
-                if (!mbar_wait(&t_full[slot], tph, abort_flag, p.err)) { ok = false; break; }
+            if (pg.n == 0 && pg.ys == 0) {
+                // ---- start of unit blk's down jobs: its h, stashed in TMEM by
+                // the gate/up jobs, goes to shared memory once the previous
+                // unit's down MMAs have finished reading the old h
+                if (!mbar_wait(h_empty, ((uint32_t)pg.blk & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t t_addr = tmem_base + lane_bits + slot * NJ;
 #pragma unroll 1
-                for (int c = 0; c < NJ; c += 32) {
-                    uint32_t yr[32];
-                    tmem_ld_32x32b_x32(t_addr + c, yr);
-                    tmem_ld_wait(yr);
-                    if (tma_y) {
+                for (int t = 0; t < C::N_HT; ++t) {
+                    uint32_t hw[32];
+                    tmem_ld_32x32b_x32(t_lane + COL_STASH + t * 32, hw);
+                    tmem_ld_wait(hw);
+                    const uint32_t tile_base = s_h + t * HT_BYTES + sw128_row(row);
 #pragma unroll
-                        for (int part = 0; part < 32 / C::Y_COLS; ++part) {
-                            if (lane == 0) bulk_wait_group_read<1>();
-                            __syncwarp();
-                            const uint32_t buf = s_y + (uint32_t)((q * 2 + (y_use & 1)) * C::Y_BUF);
-                            const uint32_t rowa = buf + lane * (C::Y_COLS * 4);
-                            constexpr int CH = C::Y_COLS / 4;            // 16-byte chunks per row
-                            const int sw = C::Y_COLS == 32 ? (lane & 7) : ((lane >> 1) & 3);
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(tile_base + ((uint32_t)(j ^ (row & 7)) << 4), hw[4 * j], hw[4 * j + 1],
+                                     hw[4 * j + 2], hw[4 * j + 3]);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) arrive_leader(h_full);
+                // this row's destination for the unit's down jobs
+                if (pg.blk != cur) { cur = pg.blk; un = unit_of(cur); }
+                valid = row < un.tile.row_count;
+                token = 0;
+                wgt = 1.0f;
+                if (valid) {
+                    const int xr = un.tile.row_start + row;
+                    token = p.row_token ? p.row_token[xr] : xr;
+                    wgt = p.row_weight ? p.row_weight[xr] : 1.0f;
+                }
+                warp_row0 = un.tile.row_start + q * 32;
+                warp_live = warp_row0 < p.T;
+            }
+            if (pg.ys != YS - 1) continue;
+            // ---- down job n complete: Y tile -> y[token, n*128 ..]
+            if (!mbar_wait(y_full, jy & 1, abort_flag, p.err)) { ok = false; break; }
+            tc_fence_after();
+            const int ncol = pg.n * NJ_Y;
+            if (tma_y) {
+                // Pairs of staging boxes: a warp's two buffers are refilled once
+                // the previous pair's reductions have read them; one proxy fence
+                // and one bulk group cover a pair.  One 32-column TMEM load
+                // fills 32 / Y_COLS boxes.
+                constexpr int BOX_PER_LD = 32 / C::Y_COLS;
+                const int sw = C::Y_COLS == 32 ? (lane & 7) : ((lane >> 1) & 3);
+                const uint32_t buf0 = s_y + (uint32_t)(q * 2 * C::Y_BUF);
+                const uint32_t rowoff = (uint32_t)lane * (C::Y_COLS * 4);
+#pragma unroll 1
+                for (int c = 0; c < NJ_Y; c += 32) {
+                    const int box0 = (c / C::Y_COLS) & 1;         // buffer of this load's first box
+                    if (box0 == 0) {
+                        if (lane == 0) bulk_wait_group_read<0>();
+                        __syncwarp();
+                    }
+                    uint32_t yv[32];
+                    tmem_ld_32x32b_x32(t_lane + COL_Y + c, yv);
+                    tmem_ld_wait(yv);
 #pragma unroll
-                            for (int j = 0; j < CH; ++j)
-                                st_shared_v4(rowa + (((uint32_t)(j ^ sw)) << 4),
-                                             yr[C::Y_COLS * part + 4 * j], yr[C::Y_COLS * part + 4 * j + 1],
-                                             yr[C::Y_COLS * part + 4 * j + 2], yr[C::Y_COLS * part + 4 * j + 3]);
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                            if (lane == 0 && warp_live) {
-                                tma_reduce_add_2d(&maps.y, smem + (buf - s_base),
-                                                  n * NJ + c + C::Y_COLS * part, warp_row0);
-                                bulk_commit_group();
-                            }
-                            ++y_use;
+                    for (int e = 0; e < 32; e += 4) {
+                        const int bx = box0 + e / C::Y_COLS, j = (e % C::Y_COLS) / 4;
+                        st_shared_v4(buf0 + bx * C::Y_BUF + rowoff + (((uint32_t)(j ^ sw)) << 4),
+                                     yv[e], yv[e + 1], yv[e + 2], yv[e + 3]);
+                    }
+                    if (box0 + BOX_PER_LD == 2) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0 && warp_live) {
+                            const int col0 = ncol + c + 32 - 2 * C::Y_COLS;   // first column of the pair
+                            tma_reduce_add_2d(&maps.y, smem + (buf0 - s_base), col0, warp_row0);
+                            tma_reduce_add_2d(&maps.y, smem + (buf0 + C::Y_BUF - s_base), col0 + C::Y_COLS,
+                                              warp_row0);
+                            bulk_commit_group();
                         }
-                    } else if (valid) {
-                        float *dst = yrow + n * NJ + c;
+                    }
+                }
+            } else {
+                float *yrow = p.y + (int64_t)token * p.H + ncol;
+#pragma unroll 1
+                for (int c = 0; c < NJ_Y; c += 32) {
+                    uint32_t yr[32];
+                    tmem_ld_32x32b_x32(t_lane + COL_Y + c, yr);
+                    tmem_ld_wait(yr);
+                    if (valid) {
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const float v0 = __uint_as_float(yr[4 * j]) * wgt;
                             const float v1 = __uint_as_float(yr[4 * j + 1]) * wgt;
                             const float v2 = __uint_as_float(yr[4 * j + 2]) * wgt;
                             const float v3 = __uint_as_float(yr[4 * j + 3]) * wgt;
-                            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4 * j),
+                            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(yrow + c + 4 * j),
                                          "f"(v0), "f"(v1), "f"(v2), "f"(v3)
                                          : "memory");
                         }
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) arrive_leader(&t_empty[slot]);
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) arrive_leader(y_empty);
+            ++jy;
         }
         // the reductions must have finished before the block exits
         if (lane == 0) bulk_wait_group_all();
@@ -716,7 +831,7 @@ cudaError_t launch_ffn_tc(const TcArgs &a, cudaStream_t s) {
     if (!encode) return cudaErrorNotSupported;
     // Dense prefill with at least one full pair tile runs on CTA pairs.
     const bool pair = a.tiles == nullptr && a.T >= 256 && di.num_sms >= 2;
-    const int rows_b = pair ? tc::Cfg<true>::ROWS_B : tc::Cfg<false>::ROWS_B;
+    const int rows_y = pair ? tc::Cfg<true>::ROWS_Y : tc::Cfg<false>::ROWS_Y;
     tc::Maps maps;
     {
         const cuuint64_t dims[2] = {(cuuint64_t)a.H, (cuuint64_t)a.x_rows};
@@ -747,8 +862,8 @@ cudaError_t launch_ffn_tc(const TcArgs &a, cudaStream_t s) {
         !encode_bytes_map(encode, &maps.g_qs, a.Wg, rbH, gu_rows, 32, tc::GU_ROWS) ||
         !encode_bytes_map(encode, &maps.u_hdr, a.Wu, rbH, gu_rows, 16, tc::GU_ROWS) ||
         !encode_bytes_map(encode, &maps.u_qs, a.Wu, rbH, gu_rows, 32, tc::GU_ROWS) ||
-        !encode_bytes_map(encode, &maps.d_hdr, a.Wd, rbI, d_rows, 16, rows_b) ||
-        !encode_bytes_map(encode, &maps.d_qs, a.Wd, rbI, d_rows, 32, rows_b))
+        !encode_bytes_map(encode, &maps.d_hdr, a.Wd, rbI, d_rows, 16, rows_y) ||
+        !encode_bytes_map(encode, &maps.d_qs, a.Wd, rbI, d_rows, 64, rows_y))
         return cudaErrorInvalidValue;
     static int attr_set_device[2] = {-1, -1};
     const void *fn = pair ? (const void *)tc::ffn_tc_kernel<true> : (const void *)tc::ffn_tc_kernel<false>;
