@@ -90,10 +90,28 @@ def load_peaks():
         return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
 
 
-def kernel_source_hash():
+# Source files that define the dominant kernel of each workload: a committed
+# ncu traffic figure stays valid while these files are unchanged.
+KERNEL_SOURCES = {
+    "prefill": ("ffn_tc.cu", "zffn_internal.cuh"),
+    "moe": ("ffn_tc.cu", "moe_route.cu", "zffn_internal.cuh"),
+    "decode": ("ffn_matvec.cu", "zffn_internal.cuh"),
+}
+
+
+def kernel_source_hash(workload=None):
+    """sha256 (16 hex digits) over the kernel sources of `workload` (all of
+    csrc when None)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_ffn_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    names = sorted(os.listdir(csrc))
+    if workload is not None:
+        kind = "moe" if workload.startswith("moe") else (
+            "decode" if workload.startswith("decode") else "prefill")
+        if workload == "moe_T1":
+            kind = "decode"
+        names = sorted(KERNEL_SOURCES[kind])
+    for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -112,7 +130,7 @@ def profiled_traffic(workload):
             if ":" in line and line.strip().startswith("- "):
                 k, v = line.strip()[2:].split(":", 1)
                 vals[k.strip()] = v.strip().strip("`")
-    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash(workload):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
