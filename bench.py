@@ -293,7 +293,7 @@ def run_gpu(args):
             zffn.moe_swiglu_q4k(xx, ids, wts, Wg_, Wu_, Wd_, I, E, y=y if out is None else out,
                                 residual=residual)
 
-    launches_per_call = 2 if T > 1 else 1          # zero fill + fused kernel, or one
+    launches_per_call = 2                          # zero fill + fused kernel, or gate/up + down
     if kind == "moe" and T > 1:
         launches_per_call = 4                      # route, gather, zero fill, fused kernel
 
@@ -407,7 +407,7 @@ def run_gpu(args):
             "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
             "frac": round(achieved / peak, 4), "traffic": traffic,
             "kernel": "ffn_tc_kernel" if bound == "tensor" else
-                      ("ffn_matvec_kernel" if T == 1 else "ffn_tc_kernel"),
+                      ("ffn_gu_kernel+ffn_down_kernel" if T == 1 else "ffn_tc_kernel"),
             "kernel_ms": round(kms, 4),
             "peak_source": f"{peaks['source']} (burst)",
             "algorithmic": {"flop": flop, "hbm_bytes": abytes},

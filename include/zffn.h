@@ -137,16 +137,15 @@ zffn_status zffn_moe_swiglu_q4k_residual(const void *x, const int32_t *expert_id
  * that cannot let the library call cudaMalloc/cudaFree during a call -- for
  * example a server whose own allocator already owns all device memory, or a
  * loop that forbids allocation after start-up.  It computes the same block as
- * zffn_swiglu_q4k with T = 1 (same kernel), but its scratch (the intermediate
- * strip and the grid-barrier words) lives in one fixed array compiled into the
- * library: 66 KB that every GPU loading the library keeps until exit.
+ * zffn_swiglu_q4k with T = 1 (same kernels), but its scratch (the fp32
+ * intermediate strip) lives in one fixed array compiled into the library:
+ * 64 KB that every GPU loading the library keeps until exit.
  *   x: bf16 [H]; Wg, Wu, Wd and y as for zffn_swiglu_q4k with T = 1.
  * Limits: I <= 16384 (the array's size); larger I returns ZFFN_ERR_INVALID_ARG
  * and zffn_last_error() says why.  The first call on a device looks up the
  * array's device address with cudaGetSymbolAddress, so make that first call
  * before capturing any stream.  All calls share the array and it keeps the
- * last call's contents; the barrier words are cleared on the stream before
- * each launch, and calls whose launches overlap on the GPU race on it.
+ * last call's contents; calls whose launches overlap on the GPU race on it.
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
 zffn_status zffn_swiglu_q4k_token_static(const void *x, const void *Wg, const void *Wu,
                                          const void *Wd, float *y, int H, int I, void *stream);

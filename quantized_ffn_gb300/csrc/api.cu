@@ -17,7 +17,6 @@ constexpr int kMaxDevices = 64;
 struct Workspace {
     void *ptr = nullptr;
     size_t bytes = 0;
-    unsigned *barrier = nullptr;   // first 256 bytes: grid-barrier words (zeroed)
 };
 
 std::mutex g_mu;
@@ -30,7 +29,7 @@ inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 // Sub-buffers carved out of one device allocation.
 struct Layout {
-    size_t barrier, h, counts, offsets, cursors, tiles, n_tiles, row_token, row_weight, x_perm,
+    size_t h, counts, offsets, cursors, tiles, n_tiles, row_token, row_weight, x_perm,
         total;
     int max_tiles;
 };
@@ -40,7 +39,6 @@ Layout layout_for(int T, int H, int I, int E, int k) {
     size_t o = 0;
     const int64_t P = (int64_t)T * k;
     L.max_tiles = (int)((P + 127) / 128 + (E < P ? E : P));
-    L.barrier = o; o = align_up(o + kGridBarrierWords * sizeof(unsigned));
     L.h = o; o = align_up(o + (size_t)P * I * sizeof(float));
     L.counts = o; o = align_up(o + (size_t)E * sizeof(int));
     L.offsets = o; o = align_up(o + (size_t)(E + 1) * sizeof(int));
@@ -78,13 +76,8 @@ zffn_status ensure_workspace(size_t bytes, Workspace **out) {
             cudaGetLastError();
             return ZFFN_ERR_NO_WORKSPACE;
         }
-        if (cudaMemset(p, 0, align_up(kGridBarrierWords * sizeof(unsigned))) != cudaSuccess) {
-            cudaFree(p);
-            return ZFFN_ERR_CUDA;
-        }
         w.ptr = p;
         w.bytes = bytes;
-        w.barrier = static_cast<unsigned *>(p);
     }
     *out = &w;
     return ZFFN_OK;
@@ -199,7 +192,6 @@ zffn_status swiglu_dense(const void *x, const void *Wg, const void *Wu, const vo
         a.wts = nullptr;
         a.y = y;
         a.h = reinterpret_cast<float *>(base + L.h);
-        a.barrier = reinterpret_cast<unsigned *>(base + L.barrier);
         a.err = di.err_word;
         a.T = T; a.H = H; a.I = I; a.E = 1; a.k = 1;
         a.accumulate = accumulate;
@@ -261,7 +253,6 @@ zffn_status swiglu_moe(const void *x, const int32_t *expert_ids, const float *ex
         a.wts = expert_weights;
         a.y = y;
         a.h = reinterpret_cast<float *>(base + L.h);
-        a.barrier = reinterpret_cast<unsigned *>(base + L.barrier);
         a.err = di.err_word;
         a.T = T; a.H = H; a.I = I; a.E = E; a.k = top_k;
         a.accumulate = accumulate;
@@ -366,13 +357,6 @@ zffn_status zffn_get_device_error(void *stream) {
     if (cudaMemcpyAsync(&v, di.err_word, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return to_status(cudaErrorUnknown);
     if (cudaMemsetAsync(di.err_word, 0, sizeof(int), s) != cudaSuccess) return ZFFN_ERR_CUDA;
-    if (v != 0) {
-        // a timed-out grid barrier may have left its counter mid-way: reset it
-        std::lock_guard<std::mutex> lk(g_mu);
-        Workspace &w = g_ws[di.device];
-        if (w.barrier && cudaMemsetAsync(w.barrier, 0, kGridBarrierWords * sizeof(unsigned), s) != cudaSuccess)
-            return ZFFN_ERR_CUDA;
-    }
     if (cudaStreamSynchronize(s) != cudaSuccess) return to_status(cudaErrorUnknown);
     return v == 0 ? ZFFN_OK : (zffn_status)v;
 }

@@ -1,8 +1,8 @@
 // ffn_decode_static.cu -- single-token dense block that allocates nothing.
 //
-// The regular entry points keep their scratch (the single-token kernel's
-// intermediate strip and its grid-barrier words) in a workspace that the
-// library allocates with cudaMalloc on first use.  Some callers cannot allow
+// The regular entry points keep their scratch (the single-token path's
+// intermediate strip) in a workspace that the library allocates with
+// cudaMalloc on first use.  Some callers cannot allow
 // that: a serving process whose own allocator has already claimed the whole
 // device, a real-time loop that forbids allocation once it is running, or a
 // caller that must never hit the implicit device synchronisation of
@@ -10,13 +10,12 @@
 // with its scratch in a fixed array compiled into the library instead.
 //
 // The array is a file-scope __device__ object: every GPU that loads the
-// library holds it (66 KB) until the process exits.  Host code cannot
+// library holds it (64 KB) until the process exits.  Host code cannot
 // use the array's name as a device address, so the first call on each device
 // looks the address up with cudaGetSymbolAddress (with that device current)
 // and caches it; that first call should therefore be made before any stream
 // capture.  All calls share the one array, which keeps the last call's
-// contents: the barrier words are cleared on the stream before every launch,
-// and calls whose launches overlap on the GPU race on the array.
+// contents; calls whose launches overlap on the GPU race on the array.
 #include <mutex>
 
 #include "zffn_internal.cuh"
@@ -24,8 +23,7 @@
 namespace zffn {
 
 constexpr int kStaticMaxI = 16384;                 // largest intermediate width
-constexpr int kStaticBarrierWords = kGridBarrierWords;   // 2 KB of grid-barrier words
-constexpr size_t kStaticScratchFloats = kStaticMaxI + kStaticBarrierWords;
+constexpr size_t kStaticScratchFloats = kStaticMaxI;
 
 static __device__ __align__(256) float g_static_scratch[kStaticScratchFloats];
 
@@ -86,10 +84,8 @@ zffn_status zffn_swiglu_q4k_token_static(const void *x, const void *Wg, const vo
         scratch = g_static_ptr[di.device];
     }
     cudaStream_t s = (cudaStream_t)stream;
-    // barrier words first (256-byte aligned), then the intermediate strip
-    unsigned *barrier = reinterpret_cast<unsigned *>(scratch);
-    cudaError_t e = cudaMemsetAsync(barrier, 0, kGridBarrierWords * sizeof(unsigned), s);
-    if (e == cudaSuccess) {
+    cudaError_t e;
+    {
         MatvecArgs a{};
         a.x = static_cast<const __nv_bfloat16 *>(x);
         a.Wg = static_cast<const uint8_t *>(Wg);
@@ -98,8 +94,7 @@ zffn_status zffn_swiglu_q4k_token_static(const void *x, const void *Wg, const vo
         a.ids = nullptr;
         a.wts = nullptr;
         a.y = y;
-        a.h = scratch + kStaticBarrierWords;
-        a.barrier = barrier;
+        a.h = scratch;
         a.err = di.err_word;
         a.T = 1; a.H = H; a.I = I; a.E = 1; a.k = 1;
         a.accumulate = false;

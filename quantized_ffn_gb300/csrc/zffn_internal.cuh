@@ -395,14 +395,9 @@ cudaError_t launch_q4k_quantize(const float *w, void *blocks, int64_t rows, int6
                                 cudaStream_t s);
 cudaError_t launch_zero_f32(float *p, int64_t n, cudaStream_t s);
 
-// Single-token / few-pair matvec path (phase 1: gate/up + SwiGLU into an
-// on-device strip; grid barrier; phase 2: down projection).
-// Words of the single-token kernel's grid barrier: [0] the launch epoch, then
-// one arrival flag per block (so at most kGridBarrierWords - 1 blocks).  All
-// zero before the first launch; each launch leaves them consistent for the
-// next one.
-constexpr int kGridBarrierWords = 512;
-
+// Single-token path: a gate/up kernel (SwiGLU into an on-device strip h)
+// followed by a down-projection kernel launched as its programmatic
+// dependent.
 struct MatvecArgs {
     const __nv_bfloat16 *x;      // [T][H]
     const uint8_t *Wg, *Wu, *Wd; // expert-stacked
@@ -410,7 +405,6 @@ struct MatvecArgs {
     const float *wts;            // [T][k] or nullptr
     float *y;                    // [T][H]
     float *h;                    // workspace [T*k][I]
-    unsigned int *barrier;       // kGridBarrierWords words (see above)
     int *err;
     int T, H, I, E, k;
     bool accumulate;             // y += result instead of y = result
