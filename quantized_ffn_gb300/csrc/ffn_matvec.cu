@@ -12,16 +12,17 @@
 //            MLP...", FAQ "Does this affect decode?").
 //   B (down): y[n] = sum_p w_p * Wd_{e_p}[n] . h[p] for the output rows of
 //            this block.  Expert ids are read on the device ("Bottleneck 2").
-// B's blocks start on the SMs that A's blocks leave and stream their W_down
-// rows into shared memory at once; only the reads of h wait (griddepcontrol)
-// until A has completed.  The dependency between the two halves is thus
-// carried by the hardware's grid completion, not by a software grid barrier
-// polled over global memory.
+// B's blocks start on the SMs that A's blocks leave; their reads of h wait
+// (griddepcontrol) until A has completed, so the dependency is carried by the
+// hardware's grid completion, not by a software grid barrier.
 //
-// Data movement: one producer warp per block streams the packed weight rows
-// into a ring of shared-memory stages with bulk asynchronous copies.  In A it
-// starts once the consumers hold x, so that the small vector load does not
-// queue behind the weight stream.  Consumer warps unpack from shared memory.
+// Data movement: every block of A first copies x into shared memory (a bulk
+// copy that nothing else is queued behind: a weight stream started earlier
+// delays these 8 KB by several microseconds).  Each warp then walks its rows
+// on its own: its lane 0 copies the packed rows of the warp's next pass into
+// one of the warp's two shared-memory slots (bulk copy, mbarrier) while the
+// warp computes on the other.  No step synchronises more than one warp.  B
+// reads h first and only then starts its own row copies, for the same reason.
 //
 // Arithmetic: the vector (x, later h) is stored in shared memory as int16 per
 // 128-element half-block with one fp32 scale each (relative rounding error
@@ -30,103 +31,70 @@
 //     d*sc * scale * sum(q * v_int) - dmin*m * sum(v)
 // where sum(q * v_int) is exact in int32: the 4-bit codes are masked into
 // int8 lanes (one LOP3 per four codes) and multiplied with int16 pairs by
-// dp2a.  Each lane owns one half-block (128 weights) of one row.
+// dp2a.  Each lane owns one half-block (128 weights) of a row at a time.
 #include "zffn_internal.cuh"
 
 namespace zffn {
 
-constexpr int kMvConsumerWarps = 12;
-constexpr int kMvConsumers = kMvConsumerWarps * 32;
-constexpr int kMvThreads = kMvConsumers + 32;          // + producer warp
-constexpr int kMvStages = 3;
-constexpr int kMvStageBytes = 55296;                   // 54 KB, multiple of 16
-constexpr int kMvMaxRows = 64;                          // rows per stage cap
+constexpr int kDecWarps = 16;
+constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kHalfBytes = 272;                         // 128 int16 + 16 pad
 
-struct MvGeom {
+struct DecGeom {
     int P;            // expert slots of the token (dense: 1)
     int nbH, nbI;     // blocks per W_gate/W_up row, per W_down row
     int64_t rbH, rbI; // bytes per row
-    int R1, R2;       // rows per stage in phase 1 (row pairs) and phase 2
-    int nhalf1, nhalf2;   // vector half-blocks in phase 1 and phase 2
+    int nhalf1, nhalf2;   // vector half-blocks of x and of h (all slots)
 };
 
-// Half-block slots reserved per row: the real count 2*nb rounded up to a
-// power of two (<= 32) or to a multiple of 32, so that rows never straddle
-// a 32-lane chunk unevenly.
-__host__ __device__ inline int slots_per_row(int nb) {
-    const int lr = 2 * nb;
-    if (lr > 32) return (lr + 31) & ~31;
-    int lp = 1;
-    while (lp < lr) lp <<= 1;
-    return lp;
-}
-
-// Rows per stage: as many as fit (at most kMvMaxRows), trimmed so that the
-// stage's 32-lane chunks split evenly over the consumer warps when that
-// costs at most a quarter of the rows.
-__host__ __device__ inline int rows_per_stage(int64_t bytes_per_row, int nmat, int nb) {
-    int r = (int)(kMvStageBytes / bytes_per_row);
-    if (r > kMvMaxRows) r = kMvMaxRows;
-    const int lp = slots_per_row(nb);
-    for (int t = r; t >= 1 && 4 * t >= 3 * r; --t) {
-        const int chunks = (nmat * t * lp + 31) / 32;
-        if (chunks % kMvConsumerWarps == 0) return t;
-    }
-    return r;
-}
-
-__host__ __device__ inline MvGeom mv_geom(int H, int I, int k) {
-    MvGeom g;
+__host__ __device__ inline DecGeom dec_geom(int H, int I, int k) {
+    DecGeom g;
     g.P = k;
     g.nbH = H / kQK;
     g.nbI = (I + kQK - 1) / kQK;
     g.rbH = (int64_t)g.nbH * kBlockBytes;
     g.rbI = (int64_t)g.nbI * kBlockBytes;
-    g.R1 = rows_per_stage(2 * g.rbH, 2, g.nbH);
-    g.R2 = rows_per_stage(g.rbI, 1, g.nbI);
     g.nhalf1 = 2 * g.nbH;
     g.nhalf2 = g.P * 2 * g.nbI;
     return g;
 }
 
-struct MvSmem {
-    size_t ring, vec, vscale, vsum, acc, yacc, bars, total;
-};
-
-__host__ __device__ inline MvSmem mv_smem_layout(const MvGeom &g) {
-    MvSmem L;
-    size_t o = 0;
-    const int nh = g.nhalf1 > g.nhalf2 ? g.nhalf1 : g.nhalf2;
-    L.ring = o; o += (size_t)kMvStages * kMvStageBytes;
-    L.vec = o; o += (size_t)nh * kHalfBytes;
-    L.vscale = o; o += (size_t)nh * 4;
-    L.vsum = o; o += (size_t)nh * 4 * 4;
-    L.acc = o; o += 2 * kMvMaxRows * 4;
-    L.yacc = o; o += kMvMaxRows * 4;
-    o = (o + 15) & ~(size_t)15;
-    L.bars = o; o += (2 * kMvStages + 1) * 8;
-    L.total = o;
-    return L;
+// Shared memory of one block: the quantised vector (int16 half-blocks, their
+// scales and sub-block sums).
+__host__ __device__ inline size_t dec_smem_bytes(int nhalf) {
+    return (size_t)nhalf * (kHalfBytes + 4 + 16);
 }
+
+// (defined below: shared memory of the gate/up and of the down kernel)
+size_t gu_smem_total(int H, int I, int k);
+size_t down_smem_total(int H, int I, int k);
 
 size_t matvec_smem_bytes(int T, int H, int I, int k) {
     (void)T;
-    const MvGeom g = mv_geom(H, I, k);
-    if (g.R1 < 1 || g.R2 < 1) return (size_t)1 << 30;   // a row does not fit a stage
-    return mv_smem_layout(g).total;
+    const size_t sa = gu_smem_total(H, I, k), sb = down_smem_total(H, I, k);
+    return sa > sb ? sa : sb;
 }
 
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
+struct DecVec {
+    uint8_t *vec;
+    float *vscale, *vsum;
+};
+__device__ __forceinline__ DecVec dec_vec(uint8_t *smem, int nhalf) {
+    DecVec V;
+    V.vec = smem;
+    V.vscale = reinterpret_cast<float *>(smem + (size_t)nhalf * kHalfBytes);
+    V.vsum = V.vscale + nhalf;
+    return V;
 }
 
-__device__ __forceinline__ void consumers_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kMvConsumers) : "memory");
+// 16 bytes from global memory that this launch only reads (no L1 allocation:
+// every byte is used once).
+__device__ __forceinline__ uint4 ldg_stream(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
 }
 
 // Quantise one 128-element half-block of a vector (one warp, 4 values per
@@ -171,18 +139,17 @@ __device__ __forceinline__ float byte_to_float(uint32_t v, int jj) {
     return __uint_as_float(f) - 8388608.0f;
 }
 
-// Integer part of the dot product of one half-block of packed codes (half hh
-// of the block at blk) with a quantised vector half-block in registers: the
+// Integer part of the dot product of one half-block of codes (qv: the 64
+// code bytes of half hh) with a quantised vector half-block in registers: the
 // four sub-block sums of q * v_int (exact in int32).
-__device__ __forceinline__ void half_block_isums(const uint8_t *blk, int hh, const uint4 (&xv)[16],
+__device__ __forceinline__ void half_block_isums(const uint4 (&qv4)[4], const uint4 (&xv)[16],
                                                  int (&acc)[4]) {
-    const uint4 *qs = reinterpret_cast<const uint4 *>(blk + 16 + 64 * hh);
     int acc_a[4] = {0, 0, 0, 0}, acc_b[4] = {0, 0, 0, 0};
 #pragma unroll
     for (int g = 0; g < 2; ++g) {            // the two 64-weight groups of the half
 #pragma unroll
         for (int c = 0; c < 2; ++c) {        // 16 code bytes: weights 16c.. (low) and 32+16c.. (high)
-            const uint4 qv = qs[2 * g + c];
+            const uint4 qv = qv4[2 * g + c];
             const uint4 xlo0 = xv[8 * g + 2 * c], xlo1 = xv[8 * g + 2 * c + 1];
             const uint4 xhi0 = xv[8 * g + 4 + 2 * c], xhi1 = xv[8 * g + 4 + 2 * c + 1];
             const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
@@ -219,356 +186,323 @@ __device__ __forceinline__ float half_block_scale(const uint4 &hd, int hh, const
     return fmaf(dv, r, -dmin * rm);
 }
 
-// Dot product of one half-block of packed weights (header at blk, codes of
-// half hh) with a quantised vector half-block held in registers (xv: 128
-// int16), its scale and its four sub-block sums.
-__device__ __forceinline__ float half_block_dot(const uint8_t *blk, int hh, const uint4 (&xv)[16],
-                                                float vscale, const float (&vsum)[4]) {
-    const uint4 hd = *reinterpret_cast<const uint4 *>(blk);
-    int acc[4];
-    half_block_isums(blk, hh, xv, acc);
-    return half_block_scale(hd, hh, acc, vscale, vsum);
+// One half-block of a packed row from global memory: the block header and
+// the 64 code bytes of half hh.
+struct HalfCodes {
+    uint4 hd;
+    uint4 qv[4];
+};
+__device__ __forceinline__ void load_codes(const uint8_t *blk, int hh, HalfCodes &c) {
+    c.hd = ldg_stream(blk);
+    const uint8_t *q = blk + 16 + 64 * hh;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c.qv[i] = ldg_stream(q + 16 * i);
 }
 
-// Two rows at once (same half-block slot): independent work for the
-// scheduler to interleave.
-__device__ __forceinline__ void half_block_dot2(const uint8_t *blk0, const uint8_t *blk1, int hh,
-                                                const uint4 (&xv)[16], float vscale,
-                                                const float (&vsum)[4], float &r0, float &r1) {
-    const uint4 hd0 = *reinterpret_cast<const uint4 *>(blk0);
-    const uint4 hd1 = *reinterpret_cast<const uint4 *>(blk1);
-    int acc0[4], acc1[4];
-    half_block_isums(blk0, hh, xv, acc0);
-    half_block_isums(blk1, hh, xv, acc1);
-    r0 = half_block_scale(hd0, hh, acc0, vscale, vsum);
-    r1 = half_block_scale(hd1, hh, acc1, vscale, vsum);
-}
-
-__device__ __forceinline__ void load_half(const uint8_t *vec, const float *vscale,
-                                          const float *vsum, int hb, uint4 (&xv)[16], float &sc,
+__device__ __forceinline__ void load_half(const DecVec &V, int hb, uint4 (&xv)[16], float &sc,
                                           float (&sm)[4]) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(vec + (size_t)hb * kHalfBytes);
+    const uint4 *src = reinterpret_cast<const uint4 *>(V.vec + (size_t)hb * kHalfBytes);
 #pragma unroll
     for (int i = 0; i < 16; ++i) xv[i] = src[i];
-    sc = vscale[hb];
+    sc = V.vscale[hb];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) sm[j] = vsum[4 * hb + j];
+    for (int j = 0; j < 4; ++j) sm[j] = V.vsum[4 * hb + j];
 }
 
-// A lane keeps one vector half-block in registers when it always owns the
-// same slot of a row: rows of at most 32 slots (slot = lane mod slots), or
-// rows of several 32-slot chunks when the consumer warps split evenly into
-// one class per chunk position.
-__device__ __forceinline__ bool slot_resident(int Lp) {
-    return Lp <= 32 || kMvConsumerWarps % (Lp >> 5) == 0;
-}
-__device__ __forceinline__ int lane_slot(int Lp, int warp, int lane) {
-    return Lp <= 32 ? (lane & (Lp - 1)) : (warp % (Lp >> 5)) * 32 + lane;
-}
-
-// Shared-memory views of one block.
-struct MvShared {
-    uint8_t *ring, *vec;
-    float *vscale, *vsum, *acc, *yacc;
-    uint64_t *full, *empty, *xready;
-};
-__device__ __forceinline__ MvShared mv_shared(uint8_t *smem, const MvSmem &L) {
-    MvShared S;
-    S.ring = smem + L.ring;
-    S.vec = smem + L.vec;
-    S.vscale = reinterpret_cast<float *>(smem + L.vscale);
-    S.vsum = reinterpret_cast<float *>(smem + L.vsum);
-    S.acc = reinterpret_cast<float *>(smem + L.acc);      // [2][kMvMaxRows]
-    S.yacc = reinterpret_cast<float *>(smem + L.yacc);    // [kMvMaxRows]
-    S.full = reinterpret_cast<uint64_t *>(smem + L.bars);
-    S.empty = S.full + kMvStages;
-    S.xready = S.empty + kMvStages;
-    return S;
-}
-
-// Quantise nhalf vector half-blocks into S; load4(hb) returns this lane's four
+// Quantise nhalf vector half-blocks into V; load4(hb) returns this lane's four
 // values of half-block hb.  A warp issues the loads of up to 8 of its
 // half-blocks before using any, so the vector arrives in one round trip.
 template <class Load4>
-__device__ __forceinline__ void quantize_vector(const MvShared &S, int nhalf, int warp, int lane,
+__device__ __forceinline__ void quantize_vector(const DecVec &V, int nhalf, int warp, int lane,
                                                 Load4 load4) {
-    for (int b0 = warp; b0 < nhalf; b0 += 8 * kMvConsumerWarps) {
+    for (int b0 = warp; b0 < nhalf; b0 += 8 * kDecWarps) {
         float4 v[8];
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-            const int hb = b0 + t * kMvConsumerWarps;
+            const int hb = b0 + t * kDecWarps;
             v[t] = load4(hb < nhalf ? hb : b0);   // always a valid half-block: no branch
         }
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-            const int hb = b0 + t * kMvConsumerWarps;
+            const int hb = b0 + t * kDecWarps;
             if (hb < nhalf)
-                quantize_half(v[t], lane, S.vec + (size_t)hb * kHalfBytes, S.vscale + hb, S.vsum + 4 * hb);
+                quantize_half(v[t], lane, V.vec + (size_t)hb * kHalfBytes, V.vscale + hb, V.vsum + 4 * hb);
         }
     }
 }
 
-// The consumer side's copy of one vector half-block kept in registers.
-struct VecReg {
-    uint4 xr[16];
-    float xs = 0.0f, xsum[4] = {0.f, 0.f, 0.f, 0.f};
+// Half-block slots per row: the real count 2*nb rounded up to a power of two
+// when it is at most 32, so that a warp holds 32 / slots whole rows.
+__host__ __device__ inline int slots_per_row(int nb) {
+    const int lr = 2 * nb;
+    int lp = 1;
+    while (lp < lr) lp <<= 1;
+    return lp;
+}
+
+// Per-warp double buffer: slot bytes sized for the larger of a gate/up pass
+// and a down row.
+struct WarpRing {
+    uint8_t *slot0, *slot1;
+    uint64_t *bar0, *bar1;
+    // selects rather than an indexed array, which would live in local memory
+    __device__ __forceinline__ uint8_t *slot(int b) const { return b ? slot1 : slot0; }
+    __device__ __forceinline__ uint64_t *bar(int b) const { return b ? bar1 : bar0; }
 };
-
-// Load this lane's resident half-block of the vector starting at vec_base.
-__device__ __forceinline__ void load_resident(const MvShared &S, VecReg &R, int nb, int vec_base,
-                                              int warp, int lane) {
-    const int Lp = slots_per_row(nb);
-    if (!slot_resident(Lp)) return;
-    const int q = lane_slot(Lp, warp, lane);
-    if (q < 2 * nb) load_half(S.vec, S.vscale, S.vsum, vec_base + q, R.xr, R.xs, R.xsum);
+__host__ __device__ inline int64_t dec_slot_bytes(const DecGeom &g, int Lp, bool down) {
+    if (down) return (int64_t)g.P * g.rbI;
+    const int rpc = Lp <= 32 ? 32 / Lp : 1;
+    return 2 * (int64_t)rpc * g.rbH;
 }
 
-// Process one stage: nmat matrices of nrows rows with nb blocks each; each
-// row's dot product with the vector half-blocks starting at vec_base lands in
-// acc[mat][row].  Rows hold slots_per_row(nb) slots (half-blocks, the real
-// ones first).  With a resident vector the lane's half-block is already in R.
-__device__ __forceinline__ void process_stage(const MvShared &S, const uint8_t *base, const VecReg &R,
-                                              int nmat, int nrows, int nb, int64_t rb, int vec_base,
-                                              int warp, int lane) {
-    const int Lr = 2 * nb;
-    const int Lp = slots_per_row(nb);
-    const int nrg = nmat * nrows;
-    auto write = [&](int rowg, float v, bool add) {
-        const int mat = rowg >= nrows;
-        float *dst = &S.acc[mat * kMvMaxRows + rowg - mat * nrows];
-        if (add) atomicAdd(dst, v); else *dst = v;
-    };
-    if (Lp <= 32) {
-        int lg = 0;
-        while ((1 << lg) < Lp) ++lg;
-        const int rpc = 32 >> lg;                     // rows per chunk
-        const int chunks = (nrg + rpc - 1) / rpc;
-        const int q = lane & (Lp - 1);
-        // two chunks per pass (c and c + kMvConsumerWarps) for instruction-level parallelism
-        for (int c = warp; c < chunks; c += 2 * kMvConsumerWarps) {
-            const int c2 = c + kMvConsumerWarps;
-            const int rowg = c * rpc + (lane >> lg), rowg2 = c2 * rpc + (lane >> lg);
-            const bool v1 = rowg < nrg && q < Lr, v2 = c2 < chunks && rowg2 < nrg && q < Lr;
-            float part = 0.0f, part2 = 0.0f;
-            const int64_t off = (q >> 1) * kBlockBytes;
-            if (v1 && v2)
-                half_block_dot2(base + (int64_t)rowg * rb + off, base + (int64_t)rowg2 * rb + off, q & 1,
-                                R.xr, R.xs, R.xsum, part, part2);
-            else if (v1)
-                part = half_block_dot(base + (int64_t)rowg * rb + off, q & 1, R.xr, R.xs, R.xsum);
-            for (int o = Lp >> 1; o > 0; o >>= 1) {
-                part += __shfl_xor_sync(0xffffffffu, part, o);
-                part2 += __shfl_xor_sync(0xffffffffu, part2, o);
-            }
-            if (rowg < nrg && q == 0) write(rowg, part, false);
-            if (c2 < chunks && rowg2 < nrg && q == 0) write(rowg2, part2, false);
-        }
-    } else if (slot_resident(Lp)) {
-        const int cpr = Lp >> 5;
-        const int q = lane_slot(Lp, warp, lane);
-        const int rstep = kMvConsumerWarps / cpr;
-        for (int rowg = warp / cpr; rowg < nrg; rowg += 2 * rstep) {
-            const int rowg2 = rowg + rstep;
-            float part = 0.0f, part2 = 0.0f;
-            const int64_t off = (q >> 1) * kBlockBytes;
-            if (q < Lr) {
-                if (rowg2 < nrg)
-                    half_block_dot2(base + (int64_t)rowg * rb + off, base + (int64_t)rowg2 * rb + off, q & 1,
-                                    R.xr, R.xs, R.xsum, part, part2);
-                else
-                    part = half_block_dot(base + (int64_t)rowg * rb + off, q & 1, R.xr, R.xs, R.xsum);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                part += __shfl_xor_sync(0xffffffffu, part, o);
-                part2 += __shfl_xor_sync(0xffffffffu, part2, o);
-            }
-            if (lane == 0) {
-                write(rowg, part, true);
-                if (rowg2 < nrg) write(rowg2, part2, true);
-            }
-        }
-    } else {
-        const int cpr = Lp >> 5;
-        for (int c = warp; c < nrg * cpr; c += kMvConsumerWarps) {
-            const int rowg = c / cpr;
-            const int q = (c - rowg * cpr) * 32 + lane;
-            float part = 0.0f;
-            if (q < Lr) {
-                uint4 xv[16];
-                float sc, sm[4];
-                load_half(S.vec, S.vscale, S.vsum, vec_base + q, xv, sc, sm);
-                part = half_block_dot(base + (int64_t)rowg * rb + (q >> 1) * kBlockBytes, q & 1, xv, sc, sm);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-            if (lane == 0) write(rowg, part, true);
-        }
-    }
-}
-
-__device__ __forceinline__ void init_ring(const MvShared &S) {
-    if (threadIdx.x == 0) {
-        for (int st = 0; st < kMvStages; ++st) {
-            mbar_init(&S.full[st], 1);
-            mbar_init(&S.empty[st], 1);
-        }
-        mbar_init(S.xready, kMvConsumerWarps);
-        fence_mbarrier_init();
-    }
-    __syncthreads();
-}
-
-// The producer waits (bounded) until the consumers released every stage,
-// i.e. until every copy it issued has landed and been read.
-__device__ __forceinline__ void drain_ring(const MvShared &S, uint32_t slot, uint32_t ph, int *err) {
-    for (int st = 0; st < kMvStages; ++st) {
-        mbar_wait(&S.empty[slot], ph ^ 1, nullptr, err, kWaitBudgetCycles / 8);
-        if (++slot == kMvStages) { slot = 0; ph ^= 1; }
-    }
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
 }
 
 // ----------------------------------------------------------------------------
 // A: gate and up rows -> h
 // ----------------------------------------------------------------------------
-__global__ void __launch_bounds__(kMvThreads, 1) ffn_gu_kernel(MatvecArgs a) {
+// Shared memory: [x raw bf16 (H*2)] [x quantised (nhalf1 half-blocks)]
+// [x bar] [per warp: 2 slot barriers, 2 slots].
+__host__ __device__ inline size_t gu_smem_bytes(const DecGeom &g, int H) {
+    const int Lp = slots_per_row(g.nbH);
+    const size_t slot = (size_t)((dec_slot_bytes(g, Lp, false) + 127) & ~(int64_t)127);
+    size_t o = ((size_t)H * 2 + 127) & ~(size_t)127;
+    o += (dec_smem_bytes(g.nhalf1) + 127) & ~(size_t)127;
+    o += 8 + (size_t)kDecWarps * 2 * 8;
+    o = (o + 127) & ~(size_t)127;
+    o += (size_t)kDecWarps * 2 * slot;
+    return o;
+}
+
+__global__ void __launch_bounds__(kDecThreads, 1) ffn_gu_kernel(MatvecArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
-    const MvGeom G = mv_geom(a.H, a.I, a.k);
-    const MvShared S = mv_shared(smem, mv_smem_layout(G));
+    const DecGeom G = dec_geom(a.H, a.I, a.k);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int I = a.I, P = G.P;
+    const int H = a.H, I = a.I, P = G.P;
     const bool moe = a.ids != nullptr;
     auto expert_of = [&](int p) -> int { return moe ? a.ids[p] : 0; };
     auto valid = [&](int e) -> bool { return e >= 0 && e < a.E; };
     const int64_t rows1 = (int64_t)P * I;
     const int r0 = (int)(rows1 * blockIdx.x / gridDim.x), r1 = (int)(rows1 * (blockIdx.x + 1) / gridDim.x);
+    const int Lr = 2 * G.nbH;
+    const int Lp = slots_per_row(G.nbH);
 
-    init_ring(S);
-    // the down-projection kernel may be scheduled as soon as SMs free up
-    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // carve shared memory
+    uint8_t *x_raw = smem;
+    size_t o = ((size_t)H * 2 + 127) & ~(size_t)127;
+    const DecVec V = dec_vec(smem + o, G.nhalf1);
+    o += (dec_smem_bytes(G.nhalf1) + 127) & ~(size_t)127;
+    uint64_t *xbar = reinterpret_cast<uint64_t *>(smem + o);
+    uint64_t *wbars = xbar + 1;
+    o += 8 + (size_t)kDecWarps * 2 * 8;
+    o = (o + 127) & ~(size_t)127;
+    const size_t slot_bytes = (size_t)((dec_slot_bytes(G, Lp, false) + 127) & ~(int64_t)127);
+    WarpRing ring;
+    ring.slot0 = smem + o + (size_t)warp * 2 * slot_bytes;
+    ring.slot1 = ring.slot0 + slot_bytes;
+    ring.bar0 = wbars + 2 * warp;
+    ring.bar1 = wbars + 2 * warp + 1;
 
-    if (warp == kMvConsumerWarps) {
-        // ------------------------- producer -------------------------------
-        if (lane == 0) {
-            uint32_t slot = 0, ph = 0;
-            bool ok = mbar_wait(S.xready, 0, nullptr, a.err);
-            // stages: chunks of up to R1 rows within one slot p
-            for (int r = r0; r < r1 && ok;) {
-                const int p = r / I, i = r % I;
-                const int cnt = min(min(G.R1, r1 - r), I - i);
-                const int e = expert_of(p);
-                if (valid(e)) {
-                    if (!mbar_wait(&S.empty[slot], ph ^ 1, nullptr, a.err)) { ok = false; break; }
-                    const uint32_t bytes = (uint32_t)(cnt * G.rbH);
-                    mbar_arrive_expect_tx(&S.full[slot], 2 * bytes);
-                    uint8_t *dst = S.ring + slot * kMvStageBytes;
-                    bulk_g2s(dst, a.Wg + ((int64_t)e * I + i) * G.rbH, bytes, &S.full[slot]);
-                    bulk_g2s(dst + bytes, a.Wu + ((int64_t)e * I + i) * G.rbH, bytes, &S.full[slot]);
-                    if (++slot == kMvStages) { slot = 0; ph ^= 1; }
-                }
-                r += cnt;
-            }
-            drain_ring(S, slot, ph, a.err);
-        }
-        return;
+    if (threadIdx.x == 0) {
+        mbar_init(xbar, 1);
+        for (int i = 0; i < 2 * kDecWarps; ++i) mbar_init(&wbars[i], 1);
+        fence_mbarrier_init();
+        // x first: the weight stream starts once x is in, so that this small
+        // load does not queue behind it
+        mbar_arrive_expect_tx(xbar, (uint32_t)(H * 2));
+        bulk_g2s(x_raw, a.x, (uint32_t)(H * 2), xbar);
+    }
+    __syncthreads();
+    if (!mbar_wait(xbar, 0, nullptr, a.err)) return;
+    if (threadIdx.x == 0) {
+        // the down-projection kernel may be scheduled as soon as SMs free up
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     }
 
-    // ----------------------------- consumers ---------------------------------
-    const int tid = threadIdx.x;
-    uint32_t slot = 0, ph = 0;
-    bool ok = true;
-    for (int t = tid; t < 3 * kMvMaxRows; t += kMvConsumers) S.acc[t] = 0.0f;   // acc and yacc
-    quantize_vector(S, G.nhalf1, warp, lane, [&](int hb) -> float4 {
-        const uint2 raw = *reinterpret_cast<const uint2 *>(a.x + hb * 128 + 4 * lane);
+    // the rows of a pass: rpc consecutive row pairs (Lr <= 32) or one
+    const int rpc = Lr <= 32 ? 32 / Lp : 1;
+    const int pass_stride = kDecWarps * rpc;
+    // lane 0 copies the packed rows of the pass starting at pair r into slot b
+    auto issue = [&](int r, int b) -> bool {
+        if (r >= r1) return false;
+        uint32_t bytes = 0;
+        for (int t = 0; t < rpc && r + t < r1; ++t) {
+            const int e = expert_of((r + t) / I);
+            if (valid(e)) bytes += 2 * (uint32_t)G.rbH;
+        }
+        if (bytes == 0) return false;
+        mbar_arrive_expect_tx(ring.bar(b), bytes);
+        for (int t = 0; t < rpc && r + t < r1; ++t) {
+            const int p = (r + t) / I, i = (r + t) % I;
+            const int e = expert_of(p);
+            if (!valid(e)) continue;
+            uint8_t *dst = ring.slot(b) + (size_t)t * 2 * G.rbH;
+            bulk_g2s(dst, a.Wg + ((int64_t)e * I + i) * G.rbH, (uint32_t)G.rbH, ring.bar(b));
+            bulk_g2s(dst + G.rbH, a.Wu + ((int64_t)e * I + i) * G.rbH, (uint32_t)G.rbH, ring.bar(b));
+        }
+        return true;
+    };
+    // bit b of pend: slot b holds a pass in flight; bit b of ph: its phase
+    uint32_t pend = 0, ph = 0;
+    const int first = r0 + warp * rpc;
+    if (lane == 0) pend = (issue(first, 0) ? 1u : 0u) | (issue(first + pass_stride, 1) ? 2u : 0u);
+    pend = __shfl_sync(0xffffffffu, pend, 0);
+
+    // quantise x (each warp its share of half-blocks)
+    quantize_vector(V, G.nhalf1, warp, lane, [&](int hb) -> float4 {
+        const uint2 raw = *reinterpret_cast<const uint2 *>(x_raw + (size_t)(hb * 128 + 4 * lane) * 2);
         return make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
                            __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
     });
-    // x is in: the weight stream may start now
-    __syncwarp();
-    if (lane == 0) mbar_arrive(S.xready);
-    consumers_sync();
-    VecReg R;
-    load_resident(S, R, G.nbH, 0, warp, lane);
-    for (int r = r0; r < r1 && ok;) {
-        const int p = r / I, i = r % I;
-        const int cnt = min(min(G.R1, r1 - r), I - i);
-        const int e = expert_of(p);
-        if (!valid(e)) {
-            for (int t = tid; t < cnt; t += kMvConsumers) a.h[(int64_t)p * I + i + t] = 0.0f;
-            r += cnt;
-            continue;
+    __syncthreads();
+
+    int lg = 0;
+    while ((1 << lg) < Lp && (1 << lg) < 32) ++lg;
+    const int q = Lr <= 32 ? (lane & (Lp - 1)) : lane;
+    uint4 xr[16];
+    float xs = 0.0f, xsum[4] = {0.f, 0.f, 0.f, 0.f};
+    if (Lr <= 32 && q < Lr) load_half(V, q, xr, xs, xsum);
+
+    int b = 0;
+    for (int pp = first; pp < r1; pp += pass_stride, b ^= 1) {
+        const bool have = (pend >> b) & 1;
+        if (have && !mbar_wait(ring.bar(b), (ph >> b) & 1, nullptr, a.err)) return;
+        if (have) ph ^= 1u << b;
+        const uint8_t *slot = ring.slot(b);
+        float g = 0.0f, u = 0.0f;
+        int r;
+        if (Lr <= 32) {
+            const int t = lane >> lg;
+            r = pp + t;
+            if (have && r < r1 && q < Lr && valid(expert_of(r / I))) {
+                const uint8_t *rowg = slot + (size_t)t * 2 * G.rbH + (size_t)(q >> 1) * kBlockBytes;
+                const uint8_t *rowu = rowg + G.rbH;
+                const uint4 hg = *reinterpret_cast<const uint4 *>(rowg);
+                const uint4 hu = *reinterpret_cast<const uint4 *>(rowu);
+                uint4 cg[4], cu[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    cg[i] = *reinterpret_cast<const uint4 *>(rowg + 16 + 64 * (q & 1) + 16 * i);
+                    cu[i] = *reinterpret_cast<const uint4 *>(rowu + 16 + 64 * (q & 1) + 16 * i);
+                }
+                int ag[4], au[4];
+                half_block_isums(cg, xr, ag);
+                half_block_isums(cu, xr, au);
+                g = half_block_scale(hg, q & 1, ag, xs, xsum);
+                u = half_block_scale(hu, q & 1, au, xs, xsum);
+            }
+            for (int o2 = Lp >> 1; o2 > 0; o2 >>= 1) {
+                g += __shfl_xor_sync(0xffffffffu, g, o2);
+                u += __shfl_xor_sync(0xffffffffu, u, o2);
+            }
+        } else {
+            r = pp;
+            if (have && valid(expert_of(r / I))) {
+                for (int qq = lane; qq < Lr; qq += 32) {
+                    uint4 xv[16];
+                    float vs, vsm[4];
+                    load_half(V, qq, xv, vs, vsm);
+                    const uint8_t *rowg = slot + (size_t)(qq >> 1) * kBlockBytes;
+                    const uint8_t *rowu = rowg + G.rbH;
+                    const uint4 hg = *reinterpret_cast<const uint4 *>(rowg);
+                    const uint4 hu = *reinterpret_cast<const uint4 *>(rowu);
+                    uint4 cg[4], cu[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        cg[i] = *reinterpret_cast<const uint4 *>(rowg + 16 + 64 * (qq & 1) + 16 * i);
+                        cu[i] = *reinterpret_cast<const uint4 *>(rowu + 16 + 64 * (qq & 1) + 16 * i);
+                    }
+                    int ag[4], au[4];
+                    half_block_isums(cg, xv, ag);
+                    half_block_isums(cu, xv, au);
+                    g += half_block_scale(hg, qq & 1, ag, vs, vsm);
+                    u += half_block_scale(hu, qq & 1, au, vs, vsm);
+                }
+            }
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) {
+                g += __shfl_xor_sync(0xffffffffu, g, o2);
+                u += __shfl_xor_sync(0xffffffffu, u, o2);
+            }
         }
-        if (!mbar_wait(&S.full[slot], ph, nullptr, a.err)) { ok = false; break; }
-        process_stage(S, S.ring + slot * kMvStageBytes, R, 2, cnt, G.nbH, G.rbH, 0, warp, lane);
-        consumers_sync();
-        if (tid == 0) mbar_arrive(&S.empty[slot]);
-        if (++slot == kMvStages) { slot = 0; ph ^= 1; }
-        if (tid < cnt) {
-            const float g = S.acc[tid], u = S.acc[kMvMaxRows + tid];
-            a.h[(int64_t)p * I + i + tid] = g / (1.0f + expf(-g)) * u;
-            S.acc[tid] = 0.0f;
-            S.acc[kMvMaxRows + tid] = 0.0f;
+        // the slot is free once every lane has read it: refill it two passes on
+        __syncwarp();
+        if (lane == 0) pend = (pend & ~(1u << b)) | (issue(pp + 2 * pass_stride, b) ? 1u << b : 0u);
+        pend = __shfl_sync(0xffffffffu, pend, 0);
+        const bool writer = Lr <= 32 ? (q == 0 && r < r1) : lane == 0;
+        if (writer) {
+            const int p = r / I, i = r % I;
+            a.h[(int64_t)p * I + i] = g / (1.0f + expf(-g)) * u;
         }
-        consumers_sync();
-        r += cnt;
     }
 }
 
 // ----------------------------------------------------------------------------
 // B: down rows, y = sum_p w_p * Wd_p . h_p
 // ----------------------------------------------------------------------------
-__global__ void __launch_bounds__(kMvThreads, 1) ffn_down_kernel(MatvecArgs a) {
+// Shared memory: [h quantised (nhalf2)] [per warp: 2 slot barriers] [per
+// warp: 2 slots of one row of every expert slot].
+__host__ __device__ inline size_t down_smem_bytes(const DecGeom &g, int depth) {
+    const size_t slot = (size_t)((dec_slot_bytes(g, 0, true) + 127) & ~(int64_t)127);
+    size_t o = (dec_smem_bytes(g.nhalf2) + 127) & ~(size_t)127;
+    o += (size_t)kDecWarps * 2 * 8;
+    o = (o + 127) & ~(size_t)127;
+    o += (size_t)kDecWarps * depth * slot;
+    return o;
+}
+
+__global__ void __launch_bounds__(kDecThreads, 1) ffn_down_kernel(MatvecArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
-    const MvGeom G = mv_geom(a.H, a.I, a.k);
-    const MvShared S = mv_shared(smem, mv_smem_layout(G));
+    const DecGeom G = dec_geom(a.H, a.I, a.k);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = a.H, I = a.I, P = G.P;
     const bool moe = a.ids != nullptr;
-    auto expert_of = [&](int p) -> int { return moe ? a.ids[p] : 0; };
-    auto valid = [&](int e) -> bool { return e >= 0 && e < a.E; };
     const int n0 = (int)((int64_t)H * blockIdx.x / gridDim.x), n1 = (int)((int64_t)H * (blockIdx.x + 1) / gridDim.x);
 
-    init_ring(S);
-
-    if (warp == kMvConsumerWarps) {
-        // ---- producer: W_down does not depend on A, so it streams at once;
-        // after two stages it waits until the consumers hold h, so that the
-        // h loads do not queue behind the rest of the weight stream ----
-        if (lane == 0) {
-            uint32_t slot = 0, ph = 0;
-            bool ok = true;
-            int issued = 0;
-            // for each chunk of up to R2 output rows, one stage per valid slot
-            for (int n = n0; n < n1 && ok;) {
-                const int cnt = min(G.R2, n1 - n);
-                for (int p = 0; p < P && ok; ++p) {
-                    const int e = expert_of(p);
-                    if (!valid(e)) continue;
-                    if (issued == 2 && !mbar_wait(S.xready, 0, nullptr, a.err)) { ok = false; break; }
-                    if (!mbar_wait(&S.empty[slot], ph ^ 1, nullptr, a.err)) { ok = false; break; }
-                    ++issued;
-                    const uint32_t bytes = (uint32_t)(cnt * G.rbI);
-                    mbar_arrive_expect_tx(&S.full[slot], bytes);
-                    bulk_g2s(S.ring + slot * kMvStageBytes, a.Wd + ((int64_t)e * H + n) * G.rbI, bytes,
-                             &S.full[slot]);
-                    if (++slot == kMvStages) { slot = 0; ph ^= 1; }
-                }
-                n += cnt;
-            }
-            drain_ring(S, slot, ph, a.err);
-        }
-        return;
+    const DecVec V = dec_vec(smem, G.nhalf2);
+    size_t o = (dec_smem_bytes(G.nhalf2) + 127) & ~(size_t)127;
+    uint64_t *wbars = reinterpret_cast<uint64_t *>(smem + o);
+    o += (size_t)kDecWarps * 2 * 8;
+    o = (o + 127) & ~(size_t)127;
+    const size_t slot_bytes = (size_t)((dec_slot_bytes(G, 0, true) + 127) & ~(int64_t)127);
+    WarpRing ring;
+    ring.slot0 = smem + o + (size_t)warp * a.ring_depth * slot_bytes;
+    ring.slot1 = ring.slot0 + (a.ring_depth == 2 ? slot_bytes : 0);
+    ring.bar0 = wbars + 2 * warp;
+    ring.bar1 = wbars + 2 * warp + 1;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2 * kDecWarps; ++i) mbar_init(&wbars[i], 1);
+        fence_mbarrier_init();
     }
+    __syncthreads();
 
-    // ----------------------------- consumers ---------------------------------
-    const int tid = threadIdx.x;
-    uint32_t slot = 0, ph = 0;
-    bool ok = true;
-    for (int t = tid; t < 3 * kMvMaxRows; t += kMvConsumers) S.acc[t] = 0.0f;   // acc and yacc
+    // lane 0 copies row n of every valid expert slot into slot b
+    auto issue = [&](int n, int b) -> bool {
+        if (n >= n1) return false;
+        uint32_t bytes = 0;
+        for (int p = 0; p < P; ++p) {
+            const int e = moe ? a.ids[p] : 0;
+            if (e >= 0 && e < a.E) bytes += (uint32_t)G.rbI;
+        }
+        if (bytes == 0) return false;
+        mbar_arrive_expect_tx(ring.bar(b), bytes);
+        for (int p = 0; p < P; ++p) {
+            const int e = moe ? a.ids[p] : 0;
+            if (e < 0 || e >= a.E) continue;
+            bulk_g2s(ring.slot(b) + (size_t)p * G.rbI, a.Wd + ((int64_t)e * H + n) * G.rbI, (uint32_t)G.rbI,
+                     ring.bar(b));
+        }
+        return true;
+    };
     // h is written by the gate/up kernel: wait until that grid has completed
     // and its memory is visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    quantize_vector(S, G.nhalf2, warp, lane, [&](int hb) -> float4 {
+    quantize_vector(V, G.nhalf2, warp, lane, [&](int hb) -> float4 {
         const int p = hb / (2 * G.nbI), hl = hb - p * (2 * G.nbI);
         const int col = hl * 128 + 4 * lane;
         // load from a valid address whatever the column, then zero past I
@@ -577,76 +511,99 @@ __global__ void __launch_bounds__(kMvThreads, 1) ffn_down_kernel(MatvecArgs a) {
         if (col >= I) v = make_float4(0.f, 0.f, 0.f, 0.f);
         return v;
     });
-    __syncwarp();
-    if (lane == 0) mbar_arrive(S.xready);
-    consumers_sync();
-    VecReg R;
-    int loaded_p = -1;
-    for (int n = n0; n < n1 && ok;) {
-        const int cnt = min(G.R2, n1 - n);
-        for (int p = 0; p < P && ok; ++p) {
-            const int e = expert_of(p);
-            if (!valid(e)) continue;
-            if (p != loaded_p) {
-                load_resident(S, R, G.nbI, p * 2 * G.nbI, warp, lane);
-                loaded_p = p;
-            }
-            if (!mbar_wait(&S.full[slot], ph, nullptr, a.err)) { ok = false; break; }
-            process_stage(S, S.ring + slot * kMvStageBytes, R, 1, cnt, G.nbI, G.rbI, p * 2 * G.nbI, warp,
-                          lane);
-            consumers_sync();
-            if (tid == 0) mbar_arrive(&S.empty[slot]);
-            if (++slot == kMvStages) { slot = 0; ph ^= 1; }
-            if (tid < cnt) {
-                const float w = moe ? a.wts[p] : 1.0f;
-                S.yacc[tid] += w * S.acc[tid];
-                S.acc[tid] = 0.0f;
-            }
-            consumers_sync();
-        }
-        if (tid < cnt) {
-            float *dst = a.y + n + tid;
-            *dst = a.accumulate ? *dst + S.yacc[tid] : S.yacc[tid];
-            S.yacc[tid] = 0.0f;
-        }
-        consumers_sync();
-        n += cnt;
+    // The W_down rows are copied only now, so that the h loads above do not
+    // queue behind them.
+    // bit b of pend: slot b holds a row in flight; bit b of ph: its phase.
+    // With a one-slot ring (long rows) slot 1 aliases slot 0 and is unused.
+    const int depth = a.ring_depth;
+    uint32_t pend = 0, ph = 0;
+    const int first = n0 + warp;
+    if (lane == 0) {
+        pend = issue(first, 0) ? 1u : 0u;
+        if (depth == 2 && issue(first + kDecWarps, 1)) pend |= 2u;
     }
+    pend = __shfl_sync(0xffffffffu, pend, 0);
+    __syncthreads();
+
+    // a row's work items are its (slot p, half-block q) pairs; lanes take
+    // items lane, lane + 32, ... and the warp sums them
+    const int Lr2 = 2 * G.nbI;
+    const int items = P * Lr2;
+    int b = 0;
+    for (int n = first; n < n1; n += kDecWarps, b = depth == 2 ? b ^ 1 : 0) {
+        const bool have = (pend >> b) & 1;
+        if (have && !mbar_wait(ring.bar(b), (ph >> b) & 1, nullptr, a.err)) return;
+        if (have) ph ^= 1u << b;
+        float acc = 0.0f;
+        if (have) {
+            for (int it = lane; it < items; it += 32) {
+                const int p = it / Lr2, q = it - p * Lr2;
+                const int e = moe ? a.ids[p] : 0;
+                if (e < 0 || e >= a.E) continue;
+                uint4 xv[16];
+                float xs, xsum[4];
+                load_half(V, it, xv, xs, xsum);
+                const uint8_t *blk = ring.slot(b) + (size_t)p * G.rbI + (size_t)(q >> 1) * kBlockBytes;
+                const uint4 hd = *reinterpret_cast<const uint4 *>(blk);
+                uint4 cq[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) cq[i] = *reinterpret_cast<const uint4 *>(blk + 16 + 64 * (q & 1) + 16 * i);
+                int ai[4];
+                half_block_isums(cq, xv, ai);
+                const float w = moe ? a.wts[p] : 1.0f;
+                acc = fmaf(w, half_block_scale(hd, q & 1, ai, xs, xsum), acc);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) pend = (pend & ~(1u << b)) | (issue(n + depth * kDecWarps, b) ? 1u << b : 0u);
+        pend = __shfl_sync(0xffffffffu, pend, 0);
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o2);
+        if (lane == 0) {
+            float *dst = a.y + n;
+            *dst = a.accumulate ? *dst + acc : acc;
+        }
+    }
+}
+
+size_t gu_smem_total(int H, int I, int k) { return gu_smem_bytes(dec_geom(H, I, k), H); }
+// The down kernel double-buffers its rows when that fits a block's shared
+// memory, else it single-buffers (long rows).
+int down_ring_depth(int H, int I, int k) {
+    return down_smem_bytes(dec_geom(H, I, k), 2) <= (size_t)device_info().max_smem_optin ? 2 : 1;
+}
+size_t down_smem_total(int H, int I, int k) {
+    return down_smem_bytes(dec_geom(H, I, k), down_ring_depth(H, I, k));
 }
 
 cudaError_t launch_ffn_matvec(const MatvecArgs &a, cudaStream_t s) {
     const DeviceInfo &di = device_info();
     if (a.T != 1) return cudaErrorInvalidValue;
-    const size_t smem = matvec_smem_bytes(1, a.H, a.I, a.k);
+    const DecGeom G = dec_geom(a.H, a.I, a.k);
+    const int depth = down_ring_depth(a.H, a.I, a.k);
+    const size_t smem_a = gu_smem_bytes(G, a.H), smem_b = down_smem_bytes(G, depth);
     static int attr_device = -1;
-    if (attr_device != di.device) {
-        cudaError_t e = cudaFuncSetAttribute(ffn_gu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+    static size_t attr_a = 0, attr_b = 0;
+    if (attr_device != di.device || attr_a < smem_a || attr_b < smem_b) {
+        // the attributes hold the largest requests so far
+        const bool same = attr_device == di.device;
+        const size_t wa = same && attr_a > smem_a ? attr_a : smem_a;
+        const size_t wb = same && attr_b > smem_b ? attr_b : smem_b;
+        cudaError_t e = cudaFuncSetAttribute(ffn_gu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wa);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(ffn_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem);
+            e = cudaFuncSetAttribute(ffn_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wb);
         if (e != cudaSuccess) return e;
         attr_device = di.device;
-    } else {
-        // the attribute holds the largest request so far; grow it when needed
-        cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, ffn_gu_kernel) == cudaSuccess &&
-            (size_t)fa.maxDynamicSharedSizeBytes < smem) {
-            cudaError_t e = cudaFuncSetAttribute(ffn_gu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)smem);
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(ffn_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-            if (e != cudaSuccess) return e;
-        }
+        attr_a = wa;
+        attr_b = wb;
     }
-    const int grid = di.num_sms;   // one block per SM
     MatvecArgs args = a;
+    args.ring_depth = depth;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kMvThreads);
-    cfg.dynamicSmemBytes = smem;
+    cfg.gridDim = dim3(di.num_sms);   // one block per SM
+    cfg.blockDim = dim3(kDecThreads);
     cfg.stream = s;
+    cfg.dynamicSmemBytes = smem_a;
     cudaError_t e = cudaLaunchKernelEx(&cfg, ffn_gu_kernel, args);
     if (e != cudaSuccess) return e;
     // the down kernel is a programmatic dependent of the gate/up kernel
@@ -655,6 +612,7 @@ cudaError_t launch_ffn_matvec(const MatvecArgs &a, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    cfg.dynamicSmemBytes = smem_b;
     return cudaLaunchKernelEx(&cfg, ffn_down_kernel, args);
 }
 

@@ -174,10 +174,6 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-__device__ __forceinline__ void prefetch_l2_bulk(const void *gptr, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gptr), "r"(bytes) : "memory");
-}
-
 // ---- tcgen05 ---------------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -408,6 +404,7 @@ struct MatvecArgs {
     int *err;
     int T, H, I, E, k;
     bool accumulate;             // y += result instead of y = result
+    int ring_depth;              // set by the launcher: row buffers per warp in the down kernel
 };
 size_t matvec_smem_bytes(int T, int H, int I, int k);
 cudaError_t launch_ffn_matvec(const MatvecArgs &a, cudaStream_t s);
