@@ -87,38 +87,6 @@ __device__ __forceinline__ DecVec dec_vec(uint8_t *smem, int nhalf) {
     return V;
 }
 
-// 16 bytes from global memory that this launch only reads (no L1 allocation:
-// every byte is used once).
-__device__ __forceinline__ uint4 ldg_stream(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-// Quantise one 128-element half-block of a vector (one warp, 4 values per
-// lane): int16 values, the half-block scale and the four sub-block sums.
-__device__ __forceinline__ void quantize_half(const float4 v4, int lane, uint8_t *vec_hb,
-                                              float *scale, float *sums) {
-    const float v[4] = {v4.x, v4.y, v4.z, v4.w};
-    float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const float inv = m > 0.0f ? 32766.0f / m : 0.0f;
-    int q[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) q[j] = __float2int_rn(v[j] * inv);
-    const uint32_t w0 = (uint32_t)(q[0] & 0xFFFF) | ((uint32_t)q[1] << 16);
-    const uint32_t w1 = (uint32_t)(q[2] & 0xFFFF) | ((uint32_t)q[3] << 16);
-    *reinterpret_cast<uint2 *>(vec_hb + 8 * lane) = make_uint2(w0, w1);
-    float s = (v[0] + v[1]) + (v[2] + v[3]);
-#pragma unroll
-    for (int o = 4; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if ((lane & 7) == 0) sums[lane >> 3] = s;
-    if (lane == 0) *scale = m > 0.0f ? m / 32766.0f : 0.0f;
-}
-
 // The 6-bit scales and mins of the four sub-blocks 4*hh .. 4*hh+3 of a
 // block, one per byte: sub-block j < 4 keeps its scale and min in the low six
 // bits of scale bytes j and 4+j; sub-block j >= 4 keeps their low four bits in
@@ -186,19 +154,6 @@ __device__ __forceinline__ float half_block_scale(const uint4 &hd, int hh, const
     return fmaf(dv, r, -dmin * rm);
 }
 
-// One half-block of a packed row from global memory: the block header and
-// the 64 code bytes of half hh.
-struct HalfCodes {
-    uint4 hd;
-    uint4 qv[4];
-};
-__device__ __forceinline__ void load_codes(const uint8_t *blk, int hh, HalfCodes &c) {
-    c.hd = ldg_stream(blk);
-    const uint8_t *q = blk + 16 + 64 * hh;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) c.qv[i] = ldg_stream(q + 16 * i);
-}
-
 __device__ __forceinline__ void load_half(const DecVec &V, int hb, uint4 (&xv)[16], float &sc,
                                           float (&sm)[4]) {
     const uint4 *src = reinterpret_cast<const uint4 *>(V.vec + (size_t)hb * kHalfBytes);
@@ -209,24 +164,54 @@ __device__ __forceinline__ void load_half(const DecVec &V, int hb, uint4 (&xv)[1
     for (int j = 0; j < 4; ++j) sm[j] = V.vsum[4 * hb + j];
 }
 
-// Quantise nhalf vector half-blocks into V; load4(hb) returns this lane's four
-// values of half-block hb.  A warp issues the loads of up to 8 of its
-// half-blocks before using any, so the vector arrives in one round trip.
-template <class Load4>
-__device__ __forceinline__ void quantize_vector(const DecVec &V, int nhalf, int warp, int lane,
+// Quantise the half-blocks wi, wi + nw, wi + 2*nw, ... of a vector into V
+// (warp wi of nw; each lane holds four values of a half-block): int16 values
+// scaled by 32766 / max|v|, the half-block scale max|v| / 32766 and the fp32
+// sum of every 32-element sub-block.  NT half-blocks are taken per round and
+// computed without branches, so that their loads, shuffles and divisions
+// overlap; only the stores are predicated.  load4(hb) returns this lane's
+// four values of half-block hb.
+template <int NT, class Load4>
+__device__ __forceinline__ void quantize_vector(const DecVec &V, int nhalf, int wi, int nw, int lane,
                                                 Load4 load4) {
-    for (int b0 = warp; b0 < nhalf; b0 += 8 * kDecWarps) {
-        float4 v[8];
+    for (int b0 = wi; b0 < nhalf; b0 += NT * nw) {
+        float4 v[NT];
+        float m[NT], sm[NT];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            const int hb = b0 + t * kDecWarps;
-            v[t] = load4(hb < nhalf ? hb : b0);   // always a valid half-block: no branch
+        for (int t = 0; t < NT; ++t) {
+            const int hb = b0 + t * nw;
+            v[t] = load4(hb < nhalf ? hb : b0);   // always a valid half-block
         }
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            const int hb = b0 + t * kDecWarps;
-            if (hb < nhalf)
-                quantize_half(v[t], lane, V.vec + (size_t)hb * kHalfBytes, V.vscale + hb, V.vsum + 4 * hb);
+        for (int t = 0; t < NT; ++t) {
+            m[t] = fmaxf(fmaxf(fabsf(v[t].x), fabsf(v[t].y)), fmaxf(fabsf(v[t].z), fabsf(v[t].w)));
+            sm[t] = (v[t].x + v[t].y) + (v[t].z + v[t].w);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int t = 0; t < NT; ++t) m[t] = fmaxf(m[t], __shfl_xor_sync(0xffffffffu, m[t], o));
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1)
+#pragma unroll
+            for (int t = 0; t < NT; ++t) sm[t] += __shfl_xor_sync(0xffffffffu, sm[t], o);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const int hb = b0 + t * nw;
+            const float inv = m[t] > 0.0f ? 32766.0f / m[t] : 0.0f;
+            // round to nearest: |v * inv| <= 32766 < 2^22, so adding 1.5 * 2^23
+            // leaves the rounded integer in the low mantissa bits
+            const int q0 = __float_as_int(fmaf(v[t].x, inv, 12582912.0f)) - 0x4B400000;
+            const int q1 = __float_as_int(fmaf(v[t].y, inv, 12582912.0f)) - 0x4B400000;
+            const int q2 = __float_as_int(fmaf(v[t].z, inv, 12582912.0f)) - 0x4B400000;
+            const int q3 = __float_as_int(fmaf(v[t].w, inv, 12582912.0f)) - 0x4B400000;
+            if (hb < nhalf) {
+                *reinterpret_cast<uint2 *>(V.vec + (size_t)hb * kHalfBytes + 8 * lane) =
+                    make_uint2((uint32_t)(q0 & 0xFFFF) | ((uint32_t)q1 << 16),
+                               (uint32_t)(q2 & 0xFFFF) | ((uint32_t)q3 << 16));
+                if ((lane & 7) == 0) V.vsum[4 * hb + (lane >> 3)] = sm[t];
+                if (lane == 0) V.vscale[hb] = m[t] > 0.0f ? m[t] / 32766.0f : 0.0f;
+            }
         }
     }
 }
@@ -249,6 +234,17 @@ struct WarpRing {
     __device__ __forceinline__ uint8_t *slot(int b) const { return b ? slot1 : slot0; }
     __device__ __forceinline__ uint64_t *bar(int b) const { return b ? bar1 : bar0; }
 };
+// The ring of warp w: its depth slots of slot_bytes each from slots, its two
+// barriers from bars.  With depth 1 slot 1 aliases slot 0 and is unused.
+__device__ __forceinline__ WarpRing warp_ring(uint8_t *slots, size_t slot_bytes, int depth, uint64_t *bars,
+                                              int w) {
+    WarpRing r;
+    r.slot0 = slots + (size_t)w * depth * slot_bytes;
+    r.slot1 = r.slot0 + (depth == 2 ? slot_bytes : 0);
+    r.bar0 = bars + 2 * w;
+    r.bar1 = bars + 2 * w + 1;
+    return r;
+}
 __host__ __device__ inline int64_t dec_slot_bytes(const DecGeom &g, int Lp, bool down) {
     if (down) return (int64_t)g.P * g.rbI;
     const int rpc = Lp <= 32 ? 32 / Lp : 1;
@@ -302,59 +298,59 @@ __global__ void __launch_bounds__(kDecThreads, 1) ffn_gu_kernel(MatvecArgs a) {
     o += 8 + (size_t)kDecWarps * 2 * 8;
     o = (o + 127) & ~(size_t)127;
     const size_t slot_bytes = (size_t)((dec_slot_bytes(G, Lp, false) + 127) & ~(int64_t)127);
-    WarpRing ring;
-    ring.slot0 = smem + o + (size_t)warp * 2 * slot_bytes;
-    ring.slot1 = ring.slot0 + slot_bytes;
-    ring.bar0 = wbars + 2 * warp;
-    ring.bar1 = wbars + 2 * warp + 1;
+    uint8_t *const slots = smem + o;
+    const WarpRing ring = warp_ring(slots, slot_bytes, 2, wbars, warp);
+
+    // the rows of a pass: rpc consecutive row pairs (Lr <= 32) or one
+    const int rpc = Lr <= 32 ? 32 / Lp : 1;
+    const int pass_stride = kDecWarps * rpc;
+    // bytes of the pass starting at pair r (0: nothing to copy)
+    auto pass_bytes = [&](int r) -> uint32_t {
+        uint32_t bytes = 0;
+        for (int t = 0; t < rpc && r + t < r1; ++t)
+            if (valid(expert_of((r + t) / I))) bytes += 2 * (uint32_t)G.rbH;
+        return bytes;
+    };
+    // copy the packed rows of the pass starting at pair r into slot b of rg
+    auto issue = [&](const WarpRing &rg, int r, int b, uint32_t bytes) {
+        mbar_arrive_expect_tx(rg.bar(b), bytes);
+        for (int t = 0; t < rpc && r + t < r1; ++t) {
+            const int p = (r + t) / I, i = (r + t) % I;
+            const int e = expert_of(p);
+            if (!valid(e)) continue;
+            uint8_t *dst = rg.slot(b) + (size_t)t * 2 * G.rbH;
+            bulk_g2s(dst, a.Wg + ((int64_t)e * I + i) * G.rbH, (uint32_t)G.rbH, rg.bar(b));
+            bulk_g2s(dst + G.rbH, a.Wu + ((int64_t)e * I + i) * G.rbH, (uint32_t)G.rbH, rg.bar(b));
+        }
+    };
+    const int first = r0 + warp * rpc;
 
     if (threadIdx.x == 0) {
         mbar_init(xbar, 1);
         for (int i = 0; i < 2 * kDecWarps; ++i) mbar_init(&wbars[i], 1);
         fence_mbarrier_init();
-        // x first: the weight stream starts once x is in, so that this small
-        // load does not queue behind it
         mbar_arrive_expect_tx(xbar, (uint32_t)(H * 2));
         bulk_g2s(x_raw, a.x, (uint32_t)(H * 2), xbar);
     }
     __syncthreads();
-    if (!mbar_wait(xbar, 0, nullptr, a.err)) return;
-    if (threadIdx.x == 0) {
-        // the down-projection kernel may be scheduled as soon as SMs free up
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    }
-
-    // the rows of a pass: rpc consecutive row pairs (Lr <= 32) or one
-    const int rpc = Lr <= 32 ? 32 / Lp : 1;
-    const int pass_stride = kDecWarps * rpc;
-    // lane 0 copies the packed rows of the pass starting at pair r into slot b
-    auto issue = [&](int r, int b) -> bool {
-        if (r >= r1) return false;
-        uint32_t bytes = 0;
-        for (int t = 0; t < rpc && r + t < r1; ++t) {
-            const int e = expert_of((r + t) / I);
-            if (valid(e)) bytes += 2 * (uint32_t)G.rbH;
-        }
-        if (bytes == 0) return false;
-        mbar_arrive_expect_tx(ring.bar(b), bytes);
-        for (int t = 0; t < rpc && r + t < r1; ++t) {
-            const int p = (r + t) / I, i = (r + t) % I;
-            const int e = expert_of(p);
-            if (!valid(e)) continue;
-            uint8_t *dst = ring.slot(b) + (size_t)t * 2 * G.rbH;
-            bulk_g2s(dst, a.Wg + ((int64_t)e * I + i) * G.rbH, (uint32_t)G.rbH, ring.bar(b));
-            bulk_g2s(dst + G.rbH, a.Wu + ((int64_t)e * I + i) * G.rbH, (uint32_t)G.rbH, ring.bar(b));
-        }
-        return true;
-    };
+    // the down-projection kernel may be scheduled as soon as SMs free up
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Each warp's first two passes, queued behind x.  A bulk copy stalls the
+    // thread that issues it for a few hundred cycles whatever its size, so
+    // every warp issues its own (in parallel) rather than one thread all.
     // bit b of pend: slot b holds a pass in flight; bit b of ph: its phase
     uint32_t pend = 0, ph = 0;
-    const int first = r0 + warp * rpc;
-    if (lane == 0) pend = (issue(first, 0) ? 1u : 0u) | (issue(first + pass_stride, 1) ? 2u : 0u);
-    pend = __shfl_sync(0xffffffffu, pend, 0);
-
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        const int r = first + b * pass_stride;
+        const uint32_t bytes = r < r1 ? pass_bytes(r) : 0u;
+        if (bytes && lane == 0) issue(ring, r, b, bytes);
+        if (bytes) pend |= 1u << b;
+    }
+    __syncwarp();
     // quantise x (each warp its share of half-blocks)
-    quantize_vector(V, G.nhalf1, warp, lane, [&](int hb) -> float4 {
+    if (!mbar_wait(xbar, 0, nullptr, a.err)) return;
+    quantize_vector<4>(V, G.nhalf1, warp, kDecWarps, lane, [&](int hb) -> float4 {
         const uint2 raw = *reinterpret_cast<const uint2 *>(x_raw + (size_t)(hb * 128 + 4 * lane) * 2);
         return make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
                            __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
@@ -432,8 +428,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) ffn_gu_kernel(MatvecArgs a) {
         }
         // the slot is free once every lane has read it: refill it two passes on
         __syncwarp();
-        if (lane == 0) pend = (pend & ~(1u << b)) | (issue(pp + 2 * pass_stride, b) ? 1u << b : 0u);
-        pend = __shfl_sync(0xffffffffu, pend, 0);
+        {
+            const int rn = pp + 2 * pass_stride;
+            const uint32_t bytes = rn < r1 ? pass_bytes(rn) : 0u;
+            if (bytes && lane == 0) issue(ring, rn, b, bytes);
+            pend = (pend & ~(1u << b)) | (bytes ? 1u << b : 0u);
+        }
         const bool writer = Lr <= 32 ? (q == 0 && r < r1) : lane == 0;
         if (writer) {
             const int p = r / I, i = r % I;
@@ -470,39 +470,45 @@ __global__ void __launch_bounds__(kDecThreads, 1) ffn_down_kernel(MatvecArgs a) 
     o += (size_t)kDecWarps * 2 * 8;
     o = (o + 127) & ~(size_t)127;
     const size_t slot_bytes = (size_t)((dec_slot_bytes(G, 0, true) + 127) & ~(int64_t)127);
-    WarpRing ring;
-    ring.slot0 = smem + o + (size_t)warp * a.ring_depth * slot_bytes;
-    ring.slot1 = ring.slot0 + (a.ring_depth == 2 ? slot_bytes : 0);
-    ring.bar0 = wbars + 2 * warp;
-    ring.bar1 = wbars + 2 * warp + 1;
+    uint8_t *const slots = smem + o;
+    const int depth = a.ring_depth;
+    const WarpRing ring = warp_ring(slots, slot_bytes, depth, wbars, warp);
+    // bytes of a row: one W_down row per valid expert slot
+    uint32_t row_bytes = 0;
+    for (int p = 0; p < P; ++p) {
+        const int e = moe ? a.ids[p] : 0;
+        if (e >= 0 && e < a.E) row_bytes += (uint32_t)G.rbI;
+    }
+    // copy row n of every valid expert slot into slot b of rg
+    auto issue = [&](const WarpRing &rg, int n, int b) {
+        mbar_arrive_expect_tx(rg.bar(b), row_bytes);
+        for (int p = 0; p < P; ++p) {
+            const int e = moe ? a.ids[p] : 0;
+            if (e < 0 || e >= a.E) continue;
+            bulk_g2s(rg.slot(b) + (size_t)p * G.rbI, a.Wd + ((int64_t)e * H + n) * G.rbI, (uint32_t)G.rbI,
+                     rg.bar(b));
+        }
+    };
+    const int first = n0 + warp;
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2 * kDecWarps; ++i) mbar_init(&wbars[i], 1);
         fence_mbarrier_init();
     }
     __syncthreads();
-
-    // lane 0 copies row n of every valid expert slot into slot b
-    auto issue = [&](int n, int b) -> bool {
-        if (n >= n1) return false;
-        uint32_t bytes = 0;
+    // W_down does not depend on the gate/up kernel: its rows are streamed
+    // into L2 now, while the gate/up kernel finishes.  (Copies into shared
+    // memory issued now would hold up the loads of h behind them.)  The rows
+    // of one expert slot are contiguous: one request each.
+    if (threadIdx.x == 0 && n1 > n0)
         for (int p = 0; p < P; ++p) {
             const int e = moe ? a.ids[p] : 0;
-            if (e >= 0 && e < a.E) bytes += (uint32_t)G.rbI;
+            if (e >= 0 && e < a.E)
+                prefetch_l2_bulk(a.Wd + ((int64_t)e * H + n0) * G.rbI, (uint32_t)((n1 - n0) * G.rbI));
         }
-        if (bytes == 0) return false;
-        mbar_arrive_expect_tx(ring.bar(b), bytes);
-        for (int p = 0; p < P; ++p) {
-            const int e = moe ? a.ids[p] : 0;
-            if (e < 0 || e >= a.E) continue;
-            bulk_g2s(ring.slot(b) + (size_t)p * G.rbI, a.Wd + ((int64_t)e * H + n) * G.rbI, (uint32_t)G.rbI,
-                     ring.bar(b));
-        }
-        return true;
-    };
     // h is written by the gate/up kernel: wait until that grid has completed
     // and its memory is visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    quantize_vector(V, G.nhalf2, warp, lane, [&](int hb) -> float4 {
+    quantize_vector<8>(V, G.nhalf2, warp, kDecWarps, lane, [&](int hb) -> float4 {
         const int p = hb / (2 * G.nbI), hl = hb - p * (2 * G.nbI);
         const int col = hl * 128 + 4 * lane;
         // load from a valid address whatever the column, then zero past I
@@ -511,18 +517,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) ffn_down_kernel(MatvecArgs a) 
         if (col >= I) v = make_float4(0.f, 0.f, 0.f, 0.f);
         return v;
     });
-    // The W_down rows are copied only now, so that the h loads above do not
-    // queue behind them.
-    // bit b of pend: slot b holds a row in flight; bit b of ph: its phase.
-    // With a one-slot ring (long rows) slot 1 aliases slot 0 and is unused.
-    const int depth = a.ring_depth;
+    // bit b of pend: slot b holds a row in flight; bit b of ph: its phase
     uint32_t pend = 0, ph = 0;
-    const int first = n0 + warp;
-    if (lane == 0) {
-        pend = issue(first, 0) ? 1u : 0u;
-        if (depth == 2 && issue(first + kDecWarps, 1)) pend |= 2u;
+    for (int b = 0; b < depth; ++b) {
+        const int n = first + b * kDecWarps;
+        if (row_bytes && n < n1) {
+            if (lane == 0) issue(ring, n, b);
+            pend |= 1u << b;
+        }
     }
-    pend = __shfl_sync(0xffffffffu, pend, 0);
     __syncthreads();
 
     // a row's work items are its (slot p, half-block q) pairs; lanes take
@@ -555,8 +558,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) ffn_down_kernel(MatvecArgs a) 
             }
         }
         __syncwarp();
-        if (lane == 0) pend = (pend & ~(1u << b)) | (issue(n + depth * kDecWarps, b) ? 1u << b : 0u);
-        pend = __shfl_sync(0xffffffffu, pend, 0);
+        {
+            const int nn = n + depth * kDecWarps;
+            const bool more = row_bytes && nn < n1;
+            if (more && lane == 0) issue(ring, nn, b);
+            pend = (pend & ~(1u << b)) | (more ? 1u << b : 0u);
+        }
 #pragma unroll
         for (int o2 = 16; o2 > 0; o2 >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o2);
         if (lane == 0) {
