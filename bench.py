@@ -7,7 +7,10 @@ Default workload: one 4096 -> 11008 -> 4096 Q4_K SwiGLU layer at T=2048 tokens
 (bf16 activations with 1% outlier rows x20, weights N(0, 0.02) quantised with
 the min/max quantiser; seed 2).  A step is one call of the block over the
 whole batch, inputs resident in HBM, L2 flushed (512 MB write) between steps
-outside the timed events.  Under torchrun each rank runs its own replica of
+outside the timed events.  The single-token dense workload instead rotates over
+eleven copies of its weights (836 MB, more than six L2s) and runs its steps
+back to back, as consecutive layers of a decode step do: every step still streams its
+weights from HBM.  Under torchrun each rank runs its own replica of
 the workload on its own GPU (no collective on the data path: tokens are
 independent), so the scaling is weak and `value` is the tokens of all ranks
 divided by the slowest rank's time.
@@ -271,9 +274,21 @@ def run_gpu(args):
     wbytes = sum(w.numel() for w in W)
     n_sets = 1
     if name == "decode_T1" or name == "moe_T1":
-        n_sets = max(1, math.ceil(3 * 129e6 / wbytes))
+        # between two uses of a copy at least six L2s' worth of other copies
+        # stream through, so (whatever the replacement policy) next to none
+        # of it is still in L2
+        n_sets = max(1, math.ceil(6 * 129e6 / wbytes) + 1)
     sets = [W] + [[w.clone() for w in W] for _ in range(n_sets - 1)]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    # Dense decode touches all of a copy every step, and the copies together
+    # exceed the L2, so its steps need no flush.  (The routed layer touches
+    # only the token's experts, which could stay in L2 across copies: it is
+    # flushed.)
+    flush_between = name != "decode_T1"
+
+    def maybe_flush():
+        if flush_between:
+            flush.zero_()
     y = torch.empty((T, H), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     zffn.reserve(max(T, 1), H, I, E, k)
@@ -302,40 +317,44 @@ def run_gpu(args):
             dist.barrier()
 
     for s in range(args.warmup):
-        flush.zero_()
+        maybe_flush()
         call(s)
     torch.cuda.synchronize()
     assert zffn.get_device_error() == zffn.OK
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    def timed(step_fn):
+        """Mean device time of one step over args.steps steps: events around
+        each step when the L2 is flushed between steps (outside the events),
+        else one pair of events around the back-to-back steps."""
+        if flush_between:
+            st = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+            en = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+            for s in range(args.steps):
+                maybe_flush()
+                st[s].record(stream)
+                step_fn(s)
+                en[s].record(stream)
+            torch.cuda.synchronize()
+            return statistics.mean(a.elapsed_time(b) for a, b in zip(st, en))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s in range(args.steps):
+            step_fn(s)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         wall0 = time.perf_counter()
-        for s in range(args.steps):
-            flush.zero_()
-            starts[s].record(stream)
-            call(s)
-            ends[s].record(stream)
-        torch.cuda.synchronize()
+        ms = timed(lambda s: call(s))
         wall = time.perf_counter() - wall0
         barrier()
         # the dominant kernel alone: the residual entry skips the zero fill
-        kst = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        ken = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        for s in range(args.steps):
-            flush.zero_()
-            kst[s].record(stream)
-            call(s, residual=True)
-            ken[s].record(stream)
-        torch.cuda.synchronize()
+        kms = timed(lambda s: call(s, residual=True))
     clocks = clk.summary()
     assert zffn.get_device_error() == zffn.OK
-    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    kern_ms = [a.elapsed_time(b) for a, b in zip(kst, ken)]
-    ms = statistics.mean(step_ms)
-    kms = statistics.mean(kern_ms)
 
     # end to end through the public API with pinned host buffers
     x_host = torch.empty(x_for(0).shape, dtype=torch.bfloat16, pin_memory=True)
@@ -343,18 +362,13 @@ def run_gpu(args):
     y_host = torch.empty((x_host.shape[0], H), dtype=torch.float32, pin_memory=True)
     x_dev = torch.empty_like(x_for(0))
     y_e2e = torch.empty((x_host.shape[0], H), dtype=torch.float32, device=dev)
-    est = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    een = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier()
-    for s in range(args.steps):
-        flush.zero_()
-        est[s].record(stream)
+
+    def e2e_step(s):
         x_dev.copy_(x_host, non_blocking=True)
         call(s, out=y_e2e, xin=x_dev)
         y_host.copy_(y_e2e, non_blocking=True)
-        een[s].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(est, een))
+    e2e_ms = timed(e2e_step)
 
     if world > 1:
         t = torch.tensor([ms, kms, e2e_ms], device=dev, dtype=torch.float64)
@@ -399,8 +413,11 @@ def run_gpu(args):
             "name": name, "T": T, "H": H, "I": I,
             **({"E": E, "top_k": k} if kind == "moe" else {}),
             "parallelism": "replicas" if world > 1 else "single-gpu",
-            "l2": "flushed between steps (512 MB write outside the timed events)"
-                  + (f"; weights rotated over {n_sets} copies" if n_sets > 1 else ""),
+            "l2": ("flushed between steps (512 MB write outside the timed events)"
+                   + (f"; weights rotated over {n_sets} copies" if n_sets > 1 else ""))
+                  if flush_between else
+                  (f"inputs larger than L2: weights rotated over {n_sets} copies "
+                   f"({n_sets * wbytes / 1e6:.0f} MB), steps back to back, no flush"),
         },
         "tflops": round(tflops, 2),
         "roofline": {

@@ -14,7 +14,11 @@
 //            this block.  Expert ids are read on the device ("Bottleneck 2").
 // B's blocks start on the SMs that A's blocks leave; their reads of h wait
 // (griddepcontrol) until A has completed, so the dependency is carried by the
-// hardware's grid completion, not by a software grid barrier.
+// hardware's grid completion, not by a software grid barrier.  A is in turn a
+// programmatic dependent of the work before it in the stream (typically the
+// previous call's B): its blocks start as that work's blocks leave and wait
+// for its completion before touching global memory, which takes the launch
+// of A off the critical path of back-to-back calls.
 //
 // Data movement: every block of A first copies x into shared memory (a bulk
 // copy that nothing else is queued behind: a weight stream started earlier
@@ -325,6 +329,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) ffn_gu_kernel(MatvecArgs a) {
     };
     const int first = r0 + warp * rpc;
 
+    // This kernel may be launched as a programmatic dependent of the work
+    // before it in the stream (the previous call's down kernel, say): its
+    // blocks then start as that work's blocks leave, and wait here, before
+    // touching global memory, until that work has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (threadIdx.x == 0) {
         mbar_init(xbar, 1);
         for (int i = 0; i < 2 * kDecWarps; ++i) mbar_init(&wbars[i], 1);
@@ -495,6 +504,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) ffn_down_kernel(MatvecArgs a) 
         fence_mbarrier_init();
     }
     __syncthreads();
+    // the next work in the stream (the next call's gate/up kernel, say) may
+    // be scheduled as this kernel's blocks leave; it waits for this kernel's
+    // completion itself
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // W_down does not depend on the gate/up kernel: its rows are streamed
     // into L2 now, while the gate/up kernel finishes.  (Copies into shared
     // memory issued now would hold up the loads of h behind them.)  The rows
@@ -611,14 +624,16 @@ cudaError_t launch_ffn_matvec(const MatvecArgs &a, cudaStream_t s) {
     cfg.blockDim = dim3(kDecThreads);
     cfg.stream = s;
     cfg.dynamicSmemBytes = smem_a;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, ffn_gu_kernel, args);
-    if (e != cudaSuccess) return e;
-    // the down kernel is a programmatic dependent of the gate/up kernel
+    // both kernels are programmatic dependents of what precedes them: the
+    // gate/up kernel of the stream's previous work, the down kernel of the
+    // gate/up kernel
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, ffn_gu_kernel, args);
+    if (e != cudaSuccess) return e;
     cfg.dynamicSmemBytes = smem_b;
     return cudaLaunchKernelEx(&cfg, ffn_down_kernel, args);
 }
