@@ -8,7 +8,7 @@ Default workload: one 4096 -> 11008 -> 4096 Q4_K SwiGLU layer at T=2048 tokens
 the min/max quantiser; seed 2).  A step is one call of the block over the
 whole batch, inputs resident in HBM, L2 flushed (512 MB write) between steps
 outside the timed events.  The single-token dense workload instead rotates over
-eleven copies of its weights (836 MB, more than six L2s) and runs its steps
+twelve copies of its weights (913 MB, more than six L2s) and runs its steps
 back to back, as consecutive layers of a decode step do: every step still streams its
 weights from HBM.  Under torchrun each rank runs its own replica of
 the workload on its own GPU (no collective on the data path: tokens are
