@@ -182,7 +182,7 @@ __device__ __forceinline__ uint32_t sw128_row(int r) {
 // fused multiply-add per weight.  The constant is rounded once, an error
 // below 2^-13 of one quantisation step, far under the bf16 rounding of the
 // result.
-__device__ __forceinline__ void unpack_row_to_smem(uint4 hd, const uint32_t (&w)[8], int g,
+__device__ __forceinline__ void unpack_row_to_smem_wide(uint4 hd, const uint32_t (&w)[8], int g,
                                                    uint32_t row_addr, int row) {
     const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
     int sc0, m0, sc1, m1;
@@ -218,6 +218,53 @@ __device__ __forceinline__ void unpack_row_to_smem(uint4 hd, const uint32_t (&w)
         st_shared_v4(row_addr + (((uint32_t)((c + 4) ^ (row & 7))) << 4), hi[4 * c],
                      hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
     }
+}
+
+// The same, storing each 16-byte chunk as soon as it is formed: fewer live
+// registers (the single-CTA kernel unpacks two tasks per step and would
+// otherwise spill).
+__device__ __forceinline__ void unpack_row_to_smem_narrow(uint4 hd, const uint32_t (&w)[8], int g,
+                                                   uint32_t row_addr, int row) {
+    const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
+    int sc0, m0, sc1, m1;
+    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g, sc0, m0);
+    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g + 1, sc1, m1);
+    const float a0 = 128.0f * (d * (float)sc0);
+    const float c0 = -(a0 + dmin * (float)m0);
+    const float a1 = 2048.0f * (d * (float)sc1);
+    const float c1 = -(a1 + dmin * (float)m1);
+    constexpr uint32_t ONE = 0x3F800000u, MLO = 0x000F0000u, MHI = 0x0000F000u;
+    // 16-byte chunk c holds weights 8c..8c+7 (chunks 0-3 low nibbles, 4-7
+    // high); two code words make a chunk, stored as soon as it is formed
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t lo[4], hi[4];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const uint32_t x = w[2 * c + k], xl8 = x << 8, xr8 = x >> 8, xl16 = x << 16, xr16 = x >> 16;
+            const float l0 = fmaf(a0, __uint_as_float((xl16 & MLO) | ONE), c0);
+            const float l1 = fmaf(a0, __uint_as_float((xl8 & MLO) | ONE), c0);
+            const float l2 = fmaf(a0, __uint_as_float((x & MLO) | ONE), c0);
+            const float l3 = fmaf(a0, __uint_as_float((xr8 & MLO) | ONE), c0);
+            const float h0 = fmaf(a1, __uint_as_float((xl8 & MHI) | ONE), c1);
+            const float h1 = fmaf(a1, __uint_as_float((x & MHI) | ONE), c1);
+            const float h2 = fmaf(a1, __uint_as_float((xr8 & MHI) | ONE), c1);
+            const float h3 = fmaf(a1, __uint_as_float((xr16 & MHI) | ONE), c1);
+            lo[2 * k] = pack_bf16x2(l0, l1);
+            lo[2 * k + 1] = pack_bf16x2(l2, l3);
+            hi[2 * k] = pack_bf16x2(h0, h1);
+            hi[2 * k + 1] = pack_bf16x2(h2, h3);
+        }
+        st_shared_v4(row_addr + (((uint32_t)(c ^ (row & 7))) << 4), lo[0], lo[1], lo[2], lo[3]);
+        st_shared_v4(row_addr + (((uint32_t)((c + 4) ^ (row & 7))) << 4), hi[0], hi[1], hi[2], hi[3]);
+    }
+}
+
+template <bool PAIR>
+__device__ __forceinline__ void unpack_row_to_smem(uint4 hd, const uint32_t (&w)[8], int g, uint32_t row_addr,
+                                                   int row) {
+    if (PAIR) unpack_row_to_smem_wide(hd, w, g, row_addr, row);
+    else unpack_row_to_smem_narrow(hd, w, g, row_addr, row);
 }
 
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
@@ -615,7 +662,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!mbar_wait(&b_empty[bi], bph ^ 1, abort_flag, p.err)) { ok = false; break; }
                 const uint32_t rb = s_b + bi * C::B_BYTES + half * (C::ROWS_Y * 128) + sw128_row(row);
                 const uint32_t w8[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                unpack_row_to_smem(hd, w8, g, rb, row);
+                unpack_row_to_smem<PAIR>(hd, w8, g, rb, row);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) arrive_leader(&b_full[bi]);
