@@ -27,6 +27,10 @@
  *   - Mixture of experts: y_t = sum_j w_{t,j} FFN_{e_{t,j}}(x_t), expert ids and
  *     weights given per token ("Four bottlenecks, one CUDA backend...",
  *     section "Bottleneck 2 -- MoE decode was paying for its routing twice").
+ *   - The router that chooses them: per token, the top_k experts by logit,
+ *     then softmax weights over the chosen logits (same page and section:
+ *     the layer computes router logits and picks the top-k experts; the
+ *     softmax over the chosen k is the reading used throughout).
  *
  * Precision: Q4_K dequantisation is done in fp32 exactly as the format states
  * (both products are exact in fp32, so only the final subtraction rounds); the
@@ -316,4 +320,58 @@ void oracle_moe_swiglu_ffn(const uint16_t *x, const int32_t *ids, const float *w
         }
     }
     free(yt);
+}
+
+/* Router: for each token t, the top_k of its E logits and their softmax
+ * weights.  Order: a ranks above b when a's logit is larger, or the logits
+ * are equal and a's index is lower; a NaN logit ranks below every number
+ * (-inf included) and NaNs among themselves by index; -0 equals +0.  ids[t]
+ * lists the chosen experts from the highest rank down.  weights[t][j] =
+ * exp(l_j - l_0) / sum_i exp(l_i - l_0) over the chosen logits (l_0 the
+ * highest), evaluated in fp64 and rounded once to fp32.  Selection is plain:
+ * top_k passes, each taking the best expert not taken yet. */
+static int router_ranks_above(float a, int64_t ia, float b, int64_t ib)
+{
+    int na = isnan(a), nb = isnan(b);
+    if (na || nb) {
+        if (na && nb)
+            return ia < ib;
+        return nb; /* the number ranks above the NaN */
+    }
+    if (a != b)
+        return a > b;
+    return ia < ib;
+}
+
+void oracle_route_top_k(const float *logits, int64_t T, int64_t E, int64_t top_k,
+                        int32_t *ids, float *weights)
+{
+    unsigned char *taken = (unsigned char *)malloc((size_t)(E > 0 ? E : 1));
+    double *ex = (double *)malloc(sizeof(double) * (size_t)(top_k > 0 ? top_k : 1));
+    for (int64_t t = 0; t < T; ++t) {
+        const float *l = logits + t * E;
+        for (int64_t e = 0; e < E; ++e)
+            taken[e] = 0;
+        for (int64_t j = 0; j < top_k; ++j) {
+            int64_t best = -1;
+            for (int64_t e = 0; e < E; ++e) {
+                if (taken[e])
+                    continue;
+                if (best < 0 || router_ranks_above(l[e], e, l[best], best))
+                    best = e;
+            }
+            taken[best] = 1;
+            ids[t * top_k + j] = (int32_t)best;
+        }
+        double top = (double)l[ids[t * top_k]];
+        double sum = 0.0;
+        for (int64_t j = 0; j < top_k; ++j) {
+            ex[j] = exp((double)l[ids[t * top_k + j]] - top);
+            sum += ex[j];
+        }
+        for (int64_t j = 0; j < top_k; ++j)
+            weights[t * top_k + j] = (float)(ex[j] / sum);
+    }
+    free(taken);
+    free(ex);
 }

@@ -66,6 +66,7 @@ def _load():
             lib.oracle_q4k_quantize.argtypes = [P, P, I64, I64]
             lib.oracle_swiglu_ffn.argtypes = [P, P, P, P, I64, I64, I64, P]
             lib.oracle_moe_swiglu_ffn.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, I64, P]
+            lib.oracle_route_top_k.argtypes = [P, I64, I64, I64, P, P]
             for f in ("oracle_q4k_dequant", "oracle_q4k_quantize",
                       "oracle_swiglu_ffn", "oracle_moe_swiglu_ffn",
                       "oracle_q4k_scale_min"):
@@ -158,3 +159,18 @@ def moe_swiglu_ffn(x_bf16: np.ndarray, ids: np.ndarray, wts: np.ndarray,
     _load().oracle_moe_swiglu_ffn(_ptr(x_bf16), _ptr(ids), _ptr(wts), _ptr(Wg), _ptr(Wu),
                                   _ptr(Wd), T, H, I, E, top_k, _ptr(y))
     return y
+
+
+def route_top_k(logits: np.ndarray, top_k: int):
+    """(ids int32 [T, top_k], weights float32 [T, top_k]) for logits [T, E].
+
+    The top_k experts of each token from the highest logit down (ties to the
+    lower index, NaN below every number), with softmax weights over the chosen
+    logits, evaluated in fp64 and rounded once to fp32."""
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    T, E = logits.shape
+    assert 1 <= top_k <= E
+    ids = np.empty((T, top_k), dtype=np.int32)
+    w = np.empty((T, top_k), dtype=np.float32)
+    _load().oracle_route_top_k(_ptr(logits), T, E, top_k, _ptr(ids), _ptr(w))
+    return ids, w

@@ -406,3 +406,82 @@ def test_intermediate_byte_model_matches_pages():
     assert round(I / H, 1) == g["width_ratio"]
     # 4.5 bits per weight for Q4_K (144 bytes per 256 weights)
     assert 144 * 8 / 256 == g["q4k_bits_per_weight"]
+
+
+# ---- router: top-k ids and softmax weights ------------------------------------
+
+def _softmax64(v):
+    v = np.asarray(v, dtype=np.float64)
+    e = np.exp(v - v.max())
+    return e / e.sum()
+
+
+def test_router_matches_stable_sort_and_softmax():
+    # Integer-valued logits in a small range make ties common; a stable sort of
+    # the negated logits orders equal logits by index, which is the stated
+    # tie rule, so it must pick the same ids in the same order.
+    rng = np.random.default_rng(21)
+    for T, E, k in [(64, 128, 8), (16, 37, 5), (8, 4096, 64), (5, 3, 3)]:
+        logits = rng.integers(-6, 7, size=(T, E)).astype(np.float32)
+        logits[: T // 2] += rng.standard_normal((T // 2, E)).astype(np.float32)
+        ids, w = orc.route_top_k(logits, k)
+        order = np.argsort(-logits, axis=1, kind="stable")[:, :k]
+        assert np.array_equal(ids, order.astype(np.int32))
+        for t in range(T):
+            ref = _softmax64(logits[t, order[t]]).astype(np.float32)
+            np.testing.assert_allclose(w[t], ref, rtol=2e-7, atol=0)
+
+
+def test_router_closed_forms():
+    # equal logits: the first k indices, weight 1/k each
+    ids, w = orc.route_top_k(np.full((3, 10), 0.75, np.float32), 4)
+    assert np.array_equal(ids, np.tile(np.arange(4, dtype=np.int32), (3, 1)))
+    assert np.all(w == np.float32(0.25))
+    # a single choice carries weight exactly 1
+    rng = np.random.default_rng(22)
+    lg = rng.standard_normal((7, 33)).astype(np.float32)
+    ids, w = orc.route_top_k(lg, 1)
+    assert np.array_equal(ids[:, 0], np.argmax(lg, axis=1).astype(np.int32))
+    assert np.all(w == 1.0)
+    # two chosen logits a > b: weights 1/(1+e^(b-a)) and e^(b-a)/(1+e^(b-a))
+    lg = np.array([[0.0, 2.0, -1.0, 0.5]], np.float32)
+    ids, w = orc.route_top_k(lg, 2)
+    assert ids.tolist() == [[1, 3]]
+    r = math.exp(0.5 - 2.0)
+    np.testing.assert_allclose(w[0], [1 / (1 + r), r / (1 + r)], rtol=1e-7)
+    # shifting every logit by an exact constant changes nothing
+    lg = rng.integers(-20, 20, size=(4, 64)).astype(np.float32)
+    a = orc.route_top_k(lg, 6)
+    b = orc.route_top_k(lg + np.float32(1024.0), 6)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    # the weights of a token sum to 1 within fp32 rounding
+    lg = rng.standard_normal((50, 128)).astype(np.float32) * np.float32(3.0)
+    _, w = orc.route_top_k(lg, 8)
+    np.testing.assert_allclose(w.astype(np.float64).sum(axis=1), 1.0, rtol=0, atol=8 * 2.0 ** -24)
+
+
+def test_router_special_values():
+    nan, inf = np.float32("nan"), np.float32("inf")
+    lg = np.array([[nan, -inf, 1.0, -0.0, 0.0, nan, -3.0]], np.float32)
+    ids, w = orc.route_top_k(lg, 7)
+    # numbers first (descending; -0 equals +0, so index decides), then -inf,
+    # then the NaNs by index
+    assert ids.tolist() == [[2, 3, 4, 6, 1, 0, 5]]
+    assert np.isnan(w[0, 5]) and np.isnan(w[0, 6])
+    ids, w = orc.route_top_k(lg, 4)
+    assert ids.tolist() == [[2, 3, 4, 6]]
+    ref = _softmax64([1.0, 0.0, 0.0, -3.0]).astype(np.float32)
+    np.testing.assert_allclose(w[0], ref, rtol=2e-7)
+
+
+def test_router_brute_force_over_all_orders():
+    # every arrangement of a small multiset of logits (ties included): the
+    # chosen ids are the k best positions under (value desc, index asc)
+    import itertools
+    vals = [2.0, 2.0, -1.0, 0.5, 0.5]
+    for perm in set(itertools.permutations(vals)):
+        lg = np.array([perm], np.float32)
+        ranked = sorted(range(len(perm)), key=lambda i: (-perm[i], i))
+        for k in (1, 3, 5):
+            ids, _ = orc.route_top_k(lg, k)
+            assert ids[0].tolist() == ranked[:k]
