@@ -266,8 +266,10 @@ def run_gpu(args):
             Wd[e] = quantize_on_gpu(d, torch, zffn)
         W = [Wg, Wu, Wd]
         x_all = torch.from_numpy(host.x.view(np.int16)).to(dev).view(torch.bfloat16)
-        ids = torch.from_numpy(host.ids).to(dev)
-        wts = torch.from_numpy(host.weights).to(dev)
+        # the layer's router turns the logits into ids and weights on the
+        # device, once, before the timed steps (the block reads them as inputs)
+        logits_dev = torch.from_numpy(host.logits).to(dev)
+        ids, wts = zffn.moe_router_topk(logits_dev, k)
     torch.cuda.synchronize()
     # Decode reads 76 MB per token, less than the L2: rotate over copies of the
     # weights at different addresses so that every step streams from HBM.
@@ -370,6 +372,17 @@ def run_gpu(args):
         y_host.copy_(y_e2e, non_blocking=True)
     e2e_ms = timed(e2e_step)
 
+    # the router of the routed layer (logits -> ids, weights), timed on its own
+    router = None
+    if kind == "moe":
+        ids_r, wts_r = torch.empty_like(ids), torch.empty_like(wts)
+        r_ms = timed(lambda s: zffn.moe_router_topk(logits_dev, k, ids_r, wts_r))
+        assert torch.equal(ids_r, ids) and torch.equal(wts_r, wts)
+        r_bytes = T * E * 4 + T * k * 8
+        router = {"kernel": "moe_router_kernel", "ms": round(r_ms, 5),
+                  "hbm_bytes": r_bytes, "achieved_gbs": round(r_bytes / (r_ms * 1e-3) / 1e9, 2),
+                  "frac_of_hbm_peak": round(r_bytes / (r_ms * 1e-3) / 1e9 / peaks["hbm"], 5)}
+
     if world > 1:
         t = torch.tensor([ms, kms, e2e_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -433,6 +446,7 @@ def run_gpu(args):
                 "h2d_bytes_per_step": int(x_host.numel() * 2),
                 "d2h_bytes_per_step": int(y_host.numel() * 4)},
         "cpu_baseline": cpu,
+        **({"router": router} if router is not None else {}),
         "clocks": clocks,
         "gpu_launches": launches_per_call * args.steps,
         "wall_s_timed_loop": round(wall, 4),
@@ -468,8 +482,8 @@ def oracle_tokens(name, host, layer, rows):
     if kind == "dense":
         x = host["x"][rows].copy()
         return orc.swiglu_ffn(x, layer["Wg"], layer["Wu"], layer["Wd"], len(rows), H, I)
-    return orc.moe_swiglu_ffn(host.x[rows].copy(), host.ids[rows].copy(),
-                              host.weights[rows].copy(), layer["Wg"], layer["Wu"], layer["Wd"],
+    ids, w = orc.route_top_k(host.logits[rows].copy(), k)
+    return orc.moe_swiglu_ffn(host.x[rows].copy(), ids, w, layer["Wg"], layer["Wu"], layer["Wd"],
                               len(rows), H, I, E, k)
 
 

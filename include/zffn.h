@@ -126,6 +126,29 @@ zffn_status zffn_moe_swiglu_q4k(const void *x, const int32_t *expert_ids,
                                 const void *Wd, float *y, int T, int H, int I, int E,
                                 int top_k, void *stream);
 
+/* Router of a routed block: for every token, the top_k experts by router
+ * logit and softmax weights over the chosen logits, written to device buffers
+ * that zffn_moe_swiglu_q4k reads as they are ("Four bottlenecks, one CUDA
+ * backend...", section "Bottleneck 2 -- MoE decode was paying for its routing
+ * twice": the layer computes router logits and picks the top-k experts; section
+ * "What's next, and what it's worth": a GPU-side step drops the last router
+ * round-trip).  The pages do not state the weighting; the softmax over the
+ * chosen k logits is the reading used here.
+ *   logits: fp32 [T][E] row-major (device).
+ *   expert_ids: output, int32 [T][top_k] (device): the chosen experts from the
+ *     highest logit down; equal logits go to the lower index; -0 equals +0; a
+ *     NaN logit ranks below every number (-inf included), NaNs by index.
+ *   expert_weights: output, fp32 [T][top_k] (device):
+ *     exp(l_j - l_0) / sum_i exp(l_i - l_0) over the chosen logits, l_0 the
+ *     largest, in fp32 (IEEE arithmetic for infinities and NaNs).
+ * Requirements: T >= 1, 1 <= E <= 4096, 1 <= top_k <= min(E, 64), T*E <= 2^31,
+ * 4-byte aligned pointers.  All buffers are the caller's; nothing is read back
+ * to the host.
+ * Errors: INVALID_ARG (checked on the host, nothing launched), CUDA. */
+zffn_status zffn_moe_router_topk(const float *logits, int32_t *expert_ids,
+                                 float *expert_weights, int T, int E, int top_k,
+                                 void *stream);
+
 /* As zffn_moe_swiglu_q4k, but y += the routed block's output. */
 zffn_status zffn_moe_swiglu_q4k_residual(const void *x, const int32_t *expert_ids,
                                          const float *expert_weights, const void *Wg,

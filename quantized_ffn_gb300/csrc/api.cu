@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "zffn_internal.cuh"
+#include "router.h"
 
 namespace zffn {
 
@@ -324,6 +325,19 @@ zffn_status zffn_moe_swiglu_q4k_residual(const void *x, const int32_t *expert_id
                                          int I, int E, int top_k, void *stream) {
     return swiglu_moe(x, expert_ids, expert_weights, Wg, Wu, Wd, y, T, H, I, E, top_k, stream,
                       true);
+}
+
+zffn_status zffn_moe_router_topk(const float *logits, int32_t *expert_ids, float *expert_weights,
+                                 int T, int E, int top_k, void *stream) {
+    if (!logits || !expert_ids || !expert_weights) return ZFFN_ERR_INVALID_ARG;
+    if (T < 1 || E < 1 || E > 4096 || top_k < 1 || top_k > 64 || top_k > E) return ZFFN_ERR_INVALID_ARG;
+    if ((int64_t)T * E > ((int64_t)1 << 31) || (int64_t)T * top_k > (1 << 24)) return ZFFN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(logits) & 3) || (reinterpret_cast<uintptr_t>(expert_ids) & 3) ||
+        (reinterpret_cast<uintptr_t>(expert_weights) & 3))
+        return ZFFN_ERR_INVALID_ARG;
+    if (device_info().device < 0) return ZFFN_ERR_CUDA;
+    return to_status(launch_moe_router(logits, T, E, top_k, expert_ids, expert_weights,
+                                       (cudaStream_t)stream));
 }
 
 zffn_status zffn_reserve(int T_max, int H_max, int I_max, int E_max, int top_k_max) {

@@ -22,9 +22,9 @@ prefill    H=4096, I=11008; W_gate, W_up [I, H], W_down [H, I] fp32 ~ N(0, 0.02)
 decode     the same layer drawn with seed 3, then 1000 tokens x_t ~ N(0, 1)
 moe        E=128 experts, H=2048, I=768, top_k=8; expert e's W_gate, W_up,
            W_down drawn from child stream e of SeedSequence(4); router logits
-           [T, 128] ~ N(0, 1) and x from child stream E; ids = the 8 largest
-           logits in descending order (ties to the lower index), weights =
-           softmax over those 8 logits
+           [T, 128] ~ N(0, 1) and x from child stream E; the expert ids and
+           weights are not drawn: the router turns the logits into them (the
+           8 largest logits, softmax over those 8)
 =========  =====================================================================
 """
 from __future__ import annotations
@@ -135,18 +135,8 @@ class MoE:
         logits = rng.standard_normal((T, E), dtype=np.float32)
         self.x = activations(rng, T, H)
         self.logits = logits
-        self.ids, self.weights = route_top_k(logits, top_k)
 
     def expert_f32(self, e: int):
         rng = np.random.default_rng(self._children[e])
         return dense_layer_f32(rng, self.H, self.I)
 
-
-def route_top_k(logits: np.ndarray, k: int):
-    """Top-k ids (descending logit, ties to the lower index) and softmax weights."""
-    order = np.argsort(-logits, axis=1, kind="stable")[:, :k]
-    top = np.take_along_axis(logits, order, axis=1).astype(np.float64)
-    top = top - top.max(axis=1, keepdims=True)
-    p = np.exp(top)
-    p = p / p.sum(axis=1, keepdims=True)
-    return order.astype(np.int32), p.astype(np.float32)

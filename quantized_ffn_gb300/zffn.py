@@ -54,6 +54,7 @@ def load() -> ctypes.CDLL:
                 "zffn_swiglu_q4k_residual": ([P, P, P, P, P, I32, I32, I32, P], I32),
                 "zffn_moe_swiglu_q4k_residual": ([P, P, P, P, P, P, P, I32, I32, I32, I32, I32, P],
                                                  I32),
+                "zffn_moe_router_topk": ([P, P, P, I32, I32, I32, P], I32),
                 "zffn_reserve": ([I32, I32, I32, I32, I32], I32),
                 "zffn_release": ([], None),
                 "zffn_get_device_error": ([P], I32),
@@ -152,6 +153,23 @@ def moe_swiglu_q4k(x: torch.Tensor, expert_ids: torch.Tensor, expert_weights: to
         _cuda(Wu, "Wu", torch.uint8), _cuda(Wd, "Wd", torch.uint8),
         _cuda(y, "y", torch.float32), T, H, I, E, top_k, _stream(stream)), "zffn_moe_swiglu_q4k")
     return y
+
+
+def moe_router_topk(logits: torch.Tensor, top_k: int, expert_ids: Optional[torch.Tensor] = None,
+                    expert_weights: Optional[torch.Tensor] = None, stream=None):
+    """(expert_ids int32 [T, top_k], expert_weights fp32 [T, top_k]) from
+    router logits fp32 [T, E]: the top_k experts of each token (highest logit
+    first, ties to the lower index) and softmax weights over the chosen logits."""
+    T, E = logits.shape
+    if expert_ids is None:
+        expert_ids = torch.empty((T, top_k), dtype=torch.int32, device=logits.device)
+    if expert_weights is None:
+        expert_weights = torch.empty((T, top_k), dtype=torch.float32, device=logits.device)
+    _check(load().zffn_moe_router_topk(
+        _cuda(logits, "logits", torch.float32), _cuda(expert_ids, "expert_ids", torch.int32),
+        _cuda(expert_weights, "expert_weights", torch.float32), T, E, top_k, _stream(stream)),
+        "zffn_moe_router_topk")
+    return expert_ids, expert_weights
 
 
 def reserve(T_max: int, H_max: int, I_max: int, E_max: int = 1, top_k_max: int = 1):

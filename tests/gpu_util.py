@@ -62,4 +62,5 @@ def moe_layer(T: int, E: int = 128, H: int = 2048, I: int = 768, top_k: int = 8,
         Wg[e] = orc.q4k_quantize(g)
         Wu[e] = orc.q4k_quantize(u)
         Wd[e] = orc.q4k_quantize(d)
-    return dict(x=m.x, ids=m.ids, w=m.weights, Wg=Wg, Wu=Wu, Wd=Wd, E=E, H=H, I=I, k=top_k)
+    ids, w = orc.route_top_k(m.logits, top_k)
+    return dict(x=m.x, logits=m.logits, ids=ids, w=w, Wg=Wg, Wu=Wu, Wd=Wd, E=E, H=H, I=I, k=top_k)

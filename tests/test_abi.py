@@ -93,3 +93,17 @@ def test_options(lib):
     old = zffn.set_option(zffn.OPT_MATVEC_MAX_T, 4)
     assert zffn.set_option(zffn.OPT_MATVEC_MAX_T, old) == 4
     assert zffn.set_option(999, 1) == -1
+
+
+@pytest.mark.parametrize("T,E,k", [(0, 8, 2), (-3, 8, 2), (4, 0, 1), (4, 5000, 8), (4, 8, 0),
+                                   (4, 8, 9), (4, 128, 65)])
+def test_router_rejects_bad_sizes(lib, T, E, k):
+    assert lib.zffn_moe_router_topk(FAKE, FAKE, FAKE, T, E, k, None) == zffn.ERR_INVALID_ARG
+
+
+def test_router_rejects_null_and_misaligned(lib):
+    assert lib.zffn_moe_router_topk(None, FAKE, FAKE, 4, 8, 2, None) == zffn.ERR_INVALID_ARG
+    assert lib.zffn_moe_router_topk(FAKE, None, FAKE, 4, 8, 2, None) == zffn.ERR_INVALID_ARG
+    assert lib.zffn_moe_router_topk(FAKE, FAKE, None, 4, 8, 2, None) == zffn.ERR_INVALID_ARG
+    odd = ctypes.c_void_p(0x10002)
+    assert lib.zffn_moe_router_topk(odd, FAKE, FAKE, 4, 8, 2, None) == zffn.ERR_INVALID_ARG

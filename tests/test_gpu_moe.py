@@ -21,7 +21,7 @@ def experts(seed, E, H, I, dscale=1e-2):
 def routing(seed, T, E, k):
     rng = np.random.default_rng(seed)
     logits = rng.standard_normal((T, E)).astype(np.float32)
-    return synth.route_top_k(logits, k)
+    return orc.route_top_k(logits, k)
 
 
 def run(x, ids, w, Wg, Wu, Wd, I, E, matvec_max_t=None):
