@@ -27,6 +27,12 @@
  *   - Mixture of experts: y_t = sum_j w_{t,j} FFN_{e_{t,j}}(x_t), expert ids and
  *     weights given per token ("Four bottlenecks, one CUDA backend...",
  *     section "Bottleneck 2 -- MoE decode was paying for its routing twice").
+ *   - The normalisation before the block and the residual connection around
+ *     it: x = RMSNorm(h) * gamma feeds the block and h += block(x) ("Four
+ *     bottlenecks, one CUDA backend...", section "Bottleneck 3 -- Gemma
+ *     decode is launch-latency bound": rms_norm and the residual accumulate
+ *     as one launch).  The pages do not write RMSNorm out; the reading is the
+ *     usual x = h / sqrt(mean(h^2) + eps) * gamma, rounded once to bf16.
  *   - The router that chooses them: per token, the top_k experts by logit,
  *     then softmax weights over the chosen logits (same page and section:
  *     the layer computes router logits and picks the top-k experts; the
@@ -374,4 +380,42 @@ void oracle_route_top_k(const float *logits, int64_t T, int64_t E, int64_t top_k
     }
     free(taken);
     free(ex);
+}
+
+/* double -> bfloat16 bits, rounded once to nearest even: the value is split
+ * as m * 2^e with 0.5 <= |m| < 1, m is rounded to 8 significant bits and
+ * scaled back.  Covers the normal range of bf16 (the only range the tests
+ * use); zero keeps its sign. */
+uint16_t oracle_bf16_from_f64(double v)
+{
+    if (v == 0.0 || isnan(v) || isinf(v)) {
+        float f = (float)v;
+        uint32_t u;
+        memcpy(&u, &f, 4);
+        return (uint16_t)(u >> 16 | (isnan(v) ? 0x40u : 0u));
+    }
+    int e;
+    double m = frexp(v, &e);
+    double q = nearbyint(ldexp(m, 8));       /* default rounding: nearest even */
+    float f = (float)ldexp(q, e - 8);        /* exact: 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return (uint16_t)(u >> 16);
+}
+
+/* RMSNorm of the rows of h [T][H] (fp32) into bf16 bits:
+ *     x[t][c] = bf16( h[t][c] / sqrt(sum_c' h[t][c']^2 / H + eps) * gamma[c] )
+ * with the sum, the root and the products in fp64 and one rounding. */
+void oracle_rmsnorm_bf16(const float *h, const float *gamma, double eps, int64_t T, int64_t H,
+                         uint16_t *x)
+{
+    for (int64_t t = 0; t < T; ++t) {
+        const float *row = h + t * H;
+        double ss = 0.0;
+        for (int64_t c = 0; c < H; ++c)
+            ss += (double)row[c] * (double)row[c];
+        double r = 1.0 / sqrt(ss / (double)H + eps);
+        for (int64_t c = 0; c < H; ++c)
+            x[t * H + c] = oracle_bf16_from_f64((double)row[c] * r * (double)gamma[c]);
+    }
 }

@@ -67,6 +67,9 @@ def _load():
             lib.oracle_swiglu_ffn.argtypes = [P, P, P, P, I64, I64, I64, P]
             lib.oracle_moe_swiglu_ffn.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, I64, P]
             lib.oracle_route_top_k.argtypes = [P, I64, I64, I64, P, P]
+            lib.oracle_bf16_from_f64.argtypes = [ctypes.c_double]
+            lib.oracle_bf16_from_f64.restype = ctypes.c_uint16
+            lib.oracle_rmsnorm_bf16.argtypes = [P, P, ctypes.c_double, I64, I64, P]
             for f in ("oracle_q4k_dequant", "oracle_q4k_quantize",
                       "oracle_swiglu_ffn", "oracle_moe_swiglu_ffn",
                       "oracle_q4k_scale_min"):
@@ -174,3 +177,29 @@ def route_top_k(logits: np.ndarray, top_k: int):
     w = np.empty((T, top_k), dtype=np.float32)
     _load().oracle_route_top_k(_ptr(logits), T, E, top_k, _ptr(ids), _ptr(w))
     return ids, w
+
+
+def bf16_from_f64(v: float) -> int:
+    """bf16 bits of v rounded once to nearest even (normal range)."""
+    return int(_load().oracle_bf16_from_f64(float(v)))
+
+
+def rmsnorm_bf16(h: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
+    """bf16 bits (uint16 [T, H]) of h / sqrt(mean(h^2) + eps) * gamma per row."""
+    h = np.ascontiguousarray(h, dtype=np.float32)
+    gamma = np.ascontiguousarray(gamma, dtype=np.float32)
+    T, H = h.shape
+    assert gamma.shape == (H,)
+    x = np.empty((T, H), dtype=np.uint16)
+    _load().oracle_rmsnorm_bf16(_ptr(h), _ptr(gamma), float(eps), T, H, _ptr(x))
+    return x
+
+
+def prenorm_swiglu_residual(h: np.ndarray, gamma: np.ndarray, eps: float, Wg: np.ndarray,
+                            Wu: np.ndarray, Wd: np.ndarray, I: int):
+    """(h + block(x), x) with x = rmsnorm_bf16(h, gamma, eps): the block with
+    its normalisation and residual connection; float64 [T, H] and bf16 bits."""
+    T, H = h.shape
+    x = rmsnorm_bf16(h, gamma, eps)
+    y = swiglu_ffn(x, Wg, Wu, Wd, T, H, I)
+    return np.asarray(h, dtype=np.float64) + y, x

@@ -485,3 +485,82 @@ def test_router_brute_force_over_all_orders():
         for k in (1, 3, 5):
             ids, _ = orc.route_top_k(lg, k)
             assert ids[0].tolist() == ranked[:k]
+
+
+# ---- RMSNorm before the block, residual around it ------------------------------
+
+def _bf16(bits):
+    return (np.asarray(bits, dtype=np.uint32) << 16).view(np.float32)
+
+
+def test_bf16_rounding_against_float32_bits():
+    # For values exact in fp32, rounding fp64 -> bf16 once equals the bit-level
+    # round-to-nearest-even of the fp32 pattern (add 0x7FFF + lsb, cut).
+    rng = np.random.default_rng(31)
+    v = np.concatenate([rng.standard_normal(20000).astype(np.float32),
+                        (rng.standard_normal(5000) * 1e4).astype(np.float32),
+                        np.array([1.0, -1.0, 1 + 2 ** -8, 1 + 2 ** -9, 1 + 3 * 2 ** -9,
+                                  1 + 2 ** -9 + 2 ** -20, 255.5, 0.0, -0.0], np.float32)])
+    u = v.view(np.uint32)
+    ref = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    got = np.array([orc.bf16_from_f64(float(a)) for a in v], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+    # a value between two bf16 numbers that fp32 cannot hold: rounded once
+    # (bf16 steps by 2^-7 on [1, 2): 1 + 2^-8 is the midpoint of 1 and 1 + 2^-7)
+    assert orc.bf16_from_f64(1 + 2 ** -8 + 2 ** -40) == 0x3F81
+    assert orc.bf16_from_f64(1 + 2 ** -8 - 2 ** -40) == 0x3F80
+    assert orc.bf16_from_f64(1 + 2 ** -8) == 0x3F80 and orc.bf16_from_f64(1 + 3 * 2 ** -8) == 0x3F82
+
+
+def test_rmsnorm_worked_example():
+    # h = (3, 4): mean square 12.5, so x = (3, 4) / sqrt(12.5) = (0.8485, 1.1314)
+    # before rounding; bf16 keeps 8 significant bits: 217/256 and 145/128.
+    x = orc.rmsnorm_bf16(np.array([[3.0, 4.0]], np.float32), np.ones(2, np.float32), 0.0)
+    assert _bf16(x[0]).tolist() == [217 / 256, 145 / 128]
+    x = orc.rmsnorm_bf16(np.array([[3.0, 4.0]], np.float32), np.array([2.0, -0.5], np.float32), 0.0)
+    assert _bf16(x[0]).tolist() == [217 / 128, -145 / 256]
+    # eps enters under the root: h = (1, 1, 1, 1), eps = 3 -> 1 / sqrt(4) = 0.5
+    x = orc.rmsnorm_bf16(np.ones((1, 4), np.float32), np.ones(4, np.float32), 3.0)
+    assert np.all(_bf16(x[0]) == 0.5)
+
+
+def test_rmsnorm_invariants():
+    rng = np.random.default_rng(32)
+    h = rng.standard_normal((6, 256)).astype(np.float32)
+    g = np.ones(256, np.float32)
+    # constant rows map to +-gamma exactly (eps = 0)
+    c = np.array([[2.5] * 8, [-7.0] * 8], np.float32)
+    x = orc.rmsnorm_bf16(c, np.ones(8, np.float32), 0.0)
+    assert np.all(_bf16(x[0]) == 1.0) and np.all(_bf16(x[1]) == -1.0)
+    # scaling a row by a power of two changes nothing (eps = 0)
+    a = orc.rmsnorm_bf16(h, g, 0.0)
+    b = orc.rmsnorm_bf16(h * np.float32(64.0), g, 0.0)
+    assert np.array_equal(a, b)
+    # gamma scales column by column: gamma = 2 doubles every value exactly
+    b = orc.rmsnorm_bf16(h, np.full(256, 2.0, np.float32), 0.0)
+    assert np.array_equal(_bf16(b), 2 * _bf16(a))
+    # unit mean square before rounding: after it, within the bf16 step
+    ms = (_bf16(a).astype(np.float64) ** 2).mean(axis=1)
+    assert np.all(np.abs(ms - 1.0) < 2 ** -7)
+    # a zero row stays zero when eps > 0
+    x = orc.rmsnorm_bf16(np.zeros((1, 16), np.float32), np.ones(16, np.float32), 1e-6)
+    assert np.all(_bf16(x) == 0.0)
+    # rows are independent
+    one = orc.rmsnorm_bf16(h[3:4], g, 1e-6)
+    assert np.array_equal(one[0], orc.rmsnorm_bf16(h, g, 1e-6)[3])
+
+
+def test_prenorm_sublayer_reduces_to_parts():
+    # with zero down weights the sublayer leaves h unchanged; otherwise it is
+    # h plus the block applied to the normalised rows
+    d = synth.tiny()
+    rng = np.random.default_rng(33)
+    h = rng.standard_normal((4, d["H"])).astype(np.float32)
+    gamma = (1.0 + 0.1 * rng.standard_normal(d["H"])).astype(np.float32)
+    zero_wd = np.zeros_like(d["Wd"])
+    out, x = orc.prenorm_swiglu_residual(h, gamma, 1e-6, d["Wg"], d["Wu"], zero_wd, d["I"])
+    assert np.array_equal(out, h.astype(np.float64))
+    out, x = orc.prenorm_swiglu_residual(h, gamma, 1e-6, d["Wg"], d["Wu"], d["Wd"], d["I"])
+    assert np.array_equal(x, orc.rmsnorm_bf16(h, gamma, 1e-6))
+    y = orc.swiglu_ffn(x, d["Wg"], d["Wu"], d["Wd"], 4, d["H"], d["I"])
+    assert np.array_equal(out, h.astype(np.float64) + y)
