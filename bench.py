@@ -372,6 +372,29 @@ def run_gpu(args):
         y_host.copy_(y_e2e, non_blocking=True)
     e2e_ms = timed(e2e_step)
 
+    # the normalisation in front of the dense block (fp32 residual stream ->
+    # bf16 block input), timed on its own over the workload's rows
+    norm = None
+    if kind == "dense":
+        h_res = x_all[:T].float().contiguous()
+        gamma = torch.ones(H, dtype=torch.float32, device=dev)
+        xn = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        # (one call between events after an L2 flush, whatever the workload:
+        # back to back, a one-row call would time the host, not the kernel)
+        n_st = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        n_en = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for s in range(args.steps):
+            flush.zero_()
+            n_st[s].record(stream)
+            zffn.rmsnorm_bf16(h_res, gamma, 1e-6, out=xn)
+            n_en[s].record(stream)
+        torch.cuda.synchronize()
+        n_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(n_st, n_en))
+        n_bytes = T * H * 6 + H * 4
+        n_gbs = n_bytes / (n_ms * 1e-3) / 1e9
+        norm = {"kernel": "rmsnorm_bf16_kernel", "ms": round(n_ms, 5), "hbm_bytes": n_bytes,
+                "achieved_gbs": round(n_gbs, 2), "frac_of_hbm_peak": round(n_gbs / peaks["hbm"], 4)}
+
     # the router of the routed layer (logits -> ids, weights), timed on its own
     router = None
     if kind == "moe":
@@ -447,6 +470,7 @@ def run_gpu(args):
                 "d2h_bytes_per_step": int(y_host.numel() * 4)},
         "cpu_baseline": cpu,
         **({"router": router} if router is not None else {}),
+        **({"rmsnorm": norm} if norm is not None else {}),
         "clocks": clocks,
         "gpu_launches": launches_per_call * args.steps,
         "wall_s_timed_loop": round(wall, 4),

@@ -107,6 +107,34 @@ zffn_status zffn_swiglu_q4k_residual(const void *x, const void *Wg, const void *
                                      const void *Wd, float *y, int T, int H, int I,
                                      void *stream);
 
+/* RMSNorm of the residual stream into the block's input:
+ *     x[t][c] = bf16( h[t][c] / sqrt(mean_c' h[t][c']^2 + eps) * gamma[c] )
+ * ("Four bottlenecks, one CUDA backend...", section "Bottleneck 3 -- Gemma
+ * decode is launch-latency bound": the rms_norm and the residual accumulate
+ * around a block; the pages do not write RMSNorm out, this is the usual form).
+ * Sum of squares and scaling in fp32, one rounding to bf16 (round to nearest
+ * even).
+ *   h: fp32 [T][H] (device), read only.  gamma: fp32 [H] (device).
+ *   x: output, bf16 [T][H] (device).
+ * Requirements: T >= 1, 256 <= H <= 16384, H % 256 == 0, 0 <= eps <= 1,
+ * 16-byte aligned pointers.  Errors: INVALID_ARG (nothing launched), CUDA. */
+zffn_status zffn_rmsnorm_bf16(const float *h, const float *gamma, float eps, void *x, int T,
+                              int H, void *stream);
+
+/* The block with its normalisation and residual connection, as a pre-norm
+ * transformer layer applies it to the residual stream h:
+ *     h[t] += W_down . (silu(W_gate . x[t]) (*) (W_up . x[t])),
+ *     x = zffn_rmsnorm_bf16(h, gamma, eps)
+ * Two launch groups in stream order: the normalisation into library workspace
+ * (bf16 [T][H], see zffn_reserve), then the block accumulating into h.
+ *   h: fp32 [T][H] (device), read and updated in place.
+ *   gamma: fp32 [H]; Wg, Wu, Wd as for zffn_swiglu_q4k.
+ * Requirements as zffn_swiglu_q4k and zffn_rmsnorm_bf16.
+ * Errors: INVALID_ARG, CUDA, NO_WORKSPACE. */
+zffn_status zffn_swiglu_q4k_prenorm_residual(float *h, const float *gamma, float eps,
+                                             const void *Wg, const void *Wu, const void *Wd,
+                                             int T, int H, int I, void *stream);
+
 /* Mixture-of-experts SwiGLU block:
  *     y[t] = sum_{j < top_k} expert_weights[t][j] * FFN_{expert_ids[t][j]}(x[t])
  * ("Four bottlenecks, one CUDA backend...", section "Bottleneck 2 -- MoE decode

@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "zffn_internal.cuh"
+#include "rmsnorm.h"
 #include "router.h"
 
 namespace zffn {
@@ -30,7 +31,7 @@ inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 // Sub-buffers carved out of one device allocation.
 struct Layout {
-    size_t h, counts, offsets, cursors, tiles, n_tiles, row_token, row_weight, x_perm,
+    size_t h, counts, offsets, cursors, tiles, n_tiles, row_token, row_weight, x_perm, xn,
         total;
     int max_tiles;
 };
@@ -49,6 +50,7 @@ Layout layout_for(int T, int H, int I, int E, int k) {
     L.row_token = o; o = align_up(o + (size_t)P * sizeof(int));
     L.row_weight = o; o = align_up(o + (size_t)P * sizeof(float));
     L.x_perm = o; o = align_up(o + (size_t)P * H * 2);
+    L.xn = o; o = align_up(o + (size_t)T * H * 2);      // normalised block input (pre-norm entry)
     L.total = o;
     return L;
 }
@@ -325,6 +327,38 @@ zffn_status zffn_moe_swiglu_q4k_residual(const void *x, const int32_t *expert_id
                                          int I, int E, int top_k, void *stream) {
     return swiglu_moe(x, expert_ids, expert_weights, Wg, Wu, Wd, y, T, H, I, E, top_k, stream,
                       true);
+}
+
+zffn_status zffn_rmsnorm_bf16(const float *h, const float *gamma, float eps, void *x, int T, int H,
+                              void *stream) {
+    if (!h || !gamma || !x) return ZFFN_ERR_INVALID_ARG;
+    if (T < 1 || H < 256 || H > 16384 || H % 256 != 0) return ZFFN_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f) || eps > 1.0f) return ZFFN_ERR_INVALID_ARG;
+    if (!aligned16(h) || !aligned16(gamma) || !aligned16(x)) return ZFFN_ERR_INVALID_ARG;
+    if (device_info().device < 0) return ZFFN_ERR_CUDA;
+    return to_status(launch_rmsnorm_bf16(h, gamma, eps, static_cast<__nv_bfloat16 *>(x), T, H,
+                                         (cudaStream_t)stream));
+}
+
+zffn_status zffn_swiglu_q4k_prenorm_residual(float *h, const float *gamma, float eps, const void *Wg,
+                                             const void *Wu, const void *Wd, int T, int H, int I,
+                                             void *stream) {
+    if (!h || !gamma || !Wg || !Wu || !Wd) return ZFFN_ERR_INVALID_ARG;
+    if (check_shape(T, H, I) != ZFFN_OK) return ZFFN_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f) || eps > 1.0f) return ZFFN_ERR_INVALID_ARG;
+    if (!aligned16(h) || !aligned16(gamma) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd))
+        return ZFFN_ERR_INVALID_ARG;
+    if (device_info().device < 0) return ZFFN_ERR_CUDA;
+    // the whole layout is reserved here, so that the block's own workspace
+    // request below finds it large enough and never moves it
+    const Layout L = layout_for(T, H, I, 1, 1);
+    Workspace *w = nullptr;
+    zffn_status st = ensure_workspace(L.total, &w);
+    if (st != ZFFN_OK) return st;
+    __nv_bfloat16 *xn = reinterpret_cast<__nv_bfloat16 *>(static_cast<uint8_t *>(w->ptr) + L.xn);
+    cudaError_t e = launch_rmsnorm_bf16(h, gamma, eps, xn, T, H, (cudaStream_t)stream);
+    if (e != cudaSuccess) return to_status(e);
+    return swiglu_dense(xn, Wg, Wu, Wd, h, T, H, I, stream, true);
 }
 
 zffn_status zffn_moe_router_topk(const float *logits, int32_t *expert_ids, float *expert_weights,

@@ -55,6 +55,9 @@ def load() -> ctypes.CDLL:
                 "zffn_moe_swiglu_q4k_residual": ([P, P, P, P, P, P, P, I32, I32, I32, I32, I32, P],
                                                  I32),
                 "zffn_moe_router_topk": ([P, P, P, I32, I32, I32, P], I32),
+                "zffn_rmsnorm_bf16": ([P, P, ctypes.c_float, P, I32, I32, P], I32),
+                "zffn_swiglu_q4k_prenorm_residual": ([P, P, ctypes.c_float, P, P, P, I32, I32, I32, P],
+                                                     I32),
                 "zffn_reserve": ([I32, I32, I32, I32, I32], I32),
                 "zffn_release": ([], None),
                 "zffn_get_device_error": ([P], I32),
@@ -153,6 +156,31 @@ def moe_swiglu_q4k(x: torch.Tensor, expert_ids: torch.Tensor, expert_weights: to
         _cuda(Wu, "Wu", torch.uint8), _cuda(Wd, "Wd", torch.uint8),
         _cuda(y, "y", torch.float32), T, H, I, E, top_k, _stream(stream)), "zffn_moe_swiglu_q4k")
     return y
+
+
+def rmsnorm_bf16(h: torch.Tensor, gamma: torch.Tensor, eps: float,
+                 out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """x[T, H] bf16 = h / sqrt(mean(h^2) + eps) * gamma, row by row (h fp32)."""
+    T, H = h.shape
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=h.device)
+    _check(load().zffn_rmsnorm_bf16(_cuda(h, "h", torch.float32), _cuda(gamma, "gamma", torch.float32),
+                                    float(eps), _cuda(out, "x", torch.bfloat16), T, H, _stream(stream)),
+           "zffn_rmsnorm_bf16")
+    return out
+
+
+def swiglu_q4k_prenorm_residual(h: torch.Tensor, gamma: torch.Tensor, eps: float, Wg: torch.Tensor,
+                                Wu: torch.Tensor, Wd: torch.Tensor, I: int, stream=None
+                                ) -> torch.Tensor:
+    """h += W_down (silu(W_gate x) * (W_up x)) with x = rmsnorm_bf16(h, gamma, eps),
+    in place on the fp32 residual stream h [T, H]; returns h."""
+    T, H = h.shape
+    _check(load().zffn_swiglu_q4k_prenorm_residual(
+        _cuda(h, "h", torch.float32), _cuda(gamma, "gamma", torch.float32), float(eps),
+        _cuda(Wg, "Wg", torch.uint8), _cuda(Wu, "Wu", torch.uint8), _cuda(Wd, "Wd", torch.uint8),
+        T, H, I, _stream(stream)), "zffn_swiglu_q4k_prenorm_residual")
+    return h
 
 
 def moe_router_topk(logits: torch.Tensor, top_k: int, expert_ids: Optional[torch.Tensor] = None,

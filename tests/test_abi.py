@@ -107,3 +107,21 @@ def test_router_rejects_null_and_misaligned(lib):
     assert lib.zffn_moe_router_topk(FAKE, FAKE, None, 4, 8, 2, None) == zffn.ERR_INVALID_ARG
     odd = ctypes.c_void_p(0x10002)
     assert lib.zffn_moe_router_topk(odd, FAKE, FAKE, 4, 8, 2, None) == zffn.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("T,H,eps", [(0, 256, 1e-6), (4, 200, 1e-6), (4, 32768, 1e-6),
+                                     (4, 256, -1.0), (4, 256, float("nan")), (4, 256, 2.0)])
+def test_rmsnorm_rejects_bad_args(lib, T, H, eps):
+    assert lib.zffn_rmsnorm_bf16(FAKE, FAKE, eps, FAKE, T, H, None) == zffn.ERR_INVALID_ARG
+    assert lib.zffn_swiglu_q4k_prenorm_residual(FAKE, FAKE, eps, FAKE, FAKE, FAKE, T, H, 256,
+                                                None) == zffn.ERR_INVALID_ARG
+
+
+def test_rmsnorm_rejects_null_and_misaligned(lib):
+    odd = ctypes.c_void_p(0x10008)
+    assert lib.zffn_rmsnorm_bf16(None, FAKE, 1e-6, FAKE, 4, 256, None) == zffn.ERR_INVALID_ARG
+    assert lib.zffn_rmsnorm_bf16(FAKE, odd, 1e-6, FAKE, 4, 256, None) == zffn.ERR_INVALID_ARG
+    assert lib.zffn_swiglu_q4k_prenorm_residual(odd, FAKE, 1e-6, FAKE, FAKE, FAKE, 4, 256, 256,
+                                                None) == zffn.ERR_INVALID_ARG
+    assert lib.zffn_swiglu_q4k_prenorm_residual(FAKE, FAKE, 1e-6, FAKE, None, FAKE, 4, 256, 256,
+                                                None) == zffn.ERR_INVALID_ARG
