@@ -135,6 +135,38 @@ zffn_status zffn_swiglu_q4k_prenorm_residual(float *h, const float *gamma, float
                                              const void *Wg, const void *Wu, const void *Wd,
                                              int T, int H, int I, void *stream);
 
+/* Host pipeline: the dense block over inputs and outputs in host memory, with
+ * the host-to-device copy of each submission's x and the device-to-host copy
+ * of its y overlapped with the blocks of the neighbouring submissions (an
+ * upload stream, a compute stream and a download stream of the library's own,
+ * ordered by events per slot; `depth` slots of device x and y, allocated once
+ * at creation).  The source pages have no counterpart; it is how a caller
+ * that keeps activations on the host feeds the block without idling it.
+ *   zffn_pipeline_create: *out = a pipeline for blocks of T tokens of width H
+ *     and intermediate width I; 2 <= depth <= ZFFN_PIPELINE_MAX_DEPTH.  Uses
+ *     the current device.  Errors: INVALID_ARG, CUDA, NO_WORKSPACE (device
+ *     memory: depth * T * H * 6 bytes).
+ *   zffn_pipeline_submit: queues upload(x_host) -> block -> download(y_host)
+ *     and returns without waiting.  x_host: bf16 [T][H], y_host: fp32 [T][H],
+ *     host memory (page-locked for the copies to overlap; pageable memory
+ *     works, with the copies serialised by the driver); both must stay valid
+ *     and x_host unchanged until zffn_pipeline_sync returns.  Wg, Wu, Wd:
+ *     device Q4_K weights as for zffn_swiglu_q4k; the pipeline's streams do
+ *     not wait for other streams, so the weights must be complete before the
+ *     call (synchronise the stream that wrote them).  Must be called on the
+ *     pipeline's device.  Errors: INVALID_ARG, CUDA, NO_WORKSPACE.
+ *   zffn_pipeline_sync: waits for every submission so far (their y_host
+ *     hold the results).  Device-side errors are reported by
+ *     zffn_get_device_error as for the other calls.
+ *   zffn_pipeline_destroy: waits, then frees everything (NULL is ignored). */
+#define ZFFN_PIPELINE_MAX_DEPTH 4
+typedef struct zffn_pipeline zffn_pipeline;
+zffn_status zffn_pipeline_create(zffn_pipeline **out, int T, int H, int I, int depth);
+zffn_status zffn_pipeline_submit(zffn_pipeline *p, const void *x_host, const void *Wg,
+                                 const void *Wu, const void *Wd, float *y_host);
+zffn_status zffn_pipeline_sync(zffn_pipeline *p);
+void zffn_pipeline_destroy(zffn_pipeline *p);
+
 /* Mixture-of-experts SwiGLU block:
  *     y[t] = sum_{j < top_k} expert_weights[t][j] * FFN_{expert_ids[t][j]}(x[t])
  * ("Four bottlenecks, one CUDA backend...", section "Bottleneck 2 -- MoE decode

@@ -429,3 +429,116 @@ zffn_status zffn_selftest_wait_timeout(int64_t budget_cycles, void *stream) {
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------------------
+// Host pipeline: blocks over host buffers with the copies overlapped.
+// ----------------------------------------------------------------------------
+// Submission n uses slot n % depth: its x goes up on the upload stream, the
+// block runs on the compute stream, y comes down on the download stream, and
+// events order the three per slot (upload n waits for the block of n - depth
+// to have read the slot's x; the block of n waits for upload n and for the
+// download of n - depth to have emptied the slot's y).  So the copies of one
+// submission overlap the blocks of its neighbours, and no call blocks the host
+// except zffn_pipeline_sync.
+struct zffn_pipeline {
+    int device = -1;
+    int T = 0, H = 0, I = 0, depth = 0;
+    cudaStream_t up = nullptr, comp = nullptr, down = nullptr;
+    void *x[ZFFN_PIPELINE_MAX_DEPTH] = {};
+    float *y[ZFFN_PIPELINE_MAX_DEPTH] = {};
+    cudaEvent_t in_done[ZFFN_PIPELINE_MAX_DEPTH] = {};
+    cudaEvent_t comp_done[ZFFN_PIPELINE_MAX_DEPTH] = {};
+    cudaEvent_t out_done[ZFFN_PIPELINE_MAX_DEPTH] = {};
+    int64_t n = 0;
+};
+
+namespace {
+
+void pipeline_free(zffn_pipeline *p) {
+    if (!p) return;
+    for (cudaStream_t s : {p->up, p->comp, p->down})
+        if (s) cudaStreamSynchronize(s);
+    for (int i = 0; i < ZFFN_PIPELINE_MAX_DEPTH; ++i) {
+        if (p->x[i]) cudaFree(p->x[i]);
+        if (p->y[i]) cudaFree(p->y[i]);
+        if (p->in_done[i]) cudaEventDestroy(p->in_done[i]);
+        if (p->comp_done[i]) cudaEventDestroy(p->comp_done[i]);
+        if (p->out_done[i]) cudaEventDestroy(p->out_done[i]);
+    }
+    for (cudaStream_t s : {p->up, p->comp, p->down})
+        if (s) cudaStreamDestroy(s);
+    cudaGetLastError();
+    delete p;
+}
+
+}  // namespace
+
+extern "C" {
+
+zffn_status zffn_pipeline_create(zffn_pipeline **out, int T, int H, int I, int depth) {
+    if (!out) return ZFFN_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (check_shape(T, H, I) != ZFFN_OK) return ZFFN_ERR_INVALID_ARG;
+    if (depth < 2 || depth > ZFFN_PIPELINE_MAX_DEPTH) return ZFFN_ERR_INVALID_ARG;
+    const DeviceInfo &di = device_info();
+    if (di.device < 0) return ZFFN_ERR_CUDA;
+    zffn_pipeline *p = new zffn_pipeline;
+    p->device = di.device;
+    p->T = T; p->H = H; p->I = I; p->depth = depth;
+    cudaError_t e = cudaSuccess;
+    for (cudaStream_t *s : {&p->up, &p->comp, &p->down})
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(s, cudaStreamNonBlocking);
+    for (int i = 0; i < depth && e == cudaSuccess; ++i) {
+        e = cudaMalloc(&p->x[i], (size_t)T * H * 2);
+        if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void **>(&p->y[i]), (size_t)T * H * 4);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->in_done[i], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->comp_done[i], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->out_done[i], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) {
+        const zffn_status st = e == cudaErrorMemoryAllocation ? ZFFN_ERR_NO_WORKSPACE : to_status(e);
+        if (st == ZFFN_ERR_NO_WORKSPACE) set_last_error(cudaGetErrorString(e));
+        pipeline_free(p);
+        return st;
+    }
+    *out = p;
+    return ZFFN_OK;
+}
+
+zffn_status zffn_pipeline_submit(zffn_pipeline *p, const void *x_host, const void *Wg, const void *Wu,
+                                 const void *Wd, float *y_host) {
+    if (!p || !x_host || !y_host || !Wg || !Wu || !Wd) return ZFFN_ERR_INVALID_ARG;
+    if (current_device() != p->device) return ZFFN_ERR_INVALID_ARG;
+    const int slot = (int)(p->n % p->depth);
+    const size_t xb = (size_t)p->T * p->H * 2, yb = (size_t)p->T * p->H * 4;
+    const bool reuse = p->n >= p->depth;
+    cudaError_t e = cudaSuccess;
+    if (reuse) e = cudaStreamWaitEvent(p->up, p->comp_done[slot], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(p->x[slot], x_host, xb, cudaMemcpyHostToDevice, p->up);
+    if (e == cudaSuccess) e = cudaEventRecord(p->in_done[slot], p->up);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(p->comp, p->in_done[slot], 0);
+    if (e == cudaSuccess && reuse) e = cudaStreamWaitEvent(p->comp, p->out_done[slot], 0);
+    if (e != cudaSuccess) return to_status(e);
+    const zffn_status st = swiglu_dense(p->x[slot], Wg, Wu, Wd, p->y[slot], p->T, p->H, p->I, p->comp, false);
+    if (st != ZFFN_OK) return st;
+    e = cudaEventRecord(p->comp_done[slot], p->comp);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(p->down, p->comp_done[slot], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(y_host, p->y[slot], yb, cudaMemcpyDeviceToHost, p->down);
+    if (e == cudaSuccess) e = cudaEventRecord(p->out_done[slot], p->down);
+    if (e != cudaSuccess) return to_status(e);
+    ++p->n;
+    return ZFFN_OK;
+}
+
+zffn_status zffn_pipeline_sync(zffn_pipeline *p) {
+    if (!p) return ZFFN_ERR_INVALID_ARG;
+    for (cudaStream_t s : {p->up, p->comp, p->down}) {
+        const cudaError_t e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return to_status(e);
+    }
+    return ZFFN_OK;
+}
+
+void zffn_pipeline_destroy(zffn_pipeline *p) { pipeline_free(p); }
+
+}  // extern "C"

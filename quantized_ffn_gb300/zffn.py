@@ -58,6 +58,10 @@ def load() -> ctypes.CDLL:
                 "zffn_rmsnorm_bf16": ([P, P, ctypes.c_float, P, I32, I32, P], I32),
                 "zffn_swiglu_q4k_prenorm_residual": ([P, P, ctypes.c_float, P, P, P, I32, I32, I32, P],
                                                      I32),
+                "zffn_pipeline_create": ([ctypes.POINTER(ctypes.c_void_p), I32, I32, I32, I32], I32),
+                "zffn_pipeline_submit": ([P, P, P, P, P, P], I32),
+                "zffn_pipeline_sync": ([P], I32),
+                "zffn_pipeline_destroy": ([P], None),
                 "zffn_reserve": ([I32, I32, I32, I32, I32], I32),
                 "zffn_release": ([], None),
                 "zffn_get_device_error": ([P], I32),
@@ -198,6 +202,57 @@ def moe_router_topk(logits: torch.Tensor, top_k: int, expert_ids: Optional[torch
         _cuda(expert_weights, "expert_weights", torch.float32), T, E, top_k, _stream(stream)),
         "zffn_moe_router_topk")
     return expert_ids, expert_weights
+
+
+def _host(t: torch.Tensor, name: str, dtype, shape):
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor")
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+class Pipeline:
+    """Dense blocks over host buffers with the copies overlapped (zffn_pipeline_*).
+
+    submit() queues upload(x_host) -> block -> download(y_host) and returns at
+    once; sync() waits for everything submitted.  x_host (bf16 [T, H]) and
+    y_host (fp32 [T, H]) are CPU tensors, page-locked for the copies to
+    overlap, and must stay alive and unchanged until sync() returns."""
+
+    def __init__(self, T: int, H: int, I: int, depth: int = 2):
+        self.T, self.H, self.I = T, H, I
+        self._p = ctypes.c_void_p()
+        _check(load().zffn_pipeline_create(ctypes.byref(self._p), T, H, I, depth),
+               "zffn_pipeline_create")
+        self._keep = []
+
+    def submit(self, x_host: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor, Wd: torch.Tensor,
+               y_host: torch.Tensor):
+        if not self._p:
+            raise RuntimeError("pipeline is closed")
+        shape = (self.T, self.H)
+        _check(load().zffn_pipeline_submit(
+            self._p, _host(x_host, "x_host", torch.bfloat16, shape), _cuda(Wg, "Wg", torch.uint8),
+            _cuda(Wu, "Wu", torch.uint8), _cuda(Wd, "Wd", torch.uint8),
+            _host(y_host, "y_host", torch.float32, shape)), "zffn_pipeline_submit")
+        self._keep.append((x_host, y_host, Wg, Wu, Wd))
+
+    def sync(self):
+        _check(load().zffn_pipeline_sync(self._p), "zffn_pipeline_sync")
+        self._keep.clear()
+
+    def close(self):
+        if self._p:
+            load().zffn_pipeline_destroy(self._p)
+            self._p = ctypes.c_void_p()
+            self._keep.clear()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def reserve(T_max: int, H_max: int, I_max: int, E_max: int = 1, top_k_max: int = 1):

@@ -125,3 +125,15 @@ def test_rmsnorm_rejects_null_and_misaligned(lib):
                                                 None) == zffn.ERR_INVALID_ARG
     assert lib.zffn_swiglu_q4k_prenorm_residual(FAKE, FAKE, 1e-6, FAKE, None, FAKE, 4, 256, 256,
                                                 None) == zffn.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("T,H,I,depth", [(0, 256, 256, 2), (4, 200, 256, 2), (4, 256, 100, 2),
+                                         (4, 256, 256, 1), (4, 256, 256, 5)])
+def test_pipeline_rejects_bad_args(lib, T, H, I, depth):
+    p = ctypes.c_void_p(1)
+    assert zffn.load().zffn_pipeline_create(ctypes.byref(p), T, H, I, depth) == zffn.ERR_INVALID_ARG
+    assert not p.value
+    assert zffn.load().zffn_pipeline_create(None, 4, 256, 256, 2) == zffn.ERR_INVALID_ARG
+    assert zffn.load().zffn_pipeline_submit(None, FAKE, FAKE, FAKE, FAKE, FAKE) == zffn.ERR_INVALID_ARG
+    assert zffn.load().zffn_pipeline_sync(None) == zffn.ERR_INVALID_ARG
+    zffn.load().zffn_pipeline_destroy(None)
