@@ -301,14 +301,12 @@ def run_gpu(args):
             return x_all[r:r + 1]
         return x_all
 
-    def call(step, residual=False, out=None, xin=None):
+    def call(step, residual=False):
         Wg_, Wu_, Wd_ = sets[step % n_sets]
-        xx = x_for(step) if xin is None else xin
         if kind == "dense":
-            zffn.swiglu_q4k(xx, Wg_, Wu_, Wd_, I, y=y if out is None else out, residual=residual)
+            zffn.swiglu_q4k(x_for(step), Wg_, Wu_, Wd_, I, y=y, residual=residual)
         else:
-            zffn.moe_swiglu_q4k(xx, ids, wts, Wg_, Wu_, Wd_, I, E, y=y if out is None else out,
-                                residual=residual)
+            zffn.moe_swiglu_q4k(x_for(step), ids, wts, Wg_, Wu_, Wd_, I, E, y=y, residual=residual)
 
     launches_per_call = 2                          # zero fill + fused kernel, or gate/up + down
     if kind == "moe" and T > 1:
@@ -358,53 +356,53 @@ def run_gpu(args):
     clocks = clk.summary()
     assert zffn.get_device_error() == zffn.OK
 
-    # end to end through the public API with pinned host buffers
-    x_host = torch.empty(x_for(0).shape, dtype=torch.bfloat16, pin_memory=True)
-    x_host.copy_(x_for(0))
-    y_host = torch.empty((x_host.shape[0], H), dtype=torch.float32, pin_memory=True)
-    x_dev = torch.empty_like(x_for(0))
-    y_e2e = torch.empty((x_host.shape[0], H), dtype=torch.float32, device=dev)
-    barrier()
+    # End to end through the library's host pipeline: every step uploads its
+    # x from pinned host memory and downloads its y into pinned host memory,
+    # overlapped with the neighbouring steps' blocks; wall clock from the
+    # first submission to the final sync.
+    n_rows = x_all.shape[0]
+    x_rows = torch.empty(tuple(x_all.shape), dtype=torch.bfloat16, pin_memory=True)
+    x_rows.copy_(x_all)
+    y_bufs = [torch.empty((T, H), dtype=torch.float32, pin_memory=True) for _ in range(2)]
+    pipe = zffn.Pipeline(T, H, I, 2)
 
-    def e2e_step(s):
-        x_dev.copy_(x_host, non_blocking=True)
-        call(s, out=y_e2e, xin=x_dev)
-        y_host.copy_(y_e2e, non_blocking=True)
+    def host_x(step):
+        if name == "decode_T1":
+            r = step % n_rows
+            return x_rows[r:r + 1]
+        return x_rows
 
-    e2e_how = "torch copies around the call on one stream, CUDA events"
-    if kind == "dense":
-        # the library's host pipeline: every step uploads its x from pinned
-        # host memory and downloads its y, overlapped with the neighbouring
-        # steps' blocks; wall clock from the first submission to the final sync
-        n_rows = x_all.shape[0]
-        x_rows = torch.empty(tuple(x_all.shape), dtype=torch.bfloat16, pin_memory=True)
-        x_rows.copy_(x_all)
-        y_bufs = [torch.empty((T, H), dtype=torch.float32, pin_memory=True) for _ in range(2)]
-        pipe = zffn.Pipeline(T, H, I, 2)
-
-        def host_x(step):
-            if name == "decode_T1":
-                r = step % n_rows
-                return x_rows[r:r + 1]
-            return x_rows
-
-        def submit_all(n):
-            for s in range(n):
-                Wg_, Wu_, Wd_ = sets[s % n_sets]
-                pipe.submit(host_x(s), Wg_, Wu_, Wd_, y_bufs[s % 2])
-            pipe.sync()
-        submit_all(args.warmup)
+    # The routed single-token steps run back to back here, without the L2
+    # flush of the device-timed loop: so that they do not keep reusing the
+    # same 8 experts' weights from L2, each step takes the route of another
+    # token (64 extra seeded logit rows through the device router).
+    routes = [(ids, wts)]
+    if kind == "moe" and T == 1:
+        more = np.random.default_rng(seed + 1000).standard_normal((64, E)).astype(np.float32)
+        r_ids, r_wts = zffn.moe_router_topk(torch.from_numpy(more).to(dev), k)
+        routes = [(r_ids[i:i + 1], r_wts[i:i + 1]) for i in range(64)]
         torch.cuda.synchronize()
-        barrier()
-        t0 = time.perf_counter()
-        submit_all(args.steps)
-        e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
-        pipe.close()
-        assert zffn.get_device_error() == zffn.OK
-        e2e_how = ("zffn_pipeline (host buffers, upload / block / download on three streams, "
-                   "overlapped across steps), wall clock")
-    else:
-        e2e_ms = timed(e2e_step)
+
+    def submit_all(n):
+        for s in range(n):
+            Wg_, Wu_, Wd_ = sets[s % n_sets]
+            if kind == "dense":
+                pipe.submit(host_x(s), Wg_, Wu_, Wd_, y_bufs[s % 2])
+            else:
+                r_ids, r_wts = routes[s % len(routes)]
+                pipe.submit_moe(host_x(s), r_ids, r_wts, Wg_, Wu_, Wd_, E, y_bufs[s % 2])
+        pipe.sync()
+    submit_all(args.warmup)
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    submit_all(args.steps)
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    pipe.close()
+    assert zffn.get_device_error() == zffn.OK
+    e2e_in, e2e_out = int(host_x(0).numel() * 2), int(y_bufs[0].numel() * 4)
+    e2e_how = ("zffn_pipeline (host buffers, upload / block / download on three streams, "
+               "overlapped across steps), wall clock")
 
     # the normalisation in front of the dense block (fp32 residual stream ->
     # bf16 block input), timed on its own over the workload's rows
@@ -500,8 +498,8 @@ def run_gpu(args):
             "algorithmic": {"flop": flop, "hbm_bytes": abytes},
         },
         "e2e": {"value": round(T * world / (e2e_ms * 1e-3), 1), "unit": "tok/s",
-                "h2d_bytes_per_step": int(x_host.numel() * 2),
-                "d2h_bytes_per_step": int(y_host.numel() * 4),
+                "h2d_bytes_per_step": e2e_in,
+                "d2h_bytes_per_step": e2e_out,
                 "ms_per_step": round(e2e_ms, 4), "how": e2e_how},
         "cpu_baseline": cpu,
         **({"router": router} if router is not None else {}),

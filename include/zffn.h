@@ -164,6 +164,15 @@ typedef struct zffn_pipeline zffn_pipeline;
 zffn_status zffn_pipeline_create(zffn_pipeline **out, int T, int H, int I, int depth);
 zffn_status zffn_pipeline_submit(zffn_pipeline *p, const void *x_host, const void *Wg,
                                  const void *Wu, const void *Wd, float *y_host);
+/* As zffn_pipeline_submit for the routed block (zffn_moe_swiglu_q4k): x_host and
+ * y_host in host memory as above; expert_ids, expert_weights (device, [T][top_k],
+ * e.g. from zffn_moe_router_topk) and the stacked expert weights as for
+ * zffn_moe_swiglu_q4k, complete before the call and unchanged until
+ * zffn_pipeline_sync returns. */
+zffn_status zffn_pipeline_submit_moe(zffn_pipeline *p, const void *x_host,
+                                     const int32_t *expert_ids, const float *expert_weights,
+                                     const void *Wg, const void *Wu, const void *Wd, int E,
+                                     int top_k, float *y_host);
 zffn_status zffn_pipeline_sync(zffn_pipeline *p);
 void zffn_pipeline_destroy(zffn_pipeline *p);
 

@@ -505,9 +505,13 @@ zffn_status zffn_pipeline_create(zffn_pipeline **out, int T, int H, int I, int d
     return ZFFN_OK;
 }
 
-zffn_status zffn_pipeline_submit(zffn_pipeline *p, const void *x_host, const void *Wg, const void *Wu,
-                                 const void *Wd, float *y_host) {
-    if (!p || !x_host || !y_host || !Wg || !Wu || !Wd) return ZFFN_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+
+// One submission: upload, the block (`block(x_dev, y_dev, stream)`), download.
+template <typename Block>
+zffn_status pipeline_submit(zffn_pipeline *p, const void *x_host, float *y_host, Block block) {
     if (current_device() != p->device) return ZFFN_ERR_INVALID_ARG;
     const int slot = (int)(p->n % p->depth);
     const size_t xb = (size_t)p->T * p->H * 2, yb = (size_t)p->T * p->H * 4;
@@ -519,7 +523,7 @@ zffn_status zffn_pipeline_submit(zffn_pipeline *p, const void *x_host, const voi
     if (e == cudaSuccess) e = cudaStreamWaitEvent(p->comp, p->in_done[slot], 0);
     if (e == cudaSuccess && reuse) e = cudaStreamWaitEvent(p->comp, p->out_done[slot], 0);
     if (e != cudaSuccess) return to_status(e);
-    const zffn_status st = swiglu_dense(p->x[slot], Wg, Wu, Wd, p->y[slot], p->T, p->H, p->I, p->comp, false);
+    const zffn_status st = block(p->x[slot], p->y[slot], p->comp);
     if (st != ZFFN_OK) return st;
     e = cudaEventRecord(p->comp_done[slot], p->comp);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(p->down, p->comp_done[slot], 0);
@@ -528,6 +532,29 @@ zffn_status zffn_pipeline_submit(zffn_pipeline *p, const void *x_host, const voi
     if (e != cudaSuccess) return to_status(e);
     ++p->n;
     return ZFFN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+zffn_status zffn_pipeline_submit(zffn_pipeline *p, const void *x_host, const void *Wg, const void *Wu,
+                                 const void *Wd, float *y_host) {
+    if (!p || !x_host || !y_host || !Wg || !Wu || !Wd) return ZFFN_ERR_INVALID_ARG;
+    return pipeline_submit(p, x_host, y_host, [&](void *x, float *y, cudaStream_t s) {
+        return swiglu_dense(x, Wg, Wu, Wd, y, p->T, p->H, p->I, s, false);
+    });
+}
+
+zffn_status zffn_pipeline_submit_moe(zffn_pipeline *p, const void *x_host, const int32_t *expert_ids,
+                                     const float *expert_weights, const void *Wg, const void *Wu,
+                                     const void *Wd, int E, int top_k, float *y_host) {
+    if (!p || !x_host || !y_host || !expert_ids || !expert_weights || !Wg || !Wu || !Wd)
+        return ZFFN_ERR_INVALID_ARG;
+    return pipeline_submit(p, x_host, y_host, [&](void *x, float *y, cudaStream_t s) {
+        return swiglu_moe(x, expert_ids, expert_weights, Wg, Wu, Wd, y, p->T, p->H, p->I, E, top_k, s,
+                          false);
+    });
 }
 
 zffn_status zffn_pipeline_sync(zffn_pipeline *p) {

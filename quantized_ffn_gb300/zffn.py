@@ -60,6 +60,7 @@ def load() -> ctypes.CDLL:
                                                      I32),
                 "zffn_pipeline_create": ([ctypes.POINTER(ctypes.c_void_p), I32, I32, I32, I32], I32),
                 "zffn_pipeline_submit": ([P, P, P, P, P, P], I32),
+                "zffn_pipeline_submit_moe": ([P, P, P, P, P, P, P, I32, I32, P], I32),
                 "zffn_pipeline_sync": ([P], I32),
                 "zffn_pipeline_destroy": ([P], None),
                 "zffn_reserve": ([I32, I32, I32, I32, I32], I32),
@@ -237,6 +238,21 @@ class Pipeline:
             _cuda(Wu, "Wu", torch.uint8), _cuda(Wd, "Wd", torch.uint8),
             _host(y_host, "y_host", torch.float32, shape)), "zffn_pipeline_submit")
         self._keep.append((x_host, y_host, Wg, Wu, Wd))
+
+    def submit_moe(self, x_host: torch.Tensor, expert_ids: torch.Tensor, expert_weights: torch.Tensor,
+                   Wg: torch.Tensor, Wu: torch.Tensor, Wd: torch.Tensor, E: int, y_host: torch.Tensor):
+        """The routed block; ids and weights [T, top_k] on the device."""
+        if not self._p:
+            raise RuntimeError("pipeline is closed")
+        shape = (self.T, self.H)
+        top_k = expert_ids.shape[1]
+        _check(load().zffn_pipeline_submit_moe(
+            self._p, _host(x_host, "x_host", torch.bfloat16, shape),
+            _cuda(expert_ids, "expert_ids", torch.int32),
+            _cuda(expert_weights, "expert_weights", torch.float32), _cuda(Wg, "Wg", torch.uint8),
+            _cuda(Wu, "Wu", torch.uint8), _cuda(Wd, "Wd", torch.uint8), E, top_k,
+            _host(y_host, "y_host", torch.float32, shape)), "zffn_pipeline_submit_moe")
+        self._keep.append((x_host, y_host, expert_ids, expert_weights, Wg, Wu, Wd))
 
     def sync(self):
         _check(load().zffn_pipeline_sync(self._p), "zffn_pipeline_sync")

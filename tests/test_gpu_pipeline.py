@@ -102,3 +102,30 @@ def test_pipeline_rejects_wrong_buffers():
                      torch.empty((d["T"], d["H"]), dtype=torch.float32))
     finally:
         p.close()
+
+
+@pytest.mark.parametrize("T", [1, 40])
+def test_pipeline_routed_block(T):
+    # router on the device, then routed blocks over host buffers
+    E, H, I, k = 16, 512, 384, 4
+    rng = np.random.default_rng(10 + T)
+    Wg = np.stack([synth.random_q4k_blocks(rng, I, H, 1e-2) for _ in range(E)])
+    Wu = np.stack([synth.random_q4k_blocks(rng, I, H, 1e-2) for _ in range(E)])
+    Wd = np.stack([synth.random_q4k_blocks(rng, H, I, 1e-2) for _ in range(E)])
+    W = [dev(Wg), dev(Wu), dev(Wd)]
+    logits = [rng.standard_normal((T, E)).astype(np.float32) for _ in range(3)]
+    routes = [zffn.moe_router_topk(dev(lg), k) for lg in logits]
+    torch.cuda.synchronize()
+    xs = [synth.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32)) for _ in range(3)]
+    ys = [torch.empty((T, H), dtype=torch.float32, pin_memory=True) for _ in xs]
+    p = zffn.Pipeline(T, H, I, 2)
+    try:
+        for x, (ids, w), y in zip(xs, routes, ys):
+            p.submit_moe(pinned_bf16(x), ids, w, *W, E, y)
+        p.sync()
+    finally:
+        p.close()
+    assert zffn.get_device_error() == zffn.OK
+    for i, (x, lg, y) in enumerate(zip(xs, logits, ys)):
+        ids, w = orc.route_top_k(lg, k)
+        assert_close(y, orc.moe_swiglu_ffn(x, ids, w, Wg, Wu, Wd, T, H, I, E, k), f"routed {i}")
