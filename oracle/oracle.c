@@ -150,6 +150,108 @@ void oracle_q4k_dequant(const uint8_t *blocks, float *out, int64_t rows, int64_t
         oracle_q4k_dequant_row(blocks + r * rb, cols, out + r * cols);
 }
 
+/* ---- other block formats (W_down of the routed and single-token paths) -----
+ * The pages name Q5_K, Q6_K and Q5_1 expert matrices ("Four bottlenecks, one
+ * CUDA backend...", section "Bottleneck 2": the down projection of the routed
+ * layers runs in Q5_K or Q5_1; section "Bottleneck 4": Q5_K and Q6_K GEMMs)
+ * without laying out their bytes.  Reading: the GGUF arrangements.
+ *   Q5_K (176 bytes / 256 weights): d, dmin (fp16), 12 scale bytes as Q4_K,
+ *     qh[32], qs[128].  Weight k: 4-bit code as Q4_K plus 16 * bit (k / 32)
+ *     of qh[k % 32]; w = d*sc*q - dmin*m, sub-block k / 32.
+ *   Q6_K (210 bytes / 256 weights): ql[128], qh[64], scales[16] (int8), d
+ *     (fp16).  Weight k in half n = k / 128 (r = k % 128, i = r / 32,
+ *     l = r % 32): low 4 bits from ql[64n + l + 32 (i & 1)] (low nibble for
+ *     i < 2, high for i >= 2), high 2 bits = bits 2i, 2i+1 of qh[32n + l];
+ *     w = d * scales[k / 16] * (q - 32).
+ *   Q5_1 (24 bytes / 32 weights): d, m (fp16), qh (32 bits, little endian),
+ *     qs[16].  Weight j < 16: low nibble of qs[j] plus 16 * bit j of qh;
+ *     weight 16 + j: high nibble of qs[j] plus 16 * bit 16 + j; w = d*q + m.
+ * In every format the products are exact in fp32 (Q5_K: 11 x 6 x 5 bits;
+ * Q6_K: 11 bits x |sc * (q - 32)| <= 4096; Q5_1: 11 x 5 bits), so the value
+ * is the exact product (Q6_K) or the exact product with one rounding of the
+ * final addition (Q5_K, Q5_1): bit-exact whatever the evaluation order, as
+ * long as the products are not rounded. */
+enum { FMT_Q4_K = 0, FMT_Q5_K = 1, FMT_Q6_K = 2, FMT_Q5_1 = 3 };
+
+int64_t oracle_fmt_block_weights(int fmt) { return fmt == FMT_Q5_1 ? 32 : 256; }
+
+int64_t oracle_fmt_block_bytes(int fmt)
+{
+    switch (fmt) {
+    case FMT_Q4_K: return 144;
+    case FMT_Q5_K: return 176;
+    case FMT_Q6_K: return 210;
+    case FMT_Q5_1: return 24;
+    default: return 0;
+    }
+}
+
+int64_t oracle_fmt_row_bytes(int fmt, int64_t cols)
+{
+    int64_t bw = oracle_fmt_block_weights(fmt);
+    return ((cols + bw - 1) / bw) * oracle_fmt_block_bytes(fmt);
+}
+
+static float fp16_at(const uint8_t *p) { return oracle_f16_to_f32((uint16_t)(p[0] | (p[1] << 8))); }
+
+/* value of weight k of one block */
+static float q5k_weight(const uint8_t *blk, int k)
+{
+    float d = fp16_at(blk), dmin = fp16_at(blk + 2);
+    const uint8_t *scales = blk + 4, *qh = blk + 16, *qs = blk + 48;
+    int sc, m;
+    oracle_q4k_scale_min(scales, k / 32, &sc, &m);
+    int q = q4k_code(qs, k) + 16 * ((qh[k % 32] >> (k / 32)) & 1);
+    float wq = (d * (float)sc) * (float)q;   /* exact: 11 x 6 x 5 bits */
+    return wq - dmin * (float)m;             /* one rounding           */
+}
+
+static float q6k_weight(const uint8_t *blk, int k)
+{
+    const uint8_t *ql = blk, *qh = blk + 128;
+    const int8_t *scales = (const int8_t *)(blk + 192);
+    float d = fp16_at(blk + 208);
+    int n = k / 128, r = k % 128, i = r / 32, l = r % 32;
+    uint8_t lb = ql[64 * n + l + 32 * (i & 1)];
+    int lo = i < 2 ? (lb & 15) : (lb >> 4);
+    int hi = (qh[32 * n + l] >> (2 * i)) & 3;
+    int q = (lo | (hi << 4)) - 32;
+    return (float)((double)d * (double)(scales[k / 16] * q));   /* exact */
+}
+
+static float q51_weight(const uint8_t *blk, int j)
+{
+    float d = fp16_at(blk), m = fp16_at(blk + 2);
+    uint32_t qh = (uint32_t)blk[4] | ((uint32_t)blk[5] << 8) | ((uint32_t)blk[6] << 16) |
+                  ((uint32_t)blk[7] << 24);
+    const uint8_t *qs = blk + 8;
+    int q = j < 16 ? ((qs[j] & 15) | (((qh >> j) & 1) << 4))
+                   : ((qs[j - 16] >> 4) | (((qh >> j) & 1) << 4));
+    return d * (float)q + m;                 /* d*q exact; one rounding */
+}
+
+void oracle_dequant_row_fmt(int fmt, const uint8_t *row, int64_t cols, float *out)
+{
+    if (fmt == FMT_Q4_K) {
+        oracle_q4k_dequant_row(row, cols, out);
+        return;
+    }
+    int64_t bw = oracle_fmt_block_weights(fmt), bb = oracle_fmt_block_bytes(fmt);
+    for (int64_t col = 0; col < cols; ++col) {
+        const uint8_t *blk = row + (col / bw) * bb;
+        int k = (int)(col % bw);
+        out[col] = fmt == FMT_Q5_K ? q5k_weight(blk, k)
+                 : fmt == FMT_Q6_K ? q6k_weight(blk, k) : q51_weight(blk, k);
+    }
+}
+
+void oracle_dequant_fmt(int fmt, const uint8_t *blocks, float *out, int64_t rows, int64_t cols)
+{
+    int64_t rb = oracle_fmt_row_bytes(fmt, cols);
+    for (int64_t r = 0; r < rows; ++r)
+        oracle_dequant_row_fmt(fmt, blocks + r * rb, cols, out + r * cols);
+}
+
 /* ---- min/max quantiser ------------------------------------------------------
  * The pages do not give a quantiser; this library's reading of a "min/max"
  * Q4_K quantiser, every step in fp32 round-to-nearest (no fused operations,
@@ -258,11 +360,12 @@ double oracle_silu(double g) { return g / (1.0 + exp(-g)); }
  *   Wg, Wu: I rows of H/256 blocks;  Wd: H rows of ceil(I/256) blocks.
  * Each weight row is dequantised once (fp32), the sums run in fp64 in
  * ascending index order. */
-void oracle_swiglu_ffn(const uint16_t *x, const uint8_t *Wg, const uint8_t *Wu,
-                       const uint8_t *Wd, int64_t T, int64_t H, int64_t I, double *y)
+void oracle_swiglu_ffn_fmt(const uint16_t *x, const uint8_t *Wg, const uint8_t *Wu,
+                           const uint8_t *Wd, int wd_fmt, int64_t T, int64_t H, int64_t I,
+                           double *y)
 {
     int64_t rb_in = ((H + QK - 1) / QK) * QK_BYTES;
-    int64_t rb_dn = ((I + QK - 1) / QK) * QK_BYTES;
+    int64_t rb_dn = oracle_fmt_row_bytes(wd_fmt, I);
     double *xf = (double *)malloc(sizeof(double) * (size_t)(T * H));
     double *h = (double *)malloc(sizeof(double) * (size_t)(T * I));
     float *wg = (float *)malloc(sizeof(float) * (size_t)H);
@@ -286,7 +389,7 @@ void oracle_swiglu_ffn(const uint16_t *x, const uint8_t *Wg, const uint8_t *Wu,
     }
     /* y = Wd h */
     for (int64_t n = 0; n < H; ++n) {
-        oracle_q4k_dequant_row(Wd + n * rb_dn, I, wd);
+        oracle_dequant_row_fmt(wd_fmt, Wd + n * rb_dn, I, wd);
         for (int64_t t = 0; t < T; ++t) {
             const double *ht = h + t * I;
             double acc = 0.0;
@@ -298,17 +401,24 @@ void oracle_swiglu_ffn(const uint16_t *x, const uint8_t *Wg, const uint8_t *Wu,
     free(xf); free(h); free(wg); free(wu); free(wd);
 }
 
+/* The block with all three matrices in Q4_K. */
+void oracle_swiglu_ffn(const uint16_t *x, const uint8_t *Wg, const uint8_t *Wu,
+                       const uint8_t *Wd, int64_t T, int64_t H, int64_t I, double *y)
+{
+    oracle_swiglu_ffn_fmt(x, Wg, Wu, Wd, FMT_Q4_K, T, H, I, y);
+}
+
 /* Mixture of experts: y_t = sum_{j < top_k} w[t][j] * FFN_{ids[t][j]}(x_t).
  * Experts are stacked: expert e's W_gate starts at Wg + e * I * rowbytes(H),
  * likewise W_up; its W_down at Wd + e * H * rowbytes(I).  An id outside
  * [0, E) contributes nothing. */
-void oracle_moe_swiglu_ffn(const uint16_t *x, const int32_t *ids, const float *wts,
-                           const uint8_t *Wg, const uint8_t *Wu, const uint8_t *Wd,
-                           int64_t T, int64_t H, int64_t I, int64_t E, int64_t top_k,
-                           double *y)
+void oracle_moe_swiglu_ffn_fmt(const uint16_t *x, const int32_t *ids, const float *wts,
+                               const uint8_t *Wg, const uint8_t *Wu, const uint8_t *Wd,
+                               int wd_fmt, int64_t T, int64_t H, int64_t I, int64_t E,
+                               int64_t top_k, double *y)
 {
     int64_t rb_in = ((H + QK - 1) / QK) * QK_BYTES;
-    int64_t rb_dn = ((I + QK - 1) / QK) * QK_BYTES;
+    int64_t rb_dn = oracle_fmt_row_bytes(wd_fmt, I);
     double *yt = (double *)malloc(sizeof(double) * (size_t)H);
     for (int64_t t = 0; t < T; ++t) {
         double *out = y + t * H;
@@ -318,14 +428,22 @@ void oracle_moe_swiglu_ffn(const uint16_t *x, const int32_t *ids, const float *w
             int64_t e = ids[t * top_k + j];
             if (e < 0 || e >= E)
                 continue;
-            oracle_swiglu_ffn(x + t * H, Wg + e * I * rb_in, Wu + e * I * rb_in,
-                              Wd + e * H * rb_dn, 1, H, I, yt);
+            oracle_swiglu_ffn_fmt(x + t * H, Wg + e * I * rb_in, Wu + e * I * rb_in,
+                                  Wd + e * H * rb_dn, wd_fmt, 1, H, I, yt);
             double w = (double)wts[t * top_k + j];
             for (int64_t n = 0; n < H; ++n)
                 out[n] += w * yt[n];
         }
     }
     free(yt);
+}
+
+void oracle_moe_swiglu_ffn(const uint16_t *x, const int32_t *ids, const float *wts,
+                           const uint8_t *Wg, const uint8_t *Wu, const uint8_t *Wd,
+                           int64_t T, int64_t H, int64_t I, int64_t E, int64_t top_k,
+                           double *y)
+{
+    oracle_moe_swiglu_ffn_fmt(x, ids, wts, Wg, Wu, Wd, FMT_Q4_K, T, H, I, E, top_k, y);
 }
 
 /* Router: for each token t, the top_k of its E logits and their softmax

@@ -27,6 +27,16 @@ _lib = None
 QK = 256
 QK_BYTES = 144
 
+# block formats of W_down (the values match the library's format codes only by
+# the shared reading of the pages; nothing is imported from it)
+FMT_Q4_K, FMT_Q5_K, FMT_Q6_K, FMT_Q5_1 = 0, 1, 2, 3
+_FMT_BLOCK = {FMT_Q4_K: (256, 144), FMT_Q5_K: (256, 176), FMT_Q6_K: (256, 210), FMT_Q5_1: (32, 24)}
+
+
+def row_bytes_fmt(fmt: int, cols: int) -> int:
+    bw, bb = _FMT_BLOCK[fmt]
+    return ((cols + bw - 1) // bw) * bb
+
 
 def row_bytes(cols: int) -> int:
     return ((cols + QK - 1) // QK) * QK_BYTES
@@ -67,6 +77,12 @@ def _load():
             lib.oracle_swiglu_ffn.argtypes = [P, P, P, P, I64, I64, I64, P]
             lib.oracle_moe_swiglu_ffn.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, I64, P]
             lib.oracle_route_top_k.argtypes = [P, I64, I64, I64, P, P]
+            lib.oracle_dequant_fmt.argtypes = [ctypes.c_int, P, P, I64, I64]
+            lib.oracle_swiglu_ffn_fmt.argtypes = [P, P, P, P, ctypes.c_int, I64, I64, I64, P]
+            lib.oracle_moe_swiglu_ffn_fmt.argtypes = [P, P, P, P, P, P, ctypes.c_int, I64, I64, I64,
+                                                      I64, I64, P]
+            lib.oracle_fmt_row_bytes.argtypes = [ctypes.c_int, I64]
+            lib.oracle_fmt_row_bytes.restype = I64
             lib.oracle_bf16_from_f64.argtypes = [ctypes.c_double]
             lib.oracle_bf16_from_f64.restype = ctypes.c_uint16
             lib.oracle_rmsnorm_bf16.argtypes = [P, P, ctypes.c_double, I64, I64, P]
@@ -132,24 +148,28 @@ def q4k_quantize(w: np.ndarray) -> np.ndarray:
 # ---- feed-forward ----------------------------------------------------------
 
 def swiglu_ffn(x_bf16: np.ndarray, Wg: np.ndarray, Wu: np.ndarray, Wd: np.ndarray,
-               T: int, H: int, I: int) -> np.ndarray:
-    """y[T, H] in float64 for bf16 bits x[T, H] and Q4_K weights."""
+               T: int, H: int, I: int, wd_fmt: int = FMT_Q4_K) -> np.ndarray:
+    """y[T, H] in float64 for bf16 bits x[T, H], Q4_K W_gate and W_up, and W_down
+    in block format wd_fmt."""
     x_bf16 = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     Wg = np.ascontiguousarray(Wg, dtype=np.uint8)
     Wu = np.ascontiguousarray(Wu, dtype=np.uint8)
     Wd = np.ascontiguousarray(Wd, dtype=np.uint8)
     assert x_bf16.size == T * H
     assert Wg.size == I * row_bytes(H) and Wu.size == I * row_bytes(H)
-    assert Wd.size == H * row_bytes(I)
+    assert Wd.size == H * row_bytes_fmt(wd_fmt, I)
     y = np.empty((T, H), dtype=np.float64)
-    _load().oracle_swiglu_ffn(_ptr(x_bf16), _ptr(Wg), _ptr(Wu), _ptr(Wd), T, H, I, _ptr(y))
+    _load().oracle_swiglu_ffn_fmt(_ptr(x_bf16), _ptr(Wg), _ptr(Wu), _ptr(Wd), wd_fmt, T, H, I,
+                                  _ptr(y))
     return y
 
 
 def moe_swiglu_ffn(x_bf16: np.ndarray, ids: np.ndarray, wts: np.ndarray,
                    Wg: np.ndarray, Wu: np.ndarray, Wd: np.ndarray,
-                   T: int, H: int, I: int, E: int, top_k: int) -> np.ndarray:
-    """y[T, H] float64 for the routed experts; weights stacked [E, rows, bytes]."""
+                   T: int, H: int, I: int, E: int, top_k: int,
+                   wd_fmt: int = FMT_Q4_K) -> np.ndarray:
+    """y[T, H] float64 for the routed experts; weights stacked [E, rows, bytes],
+    W_down in block format wd_fmt."""
     x_bf16 = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     ids = np.ascontiguousarray(ids, dtype=np.int32)
     wts = np.ascontiguousarray(wts, dtype=np.float32)
@@ -157,11 +177,20 @@ def moe_swiglu_ffn(x_bf16: np.ndarray, ids: np.ndarray, wts: np.ndarray,
     Wu = np.ascontiguousarray(Wu, dtype=np.uint8)
     Wd = np.ascontiguousarray(Wd, dtype=np.uint8)
     assert ids.size == T * top_k and wts.size == T * top_k
-    assert Wg.size == E * I * row_bytes(H) and Wd.size == E * H * row_bytes(I)
+    assert Wg.size == E * I * row_bytes(H) and Wd.size == E * H * row_bytes_fmt(wd_fmt, I)
     y = np.empty((T, H), dtype=np.float64)
-    _load().oracle_moe_swiglu_ffn(_ptr(x_bf16), _ptr(ids), _ptr(wts), _ptr(Wg), _ptr(Wu),
-                                  _ptr(Wd), T, H, I, E, top_k, _ptr(y))
+    _load().oracle_moe_swiglu_ffn_fmt(_ptr(x_bf16), _ptr(ids), _ptr(wts), _ptr(Wg), _ptr(Wu),
+                                      _ptr(Wd), wd_fmt, T, H, I, E, top_k, _ptr(y))
     return y
+
+
+def dequant_fmt(blocks: np.ndarray, fmt: int, rows: int, cols: int) -> np.ndarray:
+    """fp32 [rows, cols] from rows of blocks of format fmt."""
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+    assert blocks.size == rows * row_bytes_fmt(fmt, cols)
+    out = np.empty((rows, cols), dtype=np.float32)
+    _load().oracle_dequant_fmt(fmt, _ptr(blocks), _ptr(out), rows, cols)
+    return out
 
 
 def route_top_k(logits: np.ndarray, top_k: int):

@@ -71,6 +71,43 @@ def random_q4k_blocks(rng: np.random.Generator, rows: int, cols: int,
     return out.reshape(rows, nb * QK_BYTES)
 
 
+# block formats of W_down on the single-token paths: code, weights and bytes
+# per block
+FMT_Q4_K, FMT_Q5_K, FMT_Q6_K, FMT_Q5_1 = 0, 1, 2, 3
+FMT_BLOCK = {FMT_Q4_K: (256, 144), FMT_Q5_K: (256, 176), FMT_Q6_K: (256, 210), FMT_Q5_1: (32, 24)}
+
+
+def row_bytes_fmt(fmt: int, cols: int) -> int:
+    bw, bb = FMT_BLOCK[fmt]
+    return ((cols + bw - 1) // bw) * bb
+
+
+def random_blocks(rng: np.random.Generator, fmt: int, rows: int, cols: int,
+                  dscale: float = 1e-3) -> np.ndarray:
+    """Random rows of blocks of format fmt: uniform random bytes everywhere
+    except the fp16 scale fields, which get fp16(|N(0, dscale)|) (Q5_1's
+    offset m: fp16(N(0, dscale)), either sign).  Uniform bytes make every code
+    and every packed scale uniform on its range."""
+    if fmt == FMT_Q4_K:
+        return random_q4k_blocks(rng, rows, cols, dscale)
+    bw, bb = FMT_BLOCK[fmt]
+    nb = (cols + bw - 1) // bw
+    out = rng.integers(0, 256, size=(rows, nb, bb), dtype=np.uint8)
+    d = np.abs(rng.normal(0.0, dscale, size=(rows, nb))).astype(np.float16).view(np.uint8)
+    d = d.reshape(rows, nb, 2)
+    if fmt == FMT_Q5_K:
+        out[:, :, 0:2] = d
+        out[:, :, 2:4] = np.abs(rng.normal(0.0, dscale, size=(rows, nb))).astype(
+            np.float16).view(np.uint8).reshape(rows, nb, 2)
+    elif fmt == FMT_Q6_K:
+        out[:, :, 208:210] = d
+    else:
+        out[:, :, 0:2] = d
+        out[:, :, 2:4] = rng.normal(0.0, dscale, size=(rows, nb)).astype(
+            np.float16).view(np.uint8).reshape(rows, nb, 2)
+    return out.reshape(rows, nb * bb)
+
+
 def tiny(seed: int = 0):
     """The tiny block: T=16, H=256, I=704; weights already in Q4_K."""
     T, H, I = 16, 256, 704
