@@ -176,6 +176,51 @@ zffn_status zffn_pipeline_submit_moe(zffn_pipeline *p, const void *x_host,
 zffn_status zffn_pipeline_sync(zffn_pipeline *p);
 void zffn_pipeline_destroy(zffn_pipeline *p);
 
+/* Block formats of W_down.  The pages name Q5_K, Q6_K and Q5_1 expert and down
+ * matrices next to Q4_K ("Four bottlenecks, one CUDA backend...", section
+ * "Bottleneck 2": the routed layers' down projection in Q5_K or Q5_1; section
+ * "Bottleneck 4": Q5_K and Q6_K) without laying them out; the arrangement used
+ * is GGUF's:
+ *   ZFFN_FMT_Q5_K  176 bytes / 256 weights: fp16 d, fp16 dmin, 12 scale bytes
+ *     packed as Q4_K, qh[32], qs[128]; code = nibble (as Q4_K) + 16 * bit
+ *     (k/32) of qh[k%32]; w = d*sc*q - dmin*m.
+ *   ZFFN_FMT_Q6_K  210 bytes / 256 weights: ql[128], qh[64], int8 scales[16],
+ *     fp16 d; w = d * scales[k/16] * (q - 32), q of 6 bits (4 from ql, 2 from
+ *     qh).
+ *   ZFFN_FMT_Q5_1  24 bytes / 32 weights: fp16 d, fp16 m, 32-bit qh, qs[16];
+ *     w = d*q + m, q of 5 bits. */
+typedef enum {
+    ZFFN_FMT_Q4_K = 0,
+    ZFFN_FMT_Q5_K = 1,
+    ZFFN_FMT_Q6_K = 2,
+    ZFFN_FMT_Q5_1 = 3
+} zffn_format;
+
+/* Bytes of one row of `cols` weights in format fmt (0 for cols <= 0 or an
+ * unknown format). */
+size_t zffn_row_bytes_fmt(int fmt, int64_t cols);
+
+/* fp32 [rows][cols] from rows of blocks of format fmt, bit-exact (every product
+ * in the formats is exact in fp32; at most the final addition rounds).
+ * Errors: INVALID_ARG, CUDA. */
+zffn_status zffn_dequant_fmt(int fmt, const void *blocks, float *out, int64_t rows,
+                             int64_t cols, void *stream);
+
+/* The block with W_gate and W_up in Q4_K and W_down in format wd_fmt (rows of
+ * zffn_row_bytes_fmt(wd_fmt, I) bytes).  ZFFN_FMT_Q4_K is zffn_swiglu_q4k.  The
+ * other formats run on the single-token path only: T must be 1, otherwise
+ * ZFFN_ERR_UNSUPPORTED.  Wd needs no alignment beyond a byte.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA, NO_WORKSPACE. */
+zffn_status zffn_swiglu_q4k_wd(const void *x, const void *Wg, const void *Wu, const void *Wd,
+                               int wd_fmt, float *y, int T, int H, int I, void *stream);
+
+/* The routed block (as zffn_moe_swiglu_q4k) with every expert's W_down in
+ * format wd_fmt; the same restrictions as zffn_swiglu_q4k_wd. */
+zffn_status zffn_moe_swiglu_q4k_wd(const void *x, const int32_t *expert_ids,
+                                   const float *expert_weights, const void *Wg, const void *Wu,
+                                   const void *Wd, int wd_fmt, float *y, int T, int H, int I,
+                                   int E, int top_k, void *stream);
+
 /* Mixture-of-experts SwiGLU block:
  *     y[t] = sum_{j < top_k} expert_weights[t][j] * FFN_{expert_ids[t][j]}(x[t])
  * ("Four bottlenecks, one CUDA backend...", section "Bottleneck 2 -- MoE decode

@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "zffn_internal.cuh"
+#include "formats.h"
 #include "rmsnorm.h"
 #include "router.h"
 
@@ -327,6 +328,65 @@ zffn_status zffn_moe_swiglu_q4k_residual(const void *x, const int32_t *expert_id
                                          int I, int E, int top_k, void *stream) {
     return swiglu_moe(x, expert_ids, expert_weights, Wg, Wu, Wd, y, T, H, I, E, top_k, stream,
                       true);
+}
+
+size_t zffn_row_bytes_fmt(int fmt, int64_t cols) {
+    return cols <= 0 || !fmt_valid(fmt) ? 0 : (size_t)fmt_row_bytes(fmt, cols);
+}
+
+zffn_status zffn_dequant_fmt(int fmt, const void *blocks, float *out, int64_t rows, int64_t cols,
+                             void *stream) {
+    if (!fmt_valid(fmt) || !blocks || !out || rows <= 0 || cols <= 0) return ZFFN_ERR_INVALID_ARG;
+    if (device_info().device < 0) return ZFFN_ERR_CUDA;
+    return to_status(launch_dequant_fmt(fmt, blocks, out, rows, cols, (cudaStream_t)stream));
+}
+
+zffn_status zffn_moe_swiglu_q4k_wd(const void *x, const int32_t *expert_ids,
+                                   const float *expert_weights, const void *Wg, const void *Wu,
+                                   const void *Wd, int wd_fmt, float *y, int T, int H, int I, int E,
+                                   int top_k, void *stream) {
+    if (!fmt_valid(wd_fmt)) return ZFFN_ERR_INVALID_ARG;
+    if (wd_fmt == kFmtQ4_K)
+        return expert_ids ? swiglu_moe(x, expert_ids, expert_weights, Wg, Wu, Wd, y, T, H, I, E,
+                                       top_k, stream, false)
+                          : swiglu_dense(x, Wg, Wu, Wd, y, T, H, I, stream, false);
+    const bool moe = expert_ids != nullptr;
+    if (!x || !Wg || !Wu || !Wd || !y || (moe && !expert_weights)) return ZFFN_ERR_INVALID_ARG;
+    if (check_shape(T, H, I) != ZFFN_OK) return ZFFN_ERR_INVALID_ARG;
+    if (moe && (E < 1 || E > 4096 || top_k < 1 || top_k > 64)) return ZFFN_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wu) || (reinterpret_cast<uintptr_t>(y) & 3) ||
+        (moe && ((reinterpret_cast<uintptr_t>(expert_ids) & 3) ||
+                 (reinterpret_cast<uintptr_t>(expert_weights) & 3))))
+        return ZFFN_ERR_INVALID_ARG;
+    if (T != 1) return ZFFN_ERR_UNSUPPORTED;       // other formats: single-token paths only
+    const int k = moe ? top_k : 1;
+    const DeviceInfo &di = device_info();
+    if (di.device < 0) return ZFFN_ERR_CUDA;
+    if (gu_smem_total(H, I, k) > (size_t)di.max_smem_optin ||
+        down_fmt_smem_bytes(I, k) > (size_t)di.max_smem_optin)
+        return ZFFN_ERR_UNSUPPORTED;
+    const Layout L = layout_for(1, H, I, moe ? E : 1, k);
+    Workspace *w = nullptr;
+    zffn_status st = ensure_workspace(L.total, &w);
+    if (st != ZFFN_OK) return st;
+    MatvecArgs a{};
+    a.x = static_cast<const __nv_bfloat16 *>(x);
+    a.Wg = static_cast<const uint8_t *>(Wg);
+    a.Wu = static_cast<const uint8_t *>(Wu);
+    a.Wd = static_cast<const uint8_t *>(Wd);
+    a.ids = expert_ids;
+    a.wts = expert_weights;
+    a.y = y;
+    a.h = reinterpret_cast<float *>(static_cast<uint8_t *>(w->ptr) + L.h);
+    a.err = di.err_word;
+    a.T = 1; a.H = H; a.I = I; a.E = moe ? E : 1; a.k = k;
+    a.accumulate = false;
+    return to_status(launch_token_fmt(a, wd_fmt, (cudaStream_t)stream));
+}
+
+zffn_status zffn_swiglu_q4k_wd(const void *x, const void *Wg, const void *Wu, const void *Wd,
+                               int wd_fmt, float *y, int T, int H, int I, void *stream) {
+    return zffn_moe_swiglu_q4k_wd(x, nullptr, nullptr, Wg, Wu, Wd, wd_fmt, y, T, H, I, 1, 1, stream);
 }
 
 zffn_status zffn_rmsnorm_bf16(const float *h, const float *gamma, float eps, void *x, int T, int H,

@@ -55,6 +55,10 @@ def load() -> ctypes.CDLL:
                 "zffn_moe_swiglu_q4k_residual": ([P, P, P, P, P, P, P, I32, I32, I32, I32, I32, P],
                                                  I32),
                 "zffn_moe_router_topk": ([P, P, P, I32, I32, I32, P], I32),
+                "zffn_row_bytes_fmt": ([I32, I64], ctypes.c_size_t),
+                "zffn_dequant_fmt": ([I32, P, P, I64, I64, P], I32),
+                "zffn_swiglu_q4k_wd": ([P, P, P, P, I32, P, I32, I32, I32, P], I32),
+                "zffn_moe_swiglu_q4k_wd": ([P, P, P, P, P, P, I32, P, I32, I32, I32, I32, I32, P], I32),
                 "zffn_rmsnorm_bf16": ([P, P, ctypes.c_float, P, I32, I32, P], I32),
                 "zffn_swiglu_q4k_prenorm_residual": ([P, P, ctypes.c_float, P, P, P, I32, I32, I32, P],
                                                      I32),
@@ -160,6 +164,53 @@ def moe_swiglu_q4k(x: torch.Tensor, expert_ids: torch.Tensor, expert_weights: to
         _cuda(expert_weights, "expert_weights", torch.float32), _cuda(Wg, "Wg", torch.uint8),
         _cuda(Wu, "Wu", torch.uint8), _cuda(Wd, "Wd", torch.uint8),
         _cuda(y, "y", torch.float32), T, H, I, E, top_k, _stream(stream)), "zffn_moe_swiglu_q4k")
+    return y
+
+
+FMT_Q4_K, FMT_Q5_K, FMT_Q6_K, FMT_Q5_1 = 0, 1, 2, 3
+
+
+def row_bytes_fmt(fmt: int, cols: int) -> int:
+    return int(load().zffn_row_bytes_fmt(int(fmt), int(cols)))
+
+
+def dequant_fmt(blocks: torch.Tensor, fmt: int, rows: int, cols: int,
+                out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """fp32 [rows, cols] from rows of blocks of format fmt (bit-exact)."""
+    if out is None:
+        out = torch.empty((rows, cols), dtype=torch.float32, device=blocks.device)
+    _check(load().zffn_dequant_fmt(int(fmt), _cuda(blocks, "blocks", torch.uint8),
+                                   _cuda(out, "out", torch.float32), rows, cols, _stream(stream)),
+           "zffn_dequant_fmt")
+    return out
+
+
+def swiglu_q4k_wd(x: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor, Wd: torch.Tensor, wd_fmt: int,
+                  I: int, y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The block with W_down in block format wd_fmt (other than Q4_K: T = 1 only)."""
+    T, H = x.shape
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    _check(load().zffn_swiglu_q4k_wd(_cuda(x, "x", torch.bfloat16), _cuda(Wg, "Wg", torch.uint8),
+                                     _cuda(Wu, "Wu", torch.uint8), _cuda(Wd, "Wd", torch.uint8),
+                                     int(wd_fmt), _cuda(y, "y", torch.float32), T, H, I,
+                                     _stream(stream)), "zffn_swiglu_q4k_wd")
+    return y
+
+
+def moe_swiglu_q4k_wd(x: torch.Tensor, expert_ids: torch.Tensor, expert_weights: torch.Tensor,
+                      Wg: torch.Tensor, Wu: torch.Tensor, Wd: torch.Tensor, wd_fmt: int, I: int,
+                      E: int, y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The routed block with every expert's W_down in block format wd_fmt."""
+    T, H = x.shape
+    top_k = expert_ids.shape[1]
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    _check(load().zffn_moe_swiglu_q4k_wd(
+        _cuda(x, "x", torch.bfloat16), _cuda(expert_ids, "expert_ids", torch.int32),
+        _cuda(expert_weights, "expert_weights", torch.float32), _cuda(Wg, "Wg", torch.uint8),
+        _cuda(Wu, "Wu", torch.uint8), _cuda(Wd, "Wd", torch.uint8), int(wd_fmt),
+        _cuda(y, "y", torch.float32), T, H, I, E, top_k, _stream(stream)), "zffn_moe_swiglu_q4k_wd")
     return y
 
 

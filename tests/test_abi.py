@@ -137,3 +137,22 @@ def test_pipeline_rejects_bad_args(lib, T, H, I, depth):
     assert zffn.load().zffn_pipeline_submit(None, FAKE, FAKE, FAKE, FAKE, FAKE) == zffn.ERR_INVALID_ARG
     assert zffn.load().zffn_pipeline_sync(None) == zffn.ERR_INVALID_ARG
     zffn.load().zffn_pipeline_destroy(None)
+
+
+def test_format_row_bytes_and_rejections(lib):
+    assert zffn.row_bytes_fmt(zffn.FMT_Q4_K, 11008) == 43 * 144
+    assert zffn.row_bytes_fmt(zffn.FMT_Q5_K, 768) == 3 * 176
+    assert zffn.row_bytes_fmt(zffn.FMT_Q6_K, 11008) == 43 * 210
+    assert zffn.row_bytes_fmt(zffn.FMT_Q5_1, 704) == 22 * 24
+    assert zffn.row_bytes_fmt(7, 256) == 0 and zffn.row_bytes_fmt(zffn.FMT_Q5_K, 0) == 0
+    L = lib
+    assert L.zffn_dequant_fmt(7, FAKE, FAKE, 1, 256, None) == zffn.ERR_INVALID_ARG
+    assert L.zffn_dequant_fmt(1, FAKE, FAKE, 0, 256, None) == zffn.ERR_INVALID_ARG
+    assert L.zffn_swiglu_q4k_wd(FAKE, FAKE, FAKE, FAKE, 9, FAKE, 1, 256, 256, None) == zffn.ERR_INVALID_ARG
+    assert L.zffn_swiglu_q4k_wd(FAKE, FAKE, FAKE, FAKE, 2, FAKE, 1, 200, 256, None) == zffn.ERR_INVALID_ARG
+    # other formats of W_down: single-token paths only (checked on the host)
+    assert L.zffn_swiglu_q4k_wd(FAKE, FAKE, FAKE, FAKE, 2, FAKE, 4, 256, 256, None) == zffn.ERR_UNSUPPORTED
+    assert L.zffn_moe_swiglu_q4k_wd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 3, 256, 256, 8, 2,
+                                    None) == zffn.ERR_UNSUPPORTED
+    assert L.zffn_moe_swiglu_q4k_wd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 1, 256, 256, 0, 2,
+                                    None) == zffn.ERR_INVALID_ARG

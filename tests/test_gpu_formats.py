@@ -1,0 +1,80 @@
+"""Other block formats of W_down (Q5_K, Q6_K, Q5_1) on the GPU through the C
+ABI: the dequantisation bit-exact against the oracle, and the single-token
+dense and routed blocks with W_down in each format against the oracle at the
+block's tolerance."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as orc
+from quantized_ffn_gb300 import synth, zffn
+from tests.gpu_util import assert_close, dev, x_dev
+
+pytestmark = pytest.mark.gpu
+
+FORMATS = [zffn.FMT_Q5_K, zffn.FMT_Q6_K, zffn.FMT_Q5_1]
+
+
+@pytest.mark.parametrize("fmt", FORMATS + [zffn.FMT_Q4_K])
+@pytest.mark.parametrize("rows,cols", [(64, 768), (7, 11008), (33, 704)])
+def test_dequant_bit_exact(fmt, rows, cols):
+    rng = np.random.default_rng(fmt * 100 + rows)
+    blocks = synth.random_blocks(rng, fmt, rows, cols, 1e-2)
+    got = zffn.dequant_fmt(dev(blocks), fmt, rows, cols).cpu().numpy()
+    ref = orc.dequant_fmt(blocks, fmt, rows, cols)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def token(rng, H):
+    return synth.f32_to_bf16_bits(rng.standard_normal((1, H)).astype(np.float32))
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("H,I", [(1024, 1472), (256, 704), (4096, 11008)])
+def test_single_token_block(fmt, H, I):
+    rng = np.random.default_rng(fmt + H + I)
+    Wg = synth.random_q4k_blocks(rng, I, H, 1e-2)
+    Wu = synth.random_q4k_blocks(rng, I, H, 1e-2)
+    Wd = synth.random_blocks(rng, fmt, H, I, 1e-2)
+    x = token(rng, H)
+    y = zffn.swiglu_q4k_wd(x_dev(x), dev(Wg), dev(Wu), dev(Wd), fmt, I)
+    assert zffn.get_device_error() == zffn.OK
+    assert_close(y, orc.swiglu_ffn(x, Wg, Wu, Wd, 1, H, I, wd_fmt=fmt), f"fmt {fmt} H={H} I={I}")
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_routed_single_token_full_config(fmt):
+    # E = 128, H = 2048, I = 768, top-8 with every expert's W_down in fmt
+    E, H, I, k = 128, 2048, 768, 8
+    rng = np.random.default_rng(200 + fmt)
+    Wg = np.stack([synth.random_q4k_blocks(rng, I, H, 1e-2) for _ in range(E)])
+    Wu = np.stack([synth.random_q4k_blocks(rng, I, H, 1e-2) for _ in range(E)])
+    Wd = np.stack([synth.random_blocks(rng, fmt, H, I, 1e-2) for _ in range(E)])
+    ids, w = orc.route_top_k(rng.standard_normal((1, E)).astype(np.float32), k)
+    ids[0, 3] = E + 2                       # an invalid slot contributes nothing
+    x = token(rng, H)
+    y = zffn.moe_swiglu_q4k_wd(x_dev(x), dev(ids), dev(w), dev(Wg), dev(Wu), dev(Wd), fmt, I, E)
+    assert zffn.get_device_error() == zffn.OK
+    ref = orc.moe_swiglu_ffn(x, ids, w, Wg, Wu, Wd, 1, H, I, E, k, wd_fmt=fmt)
+    assert_close(y, ref, f"routed fmt {fmt}")
+
+
+def test_q4k_format_code_is_the_regular_block():
+    rng = np.random.default_rng(300)
+    H, I = 512, 384
+    W = [synth.random_q4k_blocks(rng, I, H, 1e-2), synth.random_q4k_blocks(rng, I, H, 1e-2),
+         synth.random_q4k_blocks(rng, H, I, 1e-2)]
+    x = synth.f32_to_bf16_bits(rng.standard_normal((5, H)).astype(np.float32))
+    y = zffn.swiglu_q4k_wd(x_dev(x), *[dev(a) for a in W], zffn.FMT_Q4_K, I)
+    assert_close(y, orc.swiglu_ffn(x, *W, 5, H, I), "Q4_K through the format entry")
+
+
+def test_other_formats_reject_several_tokens():
+    rng = np.random.default_rng(301)
+    H, I = 256, 256
+    W = [dev(synth.random_q4k_blocks(rng, I, H)), dev(synth.random_q4k_blocks(rng, I, H)),
+         dev(synth.random_blocks(rng, zffn.FMT_Q6_K, H, I))]
+    x = x_dev(synth.f32_to_bf16_bits(rng.standard_normal((3, H)).astype(np.float32)))
+    with pytest.raises(zffn.ZffnError) as e:
+        zffn.swiglu_q4k_wd(x, *W, zffn.FMT_Q6_K, I)
+    assert e.value.status == zffn.ERR_UNSUPPORTED
