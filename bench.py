@@ -427,6 +427,40 @@ def run_gpu(args):
         norm = {"kernel": "rmsnorm_bf16_kernel", "ms": round(n_ms, 5), "hbm_bytes": n_bytes,
                 "achieved_gbs": round(n_gbs, 2), "frac_of_hbm_peak": round(n_gbs / peaks["hbm"], 4)}
 
+    # single-token blocks with W_down in the other block formats (W_gate and
+    # W_up the workload's Q4_K matrices, W_down seeded random blocks of the
+    # format), one call between events after an L2 flush
+    down_formats = None
+    if T == 1:
+        from quantized_ffn_gb300 import synth as _synth
+        down_formats = {}
+        rng_f = np.random.default_rng(seed + 2000)
+        for fname, fmt in (("Q5_K", zffn.FMT_Q5_K), ("Q6_K", zffn.FMT_Q6_K), ("Q5_1", zffn.FMT_Q5_1)):
+            Wd_f = torch.from_numpy(np.stack([_synth.random_blocks(rng_f, fmt, H, I, 1e-3)
+                                              for _ in range(E)])).to(dev)
+            f_st = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+            f_en = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+            for s in range(args.steps + 2):
+                flush.zero_()
+                if s >= 2:
+                    f_st[s - 2].record(stream)
+                if kind == "dense":
+                    zffn.swiglu_q4k_wd(x_for(0), W[0], W[1], Wd_f, fmt, I, y=y)
+                else:
+                    zffn.moe_swiglu_q4k_wd(x_for(0), ids, wts, W[0], W[1], Wd_f, fmt, I, E, y=y)
+                if s >= 2:
+                    f_en[s - 2].record(stream)
+            torch.cuda.synchronize()
+            assert zffn.get_device_error() == zffn.OK
+            f_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(f_st, f_en))
+            touched = 1 if kind == "dense" else k
+            f_bytes = touched * (2 * I * row_bytes(H) + H * zffn.row_bytes_fmt(fmt, I)) + H * 2 + H * 4
+            f_gbs = f_bytes / (f_ms * 1e-3) / 1e9
+            down_formats[fname] = {"ms": round(f_ms, 5), "hbm_bytes": f_bytes,
+                                   "achieved_gbs": round(f_gbs, 1),
+                                   "frac_of_hbm_peak": round(f_gbs / peaks["hbm"], 4)}
+            del Wd_f
+
     # the router of the routed layer (logits -> ids, weights), timed on its own
     router = None
     if kind == "moe":
@@ -504,6 +538,9 @@ def run_gpu(args):
         "cpu_baseline": cpu,
         **({"router": router} if router is not None else {}),
         **({"rmsnorm": norm} if norm is not None else {}),
+        **({"down_formats": {"kernels": "ffn_gu_kernel + down_fmt_kernel", "timing":
+                             "one isolated call after an L2 flush", **down_formats}}
+           if down_formats is not None else {}),
         "clocks": clocks,
         "gpu_launches": launches_per_call * args.steps,
         "wall_s_timed_loop": round(wall, 4),

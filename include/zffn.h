@@ -209,7 +209,10 @@ zffn_status zffn_dequant_fmt(int fmt, const void *blocks, float *out, int64_t ro
 /* The block with W_gate and W_up in Q4_K and W_down in format wd_fmt (rows of
  * zffn_row_bytes_fmt(wd_fmt, I) bytes).  ZFFN_FMT_Q4_K is zffn_swiglu_q4k.  The
  * other formats run on the single-token path only: T must be 1, otherwise
- * ZFFN_ERR_UNSUPPORTED.  Wd needs no alignment beyond a byte.
+ * ZFFN_ERR_UNSUPPORTED.  Wd must be 4-byte aligned (its rows need not be: Q6_K
+ * rows are 210-byte multiples).  Also UNSUPPORTED when top_k * I fp32 values of
+ * h plus 64 KB of row buffers exceed a block's shared memory (I > 40960 at
+ * top_k = 1).
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA, NO_WORKSPACE. */
 zffn_status zffn_swiglu_q4k_wd(const void *x, const void *Wg, const void *Wu, const void *Wd,
                                int wd_fmt, float *y, int T, int H, int I, void *stream);

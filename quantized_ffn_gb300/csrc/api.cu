@@ -354,7 +354,8 @@ zffn_status zffn_moe_swiglu_q4k_wd(const void *x, const int32_t *expert_ids,
     if (!x || !Wg || !Wu || !Wd || !y || (moe && !expert_weights)) return ZFFN_ERR_INVALID_ARG;
     if (check_shape(T, H, I) != ZFFN_OK) return ZFFN_ERR_INVALID_ARG;
     if (moe && (E < 1 || E > 4096 || top_k < 1 || top_k > 64)) return ZFFN_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wu) || (reinterpret_cast<uintptr_t>(y) & 3) ||
+    if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wu) || (reinterpret_cast<uintptr_t>(Wd) & 3) ||
+        (reinterpret_cast<uintptr_t>(y) & 3) ||
         (moe && ((reinterpret_cast<uintptr_t>(expert_ids) & 3) ||
                  (reinterpret_cast<uintptr_t>(expert_weights) & 3))))
         return ZFFN_ERR_INVALID_ARG;

@@ -25,11 +25,13 @@
 //   down_fmt_kernel<F>: y[n] = sum_p w_p * Wd_{e_p}[n] . h[p] for one token,
 //     launched as a programmatic dependent of the Q4_K gate/up kernel of the
 //     single-token path, which leaves h (fp32 [P][I]) in the workspace.  One
-//     warp per output row at a time: lane t dequantises weight t of each
-//     32-weight group of the row (the group's header bytes are broadcast
-//     loads, its codes one byte per lane) and multiplies it by h, staged in
-//     shared memory; the row's sum is one warp reduction.  The rows of the
-//     grid are interleaved so that all warps stream the matrix together.
+//     warp per output row at a time: the warp copies the row, a chunk of
+//     whole 256-weight units at a time, into its shared-memory buffer (4-byte
+//     loads by all lanes, so that many are in flight), then lane t takes the
+//     eight weights 8t .. 8t+7 of each unit, which share one scale (decoded
+//     once), and multiplies them by h, staged in shared memory; the row's sum
+//     is one warp reduction.  The rows of the grid are interleaved so that
+//     all warps stream the matrix together.
 #include "formats.h"
 
 #include "zffn_internal.cuh"
@@ -53,17 +55,17 @@ __device__ __forceinline__ float fp16_at(const uint8_t *p) {
 
 // Value of weight k of the block at blk.
 template <int F>
-__device__ __forceinline__ float fmt_weight(const uint8_t *__restrict__ blk, int k) {
+__device__ __forceinline__ float fmt_weight(const uint8_t *blk, int k) {
     if (F == kFmtQ6_K) {
         const int n = k >> 7, r = k & 127, i = r >> 5, l = r & 31;
-        const uint32_t lb = __ldg(blk + 64 * n + l + 32 * (i & 1));
+        const uint32_t lb = (*(blk + 64 * n + l + 32 * (i & 1)));
         const int lo = (int)((i < 2 ? lb : lb >> 4) & 15u);
-        const int hi = (int)((__ldg(blk + 128 + 32 * n + l) >> (2 * i)) & 3u);
-        const int sc = (int)(int8_t)__ldg(blk + 192 + (k >> 4));
+        const int hi = (int)(((*(blk + 128 + 32 * n + l)) >> (2 * i)) & 3u);
+        const int sc = (int)(int8_t)(*(blk + 192 + (k >> 4)));
         return fp16_at(blk + 208) * (float)(sc * ((lo | (hi << 4)) - 32));   // exact
     } else if (F == kFmtQ5_1) {
-        const uint32_t qs = __ldg(blk + 8 + (k & 15));
-        const uint32_t qh = __ldg(blk + 4 + (k >> 3));
+        const uint32_t qs = (*(blk + 8 + (k & 15)));
+        const uint32_t qh = (*(blk + 4 + (k >> 3)));
         const int q = (int)(((k < 16 ? qs : qs >> 4) & 15u) | (((qh >> (k & 7)) & 1u) << 4));
         return fmaf(fp16_at(blk), (float)q, fp16_at(blk + 2));               // d*q exact
     } else {
@@ -72,16 +74,16 @@ __device__ __forceinline__ float fmt_weight(const uint8_t *__restrict__ blk, int
         const uint8_t *sb = blk + 4;
         int sc, m;
         if (j < 4) {
-            sc = __ldg(sb + j) & 63;
-            m = __ldg(sb + j + 4) & 63;
+            sc = (*(sb + j)) & 63;
+            m = (*(sb + j + 4)) & 63;
         } else {
-            sc = (__ldg(sb + j + 4) & 15) | ((__ldg(sb + j - 4) >> 6) << 4);
-            m = (__ldg(sb + j + 4) >> 4) | ((__ldg(sb + j) >> 6) << 4);
+            sc = ((*(sb + j + 4)) & 15) | (((*(sb + j - 4)) >> 6) << 4);
+            m = ((*(sb + j + 4)) >> 4) | (((*(sb + j)) >> 6) << 4);
         }
         const uint8_t *qs = blk + (F == kFmtQ5_K ? 48 : 16);
-        const uint32_t b = __ldg(qs + 32 * (k >> 6) + (k & 31));
+        const uint32_t b = qs[32 * (k >> 6) + (k & 31)];
         int q = (int)(((k & 32) ? b >> 4 : b) & 15u);
-        if (F == kFmtQ5_K) q |= (int)((__ldg(blk + 16 + (k & 31)) >> j) & 1u) << 4;
+        if (F == kFmtQ5_K) q |= (int)(((*(blk + 16 + (k & 31))) >> j) & 1u) << 4;
         const float wq = (fp16_at(blk) * (float)sc) * (float)q;             // exact
         return wq - fp16_at(blk + 2) * (float)m;                             // one rounding
     }
@@ -118,23 +120,127 @@ cudaError_t launch_dequant_fmt(int f, const void *blocks, float *out, int64_t ro
 }
 
 constexpr int kDownWarps = 16;
+constexpr int kDownBuf = 4096;         // bytes of a warp's row-chunk buffer
 
-// Shared memory: h of every expert slot, fp32 [P][I].
+// 8 bytes at any shared-memory address p: three aligned words and two funnel
+// shifts (the buffer has slack after its last byte).
+__device__ __forceinline__ void load8(const uint8_t *p, uint32_t &lo, uint32_t &hi) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(a & ~(uintptr_t)3);
+    const uint32_t sh = (uint32_t)(a & 3) * 8;
+    const uint32_t w0 = w[0], w1 = w[1], w2 = w[2];
+    lo = __funnelshift_r(w0, w1, sh);
+    hi = __funnelshift_r(w1, w2, sh);
+}
+
+// Byte i (0..7) of the pair (lo, hi).
+__device__ __forceinline__ uint32_t byte8(uint32_t lo, uint32_t hi, int i) {
+    return ((i < 4 ? lo : hi) >> (8 * (i & 3))) & 0xFFu;
+}
+
+// Dot product of weights k0 .. k0+7 of a 256-weight unit (one block; Q5_1:
+// eight blocks) with v[0..7].  The eight weights share one scale, so the
+// header is decoded once; each value is the format's exact product (plus at
+// most one rounding of the offset), as in fmt_weight.
 template <int F>
-__global__ void __launch_bounds__(kDownWarps * 32) down_fmt_kernel(MatvecArgs a) {
+__device__ __forceinline__ float dot8(const uint8_t *unit, int k0, const float (&v)[8]) {
+    float r = 0.0f;
+    if (F == kFmtQ6_K) {
+        const int n = k0 >> 7, rr = k0 & 127, i = rr >> 5, l = rr & 31;
+        uint32_t l0, l1, h0, h1;
+        load8(unit + 64 * n + l + 32 * (i & 1), l0, l1);
+        load8(unit + 128 + 32 * n + l, h0, h1);
+        const int sc = (int)(int8_t)unit[192 + (k0 >> 4)];
+        const float d = fp16_at(unit + 208);
+        const int lsh = i < 2 ? 0 : 4, hsh = 2 * i;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const int q = (int)((byte8(l0, l1, t) >> lsh) & 15u) | (int)(((byte8(h0, h1, t) >> hsh) & 3u) << 4);
+            r = fmaf(d * (float)(sc * (q - 32)), v[t], r);
+        }
+    } else if (F == kFmtQ5_1) {
+        const uint8_t *blk = unit + (k0 >> 5) * 24;
+        const int j0 = k0 & 31;
+        const float d = fp16_at(blk), m = fp16_at(blk + 2);
+        uint32_t q0, q1;
+        load8(blk + 8 + (j0 & 15), q0, q1);
+        const uint32_t qh = (uint32_t)blk[4] | ((uint32_t)blk[5] << 8) | ((uint32_t)blk[6] << 16) |
+                            ((uint32_t)blk[7] << 24);
+        const int nsh = j0 < 16 ? 0 : 4;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const int q = (int)((byte8(q0, q1, t) >> nsh) & 15u) | (int)(((qh >> (j0 + t)) & 1u) << 4);
+            r = fmaf(fmaf(d, (float)q, m), v[t], r);
+        }
+    } else {
+        const int j = k0 >> 5;
+        const uint8_t *sb = unit + 4;
+        int sc, m;
+        if (j < 4) {
+            sc = sb[j] & 63;
+            m = sb[j + 4] & 63;
+        } else {
+            sc = (sb[j + 4] & 15) | ((sb[j - 4] >> 6) << 4);
+            m = (sb[j + 4] >> 4) | ((sb[j] >> 6) << 4);
+        }
+        const float ds = fp16_at(unit) * (float)sc;       // exact
+        const float dm = fp16_at(unit + 2) * (float)m;    // exact
+        uint32_t q0, q1;
+        load8(unit + (F == kFmtQ5_K ? 48 : 16) + 32 * (k0 >> 6) + (k0 & 31), q0, q1);
+        const int nsh = (k0 & 32) ? 4 : 0;
+        uint32_t b0 = 0, b1 = 0;
+        if (F == kFmtQ5_K) load8(unit + 16 + (k0 & 31), b0, b1);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            int q = (int)((byte8(q0, q1, t) >> nsh) & 15u);
+            if (F == kFmtQ5_K) q |= (int)((byte8(b0, b1, t) >> j) & 1u) << 4;
+            r = fmaf(fmaf(ds, (float)q, -dm), v[t], r);    // ds*q exact: one rounding
+        }
+    }
+    return r;
+}
+
+// Shared memory: h of every expert slot (fp32 [P][I]), then one row-chunk
+// buffer per warp.  A warp copies a chunk of whole 256-weight units of its row
+// into its buffer with 4-byte loads, all lanes at once (many loads in
+// flight), then lane t takes weights 8t .. 8t+7 of each unit.
+template <int F>
+__global__ void __launch_bounds__(kDownWarps * 32, 1) down_fmt_kernel(MatvecArgs a) {
     extern __shared__ __align__(16) float hs[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = a.H, I = a.I, P = a.k;
     const bool moe = a.ids != nullptr;
+    uint8_t *buf = reinterpret_cast<uint8_t *>(hs + (size_t)P * I) + (size_t)warp * (kDownBuf + 16);
     // the next work in the stream may be scheduled as this grid's blocks leave
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // h is written by the gate/up kernel: wait until that grid has completed
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (int i = threadIdx.x; i < P * I; i += blockDim.x) hs[i] = __ldcg(a.h + i);
+    {
+        // (loads first, then stores: a load is not held behind a store to a
+        // pointer the compiler cannot tell apart from it)
+        const float4 *h4 = reinterpret_cast<const float4 *>(a.h);
+        float4 *s4 = reinterpret_cast<float4 *>(hs);
+        const int n4 = P * I / 4;
+        for (int i0 = threadIdx.x; i0 < n4; i0 += 8 * blockDim.x) {
+            float4 r[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = i0 + j * blockDim.x;
+                r[j] = i < n4 ? __ldcg(h4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = i0 + j * blockDim.x;
+                if (i < n4) s4[i] = r[j];
+            }
+        }
+    }
     __syncthreads();
     const int64_t rb = fmt_row_bytes_hd(F, I);
-    const int bw = fmt_block_weights(F), bb = fmt_block_bytes(F);
-    const int groups = I / 32;
+    const int ub = (256 / fmt_block_weights(F)) * fmt_block_bytes(F);   // bytes of a unit
+    const int nu = (I + 255) / 256;
+    const int nuc = (kDownBuf - 4) / ub;                                 // units per chunk
+    const int k0 = 8 * lane;
     const int64_t gw = (int64_t)gridDim.x * kDownWarps;
     for (int64_t n = (int64_t)warp * gridDim.x + blockIdx.x; n < H; n += gw) {
         float acc = 0.0f;
@@ -145,11 +251,49 @@ __global__ void __launch_bounds__(kDownWarps * 32) down_fmt_kernel(MatvecArgs a)
             const uint8_t *row = a.Wd + ((int64_t)e * H + n) * rb;
             const float *hp = hs + (size_t)p * I;
             float part = 0.0f;
-#pragma unroll 4
-            for (int g = 0; g < groups; ++g) {
-                const int c = g * 32 + lane;
-                const float w = fmt_weight<F>(row + (c / bw) * bb, c % bw);
-                part = fmaf(w, hp[c], part);
+            for (int u0 = 0; u0 < nu; u0 += nuc) {
+                const int u1 = min(nu, u0 + nuc);
+                // bytes [src, end) of the row (the last unit may be cut short
+                // by the row's end), read as the 4-byte words from the word
+                // holding src up to end, plus the 0-3 tail bytes one by one
+                // (W_down is 4-byte aligned: no word starts before the matrix
+                // or ends after it)
+                const uint8_t *src = row + (size_t)u0 * ub;
+                const uint8_t *end = row + min((int64_t)u1 * ub, rb);
+                const uintptr_t a0 = reinterpret_cast<uintptr_t>(src) & ~(uintptr_t)3;
+                const size_t span = reinterpret_cast<uintptr_t>(end) - a0;
+                const int nwords = (int)(span / 4), tail = (int)(span % 4);
+                __syncwarp();
+                const uint32_t *w32 = reinterpret_cast<const uint32_t *>(a0);
+                uint32_t *b32 = reinterpret_cast<uint32_t *>(buf);
+                // all of a lane's loads are issued before any of its stores
+                // (at most 32 words each: kDownBuf / 128), so they are in
+                // flight together
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t r[kDownBuf / 256];
+#pragma unroll
+                    for (int j = 0; j < kDownBuf / 256; ++j) {
+                        const int i = lane + 32 * (half * (kDownBuf / 256) + j);
+                        r[j] = i < nwords ? __ldg(w32 + i) : 0u;
+                    }
+#pragma unroll
+                    for (int j = 0; j < kDownBuf / 256; ++j) {
+                        const int i = lane + 32 * (half * (kDownBuf / 256) + j);
+                        if (i < nwords) b32[i] = r[j];
+                    }
+                }
+                if (lane < tail) buf[4 * nwords + lane] = __ldg(reinterpret_cast<const uint8_t *>(a0) + 4 * nwords + lane);
+                __syncwarp();
+                const uint8_t *sb = buf + (reinterpret_cast<uintptr_t>(src) - a0);
+                for (int u = u0; u < u1; ++u) {
+                    const int c0 = u * 256 + k0;
+                    if (c0 >= I) continue;              // past the row (I % 256 != 0)
+                    const float4 va = *reinterpret_cast<const float4 *>(hp + c0);
+                    const float4 vb = *reinterpret_cast<const float4 *>(hp + c0 + 4);
+                    const float v[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+                    part += dot8<F>(sb + (size_t)(u - u0) * ub, k0, v);
+                }
             }
             acc = fmaf(wp, part, acc);
         }
@@ -159,7 +303,9 @@ __global__ void __launch_bounds__(kDownWarps * 32) down_fmt_kernel(MatvecArgs a)
     }
 }
 
-size_t down_fmt_smem_bytes(int I, int k) { return (size_t)k * I * sizeof(float); }
+size_t down_fmt_smem_bytes(int I, int k) {
+    return (size_t)k * I * sizeof(float) + (size_t)kDownWarps * (kDownBuf + 16);
+}
 
 cudaError_t launch_token_fmt(const MatvecArgs &a, int wd_fmt, cudaStream_t s) {
     if (a.T != 1 || !fmt_valid(wd_fmt) || wd_fmt == kFmtQ4_K || a.I % 64 != 0) return cudaErrorInvalidValue;
