@@ -16,11 +16,16 @@ independent), so the scaling is weak and `value` is the tokens of all ranks
 divided by the slowest rank's time.
 
 The JSON line carries: the device-timed throughput (`value`, tok/s) and
-TFLOP/s, the end-to-end throughput through the public API with host buffers
-(`e2e`), the roofline of the dominant kernel (the fused tensor-core kernel,
-timed alone through the residual entry point), the CPU oracle timed on this
-host's cores on a bounded sample (`cpu_baseline`), SM clocks sampled during
-the timed region, and the number of this library's kernels launched.
+TFLOP/s, the end-to-end throughput with host buffers through the library's
+host pipeline (`e2e`: each step's x uploaded from and y downloaded to pinned
+host memory, overlapped with the neighbouring steps' blocks, wall clock), the
+roofline of the dominant kernel (the fused tensor-core kernel, timed alone
+through the residual entry point), the CPU oracle timed on this host's cores
+on a bounded sample (`cpu_baseline`), SM clocks sampled during the timed
+region, and the number of this library's kernels launched.  Dense lines add
+the RMSNorm in front of the block (`rmsnorm`), routed lines the device router
+(`router`), single-token lines the block with W_down in the other block
+formats (`down_formats`), each timed on its own.
 
 --impl reference times the CPU oracle itself (the only reference this
 build has: the source pages publish no code) on the same workload and metric.
