@@ -78,3 +78,21 @@ def test_other_formats_reject_several_tokens():
     with pytest.raises(zffn.ZffnError) as e:
         zffn.swiglu_q4k_wd(x, *W, zffn.FMT_Q6_K, I)
     assert e.value.status == zffn.ERR_UNSUPPORTED
+
+
+def test_small_format_call_then_larger_q4k_single_token():
+    # the gate/up kernel is shared by both single-token paths: a format call at
+    # a small width must not leave it a shared-memory limit that a later, wider
+    # Q4_K call exceeds
+    rng = np.random.default_rng(302)
+    H, I = 256, 256
+    small = [dev(synth.random_q4k_blocks(rng, I, H, 1e-2)), dev(synth.random_q4k_blocks(rng, I, H, 1e-2)),
+             dev(synth.random_blocks(rng, zffn.FMT_Q5_K, H, I, 1e-2))]
+    zffn.swiglu_q4k_wd(x_dev(token(rng, H)), *small, zffn.FMT_Q5_K, I)
+    H, I = 8192, 1024
+    W = [synth.random_q4k_blocks(rng, I, H, 1e-2), synth.random_q4k_blocks(rng, I, H, 1e-2),
+         synth.random_q4k_blocks(rng, H, I, 1e-2)]
+    x = token(rng, H)
+    y = zffn.swiglu_q4k(x_dev(x), *[dev(a) for a in W], I)
+    assert zffn.get_device_error() == zffn.OK
+    assert_close(y, orc.swiglu_ffn(x, *W, 1, H, I), "Q4_K single token after a format call")
