@@ -86,6 +86,21 @@ def algorithmic(kind, T, H, I, E, k):
     return flop, wbytes + T * H * 2 + T * H * 4
 
 
+def max_over_ranks(values, dist, device):
+    """Each value's maximum over the ranks: the slowest replica's times."""
+    import torch
+    t = torch.tensor(list(values), device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_rates(tokens_per_rank, flop_per_rank, world, ms):
+    """Whole-job tokens/s and TFLOP/s of `world` replicas, each doing the same
+    work, timed by the slowest (ms per step)."""
+    return (tokens_per_rank * world / (ms * 1e-3),
+            flop_per_rank * world / (ms * 1e-3) / 1e12)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -478,18 +493,14 @@ def run_gpu(args):
                   "frac_of_hbm_peak": round(r_bytes / (r_ms * 1e-3) / 1e9 / peaks["hbm"], 5)}
 
     if world > 1:
-        t = torch.tensor([ms, kms, e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, kms, e2e_ms = (float(v) for v in t.tolist())
+        ms, kms, e2e_ms = max_over_ranks([ms, kms, e2e_ms], dist, dev)
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
 
-    tok = T * world
-    value = tok / (ms * 1e-3)
-    tflops = flop / (ms * 1e-3) / 1e12
+    value, tflops = job_rates(T, flop, world, ms)
     # prefill is a dense contraction; decode and the routed layer stream weights
     bound = "tensor" if name.startswith("prefill") else "hbm"
     if bound == "tensor":
