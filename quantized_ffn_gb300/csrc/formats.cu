@@ -25,13 +25,14 @@
 //   down_fmt_kernel<F>: y[n] = sum_p w_p * Wd_{e_p}[n] . h[p] for one token,
 //     launched as a programmatic dependent of the Q4_K gate/up kernel of the
 //     single-token path, which leaves h (fp32 [P][I]) in the workspace.  One
-//     warp per output row at a time: the warp copies the row, a chunk of
-//     whole 256-weight units at a time, into its shared-memory buffer (4-byte
-//     loads by all lanes, so that many are in flight), then lane t takes the
-//     eight weights 8t .. 8t+7 of each unit, which share one scale (decoded
-//     once), and multiplies them by h, staged in shared memory; the row's sum
-//     is one warp reduction.  The rows of the grid are interleaved so that
-//     all warps stream the matrix together.
+//     warp per output row at a time: the warp streams the row, a chunk of
+//     whole 256-weight units at a time, through a shared-memory buffer; the
+//     next chunk's words are loaded into registers (4-byte loads by all
+//     lanes, all in flight) while the current chunk is computed.  Lane t
+//     takes the eight weights 8t .. 8t+7 of each unit, which share one scale
+//     (decoded once), and multiplies them by h, staged in shared memory; a
+//     row's sum is one warp reduction.  The rows of the grid are interleaved
+//     so that all warps stream the matrix together.
 #include "formats.h"
 
 #include "zffn_internal.cuh"
@@ -201,9 +202,18 @@ __device__ __forceinline__ float dot8(const uint8_t *unit, int k0, const float (
 }
 
 // Shared memory: h of every expert slot (fp32 [P][I]), then one row-chunk
-// buffer per warp.  A warp copies a chunk of whole 256-weight units of its row
-// into its buffer with 4-byte loads, all lanes at once (many loads in
-// flight), then lane t takes weights 8t .. 8t+7 of each unit.
+// buffer per warp.  A warp walks one stream of chunks: for each of its output
+// rows, for each valid expert slot, the row's whole 256-weight units a chunk
+// at a time.  The words of the next chunk are loaded into registers (all of a
+// lane's loads in flight) while the current chunk, already in the buffer, is
+// computed: lane t takes weights 8t .. 8t+7 of each unit.
+struct ChunkCursor {
+    int64_t n;   // output row
+    int p;       // expert slot
+    int u0;      // first unit of the chunk
+    bool done;
+};
+
 template <int F>
 __global__ void __launch_bounds__(kDownWarps * 32, 1) down_fmt_kernel(MatvecArgs a) {
     extern __shared__ __align__(16) float hs[];
@@ -242,64 +252,105 @@ __global__ void __launch_bounds__(kDownWarps * 32, 1) down_fmt_kernel(MatvecArgs
     const int nuc = (kDownBuf - 4) / ub;                                 // units per chunk
     const int k0 = 8 * lane;
     const int64_t gw = (int64_t)gridDim.x * kDownWarps;
-    for (int64_t n = (int64_t)warp * gridDim.x + blockIdx.x; n < H; n += gw) {
-        float acc = 0.0f;
-        for (int p = 0; p < P; ++p) {
-            const int e = moe ? a.ids[p] : 0;
-            if (e < 0 || e >= a.E) continue;
-            const float wp = moe ? a.wts[p] : 1.0f;
-            const uint8_t *row = a.Wd + ((int64_t)e * H + n) * rb;
-            const float *hp = hs + (size_t)p * I;
-            float part = 0.0f;
-            for (int u0 = 0; u0 < nu; u0 += nuc) {
-                const int u1 = min(nu, u0 + nuc);
-                // bytes [src, end) of the row (the last unit may be cut short
-                // by the row's end), read as the 4-byte words from the word
-                // holding src up to end, plus the 0-3 tail bytes one by one
-                // (W_down is 4-byte aligned: no word starts before the matrix
-                // or ends after it)
-                const uint8_t *src = row + (size_t)u0 * ub;
-                const uint8_t *end = row + min((int64_t)u1 * ub, rb);
-                const uintptr_t a0 = reinterpret_cast<uintptr_t>(src) & ~(uintptr_t)3;
-                const size_t span = reinterpret_cast<uintptr_t>(end) - a0;
-                const int nwords = (int)(span / 4), tail = (int)(span % 4);
-                __syncwarp();
-                const uint32_t *w32 = reinterpret_cast<const uint32_t *>(a0);
-                uint32_t *b32 = reinterpret_cast<uint32_t *>(buf);
-                // all of a lane's loads are issued before any of its stores
-                // (at most 32 words each: kDownBuf / 128), so they are in
-                // flight together
+    const int64_t n_first = (int64_t)warp * gridDim.x + blockIdx.x;
+    auto slot_valid = [&](int p) {
+        const int e = moe ? a.ids[p] : 0;
+        return e >= 0 && e < a.E;
+    };
+    auto next_slot = [&](int p) {            // first valid slot >= p (P if none)
+        while (p < P && !slot_valid(p)) ++p;
+        return p;
+    };
+    const int p_first = next_slot(0);
+    if (p_first >= P) {
+        // no valid expert slot: every output of this warp is zero
+        for (int64_t n = n_first; n < H; n += gw)
+            if (lane == 0 && !a.accumulate) a.y[n] = 0.0f;
+        return;
+    }
+    auto advance = [&](ChunkCursor &c) {
+        c.u0 += nuc;
+        if (c.u0 < nu) return;
+        c.u0 = 0;
+        c.p = next_slot(c.p + 1);
+        if (c.p < P) return;
+        c.p = p_first;
+        c.n += gw;
+        c.done = c.n >= H;
+    };
+    // The bytes of chunk c: [src, end) of its row (the last unit may be cut
+    // short by the row's end), read as the 4-byte words from the word holding
+    // src up to end, plus the 0-3 tail bytes (W_down is 4-byte aligned: no
+    // word starts before the matrix or ends after it).  At most kDownBuf / 128
+    // words per lane.
+    constexpr int kWords = kDownBuf / 128;
+    uint32_t r[kWords];
+    uint32_t rt = 0;
+    auto chunk_src = [&](const ChunkCursor &c) {
+        const int e = moe ? a.ids[c.p] : 0;
+        return a.Wd + ((int64_t)e * H + c.n) * rb + (size_t)c.u0 * ub;
+    };
+    auto chunk_end = [&](const ChunkCursor &c) {
+        const int e = moe ? a.ids[c.p] : 0;
+        return a.Wd + ((int64_t)e * H + c.n) * rb + min((int64_t)min(nu, c.u0 + nuc) * ub, rb);
+    };
+    auto issue = [&](const ChunkCursor &c) {
+        const uint8_t *src = chunk_src(c);
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(src) & ~(uintptr_t)3;
+        const size_t span = reinterpret_cast<uintptr_t>(chunk_end(c)) - a0;
+        const int nwords = (int)(span / 4), tail = (int)(span % 4);
+        const uint32_t *w32 = reinterpret_cast<const uint32_t *>(a0);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t r[kDownBuf / 256];
-#pragma unroll
-                    for (int j = 0; j < kDownBuf / 256; ++j) {
-                        const int i = lane + 32 * (half * (kDownBuf / 256) + j);
-                        r[j] = i < nwords ? __ldg(w32 + i) : 0u;
-                    }
-#pragma unroll
-                    for (int j = 0; j < kDownBuf / 256; ++j) {
-                        const int i = lane + 32 * (half * (kDownBuf / 256) + j);
-                        if (i < nwords) b32[i] = r[j];
-                    }
-                }
-                if (lane < tail) buf[4 * nwords + lane] = __ldg(reinterpret_cast<const uint8_t *>(a0) + 4 * nwords + lane);
-                __syncwarp();
-                const uint8_t *sb = buf + (reinterpret_cast<uintptr_t>(src) - a0);
-                for (int u = u0; u < u1; ++u) {
-                    const int c0 = u * 256 + k0;
-                    if (c0 >= I) continue;              // past the row (I % 256 != 0)
-                    const float4 va = *reinterpret_cast<const float4 *>(hp + c0);
-                    const float4 vb = *reinterpret_cast<const float4 *>(hp + c0 + 4);
-                    const float v[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-                    part += dot8<F>(sb + (size_t)(u - u0) * ub, k0, v);
-                }
-            }
-            acc = fmaf(wp, part, acc);
+        for (int j = 0; j < kWords; ++j) {
+            const int i = lane + 32 * j;
+            r[j] = i < nwords ? __ldg(w32 + i) : 0u;
         }
+        rt = lane < tail ? (uint32_t)__ldg(reinterpret_cast<const uint8_t *>(a0) + 4 * nwords + lane) : 0u;
+    };
+    ChunkCursor cur{n_first, p_first, 0, n_first >= H};
+    if (!cur.done) issue(cur);
+    float acc = 0.0f, part = 0.0f;
+    while (!cur.done) {
+        // the current chunk's words, loaded during the previous chunk's
+        // compute, go to the buffer (after every lane finished reading it)
+        const uint8_t *src = chunk_src(cur);
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(src) & ~(uintptr_t)3;
+        const size_t span = reinterpret_cast<uintptr_t>(chunk_end(cur)) - a0;
+        const int nwords = (int)(span / 4), tail = (int)(span % 4);
+        __syncwarp();
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) a.y[n] = a.accumulate ? a.y[n] + acc : acc;
+        for (int j = 0; j < kWords; ++j) {
+            const int i = lane + 32 * j;
+            if (i < nwords) reinterpret_cast<uint32_t *>(buf)[i] = r[j];
+        }
+        if (lane < tail) buf[4 * nwords + lane] = (uint8_t)rt;
+        __syncwarp();
+        // the next chunk's loads go out before this chunk is computed
+        ChunkCursor nx = cur;
+        advance(nx);
+        if (!nx.done) issue(nx);
+        const uint8_t *sb = buf + (reinterpret_cast<uintptr_t>(src) - a0);
+        const float *hp = hs + (size_t)cur.p * I;
+        const int u1 = min(nu, cur.u0 + nuc);
+        for (int u = cur.u0; u < u1; ++u) {
+            const int c0 = u * 256 + k0;
+            if (c0 >= I) continue;                  // past the row (I % 256 != 0)
+            const float4 va = *reinterpret_cast<const float4 *>(hp + c0);
+            const float4 vb = *reinterpret_cast<const float4 *>(hp + c0 + 4);
+            const float v[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+            part += dot8<F>(sb + (size_t)(u - cur.u0) * ub, k0, v);
+        }
+        if (u1 >= nu) {                             // last chunk of this slot's row
+            acc = fmaf(moe ? a.wts[cur.p] : 1.0f, part, acc);
+            part = 0.0f;
+            if (nx.done || nx.n != cur.n) {         // last slot of this output row
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                if (lane == 0) a.y[cur.n] = a.accumulate ? a.y[cur.n] + acc : acc;
+                acc = 0.0f;
+            }
+        }
+        cur = nx;
     }
 }
 
