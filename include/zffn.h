@@ -22,11 +22,13 @@
  * column C in a row's last block are ignored.
  *
  * Conventions for every entry point:
- *   - Pointers named x, y, W*, blocks, out, expert_* are DEVICE pointers owned
- *     by the caller; the library never frees or retains them.
+ *   - Pointers named x, y, h, gamma, logits, W*, blocks, out, expert_* are
+ *     DEVICE pointers owned by the caller; the library never frees or retains
+ *     them.  Pointers named *_host are host memory (the host pipeline only).
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
  *     call is asynchronous and stream-ordered; none synchronises the host
- *     except zffn_get_device_error, and none reads device data on the host.
+ *     except zffn_get_device_error and the host pipeline's sync and destroy,
+ *     and none reads device data on the host.
  *   - Argument checks run on the host before anything is launched; a failed
  *     check returns ZFFN_ERR_INVALID_ARG (or ZFFN_ERR_UNSUPPORTED) and launches
  *     nothing.  A failed launch returns ZFFN_ERR_CUDA.
