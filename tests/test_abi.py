@@ -156,3 +156,38 @@ def test_format_row_bytes_and_rejections(lib):
                                     None) == zffn.ERR_UNSUPPORTED
     assert L.zffn_moe_swiglu_q4k_wd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 1, 256, 256, 0, 2,
                                     None) == zffn.ERR_INVALID_ARG
+
+
+def declared_signatures():
+    """{name: (return type, parameter count)} from include/zffn.h."""
+    with open(os.path.join(ROOT, "include", "zffn.h")) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    sigs = {}
+    for m in re.finditer(r"([A-Za-z_][\w\s\*]*?)\b(zffn_\w+)\s*\(([^)]*)\)\s*;", text):
+        ret, name, params = m.group(1).strip(), m.group(2), m.group(3).strip()
+        n = 0 if params in ("", "void") else len(params.split(","))
+        sigs[name] = (ret, n)
+    return sigs
+
+
+def test_binding_signatures_match_the_header(lib):
+    # every function the binding types must have the header's arity and
+    # return type class
+    sigs = declared_signatures()
+    assert "zffn_swiglu_q4k" in sigs and sigs["zffn_swiglu_q4k"][1] == 9
+    checked = 0
+    for name, (ret, n) in sigs.items():
+        f = getattr(lib, name)
+        if f.argtypes is None:
+            continue                     # called through ctypes directly by its test
+        checked += 1
+        assert len(f.argtypes) == n, (name, len(f.argtypes), n)
+        if ret.startswith("zffn_status") or ret == "int":
+            assert f.restype is ctypes.c_int, name
+        elif ret.startswith("size_t"):
+            assert f.restype is ctypes.c_size_t, name
+        elif ret.startswith("void"):
+            assert f.restype is None, name
+        elif "char" in ret:
+            assert f.restype is ctypes.c_char_p, name
+    assert checked >= 25
