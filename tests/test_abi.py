@@ -191,3 +191,21 @@ def test_binding_signatures_match_the_header(lib):
         elif "char" in ret:
             assert f.restype is ctypes.c_char_p, name
     assert checked >= 25
+
+
+def test_header_compiles_as_plain_c(tmp_path):
+    # the boundary is a C ABI: the header must compile as C99 without warnings
+    src = tmp_path / "use.c"
+    src.write_text(
+        '#include "zffn.h"\n'
+        "int use(const void *x, const void *w, float *y, void *s) {\n"
+        "    zffn_pipeline *p = 0;\n"
+        "    size_t rb = zffn_q4k_row_bytes(4096) + zffn_row_bytes_fmt(ZFFN_FMT_Q6_K, 11008);\n"
+        "    zffn_status st = zffn_swiglu_q4k(x, w, w, w, y, 1, 4096, 11008, s);\n"
+        "    if (zffn_pipeline_create(&p, 1, 4096, 11008, 2) == ZFFN_OK) zffn_pipeline_destroy(p);\n"
+        "    return (int)st + (int)rb + (zffn_status_string(st) != 0);\n"
+        "}\n")
+    import subprocess
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                           "-I", os.path.join(ROOT, "include"), "-c", str(src), "-o",
+                           str(tmp_path / "use.o")])
