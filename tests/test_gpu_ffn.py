@@ -48,7 +48,7 @@ def test_tiny_config_single_token_path():
         assert_close(y, ref, f"tiny/matvec row {r}")
 
 
-@pytest.mark.parametrize("T", [1, 2, 63, 127, 128, 129, 255, 257, 300])
+@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 127, 128, 129, 255, 257, 300])
 def test_tile_boundaries_tokens(T):
     H, I = 512, 704
     x, Wg, Wu, Wd = random_layer(T, T, H, I)

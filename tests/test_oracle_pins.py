@@ -406,6 +406,9 @@ def test_intermediate_byte_model_matches_pages():
     assert round(I / H, 1) == g["width_ratio"]
     # 4.5 bits per weight for Q4_K (144 bytes per 256 weights)
     assert 144 * 8 / 256 == g["q4k_bits_per_weight"]
+    # staged dequant moves 4.5 + 16 + 16 bits per weight, the fused path 4.5
+    staged = g["q4k_bits_per_weight"] + 16 + 16
+    assert round(staged / g["q4k_bits_per_weight"]) == g["weight_traffic_cut"]
 
 
 # ---- router: top-k ids and softmax weights ------------------------------------
