@@ -303,8 +303,15 @@ zffn_status zffn_reserve(int T_max, int H_max, int I_max, int E_max, int top_k_m
  * the caller makes sure no call is still running. */
 void zffn_release(void);
 
-/* Description of the last CUDA failure seen by a call on this host thread
- * (static string, never NULL; "no error" if none). */
+/* Bytes of workspace the library currently holds on the current device (0 if
+ * none has been allocated, or after zffn_release).  Host-side query; launches
+ * nothing and allocates nothing. */
+size_t zffn_workspace_bytes(void);
+
+/* Description of the last failure a call on this host thread reported: the
+ * CUDA error behind a ZFFN_ERR_CUDA, or the failed check behind a
+ * ZFFN_ERR_INVALID_ARG.  A successful call leaves it unchanged.  Static
+ * string, never NULL; "no error" before the first failure. */
 const char *zffn_last_error(void);
 
 /* Synchronise `stream`, then return and clear the current device's error word:

@@ -89,13 +89,21 @@ zffn_status ensure_workspace(size_t bytes, Workspace **out) {
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-zffn_status check_shape(int T, int H, int I) {
-    if (T < 1 || H < 256 || H > 16384 || H % 256 != 0 || I < 64 || I > 65536 || I % 64 != 0)
-        return ZFFN_ERR_INVALID_ARG;
-    return ZFFN_OK;
+thread_local const char *t_last_error = "no error";
+
+// A failed host-side check: record why (zffn_last_error) and return INVALID_ARG.
+zffn_status invalid(const char *why) {
+    t_last_error = why;
+    return ZFFN_ERR_INVALID_ARG;
 }
 
-thread_local const char *t_last_error = "no error";
+zffn_status check_shape(int T, int H, int I) {
+    if (T < 1) return invalid("T must be at least 1");
+    if (H < 256 || H > 16384 || H % 256 != 0)
+        return invalid("H must be a multiple of 256 in [256, 16384]");
+    if (I < 64 || I > 65536 || I % 64 != 0) return invalid("I must be a multiple of 64 in [64, 65536]");
+    return ZFFN_OK;
+}
 
 zffn_status to_status(cudaError_t e) {
     if (e == cudaSuccess) return ZFFN_OK;
@@ -107,6 +115,37 @@ zffn_status to_status(cudaError_t e) {
 }  // namespace
 
 void set_last_error(const char *what) { t_last_error = what; }
+
+namespace {
+struct SmemAttr {
+    const void *fn;
+    int device;
+    size_t bytes;
+};
+std::mutex g_attr_mu;
+SmemAttr g_attr[256];
+int g_attr_n = 0;
+}  // namespace
+
+cudaError_t ensure_dynamic_smem(const void *fn, size_t bytes) {
+    const int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    SmemAttr *rec = nullptr;
+    for (int i = 0; i < g_attr_n; ++i)
+        if (g_attr[i].fn == fn && g_attr[i].device == dev) rec = &g_attr[i];
+    if (rec && rec->bytes >= bytes) return cudaSuccess;
+    if (!rec && g_attr_n == (int)(sizeof(g_attr) / sizeof(g_attr[0]))) return cudaErrorMemoryAllocation;
+    const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    if (!rec) {
+        rec = &g_attr[g_attr_n++];
+        rec->fn = fn;
+        rec->device = dev;
+    }
+    rec->bytes = bytes;
+    return cudaSuccess;
+}
 
 const DeviceInfo &device_info() {
     const int dev = current_device();
@@ -151,14 +190,16 @@ size_t zffn_q4k_row_bytes(int64_t cols) {
 
 zffn_status zffn_q4k_dequant(const void *blocks, float *out, int64_t rows, int64_t cols,
                              void *stream) {
-    if (!blocks || !out || rows <= 0 || cols <= 0) return ZFFN_ERR_INVALID_ARG;
+    if (!blocks || !out) return invalid("a pointer argument is NULL");
+    if (rows <= 0 || cols <= 0) return invalid("rows and cols must be positive");
     if (device_info().device < 0) return ZFFN_ERR_CUDA;
     return to_status(launch_q4k_dequant(blocks, out, rows, cols, (cudaStream_t)stream));
 }
 
 zffn_status zffn_q4k_quantize(const float *w, void *blocks, int64_t rows, int64_t cols,
                               void *stream) {
-    if (!w || !blocks || rows <= 0 || cols <= 0) return ZFFN_ERR_INVALID_ARG;
+    if (!w || !blocks) return invalid("a pointer argument is NULL");
+    if (rows <= 0 || cols <= 0) return invalid("rows and cols must be positive");
     if (device_info().device < 0) return ZFFN_ERR_CUDA;
     return to_status(launch_q4k_quantize(w, blocks, rows, cols, (cudaStream_t)stream));
 }
@@ -169,10 +210,10 @@ namespace {
 
 zffn_status swiglu_dense(const void *x, const void *Wg, const void *Wu, const void *Wd, float *y,
                          int T, int H, int I, void *stream, bool accumulate) {
-    if (!x || !Wg || !Wu || !Wd || !y) return ZFFN_ERR_INVALID_ARG;
+    if (!x || !Wg || !Wu || !Wd || !y) return invalid("a pointer argument is NULL");
     if (check_shape(T, H, I) != ZFFN_OK) return ZFFN_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd) || !aligned16(y))
-        return ZFFN_ERR_INVALID_ARG;
+        return invalid("x, Wg, Wu, Wd and y must be 16-byte aligned");
     const DeviceInfo &di = device_info();
     if (di.device < 0) return ZFFN_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
@@ -226,14 +267,15 @@ zffn_status swiglu_moe(const void *x, const int32_t *expert_ids, const float *ex
                        const void *Wg, const void *Wu, const void *Wd, float *y, int T, int H,
                        int I, int E, int top_k, void *stream, bool accumulate) {
     if (!x || !expert_ids || !expert_weights || !Wg || !Wu || !Wd || !y)
-        return ZFFN_ERR_INVALID_ARG;
+        return invalid("a pointer argument is NULL");
     if (check_shape(T, H, I) != ZFFN_OK) return ZFFN_ERR_INVALID_ARG;
-    if (E < 1 || E > 4096 || top_k < 1 || top_k > 64) return ZFFN_ERR_INVALID_ARG;
-    if ((int64_t)T * top_k > (1 << 24)) return ZFFN_ERR_INVALID_ARG;
+    if (E < 1 || E > 4096 || top_k < 1 || top_k > 64)
+        return invalid("E must be in [1, 4096] and top_k in [1, 64]");
+    if ((int64_t)T * top_k > (1 << 24)) return invalid("T * top_k must not exceed 2^24");
     if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd) || !aligned16(y) ||
         (reinterpret_cast<uintptr_t>(expert_ids) & 3) ||
         (reinterpret_cast<uintptr_t>(expert_weights) & 3))
-        return ZFFN_ERR_INVALID_ARG;
+        return invalid("x, Wg, Wu, Wd, y must be 16-byte and expert_ids, expert_weights 4-byte aligned");
     const DeviceInfo &di = device_info();
     if (di.device < 0) return ZFFN_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
@@ -336,7 +378,9 @@ size_t zffn_row_bytes_fmt(int fmt, int64_t cols) {
 
 zffn_status zffn_dequant_fmt(int fmt, const void *blocks, float *out, int64_t rows, int64_t cols,
                              void *stream) {
-    if (!fmt_valid(fmt) || !blocks || !out || rows <= 0 || cols <= 0) return ZFFN_ERR_INVALID_ARG;
+    if (!fmt_valid(fmt)) return invalid("unknown block format");
+    if (!blocks || !out) return invalid("a pointer argument is NULL");
+    if (rows <= 0 || cols <= 0) return invalid("rows and cols must be positive");
     if (device_info().device < 0) return ZFFN_ERR_CUDA;
     return to_status(launch_dequant_fmt(fmt, blocks, out, rows, cols, (cudaStream_t)stream));
 }
@@ -345,20 +389,22 @@ zffn_status zffn_moe_swiglu_q4k_wd(const void *x, const int32_t *expert_ids,
                                    const float *expert_weights, const void *Wg, const void *Wu,
                                    const void *Wd, int wd_fmt, float *y, int T, int H, int I, int E,
                                    int top_k, void *stream) {
-    if (!fmt_valid(wd_fmt)) return ZFFN_ERR_INVALID_ARG;
+    if (!fmt_valid(wd_fmt)) return invalid("unknown block format of W_down");
     if (wd_fmt == kFmtQ4_K)
         return expert_ids ? swiglu_moe(x, expert_ids, expert_weights, Wg, Wu, Wd, y, T, H, I, E,
                                        top_k, stream, false)
                           : swiglu_dense(x, Wg, Wu, Wd, y, T, H, I, stream, false);
     const bool moe = expert_ids != nullptr;
-    if (!x || !Wg || !Wu || !Wd || !y || (moe && !expert_weights)) return ZFFN_ERR_INVALID_ARG;
+    if (!x || !Wg || !Wu || !Wd || !y || (moe && !expert_weights))
+        return invalid("a pointer argument is NULL");
     if (check_shape(T, H, I) != ZFFN_OK) return ZFFN_ERR_INVALID_ARG;
-    if (moe && (E < 1 || E > 4096 || top_k < 1 || top_k > 64)) return ZFFN_ERR_INVALID_ARG;
+    if (moe && (E < 1 || E > 4096 || top_k < 1 || top_k > 64))
+        return invalid("E must be in [1, 4096] and top_k in [1, 64]");
     if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wu) || (reinterpret_cast<uintptr_t>(Wd) & 3) ||
         (reinterpret_cast<uintptr_t>(y) & 3) ||
         (moe && ((reinterpret_cast<uintptr_t>(expert_ids) & 3) ||
                  (reinterpret_cast<uintptr_t>(expert_weights) & 3))))
-        return ZFFN_ERR_INVALID_ARG;
+        return invalid("x, Wg, Wu must be 16-byte and Wd, y, expert_ids, expert_weights 4-byte aligned");
     if (T != 1) return ZFFN_ERR_UNSUPPORTED;       // other formats: single-token paths only
     const int k = moe ? top_k : 1;
     const DeviceInfo &di = device_info();
@@ -392,10 +438,12 @@ zffn_status zffn_swiglu_q4k_wd(const void *x, const void *Wg, const void *Wu, co
 
 zffn_status zffn_rmsnorm_bf16(const float *h, const float *gamma, float eps, void *x, int T, int H,
                               void *stream) {
-    if (!h || !gamma || !x) return ZFFN_ERR_INVALID_ARG;
-    if (T < 1 || H < 256 || H > 16384 || H % 256 != 0) return ZFFN_ERR_INVALID_ARG;
-    if (!(eps >= 0.0f) || eps > 1.0f) return ZFFN_ERR_INVALID_ARG;
-    if (!aligned16(h) || !aligned16(gamma) || !aligned16(x)) return ZFFN_ERR_INVALID_ARG;
+    if (!h || !gamma || !x) return invalid("a pointer argument is NULL");
+    if (T < 1) return invalid("T must be at least 1");
+    if (H < 256 || H > 16384 || H % 256 != 0) return invalid("H must be a multiple of 256 in [256, 16384]");
+    if (!(eps >= 0.0f) || eps > 1.0f) return invalid("eps must be in [0, 1]");
+    if (!aligned16(h) || !aligned16(gamma) || !aligned16(x))
+        return invalid("h, gamma and x must be 16-byte aligned");
     if (device_info().device < 0) return ZFFN_ERR_CUDA;
     return to_status(launch_rmsnorm_bf16(h, gamma, eps, static_cast<__nv_bfloat16 *>(x), T, H,
                                          (cudaStream_t)stream));
@@ -404,11 +452,11 @@ zffn_status zffn_rmsnorm_bf16(const float *h, const float *gamma, float eps, voi
 zffn_status zffn_swiglu_q4k_prenorm_residual(float *h, const float *gamma, float eps, const void *Wg,
                                              const void *Wu, const void *Wd, int T, int H, int I,
                                              void *stream) {
-    if (!h || !gamma || !Wg || !Wu || !Wd) return ZFFN_ERR_INVALID_ARG;
+    if (!h || !gamma || !Wg || !Wu || !Wd) return invalid("a pointer argument is NULL");
     if (check_shape(T, H, I) != ZFFN_OK) return ZFFN_ERR_INVALID_ARG;
-    if (!(eps >= 0.0f) || eps > 1.0f) return ZFFN_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f) || eps > 1.0f) return invalid("eps must be in [0, 1]");
     if (!aligned16(h) || !aligned16(gamma) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd))
-        return ZFFN_ERR_INVALID_ARG;
+        return invalid("h, gamma, Wg, Wu and Wd must be 16-byte aligned");
     if (device_info().device < 0) return ZFFN_ERR_CUDA;
     // the whole layout is reserved here, so that the block's own workspace
     // request below finds it large enough and never moves it
@@ -424,12 +472,14 @@ zffn_status zffn_swiglu_q4k_prenorm_residual(float *h, const float *gamma, float
 
 zffn_status zffn_moe_router_topk(const float *logits, int32_t *expert_ids, float *expert_weights,
                                  int T, int E, int top_k, void *stream) {
-    if (!logits || !expert_ids || !expert_weights) return ZFFN_ERR_INVALID_ARG;
-    if (T < 1 || E < 1 || E > 4096 || top_k < 1 || top_k > 64 || top_k > E) return ZFFN_ERR_INVALID_ARG;
-    if ((int64_t)T * E > ((int64_t)1 << 31) || (int64_t)T * top_k > (1 << 24)) return ZFFN_ERR_INVALID_ARG;
+    if (!logits || !expert_ids || !expert_weights) return invalid("a pointer argument is NULL");
+    if (T < 1 || E < 1 || E > 4096 || top_k < 1 || top_k > 64 || top_k > E)
+        return invalid("T >= 1, E in [1, 4096] and top_k in [1, min(E, 64)] are required");
+    if ((int64_t)T * E > ((int64_t)1 << 31) || (int64_t)T * top_k > (1 << 24))
+        return invalid("T * E must not exceed 2^31 nor T * top_k 2^24");
     if ((reinterpret_cast<uintptr_t>(logits) & 3) || (reinterpret_cast<uintptr_t>(expert_ids) & 3) ||
         (reinterpret_cast<uintptr_t>(expert_weights) & 3))
-        return ZFFN_ERR_INVALID_ARG;
+        return invalid("logits, expert_ids and expert_weights must be 4-byte aligned");
     if (device_info().device < 0) return ZFFN_ERR_CUDA;
     return to_status(launch_moe_router(logits, T, E, top_k, expert_ids, expert_weights,
                                        (cudaStream_t)stream));
@@ -437,11 +487,18 @@ zffn_status zffn_moe_router_topk(const float *logits, int32_t *expert_ids, float
 
 zffn_status zffn_reserve(int T_max, int H_max, int I_max, int E_max, int top_k_max) {
     if (T_max < 1 || H_max < 1 || I_max < 1 || E_max < 1 || top_k_max < 1)
-        return ZFFN_ERR_INVALID_ARG;
+        return invalid("every size must be at least 1");
     if (device_info().device < 0) return ZFFN_ERR_CUDA;
     const Layout L = layout_for(T_max, H_max, I_max, E_max, top_k_max);
     Workspace *w = nullptr;
     return ensure_workspace(L.total, &w);
+}
+
+size_t zffn_workspace_bytes(void) {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return 0;
+    std::lock_guard<std::mutex> lk(g_mu);
+    return g_ws[dev].bytes;
 }
 
 void zffn_release(void) {
@@ -483,7 +540,7 @@ int zffn_set_option(int key, int value) {
 }
 
 zffn_status zffn_selftest_wait_timeout(int64_t budget_cycles, void *stream) {
-    if (budget_cycles < 1) return ZFFN_ERR_INVALID_ARG;
+    if (budget_cycles < 1) return invalid("budget_cycles must be at least 1");
     const DeviceInfo &di = device_info();
     if (di.device < 0) return ZFFN_ERR_CUDA;
     return to_status(launch_wait_timeout_selftest(budget_cycles, di.err_word, (cudaStream_t)stream));
@@ -537,10 +594,10 @@ void pipeline_free(zffn_pipeline *p) {
 extern "C" {
 
 zffn_status zffn_pipeline_create(zffn_pipeline **out, int T, int H, int I, int depth) {
-    if (!out) return ZFFN_ERR_INVALID_ARG;
+    if (!out) return invalid("out is NULL");
     *out = nullptr;
     if (check_shape(T, H, I) != ZFFN_OK) return ZFFN_ERR_INVALID_ARG;
-    if (depth < 2 || depth > ZFFN_PIPELINE_MAX_DEPTH) return ZFFN_ERR_INVALID_ARG;
+    if (depth < 2 || depth > ZFFN_PIPELINE_MAX_DEPTH) return invalid("depth must be in [2, 4]");
     const DeviceInfo &di = device_info();
     if (di.device < 0) return ZFFN_ERR_CUDA;
     zffn_pipeline *p = new zffn_pipeline;
@@ -573,7 +630,7 @@ namespace {
 // One submission: upload, the block (`block(x_dev, y_dev, stream)`), download.
 template <typename Block>
 zffn_status pipeline_submit(zffn_pipeline *p, const void *x_host, float *y_host, Block block) {
-    if (current_device() != p->device) return ZFFN_ERR_INVALID_ARG;
+    if (current_device() != p->device) return invalid("the pipeline belongs to another device");
     const int slot = (int)(p->n % p->depth);
     const size_t xb = (size_t)p->T * p->H * 2, yb = (size_t)p->T * p->H * 4;
     const bool reuse = p->n >= p->depth;
@@ -601,7 +658,7 @@ extern "C" {
 
 zffn_status zffn_pipeline_submit(zffn_pipeline *p, const void *x_host, const void *Wg, const void *Wu,
                                  const void *Wd, float *y_host) {
-    if (!p || !x_host || !y_host || !Wg || !Wu || !Wd) return ZFFN_ERR_INVALID_ARG;
+    if (!p || !x_host || !y_host || !Wg || !Wu || !Wd) return invalid("a pointer argument is NULL");
     return pipeline_submit(p, x_host, y_host, [&](void *x, float *y, cudaStream_t s) {
         return swiglu_dense(x, Wg, Wu, Wd, y, p->T, p->H, p->I, s, false);
     });
@@ -611,7 +668,7 @@ zffn_status zffn_pipeline_submit_moe(zffn_pipeline *p, const void *x_host, const
                                      const float *expert_weights, const void *Wg, const void *Wu,
                                      const void *Wd, int E, int top_k, float *y_host) {
     if (!p || !x_host || !y_host || !expert_ids || !expert_weights || !Wg || !Wu || !Wd)
-        return ZFFN_ERR_INVALID_ARG;
+        return invalid("a pointer argument is NULL");
     return pipeline_submit(p, x_host, y_host, [&](void *x, float *y, cudaStream_t s) {
         return swiglu_moe(x, expert_ids, expert_weights, Wg, Wu, Wd, y, p->T, p->H, p->I, E, top_k, s,
                           false);
@@ -619,7 +676,7 @@ zffn_status zffn_pipeline_submit_moe(zffn_pipeline *p, const void *x_host, const
 }
 
 zffn_status zffn_pipeline_sync(zffn_pipeline *p) {
-    if (!p) return ZFFN_ERR_INVALID_ARG;
+    if (!p) return invalid("the pipeline is NULL");
     for (cudaStream_t s : {p->up, p->comp, p->down}) {
         const cudaError_t e = cudaStreamSynchronize(s);
         if (e != cudaSuccess) return to_status(e);

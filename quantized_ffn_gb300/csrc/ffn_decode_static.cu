@@ -105,7 +105,6 @@ zffn_status zffn_swiglu_q4k_token_static(const void *x, const void *Wg, const vo
         cudaGetLastError();
         return ZFFN_ERR_CUDA;
     }
-    set_last_error("no error");
     return ZFFN_OK;
 }
 

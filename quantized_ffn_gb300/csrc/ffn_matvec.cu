@@ -602,21 +602,9 @@ cudaError_t launch_ffn_matvec(const MatvecArgs &a, cudaStream_t s) {
     const DecGeom G = dec_geom(a.H, a.I, a.k);
     const int depth = down_ring_depth(a.H, a.I, a.k);
     const size_t smem_a = gu_smem_bytes(G, a.H), smem_b = down_smem_bytes(G, depth);
-    static int attr_device = -1;
-    static size_t attr_a = 0, attr_b = 0;
-    if (attr_device != di.device || attr_a < smem_a || attr_b < smem_b) {
-        // the attributes hold the largest requests so far
-        const bool same = attr_device == di.device;
-        const size_t wa = same && attr_a > smem_a ? attr_a : smem_a;
-        const size_t wb = same && attr_b > smem_b ? attr_b : smem_b;
-        cudaError_t e = cudaFuncSetAttribute(ffn_gu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wa);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(ffn_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wb);
-        if (e != cudaSuccess) return e;
-        attr_device = di.device;
-        attr_a = wa;
-        attr_b = wb;
-    }
+    cudaError_t e = ensure_dynamic_smem((const void *)ffn_gu_kernel, smem_a);
+    if (e == cudaSuccess) e = ensure_dynamic_smem((const void *)ffn_down_kernel, smem_b);
+    if (e != cudaSuccess) return e;
     MatvecArgs args = a;
     args.ring_depth = depth;
     cudaLaunchConfig_t cfg = {};
@@ -632,7 +620,7 @@ cudaError_t launch_ffn_matvec(const MatvecArgs &a, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, ffn_gu_kernel, args);
+    e = cudaLaunchKernelEx(&cfg, ffn_gu_kernel, args);
     if (e != cudaSuccess) return e;
     cfg.dynamicSmemBytes = smem_b;
     return cudaLaunchKernelEx(&cfg, ffn_down_kernel, args);

@@ -912,13 +912,11 @@ cudaError_t launch_ffn_tc(const TcArgs &a, cudaStream_t s) {
         !encode_bytes_map(encode, &maps.d_hdr, a.Wd, rbI, d_rows, 16, rows_y) ||
         !encode_bytes_map(encode, &maps.d_qs, a.Wd, rbI, d_rows, 64, rows_y))
         return cudaErrorInvalidValue;
-    static int attr_set_device[2] = {-1, -1};
     const void *fn = pair ? (const void *)tc::ffn_tc_kernel<true> : (const void *)tc::ffn_tc_kernel<false>;
     const int smem = pair ? tc::Cfg<true>::SMEM_BYTES : tc::Cfg<false>::SMEM_BYTES;
-    if (attr_set_device[pair] != di.device) {
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    {
+        cudaError_t e = ensure_dynamic_smem(fn, (size_t)smem);
         if (e != cudaSuccess) return e;
-        attr_set_device[pair] = di.device;
     }
     tc::Params p;
     p.Wg = a.Wg;

@@ -366,16 +366,12 @@ cudaError_t launch_token_fmt(const MatvecArgs &a, int wd_fmt, cudaStream_t s) {
     const void *down = wd_fmt == kFmtQ5_K ? (const void *)down_fmt_kernel<kFmtQ5_K>
                      : wd_fmt == kFmtQ6_K ? (const void *)down_fmt_kernel<kFmtQ6_K>
                                           : (const void *)down_fmt_kernel<kFmtQ5_1>;
-    // Raise, never lower, each kernel's dynamic shared-memory limit: the
-    // gate/up kernel is shared with the Q4_K single-token path, which keeps
-    // its own record of the limit it set.
-    cudaFuncAttributes fa, fb;
+    // Raise, never lower, each kernel's dynamic shared-memory limit (the
+    // gate/up kernel is shared with the Q4_K single-token path).
+    cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, ffn_gu_kernel);
-    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fb, down);
-    if (e == cudaSuccess && (size_t)fa.maxDynamicSharedSizeBytes < smem_a)
-        e = cudaFuncSetAttribute(ffn_gu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_a);
-    if (e == cudaSuccess && (size_t)fb.maxDynamicSharedSizeBytes < smem_b)
-        e = cudaFuncSetAttribute(down, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_b);
+    if (e == cudaSuccess) e = ensure_dynamic_smem((const void *)ffn_gu_kernel, smem_a);
+    if (e == cudaSuccess) e = ensure_dynamic_smem(down, smem_b);
     if (e != cudaSuccess) return e;
     // (the gate/up kernel's block size is its launch bound: fa.maxThreadsPerBlock)
     cudaLaunchConfig_t cfg = {};

@@ -109,8 +109,7 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const __nv_bfloat16 *__
 cudaError_t launch_moe_route(const RouteArgs &a, cudaStream_t s) {
     const size_t smem = (size_t)(3 * a.E + kRouteThreads) * sizeof(int);
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(moe_route_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = ensure_dynamic_smem((const void *)moe_route_kernel, smem);
         if (e != cudaSuccess) return e;
     }
     moe_route_kernel<<<1, kRouteThreads, smem, s>>>(a);

@@ -389,6 +389,10 @@ struct DeviceInfo {
 };
 const DeviceInfo &device_info();   // current device (cached per device)
 void set_last_error(const char *what);   // text returned by zffn_last_error()
+// Raise `fn`'s dynamic shared-memory limit on the current device to at least
+// `bytes` (never lowers it).  Thread-safe: one lock covers the check, the
+// attribute call and the per-device record of the largest request so far.
+cudaError_t ensure_dynamic_smem(const void *fn, size_t bytes);
 
 cudaError_t launch_q4k_dequant(const void *blocks, float *out, int64_t rows, int64_t cols,
                                cudaStream_t s);

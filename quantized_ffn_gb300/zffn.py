@@ -69,6 +69,7 @@ def load() -> ctypes.CDLL:
                 "zffn_pipeline_destroy": ([P], None),
                 "zffn_reserve": ([I32, I32, I32, I32, I32], I32),
                 "zffn_release": ([], None),
+                "zffn_workspace_bytes": ([], ctypes.c_size_t),
                 "zffn_get_device_error": ([P], I32),
                 "zffn_set_option": ([I32, I32], I32),
                 "zffn_selftest_wait_timeout": ([I64, P], I32),
@@ -328,6 +329,11 @@ def reserve(T_max: int, H_max: int, I_max: int, E_max: int = 1, top_k_max: int =
 
 def release():
     load().zffn_release()
+
+
+def workspace_bytes() -> int:
+    """Bytes of library workspace held on the current device."""
+    return int(load().zffn_workspace_bytes())
 
 
 def get_device_error(stream=None) -> int:

@@ -209,3 +209,17 @@ def test_header_compiles_as_plain_c(tmp_path):
     subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
                            "-I", os.path.join(ROOT, "include"), "-c", str(src), "-o",
                            str(tmp_path / "use.o")])
+
+
+def test_rejections_record_the_failed_check(lib):
+    st = lib.zffn_swiglu_q4k(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 200, 256, None)
+    assert st == zffn.ERR_INVALID_ARG and b"H must be" in lib.zffn_last_error()
+    odd = ctypes.c_void_p(0x10008)
+    st = lib.zffn_swiglu_q4k(odd, FAKE, FAKE, FAKE, FAKE, 4, 256, 256, None)
+    assert st == zffn.ERR_INVALID_ARG and b"aligned" in lib.zffn_last_error()
+    st = lib.zffn_moe_swiglu_q4k(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 256, 8, 0, None)
+    assert st == zffn.ERR_INVALID_ARG and b"top_k" in lib.zffn_last_error()
+
+
+def test_workspace_query_is_zero_before_any_call(lib):
+    assert zffn.workspace_bytes() == 0
