@@ -412,10 +412,16 @@ void oracle_swiglu_ffn(const uint16_t *x, const uint8_t *Wg, const uint8_t *Wu,
  * Experts are stacked: expert e's W_gate starts at Wg + e * I * rowbytes(H),
  * likewise W_up; its W_down at Wd + e * H * rowbytes(I).  An id outside
  * [0, E) contributes nothing. */
-void oracle_moe_swiglu_ffn_fmt(const uint16_t *x, const int32_t *ids, const float *wts,
-                               const uint8_t *Wg, const uint8_t *Wu, const uint8_t *Wd,
-                               int wd_fmt, int64_t T, int64_t H, int64_t I, int64_t E,
-                               int64_t top_k, double *y)
+/* Routed block with a per-expert scale on the down projection ("Four
+ * bottlenecks, one CUDA backend...", section "Bottleneck 2": a routed layer's
+ * per-expert down projection carries a scale applied inside the batched path):
+ *     y_t = sum_j w_tj * s_e * FFN_e(x_t),   e = ids[t][j],
+ * s one fp32 value per expert (down_scale NULL: every s_e = 1).  The products
+ * w_tj * s_e * FFN_e are formed in fp64. */
+void oracle_moe_swiglu_ffn_scaled(const uint16_t *x, const int32_t *ids, const float *wts,
+                                  const float *down_scale, const uint8_t *Wg, const uint8_t *Wu,
+                                  const uint8_t *Wd, int wd_fmt, int64_t T, int64_t H, int64_t I,
+                                  int64_t E, int64_t top_k, double *y)
 {
     int64_t rb_in = ((H + QK - 1) / QK) * QK_BYTES;
     int64_t rb_dn = oracle_fmt_row_bytes(wd_fmt, I);
@@ -431,11 +437,21 @@ void oracle_moe_swiglu_ffn_fmt(const uint16_t *x, const int32_t *ids, const floa
             oracle_swiglu_ffn_fmt(x + t * H, Wg + e * I * rb_in, Wu + e * I * rb_in,
                                   Wd + e * H * rb_dn, wd_fmt, 1, H, I, yt);
             double w = (double)wts[t * top_k + j];
+            if (down_scale)
+                w *= (double)down_scale[e];
             for (int64_t n = 0; n < H; ++n)
                 out[n] += w * yt[n];
         }
     }
     free(yt);
+}
+
+void oracle_moe_swiglu_ffn_fmt(const uint16_t *x, const int32_t *ids, const float *wts,
+                               const uint8_t *Wg, const uint8_t *Wu, const uint8_t *Wd,
+                               int wd_fmt, int64_t T, int64_t H, int64_t I, int64_t E,
+                               int64_t top_k, double *y)
+{
+    oracle_moe_swiglu_ffn_scaled(x, ids, wts, NULL, Wg, Wu, Wd, wd_fmt, T, H, I, E, top_k, y);
 }
 
 void oracle_moe_swiglu_ffn(const uint16_t *x, const int32_t *ids, const float *wts,

@@ -81,6 +81,8 @@ def _load():
             lib.oracle_swiglu_ffn_fmt.argtypes = [P, P, P, P, ctypes.c_int, I64, I64, I64, P]
             lib.oracle_moe_swiglu_ffn_fmt.argtypes = [P, P, P, P, P, P, ctypes.c_int, I64, I64, I64,
                                                       I64, I64, P]
+            lib.oracle_moe_swiglu_ffn_scaled.argtypes = [P, P, P, P, P, P, P, ctypes.c_int, I64, I64,
+                                                         I64, I64, I64, P]
             lib.oracle_fmt_row_bytes.argtypes = [ctypes.c_int, I64]
             lib.oracle_fmt_row_bytes.restype = I64
             lib.oracle_bf16_from_f64.argtypes = [ctypes.c_double]
@@ -167,9 +169,10 @@ def swiglu_ffn(x_bf16: np.ndarray, Wg: np.ndarray, Wu: np.ndarray, Wd: np.ndarra
 def moe_swiglu_ffn(x_bf16: np.ndarray, ids: np.ndarray, wts: np.ndarray,
                    Wg: np.ndarray, Wu: np.ndarray, Wd: np.ndarray,
                    T: int, H: int, I: int, E: int, top_k: int,
-                   wd_fmt: int = FMT_Q4_K) -> np.ndarray:
+                   wd_fmt: int = FMT_Q4_K, down_scale=None) -> np.ndarray:
     """y[T, H] float64 for the routed experts; weights stacked [E, rows, bytes],
-    W_down in block format wd_fmt."""
+    W_down in block format wd_fmt; down_scale: None or fp32 [E], a scale on
+    each expert's down projection."""
     x_bf16 = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     ids = np.ascontiguousarray(ids, dtype=np.int32)
     wts = np.ascontiguousarray(wts, dtype=np.float32)
@@ -179,8 +182,14 @@ def moe_swiglu_ffn(x_bf16: np.ndarray, ids: np.ndarray, wts: np.ndarray,
     assert ids.size == T * top_k and wts.size == T * top_k
     assert Wg.size == E * I * row_bytes(H) and Wd.size == E * H * row_bytes_fmt(wd_fmt, I)
     y = np.empty((T, H), dtype=np.float64)
-    _load().oracle_moe_swiglu_ffn_fmt(_ptr(x_bf16), _ptr(ids), _ptr(wts), _ptr(Wg), _ptr(Wu),
-                                      _ptr(Wd), wd_fmt, T, H, I, E, top_k, _ptr(y))
+    if down_scale is None:
+        sc = None
+    else:
+        down_scale = np.ascontiguousarray(down_scale, dtype=np.float32)
+        assert down_scale.size == E
+        sc = _ptr(down_scale)
+    _load().oracle_moe_swiglu_ffn_scaled(_ptr(x_bf16), _ptr(ids), _ptr(wts), sc, _ptr(Wg), _ptr(Wu),
+                                         _ptr(Wd), wd_fmt, T, H, I, E, top_k, _ptr(y))
     return y
 
 

@@ -34,6 +34,13 @@ MUTATIONS = {
     # Q5_1 offset dropped
     "q51_offset": ("return d * (float)q + m;", "return d * (float)q;",
                    [fmt_pins.test_q51_closed_form_and_partial_rows]),
+    # the per-expert down scale divided instead of multiplied
+    "moe_scale_div": ("                w *= (double)down_scale[e];", "                w /= (double)down_scale[e];",
+                      [pins.test_moe_down_scale_closed_forms]),
+    # the per-expert down scale indexed by slot instead of expert
+    "moe_scale_slot": ("                w *= (double)down_scale[e];", "                w *= (double)down_scale[j];",
+                       [pins.test_moe_down_scale_closed_forms,
+                        pins.test_moe_down_scale_recomposed_from_dense_blocks]),
     # Q5_K scale of the wrong sub-block
     "q5k_subblock": ("oracle_q4k_scale_min(scales, k / 32, &sc, &m);\n    int q = q4k_code(qs, k) + 16",
                      "oracle_q4k_scale_min(scales, (k / 32) ^ 1, &sc, &m);\n    int q = q4k_code(qs, k) + 16",

@@ -382,6 +382,54 @@ def test_moe_slot_order_and_invalid_ids():
     np.testing.assert_allclose(yb[1], keep1[1], rtol=1e-12, atol=1e-14 * np.abs(y).max())
 
 
+def test_moe_down_scale_closed_forms():
+    # Per-expert scale on the down projection ("Four bottlenecks, one CUDA
+    # backend...", section "Bottleneck 2"): y_t = sum_j w_tj s_e FFN_e(x_t).
+    E, H, I, T, k = 5, 256, 320, 3, 3
+    Wg, Wu, Wd = _experts(E, H, I, seed=40)
+    x = _x(4, T, H)
+    ids = np.array([[4, 1, 2], [0, 3, 1], [2, 2, 4]], dtype=np.int32)
+    w = np.array([[0.5, 0.3, 0.2], [0.6, 0.25, 0.15], [0.7, 0.2, 0.1]], dtype=np.float32)
+    y = orc.moe_swiglu_ffn(x, ids, w, Wg, Wu, Wd, T, H, I, E, k)
+    # no scale and unit scales agree exactly
+    assert np.array_equal(orc.moe_swiglu_ffn(x, ids, w, Wg, Wu, Wd, T, H, I, E, k,
+                                             down_scale=np.ones(E, np.float32)), y)
+    # a common power-of-two scale scales the output exactly
+    for p2 in (0.25, 8.0):
+        ys = orc.moe_swiglu_ffn(x, ids, w, Wg, Wu, Wd, T, H, I, E, k,
+                                down_scale=np.full(E, p2, np.float32))
+        assert np.array_equal(ys, y * p2)
+    # zero scales silence the output; a zero scale on one expert equals dropping its slots
+    assert not np.any(orc.moe_swiglu_ffn(x, ids, w, Wg, Wu, Wd, T, H, I, E, k,
+                                         down_scale=np.zeros(E, np.float32)))
+    s = np.ones(E, np.float32)
+    s[2] = 0.0
+    w0 = w.copy()
+    w0[ids == 2] = 0.0
+    np.testing.assert_array_equal(
+        orc.moe_swiglu_ffn(x, ids, w, Wg, Wu, Wd, T, H, I, E, k, down_scale=s),
+        orc.moe_swiglu_ffn(x, ids, w0, Wg, Wu, Wd, T, H, I, E, k))
+
+
+def test_moe_down_scale_recomposed_from_dense_blocks():
+    # General scales against the dense block of each chosen expert, weighted
+    # by w * s in fp64 here (the dense block is pinned on its own).
+    E, H, I, T, k = 4, 256, 256, 2, 2
+    Wg, Wu, Wd = _experts(E, H, I, seed=50)
+    x = _x(5, T, H)
+    ids = np.array([[3, 0], [1, 3]], dtype=np.int32)
+    w = np.array([[0.625, 0.375], [0.9, 0.1]], dtype=np.float32)
+    s = np.array([1.7, -0.4, 3.0, 0.37], dtype=np.float32)
+    y = orc.moe_swiglu_ffn(x, ids, w, Wg, Wu, Wd, T, H, I, E, k, down_scale=s)
+    for t in range(T):
+        ref = np.zeros(H)
+        for j in range(k):
+            e = ids[t, j]
+            ref += (float(w[t, j]) * float(s[e])) * orc.swiglu_ffn(
+                x[t:t + 1].copy(), Wg[e], Wu[e], Wd[e], 1, H, I)[0]
+        np.testing.assert_allclose(y[t], ref, rtol=1e-12, atol=1e-14 * np.abs(ref).max())
+
+
 # ---- the pages' byte model ---------------------------------------------------------
 
 def _golden(name):
