@@ -94,10 +94,16 @@ zffn_status zffn_q4k_quantize(const float *w, void *blocks, int64_t rows, int64_
  * Requirements: T >= 1, H % 256 == 0, I % 64 == 0, 256 <= H <= 16384,
  * 64 <= I <= 65536.  T = 1 runs the memory-bound single-token kernel; larger T
  * run the tensor-core prefill kernel (the switch-over can be changed with
- * zffn_set_option).  Accumulation is fp32; operands of the tensor-core path are
- * rounded to bf16 (x is bf16 already; unpacked weights and the SwiGLU
- * intermediate are rounded to bf16 on chip).
- * Uses library workspace (see zffn_reserve) on the single-token path.
+ * zffn_set_option).  Accumulation is fp32.  Operands of the tensor-core path:
+ * the gate/up product takes x and the unpacked W_gate, W_up in fp16 (x
+ * converted once per call; each sub-block's scale d*sc and offset dmin*m
+ * rounded to fp16, then one fused multiply-add per weight); the down product
+ * takes the SwiGLU intermediate and the unpacked W_down in bf16.  fp16 values
+ * saturate at +-65504: |x| above that, or a sub-block with d*sc > 128 or
+ * dmin*m > 65504, is clamped on that path (far outside quantised weights and
+ * normalised activations).
+ * Uses library workspace (see zffn_reserve): the single-token path's
+ * intermediate strip, and the prefill path's fp16 copy of x (T*H*2 bytes).
  * Errors: INVALID_ARG (NULL, misaligned, bad sizes), CUDA, NO_WORKSPACE. */
 zffn_status zffn_swiglu_q4k(const void *x, const void *Wg, const void *Wu, const void *Wd,
                             float *y, int T, int H, int I, void *stream);
@@ -267,6 +273,27 @@ zffn_status zffn_moe_swiglu_q4k(const void *x, const int32_t *expert_ids,
 zffn_status zffn_moe_router_topk(const float *logits, int32_t *expert_ids,
                                  float *expert_weights, int T, int E, int top_k,
                                  void *stream);
+
+/* The routed block with a scale on each expert's down projection
+ * ("Four bottlenecks, one CUDA backend...", section "Bottleneck 2 -- MoE decode
+ * was paying for its routing twice": a routed layer's per-expert
+ * down-projection scale is applied inside the batched path, not folded away):
+ *     y[t] (+)= sum_{j < top_k} expert_weights[t][j] * down_scale[e] * FFN_e(x[t]),
+ *     e = expert_ids[t][j]
+ *   down_scale: fp32 [E] (device, 4-byte aligned), or NULL for every scale 1.
+ *     It multiplies the routing weight of each (token, slot) in fp32 before the
+ *     down projection's output is added.
+ *   wd_fmt: block format of every expert's W_down (zffn_format); formats other
+ *     than ZFFN_FMT_Q4_K take T = 1 only, as for zffn_moe_swiglu_q4k_wd.
+ *   accumulate: 0 overwrites y, non-zero adds the block's output to y.
+ *   The other arguments as for zffn_moe_swiglu_q4k (expert_ids and
+ *   expert_weights must not be NULL).
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA, NO_WORKSPACE. */
+zffn_status zffn_moe_swiglu_q4k_scaled(const void *x, const int32_t *expert_ids,
+                                       const float *expert_weights, const float *down_scale,
+                                       const void *Wg, const void *Wu, const void *Wd, int wd_fmt,
+                                       float *y, int T, int H, int I, int E, int top_k,
+                                       int accumulate, void *stream);
 
 /* As zffn_moe_swiglu_q4k, but y += the routed block's output. */
 zffn_status zffn_moe_swiglu_q4k_residual(const void *x, const int32_t *expert_ids,

@@ -32,7 +32,7 @@ inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 // Sub-buffers carved out of one device allocation.
 struct Layout {
-    size_t h, counts, offsets, cursors, tiles, n_tiles, row_token, row_weight, x_perm, xn,
+    size_t h, counts, offsets, cursors, tiles, n_tiles, row_token, row_weight, x_perm, xn, x16,
         total;
     int max_tiles;
 };
@@ -52,6 +52,7 @@ Layout layout_for(int T, int H, int I, int E, int k) {
     L.row_weight = o; o = align_up(o + (size_t)P * sizeof(float));
     L.x_perm = o; o = align_up(o + (size_t)P * H * 2);
     L.xn = o; o = align_up(o + (size_t)T * H * 2);      // normalised block input (pre-norm entry)
+    L.x16 = o; o = align_up(o + (size_t)T * H * 2);     // fp16 block input of the tensor-core path
     L.total = o;
     return L;
 }
@@ -242,12 +243,17 @@ zffn_status swiglu_dense(const void *x, const void *Wg, const void *Wu, const vo
         a.accumulate = accumulate;
         return to_status(launch_ffn_matvec(a, s));
     }
-    if (!accumulate) {
-        cudaError_t e = launch_zero_f32(y, (int64_t)T * H, s);
-        if (e != cudaSuccess) return to_status(e);
-    }
+    // the tensor-core kernel's gate/up operand is fp16: convert x into
+    // workspace (and zero y for the kernel's reductions) in one pass
+    const Layout L = layout_for(T, H, I, 1, 1);
+    Workspace *w = nullptr;
+    zffn_status st = ensure_workspace(L.total, &w);
+    if (st != ZFFN_OK) return st;
+    void *x16 = static_cast<uint8_t *>(w->ptr) + L.x16;
+    cudaError_t e = launch_x_to_f16(x, x16, (int64_t)T * H, accumulate ? nullptr : y, (int64_t)T * H, s);
+    if (e != cudaSuccess) return to_status(e);
     TcArgs a{};
-    a.x = x;
+    a.x = x16;
     a.x_rows = T;
     a.Wg = static_cast<const uint8_t *>(Wg);
     a.Wu = static_cast<const uint8_t *>(Wu);
@@ -264,8 +270,9 @@ zffn_status swiglu_dense(const void *x, const void *Wg, const void *Wu, const vo
 }
 
 zffn_status swiglu_moe(const void *x, const int32_t *expert_ids, const float *expert_weights,
-                       const void *Wg, const void *Wu, const void *Wd, float *y, int T, int H,
-                       int I, int E, int top_k, void *stream, bool accumulate) {
+                       const float *down_scale, const void *Wg, const void *Wu, const void *Wd,
+                       float *y, int T, int H, int I, int E, int top_k, void *stream,
+                       bool accumulate) {
     if (!x || !expert_ids || !expert_weights || !Wg || !Wu || !Wd || !y)
         return invalid("a pointer argument is NULL");
     if (check_shape(T, H, I) != ZFFN_OK) return ZFFN_ERR_INVALID_ARG;
@@ -276,6 +283,7 @@ zffn_status swiglu_moe(const void *x, const int32_t *expert_ids, const float *ex
         (reinterpret_cast<uintptr_t>(expert_ids) & 3) ||
         (reinterpret_cast<uintptr_t>(expert_weights) & 3))
         return invalid("x, Wg, Wu, Wd, y must be 16-byte and expert_ids, expert_weights 4-byte aligned");
+    if (reinterpret_cast<uintptr_t>(down_scale) & 3) return invalid("down_scale must be 4-byte aligned");
     const DeviceInfo &di = device_info();
     if (di.device < 0) return ZFFN_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
@@ -297,6 +305,7 @@ zffn_status swiglu_moe(const void *x, const int32_t *expert_ids, const float *ex
         a.Wd = static_cast<const uint8_t *>(Wd);
         a.ids = expert_ids;
         a.wts = expert_weights;
+        a.down_scale = down_scale;
         a.y = y;
         a.h = reinterpret_cast<float *>(base + L.h);
         a.err = di.err_word;
@@ -307,6 +316,7 @@ zffn_status swiglu_moe(const void *x, const int32_t *expert_ids, const float *ex
     RouteArgs r{};
     r.ids = expert_ids;
     r.wts = expert_weights;
+    r.down_scale = down_scale;
     r.x = static_cast<const __nv_bfloat16 *>(x);
     r.T = T; r.H = H; r.E = E; r.k = top_k;
     r.counts = reinterpret_cast<int *>(base + L.counts);
@@ -316,7 +326,7 @@ zffn_status swiglu_moe(const void *x, const int32_t *expert_ids, const float *ex
     r.n_tiles = reinterpret_cast<int *>(base + L.n_tiles);
     r.row_token = reinterpret_cast<int *>(base + L.row_token);
     r.row_weight = reinterpret_cast<float *>(base + L.row_weight);
-    r.x_perm = reinterpret_cast<__nv_bfloat16 *>(base + L.x_perm);
+    r.x_perm = reinterpret_cast<__half *>(base + L.x_perm);
     r.max_tiles = L.max_tiles;
     cudaError_t e = launch_moe_route(r, s);
     if (e != cudaSuccess) return to_status(e);
@@ -360,16 +370,16 @@ zffn_status zffn_moe_swiglu_q4k(const void *x, const int32_t *expert_ids,
                                 const float *expert_weights, const void *Wg, const void *Wu,
                                 const void *Wd, float *y, int T, int H, int I, int E, int top_k,
                                 void *stream) {
-    return swiglu_moe(x, expert_ids, expert_weights, Wg, Wu, Wd, y, T, H, I, E, top_k, stream,
-                      false);
+    return swiglu_moe(x, expert_ids, expert_weights, nullptr, Wg, Wu, Wd, y, T, H, I, E, top_k,
+                      stream, false);
 }
 
 zffn_status zffn_moe_swiglu_q4k_residual(const void *x, const int32_t *expert_ids,
                                          const float *expert_weights, const void *Wg,
                                          const void *Wu, const void *Wd, float *y, int T, int H,
                                          int I, int E, int top_k, void *stream) {
-    return swiglu_moe(x, expert_ids, expert_weights, Wg, Wu, Wd, y, T, H, I, E, top_k, stream,
-                      true);
+    return swiglu_moe(x, expert_ids, expert_weights, nullptr, Wg, Wu, Wd, y, T, H, I, E, top_k,
+                      stream, true);
 }
 
 size_t zffn_row_bytes_fmt(int fmt, int64_t cols) {
@@ -385,15 +395,21 @@ zffn_status zffn_dequant_fmt(int fmt, const void *blocks, float *out, int64_t ro
     return to_status(launch_dequant_fmt(fmt, blocks, out, rows, cols, (cudaStream_t)stream));
 }
 
-zffn_status zffn_moe_swiglu_q4k_wd(const void *x, const int32_t *expert_ids,
-                                   const float *expert_weights, const void *Wg, const void *Wu,
-                                   const void *Wd, int wd_fmt, float *y, int T, int H, int I, int E,
-                                   int top_k, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// Routed (expert_ids != NULL) or dense block with W_down in any format, an
+// optional per-expert scale of the down projection, overwrite or accumulate.
+zffn_status swiglu_wd(const void *x, const int32_t *expert_ids, const float *expert_weights,
+                      const float *down_scale, const void *Wg, const void *Wu, const void *Wd,
+                      int wd_fmt, float *y, int T, int H, int I, int E, int top_k, void *stream,
+                      bool accumulate) {
     if (!fmt_valid(wd_fmt)) return invalid("unknown block format of W_down");
     if (wd_fmt == kFmtQ4_K)
-        return expert_ids ? swiglu_moe(x, expert_ids, expert_weights, Wg, Wu, Wd, y, T, H, I, E,
-                                       top_k, stream, false)
-                          : swiglu_dense(x, Wg, Wu, Wd, y, T, H, I, stream, false);
+        return expert_ids ? swiglu_moe(x, expert_ids, expert_weights, down_scale, Wg, Wu, Wd, y, T,
+                                       H, I, E, top_k, stream, accumulate)
+                          : swiglu_dense(x, Wg, Wu, Wd, y, T, H, I, stream, accumulate);
     const bool moe = expert_ids != nullptr;
     if (!x || !Wg || !Wu || !Wd || !y || (moe && !expert_weights))
         return invalid("a pointer argument is NULL");
@@ -405,6 +421,7 @@ zffn_status zffn_moe_swiglu_q4k_wd(const void *x, const int32_t *expert_ids,
         (moe && ((reinterpret_cast<uintptr_t>(expert_ids) & 3) ||
                  (reinterpret_cast<uintptr_t>(expert_weights) & 3))))
         return invalid("x, Wg, Wu must be 16-byte and Wd, y, expert_ids, expert_weights 4-byte aligned");
+    if (reinterpret_cast<uintptr_t>(down_scale) & 3) return invalid("down_scale must be 4-byte aligned");
     if (T != 1) return ZFFN_ERR_UNSUPPORTED;       // other formats: single-token paths only
     const int k = moe ? top_k : 1;
     const DeviceInfo &di = device_info();
@@ -423,12 +440,35 @@ zffn_status zffn_moe_swiglu_q4k_wd(const void *x, const int32_t *expert_ids,
     a.Wd = static_cast<const uint8_t *>(Wd);
     a.ids = expert_ids;
     a.wts = expert_weights;
+    a.down_scale = moe ? down_scale : nullptr;
     a.y = y;
     a.h = reinterpret_cast<float *>(static_cast<uint8_t *>(w->ptr) + L.h);
     a.err = di.err_word;
     a.T = 1; a.H = H; a.I = I; a.E = moe ? E : 1; a.k = k;
-    a.accumulate = false;
+    a.accumulate = accumulate;
     return to_status(launch_token_fmt(a, wd_fmt, (cudaStream_t)stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+zffn_status zffn_moe_swiglu_q4k_wd(const void *x, const int32_t *expert_ids,
+                                   const float *expert_weights, const void *Wg, const void *Wu,
+                                   const void *Wd, int wd_fmt, float *y, int T, int H, int I, int E,
+                                   int top_k, void *stream) {
+    return swiglu_wd(x, expert_ids, expert_weights, nullptr, Wg, Wu, Wd, wd_fmt, y, T, H, I, E,
+                     top_k, stream, false);
+}
+
+zffn_status zffn_moe_swiglu_q4k_scaled(const void *x, const int32_t *expert_ids,
+                                       const float *expert_weights, const float *down_scale,
+                                       const void *Wg, const void *Wu, const void *Wd, int wd_fmt,
+                                       float *y, int T, int H, int I, int E, int top_k,
+                                       int accumulate, void *stream) {
+    if (!expert_ids || !expert_weights) return invalid("expert_ids and expert_weights are required");
+    return swiglu_wd(x, expert_ids, expert_weights, down_scale, Wg, Wu, Wd, wd_fmt, y, T, H, I, E,
+                     top_k, stream, accumulate != 0);
 }
 
 zffn_status zffn_swiglu_q4k_wd(const void *x, const void *Wg, const void *Wu, const void *Wd,
@@ -670,8 +710,8 @@ zffn_status zffn_pipeline_submit_moe(zffn_pipeline *p, const void *x_host, const
     if (!p || !x_host || !y_host || !expert_ids || !expert_weights || !Wg || !Wu || !Wd)
         return invalid("a pointer argument is NULL");
     return pipeline_submit(p, x_host, y_host, [&](void *x, float *y, cudaStream_t s) {
-        return swiglu_moe(x, expert_ids, expert_weights, Wg, Wu, Wd, y, p->T, p->H, p->I, E, top_k, s,
-                          false);
+        return swiglu_moe(x, expert_ids, expert_weights, nullptr, Wg, Wu, Wd, y, p->T, p->H, p->I, E,
+                          top_k, s, false);
     });
 }
 

@@ -566,7 +566,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) ffn_down_kernel(MatvecArgs a) 
                 for (int i = 0; i < 4; ++i) cq[i] = *reinterpret_cast<const uint4 *>(blk + 16 + 64 * (q & 1) + 16 * i);
                 int ai[4];
                 half_block_isums(cq, xv, ai);
-                const float w = moe ? a.wts[p] : 1.0f;
+                const float w = moe ? (a.down_scale ? a.wts[p] * a.down_scale[e] : a.wts[p]) : 1.0f;
                 acc = fmaf(w, half_block_scale(hd, q & 1, ai, xs, xsum), acc);
             }
         }

@@ -59,6 +59,15 @@ constexpr int NJ_Y = 128;                // UMMA N of a down-projection job (out
 constexpr int A_BYTES = BM * BK * 2;     // 16 KB x tile per CTA
 constexpr int HT_BYTES = BM * BK * 2;    // one 64-column slice of h: 16 KB
 constexpr uint32_t COL_GU = 0, COL_Y = 256, COL_STASH = 384;   // TMEM columns
+// Down-projection accumulators.  While a block has a next unit, its down jobs
+// use COL_Y only (the gate/up accumulator and the h stash are busy with the
+// next unit).  In a block's last unit both are free once its h is in shared
+// memory, so its down jobs rotate over four 128-column buffers and the drain
+// of one overlaps the MMAs of the next three.
+constexpr int NYBUF = 4;
+__device__ __forceinline__ uint32_t ybuf_col(int b) {
+    return b == 0 ? COL_Y : b == 1 ? COL_STASH : b == 2 ? COL_GU : COL_GU + 128;
+}
 // Warp roles.  Warp w is scheduled by sub-partition w % 4.  The epilogue
 // needs one warp per sub-partition, because a warp reads only the TMEM lane
 // quadrant w % 4: warps 0-3.  The unpackers (warps 8-19, three groups of one
@@ -127,11 +136,11 @@ struct Cfg {
     static constexpr int OFF_R = OFF_B + NB * B_BYTES;
     static constexpr int OFF_Y = ((OFF_R + NR * R_BYTES) + 1023) & ~1023;
     static constexpr int OFF_BAR = OFF_Y + 4 * 2 * Y_BUF;
-    static constexpr int N_BARS = 2 * NA + 2 * NB + 2 * NR + 7;
+    static constexpr int N_BARS = 2 * NA + 2 * NB + 2 * NR + 5 + 2 * NYBUF;
     static constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + alignment slack
     static constexpr int EPI_ARRIVALS = PAIR ? 8 : 4;     // epilogue warps arriving per job
     static constexpr int B_ARRIVALS = (PAIR ? 2 : 1) * TASKS * UNPACK_GROUP_WARPS;
-    static constexpr uint32_t IDESC_GU = idesc_bf16_f32(PAIR ? 256 : 128, NJ_GU);
+    static constexpr uint32_t IDESC_GU = idesc_f16_f32(PAIR ? 256 : 128, NJ_GU);   // fp16 x, W_gate, W_up
     static constexpr uint32_t IDESC_Y = idesc_bf16_f32(PAIR ? 256 : 128, NJ_Y);
     static_assert(R_BYTES_Y <= R_BYTES, "down-step slice fits a weight stage");
     static_assert(!PAIR || UNPACK_GROUPS <= NB, "parity waits on B stages stay unambiguous");
@@ -267,6 +276,42 @@ __device__ __forceinline__ void unpack_row_to_smem(uint4 hd, const uint32_t (&w)
     else unpack_row_to_smem_narrow(hd, w, g, row_addr, row);
 }
 
+// The gate/up operands are fp16: unpack the 8 code words of one weight row and
+// K step into its swizzled fp16 row.  Each code pair becomes (q0, q1) * 2^-9
+// exactly (codes_to_f16x2), and one fused fp16 multiply-add per pair gives
+//     w = (q * 2^-9) * fp16(512 d sc) - fp16(dmin m),
+// rounded once to fp16 (11-bit significand): the sub-block's scale and offset
+// are rounded to fp16 first (relative error <= 2^-11 each), far below the
+// bf16 rounding the down projection's operands get.  d*sc*512 and dmin*m are
+// exact in fp32 before that rounding; values beyond the fp16 range saturate
+// at +-65504 (|d * sc| > 128 or |dmin * m| > 65504: far outside any
+// quantised weight).  Chunks are stored as soon as they are formed.
+__device__ __forceinline__ void unpack_row_to_smem_f16(uint4 hd, const uint32_t (&w)[8], int g,
+                                                       uint32_t row_addr, int row) {
+    const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
+    int sc0, m0, sc1, m1;
+    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g, sc0, m0);
+    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g + 1, sc1, m1);
+    const uint32_t a0 = f16x2_splat_satfinite(512.0f * (d * (float)sc0));
+    const uint32_t b0 = f16x2_splat_satfinite(-(dmin * (float)m0));
+    const uint32_t a1 = f16x2_splat_satfinite(512.0f * (d * (float)sc1));
+    const uint32_t b1 = f16x2_splat_satfinite(-(dmin * (float)m1));
+    constexpr uint32_t NIB = 0x0F0F0F0Fu;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        // words 2c, 2c+1: low nibbles are weights 8c..8c+7 of sub-block 2g,
+        // high nibbles weights 32+8c..32+8c+7 of sub-block 2g+1
+        const uint32_t l0 = w[2 * c] & NIB, l1 = w[2 * c + 1] & NIB;
+        const uint32_t h0 = (w[2 * c] >> 4) & NIB, h1 = (w[2 * c + 1] >> 4) & NIB;
+        st_shared_v4(row_addr + (((uint32_t)(c ^ (row & 7))) << 4),
+                     fma_f16x2(codes_to_f16x2(l0), a0, b0), fma_f16x2(codes_to_f16x2(l0 >> 16), a0, b0),
+                     fma_f16x2(codes_to_f16x2(l1), a0, b0), fma_f16x2(codes_to_f16x2(l1 >> 16), a0, b0));
+        st_shared_v4(row_addr + (((uint32_t)((c + 4) ^ (row & 7))) << 4),
+                     fma_f16x2(codes_to_f16x2(h0), a1, b1), fma_f16x2(codes_to_f16x2(h0 >> 16), a1, b1),
+                     fma_f16x2(codes_to_f16x2(h1), a1, b1), fma_f16x2(codes_to_f16x2(h1 >> 16), a1, b1));
+    }
+}
+
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
@@ -363,8 +408,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t *b_full = bars + 2 * C::NA, *b_empty = b_full + C::NB;
     uint64_t *r_full = b_empty + C::NB, *r_empty = r_full + C::NR;
     uint64_t *g_full = r_empty + C::NR, *g_empty = g_full + 1;
-    uint64_t *y_full = g_full + 2, *y_empty = g_full + 3;
-    uint64_t *h_full = g_full + 4, *h_empty = g_full + 5, *drain = g_full + 6;
+    uint64_t *h_full = g_full + 2, *h_empty = g_full + 3, *drain = g_full + 4;
+    uint64_t *y_full = g_full + 5, *y_empty = y_full + NYBUF;   // per down-projection buffer
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::N_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -398,8 +443,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         mbar_init(g_full, 1);
         mbar_init(g_empty, C::EPI_ARRIVALS);
-        mbar_init(y_full, 1);
-        mbar_init(y_empty, C::EPI_ARRIVALS);
+        for (int b = 0; b < NYBUF; ++b) {
+            mbar_init(&y_full[b], 1);
+            mbar_init(&y_empty[b], C::EPI_ARRIVALS);
+        }
         mbar_init(h_full, C::EPI_ARRIVALS);
         mbar_init(h_empty, 1);
         mbar_init(drain, 1);
@@ -537,7 +584,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         // one elected lane issues the MMAs and commits.
         if (leader) {
             const bool issuer = elect_one();
-            uint32_t ai = 0, aph = 0, bi = 0, bph = 0, jg = 0, jy = 0;
+            uint32_t ai = 0, aph = 0, bi = 0, bph = 0, jg = 0;
+            uint32_t yph = 0;    // bit b: parity of the uses of down buffer b so far
+            int yb = 0;
             bool ok = true;
             auto commit = [&](uint64_t *bar) {
                 if (issuer) {
@@ -557,7 +606,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             constexpr uint64_t A_STEP = A_BYTES >> 4, B_STEP = C::B_BYTES >> 4;
             constexpr uint64_t HT_STEP = HT_BYTES >> 4, YH_STEP = (C::ROWS_Y * 128) >> 4;
             uint64_t da = da0, db = db0;
-            const uint32_t d_gu = tmem_base + COL_GU, d_y = tmem_base + COL_Y;
+            const uint32_t d_gu = tmem_base + COL_GU;
+            uint32_t d_y = tmem_base + COL_Y;
             Prog pg;
             pg.start(m_units, ks_gu, NY, YS);
             for (; !pg.done && ok; pg.next()) {
@@ -582,7 +632,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                         // the first down job of a unit reads its h: wait until
                         // the epilogues placed all of it in shared memory
                         if (pg.n == 0 && !mbar_wait(h_full, (uint32_t)pg.blk & 1, abort_flag, p.err)) { ok = false; break; }
-                        if (!mbar_wait(y_empty, (jy & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
+                        yb = pg.blk == m_units - 1 ? pg.n % NYBUF : 0;
+                        d_y = tmem_base + ybuf_col(yb);
+                        if (!mbar_wait(&y_empty[yb], ((yph >> yb) & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
                         tc_fence_after();
                     }
                     if (!mbar_wait(&b_full[bi], bph, abort_flag, p.err)) { ok = false; break; }
@@ -595,8 +647,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     commit(&b_empty[bi]);
                     if (++bi == C::NB) { bi = 0; bph ^= 1; db = db0; } else { db += B_STEP; }
                     if (pg.ys == YS - 1) {
-                        commit(y_full);
-                        ++jy;
+                        commit(&y_full[yb]);
+                        yph ^= 1u << yb;
                         // h may be overwritten once the unit's last down MMAs finish
                         if (pg.n == NY - 1) commit(h_empty);
                     }
@@ -662,7 +714,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!mbar_wait(&b_empty[bi], bph ^ 1, abort_flag, p.err)) { ok = false; break; }
                 const uint32_t rb = s_b + bi * C::B_BYTES + half * (C::ROWS_Y * 128) + sw128_row(row);
                 const uint32_t w8[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                unpack_row_to_smem<PAIR>(hd, w8, g, rb, row);
+                if (pg.gu) unpack_row_to_smem_f16(hd, w8, g, rb, row);
+                else unpack_row_to_smem<PAIR>(hd, w8, g, rb, row);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) arrive_leader(&b_full[bi]);
@@ -681,7 +734,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         // reduction per warp and slice; routed tiles scatter rows, so each
         // thread adds its own row with vector reductions
         const bool tma_y = p.tiles == nullptr;
-        uint32_t jg = 0, jy = 0;
+        uint32_t jg = 0;
+        uint32_t yph = 0;        // bit b: parity of the uses of down buffer b so far
         bool ok = true;
         Prog pg;
         pg.start(m_units, ks_gu, NY, YS);
@@ -758,7 +812,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (pg.ys != YS - 1) continue;
             // ---- down job n complete: Y tile -> y[token, n*128 ..]
-            if (!mbar_wait(y_full, jy & 1, abort_flag, p.err)) { ok = false; break; }
+            const int yb = pg.blk == m_units - 1 ? pg.n % NYBUF : 0;
+            const uint32_t ycol = ybuf_col(yb);
+            if (!mbar_wait(&y_full[yb], (yph >> yb) & 1, abort_flag, p.err)) { ok = false; break; }
             tc_fence_after();
             const int ncol = pg.n * NJ_Y;
             if (tma_y) {
@@ -778,7 +834,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         __syncwarp();
                     }
                     uint32_t yv[32];
-                    tmem_ld_32x32b_x32(t_lane + COL_Y + c, yv);
+                    tmem_ld_32x32b_x32(t_lane + ycol + c, yv);
                     tmem_ld_wait(yv);
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
@@ -803,7 +859,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll 1
                 for (int c = 0; c < NJ_Y; c += 32) {
                     uint32_t yr[32];
-                    tmem_ld_32x32b_x32(t_lane + COL_Y + c, yr);
+                    tmem_ld_32x32b_x32(t_lane + ycol + c, yr);
                     tmem_ld_wait(yr);
                     if (valid) {
 #pragma unroll
@@ -821,8 +877,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) arrive_leader(y_empty);
-            ++jy;
+            if (lane == 0) arrive_leader(&y_empty[yb]);
+            yph ^= 1u << yb;
         }
         // the reductions must have finished before the block exits
         if (lane == 0) bulk_wait_group_all();
@@ -885,7 +941,7 @@ cudaError_t launch_ffn_tc(const TcArgs &a, cudaStream_t s) {
         const cuuint64_t strides[1] = {(cuuint64_t)a.H * 2};
         const cuuint32_t box[2] = {tc::BK, tc::BM};
         const cuuint32_t estr[2] = {1, 1};
-        CUresult r = encode(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.x),
+        CUresult r = encode(&maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(a.x),
                             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

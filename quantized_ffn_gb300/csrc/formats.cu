@@ -341,7 +341,12 @@ __global__ void __launch_bounds__(kDownWarps * 32, 1) down_fmt_kernel(MatvecArgs
             part += dot8<F>(sb + (size_t)(u - cur.u0) * ub, k0, v);
         }
         if (u1 >= nu) {                             // last chunk of this slot's row
-            acc = fmaf(moe ? a.wts[cur.p] : 1.0f, part, acc);
+            float w = 1.0f;
+            if (moe) {
+                w = a.wts[cur.p];
+                if (a.down_scale) w *= a.down_scale[a.ids[cur.p]];
+            }
+            acc = fmaf(w, part, acc);
             part = 0.0f;
             if (nx.done || nx.n != cur.n) {         // last slot of this output row
 #pragma unroll

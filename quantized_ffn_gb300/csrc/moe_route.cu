@@ -10,7 +10,8 @@
 //     (the tensor-core kernel's M), record for each gathered row its token and
 //     routing weight.  Pairs with an id outside [0, E) are dropped.
 //   gather kernel: copy the x row of every gathered row into a contiguous
-//     buffer so that the tensor-core kernel can load expert tiles with TMA.
+//     buffer, converted to fp16 (the tensor-core kernel's gate/up operand type),
+//     so that the tensor-core kernel can load expert tiles with TMA.
 #include "zffn_internal.cuh"
 
 namespace zffn {
@@ -87,7 +88,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
         if (e >= 0 && e < a.E) {
             const int pos = atomicAdd(&cnt[e], 1);
             a.row_token[pos] = i / a.k;
-            a.row_weight[pos] = a.wts[i];
+            a.row_weight[pos] = a.down_scale ? a.wts[i] * a.down_scale[e] : a.wts[i];
         }
     }
 }
@@ -95,14 +96,19 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
 __global__ void __launch_bounds__(256) moe_gather_kernel(const __nv_bfloat16 *__restrict__ x,
                                                          const int *__restrict__ offsets, int E,
                                                          const int *__restrict__ row_token,
-                                                         __nv_bfloat16 *__restrict__ x_perm,
+                                                         __half *__restrict__ x_perm,
                                                          int rows_cap, int H) {
     const int n_rows = min(offsets[E], rows_cap);
     const int vec = H / 8;   // 16-byte vectors per row
     for (int r = blockIdx.x; r < n_rows; r += gridDim.x) {
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)row_token[r] * H);
         uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (int64_t)r * H);
-        for (int v = threadIdx.x; v < vec; v += blockDim.x) dst[v] = src[v];
+        for (int v = threadIdx.x; v < vec; v += blockDim.x) {
+            // the tensor-core kernel takes its gate/up operand in fp16
+            const uint4 w = src[v];
+            dst[v] = make_uint4(bf16x2_to_f16x2_satfinite(w.x), bf16x2_to_f16x2_satfinite(w.y),
+                                bf16x2_to_f16x2_satfinite(w.z), bf16x2_to_f16x2_satfinite(w.w));
+        }
     }
 }
 

@@ -179,4 +179,38 @@ cudaError_t launch_zero_f32(float *p, int64_t n, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// The tensor-core kernel's gate/up operand: x (bf16, n values, n % 8 == 0)
+// as fp16; optionally y[0, ny) = 0 in the same pass (the reductions of the
+// tensor-core kernel add into y).
+__global__ void __launch_bounds__(256) x_to_f16_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ x16,
+                                                       int64_t n8, float4 *__restrict__ y, int64_t ny4,
+                                                       float *ytail, int nytail) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += stride) {
+        const uint4 v = x[i];
+        x16[i] = make_uint4(bf16x2_to_f16x2_satfinite(v.x), bf16x2_to_f16x2_satfinite(v.y),
+                            bf16x2_to_f16x2_satfinite(v.z), bf16x2_to_f16x2_satfinite(v.w));
+    }
+    if (y) {
+        for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < ny4; i += stride)
+            y[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (blockIdx.x == 0 && threadIdx.x < nytail) ytail[threadIdx.x] = 0.0f;
+    }
+}
+
+cudaError_t launch_x_to_f16(const void *x, void *x16, int64_t n, float *y_zero, int64_t ny,
+                            cudaStream_t s) {
+    if (n % 8 != 0) return cudaErrorInvalidValue;
+    const int64_t n8 = n / 8, ny4 = y_zero ? ny / 4 : 0;
+    const int64_t work = n8 > ny4 ? n8 : ny4;
+    int64_t grid = (work + 255) / 256;
+    const int64_t cap = (int64_t)device_info().num_sms * 8;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    x_to_f16_kernel<<<(unsigned)grid, 256, 0, s>>>(
+        static_cast<const uint4 *>(x), static_cast<uint4 *>(x16), n8, reinterpret_cast<float4 *>(y_zero), ny4,
+        y_zero ? y_zero + 4 * ny4 : nullptr, y_zero ? (int)(ny - 4 * ny4) : 0);
+    return cudaGetLastError();
+}
+
 }  // namespace zffn

@@ -357,10 +357,49 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
            | ((uint32_t)(N >> 3) << 17)       // N / 8
            | ((uint32_t)(M >> 4) << 24);      // M / 16
 }
+// The same with A = B = fp16 (format code 0).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+    return (1u << 4)                          // D format f32
+           | ((uint32_t)(N >> 3) << 17)       // N / 8
+           | ((uint32_t)(M >> 4) << 24);      // M / 16
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Two 4-bit codes as fp16: the low 16 bits of `v` hold two bytes, each a code
+// 0..15.  Read as an e4m3 bit pattern, a byte 0000qqqq is q * 2^-9 exactly
+// (exponent field 0: subnormal (q & 7) / 8 * 2^-6; exponent field 1 for
+// q >= 8: (1 + (q & 7) / 8) * 2^-6), so the fp8 -> fp16 converter turns the
+// pair into fp16 (q0 * 2^-9, q1 * 2^-9) without rounding.
+__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t v) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(r) : "r"(v));
+    return r;
+}
+// a * b + c on fp16 pairs, rounded once.
+__device__ __forceinline__ uint32_t fma_f16x2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+// fp32 -> fp16 (nearest), clamped to the largest finite fp16, in both halves.
+__device__ __forceinline__ uint32_t f16x2_splat_satfinite(float v) {
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %1;" : "=r"(r) : "f"(v));
+    return r;
+}
+
+// bf16 pair (one 32-bit word) -> fp16 pair: both widen exactly to fp32, then
+// round to fp16 (nearest, saturating at +-65504).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_satfinite(uint32_t w) {
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;"
+        : "=r"(r)
+        : "f"(__uint_as_float(w & 0xFFFF0000u)), "f"(__uint_as_float(w << 16)));
+    return r;
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -399,6 +438,10 @@ cudaError_t launch_q4k_dequant(const void *blocks, float *out, int64_t rows, int
 cudaError_t launch_q4k_quantize(const float *w, void *blocks, int64_t rows, int64_t cols,
                                 cudaStream_t s);
 cudaError_t launch_zero_f32(float *p, int64_t n, cudaStream_t s);
+// x (bf16, n values, n % 8 == 0, 16-byte aligned) -> x16 (fp16, saturating);
+// if y_zero is not null, also y_zero[0, ny) = 0.
+cudaError_t launch_x_to_f16(const void *x, void *x16, int64_t n, float *y_zero, int64_t ny,
+                            cudaStream_t s);
 
 // Single-token path: a gate/up kernel (SwiGLU into an on-device strip h)
 // followed by a down-projection kernel launched as its programmatic
@@ -408,6 +451,7 @@ struct MatvecArgs {
     const uint8_t *Wg, *Wu, *Wd; // expert-stacked
     const int32_t *ids;          // [T][k] or nullptr (dense: expert 0, weight 1)
     const float *wts;            // [T][k] or nullptr
+    const float *down_scale;     // [E] scale of each expert's down projection, or nullptr
     float *y;                    // [T][H]
     float *h;                    // workspace [T*k][I]
     int *err;
@@ -420,7 +464,7 @@ cudaError_t launch_ffn_matvec(const MatvecArgs &a, cudaStream_t s);
 
 // Tensor-core fused prefill path.
 struct TcArgs {
-    const void *x;               // bf16 rows (dense x or the gathered MoE rows)
+    const void *x;               // fp16 rows (dense x converted, or the gathered MoE rows)
     int64_t x_rows;              // rows of x visible to the tensor map
     const uint8_t *Wg, *Wu, *Wd;
     float *y;                    // [T][H], zero-filled before the launch
@@ -442,6 +486,7 @@ cudaError_t launch_ffn_tc(const TcArgs &a, cudaStream_t s);
 struct RouteArgs {
     const int32_t *ids;
     const float *wts;
+    const float *down_scale;   // [E] or nullptr: multiplies each row's routing weight
     const __nv_bfloat16 *x;
     int T, H, E, k;
     int *counts;        // [E]
@@ -451,7 +496,7 @@ struct RouteArgs {
     int *n_tiles;       // [1]
     int *row_token;     // [T*k]
     float *row_weight;  // [T*k]
-    __nv_bfloat16 *x_perm;  // [T*k][H]
+    __half *x_perm;     // [T*k][H] gathered rows, converted to fp16
     int max_tiles;
 };
 cudaError_t launch_moe_route(const RouteArgs &a, cudaStream_t s);

@@ -59,6 +59,8 @@ def load() -> ctypes.CDLL:
                 "zffn_dequant_fmt": ([I32, P, P, I64, I64, P], I32),
                 "zffn_swiglu_q4k_wd": ([P, P, P, P, I32, P, I32, I32, I32, P], I32),
                 "zffn_moe_swiglu_q4k_wd": ([P, P, P, P, P, P, I32, P, I32, I32, I32, I32, I32, P], I32),
+                "zffn_moe_swiglu_q4k_scaled": ([P, P, P, P, P, P, P, I32, P, I32, I32, I32, I32, I32, I32, P],
+                                               I32),
                 "zffn_rmsnorm_bf16": ([P, P, ctypes.c_float, P, I32, I32, P], I32),
                 "zffn_swiglu_q4k_prenorm_residual": ([P, P, ctypes.c_float, P, P, P, I32, I32, I32, P],
                                                      I32),
@@ -212,6 +214,34 @@ def moe_swiglu_q4k_wd(x: torch.Tensor, expert_ids: torch.Tensor, expert_weights:
         _cuda(expert_weights, "expert_weights", torch.float32), _cuda(Wg, "Wg", torch.uint8),
         _cuda(Wu, "Wu", torch.uint8), _cuda(Wd, "Wd", torch.uint8), int(wd_fmt),
         _cuda(y, "y", torch.float32), T, H, I, E, top_k, _stream(stream)), "zffn_moe_swiglu_q4k_wd")
+    return y
+
+
+def moe_swiglu_q4k_scaled(x: torch.Tensor, expert_ids: torch.Tensor, expert_weights: torch.Tensor,
+                          down_scale: Optional[torch.Tensor], Wg: torch.Tensor, Wu: torch.Tensor,
+                          Wd: torch.Tensor, I: int, E: int, wd_fmt: int = 0,
+                          y: Optional[torch.Tensor] = None, accumulate: bool = False,
+                          stream=None) -> torch.Tensor:
+    """Routed block with a scale on each expert's down projection:
+    y[t] (+)= sum_j w[t, j] * down_scale[ids[t, j]] * FFN_{ids[t, j]}(x[t])
+    (down_scale fp32 [E] or None for all ones; W_down in block format wd_fmt)."""
+    T, H = x.shape
+    top_k = expert_ids.shape[1]
+    if y is None:
+        if accumulate:
+            raise ValueError("accumulate=True needs y")
+        y = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    sc = None
+    if down_scale is not None:
+        if down_scale.numel() != E:
+            raise ValueError("down_scale must hold E values")
+        sc = _cuda(down_scale, "down_scale", torch.float32)
+    _check(load().zffn_moe_swiglu_q4k_scaled(
+        _cuda(x, "x", torch.bfloat16), _cuda(expert_ids, "expert_ids", torch.int32),
+        _cuda(expert_weights, "expert_weights", torch.float32), sc, _cuda(Wg, "Wg", torch.uint8),
+        _cuda(Wu, "Wu", torch.uint8), _cuda(Wd, "Wd", torch.uint8), int(wd_fmt),
+        _cuda(y, "y", torch.float32), T, H, I, E, top_k, int(bool(accumulate)), _stream(stream)),
+        "zffn_moe_swiglu_q4k_scaled")
     return y
 
 

@@ -127,7 +127,11 @@ def test_full_layer_prefill_2048_sampled_rows_with_outliers():
     layer = dense_layer(2, T=2048, outlier_frac=0.01)
     xf = synth.bf16_bits_to_f32(layer["x"])
     outliers = np.nonzero(np.abs(xf).max(axis=1) > 8.0)[0]
-    rows = sorted(set([0, 127, 128, 1000, 2047] + list(outliers[:3])))
+    assert len(outliers) == 20
+    # the first and last row of every 256-token tile, the rows either side of
+    # each tile's 128-row split between the two CTAs of a pair, every outlier row
+    tiles = [r for t in range(0, 2048, 256) for r in (t, t + 127, t + 128, t + 255)]
+    rows = sorted(set(tiles + [1000] + list(outliers)))
     _sampled(layer, 2048, rows)
 
 

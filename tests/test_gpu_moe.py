@@ -97,7 +97,56 @@ def test_full_moe_config_single_token():
 def test_full_moe_config_256_tokens_sampled_rows():
     m = moe_layer(256)
     y = run(m["x"], m["ids"], m["w"], m["Wg"], m["Wu"], m["Wd"], m["I"], m["E"])
-    rows = [0, 1, 17, 100, 128, 200, 255]
+    rows = list(range(0, 256, 16)) + [1, 17, 127, 128, 129, 255]
     ref = orc.moe_swiglu_ffn(m["x"][rows].copy(), m["ids"][rows].copy(), m["w"][rows].copy(),
                              m["Wg"], m["Wu"], m["Wd"], len(rows), m["H"], m["I"], m["E"], m["k"])
     assert_close(y[rows], ref, "moe T=256 sampled")
+
+
+@pytest.mark.parametrize("T,path,fmt", [(1, 1, zffn.FMT_Q4_K), (37, 0, zffn.FMT_Q4_K),
+                                        (1, 1, zffn.FMT_Q5_K), (1, 1, zffn.FMT_Q5_1)])
+def test_per_expert_down_scale(T, path, fmt):
+    # a scale on each expert's down projection, applied inside the routed call
+    E, H, I, k = 8, 512, 384, 3
+    rng = np.random.default_rng(77 + T + fmt)
+    Wg = np.stack([synth.random_q4k_blocks(rng, I, H, 1e-2) for _ in range(E)])
+    Wu = np.stack([synth.random_q4k_blocks(rng, I, H, 1e-2) for _ in range(E)])
+    Wd = np.stack([synth.random_blocks(rng, fmt, H, I, 1e-2) for _ in range(E)])
+    ids, w = routing(31 + T, T, E, k)
+    ids[0, 2] = -1                       # an invalid slot still contributes nothing
+    scale = np.array([1.5, -0.25, 0.0, 2.0, 0.75, 1.0, -3.0, 0.125], dtype=np.float32)
+    x = synth.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    ref = orc.moe_swiglu_ffn(x, ids, w, Wg, Wu, Wd, T, H, I, E, k, wd_fmt=fmt, down_scale=scale)
+    old = zffn.set_option(zffn.OPT_MATVEC_MAX_T, path)
+    try:
+        y = zffn.moe_swiglu_q4k_scaled(x_dev(x), dev(ids), dev(w), dev(scale), dev(Wg), dev(Wu),
+                                       dev(Wd), I, E, wd_fmt=fmt)
+        assert zffn.get_device_error() == zffn.OK
+        assert_close(y, ref, f"down scale T={T} fmt={fmt}")
+        # accumulate: y0 + the scaled block
+        y0 = torch.full((T, H), 0.5, dtype=torch.float32, device="cuda")
+        zffn.moe_swiglu_q4k_scaled(x_dev(x), dev(ids), dev(w), dev(scale), dev(Wg), dev(Wu), dev(Wd),
+                                   I, E, wd_fmt=fmt, y=y0, accumulate=True)
+        assert zffn.get_device_error() == zffn.OK
+        assert_close(y0, ref + 0.5, f"down scale accumulate T={T} fmt={fmt}")
+        # no scale equals the unscaled call
+        y1 = zffn.moe_swiglu_q4k_scaled(x_dev(x), dev(ids), dev(w), None, dev(Wg), dev(Wu), dev(Wd),
+                                        I, E, wd_fmt=fmt)
+        assert zffn.get_device_error() == zffn.OK
+        assert_close(y1, orc.moe_swiglu_ffn(x, ids, w, Wg, Wu, Wd, T, H, I, E, k, wd_fmt=fmt),
+                     f"no scale T={T} fmt={fmt}")
+    finally:
+        zffn.set_option(zffn.OPT_MATVEC_MAX_T, old)
+
+
+def test_per_expert_down_scale_full_config_256_tokens():
+    m = moe_layer(256)
+    scale = np.random.default_rng(8).uniform(0.5, 2.0, m["E"]).astype(np.float32)
+    y = zffn.moe_swiglu_q4k_scaled(x_dev(m["x"]), dev(m["ids"]), dev(m["w"]), dev(scale), dev(m["Wg"]),
+                                   dev(m["Wu"]), dev(m["Wd"]), m["I"], m["E"])
+    assert zffn.get_device_error() == zffn.OK
+    rows = list(range(0, 256, 32)) + [255]
+    ref = orc.moe_swiglu_ffn(m["x"][rows].copy(), m["ids"][rows].copy(), m["w"][rows].copy(),
+                             m["Wg"], m["Wu"], m["Wd"], len(rows), m["H"], m["I"], m["E"], m["k"],
+                             down_scale=scale)
+    assert_close(y[rows], ref, "moe T=256 down scale")
