@@ -348,9 +348,14 @@ zffn_status zffn_get_device_error(void *stream);
 
 /* Tunables (process-wide).  ZFFN_OPT_MATVEC_MAX_T: 1 (default) sends single-token
  * calls (T = 1, dense or routed) to the memory-bound single-token kernel; 0
- * sends every call to the tensor-core kernel (any value > 1 acts as 1).
+ * sends every call to the tensor-core kernels (any value > 1 acts as 1).
+ * ZFFN_OPT_MOE_KERNEL chooses the tensor-core kernel of routed calls: 0
+ * (default) the grouped kernel (groups of 32 gathered rows of one expert, the
+ * weights on the MMA's M side) when T * top_k <= 48 * E and the prefill
+ * kernel on 128-row expert tiles otherwise; 1 always the grouped kernel; 2
+ * always the 128-row tiles.
  * Returns the previous value, or -1 for an unknown key. */
-enum { ZFFN_OPT_MATVEC_MAX_T = 1 };
+enum { ZFFN_OPT_MATVEC_MAX_T = 1, ZFFN_OPT_MOE_KERNEL = 2 };
 int zffn_set_option(int key, int value);
 
 /* Self-test of the bounded-wait machinery: launches one block that waits on an

@@ -26,6 +26,7 @@ std::mutex g_mu;
 DeviceInfo g_info[kMaxDevices];
 Workspace g_ws[kMaxDevices];
 int g_matvec_max_t = 1;
+int g_moe_kernel = 0;   // ZFFN_OPT_MOE_KERNEL
 
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -41,7 +42,8 @@ Layout layout_for(int T, int H, int I, int E, int k) {
     Layout L;
     size_t o = 0;
     const int64_t P = (int64_t)T * k;
-    L.max_tiles = (int)((P + 127) / 128 + (E < P ? E : P));
+    // tiles of at least 32 rows (the grouped kernel's groups; 128 otherwise)
+    L.max_tiles = (int)((P + 31) / 32 + (E < P ? E : P));
     L.h = o; o = align_up(o + (size_t)P * I * sizeof(float));
     L.counts = o; o = align_up(o + (size_t)E * sizeof(int));
     L.offsets = o; o = align_up(o + (size_t)(E + 1) * sizeof(int));
@@ -313,7 +315,17 @@ zffn_status swiglu_moe(const void *x, const int32_t *expert_ids, const float *ex
         a.accumulate = accumulate;
         return to_status(launch_ffn_matvec(a, s));
     }
+    // Few rows per expert: the grouped kernel (weights as the MMA's M side,
+    // each Q4_K byte read once per group of 32 rows).  Many rows per expert:
+    // the prefill kernel on 128-row tiles.
+    int moe_kernel;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        moe_kernel = g_moe_kernel;
+    }
+    const bool grouped = moe_kernel == 1 || (moe_kernel == 0 && (int64_t)T * top_k <= (int64_t)48 * E);
     RouteArgs r{};
+    r.tile_rows = grouped ? moe_group_rows() : 128;
     r.ids = expert_ids;
     r.wts = expert_weights;
     r.down_scale = down_scale;
@@ -348,7 +360,7 @@ zffn_status swiglu_moe(const void *x, const int32_t *expert_ids, const float *ex
     a.n_tiles_host = L.max_tiles;
     a.err = di.err_word;
     a.T = T; a.H = H; a.I = I; a.E = E;
-    return to_status(launch_ffn_tc(a, s));
+    return to_status(grouped ? launch_moe_group(a, s) : launch_ffn_tc(a, s));
 }
 
 }  // namespace
@@ -574,6 +586,11 @@ int zffn_set_option(int key, int value) {
     if (key == ZFFN_OPT_MATVEC_MAX_T) {
         const int old = g_matvec_max_t;
         g_matvec_max_t = value < 0 ? 0 : value;
+        return old;
+    }
+    if (key == ZFFN_OPT_MOE_KERNEL) {
+        const int old = g_moe_kernel;
+        g_moe_kernel = value < 0 || value > 2 ? 0 : value;
         return old;
     }
     return -1;

@@ -175,13 +175,6 @@ struct Tile {
     int row_start, row_count, expert;
 };
 
-// Byte offset of row r in a [rows x 64] bf16 tile laid out K-major with the
-// 128-byte swizzle (groups of 8 rows, 1024 bytes apart); 16-byte chunk c of
-// the row sits at chunk position c ^ (r % 8).
-__device__ __forceinline__ uint32_t sw128_row(int r) {
-    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
-}
-
 // Unpack the 8 code words (32 bytes) of one weight row and K step into its
 // swizzled bf16 row.  Word i holds code bytes 4i..4i+3: low nibbles are
 // weights 4i..4i+3 of the step, high nibbles weights 32+4i..32+4i+3.  A code
@@ -274,51 +267,6 @@ __device__ __forceinline__ void unpack_row_to_smem(uint4 hd, const uint32_t (&w)
                                                    int row) {
     if (PAIR) unpack_row_to_smem_wide(hd, w, g, row_addr, row);
     else unpack_row_to_smem_narrow(hd, w, g, row_addr, row);
-}
-
-// The gate/up operands are fp16: unpack the 8 code words of one weight row and
-// K step into its swizzled fp16 row.  Each code pair becomes (q0, q1) * 2^-9
-// exactly (codes_to_f16x2), and one fused fp16 multiply-add per pair gives
-//     w = (q * 2^-9) * fp16(512 d sc) - fp16(dmin m),
-// rounded once to fp16 (11-bit significand): the sub-block's scale and offset
-// are rounded to fp16 first (relative error <= 2^-11 each), far below the
-// bf16 rounding the down projection's operands get.  d*sc*512 and dmin*m are
-// exact in fp32 before that rounding; values beyond the fp16 range saturate
-// at +-65504 (|d * sc| > 128 or |dmin * m| > 65504: far outside any
-// quantised weight).  Chunks are stored as soon as they are formed.
-__device__ __forceinline__ void unpack_row_to_smem_f16(uint4 hd, const uint32_t (&w)[8], int g,
-                                                       uint32_t row_addr, int row) {
-    const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
-    int sc0, m0, sc1, m1;
-    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g, sc0, m0);
-    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g + 1, sc1, m1);
-    const uint32_t a0 = f16x2_splat_satfinite(512.0f * (d * (float)sc0));
-    const uint32_t b0 = f16x2_splat_satfinite(-(dmin * (float)m0));
-    const uint32_t a1 = f16x2_splat_satfinite(512.0f * (d * (float)sc1));
-    const uint32_t b1 = f16x2_splat_satfinite(-(dmin * (float)m1));
-    constexpr uint32_t NIB = 0x0F0F0F0Fu;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        // words 2c, 2c+1: low nibbles are weights 8c..8c+7 of sub-block 2g,
-        // high nibbles weights 32+8c..32+8c+7 of sub-block 2g+1
-        const uint32_t l0 = w[2 * c] & NIB, l1 = w[2 * c + 1] & NIB;
-        const uint32_t h0 = (w[2 * c] >> 4) & NIB, h1 = (w[2 * c + 1] >> 4) & NIB;
-        st_shared_v4(row_addr + (((uint32_t)(c ^ (row & 7))) << 4),
-                     fma_f16x2(codes_to_f16x2(l0), a0, b0), fma_f16x2(codes_to_f16x2(l0 >> 16), a0, b0),
-                     fma_f16x2(codes_to_f16x2(l1), a0, b0), fma_f16x2(codes_to_f16x2(l1 >> 16), a0, b0));
-        st_shared_v4(row_addr + (((uint32_t)((c + 4) ^ (row & 7))) << 4),
-                     fma_f16x2(codes_to_f16x2(h0), a1, b1), fma_f16x2(codes_to_f16x2(h0 >> 16), a1, b1),
-                     fma_f16x2(codes_to_f16x2(h1), a1, b1), fma_f16x2(codes_to_f16x2(h1 >> 16), a1, b1));
-    }
-}
-
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
 }
 
 // Work-unit geometry shared by every role.

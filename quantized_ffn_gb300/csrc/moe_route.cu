@@ -6,9 +6,10 @@
 // themselves).
 //
 //   route kernel (one block): count pairs per expert, exclusive scan into
-//     row offsets, cut every expert's rows into tiles of at most 128 rows
-//     (the tensor-core kernel's M), record for each gathered row its token and
-//     routing weight.  Pairs with an id outside [0, E) are dropped.
+//     row offsets, cut every expert's rows into tiles of at most tile_rows rows
+//     (128, the prefill kernel's M, or 32, the grouped kernel's N), record for
+//     each gathered row its token and routing weight.  Pairs with an id outside
+//     [0, E) are dropped.
 //   gather kernel: copy the x row of every gathered row into a contiguous
 //     buffer, converted to fp16 (the tensor-core kernel's gate/up operand type),
 //     so that the tensor-core kernel can load expert tiles with TMA.
@@ -17,7 +18,6 @@
 namespace zffn {
 
 constexpr int kRouteThreads = 1024;
-constexpr int kTileRows = 128;
 
 // Exclusive scan of v[0..n) in shared memory by one block; returns the total.
 __device__ int block_exclusive_scan(int *v, int n, int *scratch) {
@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
     __syncthreads();
     for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
         off[e] = cnt[e];
-        tix[e] = (cnt[e] + kTileRows - 1) / kTileRows;
+        tix[e] = (cnt[e] + a.tile_rows - 1) / a.tile_rows;
         a.counts[e] = cnt[e];
     }
     __syncthreads();
@@ -70,11 +70,11 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
     const int n_tiles = block_exclusive_scan(tix, a.E, scratch);
     for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
         a.offsets[e] = off[e];
-        const int nt = (cnt[e] + kTileRows - 1) / kTileRows;
+        const int nt = (cnt[e] + a.tile_rows - 1) / a.tile_rows;
         for (int t = 0; t < nt; ++t) {
             const int ti = tix[e] + t;
             if (ti < a.max_tiles)
-                a.tiles[ti] = make_int4(off[e] + t * kTileRows, min(kTileRows, cnt[e] - t * kTileRows), e, 0);
+                a.tiles[ti] = make_int4(off[e] + t * a.tile_rows, min(a.tile_rows, cnt[e] - t * a.tile_rows), e, 0);
         }
         cnt[e] = off[e];                 // becomes the fill cursor
     }

@@ -1,0 +1,509 @@
+// moe_tc.cu -- the routed layer's tensor-core kernel for few tokens per expert.
+//
+// In a routed layer each expert sees only the tokens routed to it -- at the
+// routed workload's 256 tokens, top-8 of 128 experts, about 16 per expert --
+// so the expert's weights, streamed once from memory, meet a handful of token
+// rows ("Four bottlenecks, one CUDA backend...", section "Bottleneck 2 -- MoE
+// decode was paying for its routing twice": one batched call over the chosen
+// experts, ids read on the device).  Here the weights are the MMA's M side
+// (128 rows per UMMA) and an expert's group of up to 32 gathered token rows
+// its N side, so every unpacked weight feeds only useful products and every
+// Q4_K byte is read once per group:
+//
+//   for each 128-row block of the expert's intermediate chunk:
+//       G = Wg_blk . Xg^T,  U = Wu_blk . Xg^T            (TMEM, [128 x 32])
+//       h[:, blk] = fp16(silu(G) * U * 2^-8)               (epilogue -> SMEM)
+//   for each 128-row block of the output:
+//       Y = Wd_blk[:, chunk] . h^T                         (TMEM, [128 x 32])
+//       y[token, blk] += weight * 2^8 * Y                  (fp32 reductions)
+//
+// Both products take fp16 operands: x (converted when it is gathered), the
+// weights unpacked with the fp8 -> fp16 converter (zffn_internal.cuh), and the
+// intermediate scaled by 2^-8 so that its fp16 range reaches 1.7e7 (values
+// beyond saturate).  The SwiGLU intermediate of a group never leaves the SM.
+//
+// Block roles (24 warps):
+//   warps 0-3   epilogue for TMEM lane quadrants 0-3: SwiGLU -> h, Y -> y
+//   warp 4      TMEM allocator and MMA issuer (one elected lane issues)
+//   warp 5      TMA producer: whole Q4_K blocks of 128 weight rows (one box
+//               per matrix covers four K steps)
+//   warp 6      TMA producer: the group's x tiles [32 x 64] fp16
+//   warps 8-23  unpackers, four groups of four warps taking tasks in turn
+//   warp 7      idle
+#include <cudaTypedefs.h>
+
+#include "zffn_internal.cuh"
+
+namespace zffn {
+namespace mg {
+
+constexpr int NG = 32;                       // token rows of a group (UMMA N)
+constexpr int BM = 128;                      // weight rows of a UMMA (M)
+constexpr int BK = 64;                       // K per step
+constexpr int KSB = 4;                       // K steps per packed block step (256 weights)
+constexpr int IC_MAX = 768;                  // intermediate columns of a work unit
+constexpr int NUM_WARPS = 24;
+constexpr int THREADS = NUM_WARPS * 32;
+constexpr int UNPACK_GROUPS = 4;
+constexpr int NR = 2, NA = 2, NX = 8;        // packed, unpacked, x stages
+constexpr int R_BOX = BM * kBlockBytes;      // one whole-block box of 128 rows: 18432 bytes
+constexpr int R_BYTES = 2 * R_BOX;           // gate + up (the down phase uses the first half)
+constexpr int A_TILE = BM * BK * 2;          // [128 x 64] fp16
+constexpr int A_BYTES = 2 * A_TILE;          // gate + up (the down phase uses the first)
+constexpr int X_BYTES = NG * BK * 2;         // [32 x 64] fp16
+constexpr int H_TILE = NG * BK * 2;          // h columns [64j, 64j + 64) of the group
+constexpr int H_BYTES = (IC_MAX / BK) * H_TILE;
+constexpr int OFF_R = 0;
+constexpr int OFF_A = OFF_R + NR * R_BYTES;
+constexpr int OFF_X = OFF_A + NA * A_BYTES;
+constexpr int OFF_H = OFF_X + NX * X_BYTES;
+constexpr int OFF_BAR = OFF_H + H_BYTES;
+constexpr int N_BARS = 2 * NR + 2 * NA + 2 * NX + 4 + 4 + 2;
+constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + alignment slack
+static_assert(OFF_A % 1024 == 0 && OFF_X % 1024 == 0 && OFF_H % 1024 == 0, "swizzled tiles 1024-aligned");
+static_assert(SMEM_BYTES <= 232448, "shared memory budget of one block");
+static_assert(NG == 32, "one group row per lane of an epilogue warp");
+// TMEM columns: gate / up / down accumulators, two of each
+constexpr uint32_t COL_G = 0, COL_U = 2 * NG, COL_Y = 4 * NG, TMEM_COLS = 256;
+constexpr uint32_t IDESC = idesc_f16_f32(BM, NG);
+constexpr float H_SCALE = 1.0f / 256.0f;     // the intermediate is held as h * 2^-8
+
+enum Role { ROLE_EPI, ROLE_MMA, ROLE_WPROD, ROLE_XPROD, ROLE_UNPACK, ROLE_IDLE };
+__device__ __forceinline__ int warp_role(int w) {
+    if (w < 4) return ROLE_EPI;
+    if (w == 4) return ROLE_MMA;
+    if (w == 5) return ROLE_WPROD;
+    if (w == 6) return ROLE_XPROD;
+    if (w >= 8) return ROLE_UNPACK;
+    return ROLE_IDLE;
+}
+
+struct Maps {
+    CUtensorMap x;             // gathered rows, fp16 [P][H], boxes [32 rows x 64]
+    CUtensorMap wg, wu, wd;    // byte matrices, boxes [128 rows x 144 bytes]
+};
+
+struct Params {
+    float *y;
+    const int4 *tiles;         // {row_start, row_count, expert, 0}
+    const int *n_tiles_dev;
+    const int *row_token;
+    const float *row_weight;
+    int *err;
+    int n_tiles_host;
+    int H, I;
+};
+
+// Geometry of one work unit (a group of one expert's rows, one chunk of its
+// intermediate width).  Both phases run over whole Q4_K blocks of the chunk:
+// rows of the chunk past its width unpack as zeros (h = 0 there), so the down
+// phase may run over the partial last block.
+struct Unit {
+    int row_start, rows, expert;
+    int i0, ic;                // chunk start and width
+    int n_ib, ks_g;            // 128-row intermediate blocks, K steps of each
+    int n_hb, ks_y;            // 128-row output blocks, K steps of each
+};
+
+__device__ __forceinline__ Unit make_unit(const Params &p, int u, int n_tiles) {
+    Unit un;
+    const int t = u % n_tiles, c = u / n_tiles;
+    const int4 v = p.tiles[t];
+    un.row_start = v.x;
+    un.rows = v.y;
+    un.expert = v.z;
+    un.i0 = c * IC_MAX;
+    un.ic = min(IC_MAX, p.I - un.i0);
+    const int nb = (un.ic + 255) / 256;
+    un.n_ib = 2 * nb;
+    un.ks_g = p.H / BK;
+    un.n_hb = p.H / BM;
+    un.ks_y = KSB * nb;
+    return un;
+}
+
+__global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_constant__ Maps maps, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
+    uint64_t *r_full = bars, *r_empty = bars + NR;
+    uint64_t *a_full = bars + 2 * NR, *a_empty = a_full + NA;
+    uint64_t *x_full = a_empty + NA, *x_empty = x_full + NX;
+    uint64_t *g_full = x_empty + NX, *g_empty = g_full + 2;
+    uint64_t *y_full = g_empty + 2, *y_empty = y_full + 2;
+    uint64_t *h_full = y_empty + 2, *drain = h_full + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + N_BARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int role = warp_role(warp);
+    const uint32_t s_r = smem_u32(smem + OFF_R), s_a = smem_u32(smem + OFF_A);
+    const uint32_t s_x = smem_u32(smem + OFF_X), s_h = smem_u32(smem + OFF_H);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NR; ++i) {
+            mbar_init(&r_full[i], 1);
+            mbar_init(&r_empty[i], 2 * KSB * 4);      // 4 K steps x 2 tasks x 4 warps
+        }
+        for (int i = 0; i < NA; ++i) {
+            mbar_init(&a_full[i], 2 * 4);             // 2 tasks x 4 warps
+            mbar_init(&a_empty[i], 1);
+        }
+        for (int i = 0; i < NX; ++i) {
+            mbar_init(&x_full[i], 1);
+            mbar_init(&x_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&g_full[i], 1);
+            mbar_init(&g_empty[i], 4);
+            mbar_init(&y_full[i], 1);
+            mbar_init(&y_empty[i], 4);
+        }
+        mbar_init(h_full, 4);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        prefetch_tensormap(&maps.x);
+        prefetch_tensormap(&maps.wg);
+        prefetch_tensormap(&maps.wu);
+        prefetch_tensormap(&maps.wd);
+    }
+    if (role == ROLE_MMA) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int n_tiles = min(*p.n_tiles_dev, p.n_tiles_host);
+    const int n_chunks = (p.I + IC_MAX - 1) / IC_MAX;
+    const int n_units = n_tiles * n_chunks;
+    const int m_units = (int)blockIdx.x < n_units
+                            ? (n_units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    auto unit_of = [&](int k) { return make_unit(p, (int)blockIdx.x + k * (int)gridDim.x, n_tiles); };
+
+    if (role == ROLE_WPROD) {
+        // ------------- TMA producer: whole Q4_K blocks of 128 weight rows -------------
+        if (lane == 0) {
+            uint32_t ri = 0, rph = 0, issued = 0;
+            bool ok = true;
+            for (int k = 0; k < m_units && ok; ++k) {
+                const Unit un = unit_of(k);
+                const int nbs_g = un.ks_g / KSB, nbs_y = un.ks_y / KSB;
+                for (int b = 0; b < un.n_ib * nbs_g + un.n_hb * nbs_y; ++b) {
+                    if (!mbar_wait(&r_empty[ri], rph ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    uint8_t *rs = smem + OFF_R + ri * R_BYTES;
+                    if (b < un.n_ib * nbs_g) {
+                        const int ib = b / nbs_g, kb = b % nbs_g;
+                        const int row = un.expert * p.I + un.i0 + ib * BM;
+                        mbar_arrive_expect_tx(&r_full[ri], 2 * R_BOX);
+                        tma_load_2d(rs, &maps.wg, &r_full[ri], kb * kBlockBytes, row);
+                        tma_load_2d(rs + R_BOX, &maps.wu, &r_full[ri], kb * kBlockBytes, row);
+                    } else {
+                        const int bb = b - un.n_ib * nbs_g;
+                        const int hb = bb / nbs_y, kb = bb % nbs_y;
+                        const int row = un.expert * p.H + hb * BM;
+                        mbar_arrive_expect_tx(&r_full[ri], R_BOX);
+                        tma_load_2d(rs, &maps.wd, &r_full[ri], (un.i0 / 256 + kb) * kBlockBytes, row);
+                    }
+                    ++issued;
+                    if (++ri == NR) { ri = 0; rph ^= 1; }
+                }
+            }
+            // every load issued here lands before the block may exit
+            for (uint32_t i = 0; i < (uint32_t)NR && i < issued; ++i) {
+                if (ri == 0) { ri = NR; rph ^= 1; }
+                --ri;
+                mbar_wait(&r_full[ri], rph, nullptr, p.err, kWaitBudgetCycles / 8);
+            }
+        }
+    } else if (role == ROLE_XPROD) {
+        // ------------- TMA producer: x tiles of the group, one per gate/up K step -------------
+        if (lane == 0) {
+            uint32_t xi = 0, xph = 0, issued = 0;
+            bool ok = true;
+            for (int k = 0; k < m_units && ok; ++k) {
+                const Unit un = unit_of(k);
+                for (int s = 0; s < un.n_ib * un.ks_g; ++s) {
+                    const int ks = s % un.ks_g;
+                    if (!mbar_wait(&x_empty[xi], xph ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&x_full[xi], X_BYTES);
+                    tma_load_2d(smem + OFF_X + xi * X_BYTES, &maps.x, &x_full[xi], ks * BK, un.row_start);
+                    ++issued;
+                    if (++xi == NX) { xi = 0; xph ^= 1; }
+                }
+            }
+            for (uint32_t i = 0; i < (uint32_t)NX && i < issued; ++i) {
+                if (xi == 0) { xi = NX; xph ^= 1; }
+                --xi;
+                mbar_wait(&x_full[xi], xph, nullptr, p.err, kWaitBudgetCycles / 8);
+            }
+        }
+    } else if (role == ROLE_MMA) {
+        // ---------------- MMA issuer ----------------
+        const bool issuer = elect_one();
+        uint32_t ai = 0, aph = 0, xi = 0, xph = 0;
+        uint32_t gb = 0, gph = 0, yb = 0, yph = 0;   // buffer index, per-buffer parity bits
+        bool ok = true;
+        auto commit = [&](uint64_t *bar) {
+            if (issuer) tc_commit(bar);
+        };
+        const uint64_t da0 = smem_desc_k_sw128(s_a), dx0 = smem_desc_k_sw128(s_x);
+        const uint64_t dh0 = smem_desc_k_sw128(s_h);
+        for (int k = 0; k < m_units && ok; ++k) {
+            const Unit un = unit_of(k);
+            for (int ib = 0; ib < un.n_ib && ok; ++ib) {
+                for (int ks = 0; ks < un.ks_g; ++ks) {
+                    if (ks == 0) {
+                        if (!mbar_wait(&g_empty[gb], ((gph >> gb) & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    }
+                    if (!mbar_wait(&a_full[ai], aph, abort_flag, p.err) ||
+                        !mbar_wait(&x_full[xi], xph, abort_flag, p.err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t da = da0 + (uint64_t)((ai * A_BYTES) >> 4);
+                    const uint64_t dx = dx0 + (uint64_t)((xi * X_BYTES) >> 4);
+                    if (issuer) {
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            tc_mma_bf16(tmem_base + COL_G + gb * NG, da + 2 * kk, dx + 2 * kk, IDESC,
+                                        (ks | kk) != 0);
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            tc_mma_bf16(tmem_base + COL_U + gb * NG, da + (A_TILE >> 4) + 2 * kk, dx + 2 * kk,
+                                        IDESC, (ks | kk) != 0);
+                    }
+                    commit(&a_empty[ai]);
+                    commit(&x_empty[xi]);
+                    if (++ai == NA) { ai = 0; aph ^= 1; }
+                    if (++xi == NX) { xi = 0; xph ^= 1; }
+                    if (ks == un.ks_g - 1) {
+                        commit(&g_full[gb]);
+                        gph ^= 1u << gb;
+                        gb ^= 1;
+                    }
+                }
+            }
+            for (int hb = 0; hb < un.n_hb && ok; ++hb) {
+                for (int ks = 0; ks < un.ks_y; ++ks) {
+                    if (ks == 0) {
+                        // the unit's h is complete in shared memory before its first down step
+                        if (hb == 0 && !mbar_wait(h_full, (uint32_t)k & 1, abort_flag, p.err)) { ok = false; break; }
+                        if (!mbar_wait(&y_empty[yb], ((yph >> yb) & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    }
+                    if (!mbar_wait(&a_full[ai], aph, abort_flag, p.err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t da = da0 + (uint64_t)((ai * A_BYTES) >> 4);
+                    const uint64_t dh = dh0 + (uint64_t)((ks * H_TILE) >> 4);
+                    if (issuer) {
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            tc_mma_bf16(tmem_base + COL_Y + yb * NG, da + 2 * kk, dh + 2 * kk, IDESC,
+                                        (ks | kk) != 0);
+                    }
+                    commit(&a_empty[ai]);
+                    if (++ai == NA) { ai = 0; aph ^= 1; }
+                    if (ks == un.ks_y - 1) {
+                        commit(&y_full[yb]);
+                        yph ^= 1u << yb;
+                        yb ^= 1;
+                    }
+                }
+            }
+        }
+        // every MMA issued here completes before TMEM is released
+        commit(drain);
+        __syncwarp();
+        mbar_wait(drain, 0, nullptr, p.err, kWaitBudgetCycles / 8);
+    } else if (role == ROLE_UNPACK) {
+        // ------------- weight unpackers (four groups of 4 warps) -------------
+        // Every K step has two 128-thread tasks: the gate rows and the up rows
+        // (gate/up phase), or the low and the high nibbles of the 128 W_down
+        // rows (down phase).  Group g takes the tasks with index g modulo 4,
+        // counted over the whole program of this block, so groups 0-1 always
+        // fill the even K steps' stage and groups 2-3 the odd ones'.
+        const int uw = warp - 8;
+        const uint32_t grp = (uint32_t)(uw / 4);
+        const int r = (uw % 4) * 32 + lane;             // weight row within the task
+        uint32_t kstep = 0;                              // K steps of the program so far
+        bool ok = true;
+        for (int k = 0; k < m_units && ok; ++k) {
+            const Unit un = unit_of(k);
+            const int n_g = un.n_ib * un.ks_g, n_steps = n_g + un.n_hb * un.ks_y;
+            for (int s = 0; s < n_steps && ok; ++s, ++kstep) {
+#pragma unroll
+                for (int task = 0; task < 2; ++task) {
+                    if (((2 * kstep + task) & (UNPACK_GROUPS - 1)) != grp) continue;
+                    const bool gu = s < n_g;
+                    const int ks = gu ? s % un.ks_g : (s - n_g) % un.ks_y;
+                    const uint32_t bs = kstep / KSB;         // packed block step
+                    const uint32_t ri = bs % NR, rph = (bs / NR) & 1;
+                    const uint32_t ai = kstep % NA, aph = (kstep / NA) & 1;
+                    const bool zero = gu && (s / un.ks_g) * BM + r >= un.ic;
+                    if (!mbar_wait(&r_full[ri], rph, abort_flag, p.err)) { ok = false; break; }
+                    uint4 hd = make_uint4(0, 0, 0, 0), q0 = hd, q1 = hd;
+                    if (!zero) {
+                        const uint32_t src = s_r + ri * R_BYTES + (gu ? task * R_BOX : 0) + r * kBlockBytes;
+                        hd = ld_shared_v4(src);
+                        q0 = ld_shared_v4(src + 16 + 32 * (ks & 3));
+                        q1 = ld_shared_v4(src + 32 + 32 * (ks & 3));
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&r_empty[ri]);
+                    if (!mbar_wait(&a_empty[ai], aph ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    const uint32_t w8[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                    const uint32_t dst = s_a + ai * A_BYTES + (gu ? task * A_TILE : 0) + sw128_row(r);
+                    if (gu) unpack_row_to_smem_f16(hd, w8, ks & 3, dst, r);
+                    else unpack_half_row_to_smem_f16(hd, w8, ks & 3, task, dst, r);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&a_full[ai]);
+                }
+            }
+        }
+    } else if (role == ROLE_EPI) {
+        // ---------------- epilogue (4 warps) ----------------
+        const int q = warp;                           // TMEM lane quadrant of this warp
+        const uint32_t t_lane = tmem_base + ((uint32_t)(q * 32) << 16);
+        uint32_t gb = 0, gph = 0, yb = 0, yph = 0;
+        bool ok = true;
+        for (int k = 0; k < m_units && ok; ++k) {
+            const Unit un = unit_of(k);
+            // the group's rows: lane t holds row t's token and routing weight
+            // (NG == 32: one row per lane), broadcast by shuffles below
+            const bool v = lane < un.rows;
+            const int my_tok = v ? p.row_token[un.row_start + lane] : 0;
+            const float my_w = v ? p.row_weight[un.row_start + lane] * 256.0f : 0.0f;
+            // ---- gate/up blocks: h = silu(G) * U, scaled, to shared memory
+            for (int ib = 0; ib < un.n_ib; ++ib) {
+                if (!mbar_wait(&g_full[gb], (gph >> gb) & 1, abort_flag, p.err)) { ok = false; break; }
+                tc_fence_after();
+                const int i = ib * BM + q * 32 + lane;        // intermediate column within the chunk
+                const uint32_t hrow = s_h + (uint32_t)(i >> 6) * H_TILE + (uint32_t)(i & 7) * 2;
+                const uint32_t chunk = (uint32_t)((i & 63) >> 3);
+#pragma unroll
+                for (int c = 0; c < NG; c += 16) {
+                    uint32_t gr[16], ur[16];
+                    tmem_ld_32x32b_x16(t_lane + COL_G + gb * NG + c, gr);
+                    tmem_ld_32x32b_x16(t_lane + COL_U + gb * NG + c, ur);
+                    tmem_ld_wait(gr);
+                    tmem_ld_wait(ur);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int t = c + j;
+                        const float g = __uint_as_float(gr[j]), u = __uint_as_float(ur[j]);
+                        const float h = __fdividef(g * u * H_SCALE, 1.0f + __expf(-g));
+                        uint16_t hb16;
+                        asm("cvt.rn.satfinite.f16.f32 %0, %1;" : "=h"(hb16) : "f"(h));
+                        const uint32_t addr = hrow + (uint32_t)t * 128 + ((chunk ^ (uint32_t)(t & 7)) << 4);
+                        asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(hb16) : "memory");
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&g_empty[gb]);
+                    if (ib == un.n_ib - 1) mbar_arrive(h_full);
+                }
+                gph ^= 1u << gb;
+                gb ^= 1;
+            }
+            // ---- down blocks: y[token, row] += weight * 2^8 * Y
+            for (int hb = 0; hb < un.n_hb && ok; ++hb) {
+                if (!mbar_wait(&y_full[yb], (yph >> yb) & 1, abort_flag, p.err)) { ok = false; break; }
+                tc_fence_after();
+                const int row = hb * BM + q * 32 + lane;      // output column
+#pragma unroll
+                for (int c = 0; c < NG; c += 16) {
+                    uint32_t yr[16];
+                    tmem_ld_32x32b_x16(t_lane + COL_Y + yb * NG + c, yr);
+                    tmem_ld_wait(yr);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int t = c + j;
+                        const int tok = __shfl_sync(0xffffffffu, my_tok, t);
+                        const float wt = __shfl_sync(0xffffffffu, my_w, t);
+                        if (t < un.rows) {
+                            float *dst = p.y + (int64_t)tok * p.H + row;
+                            asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst), "f"(__uint_as_float(yr[j]) * wt)
+                                         : "memory");
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&y_empty[yb]);
+                yph ^= 1u << yb;
+                yb ^= 1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (role == ROLE_MMA) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace mg
+
+static bool encode_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *m, CUtensorMapDataType dt,
+                       const void *base, int64_t inner, int64_t rows, int64_t row_pitch, int box_inner,
+                       int box_rows, CUtensorMapSwizzle sw) {
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_pitch};
+    const cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int moe_group_rows() { return mg::NG; }
+
+cudaError_t launch_moe_group(const TcArgs &a, cudaStream_t s) {
+    const DeviceInfo &di = device_info();
+    if (a.H % 256 != 0 || a.I % 64 != 0) return cudaErrorInvalidValue;
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qr) !=
+            cudaSuccess || qr != cudaDriverEntryPointSuccess)
+        return cudaErrorNotSupported;
+    auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    mg::Maps maps;
+    const int64_t rbH = q4k_row_bytes(a.H), rbI = q4k_row_bytes(a.I);
+    if (!encode_map(encode, &maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.x, a.H, a.x_rows, (int64_t)a.H * 2,
+                    mg::BK, mg::NG, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_map(encode, &maps.wg, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wg, rbH, (int64_t)a.E * a.I, rbH,
+                    kBlockBytes, mg::BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_map(encode, &maps.wu, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wu, rbH, (int64_t)a.E * a.I, rbH,
+                    kBlockBytes, mg::BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_map(encode, &maps.wd, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wd, rbI, (int64_t)a.E * a.H, rbI,
+                    kBlockBytes, mg::BM, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    cudaError_t e = ensure_dynamic_smem((const void *)mg::moe_group_kernel, (size_t)mg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    mg::Params p;
+    p.y = a.y;
+    p.tiles = a.tiles;
+    p.n_tiles_dev = a.n_tiles_dev;
+    p.row_token = a.row_token;
+    p.row_weight = a.row_weight;
+    p.err = a.err;
+    p.n_tiles_host = a.n_tiles_host;
+    p.H = a.H;
+    p.I = a.I;
+    const int n_chunks = (a.I + mg::IC_MAX - 1) / mg::IC_MAX;
+    int64_t grid = (int64_t)a.n_tiles_host * n_chunks;
+    if (grid > di.num_sms) grid = di.num_sms;
+    if (grid < 1) return cudaSuccess;
+    mg::moe_group_kernel<<<(unsigned)grid, mg::THREADS, mg::SMEM_BYTES, s>>>(maps, p);
+    return cudaGetLastError();
+}
+
+}  // namespace zffn

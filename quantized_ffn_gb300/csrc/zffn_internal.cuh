@@ -418,6 +418,82 @@ __device__ __forceinline__ uint4 ld_global_nc_v4(const void *p) {
 }
 
 // ---------------------------------------------------------------------------
+// Q4_K -> fp16 operand tiles of the tensor-core kernels.
+// ---------------------------------------------------------------------------
+// Byte offset of row r in a [rows x 64] bf16 tile laid out K-major with the
+// 128-byte swizzle (groups of 8 rows, 1024 bytes apart); 16-byte chunk c of
+// the row sits at chunk position c ^ (r % 8).
+__device__ __forceinline__ uint32_t sw128_row(int r) {
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// Unpack the 8 code words of one Q4_K weight row and K step (64 weights of
+// sub-blocks 2g and 2g+1) into its swizzled fp16 row (128-byte swizzle).  Each code pair becomes (q0, q1) * 2^-9
+// exactly (codes_to_f16x2), and one fused fp16 multiply-add per pair gives
+//     w = (q * 2^-9) * fp16(512 d sc) - fp16(dmin m),
+// rounded once to fp16 (11-bit significand): the sub-block's scale and offset
+// are rounded to fp16 first (relative error <= 2^-11 each), far below the
+// bf16 rounding the down projection's operands get.  d*sc*512 and dmin*m are
+// exact in fp32 before that rounding; values beyond the fp16 range saturate
+// at +-65504 (|d * sc| > 128 or |dmin * m| > 65504: far outside any
+// quantised weight).  Chunks are stored as soon as they are formed.
+__device__ __forceinline__ void unpack_row_to_smem_f16(uint4 hd, const uint32_t (&w)[8], int g,
+                                                       uint32_t row_addr, int row) {
+    const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
+    int sc0, m0, sc1, m1;
+    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g, sc0, m0);
+    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g + 1, sc1, m1);
+    const uint32_t a0 = f16x2_splat_satfinite(512.0f * (d * (float)sc0));
+    const uint32_t b0 = f16x2_splat_satfinite(-(dmin * (float)m0));
+    const uint32_t a1 = f16x2_splat_satfinite(512.0f * (d * (float)sc1));
+    const uint32_t b1 = f16x2_splat_satfinite(-(dmin * (float)m1));
+    constexpr uint32_t NIB = 0x0F0F0F0Fu;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        // words 2c, 2c+1: low nibbles are weights 8c..8c+7 of sub-block 2g,
+        // high nibbles weights 32+8c..32+8c+7 of sub-block 2g+1
+        const uint32_t l0 = w[2 * c] & NIB, l1 = w[2 * c + 1] & NIB;
+        const uint32_t h0 = (w[2 * c] >> 4) & NIB, h1 = (w[2 * c + 1] >> 4) & NIB;
+        st_shared_v4(row_addr + (((uint32_t)(c ^ (row & 7))) << 4),
+                     fma_f16x2(codes_to_f16x2(l0), a0, b0), fma_f16x2(codes_to_f16x2(l0 >> 16), a0, b0),
+                     fma_f16x2(codes_to_f16x2(l1), a0, b0), fma_f16x2(codes_to_f16x2(l1 >> 16), a0, b0));
+        st_shared_v4(row_addr + (((uint32_t)((c + 4) ^ (row & 7))) << 4),
+                     fma_f16x2(codes_to_f16x2(h0), a1, b1), fma_f16x2(codes_to_f16x2(h0 >> 16), a1, b1),
+                     fma_f16x2(codes_to_f16x2(h1), a1, b1), fma_f16x2(codes_to_f16x2(h1 >> 16), a1, b1));
+    }
+}
+
+// One sub-block (32 weights) of the same row and K step: hi = 0 takes the low
+// nibbles of the 8 code words (sub-block 2g: 16-byte chunks 0-3 of the row),
+// hi = 1 the high nibbles (sub-block 2g+1: chunks 4-7).
+__device__ __forceinline__ void unpack_half_row_to_smem_f16(uint4 hd, const uint32_t (&w)[8], int g,
+                                                            int hi, uint32_t row_addr, int row) {
+    const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
+    int sc, m;
+    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g + hi, sc, m);
+    const uint32_t a = f16x2_splat_satfinite(512.0f * (d * (float)sc));
+    const uint32_t b = f16x2_splat_satfinite(-(dmin * (float)m));
+    constexpr uint32_t NIB = 0x0F0F0F0Fu;
+    const int sh = 4 * hi;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t v0 = (w[2 * c] >> sh) & NIB, v1 = (w[2 * c + 1] >> sh) & NIB;
+        st_shared_v4(row_addr + (((uint32_t)((c + 4 * hi) ^ (row & 7))) << 4),
+                     fma_f16x2(codes_to_f16x2(v0), a, b), fma_f16x2(codes_to_f16x2(v0 >> 16), a, b),
+                     fma_f16x2(codes_to_f16x2(v1), a, b), fma_f16x2(codes_to_f16x2(v1 >> 16), a, b));
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Host-side launchers (defined in the kernel translation units).
 // ---------------------------------------------------------------------------
 struct DeviceInfo {
@@ -480,6 +556,10 @@ struct TcArgs {
     int E;                       // experts stacked in Wg/Wu/Wd (dense: 1)
 };
 cudaError_t launch_ffn_tc(const TcArgs &a, cudaStream_t s);
+// Routed layer with few rows per expert: groups of at most moe_group_rows()
+// gathered rows of one expert, weights as the MMA's M side (moe_tc.cu).
+int moe_group_rows();
+cudaError_t launch_moe_group(const TcArgs &a, cudaStream_t s);
 
 // MoE routing on the device: bucket (token, slot) pairs by expert, build the
 // tile table and the row maps, gather x rows per expert.
@@ -498,6 +578,7 @@ struct RouteArgs {
     float *row_weight;  // [T*k]
     __half *x_perm;     // [T*k][H] gathered rows, converted to fp16
     int max_tiles;
+    int tile_rows;      // rows per tile: 128 (prefill kernel) or the grouped kernel's group
 };
 cudaError_t launch_moe_route(const RouteArgs &a, cudaStream_t s);
 

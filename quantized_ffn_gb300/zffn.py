@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libzffn.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_NO_WORKSPACE = range(6)
 OPT_MATVEC_MAX_T = 1
+OPT_MOE_KERNEL = 2
 
 _lock = threading.Lock()
 _lib = None

@@ -150,3 +150,37 @@ def test_per_expert_down_scale_full_config_256_tokens():
                              m["Wg"], m["Wu"], m["Wd"], len(rows), m["H"], m["I"], m["E"], m["k"],
                              down_scale=scale)
     assert_close(y[rows], ref, "moe T=256 down scale")
+
+
+@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("T,E,H,I,k", [(40, 8, 512, 384, 2), (300, 16, 256, 704, 4), (5, 32, 1024, 256, 8),
+                                       (64, 4, 256, 2048, 3), (200, 3, 512, 192, 2), (1, 8, 512, 384, 2)])
+def test_both_routed_tensor_core_kernels(kernel, T, E, H, I, k):
+    # kernel 1: groups of 32 rows of one expert, weights on the MMA's M side;
+    # kernel 2: 128-row expert tiles on the prefill kernel.  Shapes cover a
+    # partial last W_down block (I = 704, 192), several intermediate chunks
+    # (I = 2048), experts with more than one group (T * k / E = 200).
+    Wg, Wu, Wd = experts(T + 3 * E + I, E, H, I)
+    ids, w = routing(T * E + k, T, E, k)
+    x = synth.f32_to_bf16_bits(np.random.default_rng(T + I).standard_normal((T, H)).astype(np.float32))
+    old = zffn.set_option(zffn.OPT_MOE_KERNEL, kernel)
+    try:
+        y = run(x, ids, w, Wg, Wu, Wd, I, E, matvec_max_t=0)
+    finally:
+        zffn.set_option(zffn.OPT_MOE_KERNEL, old)
+    ref = orc.moe_swiglu_ffn(x, ids, w, Wg, Wu, Wd, T, H, I, E, k)
+    assert_close(y, ref, f"routed kernel {kernel} T={T} E={E} H={H} I={I} k={k}")
+
+
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_both_routed_kernels_full_config_256_tokens(kernel):
+    m = moe_layer(256)
+    old = zffn.set_option(zffn.OPT_MOE_KERNEL, kernel)
+    try:
+        y = run(m["x"], m["ids"], m["w"], m["Wg"], m["Wu"], m["Wd"], m["I"], m["E"])
+    finally:
+        zffn.set_option(zffn.OPT_MOE_KERNEL, old)
+    rows = list(range(0, 256, 16)) + [1, 17, 127, 128, 129, 255]
+    ref = orc.moe_swiglu_ffn(m["x"][rows].copy(), m["ids"][rows].copy(), m["w"][rows].copy(),
+                             m["Wg"], m["Wu"], m["Wd"], len(rows), m["H"], m["I"], m["E"], m["k"])
+    assert_close(y[rows], ref, f"moe T=256 kernel {kernel}")
