@@ -22,13 +22,21 @@
 // intermediate scaled by 2^-8 so that its fp16 range reaches 1.7e7 (values
 // beyond saturate).  The SwiGLU intermediate of a group never leaves the SM.
 //
+// The unpacked weights never touch shared memory: each unpacking thread owns
+// one weight row, which is one TMEM lane of the MMA's A operand, and writes
+// its 64 fp16 values of a K step straight into tensor memory (tcgen05.st);
+// the MMA reads A from there.  Four A stages live in TMEM next to the
+// accumulators, so the unpackers run up to four K steps ahead of the tensor
+// core, and shared memory holds only the packed blocks, x and h.
+//
 // Block roles (24 warps):
 //   warps 0-3   epilogue for TMEM lane quadrants 0-3: SwiGLU -> h, Y -> y
 //   warp 4      TMEM allocator and MMA issuer (one elected lane issues)
 //   warp 5      TMA producer: whole Q4_K blocks of 128 weight rows (one box
 //               per matrix covers four K steps)
 //   warp 6      TMA producer: the group's x tiles [32 x 64] fp16
-//   warps 8-23  unpackers, four groups of four warps taking tasks in turn
+//   warps 8-23  unpackers, four groups of four warps (one per TMEM lane
+//               quadrant) taking tasks in turn
 //   warp 7      idle
 #include <cudaTypedefs.h>
 
@@ -44,27 +52,27 @@ constexpr int KSB = 4;                       // K steps per packed block step (2
 constexpr int IC_MAX = 768;                  // intermediate columns of a work unit
 constexpr int NUM_WARPS = 24;
 constexpr int THREADS = NUM_WARPS * 32;
-constexpr int UNPACK_GROUPS = 4;
-constexpr int NR = 2, NA = 2, NX = 8;        // packed, unpacked, x stages
+constexpr int NR = 4, NA = 4, NX = 8;        // packed, unpacked (TMEM), x stages
 constexpr int R_BOX = BM * kBlockBytes;      // one whole-block box of 128 rows: 18432 bytes
 constexpr int R_BYTES = 2 * R_BOX;           // gate + up (the down phase uses the first half)
-constexpr int A_TILE = BM * BK * 2;          // [128 x 64] fp16
-constexpr int A_BYTES = 2 * A_TILE;          // gate + up (the down phase uses the first)
 constexpr int X_BYTES = NG * BK * 2;         // [32 x 64] fp16
 constexpr int H_TILE = NG * BK * 2;          // h columns [64j, 64j + 64) of the group
 constexpr int H_BYTES = (IC_MAX / BK) * H_TILE;
 constexpr int OFF_R = 0;
-constexpr int OFF_A = OFF_R + NR * R_BYTES;
-constexpr int OFF_X = OFF_A + NA * A_BYTES;
+constexpr int OFF_X = OFF_R + NR * R_BYTES;
 constexpr int OFF_H = OFF_X + NX * X_BYTES;
 constexpr int OFF_BAR = OFF_H + H_BYTES;
 constexpr int N_BARS = 2 * NR + 2 * NA + 2 * NX + 4 + 4 + 2;
 constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + alignment slack
-static_assert(OFF_A % 1024 == 0 && OFF_X % 1024 == 0 && OFF_H % 1024 == 0, "swizzled tiles 1024-aligned");
+static_assert(OFF_X % 1024 == 0 && OFF_H % 1024 == 0, "swizzled tiles 1024-aligned");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget of one block");
 static_assert(NG == 32, "one group row per lane of an epilogue warp");
-// TMEM columns: gate / up / down accumulators, two of each
-constexpr uint32_t COL_G = 0, COL_U = 2 * NG, COL_Y = 4 * NG, TMEM_COLS = 256;
+// TMEM columns: gate / up / down accumulators, two of each, then the A
+// stages: 64 columns each (a K step of 128 rows in fp16 pairs: gate rows in
+// the first 32 columns and up rows in the next 32, or W_down rows in the first 32)
+constexpr uint32_t COL_G = 0, COL_U = 2 * NG, COL_Y = 4 * NG, COL_A = 6 * NG, A_COLS = 64;
+constexpr uint32_t TMEM_COLS = 512;
+static_assert(COL_A + NA * A_COLS <= TMEM_COLS, "TMEM budget");
 constexpr uint32_t IDESC = idesc_f16_f32(BM, NG);
 constexpr float H_SCALE = 1.0f / 256.0f;     // the intermediate is held as h * 2^-8
 
@@ -138,13 +146,13 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int role = warp_role(warp);
-    const uint32_t s_r = smem_u32(smem + OFF_R), s_a = smem_u32(smem + OFF_A);
+    const uint32_t s_r = smem_u32(smem + OFF_R);
     const uint32_t s_x = smem_u32(smem + OFF_X), s_h = smem_u32(smem + OFF_H);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NR; ++i) {
             mbar_init(&r_full[i], 1);
-            mbar_init(&r_empty[i], 2 * KSB * 4);      // 4 K steps x 2 tasks x 4 warps
+            mbar_init(&r_empty[i], 2 * 2 * 4);        // 2 K-step pairs x 2 tasks x 4 warps
         }
         for (int i = 0; i < NA; ++i) {
             mbar_init(&a_full[i], 2 * 4);             // 2 tasks x 4 warps
@@ -251,7 +259,7 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
         auto commit = [&](uint64_t *bar) {
             if (issuer) tc_commit(bar);
         };
-        const uint64_t da0 = smem_desc_k_sw128(s_a), dx0 = smem_desc_k_sw128(s_x);
+        const uint64_t dx0 = smem_desc_k_sw128(s_x);
         const uint64_t dh0 = smem_desc_k_sw128(s_h);
         for (int k = 0; k < m_units && ok; ++k) {
             const Unit un = unit_of(k);
@@ -263,17 +271,17 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
                     if (!mbar_wait(&a_full[ai], aph, abort_flag, p.err) ||
                         !mbar_wait(&x_full[xi], xph, abort_flag, p.err)) { ok = false; break; }
                     tc_fence_after();
-                    const uint64_t da = da0 + (uint64_t)((ai * A_BYTES) >> 4);
+                    const uint32_t ta = tmem_base + COL_A + ai * A_COLS;
                     const uint64_t dx = dx0 + (uint64_t)((xi * X_BYTES) >> 4);
                     if (issuer) {
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk)
-                            tc_mma_bf16(tmem_base + COL_G + gb * NG, da + 2 * kk, dx + 2 * kk, IDESC,
-                                        (ks | kk) != 0);
+                            tc_mma_f16_ta(tmem_base + COL_G + gb * NG, ta + 8 * kk, dx + 2 * kk, IDESC,
+                                          (ks | kk) != 0);
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk)
-                            tc_mma_bf16(tmem_base + COL_U + gb * NG, da + (A_TILE >> 4) + 2 * kk, dx + 2 * kk,
-                                        IDESC, (ks | kk) != 0);
+                            tc_mma_f16_ta(tmem_base + COL_U + gb * NG, ta + 32 + 8 * kk, dx + 2 * kk, IDESC,
+                                          (ks | kk) != 0);
                     }
                     commit(&a_empty[ai]);
                     commit(&x_empty[xi]);
@@ -295,13 +303,13 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
                     }
                     if (!mbar_wait(&a_full[ai], aph, abort_flag, p.err)) { ok = false; break; }
                     tc_fence_after();
-                    const uint64_t da = da0 + (uint64_t)((ai * A_BYTES) >> 4);
+                    const uint32_t ta = tmem_base + COL_A + ai * A_COLS;
                     const uint64_t dh = dh0 + (uint64_t)((ks * H_TILE) >> 4);
                     if (issuer) {
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk)
-                            tc_mma_bf16(tmem_base + COL_Y + yb * NG, da + 2 * kk, dh + 2 * kk, IDESC,
-                                        (ks | kk) != 0);
+                            tc_mma_f16_ta(tmem_base + COL_Y + yb * NG, ta + 8 * kk, dh + 2 * kk, IDESC,
+                                          (ks | kk) != 0);
                     }
                     commit(&a_empty[ai]);
                     if (++ai == NA) { ai = 0; aph ^= 1; }
@@ -319,47 +327,76 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
         mbar_wait(drain, 0, nullptr, p.err, kWaitBudgetCycles / 8);
     } else if (role == ROLE_UNPACK) {
         // ------------- weight unpackers (four groups of 4 warps) -------------
-        // Every K step has two 128-thread tasks: the gate rows and the up rows
-        // (gate/up phase), or the low and the high nibbles of the 128 W_down
-        // rows (down phase).  Group g takes the tasks with index g modulo 4,
-        // counted over the whole program of this block, so groups 0-1 always
-        // fill the even K steps' stage and groups 2-3 the odd ones'.
+        // The program's K steps go in pairs (2m, 2m+1: both in one Q4_K
+        // block), and every pair has two 128-thread tasks: the gate rows and
+        // the up rows (gate/up phase), or the low and the high nibbles of the
+        // 128 W_down rows (down phase).  Group g takes task g % 2 of the pairs
+        // with parity g / 2: groups 0-1 fill A stages 0-1, groups 2-3 stages
+        // 2-3.  A task decodes its row's block header once for the four
+        // sub-blocks of its two K steps.  Thread r of a task owns weight row r,
+        // which is TMEM lane r: warp w writes lane quadrant w % 4 (the only one
+        // it may access).
         const int uw = warp - 8;
         const uint32_t grp = (uint32_t)(uw / 4);
+        const int task = (int)(grp & 1);
+        const uint32_t pair_parity = grp >> 1;
         const int r = (uw % 4) * 32 + lane;             // weight row within the task
-        uint32_t kstep = 0;                              // K steps of the program so far
+        const uint32_t t_row = tmem_base + ((uint32_t)((uw % 4) * 32) << 16);
+        uint32_t pair = 0;                               // K-step pairs of the program so far
         bool ok = true;
         for (int k = 0; k < m_units && ok; ++k) {
             const Unit un = unit_of(k);
             const int n_g = un.n_ib * un.ks_g, n_steps = n_g + un.n_hb * un.ks_y;
-            for (int s = 0; s < n_steps && ok; ++s, ++kstep) {
+            int blk = 0, ks = 0;                         // position within the phase
+            for (int s = 0; s < n_steps && ok; s += 2, ++pair) {
+                const bool gu = s < n_g;
+                if (s == n_g) { blk = 0; ks = 0; }
+                const int cur_blk = blk, cur_ks = ks;
+                ks += 2;
+                if (ks == (gu ? un.ks_g : un.ks_y)) { ks = 0; ++blk; }
+                if ((pair & 1) != pair_parity) continue;
+                const uint32_t bs = pair >> 1;           // packed block step
+                const uint32_t ri = bs % NR, rph = (bs / NR) & 1;
+                const uint32_t ai = (2 * pair) % NA, aph = ((2 * pair) / NA) & 1;
+                const bool zero = gu && cur_blk * BM + r >= un.ic;
+                if (!mbar_wait(&r_full[ri], rph, abort_flag, p.err)) { ok = false; break; }
+                uint4 hd = make_uint4(0, 0, 0, 0), c[4] = {hd, hd, hd, hd};
+                if (!zero) {
+                    const uint32_t src = s_r + ri * R_BYTES + (gu ? task * R_BOX : 0) + r * kBlockBytes;
+                    hd = ld_shared_v4(src);
 #pragma unroll
-                for (int task = 0; task < 2; ++task) {
-                    if (((2 * kstep + task) & (UNPACK_GROUPS - 1)) != grp) continue;
-                    const bool gu = s < n_g;
-                    const int ks = gu ? s % un.ks_g : (s - n_g) % un.ks_y;
-                    const uint32_t bs = kstep / KSB;         // packed block step
-                    const uint32_t ri = bs % NR, rph = (bs / NR) & 1;
-                    const uint32_t ai = kstep % NA, aph = (kstep / NA) & 1;
-                    const bool zero = gu && (s / un.ks_g) * BM + r >= un.ic;
-                    if (!mbar_wait(&r_full[ri], rph, abort_flag, p.err)) { ok = false; break; }
-                    uint4 hd = make_uint4(0, 0, 0, 0), q0 = hd, q1 = hd;
-                    if (!zero) {
-                        const uint32_t src = s_r + ri * R_BYTES + (gu ? task * R_BOX : 0) + r * kBlockBytes;
-                        hd = ld_shared_v4(src);
-                        q0 = ld_shared_v4(src + 16 + 32 * (ks & 3));
-                        q1 = ld_shared_v4(src + 32 + 32 * (ks & 3));
+                    for (int i = 0; i < 4; ++i) c[i] = ld_shared_v4(src + 16 + 32 * (cur_ks & 3) + 16 * i);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&r_empty[ri]);
+                if (!mbar_wait(&a_empty[ai], aph ^ 1, abort_flag, p.err) ||
+                    !mbar_wait(&a_empty[ai + 1], aph ^ 1, abort_flag, p.err)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t sa[4], sb[4];                   // sub-blocks 2 (ks & 3) .. +3
+                q4k_f16_scales4(hd, 2 * (cur_ks & 3), sa, sb);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {            // K step cur_ks + j, stage ai + j
+                    const uint32_t w[8] = {c[2 * j].x, c[2 * j].y, c[2 * j].z, c[2 * j].w,
+                                           c[2 * j + 1].x, c[2 * j + 1].y, c[2 * j + 1].z, c[2 * j + 1].w};
+                    const uint32_t dst = t_row + COL_A + (ai + j) * A_COLS;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (!gu && h != task) continue;  // down phase: one nibble half
+                        uint32_t v[16];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            codes4_to_f16((w[i] >> (4 * h)) & 0x0F0F0F0Fu, sa[2 * j + h], sb[2 * j + h],
+                                          v[2 * i], v[2 * i + 1]);
+                        // gate/up: row's columns 32 task + 16 h; down: 16 h
+                        tmem_st_32x32b_x16(dst + (gu ? 32 * task : 0) + 16 * h, v);
                     }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&r_empty[ri]);
-                    if (!mbar_wait(&a_empty[ai], aph ^ 1, abort_flag, p.err)) { ok = false; break; }
-                    const uint32_t w8[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                    const uint32_t dst = s_a + ai * A_BYTES + (gu ? task * A_TILE : 0) + sw128_row(r);
-                    if (gu) unpack_row_to_smem_f16(hd, w8, ks & 3, dst, r);
-                    else unpack_half_row_to_smem_f16(hd, w8, ks & 3, task, dst, r);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&a_full[ai]);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&a_full[ai]);
+                    mbar_arrive(&a_full[ai + 1]);
                 }
             }
         }

@@ -211,6 +211,19 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// The same with A read from tensor memory: `a_tmem` addresses lane 0 of the
+// first of the K/2 columns holding A's M rows (one row per lane, two 16-bit
+// elements per 32-bit column).
+__device__ __forceinline__ void tc_mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 op this thread issued so far completes.
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
     asm volatile(
@@ -323,6 +336,12 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
 __device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
                  "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                 ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+                 "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
                  : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() {
@@ -490,6 +509,52 @@ __device__ __forceinline__ void unpack_half_row_to_smem_f16(uint4 hd, const uint
         st_shared_v4(row_addr + (((uint32_t)((c + 4 * hi) ^ (row & 7))) << 4),
                      fma_f16x2(codes_to_f16x2(v0), a, b), fma_f16x2(codes_to_f16x2(v0 >> 16), a, b),
                      fma_f16x2(codes_to_f16x2(v1), a, b), fma_f16x2(codes_to_f16x2(v1 >> 16), a, b));
+    }
+}
+
+// One sub-block (32 weights) of a Q4_K row and K step into registers: hi = 0
+// the low nibbles of the 8 code words (sub-block 2g), hi = 1 the high nibbles
+// (sub-block 2g+1).  out[j] holds weights 2j and 2j+1 of the sub-block as an
+// fp16 pair (low half first) -- the K-packed layout of an MMA operand row in
+// tensor memory.
+__device__ __forceinline__ void unpack_half_row_f16(uint4 hd, const uint32_t (&w)[8], int g, int hi,
+                                                    uint32_t (&out)[16]) {
+    const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
+    int sc, m;
+    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g + hi, sc, m);
+    const uint32_t a = f16x2_splat_satfinite(512.0f * (d * (float)sc));
+    const uint32_t b = f16x2_splat_satfinite(-(dmin * (float)m));
+    const int sh = 4 * hi;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t v = (w[i] >> sh) & 0x0F0F0F0Fu;   // weights 4i .. 4i+3
+        out[2 * i] = fma_f16x2(codes_to_f16x2(v), a, b);
+        out[2 * i + 1] = fma_f16x2(codes_to_f16x2(v >> 16), a, b);
+    }
+}
+
+// Four code bytes (each a code 0..15) -> the fp16 weights of bytes 0-1 (o0) and
+// 2-3 (o1): w = (q * 2^-9) * a + b with a, b fp16 pairs (see codes_to_f16x2).
+__device__ __forceinline__ void codes4_to_f16(uint32_t v, uint32_t a, uint32_t b, uint32_t &o0, uint32_t &o1) {
+    uint32_t c0, c1;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(c0), "=r"(c1)
+        : "r"(v));
+    o0 = fma_f16x2(c0, a, b);
+    o1 = fma_f16x2(c1, a, b);
+}
+
+// fp16 scale and offset pairs (512 d sc, -dmin m) of the four sub-blocks
+// sb0 .. sb0+3 of a Q4_K block header (sb0 = 0 or 4).
+__device__ __forceinline__ void q4k_f16_scales4(uint4 hd, int sb0, uint32_t (&a)[4], uint32_t (&b)[4]) {
+    const float d = 512.0f * half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        int sc, m;
+        q4k_scale_min(hd.y, hd.z, hd.w, sb0 + j, sc, m);
+        a[j] = f16x2_splat_satfinite(d * (float)sc);
+        b[j] = f16x2_splat_satfinite(-(dmin * (float)m));
     }
 }
 
