@@ -117,7 +117,7 @@ def load_peaks():
 # ncu traffic figure stays valid while these files are unchanged.
 KERNEL_SOURCES = {
     "prefill": ("ffn_tc.cu", "zffn_internal.cuh"),
-    "moe": ("ffn_tc.cu", "moe_route.cu", "zffn_internal.cuh"),
+    "moe": ("moe_tc.cu", "moe_route.cu", "zffn_internal.cuh"),
     "decode": ("ffn_matvec.cu", "zffn_internal.cuh"),
 }
 
@@ -328,9 +328,9 @@ def run_gpu(args):
         else:
             zffn.moe_swiglu_q4k(x_for(step), ids, wts, Wg_, Wu_, Wd_, I, E, y=y, residual=residual)
 
-    launches_per_call = 2                          # zero fill + fused kernel, or gate/up + down
+    launches_per_call = 2                          # x conversion (+ zero fill) + fused kernel, or gate/up + down
     if kind == "moe" and T > 1:
-        launches_per_call = 4                      # route, gather, zero fill, fused kernel
+        launches_per_call = 4                      # route, gather (+ fp16), zero fill, grouped kernel
 
     def barrier():
         if world > 1:
@@ -541,8 +541,9 @@ def run_gpu(args):
         "roofline": {
             "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
             "frac": round(achieved / peak, 4), "traffic": traffic,
-            "kernel": "ffn_tc_kernel" if bound == "tensor" else
-                      ("ffn_gu_kernel+ffn_down_kernel" if T == 1 else "ffn_tc_kernel"),
+            "kernel": "x_to_f16_kernel+ffn_tc_kernel" if bound == "tensor" else
+                      ("ffn_gu_kernel+ffn_down_kernel" if T == 1 else
+                       "moe_route_kernel+moe_gather_kernel+moe_group_kernel"),
             "kernel_ms": round(kms, 4),
             "peak_source": f"{peaks['source']} (burst)",
             "algorithmic": {"flop": flop, "hbm_bytes": abytes},

@@ -146,6 +146,8 @@ void oracle_q4k_dequant_row(const uint8_t *row, int64_t cols, float *out)
 void oracle_q4k_dequant(const uint8_t *blocks, float *out, int64_t rows, int64_t cols)
 {
     int64_t rb = ((cols + QK - 1) / QK) * QK_BYTES;
+    /* rows are independent: a build with OpenMP takes them in parallel */
+    #pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; ++r)
         oracle_q4k_dequant_row(blocks + r * rb, cols, out + r * cols);
 }
@@ -368,13 +370,15 @@ void oracle_swiglu_ffn_fmt(const uint16_t *x, const uint8_t *Wg, const uint8_t *
     int64_t rb_dn = oracle_fmt_row_bytes(wd_fmt, I);
     double *xf = (double *)malloc(sizeof(double) * (size_t)(T * H));
     double *h = (double *)malloc(sizeof(double) * (size_t)(T * I));
-    float *wg = (float *)malloc(sizeof(float) * (size_t)H);
-    float *wu = (float *)malloc(sizeof(float) * (size_t)H);
-    float *wd = (float *)malloc(sizeof(float) * (size_t)I);
     for (int64_t i = 0; i < T * H; ++i)
         xf[i] = (double)oracle_bf16_to_f32(x[i]);
-    /* g = Wg x, u = Wu x, h = silu(g) * u */
+    /* g = Wg x, u = Wu x, h = silu(g) * u.  Each row i has its own scratch,
+     * so a build with OpenMP may take the rows in parallel; every sum keeps
+     * its order, so the result is the same either way. */
+    #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < I; ++i) {
+        float *wg = (float *)malloc(sizeof(float) * (size_t)H);
+        float *wu = (float *)malloc(sizeof(float) * (size_t)H);
         oracle_q4k_dequant_row(Wg + i * rb_in, H, wg);
         oracle_q4k_dequant_row(Wu + i * rb_in, H, wu);
         for (int64_t t = 0; t < T; ++t) {
@@ -386,9 +390,12 @@ void oracle_swiglu_ffn_fmt(const uint16_t *x, const uint8_t *Wg, const uint8_t *
             }
             h[t * I + i] = oracle_silu(g) * u;
         }
+        free(wg); free(wu);
     }
-    /* y = Wd h */
+    /* y = Wd h (rows n independent, as above) */
+    #pragma omp parallel for schedule(static)
     for (int64_t n = 0; n < H; ++n) {
+        float *wd = (float *)malloc(sizeof(float) * (size_t)I);
         oracle_dequant_row_fmt(wd_fmt, Wd + n * rb_dn, I, wd);
         for (int64_t t = 0; t < T; ++t) {
             const double *ht = h + t * I;
@@ -397,8 +404,9 @@ void oracle_swiglu_ffn_fmt(const uint16_t *x, const uint8_t *Wg, const uint8_t *
                 acc += (double)wd[i] * ht[i];
             y[t * H + n] = acc;
         }
+        free(wd);
     }
-    free(xf); free(h); free(wg); free(wu); free(wd);
+    free(xf); free(h);
 }
 
 /* The block with all three matrices in Q4_K. */

@@ -42,25 +42,62 @@ def row_bytes(cols: int) -> int:
     return ((cols + QK - 1) // QK) * QK_BYTES
 
 
+_FLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+
 def build(force: bool = False) -> str:
-    """Compile oracle.c (plain C, -O2, no fast-math, no FMA contraction)."""
+    """Compile oracle.c (plain C, -O2, no fast-math, no FMA contraction,
+    single-threaded: its OpenMP pragmas are ignored)."""
     os.makedirs(_OUT_DIR, exist_ok=True)
     stale = (not os.path.exists(_LIB_PATH)
              or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
     if force or stale:
         tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-        subprocess.check_call([
-            "gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
-            "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        subprocess.check_call(["gcc", *_FLAGS, "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
+
+
+_OMP_PATH = os.path.join(_OUT_DIR, "liboracle_omp.so")
+
+
+def build_omp(force: bool = False):
+    """The same source built with -fopenmp: its independent row loops run on
+    all host cores (the CPU baseline's all-cores leg).  Returns the library
+    path, or None where the compiler has no OpenMP."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    stale = (not os.path.exists(_OMP_PATH)
+             or os.path.getmtime(_OMP_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _OMP_PATH + f".{os.getpid()}.tmp"
+        try:
+            subprocess.check_call(["gcc", *_FLAGS, "-fopenmp", "-o", tmp, _SRC, "-lm"],
+                                  stderr=subprocess.DEVNULL)
+        except (subprocess.CalledProcessError, OSError):
+            return None
+        os.replace(tmp, _OMP_PATH)
+    return _OMP_PATH
+
+
+def use_library(path: str):
+    """Route the wrappers to another build of oracle.c (e.g. build_omp());
+    returns the previous path, for restoring."""
+    global _lib, _active
+    with _lock:
+        prev = _active
+        _active = path
+        _lib = None
+    return prev
+
+
+_active = None
 
 
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
+            lib = ctypes.CDLL(_active or build())
             P = ctypes.c_void_p
             I64 = ctypes.c_int64
             lib.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]

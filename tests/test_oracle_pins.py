@@ -615,3 +615,24 @@ def test_prenorm_sublayer_reduces_to_parts():
     assert np.array_equal(x, orc.rmsnorm_bf16(h, gamma, 1e-6))
     y = orc.swiglu_ffn(x, d["Wg"], d["Wu"], d["Wd"], 4, d["H"], d["I"])
     assert np.array_equal(out, h.astype(np.float64) + y)
+
+
+def test_parallel_build_of_the_oracle_gives_the_same_bits():
+    # The CPU baseline's all-cores leg runs the oracle's source built with
+    # OpenMP: its row loops are independent and keep every sum's order, so
+    # its outputs equal the single-threaded build's bit for bit.
+    path = orc.build_omp()
+    if path is None:
+        pytest.skip("no OpenMP in this compiler")
+    H, I, T = 512, 320, 3
+    Wg, Wu, Wd = _rand_rows(70, I, H), _rand_rows(71, I, H), _rand_rows(72, H, I)
+    x = _x(73, T, H)
+    y1 = orc.swiglu_ffn(x, Wg, Wu, Wd, T, H, I)
+    d1 = orc.q4k_dequant(Wg, I, H)
+    prev = orc.use_library(path)
+    try:
+        y2 = orc.swiglu_ffn(x, Wg, Wu, Wd, T, H, I)
+        d2 = orc.q4k_dequant(Wg, I, H)
+    finally:
+        orc.use_library(prev)
+    assert np.array_equal(y1, y2) and np.array_equal(d1, d2)
