@@ -447,6 +447,63 @@ def run_gpu(args):
         norm = {"kernel": "rmsnorm_bf16_kernel", "ms": round(n_ms, 5), "hbm_bytes": n_bytes,
                 "achieved_gbs": round(n_gbs, 2), "frac_of_hbm_peak": round(n_gbs / peaks["hbm"], 4)}
 
+    # The staged pipeline the fusion replaces ("Fused SwiGLU MLP...", sections
+    # "Counting the bytes the intermediate actually moves" and "What it is
+    # worth"): dequantise each matrix to a 16-bit scratch copy, then the gate
+    # and up GEMMs, the SwiGLU as its own pass, the down GEMM -- four
+    # dispatches with the intermediate crossing device memory six times.
+    # Benchmark-only: the library's dequantisation kernel, cuBLAS (torch.matmul)
+    # and torch's elementwise kernels; nothing of it is in the library.
+    staged = None
+    if kind == "dense" and T > 1:
+        import torch.nn.functional as F
+        wf = [torch.empty((I, H), dtype=torch.float32, device=dev), torch.empty((I, H), dtype=torch.float32, device=dev),
+              torch.empty((H, I), dtype=torch.float32, device=dev)]
+        wb = [torch.empty_like(w, dtype=torch.bfloat16) for w in wf]
+        gs = torch.empty((T, I), dtype=torch.bfloat16, device=dev)
+        us = torch.empty_like(gs)
+        hs = torch.empty_like(gs)
+        ys = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        xs = x_for(0)
+
+        def dequant_all():
+            for q, (r_, c_), f, b in zip(W, ((I, H), (I, H), (H, I)), wf, wb):
+                zffn.q4k_dequant(q, r_, c_, out=f)
+                b.copy_(f)
+
+        def gemms():
+            torch.matmul(xs, wb[0].t(), out=gs)
+            torch.matmul(xs, wb[1].t(), out=us)
+            torch.mul(F.silu(gs), us, out=hs)
+            torch.matmul(hs, wb[2].t(), out=ys)
+
+        def staged_call():
+            dequant_all()
+            gemms()
+
+        for _ in range(args.warmup):          # first calls carry library set-up
+            staged_call()
+        torch.cuda.synchronize()
+        s_ms = timed(lambda s: staged_call())
+        g_ms = timed(lambda s: gemms())
+        torch.cuda.synchronize()
+        y_f = zffn.swiglu_q4k(xs, W[0], W[1], W[2], I)
+        rel = float(torch.linalg.vector_norm(ys.float() - y_f) / torch.linalg.vector_norm(y_f))
+        staged = {"what": "dequant (library kernel) to fp32 and bf16 scratch, cuBLAS gate and up "
+                          "GEMMs, SwiGLU (torch elementwise), cuBLAS down GEMM; bf16 operands, "
+                          "timed like the fused call",
+                  "ms": round(s_ms, 4), "ms_gemms_only": round(g_ms, 4),
+                  "ms_dequant_to_scratch": round(s_ms - g_ms, 4),
+                  "fused_ms": round(ms, 4), "fused_speedup": round(s_ms / ms, 3),
+                  "fused_speedup_vs_gemms_only": round(g_ms / ms, 3),
+                  "intermediate_dram_bytes": {"staged_model": 6 * T * I * 2, "fused_measured": 0,
+                                              "how": "staged: g and u written, read by the SwiGLU, "
+                                                     "h written and read by the down GEMM (bf16); "
+                                                     "fused: ncu DRAM writes of the fused kernel "
+                                                     "are y only"},
+                  "rel_l2_vs_fused": round(rel, 5)}
+        del wf, wb, gs, us, hs, ys
+
     # single-token blocks with W_down in the other block formats (W_gate and
     # W_up the workload's Q4_K matrices, W_down seeded random blocks of the
     # format), one call between events after an L2 flush
@@ -555,6 +612,7 @@ def run_gpu(args):
         "cpu_baseline": cpu,
         **({"router": router} if router is not None else {}),
         **({"rmsnorm": norm} if norm is not None else {}),
+        **({"staged": staged} if staged is not None else {}),
         **({"down_formats": {"kernels": "ffn_gu_kernel + down_fmt_kernel", "timing":
                              "one isolated call after an L2 flush", **down_formats}}
            if down_formats is not None else {}),
@@ -598,22 +656,66 @@ def oracle_tokens(name, host, layer, rows):
                               len(rows), H, I, E, k)
 
 
-def cpu_baseline(name, host, seconds=10.0):
-    """The oracle as it stands, single-threaded, on a bounded sample of tokens."""
-    layer = oracle_layer(name, host)
-    T = WORKLOADS[name][1]
+def _oracle_rate(name, host, layer, seconds, per_call):
+    """Tokens per second of the oracle on consecutive tokens of the workload,
+    calls of per_call tokens, for about `seconds`."""
     n_rows = host["x"].shape[0] if isinstance(host, dict) else host.x.shape[0]
     done, t0, r = 0, time.perf_counter(), 0
-    per_call = 4 if T > 1 else 1
     while time.perf_counter() - t0 < seconds:
         rows = [(r + i) % n_rows for i in range(per_call)]
         oracle_tokens(name, host, layer, rows)
         done += per_call
         r += per_call
-    dt = time.perf_counter() - t0
-    return {"value": round(done / dt, 3), "unit": "tok/s", "cores": 1, "kind": "oracle",
-            "sample": f"{done} tokens of the workload in calls of {per_call} "
-                      f"(full weights; oracle dequantises every weight row once per call)"}
+    return done, time.perf_counter() - t0
+
+
+def cpu_baseline(name, host, seconds=10.0):
+    """The oracle timed on this host's cores: its source built with OpenMP on
+    all cores (the row loops in parallel) and the plain single-threaded
+    build, each on a bounded sample of the workload's tokens; plus the
+    dequantisation of one weight matrix on its own (the part of every call
+    that does not depend on the tokens)."""
+    from oracle import oracle as orc
+    layer = oracle_layer(name, host)
+    T = WORKLOADS[name][1]
+    kind = WORKLOADS[name][0]
+    per_call = 4 if T > 1 else 1
+    ncores = os.cpu_count() or 1
+    try:
+        ncores = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        pass
+    Wg = layer["Wg"] if kind == "dense" else layer["Wg"][0]
+    rows, cols = Wg.shape[0], WORKLOADS[name][2]
+
+    def dequant_s():
+        t0 = time.perf_counter()
+        orc.q4k_dequant(Wg, rows, cols)
+        return time.perf_counter() - t0
+
+    d1 = dequant_s()
+    n1, t1 = _oracle_rate(name, host, layer, seconds * 0.5, per_call)
+    out = {"value": round(n1 / t1, 3), "unit": "tok/s", "cores": 1, "kind": "oracle",
+           "sample": f"{n1} tokens of the workload in calls of {per_call} (full weights; the "
+                     f"oracle dequantises every weight row once per call)",
+           "dequant_s_one_matrix": {"rows": rows, "cols": cols, "1_core": round(d1, 4)}}
+    omp = orc.build_omp()
+    if omp is not None:
+        prev = orc.use_library(omp)
+        try:
+            dn = dequant_s()
+            per_n = max(per_call, ncores) if T > 1 else 1
+            nn, tn = _oracle_rate(name, host, layer, seconds * 0.5, per_n)
+        finally:
+            orc.use_library(prev)
+        out["dequant_s_one_matrix"]["all_cores"] = round(dn, 4)
+        # the all-cores build is the headline baseline; the plain build stays beside it
+        single = {k: out[k] for k in ("value", "cores", "sample")}
+        out.update({"value": round(nn / tn, 3), "cores": ncores,
+                    "sample": f"{nn} tokens in calls of {per_n}, oracle built with OpenMP "
+                              f"(row loops over {ncores} cores)",
+                    "single_core": single})
+    return out
 
 
 def run_reference(args):
