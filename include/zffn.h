@@ -215,18 +215,27 @@ zffn_status zffn_dequant_fmt(int fmt, const void *blocks, float *out, int64_t ro
                              int64_t cols, void *stream);
 
 /* The block with W_gate and W_up in Q4_K and W_down in format wd_fmt (rows of
- * zffn_row_bytes_fmt(wd_fmt, I) bytes).  ZFFN_FMT_Q4_K is zffn_swiglu_q4k.  The
- * other formats run on the single-token path only: T must be 1, otherwise
- * ZFFN_ERR_UNSUPPORTED.  Wd must be 4-byte aligned (its rows need not be: Q6_K
- * rows are 210-byte multiples).  Also UNSUPPORTED when top_k * I fp32 values of
- * h plus 64 KB of row buffers exceed a block's shared memory (I > 40960 at
- * top_k = 1).
+ * zffn_row_bytes_fmt(wd_fmt, I) bytes) ("Four bottlenecks, one CUDA
+ * backend...", section "Bottleneck 4": Q4_K, Q5_K and Q6_K GEMMs of prefill).
+ * ZFFN_FMT_Q4_K is zffn_swiglu_q4k.
+ *   T = 1: the single-token kernels, every format.  Wd must be 4-byte aligned
+ *     (its rows need not be: Q6_K rows are 210-byte multiples).  UNSUPPORTED
+ *     when top_k * I fp32 values of h plus 64 KB of row buffers exceed a
+ *     block's shared memory (I > 40960 at top_k = 1).
+ *   T > 1: Q5_K and Q5_1 on the grouped tensor-core kernel (the routed
+ *     kernel's groups of 32 token rows; a dense block runs as one expert), Wd
+ *     and y 16-byte aligned.  Its weights are unpacked once per group of 32
+ *     tokens, so it suits routed layers and short prompts rather than long
+ *     prefills.  Q6_K at T > 1 returns UNSUPPORTED: its 210-byte blocks give
+ *     row pitches that are not multiples of 16 bytes, which the tensor-core
+ *     kernels' TMA loads need.
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA, NO_WORKSPACE. */
 zffn_status zffn_swiglu_q4k_wd(const void *x, const void *Wg, const void *Wu, const void *Wd,
                                int wd_fmt, float *y, int T, int H, int I, void *stream);
 
 /* The routed block (as zffn_moe_swiglu_q4k) with every expert's W_down in
- * format wd_fmt; the same restrictions as zffn_swiglu_q4k_wd. */
+ * format wd_fmt; the same formats and restrictions as zffn_swiglu_q4k_wd (at
+ * T > 1 the grouped tensor-core kernel). */
 zffn_status zffn_moe_swiglu_q4k_wd(const void *x, const int32_t *expert_ids,
                                    const float *expert_weights, const void *Wg, const void *Wu,
                                    const void *Wd, int wd_fmt, float *y, int T, int H, int I,

@@ -274,7 +274,7 @@ zffn_status swiglu_dense(const void *x, const void *Wg, const void *Wu, const vo
 zffn_status swiglu_moe(const void *x, const int32_t *expert_ids, const float *expert_weights,
                        const float *down_scale, const void *Wg, const void *Wu, const void *Wd,
                        float *y, int T, int H, int I, int E, int top_k, void *stream,
-                       bool accumulate) {
+                       bool accumulate, int wd_fmt = kFmtQ4_K) {
     if (!x || !expert_ids || !expert_weights || !Wg || !Wu || !Wd || !y)
         return invalid("a pointer argument is NULL");
     if (check_shape(T, H, I) != ZFFN_OK) return ZFFN_ERR_INVALID_ARG;
@@ -299,7 +299,8 @@ zffn_status swiglu_moe(const void *x, const int32_t *expert_ids, const float *ex
     zffn_status st = ensure_workspace(L.total, &w);
     if (st != ZFFN_OK) return st;
     uint8_t *base = static_cast<uint8_t *>(w->ptr);
-    if (T == 1 && mv_max >= 1 && matvec_smem_bytes(T, H, I, top_k) <= (size_t)di.max_smem_optin) {
+    if (T == 1 && wd_fmt == kFmtQ4_K && mv_max >= 1 &&
+        matvec_smem_bytes(T, H, I, top_k) <= (size_t)di.max_smem_optin) {
         MatvecArgs a{};
         a.x = static_cast<const __nv_bfloat16 *>(x);
         a.Wg = static_cast<const uint8_t *>(Wg);
@@ -323,7 +324,9 @@ zffn_status swiglu_moe(const void *x, const int32_t *expert_ids, const float *ex
         std::lock_guard<std::mutex> lk(g_mu);
         moe_kernel = g_moe_kernel;
     }
-    const bool grouped = moe_kernel == 1 || (moe_kernel == 0 && (int64_t)T * top_k <= (int64_t)48 * E);
+    // (other W_down formats run on the grouped kernel only)
+    const bool grouped = wd_fmt != kFmtQ4_K || moe_kernel == 1 ||
+                         (moe_kernel == 0 && (int64_t)T * top_k <= (int64_t)48 * E);
     RouteArgs r{};
     r.tile_rows = grouped ? moe_group_rows() : 128;
     r.ids = expert_ids;
@@ -360,7 +363,46 @@ zffn_status swiglu_moe(const void *x, const int32_t *expert_ids, const float *ex
     a.n_tiles_host = L.max_tiles;
     a.err = di.err_word;
     a.T = T; a.H = H; a.I = I; a.E = E;
-    return to_status(grouped ? launch_moe_group(a, s) : launch_ffn_tc(a, s));
+    return to_status(grouped ? launch_moe_group(a, wd_fmt, s) : launch_ffn_tc(a, s));
+}
+
+// The dense block with W_down in another format at T > 1: one expert on the
+// grouped kernel, groups of 32 consecutive tokens (the weights are unpacked
+// once per group).
+zffn_status swiglu_dense_grouped(const void *x, const void *Wg, const void *Wu, const void *Wd, int wd_fmt,
+                                 float *y, int T, int H, int I, void *stream, bool accumulate) {
+    const DeviceInfo &di = device_info();
+    if (di.device < 0) return ZFFN_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    const Layout L = layout_for(T, H, I, 1, 1);
+    Workspace *w = nullptr;
+    zffn_status st = ensure_workspace(L.total, &w);
+    if (st != ZFFN_OK) return st;
+    uint8_t *base = static_cast<uint8_t *>(w->ptr);
+    int4 *tiles = reinterpret_cast<int4 *>(base + L.tiles);
+    int *n_tiles = reinterpret_cast<int *>(base + L.n_tiles);
+    int *row_token = reinterpret_cast<int *>(base + L.row_token);
+    float *row_weight = reinterpret_cast<float *>(base + L.row_weight);
+    void *x16 = base + L.x16;
+    cudaError_t e = launch_dense_groups(T, moe_group_rows(), tiles, n_tiles, row_token, row_weight, s);
+    if (e == cudaSuccess)
+        e = launch_x_to_f16(x, x16, (int64_t)T * H, accumulate ? nullptr : y, (int64_t)T * H, s);
+    if (e != cudaSuccess) return to_status(e);
+    TcArgs a{};
+    a.x = x16;
+    a.x_rows = T;
+    a.Wg = static_cast<const uint8_t *>(Wg);
+    a.Wu = static_cast<const uint8_t *>(Wu);
+    a.Wd = static_cast<const uint8_t *>(Wd);
+    a.y = y;
+    a.tiles = tiles;
+    a.n_tiles_dev = n_tiles;
+    a.row_token = row_token;
+    a.row_weight = row_weight;
+    a.n_tiles_host = (T + moe_group_rows() - 1) / moe_group_rows();
+    a.err = di.err_word;
+    a.T = T; a.H = H; a.I = I; a.E = 1;
+    return to_status(launch_moe_group(a, wd_fmt, s));
 }
 
 }  // namespace
@@ -434,7 +476,19 @@ zffn_status swiglu_wd(const void *x, const int32_t *expert_ids, const float *exp
                  (reinterpret_cast<uintptr_t>(expert_weights) & 3))))
         return invalid("x, Wg, Wu must be 16-byte and Wd, y, expert_ids, expert_weights 4-byte aligned");
     if (reinterpret_cast<uintptr_t>(down_scale) & 3) return invalid("down_scale must be 4-byte aligned");
-    if (T != 1) return ZFFN_ERR_UNSUPPORTED;       // other formats: single-token paths only
+    if (T != 1) {
+        // the grouped tensor-core kernel takes Q5_K and Q5_1 W_down; Q6_K
+        // rows (210-byte blocks) miss the 16-byte row pitch of its TMA loads
+        if (wd_fmt == kFmtQ6_K) {
+            set_last_error("W_down in Q6_K is supported for T = 1 only");
+            return ZFFN_ERR_UNSUPPORTED;
+        }
+        if (!aligned16(Wd) || !aligned16(y)) return invalid("for T > 1, Wd and y must be 16-byte aligned");
+        if (moe)
+            return swiglu_moe(x, expert_ids, expert_weights, down_scale, Wg, Wu, Wd, y, T, H, I, E, top_k,
+                              stream, accumulate, wd_fmt);
+        return swiglu_dense_grouped(x, Wg, Wu, Wd, wd_fmt, y, T, H, I, stream, accumulate);
+    }
     const int k = moe ? top_k : 1;
     const DeviceInfo &di = device_info();
     if (di.device < 0) return ZFFN_ERR_CUDA;

@@ -112,6 +112,27 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const __nv_bfloat16 *__
     }
 }
 
+// A dense block run as one expert on the grouped kernel: consecutive groups of
+// `rows` tokens, weight 1.
+__global__ void __launch_bounds__(256) dense_groups_kernel(int T, int rows, int4 *tiles, int *n_tiles,
+                                                           int *row_token, float *row_weight) {
+    const int n = (T + rows - 1) / rows;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T; i += gridDim.x * blockDim.x) {
+        row_token[i] = i;
+        row_weight[i] = 1.0f;
+        if (i % rows == 0) tiles[i / rows] = make_int4(i, min(rows, T - i), 0, 0);
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) *n_tiles = n;
+}
+
+cudaError_t launch_dense_groups(int T, int rows, int4 *tiles, int *n_tiles, int *row_token, float *row_weight,
+                                cudaStream_t s) {
+    int grid = (T + 255) / 256;
+    if (grid > device_info().num_sms * 4) grid = device_info().num_sms * 4;
+    dense_groups_kernel<<<grid, 256, 0, s>>>(T, rows, tiles, n_tiles, row_token, row_weight);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_moe_route(const RouteArgs &a, cudaStream_t s) {
     const size_t smem = (size_t)(3 * a.E + kRouteThreads) * sizeof(int);
     if (smem > 48 * 1024) {

@@ -40,10 +40,19 @@
 //   warp 7      idle
 #include <cudaTypedefs.h>
 
+#include "formats.h"
 #include "zffn_internal.cuh"
 
 namespace zffn {
 namespace mg {
+
+// Bytes of one row's 256 W_down weights in format F (whole blocks: Q5_1 has
+// eight 24-byte blocks per 256 weights); the down phase's packed boxes are
+// [128 rows x WD_BOX(F) bytes].  All are multiples of 16 bytes, as TMA needs.
+template <int F>
+__host__ __device__ constexpr int wd_box_bytes() {
+    return F == kFmtQ5_K ? 176 : F == kFmtQ5_1 ? 192 : 144;
+}
 
 constexpr int NG = 32;                       // token rows of a group (UMMA N)
 constexpr int BM = 128;                      // weight rows of a UMMA (M)
@@ -130,6 +139,80 @@ __device__ __forceinline__ Unit make_unit(const Params &p, int u, int n_tiles) {
     return un;
 }
 
+// Two K steps (128 weights of one nibble half) of a W_down row in Q5_K or
+// Q5_1, into the TMEM operand layout (column c of a K step holds weights 2c,
+// 2c+1 as an fp16 pair).  The 5-bit code q4 + 16 q5 splits into the 4-bit
+// part, turned into fp16 as for Q4_K, and the fifth bit, a second code 0/1
+// through the same converter, added with 16 times the scale:
+//     w = (q4 2^-9) (512 d sc) + (q5 2^-9) (8192 d sc) - dmin m   (Q5_K)
+//     w = (q4 2^-9) (512 d) + (q5 2^-9) (8192 d) + m              (Q5_1)
+// two roundings to fp16 instead of one.  row: the row's bytes of the packed
+// stage; ks0: the first K step (even) within the 256 weights; h: nibble half.
+// out[j][16]: the TMEM words of K step ks0 + j for this thread's half.
+template <int F>
+__device__ __forceinline__ void unpack_wd_pair_fmt(uint32_t row, int ks0, int h, uint32_t (&out)[2][16]) {
+    if (F == kFmtQ5_K) {
+        const uint4 hd = ld_shared_v4(row);
+        const uint4 qh0 = ld_shared_v4(row + 16), qh1 = ld_shared_v4(row + 32);
+        const uint32_t qh[8] = {qh0.x, qh0.y, qh0.z, qh0.w, qh1.x, qh1.y, qh1.z, qh1.w};
+        const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int g = ks0 + j, sb = 2 * g + h;
+            int sc, m;
+            q4k_scale_min(hd.y, hd.z, hd.w, sb, sc, m);
+            const uint32_t a = f16x2_splat_satfinite(512.0f * (d * (float)sc));
+            const uint32_t a16 = f16x2_splat_satfinite(8192.0f * (d * (float)sc));
+            const uint32_t b = f16x2_splat_satfinite(-(dmin * (float)m));
+            const uint4 c0 = ld_shared_v4(row + 48 + 32 * g), c1 = ld_shared_v4(row + 64 + 32 * g);
+            const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                uint32_t o0, o1, f0, f1;
+                codes4_to_f16((w[i] >> (4 * h)) & 0x0F0F0F0Fu, a, b, o0, o1);
+                // fifth bits of weights 4i..4i+3 of sub-block sb: bit sb of qh bytes 4i..4i+3
+                const uint32_t zero = 0u;
+                codes4_to_f16((qh[i] >> sb) & 0x01010101u, a16, zero, f0, f1);
+                out[j][2 * i] = fma_f16x2(0x3C003C00u, f0, o0);      // 1.0 * fifth + low part
+                out[j][2 * i + 1] = fma_f16x2(0x3C003C00u, f1, o1);
+            }
+        }
+    } else {   // Q5_1: eight 24-byte blocks per 256 weights, two per K step
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+#pragma unroll
+            for (int bb = 0; bb < 2; ++bb) {
+                const uint32_t blk = row + 24u * (uint32_t)(2 * (ks0 + j) + bb);
+                uint32_t dm, qh;
+                uint2 qa, qb;
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(dm) : "r"(blk));
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(qh) : "r"(blk + 4));
+                asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(qa.x), "=r"(qa.y) : "r"(blk + 8));
+                asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(qb.x), "=r"(qb.y) : "r"(blk + 16));
+                const float d = half_bits_to_float(dm);
+                const uint32_t a = f16x2_splat_satfinite(512.0f * d);
+                const uint32_t a16 = f16x2_splat_satfinite(8192.0f * d);
+                const uint32_t b = (dm >> 16) | (dm & 0xFFFF0000u);   // m, both halves
+                const uint32_t qs[4] = {qa.x, qa.y, qb.x, qb.y};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    // weights 16h + 4i .. +3 of the block: nibble h of qs bytes 4i..4i+3
+                    uint32_t o0, o1, f0, f1;
+                    codes4_to_f16((qs[i] >> (4 * h)) & 0x0F0F0F0Fu, a, b, o0, o1);
+                    // their fifth bits, qh bits 16h + 4i .. +3, one per byte
+                    const uint32_t hb = (((qh >> (16 * h + 4 * i)) & 15u) * 0x00204081u) & 0x01010101u;
+                    const uint32_t zero = 0u;
+                    codes4_to_f16(hb, a16, zero, f0, f1);
+                    // columns 16 bb + 8 h + 2 i, +1 of the K step
+                    out[j][8 * bb + 2 * i] = fma_f16x2(0x3C003C00u, f0, o0);
+                    out[j][8 * bb + 2 * i + 1] = fma_f16x2(0x3C003C00u, f1, o1);
+                }
+            }
+        }
+    }
+}
+
+template <int F>
 __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_constant__ Maps maps, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -214,8 +297,8 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
                         const int bb = b - un.n_ib * nbs_g;
                         const int hb = bb / nbs_y, kb = bb % nbs_y;
                         const int row = un.expert * p.H + hb * BM;
-                        mbar_arrive_expect_tx(&r_full[ri], R_BOX);
-                        tma_load_2d(rs, &maps.wd, &r_full[ri], (un.i0 / 256 + kb) * kBlockBytes, row);
+                        mbar_arrive_expect_tx(&r_full[ri], BM * wd_box_bytes<F>());
+                        tma_load_2d(rs, &maps.wd, &r_full[ri], (un.i0 / 256 + kb) * wd_box_bytes<F>(), row);
                     }
                     ++issued;
                     if (++ri == NR) { ri = 0; rph ^= 1; }
@@ -360,6 +443,41 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
                 const uint32_t ai = (2 * pair) % NA, aph = ((2 * pair) / NA) & 1;
                 const bool zero = gu && cur_blk * BM + r >= un.ic;
                 if (!mbar_wait(&r_full[ri], rph, abort_flag, p.err)) { ok = false; break; }
+                if (F != kFmtQ4_K && !gu) {
+                    // W_down in Q5_K / Q5_1: the format's unpack reads the
+                    // packed stage itself; the stage is released after it
+                    if (!mbar_wait(&a_empty[ai], aph ^ 1, abort_flag, p.err) ||
+                        !mbar_wait(&a_empty[ai + 1], aph ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    tc_fence_after();
+                    uint32_t v[2][16];
+                    unpack_wd_pair_fmt<F>(s_r + ri * R_BYTES + (uint32_t)(r * wd_box_bytes<F>()), cur_ks & 3, task, v);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&r_empty[ri]);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        if ((cur_ks + j) * BK >= un.ic) {   // past the chunk's width: zeros
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[j][i] = 0u;
+                        }
+                        const uint32_t dst = t_row + COL_A + (ai + j) * A_COLS;
+                        if (F == kFmtQ5_K) {
+                            tmem_st_32x32b_x16(dst + 16 * task, v[j]);
+                        } else {   // Q5_1: columns 8 task .. +7 of each 32-weight block
+                            const uint32_t v0[8] = {v[j][0], v[j][1], v[j][2], v[j][3], v[j][4], v[j][5], v[j][6], v[j][7]};
+                            const uint32_t v1[8] = {v[j][8], v[j][9], v[j][10], v[j][11], v[j][12], v[j][13], v[j][14], v[j][15]};
+                            tmem_st_32x32b_x8(dst + 8 * task, v0);
+                            tmem_st_32x32b_x8(dst + 16 + 8 * task, v1);
+                        }
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&a_full[ai]);
+                        mbar_arrive(&a_full[ai + 1]);
+                    }
+                    continue;
+                }
                 uint4 hd = make_uint4(0, 0, 0, 0), c[4] = {hd, hd, hd, hd};
                 if (!zero) {
                     const uint32_t src = s_r + ri * R_BYTES + (gu ? task * R_BOX : 0) + r * kBlockBytes;
@@ -387,6 +505,10 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
                         for (int i = 0; i < 8; ++i)
                             codes4_to_f16((w[i] >> (4 * h)) & 0x0F0F0F0Fu, sa[2 * j + h], sb[2 * j + h],
                                           v[2 * i], v[2 * i + 1]);
+                        if (!gu && (cur_ks + j) * BK >= un.ic) {   // past the chunk's width: zeros
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[i] = 0u;
+                        }
                         // gate/up: row's columns 32 task + 16 h; down: 16 h
                         tmem_st_32x32b_x16(dst + (gu ? 32 * task : 0) + 16 * h, v);
                     }
@@ -503,7 +625,8 @@ static bool encode_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *m,
 
 int moe_group_rows() { return mg::NG; }
 
-cudaError_t launch_moe_group(const TcArgs &a, cudaStream_t s) {
+cudaError_t launch_moe_group(const TcArgs &a, int wd_fmt, cudaStream_t s) {
+    if (wd_fmt != kFmtQ4_K && wd_fmt != kFmtQ5_K && wd_fmt != kFmtQ5_1) return cudaErrorInvalidValue;
     const DeviceInfo &di = device_info();
     if (a.H % 256 != 0 || a.I % 64 != 0) return cudaErrorInvalidValue;
     void *ptr = nullptr;
@@ -513,7 +636,9 @@ cudaError_t launch_moe_group(const TcArgs &a, cudaStream_t s) {
         return cudaErrorNotSupported;
     auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
     mg::Maps maps;
-    const int64_t rbH = q4k_row_bytes(a.H), rbI = q4k_row_bytes(a.I);
+    const int64_t rbH = q4k_row_bytes(a.H), rbI = fmt_row_bytes(wd_fmt, a.I);
+    const int wd_box = wd_fmt == kFmtQ5_K ? mg::wd_box_bytes<kFmtQ5_K>()
+                     : wd_fmt == kFmtQ5_1 ? mg::wd_box_bytes<kFmtQ5_1>() : mg::wd_box_bytes<kFmtQ4_K>();
     if (!encode_map(encode, &maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.x, a.H, a.x_rows, (int64_t)a.H * 2,
                     mg::BK, mg::NG, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_map(encode, &maps.wg, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wg, rbH, (int64_t)a.E * a.I, rbH,
@@ -521,9 +646,12 @@ cudaError_t launch_moe_group(const TcArgs &a, cudaStream_t s) {
         !encode_map(encode, &maps.wu, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wu, rbH, (int64_t)a.E * a.I, rbH,
                     kBlockBytes, mg::BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_map(encode, &maps.wd, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wd, rbI, (int64_t)a.E * a.H, rbI,
-                    kBlockBytes, mg::BM, CU_TENSOR_MAP_SWIZZLE_NONE))
+                    wd_box, mg::BM, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    cudaError_t e = ensure_dynamic_smem((const void *)mg::moe_group_kernel, (size_t)mg::SMEM_BYTES);
+    const void *fn = wd_fmt == kFmtQ5_K ? (const void *)mg::moe_group_kernel<kFmtQ5_K>
+                   : wd_fmt == kFmtQ5_1 ? (const void *)mg::moe_group_kernel<kFmtQ5_1>
+                                        : (const void *)mg::moe_group_kernel<kFmtQ4_K>;
+    cudaError_t e = ensure_dynamic_smem(fn, (size_t)mg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     mg::Params p;
     p.y = a.y;
@@ -539,8 +667,8 @@ cudaError_t launch_moe_group(const TcArgs &a, cudaStream_t s) {
     int64_t grid = (int64_t)a.n_tiles_host * n_chunks;
     if (grid > di.num_sms) grid = di.num_sms;
     if (grid < 1) return cudaSuccess;
-    mg::moe_group_kernel<<<(unsigned)grid, mg::THREADS, mg::SMEM_BYTES, s>>>(maps, p);
-    return cudaGetLastError();
+    void *kargs[] = {&maps, &p};
+    return cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(mg::THREADS), kargs, (size_t)mg::SMEM_BYTES, s);
 }
 
 }  // namespace zffn

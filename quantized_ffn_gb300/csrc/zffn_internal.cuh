@@ -624,7 +624,8 @@ cudaError_t launch_ffn_tc(const TcArgs &a, cudaStream_t s);
 // Routed layer with few rows per expert: groups of at most moe_group_rows()
 // gathered rows of one expert, weights as the MMA's M side (moe_tc.cu).
 int moe_group_rows();
-cudaError_t launch_moe_group(const TcArgs &a, cudaStream_t s);
+// wd_fmt: the W_down block format (Q4_K, Q5_K or Q5_1; a.Wd rows of its row bytes)
+cudaError_t launch_moe_group(const TcArgs &a, int wd_fmt, cudaStream_t s);
 
 // MoE routing on the device: bucket (token, slot) pairs by expert, build the
 // tile table and the row maps, gather x rows per expert.
@@ -646,6 +647,10 @@ struct RouteArgs {
     int tile_rows;      // rows per tile: 128 (prefill kernel) or the grouped kernel's group
 };
 cudaError_t launch_moe_route(const RouteArgs &a, cudaStream_t s);
+// The tile table of a dense block run as one expert: groups of `rows`
+// consecutive tokens, row_token[i] = i, row_weight[i] = 1.
+cudaError_t launch_dense_groups(int T, int rows, int4 *tiles, int *n_tiles, int *row_token, float *row_weight,
+                                cudaStream_t s);
 
 cudaError_t launch_wait_timeout_selftest(int64_t budget_cycles, int *err, cudaStream_t s);
 

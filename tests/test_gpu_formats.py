@@ -69,7 +69,45 @@ def test_q4k_format_code_is_the_regular_block():
     assert_close(y, orc.swiglu_ffn(x, *W, 5, H, I), "Q4_K through the format entry")
 
 
-def test_other_formats_reject_several_tokens():
+@pytest.mark.parametrize("fmt", [zffn.FMT_Q5_K, zffn.FMT_Q5_1])
+@pytest.mark.parametrize("T,H,I", [(2, 256, 704), (33, 1024, 1472), (100, 512, 384), (40, 256, 2048)])
+def test_several_tokens_dense(fmt, T, H, I):
+    # T > 1: the grouped tensor-core kernel (groups of 32 tokens); shapes with a
+    # partial last block (704, 1472, 384), a group boundary (33), several
+    # groups (100), several intermediate chunks (2048)
+    rng = np.random.default_rng(400 + fmt + T + I)
+    Wg = synth.random_q4k_blocks(rng, I, H, 1e-2)
+    Wu = synth.random_q4k_blocks(rng, I, H, 1e-2)
+    Wd = synth.random_blocks(rng, fmt, H, I, 1e-2)
+    x = synth.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    y = zffn.swiglu_q4k_wd(x_dev(x), dev(Wg), dev(Wu), dev(Wd), fmt, I)
+    assert zffn.get_device_error() == zffn.OK
+    assert_close(y, orc.swiglu_ffn(x, Wg, Wu, Wd, T, H, I, wd_fmt=fmt), f"fmt {fmt} T={T} H={H} I={I}")
+
+
+@pytest.mark.parametrize("fmt", [zffn.FMT_Q5_K, zffn.FMT_Q5_1])
+def test_several_tokens_routed_full_config(fmt):
+    # E = 128, H = 2048, I = 768, top-8, T = 64, every expert's W_down in fmt,
+    # with a per-expert down scale and an invalid slot
+    E, H, I, k, T = 128, 2048, 768, 8, 64
+    rng = np.random.default_rng(500 + fmt)
+    Wg = np.stack([synth.random_q4k_blocks(rng, I, H, 1e-2) for _ in range(E)])
+    Wu = np.stack([synth.random_q4k_blocks(rng, I, H, 1e-2) for _ in range(E)])
+    Wd = np.stack([synth.random_blocks(rng, fmt, H, I, 1e-2) for _ in range(E)])
+    ids, w = orc.route_top_k(rng.standard_normal((T, E)).astype(np.float32), k)
+    ids[5, 2] = -1
+    scale = rng.uniform(0.5, 1.5, E).astype(np.float32)
+    x = synth.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    y = zffn.moe_swiglu_q4k_scaled(x_dev(x), dev(ids), dev(w), dev(scale), dev(Wg), dev(Wu), dev(Wd), I, E,
+                                   wd_fmt=fmt)
+    assert zffn.get_device_error() == zffn.OK
+    rows = [0, 5, 31, 32, 63]
+    ref = orc.moe_swiglu_ffn(x[rows].copy(), ids[rows].copy(), w[rows].copy(), Wg, Wu, Wd, len(rows), H, I, E,
+                             k, wd_fmt=fmt, down_scale=scale)
+    assert_close(y[rows], ref, f"routed T=64 fmt {fmt}")
+
+
+def test_q6k_rejects_several_tokens():
     rng = np.random.default_rng(301)
     H, I = 256, 256
     W = [dev(synth.random_q4k_blocks(rng, I, H)), dev(synth.random_q4k_blocks(rng, I, H)),
