@@ -219,9 +219,11 @@ zffn_status zffn_dequant_fmt(int fmt, const void *blocks, float *out, int64_t ro
  * backend...", section "Bottleneck 4": Q4_K, Q5_K and Q6_K GEMMs of prefill).
  * ZFFN_FMT_Q4_K is zffn_swiglu_q4k.
  *   T = 1: the single-token kernels, every format.  Wd must be 4-byte aligned
- *     (its rows need not be: Q6_K rows are 210-byte multiples).  UNSUPPORTED
- *     when top_k * I fp32 values of h plus 64 KB of row buffers exceed a
- *     block's shared memory (I > 40960 at top_k = 1).
+ *     (its rows need not be: Q6_K rows are 210-byte multiples).  h is held
+ *     in shared memory as int16 with one fp32 scale per 32 and per 8 values
+ *     (2.625 bytes a value); UNSUPPORTED when top_k * I such values plus
+ *     64 KB of row buffers exceed a block's shared memory (I > 63488 at
+ *     top_k = 1 with 227 KB).
  *   T > 1: Q5_K and Q5_1 on the grouped tensor-core kernel (the routed
  *     kernel's groups of 32 token rows; a dense block runs as one expert), Wd
  *     and y 16-byte aligned.  Its weights are unpacked once per group of 32
@@ -292,8 +294,8 @@ zffn_status zffn_moe_router_topk(const float *logits, int32_t *expert_ids,
  *   down_scale: fp32 [E] (device, 4-byte aligned), or NULL for every scale 1.
  *     It multiplies the routing weight of each (token, slot) in fp32 before the
  *     down projection's output is added.
- *   wd_fmt: block format of every expert's W_down (zffn_format); formats other
- *     than ZFFN_FMT_Q4_K take T = 1 only, as for zffn_moe_swiglu_q4k_wd.
+ *   wd_fmt: block format of every expert's W_down (zffn_format), with the
+ *     same rules as zffn_moe_swiglu_q4k_wd (Q6_K at T > 1 is UNSUPPORTED).
  *   accumulate: 0 overwrites y, non-zero adds the block's output to y.
  *   The other arguments as for zffn_moe_swiglu_q4k (expert_ids and
  *   expert_weights must not be NULL).

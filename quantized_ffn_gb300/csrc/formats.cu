@@ -139,40 +139,44 @@ __device__ __forceinline__ uint32_t byte8(uint32_t lo, uint32_t hi, int i) {
     return ((i < 4 ? lo : hi) >> (8 * (i & 3))) & 0xFFu;
 }
 
-// Dot product of weights k0 .. k0+7 of a 256-weight unit (one block; Q5_1:
-// eight blocks) with v[0..7].  The eight weights share one scale, so the
-// header is decoded once; each value is the format's exact product (plus at
-// most one rounding of the offset), as in fmt_weight.
+// Dot product of eight weights with h: h is held as int16 per 32-element group (scale vs)
+// with the fp32 sum of every 8 elements (hs8), and the codes go into int8
+// lanes for dp2a; the offsets of the formats (the min of Q5_K, the -32 of
+// Q6_K, the m of Q5_1) multiply hs8 instead of each weight.
+//   Q4_K/Q5_K: sum w*h = d*sc * vs * sum(q*h_int) - dmin*m * hs8
+//   Q6_K:      sum w*h = d*sc * (vs * sum(q*h_int) - 32 * hs8)
+//   Q5_1:      sum w*h = d * vs * sum(q*h_int) + m * hs8
 template <int F>
-__device__ __forceinline__ float dot8(const uint8_t *unit, int k0, const float (&v)[8]) {
-    float r = 0.0f;
+__device__ __forceinline__ float dot8i(const uint8_t *unit, int k0, uint4 hq, float vs, float hs8) {
+    uint32_t c0, c1;   // the eight codes, one per byte (0..63)
+    float a, b;        // result = a * isum + b
     if (F == kFmtQ6_K) {
         const int n = k0 >> 7, rr = k0 & 127, i = rr >> 5, l = rr & 31;
         uint32_t l0, l1, h0, h1;
         load8(unit + 64 * n + l + 32 * (i & 1), l0, l1);
         load8(unit + 128 + 32 * n + l, h0, h1);
-        const int sc = (int)(int8_t)unit[192 + (k0 >> 4)];
-        const float d = fp16_at(unit + 208);
         const int lsh = i < 2 ? 0 : 4, hsh = 2 * i;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            const int q = (int)((byte8(l0, l1, t) >> lsh) & 15u) | (int)(((byte8(h0, h1, t) >> hsh) & 3u) << 4);
-            r = fmaf(d * (float)(sc * (q - 32)), v[t], r);
-        }
+        c0 = ((l0 >> lsh) & 0x0F0F0F0Fu) | (((h0 >> hsh) & 0x03030303u) << 4);
+        c1 = ((l1 >> lsh) & 0x0F0F0F0Fu) | (((h1 >> hsh) & 0x03030303u) << 4);
+        const float ds = fp16_at(unit + 208) * (float)(int)(int8_t)unit[192 + (k0 >> 4)];
+        a = ds * vs;
+        b = -32.0f * ds * hs8;
     } else if (F == kFmtQ5_1) {
         const uint8_t *blk = unit + (k0 >> 5) * 24;
         const int j0 = k0 & 31;
-        const float d = fp16_at(blk), m = fp16_at(blk + 2);
         uint32_t q0, q1;
         load8(blk + 8 + (j0 & 15), q0, q1);
         const uint32_t qh = (uint32_t)blk[4] | ((uint32_t)blk[5] << 8) | ((uint32_t)blk[6] << 16) |
                             ((uint32_t)blk[7] << 24);
         const int nsh = j0 < 16 ? 0 : 4;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            const int q = (int)((byte8(q0, q1, t) >> nsh) & 15u) | (int)(((qh >> (j0 + t)) & 1u) << 4);
-            r = fmaf(fmaf(d, (float)q, m), v[t], r);
-        }
+        // four bits b0..b3 to the low bit of four bytes: b * (1 + 2^7 + 2^14 + 2^21)
+        // puts bit i at bit 8i (the partial products do not overlap)
+        const uint32_t b_lo = ((((qh >> j0) & 0xFu) * 0x00204081u) & 0x01010101u) << 4;
+        const uint32_t b_hi = ((((qh >> (j0 + 4)) & 0xFu) * 0x00204081u) & 0x01010101u) << 4;
+        c0 = ((q0 >> nsh) & 0x0F0F0F0Fu) | b_lo;
+        c1 = ((q1 >> nsh) & 0x0F0F0F0Fu) | b_hi;
+        a = fp16_at(blk) * vs;
+        b = fp16_at(blk + 2) * hs8;
     } else {
         const int j = k0 >> 5;
         const uint8_t *sb = unit + 4;
@@ -184,25 +188,29 @@ __device__ __forceinline__ float dot8(const uint8_t *unit, int k0, const float (
             sc = (sb[j + 4] & 15) | ((sb[j - 4] >> 6) << 4);
             m = (sb[j + 4] >> 4) | ((sb[j] >> 6) << 4);
         }
-        const float ds = fp16_at(unit) * (float)sc;       // exact
-        const float dm = fp16_at(unit + 2) * (float)m;    // exact
         uint32_t q0, q1;
         load8(unit + (F == kFmtQ5_K ? 48 : 16) + 32 * (k0 >> 6) + (k0 & 31), q0, q1);
         const int nsh = (k0 & 32) ? 4 : 0;
-        uint32_t b0 = 0, b1 = 0;
-        if (F == kFmtQ5_K) load8(unit + 16 + (k0 & 31), b0, b1);
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            int q = (int)((byte8(q0, q1, t) >> nsh) & 15u);
-            if (F == kFmtQ5_K) q |= (int)((byte8(b0, b1, t) >> j) & 1u) << 4;
-            r = fmaf(fmaf(ds, (float)q, -dm), v[t], r);    // ds*q exact: one rounding
+        c0 = (q0 >> nsh) & 0x0F0F0F0Fu;
+        c1 = (q1 >> nsh) & 0x0F0F0F0Fu;
+        if (F == kFmtQ5_K) {
+            uint32_t e0, e1;
+            load8(unit + 16 + (k0 & 31), e0, e1);
+            c0 |= ((e0 >> j) & 0x01010101u) << 4;
+            c1 |= ((e1 >> j) & 0x01010101u) << 4;
         }
+        a = fp16_at(unit) * (float)sc * vs;
+        b = -(fp16_at(unit + 2) * (float)m) * hs8;
     }
-    return r;
+    int isum = __dp2a_lo((int)hq.x, (int)c0, 0);
+    isum = __dp2a_hi((int)hq.y, (int)c0, isum);
+    isum = __dp2a_lo((int)hq.z, (int)c1, isum);
+    isum = __dp2a_hi((int)hq.w, (int)c1, isum);
+    return fmaf(a, (float)isum, b);
 }
 
-// Shared memory: h of every expert slot (fp32 [P][I]), then one row-chunk
-// buffer per warp.  A warp walks one stream of chunks: for each of its output
+// Each expert slot's h is held quantised in shared memory (layout in the
+// kernel), followed by one row-chunk buffer per warp.  A warp walks one stream of chunks: for each of its output
 // rows, for each valid expert slot, the row's whole 256-weight units a chunk
 // at a time.  The words of the next chunk are loaded into registers (all of a
 // lane's loads in flight) while the current chunk, already in the buffer, is
@@ -216,32 +224,45 @@ struct ChunkCursor {
 
 template <int F>
 __global__ void __launch_bounds__(kDownWarps * 32, 1) down_fmt_kernel(MatvecArgs a) {
-    extern __shared__ __align__(16) float hs[];
+    // Shared memory: h as int16 [P*I], its scale per 32 elements (fp32
+    // [P*I/32]) and its sum per 8 elements (fp32 [P*I/8]), then one row-chunk
+    // buffer per warp.
+    extern __shared__ __align__(16) uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = a.H, I = a.I, P = a.k;
     const bool moe = a.ids != nullptr;
-    uint8_t *buf = reinterpret_cast<uint8_t *>(hs + (size_t)P * I) + (size_t)warp * (kDownBuf + 16);
+    const int PI = P * I;
+    int16_t *hq = reinterpret_cast<int16_t *>(smem_raw);
+    float *hvs = reinterpret_cast<float *>(smem_raw + (size_t)PI * 2);
+    float *hs8 = hvs + PI / 32;
+    uint8_t *buf = reinterpret_cast<uint8_t *>(hs8 + PI / 8) + (size_t)warp * (kDownBuf + 16);
     // the next work in the stream may be scheduled as this grid's blocks leave
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // h is written by the gate/up kernel: wait until that grid has completed
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    {
-        // (loads first, then stores: a load is not held behind a store to a
-        // pointer the compiler cannot tell apart from it)
-        const float4 *h4 = reinterpret_cast<const float4 *>(a.h);
-        float4 *s4 = reinterpret_cast<float4 *>(hs);
-        const int n4 = P * I / 4;
-        for (int i0 = threadIdx.x; i0 < n4; i0 += 8 * blockDim.x) {
-            float4 r[8];
+    // quantise h: warp w takes the 32-element groups w, w + 16, ...; lane t
+    // element t of the group (loads of four groups issued together)
+    for (int g0 = warp; g0 < PI / 32; g0 += 4 * kDownWarps) {
+        float v[4];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int i = i0 + j * blockDim.x;
-                r[j] = i < n4 ? __ldcg(h4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+        for (int u = 0; u < 4; ++u) {
+            const int g = g0 + u * kDownWarps;
+            v[u] = g < PI / 32 ? __ldcg(a.h + (size_t)g * 32 + lane) : 0.0f;
+        }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int i = i0 + j * blockDim.x;
-                if (i < n4) s4[i] = r[j];
+        for (int u = 0; u < 4; ++u) {
+            const int g = g0 + u * kDownWarps;
+            float mx = fabsf(v[u]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            float s8 = v[u];
+#pragma unroll
+            for (int o = 4; o > 0; o >>= 1) s8 += __shfl_xor_sync(0xffffffffu, s8, o);
+            if (g < PI / 32) {
+                const float inv = mx > 0.0f ? 32767.0f / mx : 0.0f;
+                hq[(size_t)g * 32 + lane] = (int16_t)__float2int_rn(v[u] * inv);
+                if (lane == 0) hvs[g] = mx > 0.0f ? mx / 32767.0f : 0.0f;
+                if ((lane & 7) == 0) hs8[(size_t)g * 4 + (lane >> 3)] = s8;
             }
         }
     }
@@ -330,15 +351,14 @@ __global__ void __launch_bounds__(kDownWarps * 32, 1) down_fmt_kernel(MatvecArgs
         advance(nx);
         if (!nx.done) issue(nx);
         const uint8_t *sb = buf + (reinterpret_cast<uintptr_t>(src) - a0);
-        const float *hp = hs + (size_t)cur.p * I;
+        const size_t hbase = (size_t)cur.p * I;
         const int u1 = min(nu, cur.u0 + nuc);
         for (int u = cur.u0; u < u1; ++u) {
             const int c0 = u * 256 + k0;
             if (c0 >= I) continue;                  // past the row (I % 256 != 0)
-            const float4 va = *reinterpret_cast<const float4 *>(hp + c0);
-            const float4 vb = *reinterpret_cast<const float4 *>(hp + c0 + 4);
-            const float v[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-            part += dot8<F>(sb + (size_t)(u - cur.u0) * ub, k0, v);
+            const size_t hc = hbase + c0;           // a multiple of 8
+            const uint4 hv = *reinterpret_cast<const uint4 *>(hq + hc);
+            part += dot8i<F>(sb + (size_t)(u - cur.u0) * ub, k0, hv, hvs[hc >> 5], hs8[hc >> 3]);
         }
         if (u1 >= nu) {                             // last chunk of this slot's row
             float w = 1.0f;
@@ -360,7 +380,8 @@ __global__ void __launch_bounds__(kDownWarps * 32, 1) down_fmt_kernel(MatvecArgs
 }
 
 size_t down_fmt_smem_bytes(int I, int k) {
-    return (size_t)k * I * sizeof(float) + (size_t)kDownWarps * (kDownBuf + 16);
+    const size_t pi = (size_t)k * I;
+    return pi * 2 + pi / 32 * 4 + pi / 8 * 4 + (size_t)kDownWarps * (kDownBuf + 16);
 }
 
 cudaError_t launch_token_fmt(const MatvecArgs &a, int wd_fmt, cudaStream_t s) {

@@ -150,9 +150,10 @@ def test_format_row_bytes_and_rejections(lib):
     assert L.zffn_dequant_fmt(1, FAKE, FAKE, 0, 256, None) == zffn.ERR_INVALID_ARG
     assert L.zffn_swiglu_q4k_wd(FAKE, FAKE, FAKE, FAKE, 9, FAKE, 1, 256, 256, None) == zffn.ERR_INVALID_ARG
     assert L.zffn_swiglu_q4k_wd(FAKE, FAKE, FAKE, FAKE, 2, FAKE, 1, 200, 256, None) == zffn.ERR_INVALID_ARG
-    # other formats of W_down: single-token paths only (checked on the host)
+    # Q6_K W_down: single-token paths only (checked on the host); Q5_K and
+    # Q5_1 at T > 1 pass the host checks and need a device
     assert L.zffn_swiglu_q4k_wd(FAKE, FAKE, FAKE, FAKE, 2, FAKE, 4, 256, 256, None) == zffn.ERR_UNSUPPORTED
-    assert L.zffn_moe_swiglu_q4k_wd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 3, 256, 256, 8, 2,
+    assert L.zffn_moe_swiglu_q4k_wd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, FAKE, 3, 256, 256, 8, 2,
                                     None) == zffn.ERR_UNSUPPORTED
     assert L.zffn_moe_swiglu_q4k_wd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 1, 256, 256, 0, 2,
                                     None) == zffn.ERR_INVALID_ARG
