@@ -219,11 +219,13 @@ zffn_status zffn_dequant_fmt(int fmt, const void *blocks, float *out, int64_t ro
  * backend...", section "Bottleneck 4": Q4_K, Q5_K and Q6_K GEMMs of prefill).
  * ZFFN_FMT_Q4_K is zffn_swiglu_q4k.
  *   T = 1: the single-token kernels, every format.  Wd must be 4-byte aligned
- *     (its rows need not be: Q6_K rows are 210-byte multiples).  h is held
- *     in shared memory as int16 with one fp32 scale per 32 and per 8 values
- *     (2.625 bytes a value); UNSUPPORTED when top_k * I such values plus
- *     64 KB of row buffers exceed a block's shared memory (I > 63488 at
- *     top_k = 1 with 227 KB).
+ *     (its rows need not be: Q6_K rows are 210-byte multiples; a 16-byte
+ *     aligned Wd is copied faster).  h is held in shared memory as int16
+ *     with one fp32 scale per 32 and one fp32 sum per 16 values (2.375 bytes
+ *     a value); UNSUPPORTED when top_k * I such values plus the row buffers
+ *     (66 KB for Q5_K, 72 KB for Q5_1, 90 KB for Q6_K) exceed a block's
+ *     shared memory (227 KB: at top_k = 1 every I for Q5_K and Q5_1, I <=
+ *     58688 for Q6_K; at top_k = 8, I <= 8576, 8256 and 7296).
  *   T > 1: Q5_K and Q5_1 on the grouped tensor-core kernel (the routed
  *     kernel's groups of 32 token rows; a dense block runs as one expert), Wd
  *     and y 16-byte aligned.  Its weights are unpacked once per group of 32

@@ -493,7 +493,7 @@ zffn_status swiglu_wd(const void *x, const int32_t *expert_ids, const float *exp
     const DeviceInfo &di = device_info();
     if (di.device < 0) return ZFFN_ERR_CUDA;
     if (gu_smem_total(H, I, k) > (size_t)di.max_smem_optin ||
-        down_fmt_smem_bytes(I, k) > (size_t)di.max_smem_optin)
+        down_fmt_smem_bytes(wd_fmt, I, k) > (size_t)di.max_smem_optin)
         return ZFFN_ERR_UNSUPPORTED;
     const Layout L = layout_for(1, H, I, moe ? E : 1, k);
     Workspace *w = nullptr;

@@ -21,8 +21,9 @@ int64_t fmt_row_bytes(int f, int64_t cols);
 cudaError_t launch_dequant_fmt(int f, const void *blocks, float *out, int64_t rows, int64_t cols,
                                cudaStream_t s);
 
-// Shared memory of the down kernel (h of every slot, fp32).
-size_t down_fmt_smem_bytes(int I, int k);
+// Shared memory of the down kernel for W_down in format f (h of every slot,
+// quantised, and the warps' chunk buffers).
+size_t down_fmt_smem_bytes(int f, int I, int k);
 
 // One token (a.T == 1): the Q4_K gate/up kernel of the single-token path, then
 // the down projection with W_down in format wd_fmt (not Q4_K) as its

@@ -42,6 +42,61 @@ def test_single_token_block(fmt, H, I):
     assert_close(y, orc.swiglu_ffn(x, Wg, Wu, Wd, 1, H, I, wd_fmt=fmt), f"fmt {fmt} H={H} I={I}")
 
 
+def offset_copy(a, offset):
+    """a (uint8) on the device, starting `offset` bytes past a 16-byte boundary."""
+    buf = torch.zeros(a.nbytes + 32, dtype=torch.uint8, device="cuda")
+    assert buf.data_ptr() % 16 == 0
+    out = buf[offset:offset + a.nbytes]
+    out.copy_(torch.from_numpy(np.ascontiguousarray(a).reshape(-1).view(np.uint8)).cuda())
+    return out
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("H,I,wd_offset", [(256, 64, 4), (512, 192, 0), (768, 320, 8), (1024, 1472, 4),
+                                           (4096, 11008, 12)])
+def test_single_token_block_short_rows_and_unaligned_wd(fmt, H, I, wd_offset):
+    # rows of fewer than four 256-weight units (several output rows in one
+    # pass of a warp), and W_down 4, 8 or 12 bytes past a 16-byte boundary
+    # (copied in 4-byte words instead of 16-byte pieces)
+    rng = np.random.default_rng(600 + fmt + H + I + wd_offset)
+    Wg = synth.random_q4k_blocks(rng, I, H, 1e-2)
+    Wu = synth.random_q4k_blocks(rng, I, H, 1e-2)
+    Wd = synth.random_blocks(rng, fmt, H, I, 1e-2)
+    x = token(rng, H)
+    Wd_dev = offset_copy(Wd, wd_offset)
+    y = zffn.swiglu_q4k_wd(x_dev(x), dev(Wg), dev(Wu), Wd_dev, fmt, I)
+    assert zffn.get_device_error() == zffn.OK
+    assert_close(y, orc.swiglu_ffn(x, Wg, Wu, Wd, 1, H, I, wd_fmt=fmt), f"fmt {fmt} H={H} I={I} +{wd_offset}")
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_routed_single_token_unaligned_wd_and_no_valid_slot(fmt):
+    # every expert's W_down 4 bytes past a 16-byte boundary, slots in any
+    # order with repeats; then a token whose slots are all invalid: y = 0, or
+    # y unchanged when accumulating
+    E, H, I, k = 6, 512, 320, 5
+    rng = np.random.default_rng(700 + fmt)
+    Wg = np.stack([synth.random_q4k_blocks(rng, I, H, 1e-2) for _ in range(E)])
+    Wu = np.stack([synth.random_q4k_blocks(rng, I, H, 1e-2) for _ in range(E)])
+    Wd = np.stack([synth.random_blocks(rng, fmt, H, I, 1e-2) for _ in range(E)])
+    ids = np.array([[5, 0, 5, -1, 2]], dtype=np.int32)
+    w = rng.uniform(0.1, 1.0, (1, k)).astype(np.float32)
+    x = token(rng, H)
+    Wd_dev = offset_copy(Wd, 4)
+    y = zffn.moe_swiglu_q4k_wd(x_dev(x), dev(ids), dev(w), dev(Wg), dev(Wu), Wd_dev, fmt, I, E)
+    assert zffn.get_device_error() == zffn.OK
+    assert_close(y, orc.moe_swiglu_ffn(x, ids, w, Wg, Wu, Wd, 1, H, I, E, k, wd_fmt=fmt), f"routed fmt {fmt} +4")
+    bad = np.array([[-1, E, E + 7, -3, 99]], dtype=np.int32)
+    y = zffn.moe_swiglu_q4k_wd(x_dev(x), dev(bad), dev(w), dev(Wg), dev(Wu), Wd_dev, fmt, I, E)
+    assert zffn.get_device_error() == zffn.OK
+    assert torch.count_nonzero(y).item() == 0
+    y0 = torch.full((1, H), 0.25, dtype=torch.float32, device="cuda")
+    zffn.moe_swiglu_q4k_scaled(x_dev(x), dev(bad), dev(w), None, dev(Wg), dev(Wu), Wd_dev, I, E, wd_fmt=fmt,
+                               y=y0, accumulate=True)
+    assert zffn.get_device_error() == zffn.OK
+    assert torch.all(y0 == 0.25).item()
+
+
 @pytest.mark.parametrize("fmt", FORMATS)
 def test_routed_single_token_full_config(fmt):
     # E = 128, H = 2048, I = 768, top-8 with every expert's W_down in fmt

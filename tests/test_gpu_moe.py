@@ -104,7 +104,7 @@ def test_full_moe_config_256_tokens_sampled_rows():
 
 
 @pytest.mark.parametrize("T,path,fmt", [(1, 1, zffn.FMT_Q4_K), (37, 0, zffn.FMT_Q4_K),
-                                        (1, 1, zffn.FMT_Q5_K), (1, 1, zffn.FMT_Q5_1)])
+                                        (1, 1, zffn.FMT_Q5_K), (1, 1, zffn.FMT_Q5_1), (1, 1, zffn.FMT_Q6_K)])
 def test_per_expert_down_scale(T, path, fmt):
     # a scale on each expert's down projection, applied inside the routed call
     E, H, I, k = 8, 512, 384, 3
