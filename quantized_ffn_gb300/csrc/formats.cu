@@ -159,10 +159,18 @@ __device__ __forceinline__ void load32_at(const uint8_t *p, uint32_t (&o)[8]) {
     for (int i = 0; i < 8; ++i) o[i] = __funnelshift_r(v[i], v[i + 1], sh);
 }
 
+// 16 bytes of shared memory at the 32-bit shared address a.
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+
 // Dot product of the 64 weights of part jp (weights 64jp .. 64jp+63: groups
 // 2jp and 2jp+1 of 32) of one unit with h.  h is held as int16 (hline: the
-// 128-byte line of the part's 64 values, its 16-byte pieces stored in the
-// order piece ^ sw; vs: the scales of its two groups) with the fp32 sums of
+// shared address of the 128-byte line of the part's 64 values with the
+// line's swizzle in bits 4-6, so that piece i is at hline ^ (i << 4); vs:
+// the scales of its two groups) with the fp32 sums of
 // its four 16-value quarters (hs); the codes go into int8 lanes for dp2a and
 // the formats' offsets (the min of Q5_K, the -32 of Q6_K, the m of Q5_1)
 // multiply the sums of h instead of each weight.  Per group of 32:
@@ -172,12 +180,11 @@ __device__ __forceinline__ void load32_at(const uint8_t *p, uint32_t (&o)[8]) {
 // u: the unit's first byte (16-byte aligned for Q5_K and Q5_1, even for
 // Q6_K).  Independent partial sums keep the dp2a chains short.
 template <int F>
-__device__ __forceinline__ float dot64(const uint8_t *u, int jp, const uint8_t *hline, int sw, float2 vs,
-                                       float4 hs) {
+__device__ __forceinline__ float dot64(const uint8_t *u, int jp, uint32_t hline, float2 vs, float4 hs) {
     uint32_t hw[32];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(hline + ((i ^ sw) << 4));
+        const uint4 v = lds128(hline ^ (uint32_t)(i << 4));
         hw[4 * i] = v.x;
         hw[4 * i + 1] = v.y;
         hw[4 * i + 2] = v.z;
@@ -270,6 +277,23 @@ __device__ __forceinline__ float dot64(const uint8_t *u, int jp, const uint8_t *
     }
 }
 
+// q = n / d and r = n % d for 0 <= n < 2^24 and 1 <= d: the product with the
+// rounded reciprocal rd is within one of the quotient (its relative error is
+// below 2^-23 and n / d < 2^23 unless d == 1, where it is exact), and one
+// correction step fixes it.
+__device__ __forceinline__ int div_small(int n, int d, float rd, int &r) {
+    int q = __float2int_rz((float)n * rd);
+    r = n - q * d;
+    if (r < 0) {
+        --q;
+        r += d;
+    } else if (r >= d) {
+        ++q;
+        r -= d;
+    }
+    return q;
+}
+
 // Bulk copy global -> shared (16-byte aligned addresses, a multiple of 16
 // bytes), counted on the barrier bar.
 __device__ __forceinline__ void bulk_copy_to_smem(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
@@ -293,12 +317,12 @@ __device__ __forceinline__ void cp_async_wait_ahead2() { asm volatile("cp.async.
 // that lanes reading the same piece of different lines use different
 // banks), its scale per 32 values (fp32, P*I/32 rounded up to a multiple of
 // 4) and its sums per 16 values (fp32 pairs [P*I/32]), the valid expert
-// slots (index and weight, 64 each), a barrier per chunk buffer, then the
-// chunk buffers of every warp.
+// slots (index, weight and expert, 64 each) and their count, a barrier per
+// chunk buffer, then the chunk buffers of every warp.
 __host__ __device__ inline int down_fmt_ng_pad(int I, int k) { return ((k * I / 32) + 3) & ~3; }
 __host__ __device__ inline size_t down_fmt_h_bytes(int I, int k) {
     const size_t pi = (size_t)k * I;
-    return (pi * 2 + (size_t)down_fmt_ng_pad(I, k) * 4 + pi / 32 * 8 + 2 * 64 * 4 +
+    return (pi * 2 + (size_t)down_fmt_ng_pad(I, k) * 4 + pi / 32 * 8 + 3 * 64 * 4 + 16 +
             (size_t)kDownWarps * kChunkBufs * 8 + 15) & ~(size_t)15;
 }
 size_t down_fmt_smem_bytes(int f, int I, int k) {
@@ -324,18 +348,26 @@ struct UnitInfo {
 
 template <int F>
 __global__ void __launch_bounds__(kDownWarps * 32, 1) down_fmt_kernel(MatvecArgs a) {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
+    extern __shared__ __align__(128) uint8_t smem_raw[];
     constexpr int UB = fmt_unit_bytes(F), SB = fmt_slot_bytes(F), K = fmt_chunk_units(F);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = a.H, I = a.I, P = a.k;
     const bool moe = a.ids != nullptr;
     const int PI = P * I, NG = PI / 32;
     int16_t *hq = reinterpret_cast<int16_t *>(smem_raw);
+    const uint32_t hq_s = smem_u32(hq);
+    // the swizzled reads of h take its lines to start on 128-byte boundaries
+    if (hq_s & 127u) {
+        if (threadIdx.x == 0) record_error(a.err, ZFFN_ERR_UNSUPPORTED);
+        return;
+    }
     float *hvs = reinterpret_cast<float *>(smem_raw + (size_t)PI * 2);
     float2 *hs16 = reinterpret_cast<float2 *>(hvs + down_fmt_ng_pad(I, P));
     int *vslot = reinterpret_cast<int *>(hs16 + NG);
     float *wslot = reinterpret_cast<float *>(vslot + 64);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(wslot + 64) + warp * kChunkBufs;
+    int *eslot = reinterpret_cast<int *>(wslot + 64);
+    int *nvalid = eslot + 64;             // the number of valid slots (16 bytes reserved)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(eslot + 68) + warp * kChunkBufs;
     uint8_t *buf = smem_raw + down_fmt_h_bytes(I, P) + (size_t)warp * kChunkBufs * K * SB;
     // the block's output rows [n0, n1)
     const int n0 = (int)((int64_t)H * blockIdx.x / gridDim.x);
@@ -359,7 +391,6 @@ __global__ void __launch_bounds__(kDownWarps * 32, 1) down_fmt_kernel(MatvecArgs
     // h is written by the gate/up kernel: wait until that grid has completed
     asm volatile("griddepcontrol.wait;" ::: "memory");
     // the valid expert slots, in slot order, with their weights
-    __shared__ int s_nvalid;
     if (warp == 0) {
         int base = 0;
         for (int p0 = 0; p0 < P; p0 += 32) {
@@ -376,18 +407,19 @@ __global__ void __launch_bounds__(kDownWarps * 32, 1) down_fmt_kernel(MatvecArgs
                 }
                 vslot[at] = p;
                 wslot[at] = w;
+                eslot[at] = e;
             }
             base += __popc(bal);
         }
-        if (lane == 0) s_nvalid = base;
+        if (lane == 0) *nvalid = base;
     }
     if (threadIdx.x == 0) {
-        uint64_t *all = reinterpret_cast<uint64_t *>(wslot + 64);
+        uint64_t *all = reinterpret_cast<uint64_t *>(eslot + 68);
         for (int i = 0; i < kDownWarps * kChunkBufs; ++i) mbar_init(&all[i], 1);
         fence_mbarrier_init();
     }
     __syncthreads();
-    const int V = s_nvalid;
+    const int V = *nvalid;
     // warp w takes the rows n0 + w, n0 + w + kDownWarps, ...
     const int gw = kDownWarps;
     const int n_first = n0 + warp;
@@ -410,13 +442,26 @@ __global__ void __launch_bounds__(kDownWarps * 32, 1) down_fmt_kernel(MatvecArgs
     const bool bulk = (reinterpret_cast<uintptr_t>(a.Wd) & 15) == 0;
     const uint32_t buf_s = (uint32_t)__cvta_generic_to_shared(buf);
 
+    // stream position s -> (row, slot, unit): reciprocal divisions while
+    // every position is below 2^24 (always, unless a launch has very few
+    // blocks)
+    const bool fdiv = S < (1 << 24);
+    const float rR = 1.0f / (float)R, rnu = 1.0f / (float)nu;
     auto info = [&](int s) {
         UnitInfo ui{nullptr, 0, 0, 0, 0};
         if (s < S) {
-            const int ri = s / R, rem = s - ri * R;
-            const int vi = rem / nu, u = rem - vi * nu;
+            int ri, rem, vi, u;
+            if (fdiv) {
+                ri = div_small(s, R, rR, rem);
+                vi = div_small(rem, nu, rnu, u);
+            } else {
+                ri = s / R;
+                rem = s - ri * R;
+                vi = rem / nu;
+                u = rem - vi * nu;
+            }
             const int p = vslot[vi];
-            const int e = moe ? a.ids[p] : 0;
+            const int e = eslot[vi];
             const int n = n_first + ri * gw;
             ui.src = a.Wd + ((int64_t)e * H + n) * rb + (int64_t)u * UB;
             ui.nbytes = (int)min((int64_t)UB, rb - (int64_t)u * UB);
@@ -547,7 +592,7 @@ __global__ void __launch_bounds__(kDownWarps * 32, 1) down_fmt_kernel(MatvecArgs
             if (g < kc && 64 * jp < lim) {
                 const int hi = hb + 64 * jp;
                 v = wslot[vi] * dot64<F>(cb + (size_t)g * SB + off, jp,
-                                         reinterpret_cast<const uint8_t *>(hq) + 2 * (size_t)hi, (hi >> 6) & 7,
+                                         hq_s + 2u * (uint32_t)hi + ((uint32_t)(hi >> 6) & 7u) * 16u,
                                          *reinterpret_cast<const float2 *>(hvs + (hi >> 5)),
                                          *reinterpret_cast<const float4 *>(hs16 + (hi >> 5)));
             }
