@@ -329,6 +329,8 @@ def run_gpu(args):
             zffn.moe_swiglu_q4k(x_for(step), ids, wts, Wg_, Wu_, Wd_, I, E, y=y, residual=residual)
 
     launches_per_call = 2                          # x conversion (+ zero fill) + fused kernel, or gate/up + down
+    if kind == "moe" and T == 1:
+        launches_per_call = zffn.single_token_launches(H, I, E, k)   # one cooperative launch, or the pair
     if kind == "moe" and T > 1:
         launches_per_call = 4                      # route, gather (+ fp16), zero fill, grouped kernel
 

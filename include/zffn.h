@@ -348,6 +348,13 @@ void zffn_release(void);
  * nothing and allocates nothing. */
 size_t zffn_workspace_bytes(void);
 
+/* Kernel launches one routed single-token call (zffn_moe_swiglu_q4k with
+ * T = 1 and Q4_K W_down) of these sizes makes on the current device under the
+ * current options (ZFFN_OPT_TOKEN_KERNEL): 1 for the one cooperative launch,
+ * 2 for the gate/up and down pair; -1 without a device or for sizes outside
+ * [1, 65536] (top_k in [1, 64]).  Host-side query; launches nothing. */
+int zffn_single_token_launches(int H, int I, int E, int top_k);
+
 /* Description of the last failure a call on this host thread reported: the
  * CUDA error behind a ZFFN_ERR_CUDA, or the failed check behind a
  * ZFFN_ERR_INVALID_ARG.  A successful call leaves it unchanged.  Static
@@ -367,8 +374,15 @@ zffn_status zffn_get_device_error(void *stream);
  * weights on the MMA's M side) when T * top_k <= 48 * E and the prefill
  * kernel on 128-row expert tiles otherwise; 1 always the grouped kernel; 2
  * always the 128-row tiles.
+ * ZFFN_OPT_TOKEN_KERNEL chooses the single-token routed path (Q4_K W_down):
+ * 0 (default) one cooperative launch (every block asks for all of its gate/up
+ * and down rows at once, computes its h rows, meets the other blocks at a
+ * grid barrier, then its output rows) whenever each block's share of the
+ * token's expert weights fits in its shared memory, else the two-kernel
+ * pair; 1 always the two-kernel pair (gate/up, then down as its
+ * programmatic dependent).
  * Returns the previous value, or -1 for an unknown key. */
-enum { ZFFN_OPT_MATVEC_MAX_T = 1, ZFFN_OPT_MOE_KERNEL = 2 };
+enum { ZFFN_OPT_MATVEC_MAX_T = 1, ZFFN_OPT_MOE_KERNEL = 2, ZFFN_OPT_TOKEN_KERNEL = 3 };
 int zffn_set_option(int key, int value);
 
 /* Self-test of the bounded-wait machinery: launches one block that waits on an

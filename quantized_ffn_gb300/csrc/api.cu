@@ -27,13 +27,14 @@ DeviceInfo g_info[kMaxDevices];
 Workspace g_ws[kMaxDevices];
 int g_matvec_max_t = 1;
 int g_moe_kernel = 0;   // ZFFN_OPT_MOE_KERNEL
+int g_token_kernel = 0; // ZFFN_OPT_TOKEN_KERNEL
 
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 // Sub-buffers carved out of one device allocation.
 struct Layout {
-    size_t h, counts, offsets, cursors, tiles, n_tiles, row_token, row_weight, x_perm, xn, x16,
+    size_t gbar, h, counts, offsets, cursors, tiles, n_tiles, row_token, row_weight, x_perm, xn, x16,
         total;
     int max_tiles;
 };
@@ -44,6 +45,9 @@ Layout layout_for(int T, int H, int I, int E, int k) {
     const int64_t P = (int64_t)T * k;
     // tiles of at least 32 rows (the grouped kernel's groups; 128 otherwise)
     L.max_tiles = (int)((P + 31) / 32 + (E < P ? E : P));
+    // the grid barrier of the one-launch routed path: first, so that it keeps
+    // its place (and its zero state) whatever the sizes of a call
+    L.gbar = o; o = align_up(o + sizeof(unsigned long long));
     L.h = o; o = align_up(o + (size_t)P * I * sizeof(float));
     L.counts = o; o = align_up(o + (size_t)E * sizeof(int));
     L.offsets = o; o = align_up(o + (size_t)(E + 1) * sizeof(int));
@@ -82,6 +86,13 @@ zffn_status ensure_workspace(size_t bytes, Workspace **out) {
         if (cudaMalloc(&p, bytes) != cudaSuccess) {
             cudaGetLastError();
             return ZFFN_ERR_NO_WORKSPACE;
+        }
+        // the barrier words (and everything else) start at zero, before any
+        // stream can use the buffer
+        if (cudaMemset(p, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+            cudaFree(p);
+            cudaGetLastError();
+            return ZFFN_ERR_CUDA;
         }
         w.ptr = p;
         w.bytes = bytes;
@@ -289,10 +300,11 @@ zffn_status swiglu_moe(const void *x, const int32_t *expert_ids, const float *ex
     const DeviceInfo &di = device_info();
     if (di.device < 0) return ZFFN_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
-    int mv_max;
+    int mv_max, token_kernel;
     {
         std::lock_guard<std::mutex> lk(g_mu);
         mv_max = g_matvec_max_t;
+        token_kernel = g_token_kernel;
     }
     const Layout L = layout_for(T, H, I, E, top_k);
     Workspace *w = nullptr;
@@ -314,6 +326,7 @@ zffn_status swiglu_moe(const void *x, const int32_t *expert_ids, const float *ex
         a.err = di.err_word;
         a.T = T; a.H = H; a.I = I; a.E = E; a.k = top_k;
         a.accumulate = accumulate;
+        a.gbar = token_kernel == 0 ? reinterpret_cast<unsigned long long *>(base + L.gbar) : nullptr;
         return to_status(launch_ffn_matvec(a, s));
     }
     // Few rows per expert: the grouped kernel (weights as the MMA's M side,
@@ -600,6 +613,17 @@ zffn_status zffn_reserve(int T_max, int H_max, int I_max, int E_max, int top_k_m
     return ensure_workspace(L.total, &w);
 }
 
+int zffn_single_token_launches(int H, int I, int E, int top_k) {
+    if (H < 1 || H > 65536 || I < 1 || I > 65536 || E < 1 || E > 65536 || top_k < 1 || top_k > 64) return -1;
+    if (device_info().device < 0) return -1;
+    int token_kernel;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        token_kernel = g_token_kernel;
+    }
+    return token_kernel == 0 && token_fused_fits_dims(H, I, top_k) ? 1 : 2;
+}
+
 size_t zffn_workspace_bytes(void) {
     const int dev = current_device();
     if (dev < 0 || dev >= kMaxDevices) return 0;
@@ -645,6 +669,11 @@ int zffn_set_option(int key, int value) {
     if (key == ZFFN_OPT_MOE_KERNEL) {
         const int old = g_moe_kernel;
         g_moe_kernel = value < 0 || value > 2 ? 0 : value;
+        return old;
+    }
+    if (key == ZFFN_OPT_TOKEN_KERNEL) {
+        const int old = g_token_kernel;
+        g_token_kernel = value == 1 ? 1 : 0;
         return old;
     }
     return -1;

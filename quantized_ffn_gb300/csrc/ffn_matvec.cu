@@ -586,6 +586,295 @@ __global__ void __launch_bounds__(kDecThreads, 1) ffn_down_kernel(MatvecArgs a) 
     }
 }
 
+// ----------------------------------------------------------------------------
+// C: the routed single-token layer in one cooperative launch
+// ----------------------------------------------------------------------------
+// When every block's share of the token's expert weights fits in its shared
+// memory (a routed layer's top_k experts: a few tens of MB for the whole
+// GPU), one launch does both steps.  Every block first asks for all of its
+// weights at once: x, its gate/up row pairs (in chunks of kTokChunkRows
+// pairs, each on its own barrier) and its down rows of every chosen expert
+// (bulk copies, one per contiguous range), so that the whole layer streams
+// from HBM together and each warp starts as soon as its rows are in.  It then
+// computes its h rows as in A, writes them to the workspace, meets the other
+// blocks at a grid barrier, quantises all of h and computes its output rows
+// as in B from the down rows already in shared memory.  The cooperative
+// launch keeps every block resident, so the barrier's waits end; each is
+// bounded all the same.
+//
+// Shared memory: [x raw bf16] [x quantised] [h quantised] [3 barriers, the
+// slot table, a flag] [gate rows] [up rows] [down rows, slot-major], each region
+// 128-byte aligned; the row regions are sized for the largest block share.
+// Gate/up row pairs are copied and waited for in chunks of kTokChunkRows,
+// each on its own barrier, so that a warp starts on its rows as soon as they
+// have landed (at most kTokMaxChunks chunks per block).
+constexpr int kTokChunkRows = 16, kTokMaxChunks = 16;
+constexpr int kTokBars = 2 + kTokMaxChunks;   // x, down rows, gate/up chunks
+__host__ __device__ inline int token_fused_rows1(const DecGeom &g, int I, int grid) {
+    return (int)(((int64_t)g.P * I + grid - 1) / grid);
+}
+__host__ __device__ inline int token_fused_rows2(int H, int grid) { return (H + grid - 1) / grid; }
+__host__ __device__ inline size_t token_fused_smem_bytes(const DecGeom &g, int H, int I, int grid) {
+    size_t o = ((size_t)H * 2 + 127) & ~(size_t)127;
+    o += (dec_smem_bytes(g.nhalf1) + 127) & ~(size_t)127;
+    o += (dec_smem_bytes(g.nhalf2) + 127) & ~(size_t)127;
+    o += kTokBars * 8 + 2 * 64 * 4 + 4;
+    o = (o + 127) & ~(size_t)127;
+    o += 2 * (size_t)token_fused_rows1(g, I, grid) * g.rbH;
+    o = (o + 127) & ~(size_t)127;
+    o += (size_t)g.P * token_fused_rows2(H, grid) * g.rbI;
+    return o;
+}
+
+// One grid-wide barrier for the blocks of a cooperative launch, on a 64-bit
+// arrival count in global memory (zero before the first use, never reset):
+// the blocks of the n-th barrier on it arrive as counts n*nblocks ..
+// (n+1)*nblocks - 1 and leave once the count has reached (n+1)*nblocks.
+// Called by one thread of each block after the block's writes (ordered
+// before it by a block barrier).  Bounded: on timeout the error word records
+// ZFFN_ERR_TIMEOUT and false is returned.
+__device__ __forceinline__ bool grid_barrier(unsigned long long *count, unsigned int nblocks, int *err) {
+    __threadfence();
+    const unsigned long long old = atomicAdd(count, 1ull);
+    const unsigned long long target = (old / nblocks + 1) * nblocks;
+    const long long t0 = clock64();
+    for (;;) {
+        unsigned long long v;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(count) : "memory");
+        if (v >= target) return true;
+        if (clock64() - t0 > kWaitBudgetCycles) {
+            record_error(err, ZFFN_ERR_TIMEOUT);
+            return false;
+        }
+        __nanosleep(32);
+    }
+}
+
+// Raise the transaction count of the current phase of bar (no arrival).
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(kDecThreads, 1) ffn_token_fused_kernel(MatvecArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const DecGeom G = dec_geom(a.H, a.I, a.k);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = a.H, I = a.I, P = G.P;
+    const int64_t rows1 = (int64_t)P * I;
+    const int r0 = (int)(rows1 * blockIdx.x / gridDim.x), r1 = (int)(rows1 * (blockIdx.x + 1) / gridDim.x);
+    const int n0 = (int)((int64_t)H * blockIdx.x / gridDim.x), n1 = (int)((int64_t)H * (blockIdx.x + 1) / gridDim.x);
+    const int nr = r1 - r0, nd = n1 - n0;
+    const int Lr = 2 * G.nbH, Lp = slots_per_row(G.nbH);
+
+    // carve shared memory
+    uint8_t *x_raw = smem;
+    size_t o = ((size_t)H * 2 + 127) & ~(size_t)127;
+    const DecVec V = dec_vec(smem + o, G.nhalf1);
+    o += (dec_smem_bytes(G.nhalf1) + 127) & ~(size_t)127;
+    const DecVec Vh = dec_vec(smem + o, G.nhalf2);
+    o += (dec_smem_bytes(G.nhalf2) + 127) & ~(size_t)127;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + o);   // x, down rows, gate/up chunks
+    int *s_e = reinterpret_cast<int *>(smem + o + kTokBars * 8);   // expert of slot p (or -1)
+    float *s_w = reinterpret_cast<float *>(s_e + 64);          // its weight (routing * down scale)
+    int *s_ok = reinterpret_cast<int *>(s_w + 64);             // the grid barrier's outcome
+    o += kTokBars * 8 + 2 * 64 * 4 + 4;
+    o = (o + 127) & ~(size_t)127;
+    uint8_t *gu = smem + o;                                    // nr gate rows, then nr up rows
+    o += 2 * (size_t)token_fused_rows1(G, I, gridDim.x) * G.rbH;
+    o = (o + 127) & ~(size_t)127;
+    uint8_t *dn = smem + o;                                    // [slot p][row n - n0]
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kTokBars; ++i) mbar_init(&bars[i], 1);
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+    // every copy this block needs, issued by three warps in parallel
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bars[0], (uint32_t)(H * 2));
+            bulk_g2s(x_raw, a.x, (uint32_t)(H * 2), &bars[0]);
+        }
+    } else if (warp == 1) {
+        // gate/up row pairs [r0, r1) in chunks of kTokChunkRows: lanes 2c and
+        // 2c + 1 copy chunk c's rows of the (at most two) slots it touches,
+        // one range of each matrix, counted on chunk c's barrier
+        const int c = lane >> 1, part = lane & 1;
+        const int cs = r0 + c * kTokChunkRows, ce = min(r1, cs + kTokChunkRows);
+        int start = 0, end = 0, p = 0;
+        if (cs < ce) {
+            const int bound = (cs / I + 1) * I;   // the first slot boundary after cs
+            start = part ? bound : cs;
+            end = part ? ce : min(ce, bound);
+            p = (part ? bound : cs) / I;
+        }
+        const int e = end > start ? a.ids[p] : -1;
+        const bool ok = e >= 0 && e < a.E;
+        const uint32_t bytes = ok ? (uint32_t)(2 * (int64_t)(end - start) * G.rbH) : 0u;
+        if (bytes) mbar_expect_tx(&bars[2 + c], bytes);
+        if (ok) {
+            const int64_t row = (int64_t)e * I + (start - p * I);
+            const uint32_t half = bytes / 2;
+            bulk_g2s(gu + (size_t)(start - r0) * G.rbH, a.Wg + row * G.rbH, half, &bars[2 + c]);
+            bulk_g2s(gu + (size_t)(nr + start - r0) * G.rbH, a.Wu + row * G.rbH, half, &bars[2 + c]);
+        }
+        __syncwarp();
+        if (part == 0 && cs < ce) mbar_arrive(&bars[2 + c]);
+    } else if (warp == 2) {
+        // down rows [n0, n1) of every valid slot, one range each; the slot
+        // table for later
+        uint32_t total = 0;
+        for (int p = lane; p < P; p += 32) {
+            const int e = a.ids[p];
+            const bool ok = e >= 0 && e < a.E;
+            s_e[p] = ok ? e : -1;
+            float w = 0.0f;
+            if (ok) {
+                w = a.wts[p];
+                if (a.down_scale) w *= a.down_scale[e];
+            }
+            s_w[p] = w;
+            if (ok) total += (uint32_t)((int64_t)nd * G.rbI);
+        }
+#pragma unroll
+        for (int s = 16; s > 0; s >>= 1) total += __shfl_xor_sync(0xffffffffu, total, s);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[1], total);
+        __syncwarp();
+        if (nd > 0)
+            for (int p = lane; p < P; p += 32) {
+                const int e = s_e[p];
+                if (e < 0) continue;
+                bulk_g2s(dn + (size_t)p * nd * G.rbI, a.Wd + ((int64_t)e * H + n0) * G.rbI,
+                         (uint32_t)((int64_t)nd * G.rbI), &bars[1]);
+            }
+    }
+    // quantise x
+    if (!mbar_wait(&bars[0], 0, nullptr, a.err)) return;
+    quantize_vector<4>(V, G.nhalf1, warp, kDecWarps, lane, [&](int hb) -> float4 {
+        const uint2 raw = *reinterpret_cast<const uint2 *>(x_raw + (size_t)(hb * 128 + 4 * lane) * 2);
+        return make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                           __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
+    });
+    __syncthreads();
+
+    // step 1: h rows [r0, r1); the pairs of a pass as in the gate/up kernel
+    // (kTokChunkRows is a multiple of a pass's pairs: one chunk per pass)
+    {
+        const int rpc = Lr <= 32 ? 32 / Lp : 1;
+        int lg = 0;
+        while ((1 << lg) < Lp && (1 << lg) < 32) ++lg;
+        const int q = Lr <= 32 ? (lane & (Lp - 1)) : lane;
+        uint4 xr[16];
+        float xs = 0.0f, xsum[4] = {0.f, 0.f, 0.f, 0.f};
+        if (Lr <= 32 && q < Lr) load_half(V, q, xr, xs, xsum);
+        for (int t0 = warp * rpc; t0 < nr; t0 += kDecWarps * rpc) {
+            if (!mbar_wait(&bars[2 + t0 / kTokChunkRows], 0, nullptr, a.err)) return;
+            float g = 0.0f, u = 0.0f;
+            int t;
+            if (Lr <= 32) {
+                t = t0 + (lane >> lg);
+                if (t < nr && q < Lr && s_e[(r0 + t) / I] >= 0) {
+                    const uint8_t *rowg = gu + (size_t)t * G.rbH + (size_t)(q >> 1) * kBlockBytes;
+                    const uint8_t *rowu = rowg + (size_t)nr * G.rbH;
+                    const uint4 hg = *reinterpret_cast<const uint4 *>(rowg);
+                    const uint4 hu = *reinterpret_cast<const uint4 *>(rowu);
+                    uint4 cg[4], cu[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        cg[i] = *reinterpret_cast<const uint4 *>(rowg + 16 + 64 * (q & 1) + 16 * i);
+                        cu[i] = *reinterpret_cast<const uint4 *>(rowu + 16 + 64 * (q & 1) + 16 * i);
+                    }
+                    int ag[4], au[4];
+                    half_block_isums(cg, xr, ag);
+                    half_block_isums(cu, xr, au);
+                    g = half_block_scale(hg, q & 1, ag, xs, xsum);
+                    u = half_block_scale(hu, q & 1, au, xs, xsum);
+                }
+                for (int o2 = Lp >> 1; o2 > 0; o2 >>= 1) {
+                    g += __shfl_xor_sync(0xffffffffu, g, o2);
+                    u += __shfl_xor_sync(0xffffffffu, u, o2);
+                }
+            } else {
+                t = t0;
+                if (s_e[(r0 + t) / I] >= 0) {
+                    for (int qq = lane; qq < Lr; qq += 32) {
+                        uint4 xv[16];
+                        float vs, vsm[4];
+                        load_half(V, qq, xv, vs, vsm);
+                        const uint8_t *rowg = gu + (size_t)t * G.rbH + (size_t)(qq >> 1) * kBlockBytes;
+                        const uint8_t *rowu = rowg + (size_t)nr * G.rbH;
+                        const uint4 hg = *reinterpret_cast<const uint4 *>(rowg);
+                        const uint4 hu = *reinterpret_cast<const uint4 *>(rowu);
+                        uint4 cg[4], cu[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            cg[i] = *reinterpret_cast<const uint4 *>(rowg + 16 + 64 * (qq & 1) + 16 * i);
+                            cu[i] = *reinterpret_cast<const uint4 *>(rowu + 16 + 64 * (qq & 1) + 16 * i);
+                        }
+                        int ag[4], au[4];
+                        half_block_isums(cg, xv, ag);
+                        half_block_isums(cu, xv, au);
+                        g += half_block_scale(hg, qq & 1, ag, vs, vsm);
+                        u += half_block_scale(hu, qq & 1, au, vs, vsm);
+                    }
+                }
+#pragma unroll
+                for (int o2 = 16; o2 > 0; o2 >>= 1) {
+                    g += __shfl_xor_sync(0xffffffffu, g, o2);
+                    u += __shfl_xor_sync(0xffffffffu, u, o2);
+                }
+            }
+            const bool writer = Lr <= 32 ? (q == 0 && t < nr) : lane == 0;
+            if (writer) {
+                const int r = r0 + t;
+                a.h[r] = g / (1.0f + expf(-g)) * u;   // h[p][i] at p * I + i = r
+            }
+        }
+    }
+    // every block's h rows (made visible by the barrier's fence), then all of h
+    __syncthreads();
+    if (threadIdx.x == 0) *s_ok = grid_barrier(a.gbar, gridDim.x, a.err) ? 1 : 0;
+    __syncthreads();
+    if (!*s_ok) return;
+    quantize_vector<8>(Vh, G.nhalf2, warp, kDecWarps, lane, [&](int hb) -> float4 {
+        const int p = hb / (2 * G.nbI), hl = hb - p * (2 * G.nbI);
+        const int col = hl * 128 + 4 * lane;
+        // load from a valid address whatever the column, then zero past I
+        const int colc = col < I ? col : 0;
+        float4 v = __ldcg(reinterpret_cast<const float4 *>(a.h + (int64_t)p * I + colc));
+        if (col >= I) v = make_float4(0.f, 0.f, 0.f, 0.f);
+        return v;
+    });
+    __syncthreads();
+
+    // step 2: output rows [n0, n1) from the down rows in shared memory
+    if (!mbar_wait(&bars[1], 0, nullptr, a.err)) return;
+    const int Lr2 = 2 * G.nbI;
+    const int items = P * Lr2;
+    for (int n = n0 + warp; n < n1; n += kDecWarps) {
+        float acc = 0.0f;
+        for (int it = lane; it < items; it += 32) {
+            const int p = it / Lr2, qh = it - p * Lr2;
+            if (s_e[p] < 0) continue;
+            uint4 xv[16];
+            float xs, xsum[4];
+            load_half(Vh, it, xv, xs, xsum);
+            const uint8_t *blk = dn + ((size_t)p * nd + (n - n0)) * G.rbI + (size_t)(qh >> 1) * kBlockBytes;
+            const uint4 hd = *reinterpret_cast<const uint4 *>(blk);
+            uint4 cq[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) cq[i] = *reinterpret_cast<const uint4 *>(blk + 16 + 64 * (qh & 1) + 16 * i);
+            int ai[4];
+            half_block_isums(cq, xv, ai);
+            acc = fmaf(s_w[p], half_block_scale(hd, qh & 1, ai, xs, xsum), acc);
+        }
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o2);
+        if (lane == 0) a.y[n] = a.accumulate ? a.y[n] + acc : acc;
+    }
+}
+
 size_t gu_smem_total(int H, int I, int k) { return gu_smem_bytes(dec_geom(H, I, k), H); }
 // The down kernel double-buffers its rows when that fits a block's shared
 // memory, else it single-buffers (long rows).
@@ -596,10 +885,43 @@ size_t down_smem_total(int H, int I, int k) {
     return down_smem_bytes(dec_geom(H, I, k), down_ring_depth(H, I, k));
 }
 
+// The one-launch routed path applies when its barrier words are given and
+// every block's share of the weights fits in its shared memory.
+bool token_fused_fits_dims(int H, int I, int k) {
+    if (k > 64) return false;
+    const DeviceInfo &di = device_info();
+    const DecGeom G = dec_geom(H, I, k);
+    const int grid = di.num_sms;
+    // a block's gate/up pairs: at most kTokMaxChunks chunks, each touching at
+    // most two slots
+    if (token_fused_rows1(G, I, grid) > kTokChunkRows * kTokMaxChunks || I < kTokChunkRows) return false;
+    return token_fused_smem_bytes(G, H, I, grid) <= (size_t)di.max_smem_optin;
+}
+bool token_fused_fits(const MatvecArgs &a) {
+    return a.T == 1 && a.ids && a.gbar && token_fused_fits_dims(a.H, a.I, a.k);
+}
+
 cudaError_t launch_ffn_matvec(const MatvecArgs &a, cudaStream_t s) {
     const DeviceInfo &di = device_info();
     if (a.T != 1) return cudaErrorInvalidValue;
     const DecGeom G = dec_geom(a.H, a.I, a.k);
+    if (token_fused_fits(a)) {
+        const size_t smem = token_fused_smem_bytes(G, a.H, a.I, di.num_sms);
+        cudaError_t e = ensure_dynamic_smem((const void *)ffn_token_fused_kernel, smem);
+        if (e != cudaSuccess) return e;
+        MatvecArgs args = a;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(di.num_sms);   // one block per SM, all resident
+        cfg.blockDim = dim3(kDecThreads);
+        cfg.stream = s;
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, ffn_token_fused_kernel, args);
+    }
     const int depth = down_ring_depth(a.H, a.I, a.k);
     const size_t smem_a = gu_smem_bytes(G, a.H), smem_b = down_smem_bytes(G, depth);
     cudaError_t e = ensure_dynamic_smem((const void *)ffn_gu_kernel, smem_a);

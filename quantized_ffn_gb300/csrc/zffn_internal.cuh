@@ -599,8 +599,12 @@ struct MatvecArgs {
     int T, H, I, E, k;
     bool accumulate;             // y += result instead of y = result
     int ring_depth;              // set by the launcher: row buffers per warp in the down kernel
+    unsigned long long *gbar;    // routed only: the one-launch path's grid-barrier count (zero
+                                 // before its first use), or nullptr for the two-kernel path
 };
 size_t matvec_smem_bytes(int T, int H, int I, int k);
+// The one-launch routed single-token path fits these sizes on this device.
+bool token_fused_fits_dims(int H, int I, int k);
 cudaError_t launch_ffn_matvec(const MatvecArgs &a, cudaStream_t s);
 
 // Tensor-core fused prefill path.

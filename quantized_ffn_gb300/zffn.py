@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libzffn.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_NO_WORKSPACE = range(6)
 OPT_MATVEC_MAX_T = 1
 OPT_MOE_KERNEL = 2
+OPT_TOKEN_KERNEL = 3
 
 _lock = threading.Lock()
 _lib = None
@@ -73,6 +74,7 @@ def load() -> ctypes.CDLL:
                 "zffn_reserve": ([I32, I32, I32, I32, I32], I32),
                 "zffn_release": ([], None),
                 "zffn_workspace_bytes": ([], ctypes.c_size_t),
+                "zffn_single_token_launches": ([I32, I32, I32, I32], I32),
                 "zffn_get_device_error": ([P], I32),
                 "zffn_set_option": ([I32, I32], I32),
                 "zffn_selftest_wait_timeout": ([I64, P], I32),
@@ -365,6 +367,12 @@ def release():
 def workspace_bytes() -> int:
     """Bytes of library workspace held on the current device."""
     return int(load().zffn_workspace_bytes())
+
+
+def single_token_launches(H: int, I: int, E: int, top_k: int) -> int:
+    """Kernel launches of one routed single-token call of these sizes (1: the
+    one cooperative launch, 2: the gate/up and down pair; -1 without a device)."""
+    return int(load().zffn_single_token_launches(H, I, E, top_k))
 
 
 def get_device_error(stream=None) -> int:

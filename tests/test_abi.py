@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from quantized_ffn_gb300 import build as zbuild
 from quantized_ffn_gb300 import zffn
@@ -93,6 +94,16 @@ def test_options(lib):
     old = zffn.set_option(zffn.OPT_MATVEC_MAX_T, 4)
     assert zffn.set_option(zffn.OPT_MATVEC_MAX_T, old) == 4
     assert zffn.set_option(999, 1) == -1
+    old = zffn.set_option(zffn.OPT_TOKEN_KERNEL, 1)
+    assert zffn.set_option(zffn.OPT_TOKEN_KERNEL, old) == 1
+
+
+def test_single_token_launch_query_without_device(lib):
+    # bad sizes, and (on a host without a GPU) no device: -1
+    assert zffn.single_token_launches(2048, 768, 128, 0) == -1
+    assert zffn.single_token_launches(2048, 768, 128, 65) == -1
+    if not torch.cuda.is_available():
+        assert zffn.single_token_launches(2048, 768, 128, 8) == -1
 
 
 @pytest.mark.parametrize("T,E,k", [(0, 8, 2), (-3, 8, 2), (4, 0, 1), (4, 5000, 8), (4, 8, 0),
