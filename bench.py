@@ -601,7 +601,8 @@ def run_gpu(args):
             "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
             "frac": round(achieved / peak, 4), "traffic": traffic,
             "kernel": "x_to_f16_kernel+ffn_tc_kernel" if bound == "tensor" else
-                      ("ffn_gu_kernel+ffn_down_kernel" if T == 1 else
+                      (("ffn_token_fused_kernel" if kind == "moe" and launches_per_call == 1 else
+                        "ffn_gu_kernel+ffn_down_kernel") if T == 1 else
                        "moe_route_kernel+moe_gather_kernel+moe_group_kernel"),
             "kernel_ms": round(kms, 4),
             "peak_source": f"{peaks['source']} (burst)",
