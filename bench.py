@@ -448,6 +448,28 @@ def run_gpu(args):
         n_gbs = n_bytes / (n_ms * 1e-3) / 1e9
         norm = {"kernel": "rmsnorm_bf16_kernel", "ms": round(n_ms, 5), "hbm_bytes": n_bytes,
                 "achieved_gbs": round(n_gbs, 2), "frac_of_hbm_peak": round(n_gbs / peaks["hbm"], 4)}
+        if T == 1:
+            # one token: the pre-norm residual block folds the normalisation
+            # into the gate/up kernel (two launches); the block alone, same
+            # setting, beside it
+            h_row = h_res.clone()
+            p_ms, b_ms = [], []
+            for s in range(args.steps):
+                for fn, acc in ((lambda: zffn.swiglu_q4k_prenorm_residual(h_row, gamma, 1e-6, W[0], W[1], W[2], I),
+                                 p_ms),
+                                (lambda: zffn.swiglu_q4k(x_for(0), W[0], W[1], W[2], I, y=y), b_ms)):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    flush.zero_()
+                    e0.record(stream)
+                    fn()
+                    e1.record(stream)
+                    acc.append((e0, e1))
+            torch.cuda.synchronize()
+            assert zffn.get_device_error() == zffn.OK
+            norm["prenorm_block_ms"] = round(statistics.mean(a.elapsed_time(b) for a, b in p_ms), 5)
+            norm["block_ms"] = round(statistics.mean(a.elapsed_time(b) for a, b in b_ms), 5)
+            norm["prenorm_block_launches"] = 2
+            norm["prenorm_timing"] = "one isolated call after an L2 flush, each"
 
     # The staged pipeline the fusion replaces ("Fused SwiGLU MLP...", sections
     # "Counting the bytes the intermediate actually moves" and "What it is

@@ -133,8 +133,14 @@ zffn_status zffn_rmsnorm_bf16(const float *h, const float *gamma, float eps, voi
  * transformer layer applies it to the residual stream h:
  *     h[t] += W_down . (silu(W_gate . x[t]) (*) (W_up . x[t])),
  *     x = zffn_rmsnorm_bf16(h, gamma, eps)
- * Two launch groups in stream order: the normalisation into library workspace
- * (bf16 [T][H], see zffn_reserve), then the block accumulating into h.
+ * T = 1 (when the single-token kernels take the sizes): the normalisation
+ * runs inside the gate/up kernel, which reads the fp32 row and gamma and
+ * builds x itself; then the down kernel adds into h (two launches, no
+ * workspace copy of x; x may differ from zffn_rmsnorm_bf16's in the last bf16
+ * place of rare elements, the sum of squares being reduced in another order).
+ * Otherwise two launch groups in stream order: the normalisation into library
+ * workspace (bf16 [T][H], see zffn_reserve), then the block accumulating
+ * into h.
  *   h: fp32 [T][H] (device), read and updated in place.
  *   gamma: fp32 [H]; Wg, Wu, Wd as for zffn_swiglu_q4k.
  * Requirements as zffn_swiglu_q4k and zffn_rmsnorm_bf16.

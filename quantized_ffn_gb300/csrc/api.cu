@@ -576,13 +576,36 @@ zffn_status zffn_swiglu_q4k_prenorm_residual(float *h, const float *gamma, float
     if (!(eps >= 0.0f) || eps > 1.0f) return invalid("eps must be in [0, 1]");
     if (!aligned16(h) || !aligned16(gamma) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd))
         return invalid("h, gamma, Wg, Wu and Wd must be 16-byte aligned");
-    if (device_info().device < 0) return ZFFN_ERR_CUDA;
+    const DeviceInfo &di = device_info();
+    if (di.device < 0) return ZFFN_ERR_CUDA;
     // the whole layout is reserved here, so that the block's own workspace
     // request below finds it large enough and never moves it
     const Layout L = layout_for(T, H, I, 1, 1);
     Workspace *w = nullptr;
     zffn_status st = ensure_workspace(L.total, &w);
     if (st != ZFFN_OK) return st;
+    int mv_max;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        mv_max = g_matvec_max_t;
+    }
+    if (T == 1 && mv_max >= 1 && matvec_smem_bytes_prenorm(H, I) <= (size_t)di.max_smem_optin) {
+        // one token: the normalisation runs inside the gate/up kernel, which
+        // reads the residual row; the down kernel then adds into it
+        MatvecArgs a{};
+        a.norm_in = h;
+        a.gamma = gamma;
+        a.eps = eps;
+        a.Wg = static_cast<const uint8_t *>(Wg);
+        a.Wu = static_cast<const uint8_t *>(Wu);
+        a.Wd = static_cast<const uint8_t *>(Wd);
+        a.y = h;
+        a.h = reinterpret_cast<float *>(static_cast<uint8_t *>(w->ptr) + L.h);
+        a.err = di.err_word;
+        a.T = 1; a.H = H; a.I = I; a.E = 1; a.k = 1;
+        a.accumulate = true;
+        return to_status(launch_ffn_matvec(a, (cudaStream_t)stream));
+    }
     __nv_bfloat16 *xn = reinterpret_cast<__nv_bfloat16 *>(static_cast<uint8_t *>(w->ptr) + L.xn);
     cudaError_t e = launch_rmsnorm_bf16(h, gamma, eps, xn, T, H, (cudaStream_t)stream);
     if (e != cudaSuccess) return to_status(e);

@@ -266,12 +266,17 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 // ----------------------------------------------------------------------------
 // A: gate and up rows -> h
 // ----------------------------------------------------------------------------
-// Shared memory: [x raw bf16 (H*2)] [x quantised (nhalf1 half-blocks)]
-// [x bar] [per warp: 2 slot barriers, 2 slots].
-__host__ __device__ inline size_t gu_smem_bytes(const DecGeom &g, int H) {
+// Shared memory: [x raw: bf16 (H*2), or with the RMSNorm folded in the fp32
+// residual row and gamma (H*4 each) and 16 floats of reduction scratch] [x
+// quantised (nhalf1 half-blocks)] [x bar] [per warp: 2 slot barriers, 2
+// slots].
+__host__ __device__ inline size_t gu_x_raw_bytes(int H, bool norm) {
+    return ((size_t)H * (norm ? 8 : 2) + (norm ? 64 : 0) + 127) & ~(size_t)127;
+}
+__host__ __device__ inline size_t gu_smem_bytes(const DecGeom &g, int H, bool norm = false) {
     const int Lp = slots_per_row(g.nbH);
     const size_t slot = (size_t)((dec_slot_bytes(g, Lp, false) + 127) & ~(int64_t)127);
-    size_t o = ((size_t)H * 2 + 127) & ~(size_t)127;
+    size_t o = gu_x_raw_bytes(H, norm);
     o += (dec_smem_bytes(g.nhalf1) + 127) & ~(size_t)127;
     o += 8 + (size_t)kDecWarps * 2 * 8;
     o = (o + 127) & ~(size_t)127;
@@ -293,8 +298,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) ffn_gu_kernel(MatvecArgs a) {
     const int Lp = slots_per_row(G.nbH);
 
     // carve shared memory
+    const bool norm = a.norm_in != nullptr;
     uint8_t *x_raw = smem;
-    size_t o = ((size_t)H * 2 + 127) & ~(size_t)127;
+    const float *gamma_s = reinterpret_cast<const float *>(smem + (size_t)H * 4);   // (norm only)
+    float *norm_part = reinterpret_cast<float *>(smem + (size_t)H * 8);            // (norm only)
+    size_t o = gu_x_raw_bytes(H, norm);
     const DecVec V = dec_vec(smem + o, G.nhalf1);
     o += (dec_smem_bytes(G.nhalf1) + 127) & ~(size_t)127;
     uint64_t *xbar = reinterpret_cast<uint64_t *>(smem + o);
@@ -338,8 +346,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) ffn_gu_kernel(MatvecArgs a) {
         mbar_init(xbar, 1);
         for (int i = 0; i < 2 * kDecWarps; ++i) mbar_init(&wbars[i], 1);
         fence_mbarrier_init();
-        mbar_arrive_expect_tx(xbar, (uint32_t)(H * 2));
-        bulk_g2s(x_raw, a.x, (uint32_t)(H * 2), xbar);
+        const uint32_t xb = (uint32_t)(H * (norm ? 4 : 2));
+        mbar_arrive_expect_tx(xbar, norm ? 2 * xb : xb);
+        bulk_g2s(x_raw, norm ? static_cast<const void *>(a.norm_in) : static_cast<const void *>(a.x), xb, xbar);
+        if (norm) bulk_g2s(x_raw + xb, a.gamma, xb, xbar);
     }
     __syncthreads();
     // the down-projection kernel may be scheduled as soon as SMs free up
@@ -359,11 +369,42 @@ __global__ void __launch_bounds__(kDecThreads, 1) ffn_gu_kernel(MatvecArgs a) {
     __syncwarp();
     // quantise x (each warp its share of half-blocks)
     if (!mbar_wait(xbar, 0, nullptr, a.err)) return;
-    quantize_vector<4>(V, G.nhalf1, warp, kDecWarps, lane, [&](int hb) -> float4 {
-        const uint2 raw = *reinterpret_cast<const uint2 *>(x_raw + (size_t)(hb * 128 + 4 * lane) * 2);
-        return make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
-                           __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
-    });
+    if (norm) {
+        // x = bf16(r * row * gamma), r = 1 / sqrt(mean(row^2) + eps), as the
+        // RMSNorm kernel computes it (its reduction order aside)
+        const float4 *row4 = reinterpret_cast<const float4 *>(x_raw);
+        float ss = 0.0f;
+        for (int i = threadIdx.x; i < H / 4; i += kDecThreads) {
+            const float4 v = row4[i];
+            ss = fmaf(v.x, v.x, ss);
+            ss = fmaf(v.y, v.y, ss);
+            ss = fmaf(v.z, v.z, ss);
+            ss = fmaf(v.w, v.w, ss);
+        }
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o2);
+        if (lane == 0) norm_part[warp] = ss;
+        __syncthreads();
+        float tot = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kDecWarps; ++w) tot += norm_part[w];
+        const float r = rsqrtf(tot / (float)H + a.eps);
+        const float4 *g4 = reinterpret_cast<const float4 *>(gamma_s);
+        quantize_vector<4>(V, G.nhalf1, warp, kDecWarps, lane, [&](int hb) -> float4 {
+            const float4 v = row4[hb * 32 + lane];
+            const float4 g = g4[hb * 32 + lane];
+            return make_float4(__bfloat162float(__float2bfloat16_rn(v.x * r * g.x)),
+                               __bfloat162float(__float2bfloat16_rn(v.y * r * g.y)),
+                               __bfloat162float(__float2bfloat16_rn(v.z * r * g.z)),
+                               __bfloat162float(__float2bfloat16_rn(v.w * r * g.w)));
+        });
+    } else {
+        quantize_vector<4>(V, G.nhalf1, warp, kDecWarps, lane, [&](int hb) -> float4 {
+            const uint2 raw = *reinterpret_cast<const uint2 *>(x_raw + (size_t)(hb * 128 + 4 * lane) * 2);
+            return make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                               __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
+        });
+    }
     __syncthreads();
 
     int lg = 0;
@@ -876,6 +917,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) ffn_token_fused_kernel(MatvecA
 }
 
 size_t gu_smem_total(int H, int I, int k) { return gu_smem_bytes(dec_geom(H, I, k), H); }
+size_t matvec_smem_bytes_prenorm(int H, int I) {
+    const size_t sa = gu_smem_bytes(dec_geom(H, I, 1), H, true), sb = down_smem_total(H, I, 1);
+    return sa > sb ? sa : sb;
+}
 // The down kernel double-buffers its rows when that fits a block's shared
 // memory, else it single-buffers (long rows).
 int down_ring_depth(int H, int I, int k) {
@@ -923,7 +968,7 @@ cudaError_t launch_ffn_matvec(const MatvecArgs &a, cudaStream_t s) {
         return cudaLaunchKernelEx(&cfg, ffn_token_fused_kernel, args);
     }
     const int depth = down_ring_depth(a.H, a.I, a.k);
-    const size_t smem_a = gu_smem_bytes(G, a.H), smem_b = down_smem_bytes(G, depth);
+    const size_t smem_a = gu_smem_bytes(G, a.H, a.norm_in != nullptr), smem_b = down_smem_bytes(G, depth);
     cudaError_t e = ensure_dynamic_smem((const void *)ffn_gu_kernel, smem_a);
     if (e == cudaSuccess) e = ensure_dynamic_smem((const void *)ffn_down_kernel, smem_b);
     if (e != cudaSuccess) return e;

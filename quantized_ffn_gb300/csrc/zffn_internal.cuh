@@ -601,8 +601,15 @@ struct MatvecArgs {
     int ring_depth;              // set by the launcher: row buffers per warp in the down kernel
     unsigned long long *gbar;    // routed only: the one-launch path's grid-barrier count (zero
                                  // before its first use), or nullptr for the two-kernel path
+    // Dense only, or nullptr: the gate/up kernel builds x itself as
+    // bf16(RMSNorm(norm_in) * gamma) from this fp32 row (x is then unused)
+    const float *norm_in;
+    const float *gamma;
+    float eps;
 };
 size_t matvec_smem_bytes(int T, int H, int I, int k);
+// The same with the RMSNorm folded into the gate/up kernel (dense, T = 1).
+size_t matvec_smem_bytes_prenorm(int H, int I);
 // The one-launch routed single-token path fits these sizes on this device.
 bool token_fused_fits_dims(int H, int I, int k);
 cudaError_t launch_ffn_matvec(const MatvecArgs &a, cudaStream_t s);

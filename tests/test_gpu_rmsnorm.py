@@ -95,6 +95,29 @@ def test_prenorm_block_full_size(T):
     assert_close(delta, out_ref - h.astype(np.float64), f"pre-norm block T={T}")
 
 
+@pytest.mark.parametrize("H,I", [(256, 704), (1024, 1472), (2048, 5632), (8192, 2048)])
+def test_prenorm_single_token_norm_in_gate_up_kernel(H, I):
+    # one token: the normalisation runs inside the gate/up kernel; against the
+    # oracle, and against the two public steps (same x up to the order of the
+    # sum of squares: an x element may round to the neighbouring bf16 value)
+    rng = np.random.default_rng(H + I)
+    W = [synth.random_q4k_blocks(rng, I, H, 1e-2), synth.random_q4k_blocks(rng, I, H, 1e-2),
+         synth.random_q4k_blocks(rng, H, I, 1e-2)]
+    h, gamma = residual_stream(H + I, 1, H, scale=3.0)
+    gamma = (gamma * np.float32(1.5)).astype(np.float32)
+    hd = dev(h)
+    zffn.swiglu_q4k_prenorm_residual(hd, dev(gamma), EPS, *[dev(w) for w in W], I)
+    assert zffn.get_device_error() == zffn.OK
+    out_ref, _ = orc.prenorm_swiglu_residual(h, gamma, EPS, *W, I)
+    delta = hd.cpu().double() - torch.from_numpy(h).double()
+    assert_close(delta, out_ref - h.astype(np.float64), f"pre-norm T=1 H={H} I={I}")
+    b = dev(h)
+    x = zffn.rmsnorm_bf16(b, dev(gamma), EPS)
+    zffn.swiglu_q4k(x, *[dev(w) for w in W], I, y=b, residual=True)
+    torch.cuda.synchronize()
+    assert_close(hd - dev(h), (b - dev(h)).cpu().double().numpy(), "folded norm vs the two steps")
+
+
 def test_prenorm_block_equals_norm_then_residual_block():
     # the composed entry equals its two public steps run by hand
     d = synth.tiny()
