@@ -332,7 +332,7 @@ def run_gpu(args):
     if kind == "moe" and T == 1:
         launches_per_call = zffn.single_token_launches(H, I, E, k)   # one cooperative launch, or the pair
     if kind == "moe" and T > 1:
-        launches_per_call = 4                      # route, gather (+ fp16), zero fill, grouped kernel
+        launches_per_call = 3                      # route, gather (+ fp16, + zero fill of y), grouped kernel
 
     def barrier():
         if world > 1:

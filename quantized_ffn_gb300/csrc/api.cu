@@ -356,12 +356,11 @@ zffn_status swiglu_moe(const void *x, const int32_t *expert_ids, const float *ex
     r.row_weight = reinterpret_cast<float *>(base + L.row_weight);
     r.x_perm = reinterpret_cast<__half *>(base + L.x_perm);
     r.max_tiles = L.max_tiles;
+    // overwrite: the gather kernel zeroes y (y is 16-byte aligned here)
+    r.y_zero = accumulate ? nullptr : y;
+    r.ny = (int64_t)T * H;
     cudaError_t e = launch_moe_route(r, s);
     if (e != cudaSuccess) return to_status(e);
-    if (!accumulate) {
-        e = launch_zero_f32(y, (int64_t)T * H, s);
-        if (e != cudaSuccess) return to_status(e);
-    }
     TcArgs a{};
     a.x = r.x_perm;
     a.x_rows = (int64_t)T * top_k;

@@ -93,11 +93,15 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
     }
 }
 
+// Gathered rows of x (fp16, the tensor-core kernel's gate/up operand) and,
+// in the same launch, y = 0 when the block is to overwrite y (its kernel adds
+// its partial sums into y).
 __global__ void __launch_bounds__(256) moe_gather_kernel(const __nv_bfloat16 *__restrict__ x,
                                                          const int *__restrict__ offsets, int E,
                                                          const int *__restrict__ row_token,
                                                          __half *__restrict__ x_perm,
-                                                         int rows_cap, int H) {
+                                                         int rows_cap, int H, float4 *__restrict__ y4,
+                                                         int64_t ny4, float *ytail, int nytail) {
     const int n_rows = min(offsets[E], rows_cap);
     const int vec = H / 8;   // 16-byte vectors per row
     for (int r = blockIdx.x; r < n_rows; r += gridDim.x) {
@@ -109,6 +113,12 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const __nv_bfloat16 *__
             dst[v] = make_uint4(bf16x2_to_f16x2_satfinite(w.x), bf16x2_to_f16x2_satfinite(w.y),
                                 bf16x2_to_f16x2_satfinite(w.z), bf16x2_to_f16x2_satfinite(w.w));
         }
+    }
+    if (y4) {
+        const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+        for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < ny4; i += stride)
+            y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (blockIdx.x == 0 && threadIdx.x < nytail) ytail[threadIdx.x] = 0.0f;
     }
 }
 
@@ -145,7 +155,11 @@ cudaError_t launch_moe_route(const RouteArgs &a, cudaStream_t s) {
     const int P = a.T * a.k;
     int grid = P < device_info().num_sms * 8 ? P : device_info().num_sms * 8;
     if (grid < 1) grid = 1;
-    moe_gather_kernel<<<grid, 256, 0, s>>>(a.x, a.offsets, a.E, a.row_token, a.x_perm, P, a.H);
+    const int64_t ny4 = a.y_zero ? a.ny / 4 : 0;
+    moe_gather_kernel<<<grid, 256, 0, s>>>(a.x, a.offsets, a.E, a.row_token, a.x_perm, P, a.H,
+                                           reinterpret_cast<float4 *>(a.y_zero), ny4,
+                                           a.y_zero ? a.y_zero + 4 * ny4 : nullptr,
+                                           a.y_zero ? (int)(a.ny - 4 * ny4) : 0);
     return cudaGetLastError();
 }
 

@@ -1,5 +1,6 @@
 // q4k.cu -- standalone Q4_K kernels: unpack to fp32 (bit-exact), the min/max
-// quantiser, and a zero fill used before the atomically reduced outputs.
+// quantiser, and the conversion of x to fp16 (with the zero fill of y that the
+// tensor-core kernel's reductions add into).
 #include "zffn_internal.cuh"
 
 namespace zffn {
@@ -154,28 +155,6 @@ cudaError_t launch_q4k_quantize(const float *w, void *blocks, int64_t rows, int6
     if (grid < 1) grid = 1;
     q4k_quantize_kernel<<<(unsigned)grid, 256, 0, s>>>(w, static_cast<uint8_t *>(blocks), rows,
                                                         cols);
-    return cudaGetLastError();
-}
-
-// ---------------------------------------------------------------------------
-// Zero fill (16-byte stores; the pointer is 16-byte aligned by contract).
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) zero_f32_kernel(float4 *p, int64_t n4, float *tail,
-                                                       int ntail) {
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += stride)
-        p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (blockIdx.x == 0 && threadIdx.x < ntail) tail[threadIdx.x] = 0.0f;
-}
-
-cudaError_t launch_zero_f32(float *p, int64_t n, cudaStream_t s) {
-    const int64_t n4 = n / 4;
-    int64_t grid = (n4 + 255) / 256;
-    const int64_t cap = (int64_t)device_info().num_sms * 8;
-    if (grid > cap) grid = cap;
-    if (grid < 1) grid = 1;
-    zero_f32_kernel<<<(unsigned)grid, 256, 0, s>>>(reinterpret_cast<float4 *>(p), n4, p + 4 * n4,
-                                                    (int)(n - 4 * n4));
     return cudaGetLastError();
 }
 

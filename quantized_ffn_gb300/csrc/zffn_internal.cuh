@@ -578,7 +578,6 @@ cudaError_t launch_q4k_dequant(const void *blocks, float *out, int64_t rows, int
                                cudaStream_t s);
 cudaError_t launch_q4k_quantize(const float *w, void *blocks, int64_t rows, int64_t cols,
                                 cudaStream_t s);
-cudaError_t launch_zero_f32(float *p, int64_t n, cudaStream_t s);
 // x (bf16, n values, n % 8 == 0, 16-byte aligned) -> x16 (fp16, saturating);
 // if y_zero is not null, also y_zero[0, ny) = 0.
 cudaError_t launch_x_to_f16(const void *x, void *x16, int64_t n, float *y_zero, int64_t ny,
@@ -656,6 +655,8 @@ struct RouteArgs {
     __half *x_perm;     // [T*k][H] gathered rows, converted to fp16
     int max_tiles;
     int tile_rows;      // rows per tile: 128 (prefill kernel) or the grouped kernel's group
+    float *y_zero;      // [ny] set to zero by the gather kernel (the block then adds into it), or nullptr
+    int64_t ny;
 };
 cudaError_t launch_moe_route(const RouteArgs &a, cudaStream_t s);
 // The tile table of a dense block run as one expert: groups of `rows`
