@@ -232,13 +232,13 @@ zffn_status zffn_dequant_fmt(int fmt, const void *blocks, float *out, int64_t ro
  *     (66 KB for Q5_K, 72 KB for Q5_1, 90 KB for Q6_K) exceed a block's
  *     shared memory (227 KB: at top_k = 1 every I for Q5_K and Q5_1, I <=
  *     58688 for Q6_K; at top_k = 8, I <= 8576, 8256 and 7296).
- *   T > 1: Q5_K and Q5_1 on the grouped tensor-core kernel (the routed
+ *   T > 1: every format on the grouped tensor-core kernel (the routed
  *     kernel's groups of 32 token rows; a dense block runs as one expert), Wd
  *     and y 16-byte aligned.  Its weights are unpacked once per group of 32
  *     tokens, so it suits routed layers and short prompts rather than long
- *     prefills.  Q6_K at T > 1 returns UNSUPPORTED: its 210-byte blocks give
- *     row pitches that are not multiples of 16 bytes, which the tensor-core
- *     kernels' TMA loads need.
+ *     prefills.  Q6_K rows (210-byte blocks, row pitches not a multiple of 16
+ *     bytes) are copied row by row instead of by TMA boxes: slower (about
+ *     1.4x the Q5_K call at the routed T = 256 layer).
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA, NO_WORKSPACE. */
 zffn_status zffn_swiglu_q4k_wd(const void *x, const void *Wg, const void *Wu, const void *Wd,
                                int wd_fmt, float *y, int T, int H, int I, void *stream);
@@ -303,7 +303,7 @@ zffn_status zffn_moe_router_topk(const float *logits, int32_t *expert_ids,
  *     It multiplies the routing weight of each (token, slot) in fp32 before the
  *     down projection's output is added.
  *   wd_fmt: block format of every expert's W_down (zffn_format), with the
- *     same rules as zffn_moe_swiglu_q4k_wd (Q6_K at T > 1 is UNSUPPORTED).
+ *     same rules as zffn_moe_swiglu_q4k_wd.
  *   accumulate: 0 overwrites y, non-zero adds the block's output to y.
  *   The other arguments as for zffn_moe_swiglu_q4k (expert_ids and
  *   expert_weights must not be NULL).

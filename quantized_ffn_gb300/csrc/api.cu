@@ -489,12 +489,8 @@ zffn_status swiglu_wd(const void *x, const int32_t *expert_ids, const float *exp
         return invalid("x, Wg, Wu must be 16-byte and Wd, y, expert_ids, expert_weights 4-byte aligned");
     if (reinterpret_cast<uintptr_t>(down_scale) & 3) return invalid("down_scale must be 4-byte aligned");
     if (T != 1) {
-        // the grouped tensor-core kernel takes Q5_K and Q5_1 W_down; Q6_K
-        // rows (210-byte blocks) miss the 16-byte row pitch of its TMA loads
-        if (wd_fmt == kFmtQ6_K) {
-            set_last_error("W_down in Q6_K is supported for T = 1 only");
-            return ZFFN_ERR_UNSUPPORTED;
-        }
+        // the grouped tensor-core kernel (Q6_K rows, 210-byte blocks, are
+        // bulk-copied row by row instead of through a tensor map)
         if (!aligned16(Wd) || !aligned16(y)) return invalid("for T > 1, Wd and y must be 16-byte aligned");
         if (moe)
             return swiglu_moe(x, expert_ids, expert_weights, down_scale, Wg, Wu, Wd, y, T, H, I, E, top_k,

@@ -32,12 +32,15 @@
 // Block roles (24 warps):
 //   warps 0-3   epilogue for TMEM lane quadrants 0-3: SwiGLU -> h, Y -> y
 //   warp 4      TMEM allocator and MMA issuer (one elected lane issues)
-//   warp 5      TMA producer: whole Q4_K blocks of 128 weight rows (one box
-//               per matrix covers four K steps)
+//   warp 5      producer: whole blocks of 128 weight rows (one TMA box per
+//               matrix covers four K steps; a Q6_K W_down stage is 128 bulk
+//               copies, four per lane)
 //   warp 6      TMA producer: the group's x tiles [32 x 64] fp16
 //   warps 8-23  unpackers, four groups of four warps (one per TMEM lane
 //               quadrant) taking tasks in turn
-//   warp 7      idle
+//   warp 7      idle (Q6_K: second producer warp for the W_down rows)
+#include <cstring>
+
 #include <cudaTypedefs.h>
 
 #include "formats.h"
@@ -46,12 +49,36 @@
 namespace zffn {
 namespace mg {
 
+// Bulk copy global -> shared (16-byte aligned addresses, a multiple of 16
+// bytes), counted on bar.
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 32 bytes at the even shared address a: nine aligned words and eight funnel
+// shifts.
+__device__ __forceinline__ void ld_shared_32_even(uint32_t a, uint32_t (&o)[8]) {
+    const uint32_t base = a & ~3u, sh = (a & 3u) * 8;
+    uint32_t v[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v[i]) : "r"(base + 4 * i));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = __funnelshift_r(v[i], v[i + 1], sh);
+}
+
 // Bytes of one row's 256 W_down weights in format F (whole blocks: Q5_1 has
 // eight 24-byte blocks per 256 weights); the down phase's packed boxes are
 // [128 rows x WD_BOX(F) bytes].  All are multiples of 16 bytes, as TMA needs.
+// Q6_K (210-byte blocks, rows at 2-byte alignment) has no tensor map: each
+// row's block is bulk-copied as the 16-byte aligned range that holds it
+// (at most 224 bytes) into a 224-byte slot, the block starting (address % 16)
+// bytes into it.
 template <int F>
 __host__ __device__ constexpr int wd_box_bytes() {
-    return F == kFmtQ5_K ? 176 : F == kFmtQ5_1 ? 192 : 144;
+    return F == kFmtQ5_K ? 176 : F == kFmtQ5_1 ? 192 : F == kFmtQ6_K ? 224 : 144;
 }
 
 constexpr int NG = 32;                       // token rows of a group (UMMA N)
@@ -101,6 +128,8 @@ struct Maps {
 };
 
 struct Params {
+    const uint8_t *Wd;         // W_down (Q6_K: bulk-copied rows; else through maps.wd)
+    int64_t rbI;               // bytes of a W_down row
     float *y;
     const int4 *tiles;         // {row_start, row_count, expert, 0}
     const int *n_tiles_dev;
@@ -151,7 +180,46 @@ __device__ __forceinline__ Unit make_unit(const Params &p, int u, int n_tiles) {
 // out[j][16]: the TMEM words of K step ks0 + j for this thread's half.
 template <int F>
 __device__ __forceinline__ void unpack_wd_pair_fmt(uint32_t row, int ks0, int h, uint32_t (&out)[2][16]) {
-    if (F == kFmtQ5_K) {
+    if (F == kFmtQ6_K) {
+        // row: the block's first byte (even).  K steps ks0, ks0 + 1 (ks0
+        // even) are half n = ks0 / 2 of the block; task h of K step j is its
+        // quarter i = 2j + h: low 4 bits from nibble j of ql[64n + 32h + l],
+        // high 2 bits = bits 2i, 2i+1 of qh[32n + l], one int8 scale per 16
+        // weights.  w = d sc (q4 + 16 q2 - 32) as
+        //     (q4 2^-9) (512 d sc) - 32 d sc + (q2 2^-9) (8192 d sc)
+        // (the high part through the same converter; two roundings to fp16).
+        const int n = ks0 >> 1;
+        uint32_t ql[8], qh[8];
+        ld_shared_32_even(row + 64 * n + 32 * h, ql);
+        ld_shared_32_even(row + 128 + 32 * n, qh);
+        uint32_t dbits, s0, s1;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=r"(dbits) : "r"(row + 208));
+        asm volatile("ld.shared.u16 %0, [%1];" : "=r"(s0) : "r"(row + 192 + 4 * ks0 + 2 * h));
+        asm volatile("ld.shared.u16 %0, [%1];" : "=r"(s1) : "r"(row + 192 + 4 * (ks0 + 1) + 2 * h));
+        const float d = half_bits_to_float(dbits);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const uint32_t sp = j ? s1 : s0;
+            const int i = 2 * j + h;
+            uint32_t a[2], a16[2], b[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float ds = d * (float)(int)(int8_t)((sp >> (8 * e)) & 0xFFu);
+                a[e] = f16x2_splat_satfinite(512.0f * ds);
+                a16[e] = f16x2_splat_satfinite(8192.0f * ds);
+                b[e] = f16x2_splat_satfinite(-32.0f * ds);
+            }
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                const int e = w >> 2;   // weights 4w..4w+3: scale 0 for l < 16, 1 after
+                uint32_t o0, o1, f0, f1;
+                codes4_to_f16((ql[w] >> (4 * j)) & 0x0F0F0F0Fu, a[e], b[e], o0, o1);
+                codes4_to_f16((qh[w] >> (2 * i)) & 0x03030303u, a16[e], 0u, f0, f1);
+                out[j][2 * w] = fma_f16x2(0x3C003C00u, f0, o0);
+                out[j][2 * w + 1] = fma_f16x2(0x3C003C00u, f1, o1);
+            }
+        }
+    } else if (F == kFmtQ5_K) {
         const uint4 hd = ld_shared_v4(row);
         const uint4 qh0 = ld_shared_v4(row + 16), qh1 = ld_shared_v4(row + 32);
         const uint32_t qh[8] = {qh0.x, qh0.y, qh0.z, qh0.w, qh1.x, qh1.y, qh1.z, qh1.w};
@@ -228,7 +296,8 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int role = warp_role(warp);
+    // (Q6_K: warp 7 shares the producer's row copies)
+    const int role = F == kFmtQ6_K && warp == 7 ? ROLE_WPROD : warp_role(warp);
     const uint32_t s_r = smem_u32(smem + OFF_R);
     const uint32_t s_x = smem_u32(smem + OFF_X), s_h = smem_u32(smem + OFF_H);
 
@@ -258,7 +327,7 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
         prefetch_tensormap(&maps.x);
         prefetch_tensormap(&maps.wg);
         prefetch_tensormap(&maps.wu);
-        prefetch_tensormap(&maps.wd);
+        if (F != kFmtQ6_K) prefetch_tensormap(&maps.wd);
     }
     if (role == ROLE_MMA) {
         tmem_alloc(tmem_slot, TMEM_COLS);
@@ -277,39 +346,64 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
     auto unit_of = [&](int k) { return make_unit(p, (int)blockIdx.x + k * (int)gridDim.x, n_tiles); };
 
     if (role == ROLE_WPROD) {
-        // ------------- TMA producer: whole Q4_K blocks of 128 weight rows -------------
-        if (lane == 0) {
-            uint32_t ri = 0, rph = 0, issued = 0;
-            bool ok = true;
-            for (int k = 0; k < m_units && ok; ++k) {
-                const Unit un = unit_of(k);
-                const int nbs_g = un.ks_g / KSB, nbs_y = un.ks_y / KSB;
-                for (int b = 0; b < un.n_ib * nbs_g + un.n_hb * nbs_y; ++b) {
-                    if (!mbar_wait(&r_empty[ri], rph ^ 1, abort_flag, p.err)) { ok = false; break; }
-                    uint8_t *rs = smem + OFF_R + ri * R_BYTES;
-                    if (b < un.n_ib * nbs_g) {
-                        const int ib = b / nbs_g, kb = b % nbs_g;
-                        const int row = un.expert * p.I + un.i0 + ib * BM;
+        // ------------- producer: whole blocks of 128 weight rows -------------
+        // Lane 0 of warp 5 issues the TMA boxes; for a Q6_K W_down stage
+        // every lane of warps 5 and 7 bulk-copies two rows' blocks (a bulk
+        // copy holds up its issuing thread for a few hundred cycles).
+        const int pw = warp == 5 ? 0 : 1;                // producer warp index
+        uint32_t ri = 0, rph = 0, issued = 0;
+        bool ok = true;
+        for (int k = 0; k < m_units && ok; ++k) {
+            const Unit un = unit_of(k);
+            const int nbs_g = un.ks_g / KSB, nbs_y = un.ks_y / KSB;
+            for (int b = 0; b < un.n_ib * nbs_g + un.n_hb * nbs_y; ++b) {
+                if (!mbar_wait(&r_empty[ri], rph ^ 1, abort_flag, p.err)) { ok = false; break; }
+                uint8_t *rs = smem + OFF_R + ri * R_BYTES;
+                if (b < un.n_ib * nbs_g) {
+                    const int ib = b / nbs_g, kb = b % nbs_g;
+                    const int row = un.expert * p.I + un.i0 + ib * BM;
+                    if (pw == 0 && lane == 0) {
                         mbar_arrive_expect_tx(&r_full[ri], 2 * R_BOX);
                         tma_load_2d(rs, &maps.wg, &r_full[ri], kb * kBlockBytes, row);
                         tma_load_2d(rs + R_BOX, &maps.wu, &r_full[ri], kb * kBlockBytes, row);
-                    } else {
-                        const int bb = b - un.n_ib * nbs_g;
-                        const int hb = bb / nbs_y, kb = bb % nbs_y;
-                        const int row = un.expert * p.H + hb * BM;
+                    }
+                } else {
+                    const int bb = b - un.n_ib * nbs_g;
+                    const int hb = bb / nbs_y, kb = bb % nbs_y;
+                    const int row = un.expert * p.H + hb * BM;
+                    if (F == kFmtQ6_K) {
+                        // row t = 64 pw + 32 q + lane: the 16-byte aligned
+                        // range of its block, which starts at an even offset
+                        // of at most 14 and so always spans 224 bytes, inside
+                        // the matrix (a 16-byte aligned W_down whose rows of
+                        // H % 256 == 0 blocks end on a 16-byte boundary).  The
+                        // stage expects 128 such ranges; the other warp's
+                        // copies may land before the count is raised (the
+                        // phase still waits for the arrival).
+                        if (pw == 0 && lane == 0) mbar_arrive_expect_tx(&r_full[ri], BM * 224u);
+#pragma unroll
+                        for (int q = 0; q < BM / 64; ++q) {
+                            const int t = 64 * pw + 32 * q + lane;
+                            const uint64_t src = reinterpret_cast<uint64_t>(p.Wd) +
+                                                 (uint64_t)((int64_t)(row + t) * p.rbI) +
+                                                 (uint64_t)(un.i0 / 256 + kb) * 210u;
+                            bulk_copy_g2s(rs + (size_t)t * wd_box_bytes<F>(),
+                                          reinterpret_cast<const void *>(src & ~15ull), 224u, &r_full[ri]);
+                        }
+                    } else if (pw == 0 && lane == 0) {
                         mbar_arrive_expect_tx(&r_full[ri], BM * wd_box_bytes<F>());
                         tma_load_2d(rs, &maps.wd, &r_full[ri], (un.i0 / 256 + kb) * wd_box_bytes<F>(), row);
                     }
-                    ++issued;
-                    if (++ri == NR) { ri = 0; rph ^= 1; }
                 }
+                ++issued;
+                if (++ri == NR) { ri = 0; rph ^= 1; }
             }
-            // every load issued here lands before the block may exit
-            for (uint32_t i = 0; i < (uint32_t)NR && i < issued; ++i) {
-                if (ri == 0) { ri = NR; rph ^= 1; }
-                --ri;
-                mbar_wait(&r_full[ri], rph, nullptr, p.err, kWaitBudgetCycles / 8);
-            }
+        }
+        // every load issued here lands before the block may exit
+        for (uint32_t i = 0; i < (uint32_t)NR && i < issued; ++i) {
+            if (ri == 0) { ri = NR; rph ^= 1; }
+            --ri;
+            mbar_wait(&r_full[ri], rph, nullptr, p.err, kWaitBudgetCycles / 8);
         }
     } else if (role == ROLE_XPROD) {
         // ------------- TMA producer: x tiles of the group, one per gate/up K step -------------
@@ -450,7 +544,14 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
                         !mbar_wait(&a_empty[ai + 1], aph ^ 1, abort_flag, p.err)) { ok = false; break; }
                     tc_fence_after();
                     uint32_t v[2][16];
-                    unpack_wd_pair_fmt<F>(s_r + ri * R_BYTES + (uint32_t)(r * wd_box_bytes<F>()), cur_ks & 3, task, v);
+                    // (Q6_K: where the row's block starts in its slot)
+                    const uint32_t off =
+                        F == kFmtQ6_K
+                            ? (uint32_t)(((int64_t)(un.expert * p.H + cur_blk * BM + r) * p.rbI +
+                                          (int64_t)(un.i0 / 256 + (cur_ks >> 2)) * 210) & 15)
+                            : 0u;
+                    unpack_wd_pair_fmt<F>(s_r + ri * R_BYTES + (uint32_t)(r * wd_box_bytes<F>()) + off, cur_ks & 3,
+                                          task, v);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&r_empty[ri]);
 #pragma unroll
@@ -460,7 +561,7 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
                             for (int i = 0; i < 16; ++i) v[j][i] = 0u;
                         }
                         const uint32_t dst = t_row + COL_A + (ai + j) * A_COLS;
-                        if (F == kFmtQ5_K) {
+                        if (F == kFmtQ5_K || F == kFmtQ6_K) {
                             tmem_st_32x32b_x16(dst + 16 * task, v[j]);
                         } else {   // Q5_1: columns 8 task .. +7 of each 32-weight block
                             const uint32_t v0[8] = {v[j][0], v[j][1], v[j][2], v[j][3], v[j][4], v[j][5], v[j][6], v[j][7]};
@@ -626,7 +727,9 @@ static bool encode_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *m,
 int moe_group_rows() { return mg::NG; }
 
 cudaError_t launch_moe_group(const TcArgs &a, int wd_fmt, cudaStream_t s) {
-    if (wd_fmt != kFmtQ4_K && wd_fmt != kFmtQ5_K && wd_fmt != kFmtQ5_1) return cudaErrorInvalidValue;
+    if (wd_fmt != kFmtQ4_K && wd_fmt != kFmtQ5_K && wd_fmt != kFmtQ5_1 && wd_fmt != kFmtQ6_K)
+        return cudaErrorInvalidValue;
+    if (wd_fmt == kFmtQ6_K && (reinterpret_cast<uintptr_t>(a.Wd) & 15)) return cudaErrorInvalidValue;
     const DeviceInfo &di = device_info();
     if (a.H % 256 != 0 || a.I % 64 != 0) return cudaErrorInvalidValue;
     void *ptr = nullptr;
@@ -639,21 +742,26 @@ cudaError_t launch_moe_group(const TcArgs &a, int wd_fmt, cudaStream_t s) {
     const int64_t rbH = q4k_row_bytes(a.H), rbI = fmt_row_bytes(wd_fmt, a.I);
     const int wd_box = wd_fmt == kFmtQ5_K ? mg::wd_box_bytes<kFmtQ5_K>()
                      : wd_fmt == kFmtQ5_1 ? mg::wd_box_bytes<kFmtQ5_1>() : mg::wd_box_bytes<kFmtQ4_K>();
+    memset(&maps, 0, sizeof(maps));
     if (!encode_map(encode, &maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.x, a.H, a.x_rows, (int64_t)a.H * 2,
                     mg::BK, mg::NG, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_map(encode, &maps.wg, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wg, rbH, (int64_t)a.E * a.I, rbH,
                     kBlockBytes, mg::BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_map(encode, &maps.wu, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wu, rbH, (int64_t)a.E * a.I, rbH,
                     kBlockBytes, mg::BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_map(encode, &maps.wd, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wd, rbI, (int64_t)a.E * a.H, rbI,
-                    wd_box, mg::BM, CU_TENSOR_MAP_SWIZZLE_NONE))
+        (wd_fmt != kFmtQ6_K &&
+         !encode_map(encode, &maps.wd, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wd, rbI, (int64_t)a.E * a.H, rbI,
+                     wd_box, mg::BM, CU_TENSOR_MAP_SWIZZLE_NONE)))
         return cudaErrorInvalidValue;
     const void *fn = wd_fmt == kFmtQ5_K ? (const void *)mg::moe_group_kernel<kFmtQ5_K>
                    : wd_fmt == kFmtQ5_1 ? (const void *)mg::moe_group_kernel<kFmtQ5_1>
+                   : wd_fmt == kFmtQ6_K ? (const void *)mg::moe_group_kernel<kFmtQ6_K>
                                         : (const void *)mg::moe_group_kernel<kFmtQ4_K>;
     cudaError_t e = ensure_dynamic_smem(fn, (size_t)mg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     mg::Params p;
+    p.Wd = a.Wd;
+    p.rbI = rbI;
     p.y = a.y;
     p.tiles = a.tiles;
     p.n_tiles_dev = a.n_tiles_dev;

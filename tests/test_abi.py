@@ -161,11 +161,12 @@ def test_format_row_bytes_and_rejections(lib):
     assert L.zffn_dequant_fmt(1, FAKE, FAKE, 0, 256, None) == zffn.ERR_INVALID_ARG
     assert L.zffn_swiglu_q4k_wd(FAKE, FAKE, FAKE, FAKE, 9, FAKE, 1, 256, 256, None) == zffn.ERR_INVALID_ARG
     assert L.zffn_swiglu_q4k_wd(FAKE, FAKE, FAKE, FAKE, 2, FAKE, 1, 200, 256, None) == zffn.ERR_INVALID_ARG
-    # Q6_K W_down: single-token paths only (checked on the host); Q5_K and
-    # Q5_1 at T > 1 pass the host checks and need a device
-    assert L.zffn_swiglu_q4k_wd(FAKE, FAKE, FAKE, FAKE, 2, FAKE, 4, 256, 256, None) == zffn.ERR_UNSUPPORTED
-    assert L.zffn_moe_swiglu_q4k_wd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, FAKE, 3, 256, 256, 8, 2,
-                                    None) == zffn.ERR_UNSUPPORTED
+    # every format at T > 1 wants a 16-byte aligned W_down (checked on the host)
+    odd4 = ctypes.c_void_p(0x10004)
+    for fmt in (1, 2, 3):
+        assert L.zffn_swiglu_q4k_wd(FAKE, FAKE, FAKE, odd4, fmt, FAKE, 4, 256, 256, None) == zffn.ERR_INVALID_ARG
+        assert L.zffn_moe_swiglu_q4k_wd(FAKE, FAKE, FAKE, FAKE, FAKE, odd4, fmt, FAKE, 3, 256, 256, 8, 2,
+                                        None) == zffn.ERR_INVALID_ARG
     assert L.zffn_moe_swiglu_q4k_wd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 1, 256, 256, 0, 2,
                                     None) == zffn.ERR_INVALID_ARG
 

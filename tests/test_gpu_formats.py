@@ -124,7 +124,7 @@ def test_q4k_format_code_is_the_regular_block():
     assert_close(y, orc.swiglu_ffn(x, *W, 5, H, I), "Q4_K through the format entry")
 
 
-@pytest.mark.parametrize("fmt", [zffn.FMT_Q5_K, zffn.FMT_Q5_1])
+@pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("T,H,I", [(2, 256, 704), (33, 1024, 1472), (100, 512, 384), (40, 256, 2048)])
 def test_several_tokens_dense(fmt, T, H, I):
     # T > 1: the grouped tensor-core kernel (groups of 32 tokens); shapes with a
@@ -140,7 +140,7 @@ def test_several_tokens_dense(fmt, T, H, I):
     assert_close(y, orc.swiglu_ffn(x, Wg, Wu, Wd, T, H, I, wd_fmt=fmt), f"fmt {fmt} T={T} H={H} I={I}")
 
 
-@pytest.mark.parametrize("fmt", [zffn.FMT_Q5_K, zffn.FMT_Q5_1])
+@pytest.mark.parametrize("fmt", FORMATS)
 def test_several_tokens_routed_full_config(fmt):
     # E = 128, H = 2048, I = 768, top-8, T = 64, every expert's W_down in fmt,
     # with a per-expert down scale and an invalid slot
@@ -160,17 +160,6 @@ def test_several_tokens_routed_full_config(fmt):
     ref = orc.moe_swiglu_ffn(x[rows].copy(), ids[rows].copy(), w[rows].copy(), Wg, Wu, Wd, len(rows), H, I, E,
                              k, wd_fmt=fmt, down_scale=scale)
     assert_close(y[rows], ref, f"routed T=64 fmt {fmt}")
-
-
-def test_q6k_rejects_several_tokens():
-    rng = np.random.default_rng(301)
-    H, I = 256, 256
-    W = [dev(synth.random_q4k_blocks(rng, I, H)), dev(synth.random_q4k_blocks(rng, I, H)),
-         dev(synth.random_blocks(rng, zffn.FMT_Q6_K, H, I))]
-    x = x_dev(synth.f32_to_bf16_bits(rng.standard_normal((3, H)).astype(np.float32)))
-    with pytest.raises(zffn.ZffnError) as e:
-        zffn.swiglu_q4k_wd(x, *W, zffn.FMT_Q6_K, I)
-    assert e.value.status == zffn.ERR_UNSUPPORTED
 
 
 def test_small_format_call_then_larger_q4k_single_token():
