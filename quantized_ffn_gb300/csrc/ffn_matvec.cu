@@ -763,8 +763,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) ffn_token_fused_kernel(MatvecA
         __syncwarp();
         if (part == 0 && cs < ce) mbar_arrive(&bars[2 + c]);
     } else if (warp == 2) {
-        // down rows [n0, n1) of every valid slot, one range each; the slot
-        // table for later
+        // the slot table, and the bytes of the down rows [n0, n1) of every
+        // valid slot (one range each, copied once this warp's part of step 1
+        // is done: issued now, they would compete with the gate/up rows that
+        // step 1 and the grid barrier wait for)
         uint32_t total = 0;
         for (int p = lane; p < P; p += 32) {
             const int e = a.ids[p];
@@ -781,14 +783,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) ffn_token_fused_kernel(MatvecA
 #pragma unroll
         for (int s = 16; s > 0; s >>= 1) total += __shfl_xor_sync(0xffffffffu, total, s);
         if (lane == 0) mbar_arrive_expect_tx(&bars[1], total);
-        __syncwarp();
-        if (nd > 0)
-            for (int p = lane; p < P; p += 32) {
-                const int e = s_e[p];
-                if (e < 0) continue;
-                bulk_g2s(dn + (size_t)p * nd * G.rbI, a.Wd + ((int64_t)e * H + n0) * G.rbI,
-                         (uint32_t)((int64_t)nd * G.rbI), &bars[1]);
-            }
     }
     // quantise x
     if (!mbar_wait(&bars[0], 0, nullptr, a.err)) return;
@@ -873,6 +867,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) ffn_token_fused_kernel(MatvecA
             }
         }
     }
+    if (warp == 2 && nd > 0)
+        for (int p = lane; p < P; p += 32) {
+            const int e = s_e[p];
+            if (e < 0) continue;
+            bulk_g2s(dn + (size_t)p * nd * G.rbI, a.Wd + ((int64_t)e * H + n0) * G.rbI,
+                     (uint32_t)((int64_t)nd * G.rbI), &bars[1]);
+        }
     // every block's h rows (made visible by the barrier's fence), then all of h
     __syncthreads();
     if (threadIdx.x == 0) *s_ok = grid_barrier(a.gbar, gridDim.x, a.err) ? 1 : 0;
