@@ -528,11 +528,12 @@ def run_gpu(args):
                   "rel_l2_vs_fused": round(rel, 5)}
         del wf, wb, gs, us, hs, ys
 
-    # single-token blocks with W_down in the other block formats (W_gate and
-    # W_up the workload's Q4_K matrices, W_down seeded random blocks of the
-    # format), one call between events after an L2 flush
+    # blocks with W_down in the other block formats (W_gate and W_up the
+    # workload's Q4_K matrices, W_down seeded random blocks of the format),
+    # one call between events after an L2 flush: the single-token workloads,
+    # and the routed layer at T > 1 (the grouped tensor-core kernel)
     down_formats = None
-    if T == 1:
+    if T == 1 or kind == "moe":
         from quantized_ffn_gb300 import synth as _synth
         down_formats = {}
         rng_f = np.random.default_rng(seed + 2000)
@@ -554,8 +555,8 @@ def run_gpu(args):
             torch.cuda.synchronize()
             assert zffn.get_device_error() == zffn.OK
             f_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(f_st, f_en))
-            touched = 1 if kind == "dense" else k
-            f_bytes = touched * (2 * I * row_bytes(H) + H * zffn.row_bytes_fmt(fmt, I)) + H * 2 + H * 4
+            touched = 1 if kind == "dense" else (k if T == 1 else int(torch.unique(ids[ids >= 0]).numel()))
+            f_bytes = touched * (2 * I * row_bytes(H) + H * zffn.row_bytes_fmt(fmt, I)) + T * H * 2 + T * H * 4
             f_gbs = f_bytes / (f_ms * 1e-3) / 1e9
             down_formats[fname] = {"ms": round(f_ms, 5), "hbm_bytes": f_bytes,
                                    "achieved_gbs": round(f_gbs, 1),
@@ -638,8 +639,9 @@ def run_gpu(args):
         **({"router": router} if router is not None else {}),
         **({"rmsnorm": norm} if norm is not None else {}),
         **({"staged": staged} if staged is not None else {}),
-        **({"down_formats": {"kernels": "ffn_gu_kernel + down_fmt_kernel", "timing":
-                             "one isolated call after an L2 flush", **down_formats}}
+        **({"down_formats": {"kernels": ("ffn_gu_kernel + down_fmt_kernel" if T == 1 else
+                                         "moe_route_kernel + moe_gather_kernel + moe_group_kernel<F>"),
+                             "timing": "one isolated call after an L2 flush", **down_formats}}
            if down_formats is not None else {}),
         "clocks": clocks,
         "gpu_launches": launches_per_call * args.steps,
