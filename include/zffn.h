@@ -369,7 +369,11 @@ const char *zffn_last_error(void);
 
 /* Synchronise `stream`, then return and clear the current device's error word:
  * ZFFN_OK, or ZFFN_ERR_TIMEOUT if a bounded device wait ran out since the last
- * read.  ZFFN_ERR_CUDA if the synchronisation itself failed. */
+ * read.  ZFFN_ERR_CUDA if the synchronisation itself failed.  On
+ * ZFFN_ERR_TIMEOUT it also resets the grid-barrier count of the one-launch
+ * routed path in the device's workspace (a barrier that ran out leaves it
+ * mid-count), so the caller must have no call of the library still running
+ * on the device (the calls share the workspace anyway). */
 zffn_status zffn_get_device_error(void *stream);
 
 /* Tunables (process-wide).  ZFFN_OPT_MATVEC_MAX_T: 1 (default) sends single-token

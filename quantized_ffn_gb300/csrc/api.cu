@@ -672,6 +672,17 @@ zffn_status zffn_get_device_error(void *stream) {
         return to_status(cudaErrorUnknown);
     if (cudaMemsetAsync(di.err_word, 0, sizeof(int), s) != cudaSuccess) return ZFFN_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return to_status(cudaErrorUnknown);
+    if (v == ZFFN_ERR_TIMEOUT) {
+        // a grid barrier that ran out leaves its count mid-count: start over
+        std::lock_guard<std::mutex> lk(g_mu);
+        Workspace &w = g_ws[di.device];
+        if (w.ptr) {
+            const Layout L = layout_for(1, 1, 1, 1, 1);
+            if (cudaMemset(static_cast<uint8_t *>(w.ptr) + L.gbar, 0, sizeof(unsigned long long)) != cudaSuccess ||
+                cudaDeviceSynchronize() != cudaSuccess)
+                return to_status(cudaErrorUnknown);
+        }
+    }
     return v == 0 ? ZFFN_OK : (zffn_status)v;
 }
 

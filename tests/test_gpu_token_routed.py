@@ -122,3 +122,22 @@ def test_layer_too_large_for_one_launch_falls_back():
         y = zffn.moe_swiglu_q4k(x_dev(x), dev(ids), dev(w), dev(Wg), dev(Wu), dev(Wd), I, E)
         assert zffn.get_device_error() == zffn.OK
     assert_close(y, orc.moe_swiglu_ffn(x, ids, w, Wg, Wu, Wd, 1, H, I, E, k), "fallback to the pair")
+
+
+def test_timeout_report_resets_the_barrier_and_the_path_still_works():
+    # a reported timeout (here from the bounded-wait self test) resets the
+    # one-launch path's barrier count; calls before and after stay correct
+    E, H, I, k = 16, 512, 384, 4
+    rng = np.random.default_rng(980)
+    Wg, Wu, Wd = experts(rng, E, H, I)
+    dW = [dev(Wg), dev(Wu), dev(Wd)]
+    with token_kernel(0):
+        for call in range(3):
+            ids, w = orc.route_top_k(rng.standard_normal((1, E)).astype(np.float32), k)
+            x = token(rng, H)
+            y = zffn.moe_swiglu_q4k(x_dev(x), dev(ids), dev(w), *dW, I, E)
+            assert zffn.get_device_error() == zffn.OK
+            assert_close(y, orc.moe_swiglu_ffn(x, ids, w, Wg, Wu, Wd, 1, H, I, E, k), f"call {call}")
+            if call == 0:
+                zffn.selftest_wait_timeout(2_000_000)
+                assert zffn.get_device_error() == zffn.ERR_TIMEOUT
