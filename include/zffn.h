@@ -263,6 +263,10 @@ zffn_status zffn_moe_swiglu_q4k_wd(const void *x, const int32_t *expert_ids,
  *   Wd: E stacked experts, each H rows of ceil(I/256) blocks.
  *   y:  fp32 [T][H], overwritten.
  * Requirements as zffn_swiglu_q4k, plus 1 <= E <= 4096, 1 <= top_k <= 64.
+ * T = 1: one cooperative launch when every block's share of the token's
+ * expert weights fits in its shared memory (see ZFFN_OPT_TOKEN_KERNEL and
+ * zffn_single_token_launches), else the two single-token kernels; T > 1:
+ * routing, gathering and a tensor-core kernel.
  * Uses library workspace (see zffn_reserve).
  * Errors: INVALID_ARG, CUDA, NO_WORKSPACE. */
 zffn_status zffn_moe_swiglu_q4k(const void *x, const int32_t *expert_ids,
