@@ -193,7 +193,8 @@ def dequant_fmt(blocks: torch.Tensor, fmt: int, rows: int, cols: int,
 
 def swiglu_q4k_wd(x: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor, Wd: torch.Tensor, wd_fmt: int,
                   I: int, y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """The block with W_down in block format wd_fmt (other than Q4_K: T = 1 only)."""
+    """The block with W_down in block format wd_fmt (zffn_format: Q4_K, Q5_K, Q6_K, Q5_1);
+    T = 1 on the single-token kernels, T > 1 on the grouped tensor-core kernel."""
     T, H = x.shape
     if y is None:
         y = torch.empty((T, H), dtype=torch.float32, device=x.device)
