@@ -238,7 +238,7 @@ zffn_status zffn_dequant_fmt(int fmt, const void *blocks, float *out, int64_t ro
  *     tokens, so it suits routed layers and short prompts rather than long
  *     prefills.  Q6_K rows (210-byte blocks, row pitches not a multiple of 16
  *     bytes) are copied row by row instead of by TMA boxes: slower (about
- *     1.4x the Q5_K call at the routed T = 256 layer).
+ *     1.3x the Q5_K call at the routed T = 256 layer).
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA, NO_WORKSPACE. */
 zffn_status zffn_swiglu_q4k_wd(const void *x, const void *Wg, const void *Wu, const void *Wd,
                                int wd_fmt, float *y, int T, int H, int I, void *stream);

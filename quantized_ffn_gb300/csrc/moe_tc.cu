@@ -33,8 +33,8 @@
 //   warps 0-3   epilogue for TMEM lane quadrants 0-3: SwiGLU -> h, Y -> y
 //   warp 4      TMEM allocator and MMA issuer (one elected lane issues)
 //   warp 5      producer: whole blocks of 128 weight rows (one TMA box per
-//               matrix covers four K steps; a Q6_K W_down stage is 128 bulk
-//               copies, four per lane)
+//               matrix covers four K steps; a Q6_K W_down stage is copied in
+//               16-byte pieces by the threads of warps 5 and 7)
 //   warp 6      TMA producer: the group's x tiles [32 x 64] fp16
 //   warps 8-23  unpackers, four groups of four warps (one per TMEM lane
 //               quadrant) taking tasks in turn
@@ -48,15 +48,6 @@
 
 namespace zffn {
 namespace mg {
-
-// Bulk copy global -> shared (16-byte aligned addresses, a multiple of 16
-// bytes), counted on bar.
-__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
 
 // 32 bytes at the even shared address a: nine aligned words and eight funnel
 // shifts.
@@ -73,9 +64,9 @@ __device__ __forceinline__ void ld_shared_32_even(uint32_t a, uint32_t (&o)[8]) 
 // eight 24-byte blocks per 256 weights); the down phase's packed boxes are
 // [128 rows x WD_BOX(F) bytes].  All are multiples of 16 bytes, as TMA needs.
 // Q6_K (210-byte blocks, rows at 2-byte alignment) has no tensor map: each
-// row's block is bulk-copied as the 16-byte aligned range that holds it
-// (at most 224 bytes) into a 224-byte slot, the block starting (address % 16)
-// bytes into it.
+// row's block is copied as the 16-byte aligned range that holds it (224
+// bytes) into a 224-byte slot, the block starting (address % 16) bytes into
+// it.
 template <int F>
 __host__ __device__ constexpr int wd_box_bytes() {
     return F == kFmtQ5_K ? 176 : F == kFmtQ5_1 ? 192 : F == kFmtQ6_K ? 224 : 144;
@@ -303,7 +294,8 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NR; ++i) {
-            mbar_init(&r_full[i], 1);
+            // (Q6_K: every thread of the two producer warps arrives)
+            mbar_init(&r_full[i], F == kFmtQ6_K ? 64 : 1);
             mbar_init(&r_empty[i], 2 * 2 * 4);        // 2 K-step pairs x 2 tasks x 4 warps
         }
         for (int i = 0; i < NA; ++i) {
@@ -347,9 +339,13 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
 
     if (role == ROLE_WPROD) {
         // ------------- producer: whole blocks of 128 weight rows -------------
-        // Lane 0 of warp 5 issues the TMA boxes; for a Q6_K W_down stage
-        // every lane of warps 5 and 7 bulk-copies two rows' blocks (a bulk
-        // copy holds up its issuing thread for a few hundred cycles).
+        // Lane 0 of warp 5 issues the TMA boxes.  Q6_K: warps 5 and 7 both
+        // run this loop and every one of their threads arrives once per stage
+        // (the stage barrier expects 64 arrivals): on a gate/up stage lane 0
+        // of warp 5 with the TMA bytes and the others plainly; on a W_down
+        // stage each thread copies two rows' blocks in 16-byte pieces
+        // (cp.async, no TMA: 128 small bulk copies a stage were bound by the
+        // copy engine) and arrives when they have landed.
         const int pw = warp == 5 ? 0 : 1;                // producer warp index
         uint32_t ri = 0, rph = 0, issued = 0;
         bool ok = true;
@@ -366,6 +362,8 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
                         mbar_arrive_expect_tx(&r_full[ri], 2 * R_BOX);
                         tma_load_2d(rs, &maps.wg, &r_full[ri], kb * kBlockBytes, row);
                         tma_load_2d(rs + R_BOX, &maps.wu, &r_full[ri], kb * kBlockBytes, row);
+                    } else if (F == kFmtQ6_K) {
+                        mbar_arrive(&r_full[ri]);
                     }
                 } else {
                     const int bb = b - un.n_ib * nbs_g;
@@ -374,22 +372,26 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
                     if (F == kFmtQ6_K) {
                         // row t = 64 pw + 32 q + lane: the 16-byte aligned
                         // range of its block, which starts at an even offset
-                        // of at most 14 and so always spans 224 bytes, inside
-                        // the matrix (a 16-byte aligned W_down whose rows of
-                        // H % 256 == 0 blocks end on a 16-byte boundary).  The
-                        // stage expects 128 such ranges; the other warp's
-                        // copies may land before the count is raised (the
-                        // phase still waits for the arrival).
-                        if (pw == 0 && lane == 0) mbar_arrive_expect_tx(&r_full[ri], BM * 224u);
+                        // of at most 14 and so always spans 224 bytes (14
+                        // pieces), inside the matrix (a 16-byte aligned
+                        // W_down whose rows of H % 256 == 0 blocks end on a
+                        // 16-byte boundary)
+                        const uint32_t dst0 = smem_u32(rs);
 #pragma unroll
                         for (int q = 0; q < BM / 64; ++q) {
                             const int t = 64 * pw + 32 * q + lane;
-                            const uint64_t src = reinterpret_cast<uint64_t>(p.Wd) +
-                                                 (uint64_t)((int64_t)(row + t) * p.rbI) +
-                                                 (uint64_t)(un.i0 / 256 + kb) * 210u;
-                            bulk_copy_g2s(rs + (size_t)t * wd_box_bytes<F>(),
-                                          reinterpret_cast<const void *>(src & ~15ull), 224u, &r_full[ri]);
+                            const uint64_t src = (reinterpret_cast<uint64_t>(p.Wd) +
+                                                  (uint64_t)((int64_t)(row + t) * p.rbI) +
+                                                  (uint64_t)(un.i0 / 256 + kb) * 210u) & ~15ull;
+#pragma unroll
+                            for (int c = 0; c < 14; ++c)
+                                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                                                 dst0 + (uint32_t)(t * wd_box_bytes<F>() + 16 * c)),
+                                             "l"(src + 16ull * c)
+                                             : "memory");
                         }
+                        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&r_full[ri]))
+                                     : "memory");
                     } else if (pw == 0 && lane == 0) {
                         mbar_arrive_expect_tx(&r_full[ri], BM * wd_box_bytes<F>());
                         tma_load_2d(rs, &maps.wd, &r_full[ri], (un.i0 / 256 + kb) * wd_box_bytes<F>(), row);
