@@ -3,10 +3,10 @@
 // What it computes, per (token tile, intermediate chunk) work unit:
 //   for each 128-row slice s of the chunk:
 //       [G | U] = X_tile . [W_gate rows ; W_up rows]^T        (tcgen05, TMEM)
-//       h[:, s] = bf16( silu(G) * U )                           (epilogue)
+//       h[:, s] = fp16( silu(G) * U * 2^-8 )                    (epilogue)
 //   for each 128-column slice n of the output:
 //       Y = h . W_down[n rows, chunk cols]^T                   (tcgen05, TMEM)
-//       y[token, n cols] += Y                                   (fp32 reductions in L2)
+//       y[token, n cols] += 2^8 * Y                             (fp32 reductions in L2)
 // This is the producer/consumer interleave along the intermediate dimension
 // ("Fused SwiGLU MLP: ZINC RDNA4 Down-Projection Bandwidth", section "Why
 // this fusion is harder than the last one"): a block of the intermediate is
@@ -14,7 +14,7 @@
 // next block; only x and y touch device memory.  Q4_K weights are unpacked
 // on chip on their way into the multiply (same page, FAQ "Why is fusing the
 // SwiGLU intermediate harder..."): dedicated warps read the packed blocks and
-// write bf16 operand tiles straight into shared memory; no unpacked copy of a
+// write fp16 operand tiles straight into shared memory; no unpacked copy of a
 // weight ever exists in device memory.  The scale/min pair of a sub-block is
 // decoded once per row and step, not per weight ("VGPR pressure caps the
 // fused RDNA4 prefill GEMM at nine waves", section "The recoverable registers
@@ -29,7 +29,7 @@
 // (each Y job is followed by an equal share of the next unit's gate/up
 // steps), so the y traffic is spread over the whole run.  TMEM holds one
 // gate/up accumulator (256 columns), one down-projection accumulator (128
-// columns) and a stash of the next unit's h (128 columns of bf16 pairs),
+// columns) and a stash of the next unit's h (128 columns of fp16 pairs),
 // copied into shared memory once the current unit's down projection has
 // consumed the previous h.
 //
@@ -38,8 +38,8 @@
 //               h stash -> shared memory, down-projection tile -> y
 //   warp 4      TMEM allocator and MMA issuer (one elected lane issues)
 //   warp 5      TMA producer: packed Q4_K weight slices into a ring
-//   warp 6      TMA producer: x tiles [128 x 64] bf16, 128-byte swizzle
-//   warps 8-19  weight unpackers: packed slices -> bf16 tiles, 128-byte
+//   warp 6      TMA producer: x tiles [128 x 64] fp16, 128-byte swizzle
+//   warps 8-19  weight unpackers: packed slices -> fp16 tiles, 128-byte
 //               swizzle
 //   warps 7, 20-23  idle
 // Every role walks the same step program (Prog below) in the same order.
@@ -51,7 +51,7 @@ namespace zffn {
 namespace tc {
 
 constexpr int BM = 128;                  // token rows per CTA per tile (UMMA M per CTA)
-constexpr int BK = 64;                   // K per gate/up step (128 bytes of bf16)
+constexpr int BK = 64;                   // K per gate/up step (128 bytes of fp16)
 constexpr int YK = 128;                  // K per down-projection step
 constexpr int GU_ROWS = 128;             // intermediate rows per gate/up job
 constexpr int NJ_GU = 256;               // UMMA N of a gate/up job (128 gate + 128 up rows)
@@ -59,6 +59,19 @@ constexpr int NJ_Y = 128;                // UMMA N of a down-projection job (out
 constexpr int A_BYTES = BM * BK * 2;     // 16 KB x tile per CTA
 constexpr int HT_BYTES = BM * BK * 2;    // one 64-column slice of h: 16 KB
 constexpr uint32_t COL_GU = 0, COL_Y = 256, COL_STASH = 384;   // TMEM columns
+// Both products take fp16 operands: x (converted once per call), the weights
+// (unpacked with the fp8 -> fp16 converter) and the intermediate, held as
+// h * 2^-8 so that its fp16 range reaches 1.7e7 (values beyond saturate);
+// the down projection's result is scaled back by 2^8 when it is drained.
+constexpr float H_SCALE = 1.0f / 256.0f;
+constexpr float Y_SCALE = 256.0f;
+// Two fp32 values -> one fp16 pair (lo in the low half), nearest, clamped to
+// the largest finite fp16.
+__device__ __forceinline__ uint32_t pack_f16x2_satfinite(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
 // Down-projection accumulators.  While a block has a next unit, its down jobs
 // use COL_Y only (the gate/up accumulator and the h stash are busy with the
 // next unit).  In a block's last unit both are free once its h is in shared
@@ -141,7 +154,7 @@ struct Cfg {
     static constexpr int EPI_ARRIVALS = PAIR ? 8 : 4;     // epilogue warps arriving per job
     static constexpr int B_ARRIVALS = (PAIR ? 2 : 1) * TASKS * UNPACK_GROUP_WARPS;
     static constexpr uint32_t IDESC_GU = idesc_f16_f32(PAIR ? 256 : 128, NJ_GU);   // fp16 x, W_gate, W_up
-    static constexpr uint32_t IDESC_Y = idesc_bf16_f32(PAIR ? 256 : 128, NJ_Y);
+    static constexpr uint32_t IDESC_Y = idesc_f16_f32(PAIR ? 256 : 128, NJ_Y);     // fp16 h * 2^-8, W_down
     static_assert(R_BYTES_Y <= R_BYTES, "down-step slice fits a weight stage");
     static_assert(!PAIR || UNPACK_GROUPS <= NB, "parity waits on B stages stay unambiguous");
     static_assert(PAIR || UNPACK_GROUPS <= 2 * NB, "parity waits on B stages stay unambiguous");
@@ -174,100 +187,6 @@ struct Params {
 struct Tile {
     int row_start, row_count, expert;
 };
-
-// Unpack the 8 code words (32 bytes) of one weight row and K step into its
-// swizzled bf16 row.  Word i holds code bytes 4i..4i+3: low nibbles are
-// weights 4i..4i+3 of the step, high nibbles weights 32+4i..32+4i+3.  A code
-// q becomes the float 1 + q/128 (low nibbles, at bits 16..19) or 1 + q/2048
-// (high nibbles, bits 12..15) by OR-ing it into the bits of 1.0f; then
-// d*sc*q - dmin*m = (S*d*sc)*f - (S*d*sc + dmin*m) with S = 128 or 2048, one
-// fused multiply-add per weight.  The constant is rounded once, an error
-// below 2^-13 of one quantisation step, far under the bf16 rounding of the
-// result.
-__device__ __forceinline__ void unpack_row_to_smem_wide(uint4 hd, const uint32_t (&w)[8], int g,
-                                                   uint32_t row_addr, int row) {
-    const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
-    int sc0, m0, sc1, m1;
-    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g, sc0, m0);
-    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g + 1, sc1, m1);
-    const float a0 = 128.0f * (d * (float)sc0);
-    const float c0 = -(a0 + dmin * (float)m0);
-    const float a1 = 2048.0f * (d * (float)sc1);
-    const float c1 = -(a1 + dmin * (float)m1);
-    constexpr uint32_t ONE = 0x3F800000u, MLO = 0x000F0000u, MHI = 0x0000F000u;
-    uint32_t lo[16], hi[16];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t x = w[i], xl8 = x << 8, xr8 = x >> 8, xl16 = x << 16, xr16 = x >> 16;
-        const float l0 = fmaf(a0, __uint_as_float((xl16 & MLO) | ONE), c0);
-        const float l1 = fmaf(a0, __uint_as_float((xl8 & MLO) | ONE), c0);
-        const float l2 = fmaf(a0, __uint_as_float((x & MLO) | ONE), c0);
-        const float l3 = fmaf(a0, __uint_as_float((xr8 & MLO) | ONE), c0);
-        const float h0 = fmaf(a1, __uint_as_float((xl8 & MHI) | ONE), c1);
-        const float h1 = fmaf(a1, __uint_as_float((x & MHI) | ONE), c1);
-        const float h2 = fmaf(a1, __uint_as_float((xr8 & MHI) | ONE), c1);
-        const float h3 = fmaf(a1, __uint_as_float((xr16 & MHI) | ONE), c1);
-        lo[2 * i] = pack_bf16x2(l0, l1);
-        lo[2 * i + 1] = pack_bf16x2(l2, l3);
-        hi[2 * i] = pack_bf16x2(h0, h1);
-        hi[2 * i + 1] = pack_bf16x2(h2, h3);
-    }
-    // 16-byte chunk c holds weights 8c..8c+7 (chunks 0-3 low nibbles, 4-7 high)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        st_shared_v4(row_addr + (((uint32_t)(c ^ (row & 7))) << 4), lo[4 * c], lo[4 * c + 1],
-                     lo[4 * c + 2], lo[4 * c + 3]);
-        st_shared_v4(row_addr + (((uint32_t)((c + 4) ^ (row & 7))) << 4), hi[4 * c],
-                     hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
-    }
-}
-
-// The same, storing each 16-byte chunk as soon as it is formed: fewer live
-// registers (the single-CTA kernel unpacks two tasks per step and would
-// otherwise spill).
-__device__ __forceinline__ void unpack_row_to_smem_narrow(uint4 hd, const uint32_t (&w)[8], int g,
-                                                   uint32_t row_addr, int row) {
-    const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
-    int sc0, m0, sc1, m1;
-    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g, sc0, m0);
-    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g + 1, sc1, m1);
-    const float a0 = 128.0f * (d * (float)sc0);
-    const float c0 = -(a0 + dmin * (float)m0);
-    const float a1 = 2048.0f * (d * (float)sc1);
-    const float c1 = -(a1 + dmin * (float)m1);
-    constexpr uint32_t ONE = 0x3F800000u, MLO = 0x000F0000u, MHI = 0x0000F000u;
-    // 16-byte chunk c holds weights 8c..8c+7 (chunks 0-3 low nibbles, 4-7
-    // high); two code words make a chunk, stored as soon as it is formed
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        uint32_t lo[4], hi[4];
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const uint32_t x = w[2 * c + k], xl8 = x << 8, xr8 = x >> 8, xl16 = x << 16, xr16 = x >> 16;
-            const float l0 = fmaf(a0, __uint_as_float((xl16 & MLO) | ONE), c0);
-            const float l1 = fmaf(a0, __uint_as_float((xl8 & MLO) | ONE), c0);
-            const float l2 = fmaf(a0, __uint_as_float((x & MLO) | ONE), c0);
-            const float l3 = fmaf(a0, __uint_as_float((xr8 & MLO) | ONE), c0);
-            const float h0 = fmaf(a1, __uint_as_float((xl8 & MHI) | ONE), c1);
-            const float h1 = fmaf(a1, __uint_as_float((x & MHI) | ONE), c1);
-            const float h2 = fmaf(a1, __uint_as_float((xr8 & MHI) | ONE), c1);
-            const float h3 = fmaf(a1, __uint_as_float((xr16 & MHI) | ONE), c1);
-            lo[2 * k] = pack_bf16x2(l0, l1);
-            lo[2 * k + 1] = pack_bf16x2(l2, l3);
-            hi[2 * k] = pack_bf16x2(h0, h1);
-            hi[2 * k + 1] = pack_bf16x2(h2, h3);
-        }
-        st_shared_v4(row_addr + (((uint32_t)(c ^ (row & 7))) << 4), lo[0], lo[1], lo[2], lo[3]);
-        st_shared_v4(row_addr + (((uint32_t)((c + 4) ^ (row & 7))) << 4), hi[0], hi[1], hi[2], hi[3]);
-    }
-}
-
-template <bool PAIR>
-__device__ __forceinline__ void unpack_row_to_smem(uint4 hd, const uint32_t (&w)[8], int g, uint32_t row_addr,
-                                                   int row) {
-    if (PAIR) unpack_row_to_smem_wide(hd, w, g, row_addr, row);
-    else unpack_row_to_smem_narrow(hd, w, g, row_addr, row);
-}
 
 // Work-unit geometry shared by every role.
 struct Unit {
@@ -662,8 +581,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!mbar_wait(&b_empty[bi], bph ^ 1, abort_flag, p.err)) { ok = false; break; }
                 const uint32_t rb = s_b + bi * C::B_BYTES + half * (C::ROWS_Y * 128) + sw128_row(row);
                 const uint32_t w8[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                if (pg.gu) unpack_row_to_smem_f16(hd, w8, g, rb, row);
-                else unpack_row_to_smem<PAIR>(hd, w8, g, rb, row);
+                unpack_row_to_smem_f16(hd, w8, g, rb, row);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) arrive_leader(&b_full[bi]);
@@ -710,9 +628,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int j = 0; j < 8; ++j) {
                         const float g0 = __uint_as_float(gr[2 * j]), g1 = __uint_as_float(gr[2 * j + 1]);
                         const float u0 = __uint_as_float(ur[2 * j]), u1 = __uint_as_float(ur[2 * j + 1]);
-                        const float h0 = __fdividef(g0 * u0, 1.0f + __expf(-g0));
-                        const float h1 = __fdividef(g1 * u1, 1.0f + __expf(-g1));
-                        hw[j] = pack_bf16x2(h0, h1);
+                        const float h0 = __fdividef(g0 * u0 * H_SCALE, 1.0f + __expf(-g0));
+                        const float h1 = __fdividef(g1 * u1 * H_SCALE, 1.0f + __expf(-g1));
+                        hw[j] = pack_f16x2_satfinite(h0, h1);
                     }
                     // stash column s*64 + c/2 holds h columns s*128 + c, +1
                     tmem_st_32x32b_x8(t_lane + COL_STASH + s * 64 + c / 2, hw);
@@ -749,11 +667,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (pg.blk != cur) { cur = pg.blk; un = unit_of(cur); }
                 valid = row < un.tile.row_count;
                 token = 0;
-                wgt = 1.0f;
+                wgt = Y_SCALE;
                 if (valid) {
                     const int xr = un.tile.row_start + row;
                     token = p.row_token ? p.row_token[xr] : xr;
-                    wgt = p.row_weight ? p.row_weight[xr] : 1.0f;
+                    wgt = (p.row_weight ? p.row_weight[xr] : 1.0f) * Y_SCALE;
                 }
                 warp_row0 = un.tile.row_start + q * 32;
                 warp_live = warp_row0 < p.T;
@@ -784,6 +702,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     uint32_t yv[32];
                     tmem_ld_32x32b_x32(t_lane + ycol + c, yv);
                     tmem_ld_wait(yv);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) yv[e] = __float_as_uint(__uint_as_float(yv[e]) * Y_SCALE);
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
                         const int bx = box0 + e / C::Y_COLS, j = (e % C::Y_COLS) / 4;
