@@ -580,12 +580,61 @@ __global__ void __launch_bounds__(kDecThreads, 1) ffn_down_kernel(MatvecArgs a) 
             pend |= 1u << b;
         }
     }
-    __syncthreads();
-
-    // a row's work items are its (slot p, half-block q) pairs; lanes take
-    // items lane, lane + 32, ... and the warp sums them
+    // a row's work items are its (slot p, half-block q) pairs
     const int Lr2 = 2 * G.nbI;
     const int items = P * Lr2;
+    const int nrows = n1 - n0;
+    // Every row of the block was asked for above when they fit the warps'
+    // slots together: then each thread keeps one h half-block in registers
+    // and runs it against several rows, so that the block reads h from
+    // shared memory once instead of once per row; the warps' row sums are
+    // added into y (zeroed here unless the call accumulates).
+    const bool resident = row_bytes && nrows <= kDecWarps * depth;
+    if (resident && !a.accumulate)
+        for (int t = threadIdx.x; t < nrows; t += kDecThreads) a.y[n0 + t] = 0.0f;
+    __syncthreads();
+    if (resident) {
+        const int WI = (items + 31) / 32;                   // warps covering the items once
+        const int groups = WI <= kDecWarps ? kDecWarps / WI : 1;
+        const int wi = WI <= kDecWarps ? warp % WI : warp;
+        const int j = WI <= kDecWarps ? warp / WI : 0;      // this warp's rows: j, j + groups, ...
+        const int stride = WI <= kDecWarps ? WI * 32 : kDecWarps * 32;
+        if (j >= groups) return;
+        for (int base = wi * 32; base < items; base += stride) {
+            const int it = base + lane;
+            const int p = it / Lr2, q = it - p * Lr2;
+            const int e = it < items ? (moe ? a.ids[p] : 0) : -1;
+            const bool iv = e >= 0 && e < a.E;
+            uint4 xv[16];
+            float xs = 0.0f, xsum[4] = {0.f, 0.f, 0.f, 0.f};
+            if (iv) load_half(V, it, xv, xs, xsum);
+            const float w = iv && moe ? (a.down_scale ? a.wts[p] * a.down_scale[e] : a.wts[p]) : 1.0f;
+            for (int k = j; k < nrows; k += groups) {
+                // row n0 + k went to slot k / kDecWarps of warp k % kDecWarps
+                const int ow = k % kDecWarps, ob = k / kDecWarps;
+                if (!mbar_wait(&wbars[2 * ow + ob], 0, nullptr, a.err)) return;
+                float v = 0.0f;
+                if (iv) {
+                    const uint8_t *blk = slots + (size_t)(ow * depth + ob) * slot_bytes + (size_t)p * G.rbI +
+                                         (size_t)(q >> 1) * kBlockBytes;
+                    const uint4 hd = *reinterpret_cast<const uint4 *>(blk);
+                    uint4 cq[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) cq[i] = *reinterpret_cast<const uint4 *>(blk + 16 + 64 * (q & 1) + 16 * i);
+                    int ai[4];
+                    half_block_isums(cq, xv, ai);
+                    v = w * half_block_scale(hd, q & 1, ai, xs, xsum);
+                }
+#pragma unroll
+                for (int o2 = 16; o2 > 0; o2 >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o2);
+                if (lane == 0) atomicAdd(a.y + n0 + k, v);
+            }
+        }
+        return;
+    }
+
+    // otherwise rows stream through the warps' slots: lanes take items lane,
+    // lane + 32, ... of a row and the warp sums them
     int b = 0;
     for (int n = first; n < n1; n += kDecWarps, b = depth == 2 ? b ^ 1 : 0) {
         const bool have = (pend >> b) & 1;
