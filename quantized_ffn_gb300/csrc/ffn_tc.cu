@@ -85,9 +85,8 @@ __device__ __forceinline__ uint32_t ybuf_col(int b) {
 // needs one warp per sub-partition, because a warp reads only the TMEM lane
 // quadrant w % 4: warps 0-3.  The unpackers (warps 8-19, three groups of one
 // warp per sub-partition) spread the arithmetic evenly over the four
-// sub-partitions.  The MMA issuer walks its program as a whole warp with
-// warp-uniform control flow and descriptors, so its tcgen05.mma issue stays
-// short even next to arithmetic-heavy warps.
+// sub-partitions.  One lane of the MMA warp walks its program and issues the
+// MMAs, without per-instruction divergence.
 //
 // Groups and B stages: group k takes the tasks with index k modulo
 // UNPACK_GROUPS, and the waits on a stage's "empty" barrier test a phase
@@ -446,25 +445,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (role == ROLE_MMA) {
         // ---------------- MMA issuer (the pair's leader only) ----------------
-        // The whole warp walks the program (its control flow and descriptors
-        // stay warp-uniform, which keeps the issue of each tcgen05.mma short);
-        // one elected lane issues the MMAs and commits.
+        // One elected lane walks the program and issues every MMA and commit
+        // (no divergence inside the loop); the rest of the warp waits for the
+        // final drain.
         if (leader) {
-            const bool issuer = elect_one();
+          const bool issuer = elect_one();
+          if (issuer) {
             uint32_t ai = 0, aph = 0, bi = 0, bph = 0, jg = 0;
             uint32_t yph = 0;    // bit b: parity of the uses of down buffer b so far
             int yb = 0;
             bool ok = true;
             auto commit = [&](uint64_t *bar) {
-                if (issuer) {
-                    if (PAIR) tc_commit_pair(bar); else tc_commit(bar);
-                }
+                if (PAIR) tc_commit_pair(bar); else tc_commit(bar);
             };
             auto mma = [&](uint32_t d, uint64_t da, uint64_t db, uint32_t idesc, bool acc) {
-                if (issuer) {
-                    if (PAIR) tc_mma_bf16_pair(d, da, db, idesc, acc);
-                    else tc_mma_bf16(d, da, db, idesc, acc);
-                }
+                if (PAIR) tc_mma_bf16_pair(d, da, db, idesc, acc);
+                else tc_mma_bf16(d, da, db, idesc, acc);
             };
             // Descriptors advance by the stage strides (start address field in
             // 16-byte units); every operand lies below 256 KB.
@@ -523,8 +519,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             // every MMA issued here completes before TMEM is released
             commit(drain);
-            __syncwarp();
-            mbar_wait(drain, 0, nullptr, p.err, kWaitBudgetCycles / 8);
+          }
+          __syncwarp();
+          mbar_wait(drain, 0, nullptr, p.err, kWaitBudgetCycles / 8);
         }
     } else if (role == ROLE_UNPACK) {
         // ------------- weight unpackers (three groups of 4 warps) -------------
