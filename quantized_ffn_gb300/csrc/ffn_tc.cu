@@ -158,6 +158,7 @@ struct Cfg {
     static_assert(!PAIR || UNPACK_GROUPS <= NB, "parity waits on B stages stay unambiguous");
     static_assert(PAIR || UNPACK_GROUPS <= 2 * NB, "parity waits on B stages stay unambiguous");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget of one block");
+    static_assert(NA == NB, "x stage i goes with unpacked-weight stage i");
 };
 
 // Tensor maps: x tiles, y tiles, and the packed weights viewed as byte
@@ -409,38 +410,45 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (role == ROLE_XPROD) {
         // ------------- TMA producer: x tiles of the gate/up steps -------------
+        // x stage i goes with unpacked-weight stage i: the step that uses
+        // both releases both with one commit (b_empty), so this producer
+        // walks every step of the program on the B ring's index and loads x
+        // for the gate/up steps only.
         if (lane == 0) {
-            uint32_t ai = 0, aph = 0, a_issued = 0;
+            uint32_t bi = 0, bph = 0, apb = 0, issued = 0;
             Prog pg;
             pg.start(m_units, ks_gu, NY, YS);
             int cur = -1;
             Unit un{};
             for (; !pg.done; pg.next()) {
-                if (!pg.gu) continue;
-                if (pg.unit() != cur) { cur = pg.unit(); un = unit_of(cur); }
-                const int ks = pg.ks;
-                if (!mbar_wait(&a_empty[ai], aph ^ 1, abort_flag, p.err)) break;
-                void *dst = smem + C::OFF_A + ai * A_BYTES;
-                if (PAIR) {
-                    // both CTAs' tiles complete on the leader's barrier
-                    if (leader) mbar_arrive_expect_tx(&a_full[ai], 2 * A_BYTES);
-                    tma_load_2d_pair(dst, &maps.x, mapa_shared(smem_u32(&a_full[ai]), 0), ks * BK,
-                                     un.tile.row_start);
-                } else {
-                    mbar_arrive_expect_tx(&a_full[ai], A_BYTES);
-                    tma_load_2d(dst, &maps.x, &a_full[ai], ks * BK, un.tile.row_start);
+                // every step's stage is waited for, so that each wait tests
+                // the phase right after the one the previous wait saw (parity
+                // waits are unambiguous only then)
+                if (!mbar_wait(&b_empty[bi], bph ^ 1, abort_flag, p.err)) break;
+                if (pg.gu) {
+                    if (pg.unit() != cur) { cur = pg.unit(); un = unit_of(cur); }
+                    const int ks = pg.ks;
+                    void *dst = smem + C::OFF_A + bi * A_BYTES;
+                    if (PAIR) {
+                        // both CTAs' tiles complete on the leader's barrier
+                        if (leader) mbar_arrive_expect_tx(&a_full[bi], 2 * A_BYTES);
+                        tma_load_2d_pair(dst, &maps.x, mapa_shared(smem_u32(&a_full[bi]), 0), ks * BK,
+                                         un.tile.row_start);
+                    } else {
+                        mbar_arrive_expect_tx(&a_full[bi], A_BYTES);
+                        tma_load_2d(dst, &maps.x, &a_full[bi], ks * BK, un.tile.row_start);
+                    }
+                    apb ^= 1u << bi;
+                    issued |= 1u << bi;
                 }
-                ++a_issued;
-                if (++ai == C::NA) { ai = 0; aph ^= 1; }
+                if (++bi == C::NB) { bi = 0; bph ^= 1; }
             }
             // In a pair the x tiles complete on the leader's barriers, which the
             // leader's issuer has waited for before its final MMAs.
             if (!PAIR || leader) {
-                for (uint32_t i = 0; i < (uint32_t)C::NA && i < a_issued; ++i) {
-                    if (ai == 0) { ai = C::NA; aph ^= 1; }
-                    --ai;
-                    mbar_wait(&a_full[ai], aph, nullptr, p.err, kWaitBudgetCycles / 8);
-                }
+                for (int i = 0; i < C::NA; ++i)
+                    if ((issued >> i) & 1)
+                        mbar_wait(&a_full[i], ((apb >> i) & 1) ^ 1, nullptr, p.err, kWaitBudgetCycles / 8);
             }
         }
     } else if (role == ROLE_MMA) {
@@ -451,7 +459,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (leader) {
           const bool issuer = elect_one();
           if (issuer) {
-            uint32_t ai = 0, aph = 0, bi = 0, bph = 0, jg = 0;
+            uint32_t bi = 0, bph = 0, jg = 0;
+            uint32_t apb = 0;    // bit i: parity of the uses of x stage i so far
             uint32_t yph = 0;    // bit b: parity of the uses of down buffer b so far
             int yb = 0;
             bool ok = true;
@@ -468,7 +477,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t dh0 = smem_desc_k_sw128(s_h);
             constexpr uint64_t A_STEP = A_BYTES >> 4, B_STEP = C::B_BYTES >> 4;
             constexpr uint64_t HT_STEP = HT_BYTES >> 4, YH_STEP = (C::ROWS_Y * 128) >> 4;
-            uint64_t da = da0, db = db0;
+            uint64_t db = db0;
             const uint32_t d_gu = tmem_base + COL_GU;
             uint32_t d_y = tmem_base + COL_Y;
             Prog pg;
@@ -479,15 +488,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                         if (!mbar_wait(g_empty, (jg & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
                         tc_fence_after();
                     }
-                    if (!mbar_wait(&a_full[ai], aph, abort_flag, p.err) ||
+                    if (!mbar_wait(&a_full[bi], (apb >> bi) & 1, abort_flag, p.err) ||
                         !mbar_wait(&b_full[bi], bph, abort_flag, p.err)) { ok = false; break; }
                     tc_fence_after();
+                    const uint64_t da = da0 + bi * A_STEP;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
                         mma(d_gu, da + 2 * kk, db + 2 * kk, C::IDESC_GU, (pg.ks | kk) != 0);
-                    commit(&a_empty[ai]);
+                    // one commit frees the step's x and weight stages
                     commit(&b_empty[bi]);
-                    if (++ai == C::NA) { ai = 0; aph ^= 1; da = da0; } else { da += A_STEP; }
+                    apb ^= 1u << bi;
                     if (++bi == C::NB) { bi = 0; bph ^= 1; db = db0; } else { db += B_STEP; }
                     if (pg.gu_last()) { commit(g_full); ++jg; }
                 } else {
