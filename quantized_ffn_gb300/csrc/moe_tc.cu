@@ -431,13 +431,13 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
         }
     } else if (role == ROLE_MMA) {
         // ---------------- MMA issuer ----------------
+        // One elected lane walks the program and issues every MMA and commit.
         const bool issuer = elect_one();
+      if (issuer) {
         uint32_t ai = 0, aph = 0, xi = 0, xph = 0;
         uint32_t gb = 0, gph = 0, yb = 0, yph = 0;   // buffer index, per-buffer parity bits
         bool ok = true;
-        auto commit = [&](uint64_t *bar) {
-            if (issuer) tc_commit(bar);
-        };
+        auto commit = [&](uint64_t *bar) { tc_commit(bar); };
         const uint64_t dx0 = smem_desc_k_sw128(s_x);
         const uint64_t dh0 = smem_desc_k_sw128(s_h);
         for (int k = 0; k < m_units && ok; ++k) {
@@ -452,16 +452,14 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
                     tc_fence_after();
                     const uint32_t ta = tmem_base + COL_A + ai * A_COLS;
                     const uint64_t dx = dx0 + (uint64_t)((xi * X_BYTES) >> 4);
-                    if (issuer) {
 #pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk)
-                            tc_mma_f16_ta(tmem_base + COL_G + gb * NG, ta + 8 * kk, dx + 2 * kk, IDESC,
-                                          (ks | kk) != 0);
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        tc_mma_f16_ta(tmem_base + COL_G + gb * NG, ta + 8 * kk, dx + 2 * kk, IDESC,
+                                      (ks | kk) != 0);
 #pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk)
-                            tc_mma_f16_ta(tmem_base + COL_U + gb * NG, ta + 32 + 8 * kk, dx + 2 * kk, IDESC,
-                                          (ks | kk) != 0);
-                    }
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        tc_mma_f16_ta(tmem_base + COL_U + gb * NG, ta + 32 + 8 * kk, dx + 2 * kk, IDESC,
+                                      (ks | kk) != 0);
                     commit(&a_empty[ai]);
                     commit(&x_empty[xi]);
                     if (++ai == NA) { ai = 0; aph ^= 1; }
@@ -484,12 +482,10 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
                     tc_fence_after();
                     const uint32_t ta = tmem_base + COL_A + ai * A_COLS;
                     const uint64_t dh = dh0 + (uint64_t)((ks * H_TILE) >> 4);
-                    if (issuer) {
 #pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk)
-                            tc_mma_f16_ta(tmem_base + COL_Y + yb * NG, ta + 8 * kk, dh + 2 * kk, IDESC,
-                                          (ks | kk) != 0);
-                    }
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        tc_mma_f16_ta(tmem_base + COL_Y + yb * NG, ta + 8 * kk, dh + 2 * kk, IDESC,
+                                      (ks | kk) != 0);
                     commit(&a_empty[ai]);
                     if (++ai == NA) { ai = 0; aph ^= 1; }
                     if (ks == un.ks_y - 1) {
@@ -502,6 +498,7 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
         }
         // every MMA issued here completes before TMEM is released
         commit(drain);
+      }
         __syncwarp();
         mbar_wait(drain, 0, nullptr, p.err, kWaitBudgetCycles / 8);
     } else if (role == ROLE_UNPACK) {
