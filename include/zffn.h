@@ -98,11 +98,12 @@ zffn_status zffn_q4k_quantize(const float *w, void *blocks, int64_t rows, int64_
  * the gate/up product takes x and the unpacked W_gate, W_up in fp16 (x
  * converted once per call; each sub-block's scale d*sc and offset dmin*m
  * rounded to fp16, then one fused multiply-add per weight); the down product
- * takes the unpacked W_down the same way and the SwiGLU intermediate as
- * fp16(h * 2^-8) (its result scaled back by 2^8).  fp16 values saturate at
- * +-65504: |x| above that, a sub-block with d*sc > 128 or dmin*m > 65504, or
- * |h| above 1.7e7, is clamped on that path (far outside quantised weights and
- * normalised activations).
+ * takes 16 times the unpacked W_down (formed the same way) and the SwiGLU
+ * intermediate as fp16(h / 16), so that its result needs no rescaling.  fp16
+ * values saturate at +-65504: |x| above that, a W_gate or W_up sub-block with
+ * d*sc > 128 or dmin*m > 65504, a W_down sub-block with d*sc > 8 or
+ * dmin*m > 4094, or |h| above 1.05e6, is clamped on that path (far outside
+ * quantised weights and normalised activations).
  * Uses library workspace (see zffn_reserve): the single-token path's
  * intermediate strip, and the prefill path's fp16 copy of x (T*H*2 bytes).
  * Errors: INVALID_ARG (NULL, misaligned, bad sizes), CUDA, NO_WORKSPACE. */

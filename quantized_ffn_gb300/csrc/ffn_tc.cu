@@ -3,10 +3,10 @@
 // What it computes, per (token tile, intermediate chunk) work unit:
 //   for each 128-row slice s of the chunk:
 //       [G | U] = X_tile . [W_gate rows ; W_up rows]^T        (tcgen05, TMEM)
-//       h[:, s] = fp16( silu(G) * U * 2^-8 )                    (epilogue)
+//       h[:, s] = fp16( silu(G) * U / 16 )                      (epilogue)
 //   for each 128-column slice n of the output:
-//       Y = h . W_down[n rows, chunk cols]^T                   (tcgen05, TMEM)
-//       y[token, n cols] += 2^8 * Y                             (fp32 reductions in L2)
+//       Y = h . (16 W_down[n rows, chunk cols])^T              (tcgen05, TMEM)
+//       y[token, n cols] += Y                                   (fp32 reductions in L2)
 // This is the producer/consumer interleave along the intermediate dimension
 // ("Fused SwiGLU MLP: ZINC RDNA4 Down-Projection Bandwidth", section "Why
 // this fusion is harder than the last one"): a block of the intermediate is
@@ -60,17 +60,52 @@ constexpr int A_BYTES = BM * BK * 2;     // 16 KB x tile per CTA
 constexpr int HT_BYTES = BM * BK * 2;    // one 64-column slice of h: 16 KB
 constexpr uint32_t COL_GU = 0, COL_Y = 256, COL_STASH = 384;   // TMEM columns
 // Both products take fp16 operands: x (converted once per call), the weights
-// (unpacked with the fp8 -> fp16 converter) and the intermediate, held as
-// h * 2^-8 so that its fp16 range reaches 1.7e7 (values beyond saturate);
-// the down projection's result is scaled back by 2^8 when it is drained.
-constexpr float H_SCALE = 1.0f / 256.0f;
-constexpr float Y_SCALE = 256.0f;
+// (unpacked with the fp8 -> fp16 converter) and the intermediate.  The
+// intermediate is held as h / W_SCALE (fp16 range to 1.05e6) and W_down as
+// W_SCALE * w (sub-blocks up to d*sc = 8, dmin*m = 4094 in range; values
+// beyond saturate), so the down product needs no rescaling: both factors are
+// powers of two and change no significand.
+constexpr float W_SCALE = 16.0f;
+constexpr float H_SCALE = 1.0f / W_SCALE;
 // Two fp32 values -> one fp16 pair (lo in the low half), nearest, clamped to
 // the largest finite fp16.
 __device__ __forceinline__ uint32_t pack_f16x2_satfinite(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+// Unpack the 8 code words of one Q4_K weight row and K step (64 weights of
+// sub-blocks 2g and 2g+1) into its swizzled fp16 row (128-byte swizzle),
+// times ws (1, or W_SCALE for W_down).  Each code pair becomes (q0, q1) *
+// 2^-9 exactly (codes_to_f16x2), and one fused fp16 multiply-add per pair
+// gives  w = (q * 2^-9) * fp16(512 ws d sc) - fp16(ws dmin m),  rounded once
+// to fp16: the sub-block's scale and offset are exact in fp32 before their
+// rounding to fp16 (ws is a power of two); values beyond the fp16 range
+// saturate at +-65504.  Chunks are stored as soon as they are formed.
+__device__ __forceinline__ void unpack_row_to_smem_f16(uint4 hd, const uint32_t (&w)[8], int g, float ws,
+                                                       uint32_t row_addr, int row) {
+    const float d = ws * half_bits_to_float(hd.x), dmin = ws * half_bits_to_float(hd.x >> 16);
+    int sc0, m0, sc1, m1;
+    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g, sc0, m0);
+    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g + 1, sc1, m1);
+    const uint32_t a0 = f16x2_splat_satfinite(512.0f * (d * (float)sc0));
+    const uint32_t b0 = f16x2_splat_satfinite(-(dmin * (float)m0));
+    const uint32_t a1 = f16x2_splat_satfinite(512.0f * (d * (float)sc1));
+    const uint32_t b1 = f16x2_splat_satfinite(-(dmin * (float)m1));
+    constexpr uint32_t NIB = 0x0F0F0F0Fu;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        // words 2c, 2c+1: low nibbles are weights 8c..8c+7 of sub-block 2g,
+        // high nibbles weights 32+8c..32+8c+7 of sub-block 2g+1
+        const uint32_t l0 = w[2 * c] & NIB, l1 = w[2 * c + 1] & NIB;
+        const uint32_t h0 = (w[2 * c] >> 4) & NIB, h1 = (w[2 * c + 1] >> 4) & NIB;
+        st_shared_v4(row_addr + (((uint32_t)(c ^ (row & 7))) << 4),
+                     fma_f16x2(codes_to_f16x2(l0), a0, b0), fma_f16x2(codes_to_f16x2(l0 >> 16), a0, b0),
+                     fma_f16x2(codes_to_f16x2(l1), a0, b0), fma_f16x2(codes_to_f16x2(l1 >> 16), a0, b0));
+        st_shared_v4(row_addr + (((uint32_t)((c + 4) ^ (row & 7))) << 4),
+                     fma_f16x2(codes_to_f16x2(h0), a1, b1), fma_f16x2(codes_to_f16x2(h0 >> 16), a1, b1),
+                     fma_f16x2(codes_to_f16x2(h1), a1, b1), fma_f16x2(codes_to_f16x2(h1 >> 16), a1, b1));
+    }
 }
 // Down-projection accumulators.  While a block has a next unit, its down jobs
 // use COL_Y only (the gate/up accumulator and the h stash are busy with the
@@ -588,7 +623,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!mbar_wait(&b_empty[bi], bph ^ 1, abort_flag, p.err)) { ok = false; break; }
                 const uint32_t rb = s_b + bi * C::B_BYTES + half * (C::ROWS_Y * 128) + sw128_row(row);
                 const uint32_t w8[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                unpack_row_to_smem_f16(hd, w8, g, rb, row);
+                unpack_row_to_smem_f16(hd, w8, g, pg.gu ? 1.0f : W_SCALE, rb, row);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) arrive_leader(&b_full[bi]);
@@ -674,11 +709,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (pg.blk != cur) { cur = pg.blk; un = unit_of(cur); }
                 valid = row < un.tile.row_count;
                 token = 0;
-                wgt = Y_SCALE;
+                wgt = 1.0f;
                 if (valid) {
                     const int xr = un.tile.row_start + row;
                     token = p.row_token ? p.row_token[xr] : xr;
-                    wgt = (p.row_weight ? p.row_weight[xr] : 1.0f) * Y_SCALE;
+                    wgt = p.row_weight ? p.row_weight[xr] : 1.0f;
                 }
                 warp_row0 = un.tile.row_start + q * 32;
                 warp_live = warp_row0 < p.T;
@@ -709,8 +744,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                     uint32_t yv[32];
                     tmem_ld_32x32b_x32(t_lane + ycol + c, yv);
                     tmem_ld_wait(yv);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) yv[e] = __float_as_uint(__uint_as_float(yv[e]) * Y_SCALE);
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
                         const int bx = box0 + e / C::Y_COLS, j = (e % C::Y_COLS) / 4;
