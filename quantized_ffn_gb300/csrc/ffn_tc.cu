@@ -108,13 +108,22 @@ __device__ __forceinline__ void unpack_row_to_smem_f16(uint4 hd, const uint32_t 
     }
 }
 // Down-projection accumulators.  While a block has a next unit, its down jobs
-// use COL_Y only (the gate/up accumulator and the h stash are busy with the
-// next unit).  In a block's last unit both are free once its h is in shared
+// use COL_Y (the gate/up accumulator is busy with the next unit), the first
+// half of them alternating with the h stash (ybuf_of).  In a block's last unit
+// the stash and the gate/up accumulator are free once its h is in shared
 // memory, so its down jobs rotate over four 128-column buffers and the drain
 // of one overlaps the MMAs of the next three.
 constexpr int NYBUF = 4;
 __device__ __forceinline__ uint32_t ybuf_col(int b) {
     return b == 0 ? COL_Y : b == 1 ? COL_STASH : b == 2 ? COL_GU : COL_GU + 128;
+}
+// The buffer of down job n (of NY) of a unit.  In a block's last unit the
+// jobs rotate over all four.  Otherwise the stash is free from the moment the
+// unit's h has gone to shared memory until the next unit's first gate/up job
+// completes, which the program places after down job NY/2 - 1: jobs before
+// it alternate between COL_Y and the stash, later ones use COL_Y.
+__device__ __forceinline__ int ybuf_of(int n, int NY, bool last) {
+    return last ? n % NYBUF : (n < NY / 2 ? (n & 1) : 0);
 }
 // Warp roles.  Warp w is scheduled by sub-partition w % 4.  The epilogue
 // needs one warp per sub-partition, because a warp reads only the TMEM lane
@@ -540,7 +549,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         // the first down job of a unit reads its h: wait until
                         // the epilogues placed all of it in shared memory
                         if (pg.n == 0 && !mbar_wait(h_full, (uint32_t)pg.blk & 1, abort_flag, p.err)) { ok = false; break; }
-                        yb = pg.blk == m_units - 1 ? pg.n % NYBUF : 0;
+                        yb = ybuf_of(pg.n, NY, pg.blk == m_units - 1);
                         d_y = tmem_base + ybuf_col(yb);
                         if (!mbar_wait(&y_empty[yb], ((yph >> yb) & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
                         tc_fence_after();
@@ -720,7 +729,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (pg.ys != YS - 1) continue;
             // ---- down job n complete: Y tile -> y[token, n*128 ..]
-            const int yb = pg.blk == m_units - 1 ? pg.n % NYBUF : 0;
+            const int yb = ybuf_of(pg.n, NY, pg.blk == m_units - 1);
             const uint32_t ycol = ybuf_col(yb);
             if (!mbar_wait(&y_full[yb], (yph >> yb) & 1, abort_flag, p.err)) { ok = false; break; }
             tc_fence_after();
