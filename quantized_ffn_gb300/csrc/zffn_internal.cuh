@@ -324,15 +324,6 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
                  :
                  : "memory");
 }
-// Store 32 consecutive 32-bit TMEM columns of this warp's 32 lanes (one
-// register per column), and wait for this thread's TMEM stores.
-__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
-        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
 __device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
                  "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
@@ -368,25 +359,14 @@ __device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor: kind::f16, A = B = bf16, D = fp32, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-    return (1u << 4)                          // D format f32
-           | (1u << 7)                        // A format bf16
-           | (1u << 10)                       // B format bf16
-           | ((uint32_t)(N >> 3) << 17)       // N / 8
-           | ((uint32_t)(M >> 4) << 24);      // M / 16
-}
-// The same with A = B = fp16 (format code 0).
+// Instruction descriptor: kind::f16 with A = B = fp16 (format code 0),
+// D = fp32, both K-major.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
     return (1u << 4)                          // D format f32
            | ((uint32_t)(N >> 3) << 17)       // N / 8
            | ((uint32_t)(M >> 4) << 24);      // M / 16
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
 
 // Two 4-bit codes as fp16: the low 16 bits of `v` hold two bytes, each a code
 // 0..15.  Read as an e4m3 bit pattern, a byte 0000qqqq is q * 2^-9 exactly
@@ -428,13 +408,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
-__device__ __forceinline__ uint4 ld_global_nc_v4(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
 
 // ---------------------------------------------------------------------------
 // Q4_K -> fp16 operand tiles of the tensor-core kernels.
@@ -455,83 +428,8 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     return v;
 }
 
-// Unpack the 8 code words of one Q4_K weight row and K step (64 weights of
-// sub-blocks 2g and 2g+1) into its swizzled fp16 row (128-byte swizzle).  Each code pair becomes (q0, q1) * 2^-9
-// exactly (codes_to_f16x2), and one fused fp16 multiply-add per pair gives
-//     w = (q * 2^-9) * fp16(512 d sc) - fp16(dmin m),
-// rounded once to fp16 (11-bit significand): the sub-block's scale and offset
-// are rounded to fp16 first (relative error <= 2^-11 each), far below the
-// bf16 rounding the down projection's operands get.  d*sc*512 and dmin*m are
-// exact in fp32 before that rounding; values beyond the fp16 range saturate
-// at +-65504 (|d * sc| > 128 or |dmin * m| > 65504: far outside any
-// quantised weight).  Chunks are stored as soon as they are formed.
-__device__ __forceinline__ void unpack_row_to_smem_f16(uint4 hd, const uint32_t (&w)[8], int g,
-                                                       uint32_t row_addr, int row) {
-    const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
-    int sc0, m0, sc1, m1;
-    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g, sc0, m0);
-    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g + 1, sc1, m1);
-    const uint32_t a0 = f16x2_splat_satfinite(512.0f * (d * (float)sc0));
-    const uint32_t b0 = f16x2_splat_satfinite(-(dmin * (float)m0));
-    const uint32_t a1 = f16x2_splat_satfinite(512.0f * (d * (float)sc1));
-    const uint32_t b1 = f16x2_splat_satfinite(-(dmin * (float)m1));
-    constexpr uint32_t NIB = 0x0F0F0F0Fu;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        // words 2c, 2c+1: low nibbles are weights 8c..8c+7 of sub-block 2g,
-        // high nibbles weights 32+8c..32+8c+7 of sub-block 2g+1
-        const uint32_t l0 = w[2 * c] & NIB, l1 = w[2 * c + 1] & NIB;
-        const uint32_t h0 = (w[2 * c] >> 4) & NIB, h1 = (w[2 * c + 1] >> 4) & NIB;
-        st_shared_v4(row_addr + (((uint32_t)(c ^ (row & 7))) << 4),
-                     fma_f16x2(codes_to_f16x2(l0), a0, b0), fma_f16x2(codes_to_f16x2(l0 >> 16), a0, b0),
-                     fma_f16x2(codes_to_f16x2(l1), a0, b0), fma_f16x2(codes_to_f16x2(l1 >> 16), a0, b0));
-        st_shared_v4(row_addr + (((uint32_t)((c + 4) ^ (row & 7))) << 4),
-                     fma_f16x2(codes_to_f16x2(h0), a1, b1), fma_f16x2(codes_to_f16x2(h0 >> 16), a1, b1),
-                     fma_f16x2(codes_to_f16x2(h1), a1, b1), fma_f16x2(codes_to_f16x2(h1 >> 16), a1, b1));
-    }
-}
 
-// One sub-block (32 weights) of the same row and K step: hi = 0 takes the low
-// nibbles of the 8 code words (sub-block 2g: 16-byte chunks 0-3 of the row),
-// hi = 1 the high nibbles (sub-block 2g+1: chunks 4-7).
-__device__ __forceinline__ void unpack_half_row_to_smem_f16(uint4 hd, const uint32_t (&w)[8], int g,
-                                                            int hi, uint32_t row_addr, int row) {
-    const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
-    int sc, m;
-    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g + hi, sc, m);
-    const uint32_t a = f16x2_splat_satfinite(512.0f * (d * (float)sc));
-    const uint32_t b = f16x2_splat_satfinite(-(dmin * (float)m));
-    constexpr uint32_t NIB = 0x0F0F0F0Fu;
-    const int sh = 4 * hi;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const uint32_t v0 = (w[2 * c] >> sh) & NIB, v1 = (w[2 * c + 1] >> sh) & NIB;
-        st_shared_v4(row_addr + (((uint32_t)((c + 4 * hi) ^ (row & 7))) << 4),
-                     fma_f16x2(codes_to_f16x2(v0), a, b), fma_f16x2(codes_to_f16x2(v0 >> 16), a, b),
-                     fma_f16x2(codes_to_f16x2(v1), a, b), fma_f16x2(codes_to_f16x2(v1 >> 16), a, b));
-    }
-}
 
-// One sub-block (32 weights) of a Q4_K row and K step into registers: hi = 0
-// the low nibbles of the 8 code words (sub-block 2g), hi = 1 the high nibbles
-// (sub-block 2g+1).  out[j] holds weights 2j and 2j+1 of the sub-block as an
-// fp16 pair (low half first) -- the K-packed layout of an MMA operand row in
-// tensor memory.
-__device__ __forceinline__ void unpack_half_row_f16(uint4 hd, const uint32_t (&w)[8], int g, int hi,
-                                                    uint32_t (&out)[16]) {
-    const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
-    int sc, m;
-    q4k_scale_min(hd.y, hd.z, hd.w, 2 * g + hi, sc, m);
-    const uint32_t a = f16x2_splat_satfinite(512.0f * (d * (float)sc));
-    const uint32_t b = f16x2_splat_satfinite(-(dmin * (float)m));
-    const int sh = 4 * hi;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t v = (w[i] >> sh) & 0x0F0F0F0Fu;   // weights 4i .. 4i+3
-        out[2 * i] = fma_f16x2(codes_to_f16x2(v), a, b);
-        out[2 * i + 1] = fma_f16x2(codes_to_f16x2(v >> 16), a, b);
-    }
-}
 
 // Four code bytes (each a code 0..15) -> the fp16 weights of bytes 0-1 (o0) and
 // 2-3 (o1): w = (q * 2^-9) * a + b with a, b fp16 pairs (see codes_to_f16x2).
