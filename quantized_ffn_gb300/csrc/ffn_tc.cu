@@ -197,7 +197,7 @@ struct Cfg {
     static constexpr int EPI_ARRIVALS = PAIR ? 8 : 4;     // epilogue warps arriving per job
     static constexpr int B_ARRIVALS = (PAIR ? 2 : 1) * TASKS * UNPACK_GROUP_WARPS;
     static constexpr uint32_t IDESC_GU = idesc_f16_f32(PAIR ? 256 : 128, NJ_GU);   // fp16 x, W_gate, W_up
-    static constexpr uint32_t IDESC_Y = idesc_f16_f32(PAIR ? 256 : 128, NJ_Y);     // fp16 h * 2^-8, W_down
+    static constexpr uint32_t IDESC_Y = idesc_f16_f32(PAIR ? 256 : 128, NJ_Y);     // fp16 h / 16, 16 W_down
     static_assert(R_BYTES_Y <= R_BYTES, "down-step slice fits a weight stage");
     static_assert(!PAIR || UNPACK_GROUPS <= NB, "parity waits on B stages stay unambiguous");
     static_assert(PAIR || UNPACK_GROUPS <= 2 * NB, "parity waits on B stages stay unambiguous");
