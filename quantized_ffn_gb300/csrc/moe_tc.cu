@@ -591,7 +591,20 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
                     !mbar_wait(&a_empty[ai + 1], aph ^ 1, abort_flag, p.err)) { ok = false; break; }
                 tc_fence_after();
                 uint32_t sa[4], sb[4];                   // sub-blocks 2 (ks & 3) .. +3
-                q4k_f16_scales4(hd, 2 * (cur_ks & 3), sa, sb);
+                if (gu) {
+                    q4k_f16_scales4(hd, 2 * (cur_ks & 3), sa, sb);
+                } else {
+                    // down phase: only this task's nibble half of each K step,
+                    // sub-blocks 2 (ks & 3) + task and 2 (ks & 3) + 2 + task
+                    const float d = 512.0f * half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        int sc, m;
+                        q4k_scale_min(hd.y, hd.z, hd.w, 2 * (cur_ks & 3) + 2 * j + task, sc, m);
+                        sa[2 * j] = sa[2 * j + 1] = f16x2_splat_satfinite(d * (float)sc);
+                        sb[2 * j] = sb[2 * j + 1] = f16x2_splat_satfinite(-(dmin * (float)m));
+                    }
+                }
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {            // K step cur_ks + j, stage ai + j
                     const uint32_t w[8] = {c[2 * j].x, c[2 * j].y, c[2 * j].z, c[2 * j].w,
