@@ -53,6 +53,9 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
     int *tix = sm + 2 * a.E;             // [E]
     int *scratch = sm + 3 * a.E;         // [blockDim]
     const int P = a.T * a.k;
+    // the gather kernel may be scheduled now; it waits for this grid's
+    // completion before reading what this kernel writes
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     for (int e = threadIdx.x; e < a.E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
     for (int i = threadIdx.x; i < P; i += blockDim.x) {
@@ -102,6 +105,10 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const __nv_bfloat16 *__
                                                          __half *__restrict__ x_perm,
                                                          int rows_cap, int H, float4 *__restrict__ y4,
                                                          int64_t ny4, float *ytail, int nytail) {
+    // launched as a programmatic dependent of the routing kernel: wait for
+    // its row lists (and for any earlier work on y) before touching memory
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int n_rows = min(offsets[E], rows_cap);
     const int vec = H / 8;   // 16-byte vectors per row
     for (int r = blockIdx.x; r < n_rows; r += gridDim.x) {
@@ -156,11 +163,21 @@ cudaError_t launch_moe_route(const RouteArgs &a, cudaStream_t s) {
     int grid = P < device_info().num_sms * 8 ? P : device_info().num_sms * 8;
     if (grid < 1) grid = 1;
     const int64_t ny4 = a.y_zero ? a.ny / 4 : 0;
-    moe_gather_kernel<<<grid, 256, 0, s>>>(a.x, a.offsets, a.E, a.row_token, a.x_perm, P, a.H,
-                                           reinterpret_cast<float4 *>(a.y_zero), ny4,
-                                           a.y_zero ? a.y_zero + 4 * ny4 : nullptr,
-                                           a.y_zero ? (int)(a.ny - 4 * ny4) : 0);
-    return cudaGetLastError();
+    // a programmatic dependent of the routing kernel: its launch overlaps
+    // that kernel, and it waits for its completion itself
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, moe_gather_kernel, a.x, (const int *)a.offsets, a.E, (const int *)a.row_token,
+                              a.x_perm, P, a.H, reinterpret_cast<float4 *>(a.y_zero), ny4,
+                              a.y_zero ? a.y_zero + 4 * ny4 : (float *)nullptr,
+                              a.y_zero ? (int)(a.ny - 4 * ny4) : 0);
 }
 
 // ---------------------------------------------------------------------------

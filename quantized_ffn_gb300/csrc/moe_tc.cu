@@ -329,6 +329,11 @@ __global__ void __launch_bounds__(THREADS, 1) moe_group_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // This kernel is launched as a programmatic dependent of the kernel that
+    // writes its tile table and gathered rows: wait for that grid's
+    // completion before the first read of them.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int n_tiles = min(*p.n_tiles_dev, p.n_tiles_host);
     const int n_chunks = (p.I + IC_MAX - 1) / IC_MAX;
@@ -788,7 +793,20 @@ cudaError_t launch_moe_group(const TcArgs &a, int wd_fmt, cudaStream_t s) {
     if (grid > di.num_sms) grid = di.num_sms;
     if (grid < 1) return cudaSuccess;
     void *kargs[] = {&maps, &p};
-    return cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(mg::THREADS), kargs, (size_t)mg::SMEM_BYTES, s);
+    // a programmatic dependent of the kernel before it (the gather of the
+    // routed rows, or the tile table of a dense call): its launch overlaps
+    // that kernel's tail and it waits for its completion itself
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(mg::THREADS);
+    cfg.dynamicSmemBytes = (size_t)mg::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, kargs);
 }
 
 }  // namespace zffn
