@@ -454,11 +454,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (role == ROLE_XPROD) {
         // ------------- TMA producer: x tiles of the gate/up steps -------------
+        // (A dense call launches this kernel as a programmatic dependent of
+        // the x conversion: x and y are read only after that grid completes;
+        // the weight roles start at once.)
         // x stage i goes with unpacked-weight stage i: the step that uses
         // both releases both with one commit (b_empty), so this producer
         // walks every step of the program on the B ring's index and loads x
         // for the gate/up steps only.
         if (lane == 0) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             uint32_t bi = 0, bph = 0, apb = 0, issued = 0;
             Prog pg;
             pg.start(m_units, ks_gu, NY, YS);
@@ -642,6 +646,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (role == ROLE_EPI) {
         // ---------------- epilogue (4 warps) ----------------
+        // y (zero-filled by the x conversion of a dense call) is touched only
+        // after the grid before this one has completed
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         const int q = warp & 3;                      // TMEM lane quadrant of this warp
         const int row = q * 32 + lane;               // token row within the CTA's tile
         const uint32_t lane_bits = (uint32_t)(q * 32) << 16;
@@ -910,19 +917,24 @@ cudaError_t launch_ffn_tc(const TcArgs &a, cudaStream_t s) {
         p.n_tiles_host = (a.T + 255) / 256;
         const int64_t units = (int64_t)p.n_tiles_host * n_chunks;
         int64_t pairs = di.num_sms / 2;
+        // a programmatic dependent of the x conversion when the units fill
+        // every pair (measured: earlier start pays there, costs with idle pairs)
+        const bool early = units >= pairs;
         if (units < pairs) pairs = units;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(2 * pairs));
         cfg.blockDim = dim3(tc::THREADS);
         cfg.dynamicSmemBytes = (size_t)smem;
         cfg.stream = s;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = early ? 2 : 1;
         return cudaLaunchKernelEx(&cfg, tc::ffn_tc_kernel<true>, maps, p);
     }
     p.n_tiles_host = a.n_tiles_host;
@@ -930,8 +942,23 @@ cudaError_t launch_ffn_tc(const TcArgs &a, cudaStream_t s) {
     int grid = di.num_sms;
     if (units < grid) grid = (int)units;
     if (grid < 1) return cudaSuccess;
-    tc::ffn_tc_kernel<false><<<grid, tc::THREADS, smem, s>>>(maps, p);
-    return cudaGetLastError();
+    if (a.tiles || units < di.num_sms) {
+        // routed tiles: every role reads the tile table, so no early start;
+        // nor with idle SMs (as for pairs)
+        tc::ffn_tc_kernel<false><<<grid, tc::THREADS, smem, s>>>(maps, p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(tc::THREADS);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc::ffn_tc_kernel<false>, maps, p);
 }
 
 }  // namespace zffn

@@ -164,6 +164,9 @@ cudaError_t launch_q4k_quantize(const float *w, void *blocks, int64_t rows, int6
 __global__ void __launch_bounds__(256) x_to_f16_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ x16,
                                                        int64_t n8, float4 *__restrict__ y, int64_t ny4,
                                                        float *ytail, int nytail) {
+    // the block that consumes x16 and y may be scheduled now; it waits for
+    // this grid's completion before it reads them
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += stride) {
         const uint4 v = x[i];
