@@ -20,28 +20,44 @@ namespace zffn {
 constexpr int kRouteThreads = 1024;
 
 // Exclusive scan of v[0..n) in shared memory by one block; returns the total.
+// Each thread sums a contiguous range, the per-thread sums are scanned with
+// warp shuffles (within each warp, then across the warps' totals), and each
+// thread writes the exclusive prefixes of its range.
 __device__ int block_exclusive_scan(int *v, int n, int *scratch) {
     const int per = (n + blockDim.x - 1) / blockDim.x;
     const int lo = threadIdx.x * per, hi = min(n, lo + per);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = (blockDim.x + 31) >> 5;
     int sum = 0;
     for (int i = lo; i < hi; ++i) sum += v[i];
-    scratch[threadIdx.x] = sum;
-    __syncthreads();
-    // Hillis-Steele over the per-thread sums
-    for (int o = 1; o < (int)blockDim.x; o <<= 1) {
-        const int add = threadIdx.x >= (unsigned)o ? scratch[threadIdx.x - o] : 0;
-        __syncthreads();
-        scratch[threadIdx.x] += add;
-        __syncthreads();
+    // inclusive scan of the per-thread sums within the warp
+    int inc = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
     }
-    int run = scratch[threadIdx.x] - sum;   // exclusive prefix of this thread's range
+    if (lane == 31) scratch[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        // exclusive scan of the warp totals (at most 32 warps)
+        const int wt = lane < nwarps ? scratch[lane] : 0;
+        int winc = wt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, winc, o);
+            if (lane >= o) winc += t;
+        }
+        scratch[lane] = winc - wt;                  // exclusive prefix of warp `lane`
+        if (lane == 31) scratch[32] = winc;         // the total
+    }
+    __syncthreads();
+    int run = scratch[warp] + inc - sum;            // exclusive prefix of this thread's range
     for (int i = lo; i < hi; ++i) {
         const int c = v[i];
         v[i] = run;
         run += c;
     }
-    __syncthreads();
-    const int total = scratch[blockDim.x - 1];
+    const int total = scratch[32];
     __syncthreads();
     return total;
 }
