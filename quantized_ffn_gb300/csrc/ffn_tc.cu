@@ -454,9 +454,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (role == ROLE_XPROD) {
         // ------------- TMA producer: x tiles of the gate/up steps -------------
-        // (A dense call launches this kernel as a programmatic dependent of
-        // the x conversion: x and y are read only after that grid completes;
-        // the weight roles start at once.)
+        // (A dense call whose units fill every pair launches this kernel as
+        // a programmatic dependent of the x conversion: x and y are read only
+        // after that grid completes, the weight roles start at once.)
         // x stage i goes with unpacked-weight stage i: the step that uses
         // both releases both with one commit (b_empty), so this producer
         // walks every step of the program on the B ring's index and loads x
