@@ -144,3 +144,26 @@ def test_full_layer_decode_tokens():
         assert zffn.get_device_error() == zffn.OK
         ref = orc.swiglu_ffn(x, layer["Wg"], layer["Wu"], layer["Wd"], 1, layer["H"], layer["I"])
         assert_close(y, ref, f"decode token {r}")
+
+
+# ---- calls chained on one stream ----------------------------------------------
+
+def test_chained_calls_on_one_stream_when_the_units_fill_the_gpu():
+    # 2 token tiles x 38 intermediate chunks = 76 units: one per CTA pair, so
+    # the prefill kernel starts while the x conversion before it runs.  A
+    # plain call, then two residual calls into the same y, back to back on one
+    # stream (nothing synchronises the host in between): y = 3 * block(x).
+    H, I, T = 256, 9728, 512
+    rng = np.random.default_rng(910)
+    Wg = synth.random_q4k_blocks(rng, I, H, 1e-2)
+    Wu = synth.random_q4k_blocks(rng, I, H, 1e-2)
+    Wd = synth.random_q4k_blocks(rng, H, I, 1e-2)
+    x = synth.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    xd, Wgd, Wud, Wdd = x_dev(x), dev(Wg), dev(Wu), dev(Wd)
+    y = zffn.swiglu_q4k(xd, Wgd, Wud, Wdd, I)
+    zffn.swiglu_q4k(xd, Wgd, Wud, Wdd, I, y=y, residual=True)
+    zffn.swiglu_q4k(xd, Wgd, Wud, Wdd, I, y=y, residual=True)
+    assert zffn.get_device_error() == zffn.OK
+    rows = [0, 1, 127, 128, 255, 256, 383, 384, 511]
+    ref = orc.swiglu_ffn(x[rows].copy(), Wg, Wu, Wd, len(rows), H, I)
+    assert_close(y[rows], 3.0 * ref, "three chained calls")

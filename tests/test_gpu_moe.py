@@ -184,3 +184,20 @@ def test_both_routed_kernels_full_config_256_tokens(kernel):
     ref = orc.moe_swiglu_ffn(m["x"][rows].copy(), m["ids"][rows].copy(), m["w"][rows].copy(),
                              m["Wg"], m["Wu"], m["Wd"], len(rows), m["H"], m["I"], m["E"], m["k"])
     assert_close(y[rows], ref, f"moe T=256 kernel {kernel}")
+
+
+def test_chained_routed_calls_on_one_stream():
+    # routing, gather and the grouped kernel of one call are chained by
+    # programmatic dependent launch; a plain call and two residual calls into
+    # the same y, back to back on one stream, give 3 times the block
+    E, H, I, k, T = 16, 512, 768, 4, 96
+    Wg, Wu, Wd = experts(930, E, H, I)
+    ids, w = routing(931, T, E, k)
+    x = synth.f32_to_bf16_bits(np.random.default_rng(932).standard_normal((T, H)).astype(np.float32))
+    args = (x_dev(x), dev(ids), dev(w), dev(Wg), dev(Wu), dev(Wd), I, E)
+    y = zffn.moe_swiglu_q4k(*args)
+    zffn.moe_swiglu_q4k(*args, y=y, residual=True)
+    zffn.moe_swiglu_q4k(*args, y=y, residual=True)
+    assert zffn.get_device_error() == zffn.OK
+    ref = orc.moe_swiglu_ffn(x, ids, w, Wg, Wu, Wd, T, H, I, E, k)
+    assert_close(y, 3.0 * ref, "three chained routed calls")
