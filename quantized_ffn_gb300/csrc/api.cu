@@ -29,6 +29,8 @@ int g_matvec_max_t = 1;
 int g_moe_kernel = 0;   // ZFFN_OPT_MOE_KERNEL
 int g_token_kernel = 0; // ZFFN_OPT_TOKEN_KERNEL
 
+thread_local const char *t_last_error = "no error";   // zffn_last_error()
+
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -72,7 +74,10 @@ int current_device() {
 // Make sure the current device's workspace holds at least `bytes`.
 zffn_status ensure_workspace(size_t bytes, Workspace **out) {
     const int dev = current_device();
-    if (dev < 0 || dev >= kMaxDevices) return ZFFN_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) {
+        t_last_error = "no usable CUDA device";
+        return ZFFN_ERR_CUDA;
+    }
     std::lock_guard<std::mutex> lk(g_mu);
     Workspace &w = g_ws[dev];
     if (w.bytes < bytes) {
@@ -102,8 +107,6 @@ zffn_status ensure_workspace(size_t bytes, Workspace **out) {
 }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
-
-thread_local const char *t_last_error = "no error";
 
 // A failed host-side check: record why (zffn_last_error) and return INVALID_ARG.
 zffn_status invalid(const char *why) {
@@ -161,19 +164,33 @@ cudaError_t ensure_dynamic_smem(const void *fn, size_t bytes) {
     return cudaSuccess;
 }
 
+namespace {
+// No usable device: record why for zffn_last_error and hand back the empty
+// record (device -1), which every entry turns into ZFFN_ERR_CUDA.
+const DeviceInfo &no_device(cudaError_t e) {
+    static const DeviceInfo none;
+    t_last_error = e == cudaSuccess ? "device index beyond the library's device table"
+                                    : cudaGetErrorString(e);
+    cudaGetLastError();
+    return none;
+}
+}  // namespace
+
 const DeviceInfo &device_info() {
-    const int dev = current_device();
-    static DeviceInfo none;
-    if (dev < 0 || dev >= kMaxDevices) return none;
+    int dev = -1;
+    const cudaError_t ge = cudaGetDevice(&dev);
+    if (ge != cudaSuccess || dev < 0 || dev >= kMaxDevices) return no_device(ge);
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceInfo &di = g_info[dev];
     if (di.device != dev) {
         cudaDeviceProp prop;
-        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return none;
+        cudaError_t e = cudaGetDeviceProperties(&prop, dev);
+        if (e != cudaSuccess) return no_device(e);
         di.num_sms = prop.multiProcessorCount;
         di.max_smem_optin = (int)prop.sharedMemPerBlockOptin;
         void *addr = nullptr;
-        if (cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess) return none;
+        e = cudaGetSymbolAddress(&addr, g_device_error);
+        if (e != cudaSuccess) return no_device(e);
         di.err_word = static_cast<int *>(addr);
         di.device = dev;
     }

@@ -60,8 +60,9 @@ zffn_status zffn_swiglu_q4k_token_static(const void *x, const void *Wg, const vo
         return ZFFN_ERR_INVALID_ARG;
     }
     const DeviceInfo &di = device_info();
-    if (di.device < 0 || di.device >= 64) {
-        set_last_error("no usable CUDA device");
+    if (di.device < 0) return ZFFN_ERR_CUDA;   // device_info recorded why
+    if (di.device >= 64) {                     // g_static_ptr's size
+        set_last_error("device index beyond the static scratch table");
         return ZFFN_ERR_CUDA;
     }
     if (matvec_smem_bytes(1, H, I, 1) > (size_t)di.max_smem_optin) {

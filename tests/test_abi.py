@@ -236,3 +236,17 @@ def test_rejections_record_the_failed_check(lib):
 
 def test_workspace_query_is_zero_before_any_call(lib):
     assert zffn.workspace_bytes() == 0
+
+
+def test_no_device_failure_records_its_reason(lib):
+    # well-formed arguments on a host without a GPU: the device lookup fails,
+    # the call returns ZFFN_ERR_CUDA and zffn_last_error gives the runtime's text
+    if torch.cuda.is_available() or zffn.single_token_launches(2048, 768, 128, 8) != -1:
+        pytest.skip("a device is present: the call would launch on the fake pointers")
+    lib.zffn_swiglu_q4k(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 200, 256, None)
+    assert b"H must be" in lib.zffn_last_error()
+    assert lib.zffn_q4k_dequant(FAKE, FAKE, 1, 256, None) == zffn.ERR_CUDA
+    msg = lib.zffn_last_error()
+    assert msg and msg != b"no error" and b"H must be" not in msg
+    assert lib.zffn_swiglu_q4k_token_static(FAKE, FAKE, FAKE, FAKE, FAKE, 256, 256, None) == zffn.ERR_CUDA
+    assert lib.zffn_last_error() == msg
