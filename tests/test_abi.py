@@ -235,7 +235,14 @@ def test_rejections_record_the_failed_check(lib):
 
 
 def test_workspace_query_is_zero_before_any_call(lib):
-    assert zffn.workspace_bytes() == 0
+    # in a fresh process, so that no earlier call of this one counts
+    import subprocess
+    import sys
+    code = "from quantized_ffn_gb300 import zffn; print(zffn.workspace_bytes())"
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.split()[-1] == "0", r.stdout
 
 
 def test_no_device_failure_records_its_reason(lib):
