@@ -264,7 +264,8 @@ zffn_status zffn_moe_swiglu_q4k_wd(const void *x, const int32_t *expert_ids,
  *   Wg, Wu: E stacked experts, each I rows of H/256 blocks.
  *   Wd: E stacked experts, each H rows of ceil(I/256) blocks.
  *   y:  fp32 [T][H], overwritten.
- * Requirements as zffn_swiglu_q4k, plus 1 <= E <= 4096, 1 <= top_k <= 64.
+ * Requirements as zffn_swiglu_q4k, plus 1 <= E <= 4096, 1 <= top_k <= 64,
+ * T * top_k <= 2^24, expert_ids and expert_weights 4-byte aligned.
  * T = 1: one cooperative launch when every block's share of the token's
  * expert weights fits in its shared memory (see ZFFN_OPT_TOKEN_KERNEL and
  * zffn_single_token_launches), else the two single-token kernels; T > 1:

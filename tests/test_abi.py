@@ -257,3 +257,14 @@ def test_no_device_failure_records_its_reason(lib):
     assert msg and msg != b"no error" and b"H must be" not in msg
     assert lib.zffn_swiglu_q4k_token_static(FAKE, FAKE, FAKE, FAKE, FAKE, 256, 256, None) == zffn.ERR_CUDA
     assert lib.zffn_last_error() == msg
+
+
+def test_routed_entry_rejects_its_own_limits(lib):
+    # T * top_k above 2^24, and expert ids or weights not 4-byte aligned
+    st = lib.zffn_moe_swiglu_q4k(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, (1 << 18) + 1, 256, 256,
+                                 128, 64, None)
+    assert st == zffn.ERR_INVALID_ARG and b"2^24" in lib.zffn_last_error()
+    odd = ctypes.c_void_p(0x10002)
+    for ids, wts in ((odd, FAKE), (FAKE, odd)):
+        st = lib.zffn_moe_swiglu_q4k(FAKE, ids, wts, FAKE, FAKE, FAKE, FAKE, 4, 256, 256, 8, 2, None)
+        assert st == zffn.ERR_INVALID_ARG and b"4-byte" in lib.zffn_last_error()
