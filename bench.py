@@ -161,6 +161,24 @@ def profiled_traffic(workload):
         return None
 
 
+THROTTLE_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def clocks_rejected(clocks):
+    """Why a timed region's clock record rejects its numbers, or None if they
+    stand: a hardware or thermal slowdown, or a median SM clock under load
+    well below the maximum with no reason reported (a clock lock left
+    behind).  A power cap is normal under a dense load and is kept."""
+    reasons = clocks.get("reasons") or []
+    bad = [r for r in reasons if r in THROTTLE_REASONS]
+    if bad:
+        return ",".join(bad)
+    sm, mx = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    if sm and mx and sm < 0.85 * mx and "sw_power_cap" not in reasons:
+        return "SM clock %.0f of %.0f MHz with no reason reported" % (sm, mx)
+    return None
+
+
 class ClockSampler:
     """nvidia-smi samples every 100 ms while the timed region runs."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -366,16 +384,26 @@ def run_gpu(args):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / args.steps
 
-    barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        wall0 = time.perf_counter()
-        ms = timed(lambda s: call(s))
-        wall = time.perf_counter() - wall0
+    def measure():
         barrier()
-        # the dominant kernel alone: the residual entry skips the zero fill
-        kms = timed(lambda s: call(s, residual=True))
-    clocks = clk.summary()
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clk:
+            wall0 = time.perf_counter()
+            ms = timed(lambda s: call(s))
+            wall = time.perf_counter() - wall0
+            barrier()
+            # the dominant kernel alone: the residual entry skips the zero fill
+            kms = timed(lambda s: call(s, residual=True))
+        return ms, wall, kms, clk.summary()
+
+    ms, wall, kms, clocks = measure()
+    why = clocks_rejected(clocks)
+    # every rank re-measures if any rank's clock record rejects its number
+    redo = bool(why) if world == 1 else max_over_ranks([1.0 if why else 0.0], dist, dev)[0] > 0
+    if redo:
+        first = dict(clocks, rejected=why or "another rank's clock record")
+        ms, wall, kms, clocks = measure()
+        clocks["first_run"] = first
     assert zffn.get_device_error() == zffn.OK
 
     # End to end through the library's host pipeline: every step uploads its
